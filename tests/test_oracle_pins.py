@@ -1,0 +1,525 @@
+"""Pins of the CPU oracle against the pages, closed forms and brute force.
+
+Each test checks one oracle function against something other than itself:
+figures the pages print (tests/golden/pages_facts.txt), closed forms,
+invariants, or brute-force enumeration.  Tests at the end plant mistakes in
+the oracle (on the CPU) and check that a pin catches each of them.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+from dualar_inputs import S2PRO, TINY, FRAMES_PER_AUDIO_SECOND
+from dualar_inputs import generators as g
+import oracle
+from oracle import model as om
+from oracle.sampler import sample_top_p, sample_q0
+from oracle.model import Sampling, SeqState
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_facts.txt")
+
+
+def facts():
+    out = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            out[k] = float(v) if "." in v else int(v)
+    return out
+
+
+# ---------------------------------------------------------------- shapes --
+
+def test_param_counts_match_pages():
+    f = facts()
+    assert S2PRO.total_params() == f["total_params"]
+    assert S2PRO.slow_params() == f["slow_params"]
+    assert round(S2PRO.fast_params() / 1e6, 1) == f["fast_params_millions"]
+    assert S2PRO.fusion_rows == f["fusion_rows"]
+    assert round(S2PRO.fusion_params() / 1e6, 1) == f["fusion_params_millions"]
+    assert round(S2PRO.fast_pass_params() / 1e6, 1) == f["fast_pass_params_millions"]
+    assert S2PRO.slow_params() - f["qwen3_4b_params"] == f["extra_embedding_rows"] * S2PRO.dim
+    assert S2PRO.sem_begin == f["semantic_first_id"]
+    assert S2PRO.sem_begin + S2PRO.n_sem - 1 == f["semantic_last_id"]
+    assert S2PRO.vocab == f["vocab"]
+    assert S2PRO.n_codebooks == f["n_codebooks"]
+    assert round(FRAMES_PER_AUDIO_SECOND, 2) == f["frames_per_second_2dp"]
+    assert S2PRO.n_cand_q0 == f["allowed_q0_candidates"]
+
+
+def test_fusion_offsets_layout():
+    # full size: ten codebooks of 4,096 rows stacked in one 40,960-row table
+    assert [S2PRO.fusion_offset(k) for k in range(10)] == [4096 * k for k in range(10)]
+    # tiny: 1 x 512 semantic + 3 x 128 acoustic = 896 rows
+    assert [TINY.fusion_offset(k) for k in range(4)] == [0, 512, 640, 768]
+    assert TINY.fusion_rows == 896
+
+
+# -------------------------------------------------------------- RMSNorm --
+
+def test_rmsnorm_constant_vector_closed_form():
+    for c in (0.5, -3.0, 1e-2):
+        x = np.full(256, c, np.float32)
+        w = np.linspace(0.5, 1.5, 256).astype(np.float32)
+        y = om.rmsnorm(x, w, 1e-6)
+        expect = w.astype(np.float64) * c / math.sqrt(c * c + 1e-6)
+        np.testing.assert_allclose(y, expect, rtol=2e-6)
+
+
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((5, 2560)).astype(np.float32) * 7
+    y = om.rmsnorm(x, np.ones(2560, np.float32), 1e-6)
+    np.testing.assert_allclose(np.sqrt(np.mean(y.astype(np.float64) ** 2, axis=-1)), 1.0, rtol=1e-5)
+    np.testing.assert_allclose(om.rmsnorm(3 * x, np.ones(2560, np.float32), 1e-6), y, rtol=1e-5, atol=1e-6)
+
+
+# ----------------------------------------------------------------- RoPE --
+
+def test_rope_tables_are_rounded_bf16_of_cos_sin():
+    cos, sin = om.rope_table(300, 128, 1e6)
+    # every entry is a bf16 value
+    for t in (cos, sin):
+        bits = t.view(np.uint32)
+        assert np.all(bits & 0xFFFF == 0)
+    # and within half a bf16 ulp of the exact value
+    i = np.arange(64)
+    for p in (0, 1, 7, 299):
+        ang = p * (1e6 ** (-2.0 * i / 128))
+        for tab, fn in ((cos, np.cos), (sin, np.sin)):
+            exact = fn(ang)
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - 7)
+            assert np.all(np.abs(tab[p] - exact) <= ulp / 2 + 1e-30)
+
+
+def test_rope_position_zero_is_identity():
+    cos, sin = om.rope_table(16, 64, 1e6)
+    x = np.random.default_rng(1).standard_normal((3, 64)).astype(np.float32)
+    np.testing.assert_array_equal(om.apply_rope(x, 0, cos, sin), x)
+
+
+def test_rope_pair_layout_and_angle():
+    hd, base = 64, 1e6
+    cos, sin = om.rope_table(100, hd, base)
+    for i in (0, 1, 5, 31):
+        for p in (1, 3, 37, 99):
+            e = np.zeros((1, hd), np.float32)
+            e[0, 2 * i] = 1.0
+            y = om.apply_rope(e, p, cos, sin)[0]
+            # the unit vector of pair i rotates within its own pair
+            others = np.delete(y, [2 * i, 2 * i + 1])
+            assert np.all(others == 0)
+            ang = p * base ** (-2.0 * i / hd)
+            assert abs(y[2 * i] - math.cos(ang)) < 4e-3
+            assert abs(y[2 * i + 1] - math.sin(ang)) < 4e-3
+            e2 = np.zeros((1, hd), np.float32)
+            e2[0, 2 * i + 1] = 1.0
+            y2 = om.apply_rope(e2, p, cos, sin)[0]
+            assert abs(y2[2 * i] + math.sin(ang)) < 4e-3
+            assert abs(y2[2 * i + 1] - math.cos(ang)) < 4e-3
+
+
+def test_rope_relative_position_property():
+    hd = 64
+    cos, sin = om.rope_table(200, hd, 1e6)
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((1, hd)).astype(np.float32)
+    k = rng.standard_normal((1, hd)).astype(np.float32)
+    d = []
+    for p, s in ((10, 3), (50, 43), (107, 100)):
+        d.append(float(om.apply_rope(q, p, cos, sin)[0] @ om.apply_rope(k, s, cos, sin)[0]))
+    # depends on p - s only (bf16 tables: agreement to ~1e-2 relative)
+    assert max(d) - min(d) < 0.03 * max(1.0, abs(d[0]))
+    # and norms are preserved up to the bf16 table error
+    y = om.apply_rope(q, 77, cos, sin)
+    assert abs(np.linalg.norm(y) / np.linalg.norm(q) - 1) < 1e-2
+
+
+# ------------------------------------------------------------ attention --
+
+def brute_attention(q, k, v, n_rep, causal_offset):
+    tq, hq, hd = q.shape
+    out = np.zeros((tq, hq, hd))
+    for t in range(tq):
+        for h in range(hq):
+            gk = h // n_rep
+            limit = k.shape[0] if causal_offset is None else causal_offset + t + 1
+            s = [sum(float(q[t, h, d]) * float(k[j, gk, d]) for d in range(hd)) / math.sqrt(hd)
+                 for j in range(limit)]
+            m = max(s)
+            e = [math.exp(x - m) for x in s]
+            z = sum(e)
+            for d in range(hd):
+                out[t, h, d] = sum(e[j] / z * float(v[j, gk, d]) for j in range(limit))
+    return out
+
+
+@pytest.mark.parametrize("tq,tk,hq,hkv,off", [(1, 5, 4, 2, 4), (3, 7, 4, 1, 4), (4, 4, 2, 2, 0)])
+def test_attention_matches_brute_force(tq, tk, hq, hkv, off):
+    rng = np.random.default_rng(3)
+    hd = 8
+    q = rng.standard_normal((tq, hq, hd)).astype(np.float32)
+    k = rng.standard_normal((tk, hkv, hd)).astype(np.float32)
+    v = rng.standard_normal((tk, hkv, hd)).astype(np.float32)
+    got = om.gqa_attention(q, k, v, hq // hkv, causal_offset=off)
+    np.testing.assert_allclose(got, brute_attention(q, k, v, hq // hkv, off), rtol=1e-5, atol=1e-5)
+
+
+def test_attention_single_key_returns_value():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((1, 4, 16)).astype(np.float32) * 10
+    k = rng.standard_normal((1, 2, 16)).astype(np.float32)
+    v = rng.standard_normal((1, 2, 16)).astype(np.float32)
+    out = om.gqa_attention(q, k, v, 2, causal_offset=0)
+    np.testing.assert_allclose(out[0], np.repeat(v[0], 2, axis=0), rtol=1e-6)
+
+
+def test_silu_values():
+    x = np.array([0.0, 1.0, 30.0, -30.0], np.float32)
+    y = om.silu(x)
+    assert y[0] == 0.0
+    assert abs(y[1] - 0.7310585786300049) < 1e-7       # logistic(1)
+    assert abs(y[2] - 30.0) < 1e-5 and abs(y[3]) < 1e-10
+
+
+# ------------------------------------------------ incremental == recompute --
+
+def test_slow_incremental_equals_full_recompute(tiny_oracle):
+    o = tiny_oracle
+    cfg = TINY
+    prompt = g.make_prompt(cfg, 20, seed=5)
+    seq = o.prefill(prompt[:12])
+    # the rest of the prompt one position at a time
+    hs = []
+    for t in prompt[12:]:
+        hs.append(o.slow_rows(seq, o.w.tok_emb[[t]])[0])
+    # then 6 forced frames (fusion inputs)
+    forced = g.make_forced_codes(6, 1, cfg, seed=6)
+    u = g.make_uniforms(6, 1, cfg, seed=7)
+    xs = []
+    for f in range(6):
+        r = o.decode_frame(seq, u[f, 0], Sampling(), forced=forced[f, 0])
+        xs.append(r.x_next)
+        hs.append(seq.h_last)
+    rows = np.concatenate([o.w.tok_emb[prompt], np.stack(xs)], axis=0)
+    full = o.slow_full_recompute(rows)
+    np.testing.assert_allclose(np.stack(hs), full[12:], rtol=1e-4, atol=1e-4)
+    # logits from the full head + bias equal the restricted head on allowed ids
+    zfull = o.full_biased_logits(full[-1])
+    zr = o.restricted_logits(full[-1])
+    np.testing.assert_allclose(zfull[cfg.sem_begin:cfg.sem_begin + cfg.n_sem], zr[:-1], rtol=1e-5, atol=1e-6)
+    assert abs(zfull[cfg.im_end_id] - zr[-1]) < 1e-5
+
+
+def test_fast_incremental_equals_full_recompute(tiny_oracle):
+    o = tiny_oracle
+    rng = np.random.default_rng(8)
+    h = om.rmsnorm(rng.standard_normal(TINY.dim).astype(np.float32), np.ones(TINY.dim, np.float32), 1e-6)
+    forced = np.array([300, 5, 77, 127], np.int32)
+    u = np.full(TINY.n_codebooks + 1, 0.5, np.float32)
+    codes, logits, _ = o.fast_ar(h, int(forced[0]), u, Sampling(), forced=forced)
+    assert list(codes) == list(forced)
+    full = o.fast_full_recompute(h, forced)
+    np.testing.assert_allclose(logits, full, rtol=1e-4, atol=1e-5)
+
+
+def test_fast_kv_overwritten_each_frame(tiny_oracle):
+    """The fast AR starts every frame from an empty num_codebooks-long cache:
+    the same slow state and codes give the same logits whatever ran before."""
+    o = tiny_oracle
+    h = np.ones(TINY.dim, np.float32)
+    f = np.array([3, 4, 5, 6], np.int32)
+    u = np.full(5, 0.3, np.float32)
+    a = o.fast_ar(h, 3, u, Sampling(), forced=f)[1]
+    o.fast_ar(2 * h, 9, u, Sampling(), forced=np.array([9, 1, 2, 3], np.int32))
+    b = o.fast_ar(h, 3, u, Sampling(), forced=f)[1]
+    np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------- fusion --
+
+class _FusionStub:
+    pass
+
+
+def _fusion_oracle(cfg, tok_emb, fusion):
+    o = object.__new__(om.DualAROracle)
+    o.cfg = cfg
+    o.w = _FusionStub()
+    o.w.tok_emb = tok_emb
+    o.w.fusion = fusion
+    return o
+
+
+def test_fusion_unit_rows_closed_form():
+    for cfg in (TINY, S2PRO):
+        d = 8
+        o = _fusion_oracle(cfg, np.ones((cfg.vocab, d), np.float32), np.ones((cfg.fusion_rows, d), np.float32))
+        codes = np.zeros(cfg.n_codebooks, np.int32)
+        x = o.fuse(codes)
+        np.testing.assert_allclose(x, math.sqrt(cfg.n_codebooks + 1), rtol=1e-6)
+    # full size: eleven unit rows scaled by 1/sqrt(11)
+    assert abs(math.sqrt(11) - x[0]) < 1e-5
+
+
+def test_fusion_gathers_the_right_rows():
+    cfg = TINY
+    rng = np.random.default_rng(9)
+    # one-hot rows: tok_emb row r has a 1 at column r, fusion row r at V + r
+    width = cfg.vocab + cfg.fusion_rows
+    tok = np.zeros((cfg.vocab, width), np.float32)
+    tok[np.arange(cfg.vocab), np.arange(cfg.vocab)] = 1
+    fus = np.zeros((cfg.fusion_rows, width), np.float32)
+    fus[np.arange(cfg.fusion_rows), cfg.vocab + np.arange(cfg.fusion_rows)] = 1
+    o = _fusion_oracle(cfg, tok, fus)
+    for _ in range(5):
+        codes = np.array([rng.integers(cfg.n_sem)] + list(rng.integers(cfg.fast_vocab, size=3)), np.int32)
+        x = o.fuse(codes) * math.sqrt(cfg.n_codebooks + 1)
+        hot = set(np.flatnonzero(np.abs(x) > 0.5).tolist())
+        expect = {cfg.sem_begin + codes[0], cfg.vocab + codes[0]} | {
+            cfg.vocab + [0, 512, 640, 768][k] + codes[k] for k in range(1, 4)}
+        assert hot == expect
+
+
+# ------------------------------------------------------------------ bias --
+
+def test_bias_keeps_exactly_semantic_and_im_end():
+    f = facts()
+    o = object.__new__(om.DualAROracle)
+    o.cfg = S2PRO
+    o.w = _FusionStub()
+    o.w.tok_emb = np.ones((S2PRO.vocab, 1), np.float32)
+    z = o.full_biased_logits(np.ones(1, np.float32))
+    finite = np.flatnonzero(np.isfinite(z))
+    assert finite.size == f["allowed_q0_candidates"]
+    assert set(finite.tolist()) == set(range(f["semantic_first_id"], f["semantic_last_id"] + 1)) | {S2PRO.im_end_id}
+
+
+# --------------------------------------------------------------- sampler --
+
+def brute_nucleus(p, ids, top_p):
+    """Smallest set of candidates reaching top_p, preferring higher mass, then
+    lower ids -- by enumeration of all subsets."""
+    n = len(p)
+    best = None
+    for r in range(1, n + 1):
+        for sub in itertools.combinations(range(n), r):
+            m = sum(p[i] for i in sub)
+            if m >= top_p - 1e-12:
+                key = (-m, sorted(ids[i] for i in sub))
+                if best is None or key < best[0]:
+                    best = (key, sub)
+        if best is not None:
+            return set(best[1])
+    return set(range(n))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_top_p_distribution_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(2, 9))
+    z = rng.standard_normal(n) * 2
+    ids = rng.permutation(100)[:n]
+    T = float(rng.choice([0.5, 0.8, 1.0, 1.7]))
+    top_p = float(rng.choice([0.3, 0.6, 0.8, 0.9, 1.0]))
+    p = np.exp(z / T - np.max(z / T))
+    p /= p.sum()
+    kept = brute_nucleus(p, ids, top_p)
+    zk = sum(p[i] for i in kept)
+    m = 20000
+    counts = np.zeros(n)
+    for j in range(m):
+        counts[sample_top_p(z, ids, T, top_p, (j + 0.5) / m).index] += 1
+    for i in range(n):
+        expect = p[i] / zk if i in kept else 0.0
+        assert abs(counts[i] / m - expect) <= 1.5 / m
+
+
+def test_top_p_temperature_two_candidates():
+    a, T = 1.3, 0.7
+    z = np.array([0.0, a])
+    m = 40000
+    hits = sum(sample_top_p(z, [0, 1], T, 1.0, (j + 0.5) / m).index == 1 for j in range(m))
+    assert abs(hits / m - 1 / (1 + math.exp(-a / T))) < 1e-4
+
+
+def test_top_p_one_is_plain_inverse_cdf():
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal(6)
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    order = sorted(range(6), key=lambda i: -p[i])
+    for u in np.linspace(0.001, 0.999, 57):
+        c = 0.0
+        for i in order:
+            c += p[i]
+            if c > u:
+                break
+        assert sample_top_p(z, np.arange(6), 1.0, 1.0, u).index == i
+
+
+def test_greedy_and_low_temperature_limit():
+    z = np.array([0.1, 2.0, -1.0, 2.0, 1.5])
+    ids = np.array([10, 7, 3, 5, 1])
+    assert sample_top_p(z, ids, 0.0, 0.8, 0.9).index == 3     # tie at 2.0 -> lowest id (5)
+    z2 = np.array([0.1, 2.0, -1.0, 1.9, 1.5])
+    for u in (0.0, 0.5, 0.999):
+        assert sample_top_p(z2, ids, 1e-3, 0.8, u).index == 1
+
+
+def test_sampler_margins_reported():
+    r = sample_top_p(np.array([0.0, 0.0]), [0, 1], 1.0, 1.0, 0.5)
+    assert r.cdf_margin < 1e-12           # u*Z sits on the boundary 0.5
+
+
+# ------------------------------------------------------------------- RAS --
+
+def _q0(history, normal_target, ras_win=10, allow_eos=True):
+    """Logits that make the normal draw (T=0) pick normal_target; the RAS
+    draw (T=1, top-p 0.9) with u=0 picks the top candidate too, so make the
+    RAS draw land elsewhere with u close to 1."""
+    cfg = TINY
+    z = np.zeros(cfg.n_sem + 1)
+    z[normal_target] = 5.0
+    smp = Sampling(temperature=0.0, top_p=0.8, ras_win=ras_win, allow_eos=allow_eos)
+    return sample_q0(cfg, z, smp, history, 0.5, 0.999)
+
+
+def test_ras_cases():
+    # repeat inside the window -> resample (the RAS draw differs from 7)
+    n, r, c = _q0([1, 2, 7], 7)
+    assert n.index == 7 and c == r.index and c != 7
+    # repeat only outside the last 10 frames -> keep
+    n, r, c = _q0([7] + list(range(100, 110)), 7)
+    assert c == 7
+    # window shorter than 10 frames so far
+    n, r, c = _q0([7], 7)
+    assert c != 7
+    # no repeat
+    n, r, c = _q0([1, 2, 3], 7)
+    assert c == 7
+    # window 0 disables RAS
+    n, r, c = _q0([7], 7, ras_win=0)
+    assert c == 7
+    # <|im_end|> never triggers the resample
+    n, r, c = _q0([TINY.n_sem], TINY.n_sem)
+    assert c == TINY.n_sem
+    # allow_eos=False removes <|im_end|> from the candidates
+    n, r, c = _q0([], TINY.n_sem, allow_eos=False)
+    assert c != TINY.n_sem
+
+
+def test_eos_frame_finishes_sequence(tiny_oracle):
+    o = tiny_oracle
+    seq = o.prefill(g.make_prompt(TINY, 8, seed=12))
+    seq.z_last = np.full(TINY.n_sem + 1, -5.0, np.float32)
+    seq.z_last[TINY.n_sem] = 50.0
+    r = o.decode_frame(seq, np.full(5, 0.5, np.float32), Sampling())
+    assert r.status == 1 and np.all(r.codes == -1) and seq.finished
+
+
+# ----------------------------------------------------------------- pages --
+
+def test_page_oracle_lowest_free_first():
+    p = oracle.PageOracle(8, 4)
+    p.append(0, 5)          # positions 0..4 -> pages 0, 1
+    p.append(1, 1)          # page 2
+    p.append(0, 4)          # positions 5..8 -> page 3 at position 8
+    assert p.table == {0: [0, 1, 3], 1: [2]}
+    p.release(0)
+    p.append(2, 9)          # pages 0, 1, 3 again, lowest first
+    assert p.table[2] == [0, 1, 3]
+    with pytest.raises(MemoryError):
+        p.append(3, 4 * 5)
+
+
+# ------------------------------------------------------ planted mistakes --
+
+def _expect_pin_failure(monkeypatch, target, name, bad, pin, *args):
+    monkeypatch.setattr(target, name, bad)
+    with pytest.raises(AssertionError):
+        pin(*args)
+    monkeypatch.undo()
+
+
+def test_planted_rope_sign_error_is_caught(monkeypatch):
+    orig = om.apply_rope
+
+    def bad(x, pos, cos, sin):
+        return orig(x, pos, cos, -sin)
+    _expect_pin_failure(monkeypatch, om, "apply_rope", bad, test_rope_pair_layout_and_angle)
+
+
+def test_planted_gqa_mapping_error_is_caught(monkeypatch):
+    def bad(q, k, v, n_rep, causal_offset=None):
+        kk = np.tile(k, (1, n_rep, 1))        # head h -> kv head h % Hkv
+        vv = np.tile(v, (1, n_rep, 1))
+        return om.gqa_attention.__wrapped__(q, kk, vv, 1, causal_offset) if hasattr(
+            om.gqa_attention, "__wrapped__") else _plain_attention(q, kk, vv, causal_offset)
+    _expect_pin_failure(monkeypatch, om, "gqa_attention", bad,
+                        test_attention_matches_brute_force, 1, 5, 4, 2, 4)
+
+
+def _plain_attention(q, k, v, off):
+    s = np.einsum("qhd,khd->hqk", q, k) / math.sqrt(q.shape[-1])
+    tq, tk = q.shape[0], k.shape[0]
+    allowed = np.arange(tk)[None, :] <= (off + np.arange(tq))[:, None]
+    s = np.where(allowed[None], s, -np.inf)
+    p = np.exp(s - s.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    return np.einsum("hqk,khd->qhd", p, v).astype(np.float32)
+
+
+def test_planted_causal_off_by_one_is_caught(monkeypatch):
+    orig = om.gqa_attention
+
+    def bad(q, k, v, n_rep, causal_offset=None):
+        return orig(q, k, v, n_rep, None if causal_offset is None else causal_offset + 1)
+    _expect_pin_failure(monkeypatch, om, "gqa_attention", bad,
+                        test_attention_matches_brute_force, 3, 7, 4, 1, 3)
+
+
+def test_planted_fusion_scale_error_is_caught(monkeypatch):
+    orig = om.DualAROracle.fuse
+
+    def bad(self, codes):
+        return orig(self, codes) * math.sqrt(self.cfg.n_codebooks + 1) / math.sqrt(self.cfg.n_codebooks)
+    _expect_pin_failure(monkeypatch, om.DualAROracle, "fuse", bad, test_fusion_unit_rows_closed_form)
+
+
+def test_planted_top_p_off_by_one_is_caught(monkeypatch):
+    import oracle.sampler as osm
+    orig = osm.sample_top_p
+
+    def bad(z, ids, temperature, top_p, u):
+        # keeps one candidate too many
+        r = orig(z, ids, temperature, min(1.0, top_p + 0.15), u)
+        return r
+    monkeypatch.setattr(osm, "sample_top_p", bad)
+    with pytest.raises(AssertionError):
+        for s in range(6):
+            _tp_check(s, osm.sample_top_p)
+
+
+def _tp_check(seed, fn):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(2, 9))
+    z = rng.standard_normal(n) * 2
+    ids = rng.permutation(100)[:n]
+    T = float(rng.choice([0.5, 0.8, 1.0, 1.7]))
+    top_p = float(rng.choice([0.3, 0.6, 0.8, 0.9, 1.0]))
+    p = np.exp(z / T - np.max(z / T))
+    p /= p.sum()
+    kept = brute_nucleus(p, ids, top_p)
+    zk = sum(p[i] for i in kept)
+    m = 4000
+    counts = np.zeros(n)
+    for j in range(m):
+        counts[fn(z, ids, T, top_p, (j + 0.5) / m).index] += 1
+    for i in range(n):
+        expect = p[i] / zk if i in kept else 0.0
+        assert abs(counts[i] / m - expect) <= 1.5 / m
