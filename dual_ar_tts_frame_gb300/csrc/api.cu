@@ -1,0 +1,702 @@
+// Host runtime of libdualar.so: the C ABI declared in include/dualar.h.
+//
+// Owns the KV page pool and per-slot state, allocates pages on the host
+// (lowest free page first), and queues the kernels of a prefill or a frame
+// on the handle's stream.  Kernels are in kernels.cu.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "dualar.h"
+#include "internal.h"
+
+using namespace dualar;
+
+struct dualar_handle {
+  dualar_config cfg{};
+  dualar_weights w{};
+  std::vector<dualar_layer_weights> slow, fast;
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  int n_sm = 0;
+  DevPtrs d{};
+  std::vector<void*> allocs;
+  // host mirrors
+  std::vector<int> length;               // next position per slot, -1 = empty
+  std::vector<std::vector<int>> pages;   // pages per slot
+  std::set<int> free_pages;
+  std::string err;
+  int launches = 0;
+};
+
+namespace {
+
+void set_err(dualar_handle* h, const char* fmt, ...) {
+  if (!h) return;
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  h->err = buf;
+}
+
+#define CUDA_TRY(h, call)                                                               \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess) {                                                            \
+      set_err(h, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return DUALAR_ERR_CUDA;                                                           \
+    }                                                                                   \
+  } while (0)
+
+#define LAUNCH(h, call)                                                                 \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    ++(h)->launches;                                                                    \
+    if (e_ != cudaSuccess) {                                                            \
+      set_err(h, "launch %s failed: %s", #call, cudaGetErrorString(e_));                \
+      return DUALAR_ERR_CUDA;                                                           \
+    }                                                                                   \
+  } while (0)
+
+template <typename T>
+int dev_alloc(dualar_handle* h, T** p, size_t count) {
+  void* q = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 256);
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    set_err(h, "cudaMalloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+    return DUALAR_ERR_CUDA;
+  }
+  h->allocs.push_back(q);
+  e = cudaMemsetAsync(q, 0, bytes, h->stream);
+  if (e != cudaSuccess) {
+    set_err(h, "cudaMemsetAsync failed: %s", cudaGetErrorString(e));
+    return DUALAR_ERR_CUDA;
+  }
+  *p = static_cast<T*>(q);
+  return DUALAR_OK;
+}
+
+// float -> bf16 bits, round to nearest even (host).
+uint16_t host_f32_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u) return static_cast<uint16_t>(u >> 16);  // inf / nan
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_layer(dualar_handle* h, const dualar_layer_weights& l, bool qk, const char* which, int i) {
+  const void* ptrs[] = {l.attn_norm, l.wqkv, l.wo, l.ffn_norm, l.w_gate, l.w_up, l.w_down};
+  for (const void* p : ptrs) {
+    if (!p || !aligned16(p)) {
+      set_err(h, "%s layer %d: a weight pointer is NULL or not 16-byte aligned", which, i);
+      return DUALAR_ERR_INVALID_ARG;
+    }
+  }
+  if (qk && (!l.q_norm || !l.k_norm)) {
+    set_err(h, "%s layer %d: qk-norm enabled but q_norm/k_norm missing", which, i);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  return DUALAR_OK;
+}
+
+int validate_config(dualar_handle* h, const dualar_config& c) {
+  auto bad = [&](const char* what) {
+    set_err(h, "invalid config: %s", what);
+    return DUALAR_ERR_INVALID_ARG;
+  };
+  if (c.dim <= 0 || c.dim % 8) return bad("dim must be a positive multiple of 8");
+  if (c.ffn <= 0 || c.ffn % 8) return bad("ffn must be a positive multiple of 8");
+  if (c.head_dim != 64 && c.head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c.n_head <= 0 || c.n_kv_head <= 0 || c.n_head % c.n_kv_head) return bad("heads");
+  const int g = c.n_head / c.n_kv_head;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return bad("n_head / n_kv_head must be 1, 2, 4 or 8");
+  if (c.n_layer <= 0 || c.fast_n_layer <= 0) return bad("layer counts");
+  if (c.page_tokens != 64) return bad("page_tokens must be 64");
+  if (c.n_codebooks < 2 || c.n_codebooks > kMaxCodebooks) return bad("n_codebooks in [2, 16]");
+  if (c.n_sem <= 0 || c.n_sem + 1 > kSampThreads * kSampPerThread) return bad("n_sem");
+  if (c.fast_vocab <= 0 || c.fast_vocab > kSampThreads * kSampPerThread) return bad("fast_vocab");
+  if (c.sem_begin < 0 || c.sem_begin + c.n_sem > c.vocab) return bad("semantic id range");
+  if (c.im_end_id < 0 || c.im_end_id >= c.vocab ||
+      (c.im_end_id >= c.sem_begin && c.im_end_id < c.sem_begin + c.n_sem))
+    return bad("im_end_id must be a non-semantic id");
+  if (c.max_seqs <= 0 || c.max_seqs > kMaxRows) return bad("max_seqs in [1, 128]");
+  if (c.max_pages <= 0) return bad("max_pages");
+  if (c.max_ctx <= 0 || (c.max_ctx + 63) / 64 > kMaxChunks * 1024) return bad("max_ctx");
+  if (!(c.norm_eps > 0.f) || !(c.rope_base > 1.f)) return bad("norm_eps / rope_base");
+  if ((c.n_head * c.head_dim) % 8) return bad("n_head * head_dim");
+  return DUALAR_OK;
+}
+
+// ---- launch helpers --------------------------------------------------------
+GemvArgs gemv_base(dualar_handle* h) {
+  GemvArgs a{};
+  a.eps = h->cfg.norm_eps;
+  a.err = h->d.err;
+  a.wait_limit_ns = h->d.wait_limit_ns;
+  return a;
+}
+
+int run_gemv(dualar_handle* h, GemvArgs a) {
+  LAUNCH(h, launch_gemv(a, h->n_sm, h->stream));
+  return DUALAR_OK;
+}
+
+#define TRY(x)                    \
+  do {                            \
+    int rc_ = (x);                \
+    if (rc_ != DUALAR_OK) return rc_; \
+  } while (0)
+
+const uint16_t* U16(const void* p) { return static_cast<const uint16_t*>(p); }
+
+// One transformer block over nrows rows.  Slow blocks attend over the paged
+// cache; fast blocks over the per-frame codebook cache.
+int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast, int nrows,
+          const float* xin, float* hres, int fast_pos, int units, int chunk) {
+  const dualar_config& c = h->cfg;
+  const DevPtrs& d = h->d;
+  const int qd = c.n_head * c.head_dim;
+  // u = RMSNorm(x); qkv = Wqkv u
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(lw.wqkv);
+  a.n0 = d.qkv_dim;
+  a.K = c.dim;
+  a.mode = GEMV_STORE;
+  a.nb = nrows;
+  a.x = xin;
+  a.ldx = c.dim;
+  a.norm_w = U16(lw.attn_norm);
+  a.out = d.qkv;
+  a.ldo = d.qkv_dim;
+  TRY(run_gemv(h, a));
+  const bool qk = fast ? c.fast_qk_norm : c.slow_qk_norm;
+  LAUNCH(h, launch_append(d, nrows, layer, fast, fast_pos, qk ? U16(lw.q_norm) : nullptr,
+                          qk ? U16(lw.k_norm) : nullptr, h->stream));
+  if (fast)
+    LAUNCH(h, launch_attn_fast(d, nrows, layer, fast_pos + 1, h->stream));
+  else
+    LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, h->stream));
+  // h = x + Wo attn
+  a = gemv_base(h);
+  a.w0 = U16(lw.wo);
+  a.n0 = c.dim;
+  a.K = qd;
+  a.mode = GEMV_ADD;
+  a.nb = nrows;
+  a.x = d.attn;
+  a.ldx = qd;
+  a.base = xin;
+  a.ldb = c.dim;
+  a.out = hres;
+  a.ldo = c.dim;
+  TRY(run_gemv(h, a));
+  // act = SiLU(Wgate u) * (Wup u), u = RMSNorm(h)
+  a = gemv_base(h);
+  a.w0 = U16(lw.w_gate);
+  a.w1 = U16(lw.w_up);
+  a.n0 = c.ffn;
+  a.n1 = c.ffn;
+  a.K = c.dim;
+  a.mode = GEMV_SWIGLU;
+  a.nb = nrows;
+  a.x = hres;
+  a.ldx = c.dim;
+  a.norm_w = U16(lw.ffn_norm);
+  a.out = d.act;
+  a.ldo = c.ffn;
+  TRY(run_gemv(h, a));
+  // h += Wdown act
+  a = gemv_base(h);
+  a.w0 = U16(lw.w_down);
+  a.n0 = c.dim;
+  a.K = c.ffn;
+  a.mode = GEMV_ADD;
+  a.nb = nrows;
+  a.x = d.act;
+  a.ldx = c.ffn;
+  a.base = hres;
+  a.ldb = c.dim;
+  a.out = hres;
+  a.ldo = c.dim;
+  return run_gemv(h, a);
+}
+
+// Split-KV work list: chunk size and per-row first unit.
+void plan_attention(dualar_handle* h, LaunchSetup& s, int* units, int* chunk) {
+  int max_len = 0;
+  for (int r = 0; r < s.n_rows; ++r) max_len = std::max(max_len, s.rows[r].pos + 1);
+  const int pt = h->cfg.page_tokens;
+  const int pages = (max_len + pt - 1) / pt;
+  const int ppc = std::max(1, (pages + kMaxChunks - 1) / kMaxChunks);
+  *chunk = ppc * pt;
+  int u = 0;
+  for (int r = 0; r < s.n_rows; ++r) {
+    s.rows[r].unit0 = u;
+    u += h->cfg.n_kv_head * ((s.rows[r].pos + 1 + *chunk - 1) / *chunk);
+  }
+  *units = u;
+}
+
+int slow_stack(dualar_handle* h, int nrows, int units, int chunk) {
+  for (int l = 0; l < h->cfg.n_layer; ++l)
+    TRY(block(h, h->slow[l], l, false, nrows, l == 0 ? h->d.xs : h->d.hs, h->d.hs, 0, units, chunk));
+  return DUALAR_OK;
+}
+
+// Final RMSNorm + restricted head for rows [r0, r0 + n): commits the normed
+// hidden state and the logits of rows whose commit_map entry is a slot.
+// [P2] "Two autoregressions" (bias keeps semantic ids + <|im_end|>) and "The
+// slow AR is Qwen3-4B" (tied head): only those 4,097 rows are computed.
+int restricted_head(dualar_handle* h, int r0, int n) {
+  const dualar_config& c = h->cfg;
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(h->w.tok_emb) + static_cast<size_t>(c.sem_begin) * c.dim;
+  a.n0 = c.n_sem;
+  a.w1 = U16(h->w.tok_emb) + static_cast<size_t>(c.im_end_id) * c.dim;
+  a.n1 = 1;
+  a.K = c.dim;
+  a.mode = GEMV_STORE;
+  a.nb = n;
+  a.x = h->d.hs + static_cast<size_t>(r0) * c.dim;
+  a.ldx = c.dim;
+  a.norm_w = U16(h->w.final_norm);
+  a.out = h->d.z_last;
+  a.ldo = c.n_sem + 1;
+  a.out_map = h->d.commit_map + r0;
+  a.save_x = h->d.h_last;
+  a.save_map = h->d.commit_map + r0;
+  a.lds = c.dim;
+  return run_gemv(h, a);
+}
+
+int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const float* uniforms,
+                const dualar_sampling* smp, const int32_t* forced, int32_t* codes, int32_t* status,
+                float* slow_logits, float* fast_logits, int32_t* draws) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  const dualar_config& c = h->cfg;
+  if (batch < 1 || batch > c.max_seqs) {
+    set_err(h, "batch %d outside [1, %d]", batch, c.max_seqs);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  if (!slots || !uniforms || !smp || !codes || !status) {
+    set_err(h, "decode: NULL argument");
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  if (!(smp->temperature >= 0.f) || !(smp->top_p > 0.f && smp->top_p <= 1.f) || smp->ras_win < 0 ||
+      smp->ras_win > kRasRing || !(smp->ras_temperature >= 0.f) ||
+      !(smp->ras_top_p > 0.f && smp->ras_top_p <= 1.f)) {
+    set_err(h, "decode: invalid sampling parameters");
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  std::vector<char> seen(c.max_seqs, 0);
+  int need = 0;
+  for (int r = 0; r < batch; ++r) {
+    const int s = slots[r];
+    if (s < 0 || s >= c.max_seqs || seen[s]) {
+      set_err(h, "decode: slot %d invalid or repeated", s);
+      return DUALAR_ERR_INVALID_ARG;
+    }
+    seen[s] = 1;
+    if (h->length[s] < 0) {
+      set_err(h, "decode: slot %d is empty", s);
+      return DUALAR_ERR_SLOT_EMPTY;
+    }
+    if (h->length[s] >= c.max_ctx) {
+      set_err(h, "decode: slot %d reached max_ctx %d", s, c.max_ctx);
+      return DUALAR_ERR_CONTEXT_FULL;
+    }
+    if (h->length[s] % c.page_tokens == 0) ++need;
+  }
+  if (need > static_cast<int>(h->free_pages.size())) {
+    set_err(h, "decode: %d pages needed, %zu free", need, h->free_pages.size());
+    return DUALAR_ERR_OOM_PAGES;
+  }
+  static LaunchSetup s;   // large; filled per call, copied into the launch
+  std::memset(&s, 0, sizeof(s));
+  s.n_rows = batch;
+  s.commit_last_only = 0;
+  s.embed = 0;
+  for (int r = 0; r < batch; ++r) {
+    const int sl = slots[r];
+    const int pos = h->length[sl];
+    s.rows[r] = RowInfo{sl, pos, 1, 0};
+    if (pos % c.page_tokens == 0) {
+      const int pg = *h->free_pages.begin();
+      h->free_pages.erase(h->free_pages.begin());
+      h->pages[sl].push_back(pg);
+      s.upd_slot[s.n_updates] = sl;
+      s.upd_index[s.n_updates] = pos / c.page_tokens;
+      s.upd_page[s.n_updates] = pg;
+      ++s.n_updates;
+    }
+  }
+  int units = 0, chunk = 0;
+  plan_attention(h, s, &units, &chunk);
+  h->launches = 0;
+  const DevPtrs& d = h->d;
+  SamplingParams sp{smp->temperature, smp->top_p, smp->ras_win, smp->ras_temperature,
+                    smp->ras_top_p, smp->allow_eos};
+  const int N = c.n_codebooks;
+  LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
+  // 1. q0 from the held restricted logits (+ repetition-aware resample)
+  LAUNCH(h, launch_sample_q0(d, batch, uniforms, N + 1, sp, forced, N, codes, status, slow_logits,
+                             draws, U16(h->w.fast_emb), h->stream));
+  // 2. fast AR: pass 0 stores the slow hidden state; passes 1..N-1 draw q_k
+  for (int p = 0; p < N; ++p) {
+    const float* xin = d.fin + static_cast<size_t>(p & 1) * kMaxRows * c.dim;
+    for (int l = 0; l < c.fast_n_layer; ++l)
+      TRY(block(h, h->fast[l], l, true, batch, l == 0 ? xin : d.hf, d.hf, p, 0, 0));
+    if (p == 0) continue;
+    GemvArgs a = gemv_base(h);
+    a.w0 = U16(h->w.fast_out);
+    a.n0 = c.fast_vocab;
+    a.K = c.dim;
+    a.mode = GEMV_STORE;
+    a.nb = batch;
+    a.x = d.hf;
+    a.ldx = c.dim;
+    a.norm_w = U16(h->w.fast_norm);
+    a.out = d.logits;
+    a.ldo = d.logit_ld;
+    TRY(run_gemv(h, a));
+    LAUNCH(h, launch_sample_fast(d, batch, p, uniforms, N + 1, sp, forced, N, codes, fast_logits,
+                                 draws, U16(h->w.fast_emb), h->stream));
+  }
+  // 3. fusion -> next slow input; 4. one slow position; restricted head
+  LAUNCH(h, launch_fusion(d, batch, U16(h->w.tok_emb), U16(h->w.fusion), h->stream));
+  TRY(slow_stack(h, batch, units, chunk));
+  TRY(restricted_head(h, 0, batch));
+  for (int r = 0; r < batch; ++r) h->length[slots[r]] += 1;
+  return DUALAR_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_stream,
+                  dualar_handle** out) {
+  if (!out) return DUALAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w) return DUALAR_ERR_INVALID_ARG;
+  dualar_handle* h = new dualar_handle();
+  h->cfg = *cfg;
+  h->stream = static_cast<cudaStream_t>(cuda_stream);
+  auto fail = [&](int rc) {
+    // keep the message readable by printing it: the handle is not returned
+    fprintf(stderr, "dualar_create: %s\n", h->err.c_str());
+    dualar_destroy(h);
+    return rc;
+  };
+  int rc = validate_config(h, *cfg);
+  if (rc != DUALAR_OK) return fail(rc);
+  const dualar_config& c = h->cfg;
+  const void* top[] = {w->tok_emb, w->final_norm, w->fast_emb, w->fast_norm, w->fast_out, w->fusion};
+  for (const void* p : top)
+    if (!p || !aligned16(p)) {
+      set_err(h, "a weight pointer is NULL or not 16-byte aligned");
+      return fail(DUALAR_ERR_INVALID_ARG);
+    }
+  if (!w->slow || !w->fast) {
+    set_err(h, "per-layer weight arrays missing");
+    return fail(DUALAR_ERR_INVALID_ARG);
+  }
+  h->w = *w;
+  h->slow.assign(w->slow, w->slow + c.n_layer);
+  h->fast.assign(w->fast, w->fast + c.fast_n_layer);
+  for (int i = 0; i < c.n_layer; ++i)
+    if ((rc = check_layer(h, h->slow[i], c.slow_qk_norm, "slow", i)) != DUALAR_OK) return fail(rc);
+  for (int i = 0; i < c.fast_n_layer; ++i)
+    if ((rc = check_layer(h, h->fast[i], c.fast_qk_norm, "fast", i)) != DUALAR_OK) return fail(rc);
+  h->w.slow = nullptr;
+  h->w.fast = nullptr;
+
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    set_err(h, "no CUDA device");
+    return fail(DUALAR_ERR_CUDA);
+  }
+
+  DevPtrs& d = h->d;
+  d.D = c.dim;
+  d.Hq = c.n_head;
+  d.Hkv = c.n_kv_head;
+  d.hd = c.head_dim;
+  d.F = c.ffn;
+  d.n_sem = c.n_sem;
+  d.sem_begin = c.sem_begin;
+  d.im_end = c.im_end_id;
+  d.Cf = c.fast_vocab;
+  d.N = c.n_codebooks;
+  d.page_tokens = c.page_tokens;
+  d.pages_per_seq = (c.max_ctx + c.page_tokens - 1) / c.page_tokens;
+  d.n_layer = c.n_layer;
+  d.fast_n_layer = c.fast_n_layer;
+  d.max_pages = c.max_pages;
+  d.rope_len = std::max(c.max_ctx, c.n_codebooks) + 1;
+  d.max_seqs = c.max_seqs;
+  d.qkv_dim = (c.n_head + 2 * c.n_kv_head) * c.head_dim;
+  d.logit_ld = ((std::max(c.n_sem + 1, c.fast_vocab) + 3) / 4) * 4;
+  d.eps = c.norm_eps;
+  d.wait_limit_ns = 2000000000ull;
+
+  const size_t R = kMaxRows;
+  const int half = c.head_dim / 2;
+  const int G = c.n_head / c.n_kv_head;
+  uint16_t *rc_cos = nullptr, *rc_sin = nullptr;
+  const size_t kv_elems = static_cast<size_t>(c.max_pages) * c.n_layer * 2 * c.n_kv_head *
+                          c.page_tokens * c.head_dim;
+#define ALLOC(p, n)                                   \
+  do {                                                \
+    if ((rc = dev_alloc(h, &(p), (n))) != DUALAR_OK) return fail(rc); \
+  } while (0)
+  ALLOC(rc_cos, static_cast<size_t>(d.rope_len) * half);
+  ALLOC(rc_sin, static_cast<size_t>(d.rope_len) * half);
+  d.rope_cos = rc_cos;
+  d.rope_sin = rc_sin;
+  ALLOC(d.kv_pool, kv_elems);
+  ALLOC(d.page_table, static_cast<size_t>(c.max_seqs) * d.pages_per_seq);
+  ALLOC(d.fast_kv, R * c.fast_n_layer * 2 * c.n_kv_head * c.n_codebooks * c.head_dim);
+  ALLOC(d.h_last, static_cast<size_t>(c.max_seqs) * c.dim);
+  ALLOC(d.z_last, static_cast<size_t>(c.max_seqs) * (c.n_sem + 1));
+  ALLOC(d.hist, static_cast<size_t>(c.max_seqs) * kRasRing);
+  ALLOC(d.hist_n, c.max_seqs);
+  ALLOC(d.finished, c.max_seqs);
+  ALLOC(d.rows, R);
+  ALLOC(d.commit_map, R);
+  ALLOC(d.xs, R * c.dim);
+  ALLOC(d.hs, R * c.dim);
+  ALLOC(d.hf, R * c.dim);
+  ALLOC(d.fin, 2 * R * c.dim);
+  ALLOC(d.qkv, R * d.qkv_dim);
+  ALLOC(d.qrot, R * c.n_head * c.head_dim);
+  ALLOC(d.attn, R * c.n_head * c.head_dim);
+  ALLOC(d.act, R * c.ffn);
+  ALLOC(d.logits, R * d.logit_ld);
+  ALLOC(d.part, R * c.n_kv_head * kMaxChunks * G * (c.head_dim + 2));
+  ALLOC(d.arrive, R * c.n_kv_head);
+  ALLOC(d.codes_ws, R * kMaxCodebooks);
+  ALLOC(d.err, 1);
+#undef ALLOC
+
+  // RoPE tables: angle = pos * base^(-2i/head_dim) in double, cos/sin rounded
+  // once to bf16.  [P2] "Streaming: whose numbers": bf16 tables; "The slow AR
+  // is Qwen3-4B": rope_base 1e6.
+  {
+    std::vector<uint16_t> hc(static_cast<size_t>(d.rope_len) * half), hs(hc.size());
+    for (int p = 0; p < d.rope_len; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double inv = std::pow(static_cast<double>(c.rope_base), -(2.0 * i) / c.head_dim);
+        const double ang = static_cast<double>(p) * inv;
+        hc[static_cast<size_t>(p) * half + i] = host_f32_to_bf16(static_cast<float>(std::cos(ang)));
+        hs[static_cast<size_t>(p) * half + i] = host_f32_to_bf16(static_cast<float>(std::sin(ang)));
+      }
+    cudaError_t e = cudaMemcpy(rc_cos, hc.data(), hc.size() * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(rc_sin, hs.data(), hs.size() * 2, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      set_err(h, "rope upload: %s", cudaGetErrorString(e));
+      return fail(DUALAR_ERR_CUDA);
+    }
+  }
+  // page table entries start at -1 (no page)
+  {
+    std::vector<int32_t> neg(static_cast<size_t>(c.max_seqs) * d.pages_per_seq, -1);
+    if (cudaMemcpy(d.page_table, neg.data(), neg.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+      set_err(h, "page table init failed");
+      return fail(DUALAR_ERR_CUDA);
+    }
+  }
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) {
+    set_err(h, "stream sync failed after allocation");
+    return fail(DUALAR_ERR_CUDA);
+  }
+  h->length.assign(c.max_seqs, -1);
+  h->pages.assign(c.max_seqs, {});
+  for (int p = 0; p < c.max_pages; ++p) h->free_pages.insert(p);
+  *out = h;
+  return DUALAR_OK;
+}
+
+int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  const dualar_config& c = h->cfg;
+  if (slot < 0 || slot >= c.max_seqs || !tokens || n_tokens <= 0) {
+    set_err(h, "prefill: bad slot or tokens");
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  if (h->length[slot] >= 0) {
+    set_err(h, "prefill: slot %d holds a sequence", slot);
+    return DUALAR_ERR_SLOT_BUSY;
+  }
+  if (n_tokens > c.max_ctx) {
+    set_err(h, "prefill: %d tokens exceed max_ctx %d", n_tokens, c.max_ctx);
+    return DUALAR_ERR_CONTEXT_FULL;
+  }
+  for (int i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c.vocab) {
+      set_err(h, "prefill: token %d out of range", tokens[i]);
+      return DUALAR_ERR_INVALID_ARG;
+    }
+  const int need = (n_tokens + c.page_tokens - 1) / c.page_tokens;
+  if (need > static_cast<int>(h->free_pages.size())) {
+    set_err(h, "prefill: %d pages needed, %zu free", need, h->free_pages.size());
+    return DUALAR_ERR_OOM_PAGES;
+  }
+  const DevPtrs& d = h->d;
+  CUDA_TRY(h, cudaMemsetAsync(d.hist_n + slot, 0, 4, h->stream));
+  CUDA_TRY(h, cudaMemsetAsync(d.finished + slot, 0, 4, h->stream));
+  h->length[slot] = 0;
+  h->launches = 0;
+  static LaunchSetup s;
+  for (int c0 = 0; c0 < n_tokens; c0 += kMaxRows) {
+    const int m = std::min(kMaxRows, n_tokens - c0);
+    std::memset(&s, 0, sizeof(s));
+    s.n_rows = m;
+    s.commit_last_only = 1;
+    s.embed = 1;
+    for (int r = 0; r < m; ++r) {
+      const int pos = c0 + r;
+      s.rows[r] = RowInfo{slot, pos, 1, 0};
+      s.tokens[r] = tokens[pos];
+      if (pos % c.page_tokens == 0) {
+        const int pg = *h->free_pages.begin();
+        h->free_pages.erase(h->free_pages.begin());
+        h->pages[slot].push_back(pg);
+        s.upd_slot[s.n_updates] = slot;
+        s.upd_index[s.n_updates] = pos / c.page_tokens;
+        s.upd_page[s.n_updates] = pg;
+        ++s.n_updates;
+      }
+    }
+    int units = 0, chunk = 0;
+    plan_attention(h, s, &units, &chunk);
+    LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
+    TRY(slow_stack(h, m, units, chunk));
+    if (c0 + m == n_tokens) TRY(restricted_head(h, m - 1, 1));
+  }
+  h->length[slot] = n_tokens;
+  return DUALAR_OK;
+}
+
+int dualar_decode_frame(dualar_handle* h, int32_t batch, const int32_t* slots,
+                        const float* uniforms, const dualar_sampling* sampling, int32_t* codes,
+                        int32_t* status) {
+  return decode_impl(h, batch, slots, uniforms, sampling, nullptr, codes, status, nullptr, nullptr,
+                     nullptr);
+}
+
+int dualar_decode_frame_forced(dualar_handle* h, int32_t batch, const int32_t* slots,
+                               const float* uniforms, const dualar_sampling* sampling,
+                               const int32_t* forced_codes, int32_t* codes, int32_t* status,
+                               float* slow_logits, float* fast_logits, int32_t* draws) {
+  return decode_impl(h, batch, slots, uniforms, sampling, forced_codes, codes, status, slow_logits,
+                     fast_logits, draws);
+}
+
+int dualar_release(dualar_handle* h, int32_t slot) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  if (slot < 0 || slot >= h->cfg.max_seqs) {
+    set_err(h, "release: bad slot %d", slot);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  for (int p : h->pages[slot]) h->free_pages.insert(p);
+  h->pages[slot].clear();
+  h->length[slot] = -1;
+  return DUALAR_OK;
+}
+
+int dualar_sync(dualar_handle* h) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  uint32_t e = 0;
+  CUDA_TRY(h, cudaMemcpy(&e, h->d.err, 4, cudaMemcpyDeviceToHost));
+  if (e) {
+    CUDA_TRY(h, cudaMemset(h->d.err, 0, 4));
+    if (e & (DEV_ERR_MBAR_TIMEOUT | DEV_ERR_GRID_TIMEOUT)) {
+      set_err(h, "a device-side wait timed out (error word 0x%x)", e);
+      return DUALAR_ERR_TIMEOUT;
+    }
+    set_err(h, "a device-side bounds check failed (error word 0x%x)", e);
+    return DUALAR_ERR_DEVICE;
+  }
+  return DUALAR_OK;
+}
+
+int dualar_get_error(const dualar_handle* h, char* buf, size_t len) {
+  if (!h || !buf || len == 0) return DUALAR_ERR_INVALID_ARG;
+  std::snprintf(buf, len, "%s", h->err.c_str());
+  return DUALAR_OK;
+}
+
+void dualar_destroy(dualar_handle* h) {
+  if (!h) return;
+  if (!h->allocs.empty()) cudaStreamSynchronize(h->stream);
+  for (void* p : h->allocs) cudaFree(p);
+  delete h;
+}
+
+int dualar_get_page_table(const dualar_handle* h, int32_t slot, int32_t* pages,
+                          int32_t max_entries, int32_t* n_pages) {
+  if (!h || slot < 0 || slot >= h->cfg.max_seqs || !n_pages) return DUALAR_ERR_INVALID_ARG;
+  const auto& v = h->pages[slot];
+  *n_pages = static_cast<int32_t>(v.size());
+  if (pages) {
+    // read the device table (what the kernels use)
+    std::vector<int32_t> dev(h->d.pages_per_seq);
+    if (cudaMemcpy(dev.data(), h->d.page_table + static_cast<size_t>(slot) * h->d.pages_per_seq,
+                   dev.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return DUALAR_ERR_CUDA;
+    for (int i = 0; i < std::min<int>(max_entries, static_cast<int>(v.size())); ++i) pages[i] = dev[i];
+  }
+  return DUALAR_OK;
+}
+
+int dualar_get_rope_table(dualar_handle* h, int32_t n_pos, uint16_t* cos_bits, uint16_t* sin_bits) {
+  if (!h || n_pos <= 0 || n_pos > h->d.rope_len || !cos_bits || !sin_bits)
+    return DUALAR_ERR_INVALID_ARG;
+  const size_t n = static_cast<size_t>(n_pos) * (h->cfg.head_dim / 2);
+  CUDA_TRY(h, cudaMemcpy(cos_bits, h->d.rope_cos, n * 2, cudaMemcpyDeviceToHost));
+  CUDA_TRY(h, cudaMemcpy(sin_bits, h->d.rope_sin, n * 2, cudaMemcpyDeviceToHost));
+  return DUALAR_OK;
+}
+
+int dualar_read_state(dualar_handle* h, int32_t slot, float* hidden, float* logits) {
+  if (!h || slot < 0 || slot >= h->cfg.max_seqs) return DUALAR_ERR_INVALID_ARG;
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  if (hidden)
+    CUDA_TRY(h, cudaMemcpy(hidden, h->d.h_last + static_cast<size_t>(slot) * h->cfg.dim,
+                           sizeof(float) * h->cfg.dim, cudaMemcpyDeviceToHost));
+  if (logits)
+    CUDA_TRY(h, cudaMemcpy(logits, h->d.z_last + static_cast<size_t>(slot) * (h->cfg.n_sem + 1),
+                           sizeof(float) * (h->cfg.n_sem + 1), cudaMemcpyDeviceToHost));
+  return DUALAR_OK;
+}
+
+int32_t dualar_slot_length(const dualar_handle* h, int32_t slot) {
+  if (!h || slot < 0 || slot >= h->cfg.max_seqs) return -1;
+  return h->length[slot];
+}
+
+int dualar_set_wait_limit(dualar_handle* h, uint64_t nanoseconds) {
+  if (!h || nanoseconds == 0) return DUALAR_ERR_INVALID_ARG;
+  h->d.wait_limit_ns = nanoseconds;
+  return DUALAR_OK;
+}
+
+int32_t dualar_last_launch_count(const dualar_handle* h) { return h ? h->launches : -1; }
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// Device-side helpers shared by the Dual-AR kernels (sm_103a).
+//
+// PTX wrappers for mbarriers and the bulk-copy engine (cp.async.bulk), bf16
+// unpacking, warp/block reductions and bounded waits.  Every wait in this
+// library gives up after a time limit, records an error code in the device
+// error word and returns, so a missed arrival never hangs the GPU.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+#define DEVI __device__ __forceinline__
+
+namespace dualar {
+
+DEVI void raise_error(uint32_t* err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+DEVI uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- shared-memory addresses and mbarriers ---------------------------------
+DEVI uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+DEVI void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+DEVI void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+DEVI void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; gives up after
+// limit_ns, raising DEV_ERR_MBAR_TIMEOUT.  Returns false on timeout.
+DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      raise_error(err, DEV_ERR_MBAR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// One bulk copy global -> shared (no tensor map), completing on an mbarrier
+// with a transaction count.  dst/src 16-byte aligned, bytes a multiple of 16.
+// The L2 policy marks the source lines evict-first: weights are streamed
+// once per use and should not push activations or KV out of L2.
+DEVI void bulk_load_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                        uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+DEVI uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Named barrier over a subset of the block's warps (the consumer warps).
+DEVI void named_barrier(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+DEVI uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+DEVI uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// ---- bf16 ------------------------------------------------------------------
+// Two bf16 packed in a 32-bit word -> two floats (exact widening).
+DEVI float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+DEVI float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+DEVI float bf16bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+DEVI uint16_t f32_to_bf16bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// 8 bf16 (one 16-byte vector) dotted with 8 floats.
+DEVI float dot8(const uint4 w, const float4 a, const float4 b, float acc) {
+  acc = fmaf(bf16lo(w.x), a.x, acc);
+  acc = fmaf(bf16hi(w.x), a.y, acc);
+  acc = fmaf(bf16lo(w.y), a.z, acc);
+  acc = fmaf(bf16hi(w.y), a.w, acc);
+  acc = fmaf(bf16lo(w.z), b.x, acc);
+  acc = fmaf(bf16hi(w.z), b.y, acc);
+  acc = fmaf(bf16lo(w.w), b.z, acc);
+  acc = fmaf(bf16hi(w.w), b.w, acc);
+  return acc;
+}
+
+// ---- reductions --------------------------------------------------------------
+DEVI float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+DEVI float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+DEVI float silu(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace dualar

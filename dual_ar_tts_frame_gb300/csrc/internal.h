@@ -1,0 +1,140 @@
+// Internal declarations shared by the host runtime (api.cu) and the kernels
+// (kernels.cu).  Not part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dualar {
+
+constexpr int kMaxRows = 128;        // rows per launch: decode batch or prefill chunk
+constexpr int kMaxCodebooks = 16;
+constexpr int kRasRing = 16;         // RAS history ring per slot (window <= 16)
+constexpr int kMaxChunks = 64;       // split-KV chunks per (row, KV head)
+constexpr int kMaxGroup = 8;         // query heads per KV head
+constexpr int kGemvConsumerWarps = 8;
+constexpr int kGemvThreads = (kGemvConsumerWarps + 1) * 32;
+constexpr int kSampThreads = 512;
+constexpr int kSampPerThread = 9;    // candidates per sampler thread (<= 4608 candidates)
+
+// Device error word: bit flags OR-ed in by kernels, read by dualar_sync.
+enum : uint32_t {
+  DEV_ERR_MBAR_TIMEOUT = 1u << 0,   // an mbarrier wait gave up
+  DEV_ERR_GRID_TIMEOUT = 1u << 1,   // a grid-wide barrier gave up
+  DEV_ERR_BAD_INDEX = 1u << 2,      // an index failed its bounds check (access skipped)
+  DEV_ERR_BAD_PAGE = 1u << 3,       // a page-table entry was out of range (access skipped)
+};
+
+// One row of a launch: a sequence (slot) writing one position.
+struct RowInfo {
+  int32_t slot;
+  int32_t pos;
+  int32_t active;    // 0: this row's KV writes and state commits are skipped
+  int32_t unit0;     // first split-KV attention unit of this row
+};
+
+// Passed by value to the setup kernel at the start of every launch sequence.
+struct LaunchSetup {
+  int32_t n_rows;
+  int32_t n_updates;                 // page-table updates
+  int32_t commit_last_only;          // prefill: only the last row commits state
+  int32_t embed;                     // prefill: gather tok_emb rows into xs
+  RowInfo rows[kMaxRows];
+  int32_t upd_slot[kMaxRows];
+  int32_t upd_index[kMaxRows];
+  int32_t upd_page[kMaxRows];
+  int32_t tokens[kMaxRows];          // prefill ids (unused in decode)
+};
+
+enum GemvMode : int { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2 };
+
+struct GemvArgs {
+  const uint16_t* w0;      // [n0][K] bf16 (segment 0, or the gate matrix)
+  const uint16_t* w1;      // [n1][K] bf16 (segment 1, or the up matrix)
+  int n0, n1;              // rows of the two segments (SWIGLU: n1 = n0)
+  int K;
+  int mode;
+  int nb;                  // activation rows in this launch
+  const float* x;          // [nb][ldx] input rows (fp32)
+  int ldx;
+  const uint16_t* norm_w;  // RMSNorm gain [K] (bf16) applied to x first, or null
+  float eps;
+  const float* base;       // GEMV_ADD: out = base + W x  (may alias out)
+  int ldb;
+  float* out;
+  int ldo;
+  const int32_t* out_map;  // optional: batch row b writes out row out_map[b] (< 0: skip)
+  float* save_x;           // optional: CTA 0 stores the normalized x rows here
+  const int32_t* save_map; // row map for save_x (< 0: skip)
+  int lds;
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+};
+
+// Device buffers of one handle that kernels need (plain pointers).
+struct DevPtrs {
+  // shapes
+  int D, Hq, Hkv, hd, F, n_sem, sem_begin, im_end, Cf, N, page_tokens, pages_per_seq, n_layer,
+      fast_n_layer, max_pages, rope_len, max_seqs, qkv_dim, logit_ld;
+  float eps;
+  // tables and caches
+  const uint16_t* rope_cos;   // [rope_len][hd/2] bf16
+  const uint16_t* rope_sin;
+  uint16_t* kv_pool;          // [max_pages][n_layer][2][Hkv][page_tokens][hd] bf16
+  int32_t* page_table;        // [max_seqs][pages_per_seq]
+  float* fast_kv;             // [kMaxRows][fast_n_layer][2][Hkv][N][hd] fp32
+  // per-slot state
+  float* h_last;              // [max_seqs][D]   final-normed hidden of the last position
+  float* z_last;              // [max_seqs][n_sem+1] restricted logits
+  int32_t* hist;              // [max_seqs][kRasRing]
+  int32_t* hist_n;            // [max_seqs]
+  int32_t* finished;          // [max_seqs]
+  // per-launch rows
+  RowInfo* rows;              // [kMaxRows]
+  int32_t* commit_map;        // [kMaxRows] slot to commit state to, or -1
+  // work buffers
+  float* xs;                  // [kMaxRows][D] slow input (fusion / embedding)
+  float* hs;                  // [kMaxRows][D] slow residual stream
+  float* hf;                  // [kMaxRows][D] fast residual stream
+  float* fin;                 // [2][kMaxRows][D] fast-pass inputs
+  float* qkv;                 // [kMaxRows][qkv_dim]
+  float* qrot;                // [kMaxRows][Hq][hd]
+  float* attn;                // [kMaxRows][Hq*hd]
+  float* act;                 // [kMaxRows][F]
+  float* logits;              // [kMaxRows][logit_ld]
+  float* part;                // split-KV partials [kMaxRows][Hkv][kMaxChunks][G][hd+2]
+  uint32_t* arrive;           // [kMaxRows][Hkv] last-arriver counters
+  int32_t* codes_ws;          // [kMaxRows][kMaxCodebooks] codes of the current frame
+  uint32_t* err;              // device error word
+  uint64_t wait_limit_ns;
+};
+
+struct SamplingParams {
+  float temperature, top_p;
+  int32_t ras_win;
+  float ras_temperature, ras_top_p;
+  int32_t allow_eos;
+};
+
+// ---- launchers (kernels.cu) -------------------------------------------------
+cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t* tok_emb,
+                         cudaStream_t st);
+cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st);
+cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int fast_pos,
+                          const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st);
+cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,
+                              int chunk_tokens, int n_sm, cudaStream_t st);
+cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int npos, cudaStream_t st);
+cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms, int ldu,
+                             const SamplingParams& sp, const int32_t* forced, int ldf,
+                             int32_t* codes_out, int32_t* status_out, float* slow_logits_out,
+                             int32_t* draws_out, const uint16_t* fast_emb, cudaStream_t st);
+cudaError_t launch_sample_fast(const DevPtrs& d, int nrows, int k, const float* uniforms, int ldu,
+                               const SamplingParams& sp, const int32_t* forced, int ldf,
+                               int32_t* codes_out, float* fast_logits_out, int32_t* draws_out,
+                               const uint16_t* fast_emb, cudaStream_t st);
+cudaError_t launch_fusion(const DevPtrs& d, int nrows, const uint16_t* tok_emb,
+                          const uint16_t* fusion, cudaStream_t st);
+
+
+}  // namespace dualar

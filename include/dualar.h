@@ -1,0 +1,229 @@
+/* dualar.h -- C ABI of the GB300 Dual-AR frame decoder (libdualar.so).
+ *
+ * One call of dualar_decode_frame runs, for every sequence of a batch, the
+ * per-frame Dual-Autoregressive decode step of a Fish-Speech-S2-shaped model:
+ *
+ *   1. draw q0 from the restricted slow-AR logits held since the last slow step
+ *      (temperature / top-p, with the repetition-aware resample);
+ *   2. N fast-AR passes along the codebook axis, drawing q1 .. q(N-1);
+ *   3. multi-codebook fusion of the N codes into the next slow-AR input;
+ *   4. one slow-AR decode position on that input over the paged KV cache,
+ *      ending in the restricted head (semantic ids + <|im_end|>).
+ *
+ * Pages the operations follow (title, section):
+ *   [P1] "How the Dual-Autoregressive Architecture Works in Fish Speech S2:
+ *        A Deep Dive" -- Core Components (slow BaseTransformer, fast
+ *        sub-network, DualARModelArgs), Inference Pipeline
+ *        (decode_one_token_ar, generate).
+ *   [P2] "Fish Audio S2: a Qwen3-4B on the time axis, four layers on the
+ *        codebook axis, and tags that are only text" -- fact table (shapes),
+ *        "Two autoregressions" (per-frame order, semantic logit bias,
+ *        repetition-aware sampling, fast KV cache, Eq. 1 fusion with the
+ *        1/sqrt(N+1) scale), "The slow AR is Qwen3-4B" (Qwen3 layer,
+ *        qk-norm, rope_base, tied head, semantic id range), "Streaming"
+ *        (bf16 RoPE tables).
+ *
+ * Conventions for every call:
+ *   - Return value: DUALAR_OK (0) or a negative DUALAR_ERR_* code.  Nothing
+ *     aborts the process; dualar_get_error returns the last message.
+ *   - All GPU work is queued on the CUDA stream given to dualar_create and is
+ *     asynchronous: outputs and device-side errors become visible after the
+ *     stream is synchronised (dualar_sync does that and reports device-side
+ *     errors such as a wait that timed out).
+ *   - "device" pointers are CUDA device memory, "host" pointers CPU memory.
+ *   - The caller owns the weights, uniforms and output buffers; the library
+ *     owns the KV page pool, per-sequence state and work buffers, all
+ *     allocated by dualar_create and freed by dualar_destroy.
+ *   - One handle is not thread-safe; calls on it must be serialised.
+ */
+#ifndef DUALAR_H
+#define DUALAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  DUALAR_OK = 0,
+  DUALAR_ERR_INVALID_ARG = -1,   /* bad pointer, size, slot or config field */
+  DUALAR_ERR_OOM_PAGES = -2,     /* the KV page pool has no free page left */
+  DUALAR_ERR_SLOT_BUSY = -3,     /* prefill on a slot that holds a sequence */
+  DUALAR_ERR_SLOT_EMPTY = -4,    /* decode on a slot that was never prefilled */
+  DUALAR_ERR_CUDA = -5,          /* a CUDA runtime call failed */
+  DUALAR_ERR_TIMEOUT = -6,       /* a device-side wait gave up (see dualar_sync) */
+  DUALAR_ERR_DEVICE = -7,        /* a device-side bounds check failed (see dualar_sync) */
+  DUALAR_ERR_CONTEXT_FULL = -8   /* the sequence reached max_ctx positions */
+};
+
+/* Model shapes and runtime limits.  [P1] DualARModelArgs: the fast AR has
+ * the slow AR's width and heads (fast_dim = dim; no fast_project_in).
+ * Requirements: dim % 8 == 0, ffn % 8 == 0, head_dim in {64, 128},
+ * n_head % n_kv_head == 0 with n_head / n_kv_head in {1, 2, 4, 8},
+ * page_tokens == 64, n_codebooks in [2, 16], n_sem + 1 <= 4608,
+ * fast_vocab <= 4608, im_end_id outside [sem_begin, sem_begin + n_sem). */
+typedef struct dualar_config {
+  int32_t dim;           /* model width D */
+  int32_t n_layer;       /* slow-AR layers */
+  int32_t n_head;        /* query heads */
+  int32_t n_kv_head;     /* key/value heads */
+  int32_t head_dim;
+  int32_t ffn;           /* SwiGLU intermediate size */
+  int32_t vocab;         /* slow vocabulary (tied embedding rows) */
+  int32_t sem_begin;     /* first <|semantic:i|> id */
+  int32_t n_sem;         /* number of semantic ids S */
+  int32_t im_end_id;     /* <|im_end|> id */
+  int32_t fast_n_layer;  /* fast-AR layers */
+  int32_t fast_vocab;    /* fast embedding / head rows (codebook_size) */
+  int32_t n_codebooks;   /* N codes per frame */
+  int32_t slow_qk_norm;  /* 1: per-head RMSNorm on q, k in the slow AR */
+  int32_t fast_qk_norm;  /* 1: same in the fast AR (0 for S2) */
+  int32_t page_tokens;   /* positions per KV page (64) */
+  int32_t max_pages;     /* KV pages in the pool */
+  int32_t max_seqs;      /* slots; also the largest decode batch (<= 128) */
+  int32_t max_ctx;       /* positions per sequence */
+  float rope_base;       /* 1e6 for S2 */
+  float norm_eps;        /* RMSNorm epsilon */
+} dualar_config;
+
+/* One transformer block's weights: device pointers to bf16 row-major
+ * matrices [out][in], 16-byte aligned.  q_norm / k_norm may be NULL when the
+ * block has no QK-norm. */
+typedef struct dualar_layer_weights {
+  const void* attn_norm;  /* [dim] */
+  const void* wqkv;       /* [(n_head + 2 n_kv_head) head_dim][dim]: q rows, then k, then v */
+  const void* q_norm;     /* [head_dim] */
+  const void* k_norm;     /* [head_dim] */
+  const void* wo;         /* [dim][n_head head_dim] */
+  const void* ffn_norm;   /* [dim] */
+  const void* w_gate;     /* [ffn][dim] */
+  const void* w_up;       /* [ffn][dim] */
+  const void* w_down;     /* [dim][ffn] */
+} dualar_layer_weights;
+
+/* All weights (device pointers, bf16, 16-byte aligned; they must stay valid
+ * for the handle's lifetime).  slow and fast are HOST arrays of per-layer
+ * structs, copied by dualar_create. */
+typedef struct dualar_weights {
+  const void* tok_emb;                 /* [vocab][dim]; also the tied slow head */
+  const void* final_norm;              /* [dim] */
+  const dualar_layer_weights* slow;    /* host array [n_layer] */
+  const void* fast_emb;                /* [fast_vocab][dim] */
+  const dualar_layer_weights* fast;    /* host array [fast_n_layer] */
+  const void* fast_norm;               /* [dim] */
+  const void* fast_out;                /* [fast_vocab][dim] (untied) */
+  const void* fusion;                  /* [n_sem + (n_codebooks-1) fast_vocab][dim]:
+                                          codebook 0 rows, then codebooks 1..N-1 */
+} dualar_weights;
+
+/* Sampling parameters of a decode call.  [P2] "Two autoregressions": the
+ * repetition-aware resample draws at ras_temperature 1.0 / ras_top_p 0.9 and
+ * replaces q0 when q0 repeats a semantic code among the last ras_win
+ * (<= 16; 0 disables) committed q0 of the sequence.  temperature 0 is greedy
+ * (largest logit, lowest id on ties).  allow_eos = 0 removes <|im_end|> from
+ * the q0 candidates. */
+typedef struct dualar_sampling {
+  float temperature;
+  float top_p;
+  int32_t ras_win;
+  float ras_temperature;
+  float ras_top_p;
+  int32_t allow_eos;
+} dualar_sampling;
+
+typedef struct dualar_handle dualar_handle;
+
+/* Creates a decoder on the current CUDA device.  cfg, w: host structs (read
+ * during the call).  cuda_stream: a cudaStream_t (NULL = legacy default
+ * stream) on which all later work is queued.  Allocates the KV pool
+ * (max_pages x n_layer x 2 x n_kv_head x page_tokens x head_dim bf16), the
+ * per-slot state and the work buffers.  On failure *out is NULL. */
+int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_stream,
+                  dualar_handle** out);
+
+/* Runs the slow AR over a prompt and starts a sequence in an empty slot.
+ * [P2] "Two autoregressions" / "Speakers and turns": prompt ids are embedded
+ * with the slow embedding (no fusion).  tokens: host int32[n_tokens], ids in
+ * [0, vocab).  Leaves the slot holding the final-normed hidden state and the
+ * restricted logits of the last prompt position, from which the first
+ * decode_frame draws q0.  Errors: INVALID_ARG, SLOT_BUSY, OOM_PAGES,
+ * CONTEXT_FULL, CUDA. */
+int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens);
+
+/* Decodes one frame for `batch` sequences.  [P1] "decode_one_token_ar";
+ * [P2] "Two autoregressions".
+ *   slots:    host int32[batch], distinct prefilled slots
+ *   uniforms: device float[batch][n_codebooks + 1] in [0, 1):
+ *             u[0] normal q0 draw, u[1] resample draw, u[k+1] draw of q_k
+ *   codes:    device int32[batch][n_codebooks] out: q0 as a semantic index in
+ *             [0, n_sem), q1..q(N-1) in [0, fast_vocab); -1 for a row that ended
+ *   status:   device int32[batch] out: 0 ok, 1 q0 was <|im_end|> (the sequence
+ *             ends; release the slot), 2 the slot had already ended
+ * Host-side page allocation happens before any GPU work; on OOM_PAGES or
+ * CONTEXT_FULL nothing is queued.  Errors: INVALID_ARG, SLOT_EMPTY,
+ * OOM_PAGES, CONTEXT_FULL, CUDA. */
+int dualar_decode_frame(dualar_handle* h, int32_t batch, const int32_t* slots,
+                        const float* uniforms, const dualar_sampling* sampling, int32_t* codes,
+                        int32_t* status);
+
+/* Teacher-forced / instrumented variant of dualar_decode_frame.  The draws are
+ * made exactly as in dualar_decode_frame, but when forced_codes is not NULL the
+ * codes committed (fed to the fast AR, fusion and history) are forced_codes
+ * (device int32[batch][n_codebooks], same layout as codes).  Optional device
+ * outputs (NULL to skip):
+ *   slow_logits: float[batch][n_sem + 1] restricted logits q0 was drawn from
+ *                (semantic ids in order, <|im_end|> last)
+ *   fast_logits: float[batch][n_codebooks - 1][fast_vocab] fast-head logits of
+ *                passes 1..N-1
+ *   draws:       int32[batch][n_codebooks + 2]: normal q0 draw, resample draw,
+ *                chosen q0 (before forcing), then the draws of q1..q(N-1) */
+int dualar_decode_frame_forced(dualar_handle* h, int32_t batch, const int32_t* slots,
+                               const float* uniforms, const dualar_sampling* sampling,
+                               const int32_t* forced_codes, int32_t* codes, int32_t* status,
+                               float* slow_logits, float* fast_logits, int32_t* draws);
+
+/* Ends the sequence in a slot and returns its KV pages to the pool (lowest
+ * page numbers are handed out first).  Queues nothing on the GPU. */
+int dualar_release(dualar_handle* h, int32_t slot);
+
+/* Synchronises the handle's stream and reports device-side errors:
+ * DUALAR_ERR_TIMEOUT if a bounded wait gave up, DUALAR_ERR_DEVICE if a bounds
+ * check skipped an access.  Clears the device error word. */
+int dualar_sync(dualar_handle* h);
+
+/* Copies the last error message (NUL-terminated, truncated to len). */
+int dualar_get_error(const dualar_handle* h, char* buf, size_t len);
+
+/* Frees everything the handle allocated (after synchronising its stream). */
+void dualar_destroy(dualar_handle* h);
+
+/* ---- inspection (tests) ------------------------------------------------ */
+
+/* Host copy of a slot's page-table entries: pages[0 .. *n_pages-1]. */
+int dualar_get_page_table(const dualar_handle* h, int32_t slot, int32_t* pages,
+                          int32_t max_entries, int32_t* n_pages);
+
+/* Host copy of the bf16 RoPE tables (bits), [n_pos][head_dim / 2] each. */
+int dualar_get_rope_table(dualar_handle* h, int32_t n_pos, uint16_t* cos_bits,
+                          uint16_t* sin_bits);
+
+/* Synchronous host copy of a slot's held state: hidden [dim] (final-normed)
+ * and restricted logits [n_sem + 1]; either pointer may be NULL. */
+int dualar_read_state(dualar_handle* h, int32_t slot, float* hidden, float* logits);
+
+/* Next position of a slot (prompt length + frames decoded); -1 if empty. */
+int32_t dualar_slot_length(const dualar_handle* h, int32_t slot);
+
+/* Time limit of every device-side wait, in nanoseconds (default 2 s). */
+int dualar_set_wait_limit(dualar_handle* h, uint64_t nanoseconds);
+
+/* Number of kernel launches queued by the last decode call. */
+int32_t dualar_last_launch_count(const dualar_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUALAR_H */
