@@ -1,0 +1,335 @@
+#!/usr/bin/env python3
+"""Dual-AR frame-decode benchmark: frames/s, RTF and fraction of the HBM roofline.
+
+Default workload (one GPU): the full S2-Pro-shaped model at batch 1 -- a
+512-token prompt, then 256 frames (warm-up + timed) with seeded uniforms,
+T = 0.8, top-p 0.8, repetition-aware window 10, <|im_end|> excluded so every
+frame runs.  A step is one frame: q0 draw, ten fast-AR passes, fusion, one
+slow position with the restricted head.  Weights (9.1 GB) exceed L2, so no
+flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica (no collective
+on the data path); the value is the frames of all ranks over the slowest
+rank's time.  `--impl reference` times the CPU oracle on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dualar_inputs import CONFIGS, FRAMES_PER_AUDIO_SECOND  # noqa: E402
+from dualar_inputs import generators as gen  # noqa: E402
+
+METRIC = "Dual-AR frames/s (and RTF) at batch 1 and 64 on 1 GB300; % of HBM roofline"
+
+WORKLOADS = {
+    "s2pro_b1": dict(cfg="s2pro", batch=1, prompt=512, frames=256, temperature=0.8, top_p=0.8,
+                     ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 1, 512-token prompt, 256 frames, "
+                                       "T=0.8 top-p 0.8 RAS window 10"),
+    "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
+                    desc="tiny Dual-AR, batch 1, 32-token prompt, 16 frames"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="s2pro_b1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def traffic_record():
+    """ncu DRAM bytes per GEMV launch, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    src = os.path.join(ROOT, "dual_ar_tts_frame_gb300", "csrc", "kernels.cu")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p))
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return rec if rec.get("kernels_sha256") == sha else None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.th.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def time_oracle(cfg, bits, wl, prompt, uniforms, n_frames, budget_s):
+    from oracle import DualAROracle, Sampling as OSampling
+    o = DualAROracle(cfg, bits, max_pos=wl["prompt"] + wl["frames"] + 8)
+    seq = o.prefill(prompt)
+    smp = OSampling(temperature=wl["temperature"], top_p=wl["top_p"], ras_win=wl["ras_win"], allow_eos=False)
+    done = 0
+    t0 = time.perf_counter()
+    for f in range(n_frames):
+        o.decode_frame(seq, uniforms[f, 0], smp)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done, el
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    wl = WORKLOADS[args.workload]
+    cfg = CONFIGS[wl["cfg"]]
+    ws, rank, local = dist_env()
+    W = args.warmup if args.warmup is not None else min(16, wl["frames"] // 4)
+    K = args.steps if args.steps is not None else wl["frames"] - W
+    assert W >= 0 and K >= 1
+    prompt = gen.make_prompt(cfg, wl["prompt"], seed=0)
+    uni_all = gen.make_uniforms(W + K, wl["batch"], cfg, seed=1)
+    config = {"workload": f"{args.workload}: {wl['desc']}", "batch": wl["batch"],
+              "prompt_tokens": wl["prompt"], "frames": W + K,
+              "l2": "inputs larger than L2 (9.1 GB of weights streamed per frame); no flush"}
+    if args.workload == "tiny_b1":
+        config["l2"] = "tiny weights fit in L2 (parity workload, not a bench line)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        bits = gen.make_weights(cfg, seed=0)
+        done, el = time_oracle(cfg, bits, wl, prompt, uni_all, W + K, budget_s=150.0)
+        fps = done / el
+        cores = os.cpu_count()
+        line = {"impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": ws,
+                "steps": done, "warmup": 0, "ms_per_step": 1000.0 * el / done, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"{done} frames after a {wl['prompt']}-token prefill "
+                                           f"(prefill untimed), NumPy fp32 on {cores} host threads"},
+                "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling, build, upload_weights
+    from dual_ar_tts_frame_gb300 import bytemodel
+    build()
+    bits = gen.make_weights(cfg, seed=0)
+    w = upload_weights(bits)
+    if ws > 1 or args.no_cpu_baseline:
+        del bits
+        bits = None
+    b = wl["batch"]
+    max_ctx = wl["prompt"] + W + K + 8
+    pages_per = (max_ctx + cfg.page_tokens - 1) // cfg.page_tokens
+    dec = DualARDecoder(cfg, w, max_pages=2 * b * pages_per + 2, max_seqs=2 * b, max_ctx=max_ctx)
+    smp = Sampling(temperature=wl["temperature"], top_p=wl["top_p"], ras_win=wl["ras_win"], allow_eos=False)
+    slots = list(range(b))
+    for s in slots:
+        dec.prefill(s, prompt)
+    dec.sync()
+    uni = torch.from_numpy(uni_all).cuda()
+    codes = torch.empty((b, cfg.n_codebooks), dtype=torch.int32, device="cuda")
+    status = torch.empty((b,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for f in range(W):
+        dec.decode_frame(slots, uni[f], smp, codes, status)
+    dec.sync()
+    launches_per_frame = dec.last_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    dec.profile(True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for f in range(W, W + K):
+            dec.decode_frame(slots, uni[f], smp, codes, status)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    dec.profile(False)
+    dec.sync()
+    prof = dec.profile_read()
+    ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    frames = b * K * ws
+    value = frames / (ms / 1000.0)
+    ms_per_step = ms / K
+    # byte model over the timed frames: contexts grow by one per frame
+    att = [wl["prompt"] + f + 1 for f in range(W, W + K)]
+    bytes_total = sum(bytemodel.frame_bytes(cfg, [a] * b) for a in att)
+    peak, peak_src = peaks()
+    frame_gbs = bytes_total / (ms / 1000.0) / 1e9
+    gemv_gbs = prof["total_bytes"] / (prof["total_ms"] / 1000.0) / 1e9 if prof["total_ms"] > 0 else None
+    tr = traffic_record()
+
+    e2e = None
+    if not args.no_e2e:
+        # end to end through the public API: pinned host uniforms in, codes and
+        # status out, the host reading each frame's result before the next
+        eslots = [b + s for s in slots]
+        for s in eslots:
+            dec.prefill(s, prompt)
+        dec.sync()
+        hu = torch.from_numpy(uni_all).pin_memory()
+        du = torch.empty((b, cfg.n_codebooks + 1), dtype=torch.float32, device="cuda")
+        hc = torch.empty((b, cfg.n_codebooks), dtype=torch.int32).pin_memory()
+        hs = torch.empty((b,), dtype=torch.int32).pin_memory()
+        for f in range(W):
+            du.copy_(hu[f], non_blocking=True)
+            dec.decode_frame(eslots, du, smp, codes, status)
+            hc.copy_(codes, non_blocking=True)
+            hs.copy_(status, non_blocking=True)
+            stream.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for f in range(W, W + K):
+            du.copy_(hu[f], non_blocking=True)
+            dec.decode_frame(eslots, du, smp, codes, status)
+            hc.copy_(codes, non_blocking=True)
+            hs.copy_(status, non_blocking=True)
+            stream.synchronize()
+            assert int(hs[0]) == 0
+        el = time.perf_counter() - t0
+        if ws > 1:
+            t = torch.tensor([el], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            el = float(t.item())
+        e2e = {"value": b * K * ws / el, "unit": "frames/s", "h2d_bytes_per_step": hu[0].numel() * 4,
+               "d2h_bytes_per_step": hc.numel() * 4 + hs.numel() * 4}
+
+    cpu = None
+    if rank == 0 and ws == 1 and bits is not None:
+        n_or = 8 if cfg.name == "s2pro" else 16
+        done, el = time_oracle(cfg, bits, wl, prompt, uni_all, n_or, budget_s=25.0)
+        cpu = {"value": done / el, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{done} frames of this workload after a {wl['prompt']}-token prefill "
+                         f"(prefill untimed), batch 1, NumPy fp32"}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "weights_dtype": "bf16",
+            "data": "synthetic: seeded random-init weights N(0,0.02) (norm gains 1+N(0,0.02)), "
+                    "uniform prompt ids, counter-based uniforms",
+            "config": config,
+            "rtf": FRAMES_PER_AUDIO_SECOND / (value / (b * ws)),
+            "frame_bytes_per_step": bytes_total / K,
+            "frame_roofline": {"achieved": frame_gbs, "peak": peak, "unit": "GB/s",
+                               "frac": frame_gbs / peak},
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel (weight-streaming GEMV)",
+                         "achieved": gemv_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": (gemv_gbs / peak) if gemv_gbs else None,
+                         "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                         "bytes_per_launch": prof["total_bytes"] / max(1, prof["launches"]),
+                         "avg_launch_us": 1000.0 * prof["total_ms"] / max(1, prof["launches"]),
+                         "launches": prof["launches"], "share_of_step": prof["total_ms"] / ms,
+                         "peak_source": peak_src},
+            "e2e": e2e,
+            "gpu_launches": launches_per_frame * K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

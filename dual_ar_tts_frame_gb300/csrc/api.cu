@@ -32,6 +32,11 @@ struct dualar_handle {
   std::set<int> free_pages;
   std::string err;
   int launches = 0;
+  // GEMV timing (dualar_profile)
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<double> prof_bytes;
 };
 
 namespace {
@@ -147,8 +152,42 @@ GemvArgs gemv_base(dualar_handle* h) {
   return a;
 }
 
+double gemv_bytes(const GemvArgs& a) {
+  const double rows = (a.mode == GEMV_SWIGLU) ? 2.0 * a.n0 : static_cast<double>(a.n0 + a.n1);
+  const double out_rows = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
+  double b = rows * a.K * 2.0;                       // weights
+  b += static_cast<double>(a.nb) * a.K * 4.0;        // x
+  if (a.norm_w) b += a.K * 2.0;                      // norm gain
+  b += static_cast<double>(a.nb) * out_rows * 4.0;   // y
+  if (a.mode == GEMV_ADD) b += static_cast<double>(a.nb) * out_rows * 4.0;   // residual base
+  return b;
+}
+
+cudaEvent_t next_event(dualar_handle* h) {
+  if (h->ev_used == h->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->ev_pool.push_back(e);
+  }
+  return h->ev_pool[h->ev_used++];
+}
+
 int run_gemv(dualar_handle* h, GemvArgs a) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (h->profiling) {
+    e0 = next_event(h);
+    e1 = next_event(h);
+    if (!e0 || !e1) {
+      set_err(h, "cudaEventCreate failed");
+      return DUALAR_ERR_CUDA;
+    }
+    CUDA_TRY(h, cudaEventRecord(e0, h->stream));
+  }
   LAUNCH(h, launch_gemv(a, h->n_sm, h->stream));
+  if (h->profiling) {
+    CUDA_TRY(h, cudaEventRecord(e1, h->stream));
+    h->prof_bytes.push_back(gemv_bytes(a));
+  }
   return DUALAR_OK;
 }
 
@@ -646,6 +685,7 @@ void dualar_destroy(dualar_handle* h) {
   if (!h) return;
   if (!h->allocs.empty()) cudaStreamSynchronize(h->stream);
   for (void* p : h->allocs) cudaFree(p);
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   delete h;
 }
 
@@ -698,5 +738,33 @@ int dualar_set_wait_limit(dualar_handle* h, uint64_t nanoseconds) {
 }
 
 int32_t dualar_last_launch_count(const dualar_handle* h) { return h ? h->launches : -1; }
+
+int dualar_profile(dualar_handle* h, int32_t enable) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  h->profiling = enable != 0;
+  return DUALAR_OK;
+}
+
+int dualar_profile_read(dualar_handle* h, int64_t* launches, double* total_ms, double* total_bytes,
+                        double* max_ms) {
+  if (!h || !launches || !total_ms || !total_bytes || !max_ms) return DUALAR_ERR_INVALID_ARG;
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  const size_t n = h->prof_bytes.size();
+  double t = 0.0, b = 0.0, mx = 0.0;
+  for (size_t i = 0; i < n; ++i) {
+    float ms = 0.f;
+    CUDA_TRY(h, cudaEventElapsedTime(&ms, h->ev_pool[2 * i], h->ev_pool[2 * i + 1]));
+    t += ms;
+    mx = std::max(mx, static_cast<double>(ms));
+    b += h->prof_bytes[i];
+  }
+  *launches = static_cast<int64_t>(n);
+  *total_ms = t;
+  *total_bytes = b;
+  *max_ms = mx;
+  h->prof_bytes.clear();
+  h->ev_used = 0;
+  return DUALAR_OK;
+}
 
 }  // extern "C"

@@ -1,0 +1,187 @@
+"""Thin Python wrapper over the C ABI: holds the handle and the weight tensors.
+
+PyTorch is used for device memory and streams only; each method marshals its
+arguments and calls one libdualar.so entry point.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+@dataclasses.dataclass
+class Sampling:
+    temperature: float = 0.8
+    top_p: float = 0.8
+    ras_win: int = 10
+    allow_eos: bool = True
+    ras_temperature: float = 1.0
+    ras_top_p: float = 0.9
+
+    def c(self) -> L.dualar_sampling:
+        return L.dualar_sampling(self.temperature, self.top_p, self.ras_win, self.ras_temperature,
+                                 self.ras_top_p, int(self.allow_eos))
+
+
+def upload_weights(bits: dict[str, np.ndarray], device="cuda") -> dict[str, torch.Tensor]:
+    """bf16 bit arrays (uint16) -> bf16 device tensors, unchanged bytes."""
+    out = {}
+    for k, v in bits.items():
+        t = torch.from_numpy(np.ascontiguousarray(v).view(np.int16))
+        out[k] = t.to(device).view(torch.bfloat16)
+    return out
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+class DualARDecoder:
+    def __init__(self, cfg, weights: dict[str, torch.Tensor], max_pages: int, max_seqs: int,
+                 max_ctx: int, stream: torch.cuda.Stream | None = None):
+        self.lib = L.lib()
+        self.cfg = cfg
+        self.max_pages = max_pages
+        self.max_seqs = max_seqs
+        self.max_ctx = max_ctx
+        self.weights = weights        # keeps the device memory alive
+        self.stream = stream or torch.cuda.current_stream()
+        c = L.dualar_config(
+            dim=cfg.dim, n_layer=cfg.n_layer, n_head=cfg.n_head, n_kv_head=cfg.n_kv_head,
+            head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab, sem_begin=cfg.sem_begin,
+            n_sem=cfg.n_sem, im_end_id=cfg.im_end_id, fast_n_layer=cfg.fast_n_layer,
+            fast_vocab=cfg.fast_vocab, n_codebooks=cfg.n_codebooks, slow_qk_norm=int(cfg.slow_qk_norm),
+            fast_qk_norm=int(cfg.fast_qk_norm), page_tokens=cfg.page_tokens, max_pages=max_pages,
+            max_seqs=max_seqs, max_ctx=max_ctx, rope_base=cfg.rope_base, norm_eps=cfg.norm_eps)
+        w = weights
+
+        def layer(p, qk):
+            return L.dualar_layer_weights(
+                w[p + ".attn_norm"].data_ptr(), w[p + ".wqkv"].data_ptr(),
+                w[p + ".q_norm"].data_ptr() if qk else None, w[p + ".k_norm"].data_ptr() if qk else None,
+                w[p + ".wo"].data_ptr(), w[p + ".ffn_norm"].data_ptr(), w[p + ".w_gate"].data_ptr(),
+                w[p + ".w_up"].data_ptr(), w[p + ".w_down"].data_ptr())
+
+        slow = (L.dualar_layer_weights * cfg.n_layer)(
+            *[layer(f"slow.{i}", cfg.slow_qk_norm) for i in range(cfg.n_layer)])
+        fast = (L.dualar_layer_weights * cfg.fast_n_layer)(
+            *[layer(f"fast.{i}", cfg.fast_qk_norm) for i in range(cfg.fast_n_layer)])
+        cw = L.dualar_weights(w["tok_emb"].data_ptr(), w["final_norm"].data_ptr(), slow,
+                              w["fast_emb"].data_ptr(), fast, w["fast_norm"].data_ptr(),
+                              w["fast_out"].data_ptr(), w["fusion"].data_ptr())
+        h = ctypes.c_void_p()
+        rc = self.lib.dualar_create(ctypes.byref(c), ctypes.byref(cw),
+                                    ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
+        if rc != L.DUALAR_OK:
+            raise L.DualARError(rc, "dualar_create failed (message on stderr)")
+        self.h = h
+
+    # ---- helpers ----------------------------------------------------------
+    def _check(self, rc: int):
+        if rc != L.DUALAR_OK:
+            buf = ctypes.create_string_buffer(512)
+            self.lib.dualar_get_error(self.h, buf, 512)
+            raise L.DualARError(rc, buf.value.decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.dualar_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- C ABI ------------------------------------------------------------
+    def prefill(self, slot: int, tokens) -> None:
+        t = np.ascontiguousarray(np.asarray(tokens, np.int32))
+        self._check(self.lib.dualar_prefill(self.h, slot, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                            t.size))
+
+    def decode_frame(self, slots, uniforms: torch.Tensor, sampling: Sampling,
+                     codes: torch.Tensor | None = None, status: torch.Tensor | None = None):
+        s = np.ascontiguousarray(np.asarray(slots, np.int32))
+        b = s.size
+        n = self.cfg.n_codebooks
+        if codes is None:
+            codes = torch.empty((b, n), dtype=torch.int32, device=uniforms.device)
+        if status is None:
+            status = torch.empty((b,), dtype=torch.int32, device=uniforms.device)
+        smp = sampling.c()
+        self._check(self.lib.dualar_decode_frame(
+            self.h, b, s.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(uniforms),
+            ctypes.byref(smp), _ptr(codes), _ptr(status)))
+        return codes, status
+
+    def decode_frame_forced(self, slots, uniforms: torch.Tensor, sampling: Sampling,
+                            forced: torch.Tensor | None, want_logits: bool = True):
+        s = np.ascontiguousarray(np.asarray(slots, np.int32))
+        b = s.size
+        cfg = self.cfg
+        dev = uniforms.device
+        codes = torch.empty((b, cfg.n_codebooks), dtype=torch.int32, device=dev)
+        status = torch.empty((b,), dtype=torch.int32, device=dev)
+        slow = torch.empty((b, cfg.n_sem + 1), dtype=torch.float32, device=dev) if want_logits else None
+        fastl = (torch.empty((b, cfg.n_codebooks - 1, cfg.fast_vocab), dtype=torch.float32, device=dev)
+                 if want_logits else None)
+        draws = torch.empty((b, cfg.n_codebooks + 2), dtype=torch.int32, device=dev)
+        smp = sampling.c()
+        self._check(self.lib.dualar_decode_frame_forced(
+            self.h, b, s.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(uniforms),
+            ctypes.byref(smp), _ptr(forced), _ptr(codes), _ptr(status), _ptr(slow), _ptr(fastl),
+            _ptr(draws)))
+        return codes, status, slow, fastl, draws
+
+    def release(self, slot: int) -> None:
+        self._check(self.lib.dualar_release(self.h, slot))
+
+    def sync(self) -> None:
+        self._check(self.lib.dualar_sync(self.h))
+
+    def page_table(self, slot: int) -> list[int]:
+        n = ctypes.c_int32()
+        self._check(self.lib.dualar_get_page_table(self.h, slot, None, 0, ctypes.byref(n)))
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        self._check(self.lib.dualar_get_page_table(self.h, slot, buf, n.value, ctypes.byref(n)))
+        return list(buf)[:n.value]
+
+    def rope_table(self, n_pos: int) -> tuple[np.ndarray, np.ndarray]:
+        half = self.cfg.head_dim // 2
+        c = np.empty((n_pos, half), np.uint16)
+        s = np.empty((n_pos, half), np.uint16)
+        self._check(self.lib.dualar_get_rope_table(self.h, n_pos, c.ctypes.data, s.ctypes.data))
+        return c, s
+
+    def read_state(self, slot: int) -> tuple[np.ndarray, np.ndarray]:
+        hid = np.empty(self.cfg.dim, np.float32)
+        z = np.empty(self.cfg.n_sem + 1, np.float32)
+        self._check(self.lib.dualar_read_state(self.h, slot, hid.ctypes.data, z.ctypes.data))
+        return hid, z
+
+    def slot_length(self, slot: int) -> int:
+        return int(self.lib.dualar_slot_length(self.h, slot))
+
+    def set_wait_limit(self, ns: int) -> None:
+        self._check(self.lib.dualar_set_wait_limit(self.h, ns))
+
+    def last_launch_count(self) -> int:
+        return int(self.lib.dualar_last_launch_count(self.h))
+
+    def profile(self, enable: bool) -> None:
+        self._check(self.lib.dualar_profile(self.h, int(enable)))
+
+    def profile_read(self) -> dict:
+        n = ctypes.c_int64()
+        t = ctypes.c_double()
+        b = ctypes.c_double()
+        m = ctypes.c_double()
+        self._check(self.lib.dualar_profile_read(self.h, ctypes.byref(n), ctypes.byref(t), ctypes.byref(b),
+                                                 ctypes.byref(m)))
+        return {"launches": n.value, "total_ms": t.value, "total_bytes": b.value, "max_ms": m.value}

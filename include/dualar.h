@@ -222,6 +222,18 @@ int dualar_set_wait_limit(dualar_handle* h, uint64_t nanoseconds);
 /* Number of kernel launches queued by the last decode call. */
 int32_t dualar_last_launch_count(const dualar_handle* h);
 
+/* GEMV timing: with enable = 1, every weight-streaming GEMV launch queued from
+ * now on is bracketed by CUDA events on the handle's stream and its
+ * algorithmic bytes (weights read + activations read and written) are
+ * recorded; enable = 0 stops recording. */
+int dualar_profile(dualar_handle* h, int32_t enable);
+
+/* Synchronises the stream, then reports the recorded GEMV launches: their
+ * count, summed device time (ms), summed algorithmic bytes, and the longest
+ * single launch (ms).  Clears the record. */
+int dualar_profile_read(dualar_handle* h, int64_t* launches, double* total_ms, double* total_bytes,
+                        double* max_ms);
+
 #ifdef __cplusplus
 }
 #endif

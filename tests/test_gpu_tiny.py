@@ -1,0 +1,260 @@
+"""GPU parity of the tiny Dual-AR against the CPU oracle, through the C ABI.
+
+Tiny config: 2+2 layers, dim 256, 4/2 heads of 64, FFN 768, vocab 1,024
+(512 semantic ids), fast vocab 128, N = 4; 32-token prompt, 16 frames under
+teacher forcing, greedy and sampled decoding.  Sizes span several GEMV
+tiles, several KV pages and split-KV chunks, and ragged batches.
+"""
+import numpy as np
+import pytest
+
+from dualar_inputs import TINY
+from dualar_inputs import generators as g
+from oracle import DualAROracle, PageOracle, Sampling as OSampling
+from oracle import model as om
+from oracle.sampler import sample_q0, sample_top_p
+from parity import DrawStats, assert_logits_close
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev_weights(tiny_bits):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dual_ar_tts_frame_gb300 import build, upload_weights
+    build()
+    return upload_weights(tiny_bits)
+
+
+def make(dev_weights, max_pages=64, max_seqs=4, max_ctx=1024):
+    from dual_ar_tts_frame_gb300 import DualARDecoder
+    return DualARDecoder(TINY, dev_weights, max_pages=max_pages, max_seqs=max_seqs, max_ctx=max_ctx)
+
+
+def gpu_sampling(o: OSampling):
+    from dual_ar_tts_frame_gb300 import Sampling
+    return Sampling(o.temperature, o.top_p, o.ras_win, o.allow_eos, o.ras_temperature, o.ras_top_p)
+
+
+def dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.cuda() if dtype is None else t.to(dtype).cuda()
+
+
+# ------------------------------------------------------------------ tables --
+
+def test_rope_table_bit_exact(dev_weights):
+    d = make(dev_weights)
+    n = 1025
+    c, s = d.rope_table(n)
+    oc, os_ = om.rope_table(n, TINY.head_dim, TINY.rope_base)
+    np.testing.assert_array_equal(c, (oc.view(np.uint32) >> 16).astype(np.uint16))
+    np.testing.assert_array_equal(s, (os_.view(np.uint32) >> 16).astype(np.uint16))
+    d.close()
+
+
+# ----------------------------------------------------------------- prefill --
+
+def test_prefill_state_matches_oracle(dev_weights, tiny_oracle):
+    d = make(dev_weights)
+    prompt = g.make_prompt(TINY, 32, seed=0)
+    d.prefill(0, prompt)
+    hid, z = d.read_state(0)
+    d.sync()
+    seq = tiny_oracle.prefill(prompt)
+    assert_logits_close(hid, seq.h_last, "prefill hidden")
+    assert_logits_close(z, seq.z_last, "prefill logits")
+    assert d.slot_length(0) == 32
+    d.close()
+
+
+# --------------------------------------------------------- teacher forcing --
+
+def run_forced(d, o, slot_prompts, n_frames, smp, seed):
+    """Teacher-forced frames for several slots; checks logits, codes, draws
+    (sampler on the GPU's own logits) and page tables."""
+    slots = list(slot_prompts)
+    seqs = {}
+    pages = PageOracle(d.max_pages, TINY.page_tokens)
+    for s, p in slot_prompts.items():
+        d.prefill(s, p)
+        seqs[s] = o.prefill(p)
+        pages.append(s, len(p))
+    b = len(slots)
+    forced = g.make_forced_codes(n_frames, b, TINY, seed=seed)
+    uni = g.make_uniforms(n_frames, b, TINY, seed=seed + 1)
+    stats = DrawStats()
+    for f in range(n_frames):
+        codes, status, slow, fast, draws = d.decode_frame_forced(
+            slots, dev(uni[f]), gpu_sampling(smp), dev(forced[f]))
+        d.sync()
+        codes, status = codes.cpu().numpy(), status.cpu().numpy()
+        slow, fast, draws = slow.cpu().numpy(), fast.cpu().numpy(), draws.cpu().numpy()
+        np.testing.assert_array_equal(codes, forced[f])
+        np.testing.assert_array_equal(status, 0)
+        for i, s in enumerate(slots):
+            hist = list(seqs[s].history)
+            r = o.decode_frame(seqs[s], uni[f, i], smp, forced=forced[f, i])
+            assert_logits_close(slow[i], r.slow_logits, f"slow logits f{f} slot {s}")
+            assert_logits_close(fast[i], r.fast_logits, f"fast logits f{f} slot {s}")
+            # sampler alone: the oracle's draws from the GPU's logits
+            n0, ras, ch = sample_q0(TINY, slow[i], smp, hist, float(uni[f, i, 0]), float(uni[f, i, 1]))
+            stats.check(draws[i, 0], n0, smp.temperature, f"q0 draw f{f}")
+            stats.check(draws[i, 1], ras, smp.ras_temperature, f"ras draw f{f}")
+            for k in range(1, TINY.n_codebooks):
+                rk = sample_top_p(fast[i, k - 1], np.arange(TINY.fast_vocab), smp.temperature, smp.top_p,
+                                  float(uni[f, i, k + 1]))
+                stats.check(draws[i, k + 2], rk, smp.temperature, f"q{k} draw f{f}")
+            pages.append(s, 1)
+    for s in slots:
+        assert d.page_table(s) == pages.table[s]
+        assert d.slot_length(s) == len(slot_prompts[s]) + n_frames
+    assert stats.compared > 0
+    return stats
+
+
+@pytest.fixture
+def dec(dev_weights):
+    d = make(dev_weights)
+    yield d
+    d.close()
+
+
+def test_teacher_forced_b1(dec, tiny_oracle):
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
+    run_forced(dec, tiny_oracle, {0: g.make_prompt(TINY, 32, seed=0)}, 16, smp, seed=3)
+
+
+def test_teacher_forced_ragged_batch(dec, tiny_oracle):
+    """Three slots with ragged contexts: multi-chunk prefill (300 > 128 rows),
+    several pages and split-KV chunks with the last-arriver combine."""
+    smp = OSampling(temperature=1.0, top_p=0.95, ras_win=10)
+    prompts = {2: g.make_prompt(TINY, 40, seed=10), 0: g.make_prompt(TINY, 300, seed=11),
+               3: g.make_prompt(TINY, 127, seed=12)}
+    run_forced(dec, tiny_oracle, prompts, 6, smp, seed=13)
+
+
+# --------------------------------------------------------- sampled replay --
+
+def run_replay(d, o, prompt, n_frames, smp, seed, use_forced_api):
+    d.prefill(1, prompt)
+    seq = o.prefill(prompt)
+    uni = g.make_uniforms(n_frames, 1, TINY, seed=seed)
+    stats = DrawStats()
+    for f in range(n_frames):
+        if use_forced_api:
+            codes, status, slow, fast, draws = d.decode_frame_forced([1], dev(uni[f]), gpu_sampling(smp), None)
+            slow, fast = slow.cpu().numpy(), fast.cpu().numpy()
+        else:
+            codes, status = d.decode_frame([1], dev(uni[f]), gpu_sampling(smp))
+            slow = fast = None
+        d.sync()
+        codes, status = codes.cpu().numpy()[0], int(status.cpu()[0])
+        assert status == 0
+        hist = list(seq.history)
+        r = o.decode_frame(seq, uni[f, 0], smp, forced=codes)   # replay the GPU trajectory
+        n0, ras, chosen = r.draws[0]
+        if slow is not None:
+            assert_logits_close(slow[0], r.slow_logits, f"slow f{f}")
+            assert_logits_close(fast[0], r.fast_logits, f"fast f{f}")
+        # q0: the committed code must be the oracle's choice when both draws
+        # that could decide it are away from every boundary
+        triggered = smp.ras_win > 0 and n0.index != TINY.n_sem and n0.index in hist[-smp.ras_win:]
+        from parity import draw_decidable
+        if draw_decidable(n0, smp.temperature) and (not triggered or draw_decidable(ras, smp.ras_temperature)):
+            stats.compared += 1
+            assert codes[0] == chosen, f"q0 f{f}: gpu {codes[0]} oracle {chosen}"
+        else:
+            stats.excluded += 1
+        for k in range(1, TINY.n_codebooks):
+            stats.check(codes[k], r.draws[k], smp.temperature, f"q{k} f{f}")
+    assert stats.compared > 0
+    return stats
+
+
+@pytest.mark.parametrize("ras_win", [0, 10])
+def test_greedy_replay(dec, tiny_oracle, ras_win):
+    smp = OSampling(temperature=0.0, top_p=0.8, ras_win=ras_win)
+    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=0), 16, smp, seed=21, use_forced_api=True)
+
+
+def test_sampled_replay_main_entry_point(dec, tiny_oracle):
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
+    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=0), 16, smp, seed=22, use_forced_api=False)
+
+
+def test_sampled_replay_with_logits(dec, tiny_oracle):
+    smp = OSampling(temperature=1.3, top_p=0.6, ras_win=4)
+    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 70, seed=5), 12, smp, seed=23, use_forced_api=True)
+
+
+# ---------------------------------------------------------- end of stream --
+
+def test_eos_and_finished_slot(dec):
+    p = g.make_prompt(TINY, 20, seed=1)
+    dec.prefill(0, p)
+    dec.prefill(1, p)
+    uni = dev(g.make_uniforms(1, 2, TINY, seed=2)[0])
+    forced = dev(np.array([[TINY.n_sem, 1, 2, 3], [5, 1, 2, 3]], np.int32))
+    smp = gpu_sampling(OSampling())
+    codes, status, _, _, _ = dec.decode_frame_forced([0, 1], uni, smp, forced)
+    dec.sync()
+    assert status.cpu().tolist() == [1, 0]
+    assert codes.cpu().numpy()[0].tolist() == [-1] * TINY.n_codebooks
+    assert codes.cpu().numpy()[1].tolist() == [5, 1, 2, 3]
+    codes, status = dec.decode_frame([0, 1], uni, smp)
+    dec.sync()
+    assert status.cpu().tolist()[0] == 2
+    assert codes.cpu().numpy()[0].tolist() == [-1] * TINY.n_codebooks
+    dec.release(0)
+    dec.prefill(0, p)           # the slot is reusable
+    codes, status = dec.decode_frame([0], uni[:1], smp)
+    dec.sync()
+    assert status.cpu().tolist() == [0]
+
+
+def test_eos_excluded_when_disallowed(dec):
+    """allow_eos = 0 removes <|im_end|> from the q0 candidates: with greedy
+    sampling and the held logits unchanged, q0 is never <|im_end|>."""
+    p = g.make_prompt(TINY, 20, seed=1)
+    dec.prefill(0, p)
+    uni = dev(g.make_uniforms(4, 1, TINY, seed=4))
+    smp = gpu_sampling(OSampling(temperature=0.0, ras_win=0, allow_eos=False))
+    for f in range(4):
+        codes, status = dec.decode_frame([0], uni[f], smp)
+        dec.sync()
+        assert status.cpu().tolist() == [0]
+        assert 0 <= int(codes.cpu()[0, 0]) < TINY.n_sem
+
+
+# ------------------------------------------------------------ error paths --
+
+def test_error_codes(dev_weights):
+    from dual_ar_tts_frame_gb300._lib import DualARError
+    d = make(dev_weights, max_pages=3, max_seqs=2, max_ctx=200)
+    p = g.make_prompt(TINY, 128, seed=1)
+    d.prefill(0, p)                                         # 2 pages
+    with pytest.raises(DualARError) as e:
+        d.prefill(0, p)
+    assert e.value.code == -3                               # SLOT_BUSY
+    with pytest.raises(DualARError) as e:
+        d.prefill(1, g.make_prompt(TINY, 129, seed=1))      # needs 3 pages, 1 free
+    assert e.value.code == -2                               # OOM_PAGES
+    uni = dev(g.make_uniforms(1, 1, TINY, seed=2)[0])
+    smp = gpu_sampling(OSampling())
+    with pytest.raises(DualARError) as e:
+        d.decode_frame([1], uni, smp)
+    assert e.value.code == -4                               # SLOT_EMPTY
+    with pytest.raises(DualARError) as e:
+        d.decode_frame([0], uni, gpu_sampling(OSampling(top_p=0.0)))
+    assert e.value.code == -1                               # INVALID_ARG
+    with pytest.raises(DualARError) as e:
+        d.prefill(1, g.make_prompt(TINY, 201, seed=1))
+    assert e.value.code == -8                               # CONTEXT_FULL
+    d.decode_frame([0], uni, smp)                           # position 128 takes page 3
+    d.sync()
+    assert d.page_table(0) == [0, 1, 2]
+    d.release(0)
+    d.close()
