@@ -34,6 +34,11 @@ class SampleResult:
     cdf_margin: float     # min |u*Z - B| / Z over the kept CDF boundaries B (incl. 0)
     cut_margin: float     # min |C - top_p| over the cumulative masses C at the cut
     gap: float            # largest minus second-largest logit
+    # diagnostics for comparisons under perturbed logits (not used by the draw)
+    pos: int = 0                       # rank of the chosen candidate in the sorted order
+    z_sorted: np.ndarray | None = None  # candidate logits in the sorted order
+    cum: np.ndarray | None = None       # cumulative normalised mass in that order
+    u: float = 0.0
 
 
 def _gap(z: np.ndarray) -> float:
@@ -51,7 +56,7 @@ def sample_top_p(z, ids, temperature: float, top_p: float, u: float) -> SampleRe
         m = z.max()
         cand = np.flatnonzero(z == m)
         idx = int(cand[np.argmin(ids[cand])])
-        return SampleResult(idx, 1, float("inf"), float("inf"), gap)
+        return SampleResult(idx, 1, float("inf"), float("inf"), gap, u=u)
     p = np.exp((z - z.max()) / temperature)
     p = p / p.sum()
     order = np.lexsort((ids, -p))          # p descending, then id ascending
@@ -68,7 +73,8 @@ def sample_top_p(z, ids, temperature: float, top_p: float, u: float) -> SampleRe
     cut = [abs(cum[k - 1] - top_p)]
     if k >= 2:
         cut.append(abs(cum[k - 2] - top_p))
-    return SampleResult(int(order[j]), k, cdf_margin, float(min(cut)), gap)
+    return SampleResult(int(order[j]), k, cdf_margin, float(min(cut)), gap, pos=j,
+                        z_sorted=z[order], cum=cum, u=u)
 
 
 def q0_candidates(cfg, allow_eos: bool):

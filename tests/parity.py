@@ -30,11 +30,31 @@ def assert_logits_close(gpu, ref, what=""):
     return err, rel
 
 
-def draw_decidable(r, temperature: float) -> bool:
-    """Whether an oracle draw is far enough from every boundary to compare."""
+def draw_decidable(r, temperature: float, eps: float = 0.0) -> bool:
+    """Whether an oracle draw must be reproduced by a sampler whose logits
+    differ from the oracle's by at most eps (max abs) -- i.e. the draw is the
+    same for every logit perturbation of that size.
+
+    Greedy: the top-1/top-2 gap exceeds max(0.1, 2 eps).  Sampled: with
+    p ~ exp(z / T), a perturbation of eps scales each mass by at most
+    exp(+-2 eps / T) after normalisation, so cumulative masses move by at
+    most exp(2 eps / T) - 1 (the top-p cut) and normalised-to-kept CDF
+    boundaries by at most exp(4 eps / T) - 1 (the draw); adjacent candidates
+    whose logits are within 2 eps may swap order.  The draw is decidable when
+    the CDF boundaries, the cut, and the logit gaps next to the chosen
+    candidate and at the cut all clear those bounds (and the fixed 1e-3
+    margins)."""
     if temperature <= 0:
-        return r.gap > GREEDY_GAP
-    return r.cdf_margin > CDF_DELTA and r.cut_margin > CUT_DELTA
+        return r.gap > max(GREEDY_GAP, 2 * eps)
+    if not (r.cdf_margin > max(CDF_DELTA, np.expm1(4 * eps / temperature))
+            and r.cut_margin > max(CUT_DELTA, np.expm1(2 * eps / temperature))):
+        return False
+    if eps > 0 and r.z_sorted is not None:
+        zs = r.z_sorted
+        for a in (r.pos - 1, r.pos, r.kept - 2, r.kept - 1):
+            if 0 <= a and a + 1 < zs.size and zs[a] - zs[a + 1] <= 2 * eps:
+                return False
+    return True
 
 
 class DrawStats:
@@ -42,8 +62,8 @@ class DrawStats:
         self.compared = 0
         self.excluded = 0
 
-    def check(self, gpu_idx: int, r, temperature: float, what: str):
-        if draw_decidable(r, temperature):
+    def check(self, gpu_idx: int, r, temperature: float, what: str, eps: float = 0.0):
+        if draw_decidable(r, temperature, eps):
             self.compared += 1
             assert int(gpu_idx) == int(r.index), f"{what}: gpu {gpu_idx} oracle {r.index}"
         else:

@@ -138,38 +138,50 @@ def test_teacher_forced_ragged_batch(dec, tiny_oracle):
 
 # --------------------------------------------------------- sampled replay --
 
-def run_replay(d, o, prompt, n_frames, smp, seed, use_forced_api):
+def run_replay(d, o, prompt, n_frames, smp, seed, twin_main_entry=False):
+    """Sampled decoding, replayed by the oracle along the GPU's trajectory.
+
+    Each GPU draw is compared with the oracle's draw from the oracle's logits
+    whenever that draw is stable under the measured logit difference eps
+    (tests/parity.py: draw_decidable).  With twin_main_entry, a second slot
+    with the same prompt runs through dualar_decode_frame and must commit
+    bit-identical codes."""
+    from parity import draw_decidable
     d.prefill(1, prompt)
+    if twin_main_entry:
+        d.prefill(2, prompt)
     seq = o.prefill(prompt)
     uni = g.make_uniforms(n_frames, 1, TINY, seed=seed)
     stats = DrawStats()
     for f in range(n_frames):
-        if use_forced_api:
-            codes, status, slow, fast, draws = d.decode_frame_forced([1], dev(uni[f]), gpu_sampling(smp), None)
-            slow, fast = slow.cpu().numpy(), fast.cpu().numpy()
-        else:
-            codes, status = d.decode_frame([1], dev(uni[f]), gpu_sampling(smp))
-            slow = fast = None
+        codes, status, slow, fast, draws = d.decode_frame_forced([1], dev(uni[f]), gpu_sampling(smp), None)
+        if twin_main_entry:
+            c2, s2 = d.decode_frame([2], dev(uni[f]), gpu_sampling(smp))
         d.sync()
         codes, status = codes.cpu().numpy()[0], int(status.cpu()[0])
+        slow, fast = slow.cpu().numpy()[0], fast.cpu().numpy()[0]
         assert status == 0
+        if twin_main_entry:
+            np.testing.assert_array_equal(c2.cpu().numpy()[0], codes)
+            assert int(s2.cpu()[0]) == 0
         hist = list(seq.history)
         r = o.decode_frame(seq, uni[f, 0], smp, forced=codes)   # replay the GPU trajectory
         n0, ras, chosen = r.draws[0]
-        if slow is not None:
-            assert_logits_close(slow[0], r.slow_logits, f"slow f{f}")
-            assert_logits_close(fast[0], r.fast_logits, f"fast f{f}")
-        # q0: the committed code must be the oracle's choice when both draws
-        # that could decide it are away from every boundary
+        assert_logits_close(slow, r.slow_logits, f"slow f{f}")
+        assert_logits_close(fast, r.fast_logits, f"fast f{f}")
+        eps0 = float(np.abs(slow - r.slow_logits).max())
+        # q0: the committed code must be the oracle's choice when every draw
+        # that decides it is stable
         triggered = smp.ras_win > 0 and n0.index != TINY.n_sem and n0.index in hist[-smp.ras_win:]
-        from parity import draw_decidable
-        if draw_decidable(n0, smp.temperature) and (not triggered or draw_decidable(ras, smp.ras_temperature)):
+        if draw_decidable(n0, smp.temperature, eps0) and (
+                not triggered or draw_decidable(ras, smp.ras_temperature, eps0)):
             stats.compared += 1
             assert codes[0] == chosen, f"q0 f{f}: gpu {codes[0]} oracle {chosen}"
         else:
             stats.excluded += 1
         for k in range(1, TINY.n_codebooks):
-            stats.check(codes[k], r.draws[k], smp.temperature, f"q{k} f{f}")
+            epsk = float(np.abs(fast[k - 1] - r.fast_logits[k - 1]).max())
+            stats.check(codes[k], r.draws[k], smp.temperature, f"q{k} f{f}", epsk)
     assert stats.compared > 0
     return stats
 
@@ -177,17 +189,17 @@ def run_replay(d, o, prompt, n_frames, smp, seed, use_forced_api):
 @pytest.mark.parametrize("ras_win", [0, 10])
 def test_greedy_replay(dec, tiny_oracle, ras_win):
     smp = OSampling(temperature=0.0, top_p=0.8, ras_win=ras_win)
-    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=0), 16, smp, seed=21, use_forced_api=True)
+    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=0), 16, smp, seed=21)
 
 
-def test_sampled_replay_main_entry_point(dec, tiny_oracle):
+def test_sampled_replay_and_main_entry_point(dec, tiny_oracle):
     smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
-    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=0), 16, smp, seed=22, use_forced_api=False)
+    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=0), 16, smp, seed=22, twin_main_entry=True)
 
 
-def test_sampled_replay_with_logits(dec, tiny_oracle):
+def test_sampled_replay_other_params(dec, tiny_oracle):
     smp = OSampling(temperature=1.3, top_p=0.6, ras_win=4)
-    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 70, seed=5), 12, smp, seed=23, use_forced_api=True)
+    run_replay(dec, tiny_oracle, g.make_prompt(TINY, 70, seed=5), 12, smp, seed=23)
 
 
 # ---------------------------------------------------------- end of stream --
