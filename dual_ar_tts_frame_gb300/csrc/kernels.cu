@@ -71,78 +71,56 @@ cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t*
 // ============================================================================
 // GEMV: y[b][n] = sum_k W[n][k] x'[b][k], x' = RMSNorm(x) (optional)
 // ============================================================================
-constexpr int kMaxTileRows = 8;
+// Each CTA owns a contiguous range of output rows (balanced to +-1 row) and
+// walks it in groups of 8 rows, one row per consumer warp.  K is cut into
+// chunks of at most kChunk elements; a ring stage holds one (group, chunk)
+// tile: up to 8 row-chunks per matrix (16 for the SwiGLU gate/up pair), each
+// fetched by one bulk copy.  A warp accumulates its row over the chunks and
+// reduces with shuffles only, so consumer warps never synchronise with each
+// other; the producer thread runs ahead by the ring depth.
+constexpr int kRowsPerGroup = kGemvConsumerWarps;   // 8
+constexpr int kChunk = 2560;                        // elements per row-chunk (one matrix)
 constexpr int kMaxStages = 8;
-constexpr int kTileTarget = 40960;       // bytes of weights per ring stage
-constexpr int kSmemBudget = 225 * 1024;  // dynamic shared memory per CTA
+constexpr int kSmemBudget = 225 * 1024;             // dynamic shared memory per CTA
 
 struct GemvPlan {
-  int R;           // rows per tile
+  int kc;          // chunk length (elements, multiple of 8)
+  int n_chunks;
+  int nmat;        // 1, or 2 for SwiGLU
   int tile_bytes;  // ring stage size
   int stages;
   int nbt;         // activation rows per launch (template)
   size_t smem;
 };
 
-__host__ __device__ inline int gemv_rows_per_tile(int K) {
-  int r = kTileTarget / (2 * K);
-  return r < 1 ? 1 : (r > kMaxTileRows ? kMaxTileRows : r);
-}
-
 // Shared-memory layout of gemv_kernel (offsets in bytes).
-__host__ __device__ inline size_t gemv_red_off() { return 256; }
-__host__ __device__ inline size_t gemv_misc_off(int nbt) {
-  return gemv_red_off() + sizeof(float) * 2 * kGemvConsumerWarps * kMaxTileRows * nbt;
-}
-__host__ __device__ inline size_t gemv_xs_off(int nbt) {
-  return (gemv_misc_off(nbt) + sizeof(float) * 64 + 127) & ~size_t(127);
-}
+__host__ __device__ inline size_t gemv_misc_off() { return 256; }
+__host__ __device__ inline size_t gemv_xs_off() { return 256 + 4 * 128; }
 __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
-  return (gemv_xs_off(nbt) + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
+  return (gemv_xs_off() + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
 }
-
-// Iterates the loads of one CTA: tiles of up to R rows inside one segment; a
-// SWIGLU tile is two loads (gate rows, then up rows).
-struct TileIter {
-  int v, v_end, n0, n1, R, mode;
-  int sub;  // SWIGLU: 0 = gate load, 1 = up load
-  __device__ bool next(int& row0, int& rows, int& seg, int& part) {
-    if (v >= v_end) return false;
-    if (mode == GEMV_SWIGLU) {
-      rows = min(R, v_end - v);
-      row0 = v;
-      seg = 0;
-      part = sub;
-      if (sub == 1) v += rows;
-      sub ^= 1;
-      return true;
-    }
-    seg = v < n0 ? 0 : 1;
-    const int seg_end = seg ? n0 + n1 : n0;
-    rows = min(R, min(v_end, seg_end) - v);
-    row0 = v;
-    part = 0;
-    v += rows;
-    return true;
-  }
-};
 
 template <int NB>
 __global__ void __launch_bounds__(kGemvThreads, 1)
-    gemv_kernel(const GemvArgs a, const int R, const int stages, const int tile_bytes) {
+    gemv_kernel(const GemvArgs a, const int kc, const int n_chunks, const int stages,
+                const int tile_bytes) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  float* red = reinterpret_cast<float*>(smem + gemv_red_off());
-  float* misc = reinterpret_cast<float*>(smem + gemv_misc_off(NB));
-  float* xs = reinterpret_cast<float*>(smem + gemv_xs_off(NB));
+  float* misc = reinterpret_cast<float*>(smem + gemv_misc_off());
+  float* xs = reinterpret_cast<float*>(smem + gemv_xs_off());
   unsigned char* ring = smem + gemv_ring_off(NB, a.K);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = a.K;
-  const int nv = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
+  const bool swiglu = a.mode == GEMV_SWIGLU;
+  const int nmat = swiglu ? 2 : 1;
+  const int nv = swiglu ? a.n0 : a.n0 + a.n1;
   const int v_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * nv) / gridDim.x);
   const int v_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * nv) / gridDim.x);
+  const int n_groups = (v_end - v_begin + kRowsPerGroup - 1) / kRowsPerGroup;
+  const int n_tiles = n_groups * n_chunks;
+  const size_t slot_bytes = static_cast<size_t>(kc) * 2;   // one row-chunk in a stage
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -158,24 +136,29 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // ---------------- producer: one thread streams the CTA's weight rows ---
     if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
-    TileIter it{v_begin, v_end, a.n0, a.n1, R, a.mode, 0};
-    int row0, rows, seg, part;
-    int i = 0;
-    while (it.next(row0, rows, seg, part)) {
-      const int s = i % stages;
-      if (i >= stages) {
-        if (!mbar_wait(&empty[s], ((i / stages) - 1) & 1, a.err, a.wait_limit_ns)) return;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int s = t % stages;
+      if (t >= stages) {
+        if (!mbar_wait(&empty[s], ((t / stages) - 1) & 1, a.err, a.wait_limit_ns)) return;
       }
-      const uint16_t* src;
-      if (a.mode == GEMV_SWIGLU)
-        src = (part ? a.w1 : a.w0) + static_cast<size_t>(row0) * K;
-      else
-        src = seg ? a.w1 + static_cast<size_t>(row0 - a.n0) * K
-                  : a.w0 + static_cast<size_t>(row0) * K;
-      const uint32_t bytes = static_cast<uint32_t>(rows) * K * 2;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_load_g2s(ring + static_cast<size_t>(s) * tile_bytes, src, bytes, &full[s], pol);
-      ++i;
+      const int g = t / n_chunks, c = t % n_chunks;
+      const int v0 = v_begin + g * kRowsPerGroup;
+      const int rows = min(kRowsPerGroup, v_end - v0);
+      const int k0 = c * kc;
+      const int len = min(kc, K - k0);
+      const uint32_t bytes = static_cast<uint32_t>(len) * 2;
+      mbar_arrive_expect_tx(&full[s], bytes * rows * nmat);
+      unsigned char* st = ring + static_cast<size_t>(s) * tile_bytes;
+      for (int m = 0; m < nmat; ++m) {
+        for (int w = 0; w < rows; ++w) {
+          const int v = v0 + w;
+          const uint16_t* rowp;
+          if (swiglu) rowp = (m ? a.w1 : a.w0) + static_cast<size_t>(v) * K;
+          else rowp = v < a.n0 ? a.w0 + static_cast<size_t>(v) * K
+                               : a.w1 + static_cast<size_t>(v - a.n0) * K;
+          bulk_load_g2s(st + (m * kRowsPerGroup + w) * slot_bytes, rowp + k0, bytes, &full[s], pol);
+        }
+      }
     }
     return;
   }
@@ -202,6 +185,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   }
   if (a.norm_w != nullptr) {
     // [P1] "Fast Transformer": RMSNorm(dim, eps=norm_eps), pre-norm blocks.
+    float* red = misc + 8;   // [8 warps][NB]
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const float w = warp_sum(ss[b]);
@@ -230,90 +214,93 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
   }
 
-  const int KV = K >> 3;  // 16-byte weight vectors per row
   const float4* xs4 = reinterpret_cast<const float4*>(xs);
-  TileIter it{v_begin, v_end, a.n0, a.n1, R, a.mode, 0};
-  int row0, rows, seg, part;
-  int i = 0;
-  float keep = 0.f;  // SWIGLU: gate output held between the two loads
-  while (it.next(row0, rows, seg, part)) {
-    const int s = i % stages;
-    if (!mbar_wait(&full[s], (i / stages) & 1, a.err, a.wait_limit_ns)) return;
-    const uint4* wt = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * tile_bytes);
-    float acc[kMaxTileRows][NB];
+  float acc[2][NB];
+  for (int t = 0; t < n_tiles; ++t) {
+    const int s = t % stages;
+    const int g = t / n_chunks, c = t % n_chunks;
+    const int v0 = v_begin + g * kRowsPerGroup;
+    const int rows = min(kRowsPerGroup, v_end - v0);
+    if (c == 0) {
 #pragma unroll
-    for (int r = 0; r < kMaxTileRows; ++r)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
-    for (int j = tid; j < KV; j += NCT) {
-      float4 xa[NB], xb[NB];
+        for (int b = 0; b < NB; ++b) acc[m][b] = 0.f;
+    }
+    if (!mbar_wait(&full[s], (t / stages) & 1, a.err, a.wait_limit_ns)) return;
+    if (warp < rows) {
+      const int k0 = c * kc;
+      const int nvec = min(kc, K - k0) >> 3;
+      const unsigned char* st = ring + static_cast<size_t>(s) * tile_bytes;
+      for (int m = 0; m < nmat; ++m) {
+        const uint4* wr = reinterpret_cast<const uint4*>(st + (m * kRowsPerGroup + warp) * slot_bytes);
+        float p0[NB], p1[NB];
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        xa[b] = xs4[(static_cast<size_t>(b) * K >> 2) + 2 * j];
-        xb[b] = xs4[(static_cast<size_t>(b) * K >> 2) + 2 * j + 1];
-      }
+        for (int b = 0; b < NB; ++b) p0[b] = p1[b] = 0.f;
+        int j = lane;
+#pragma unroll 2
+        for (; j + 32 < nvec; j += 64) {
+          const uint4 w0 = wr[j], w1 = wr[j + 32];
 #pragma unroll
-      for (int r = 0; r < kMaxTileRows; ++r) {
-        if (r < rows) {
-          const uint4 w = wt[r * KV + j];
-#pragma unroll
-          for (int b = 0; b < NB; ++b) acc[r][b] = dot8(w, xa[b], xb[b], acc[r][b]);
+          for (int b = 0; b < NB; ++b) {
+            const size_t xb = (static_cast<size_t>(b) * K + k0) >> 2;
+            p0[b] = dot8(w0, xs4[xb + 2 * j], xs4[xb + 2 * j + 1], p0[b]);
+            p1[b] = dot8(w1, xs4[xb + 2 * (j + 32)], xs4[xb + 2 * (j + 32) + 1], p1[b]);
+          }
         }
+        if (j < nvec) {
+          const uint4 w0 = wr[j];
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const size_t xb = (static_cast<size_t>(b) * K + k0) >> 2;
+            p0[b] = dot8(w0, xs4[xb + 2 * j], xs4[xb + 2 * j + 1], p0[b]);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[m][b] += p0[b] + p1[b];
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-
-    // Reduce over the consumer threads (double-buffered by tile parity).
-    float* rb = red + (i & 1) * (kGemvConsumerWarps * kMaxTileRows * NB);
+    if (c == n_chunks - 1 && warp < rows) {
+      const int n = v0 + warp;
 #pragma unroll
-    for (int r = 0; r < kMaxTileRows; ++r) {
-      if (r < rows) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float v = warp_sum(acc[r][b]);
-          if (lane == 0) rb[warp * (kMaxTileRows * NB) + r * NB + b] = v;
-        }
+      for (int b = 0; b < NB; ++b) {
+        acc[0][b] = warp_sum(acc[0][b]);
+        if (swiglu) acc[1][b] = warp_sum(acc[1][b]);
       }
-    }
-    named_barrier(1, NCT);
-    if (tid < rows * NB) {
-      const int r = tid / NB, b = tid % NB;
-      float y = 0.f;
 #pragma unroll
-      for (int w = 0; w < kGemvConsumerWarps; ++w) y += rb[w * (kMaxTileRows * NB) + tid];
-      if (b < nb) {
-        const int orow = a.out_map ? a.out_map[b] : b;
-        const int n = row0 + r;
-        if (orow >= 0) {
-          float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
-          if (a.mode == GEMV_STORE) {
-            *o = y;
-          } else if (a.mode == GEMV_ADD) {
-            *o = a.base[static_cast<size_t>(orow) * a.ldb + n] + y;
-          } else {
+      for (int b = 0; b < NB; ++b) {
+        if (lane == b && b < nb) {
+          const int orow = a.out_map ? a.out_map[b] : b;
+          if (orow >= 0) {
+            float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
+            if (a.mode == GEMV_STORE) *o = acc[0][b];
+            else if (a.mode == GEMV_ADD) *o = a.base[static_cast<size_t>(orow) * a.ldb + n] + acc[0][b];
             // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
-            if (part == 0) keep = y;
-            else *o = silu(keep) * y;
+            else *o = silu(acc[0][b]) * acc[1][b];
           }
         }
       }
     }
-    ++i;
   }
 }
 
-static GemvPlan plan_gemv(int K, int nb) {
+static GemvPlan plan_gemv(int K, int nb, int mode) {
   GemvPlan p;
-  p.R = gemv_rows_per_tile(K);
-  p.tile_bytes = (p.R * K * 2 + 127) & ~127;
+  p.nmat = mode == GEMV_SWIGLU ? 2 : 1;
+  const int kmax = kChunk / p.nmat;
+  p.n_chunks = (K + kmax - 1) / kmax;
+  p.kc = ((K + p.n_chunks - 1) / p.n_chunks + 7) & ~7;
+  p.tile_bytes = (kRowsPerGroup * p.nmat * p.kc * 2 + 127) & ~127;
   int nbt = nb >= 8 ? 8 : nb >= 4 ? 4 : nb >= 2 ? 2 : 1;
   while (true) {
     const size_t ring = gemv_ring_off(nbt, K);
-    int st = static_cast<int>((kSmemBudget - static_cast<long long>(ring)) / p.tile_bytes);
+    const long long room = static_cast<long long>(kSmemBudget) - static_cast<long long>(ring);
+    int st = room > 0 ? static_cast<int>(room / p.tile_bytes) : 0;
     if (st >= 2 || nbt == 1) {
       p.nbt = nbt;
-      p.stages = st > kMaxStages ? kMaxStages : (st < 2 ? 2 : st);
+      p.stages = st > kMaxStages ? kMaxStages : st;
       p.smem = ring + static_cast<size_t>(p.stages) * p.tile_bytes;
       return p;
     }
@@ -330,14 +317,15 @@ static cudaError_t launch_gemv_nb(const GemvArgs& a, const GemvPlan& p, int grid
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  gemv_kernel<NB><<<grid, kGemvThreads, p.smem, st>>>(a, p.R, p.stages, p.tile_bytes);
+  gemv_kernel<NB><<<grid, kGemvThreads, p.smem, st>>>(a, p.kc, p.n_chunks, p.stages, p.tile_bytes);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
   if (a.nb <= 0) return cudaSuccess;
-  const GemvPlan p = plan_gemv(a.K, a.nb);
-  if (p.smem > static_cast<size_t>(kSmemBudget)) return cudaErrorInvalidValue;
+  if (a.K % 8 != 0) return cudaErrorInvalidValue;
+  const GemvPlan p = plan_gemv(a.K, a.nb, a.mode);
+  if (p.stages < 1 || p.smem > static_cast<size_t>(kSmemBudget)) return cudaErrorInvalidValue;
   const int nv = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
   const int grid = nv < n_sm ? nv : n_sm;
   for (int g0 = 0; g0 < a.nb; g0 += p.nbt) {

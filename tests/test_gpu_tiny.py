@@ -152,26 +152,36 @@ def run_replay(d, o, prompt, n_frames, smp, seed, twin_main_entry=False):
         d.prefill(2, prompt)
     seq = o.prefill(prompt)
     uni = g.make_uniforms(n_frames, 1, TINY, seed=seed)
-    stats = DrawStats()
+    stats = DrawStats()      # oracle logits, draws stable under the measured eps
+    samp = DrawStats()       # oracle sampler on the GPU's own logits
     for f in range(n_frames):
         codes, status, slow, fast, draws = d.decode_frame_forced([1], dev(uni[f]), gpu_sampling(smp), None)
         if twin_main_entry:
             c2, s2 = d.decode_frame([2], dev(uni[f]), gpu_sampling(smp))
         d.sync()
         codes, status = codes.cpu().numpy()[0], int(status.cpu()[0])
-        slow, fast = slow.cpu().numpy()[0], fast.cpu().numpy()[0]
+        slow, fast, draws = slow.cpu().numpy()[0], fast.cpu().numpy()[0], draws.cpu().numpy()[0]
         assert status == 0
         if twin_main_entry:
             np.testing.assert_array_equal(c2.cpu().numpy()[0], codes)
             assert int(s2.cpu()[0]) == 0
         hist = list(seq.history)
-        r = o.decode_frame(seq, uni[f, 0], smp, forced=codes)   # replay the GPU trajectory
+        # the sampler alone, on the GPU's logits
+        g0, gr, gch = sample_q0(TINY, slow, smp, hist, float(uni[f, 0, 0]), float(uni[f, 0, 1]))
+        samp.check(draws[0], g0, smp.temperature, f"q0 draw f{f}")
+        samp.check(draws[1], gr, smp.ras_temperature, f"ras draw f{f}")
+        if draw_decidable(g0, smp.temperature) and draw_decidable(gr, smp.ras_temperature):
+            assert draws[2] == gch and codes[0] == gch
+        for k in range(1, TINY.n_codebooks):
+            rk = sample_top_p(fast[k - 1], np.arange(TINY.fast_vocab), smp.temperature, smp.top_p,
+                              float(uni[f, 0, k + 1]))
+            samp.check(codes[k], rk, smp.temperature, f"q{k} draw f{f}")
+        # replay the GPU trajectory in the oracle
+        r = o.decode_frame(seq, uni[f, 0], smp, forced=codes)
         n0, ras, chosen = r.draws[0]
         assert_logits_close(slow, r.slow_logits, f"slow f{f}")
         assert_logits_close(fast, r.fast_logits, f"fast f{f}")
         eps0 = float(np.abs(slow - r.slow_logits).max())
-        # q0: the committed code must be the oracle's choice when every draw
-        # that decides it is stable
         triggered = smp.ras_win > 0 and n0.index != TINY.n_sem and n0.index in hist[-smp.ras_win:]
         if draw_decidable(n0, smp.temperature, eps0) and (
                 not triggered or draw_decidable(ras, smp.ras_temperature, eps0)):
@@ -182,7 +192,11 @@ def run_replay(d, o, prompt, n_frames, smp, seed, twin_main_entry=False):
         for k in range(1, TINY.n_codebooks):
             epsk = float(np.abs(fast[k - 1] - r.fast_logits[k - 1]).max())
             stats.check(codes[k], r.draws[k], smp.temperature, f"q{k} f{f}", epsk)
-    assert stats.compared > 0
+    assert samp.compared > 0
+    if smp.temperature <= 0:
+        assert stats.compared > 0
+    print(f"draws on oracle logits: {stats.compared} compared, {stats.excluded} not stable under eps; "
+          f"sampler on GPU logits: {samp.compared} compared, {samp.excluded} at a boundary")
     return stats
 
 
@@ -200,6 +214,14 @@ def test_sampled_replay_and_main_entry_point(dec, tiny_oracle):
 def test_sampled_replay_other_params(dec, tiny_oracle):
     smp = OSampling(temperature=1.3, top_p=0.6, ras_win=4)
     run_replay(dec, tiny_oracle, g.make_prompt(TINY, 70, seed=5), 12, smp, seed=23)
+
+
+def test_sampled_replay_sharp(dec, tiny_oracle):
+    """Low temperature: few candidates carry the mass, so trajectory draws are
+    stable under eps and are compared on the oracle's own logits."""
+    smp = OSampling(temperature=0.1, top_p=0.9, ras_win=10)
+    st = run_replay(dec, tiny_oracle, g.make_prompt(TINY, 32, seed=7), 16, smp, seed=24)
+    assert st.compared > 0
 
 
 # ---------------------------------------------------------- end of stream --
