@@ -129,8 +129,8 @@ int validate_config(dualar_handle* h, const dualar_config& c) {
   if (c.n_layer <= 0 || c.fast_n_layer <= 0) return bad("layer counts");
   if (c.page_tokens != 64) return bad("page_tokens must be 64");
   if (c.n_codebooks < 2 || c.n_codebooks > kMaxCodebooks) return bad("n_codebooks in [2, 16]");
-  if (c.n_sem <= 0 || c.n_sem + 1 > kSampThreads * kSampPerThread) return bad("n_sem");
-  if (c.fast_vocab <= 0 || c.fast_vocab > kSampThreads * kSampPerThread) return bad("fast_vocab");
+  if (c.n_sem <= 0 || c.n_sem > 4096) return bad("n_sem in [1, 4096]");
+  if (c.fast_vocab <= 0 || c.fast_vocab > 4096) return bad("fast_vocab in [1, 4096]");
   if (c.sem_begin < 0 || c.sem_begin + c.n_sem > c.vocab) return bad("semantic id range");
   if (c.im_end_id < 0 || c.im_end_id >= c.vocab ||
       (c.im_end_id >= c.sem_begin && c.im_end_id < c.sem_begin + c.n_sem))
@@ -202,7 +202,7 @@ const uint16_t* U16(const void* p) { return static_cast<const uint16_t*>(p); }
 // One transformer block over nrows rows.  Slow blocks attend over the paged
 // cache; fast blocks over the per-frame codebook cache.
 int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast, int nrows,
-          const float* xin, float* hres, int fast_pos, int units, int chunk) {
+          const float* xin, float* hres, int fast_pos, int units, int chunk, bool fuse_append) {
   const dualar_config& c = h->cfg;
   const DevPtrs& d = h->d;
   const int qd = c.n_head * c.head_dim;
@@ -220,12 +220,16 @@ int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast
   a.ldo = d.qkv_dim;
   TRY(run_gemv(h, a));
   const bool qk = fast ? c.fast_qk_norm : c.slow_qk_norm;
-  LAUNCH(h, launch_append(d, nrows, layer, fast, fast_pos, qk ? U16(lw.q_norm) : nullptr,
-                          qk ? U16(lw.k_norm) : nullptr, h->stream));
-  if (fast)
-    LAUNCH(h, launch_attn_fast(d, nrows, layer, fast_pos + 1, h->stream));
-  else
-    LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, h->stream));
+  const uint16_t* qn = qk ? U16(lw.q_norm) : nullptr;
+  const uint16_t* kn = qk ? U16(lw.k_norm) : nullptr;
+  if (fast) {
+    LAUNCH(h, launch_attn_fast(d, nrows, layer, fast_pos, qn, kn, h->stream));
+  } else if (fuse_append) {
+    LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, true, qn, kn, h->stream));
+  } else {
+    LAUNCH(h, launch_append(d, nrows, layer, false, 0, qn, kn, h->stream));
+    LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, false, nullptr, nullptr, h->stream));
+  }
   // h = x + Wo attn
   a = gemv_base(h);
   a.w0 = U16(lw.wo);
@@ -287,9 +291,12 @@ void plan_attention(dualar_handle* h, LaunchSetup& s, int* units, int* chunk) {
   *units = u;
 }
 
-int slow_stack(dualar_handle* h, int nrows, int units, int chunk) {
+// Decode rows are distinct sequences, so the KV append fuses into attention;
+// prefill rows of one sequence must see each other's KV (separate append).
+int slow_stack(dualar_handle* h, int nrows, int units, int chunk, bool decode) {
   for (int l = 0; l < h->cfg.n_layer; ++l)
-    TRY(block(h, h->slow[l], l, false, nrows, l == 0 ? h->d.xs : h->d.hs, h->d.hs, 0, units, chunk));
+    TRY(block(h, h->slow[l], l, false, nrows, l == 0 ? h->d.xs : h->d.hs, h->d.hs, 0, units, chunk,
+              decode));
   return DUALAR_OK;
 }
 
@@ -395,7 +402,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
   for (int p = 0; p < N; ++p) {
     const float* xin = d.fin + static_cast<size_t>(p & 1) * kMaxRows * c.dim;
     for (int l = 0; l < c.fast_n_layer; ++l)
-      TRY(block(h, h->fast[l], l, true, batch, l == 0 ? xin : d.hf, d.hf, p, 0, 0));
+      TRY(block(h, h->fast[l], l, true, batch, l == 0 ? xin : d.hf, d.hf, p, 0, 0, false));
     if (p == 0) continue;
     GemvArgs a = gemv_base(h);
     a.w0 = U16(h->w.fast_out);
@@ -414,7 +421,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
   }
   // 3. fusion -> next slow input; 4. one slow position; restricted head
   LAUNCH(h, launch_fusion(d, batch, U16(h->w.tok_emb), U16(h->w.fusion), h->stream));
-  TRY(slow_stack(h, batch, units, chunk));
+  TRY(slow_stack(h, batch, units, chunk, true));
   TRY(restricted_head(h, 0, batch));
   for (int r = 0; r < batch; ++r) h->length[slots[r]] += 1;
   return DUALAR_OK;
@@ -624,7 +631,7 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
     int units = 0, chunk = 0;
     plan_attention(h, s, &units, &chunk);
     LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
-    TRY(slow_stack(h, m, units, chunk));
+    TRY(slow_stack(h, m, units, chunk, false));
     if (c0 + m == n_tokens) TRY(restricted_head(h, m - 1, 1));
   }
   h->length[slot] = n_tokens;

@@ -85,6 +85,15 @@ DEVI void bulk_load_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* ba
       : "memory");
 }
 
+// Same without an L2 policy (data that is worth keeping in L2).
+DEVI void bulk_load_g2s_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 DEVI uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -15,7 +15,6 @@ constexpr int kMaxGroup = 8;         // query heads per KV head
 constexpr int kGemvConsumerWarps = 8;
 constexpr int kGemvThreads = (kGemvConsumerWarps + 1) * 32;
 constexpr int kSampThreads = 512;
-constexpr int kSampPerThread = 9;    // candidates per sampler thread (<= 4608 candidates)
 
 // Device error word: bit flags OR-ed in by kernels, read by dualar_sync.
 enum : uint32_t {
@@ -123,8 +122,10 @@ cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st);
 cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int fast_pos,
                           const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st);
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,
-                              int chunk_tokens, int n_sm, cudaStream_t st);
-cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int npos, cudaStream_t st);
+                              int chunk_tokens, int n_sm, bool fuse_append, const uint16_t* q_norm,
+                              const uint16_t* k_norm, cudaStream_t st);
+cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* q_norm,
+                             const uint16_t* k_norm, cudaStream_t st);
 cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms, int ldu,
                              const SamplingParams& sp, const int32_t* forced, int ldf,
                              int32_t* codes_out, int32_t* status_out, float* slow_logits_out,

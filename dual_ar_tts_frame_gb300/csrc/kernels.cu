@@ -456,33 +456,82 @@ cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int
   return cudaGetLastError();
 }
 
+// QK-norm (optional) + RoPE of one head vector held as EPL elements per lane.
+template <int EPL>
+DEVI void head_norm_rope(float (&v)[EPL], const uint16_t* nw, float eps, int pos, const DevPtrs& d,
+                         int lane) {
+  const int hd = EPL * 32, half = hd / 2;
+  if (nw != nullptr) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s += v[j] * v[j];
+    s = warp_sum(s);
+    const float inv = 1.0f / sqrtf(s / static_cast<float>(hd) + eps);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) v[j] = (v[j] * inv) * bf16bits_to_f32(nw[lane * EPL + j]);
+  }
+#pragma unroll
+  for (int pp = 0; pp < EPL / 2; ++pp) {
+    const int i = (lane * EPL) / 2 + pp;
+    const float c = bf16bits_to_f32(d.rope_cos[static_cast<size_t>(pos) * half + i]);
+    const float sn = bf16bits_to_f32(d.rope_sin[static_cast<size_t>(pos) * half + i]);
+    const float x0 = v[2 * pp], x1 = v[2 * pp + 1];
+    v[2 * pp] = x0 * c - x1 * sn;
+    v[2 * pp + 1] = x1 * c + x0 * sn;
+  }
+}
+
 // ============================================================================
 // Paged split-KV decode attention
 // ============================================================================
 // A unit is (row, KV head g, chunk c of chunk_tokens positions).  The unit
 // computes softmax(q K^T / sqrt(hd)) V for the G query heads of g over its
-// chunk with a running max; the last unit of (row, g) to finish merges the
-// chunks in chunk order (deterministic).  [P2] fact table: 32 query heads
-// over 8 KV heads.
+// chunk with a running max; K and V pages (64 positions x hd, bf16) are
+// staged in shared memory by double-buffered bulk copies.  The last unit of
+// (row, g) to finish merges the chunks in chunk order (deterministic).
+// With fuse_append (decode: one row per sequence) the unit applies QK-norm
+// and RoPE to its query heads itself, and the unit holding the newest
+// position also computes that position's K and V, writes them to the page
+// and uses them directly.  [P2] fact table: 32 query heads over 8 KV heads.
 constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kPageTokens = 64;
 
 template <int HD, int G>
+struct AttnSmem {
+  uint16_t kv[2][2][kPageTokens * HD];   // [buffer][K/V][tok][dim]
+  float qs[G][4][HD / 4 + 1];
+  float sc[G][kPageTokens];
+  float ored[kAttnThreads / HD][G][HD];
+  float knew[HD], vnew[HD];
+  float scl[G], msm[G], lsm[G];
+  uint64_t bar[2];
+  int s_last;
+};
+
+template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads)
-    attn_paged_kernel(DevPtrs d, int nrows, int layer, int total_units, int chunk_tokens) {
-  constexpr int QD = HD / 4;              // dims per thread in the score pass
+    attn_paged_kernel(DevPtrs d, int nrows, int layer, int total_units, int chunk_tokens,
+                      int fuse_append, const uint16_t* q_norm, const uint16_t* k_norm) {
+  constexpr int EPL = HD / 32;
+  constexpr int QD = HD / 4;                // dims per thread in the score pass
   constexpr int PARTS = kAttnThreads / HD;  // token groups in the value pass
   constexpr int TPP = kPageTokens / PARTS;  // tokens per group
-  __shared__ float qs[G][4][QD + 1];
-  __shared__ float sc[G][kPageTokens];
-  __shared__ float scl[G], msm[G], lsm[G];
-  __shared__ float ored[PARTS][G][HD];
-  __shared__ int s_last;
+  constexpr uint32_t kPageBytes = kPageTokens * HD * 2;
+  extern __shared__ __align__(128) unsigned char attn_smem_raw[];
+  AttnSmem<HD, G>& sm = *reinterpret_cast<AttnSmem<HD, G>*>(attn_smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hq = d.Hq, hkv = d.Hkv;
   const float qscale = 1.0f / sqrtf(static_cast<float>(HD));
   const size_t page_stride = static_cast<size_t>(kPageTokens) * HD;
+  if (tid == 0) {
+    mbar_init(&sm.bar[0], 1);
+    mbar_init(&sm.bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  uint32_t phase[2] = {0u, 0u};
 
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     // row of this unit: rows are sorted by unit0
@@ -501,14 +550,82 @@ __global__ void __launch_bounds__(kAttnThreads)
     if (!ri.active || g >= hkv) continue;
     const int t0 = c * chunk_tokens;
     const int t1 = min(L, t0 + chunk_tokens);
+    const int npages = (t1 - t0 + kPageTokens - 1) / kPageTokens;
+    const bool newest = fuse_append && (c == nch - 1);
 
-    for (int e = tid; e < G * HD; e += kAttnThreads) {
-      const int h = e / HD, dd = e % HD;
-      qs[h][dd / QD][dd % QD] = d.qrot[(static_cast<size_t>(r) * hq + g * G + h) * HD + dd] * qscale;
+    // page table lookups (all threads agree); a bad entry skips the unit
+    auto page_of = [&](int p) -> int {
+      return d.page_table[ri.slot * d.pages_per_seq + (t0 / kPageTokens) + p];
+    };
+    bool ok = true;
+    for (int p = 0; p < npages; ++p) {
+      const int pg = page_of(p);
+      if (pg < 0 || pg >= d.max_pages) ok = false;
+    }
+    if (!ok) {
+      if (tid == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
+      continue;
+    }
+    auto issue = [&](int p, int buf) {
+      const uint16_t* kp = d.kv_pool +
+          (((static_cast<size_t>(page_of(p)) * d.n_layer + layer) * 2 + 0) * hkv + g) * page_stride;
+      const uint16_t* vp = kp + static_cast<size_t>(hkv) * page_stride;
+      mbar_arrive_expect_tx(&sm.bar[buf], 2 * kPageBytes);
+      bulk_load_g2s_plain(sm.kv[buf][0], kp, kPageBytes, &sm.bar[buf]);
+      bulk_load_g2s_plain(sm.kv[buf][1], vp, kPageBytes, &sm.bar[buf]);
+    };
+    if (tid == 0) {
+      issue(0, 0);
+      if (npages > 1) issue(1, 1);
+    }
+
+    // query heads of g (norm + RoPE in place when fused)
+    if (fuse_append) {
+      if (warp < G) {
+        const int h = g * G + warp;
+        const float* src = d.qkv + static_cast<size_t>(r) * d.qkv_dim + h * HD;
+        float v[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) v[j] = src[lane * EPL + j];
+        head_norm_rope<EPL>(v, q_norm, d.eps, ri.pos, d, lane);
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          const int dd = lane * EPL + j;
+          sm.qs[warp][dd / QD][dd % QD] = v[j] * qscale;
+        }
+      }
+      if (warp == (G % kAttnWarps) && newest) {
+        const float* base = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
+        float kv[EPL], vv[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          kv[j] = base[hq * HD + g * HD + lane * EPL + j];
+          vv[j] = base[hq * HD + hkv * HD + g * HD + lane * EPL + j];
+        }
+        head_norm_rope<EPL>(kv, k_norm, d.eps, ri.pos, d, lane);
+        const int pidx = ri.pos / kPageTokens;
+        const int pg = d.page_table[ri.slot * d.pages_per_seq + pidx];
+        uint16_t* kd = d.kv_pool + (((static_cast<size_t>(pg) * d.n_layer + layer) * 2 + 0) * hkv + g) *
+                                       page_stride + static_cast<size_t>(ri.pos % kPageTokens) * HD;
+        uint16_t* vd = kd + static_cast<size_t>(hkv) * page_stride;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          const uint16_t kb = f32_to_bf16bits(kv[j]), vb = f32_to_bf16bits(vv[j]);
+          kd[lane * EPL + j] = kb;
+          vd[lane * EPL + j] = vb;
+          sm.knew[lane * EPL + j] = bf16bits_to_f32(kb);
+          sm.vnew[lane * EPL + j] = bf16bits_to_f32(vb);
+        }
+      }
+    } else {
+      for (int e = tid; e < G * HD; e += kAttnThreads) {
+        const int h = e / HD, dd = e % HD;
+        sm.qs[h][dd / QD][dd % QD] = d.qrot[(static_cast<size_t>(r) * hq + g * G + h) * HD + dd] * qscale;
+      }
     }
     if (tid < G) {
-      msm[tid] = -INFINITY;
-      lsm[tid] = 0.f;
+      sm.msm[tid] = -INFINITY;
+      sm.lsm[tid] = 0.f;
     }
     float o[G];
 #pragma unroll
@@ -516,31 +633,40 @@ __global__ void __launch_bounds__(kAttnThreads)
     __syncthreads();
 
     const int tok = tid >> 2, qd = tid & 3;
-    const int vd = tid % HD, vpart = tid / HD;
-    for (int ps = t0; ps < t1; ps += kPageTokens) {
-      const int page = d.page_table[ri.slot * d.pages_per_seq + ps / kPageTokens];
-      const bool page_ok = page >= 0 && page < d.max_pages;
-      if (!page_ok && tid == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
-      const int ntok = page_ok ? min(kPageTokens, t1 - ps) : 0;
-      const uint16_t* kp =
-          d.kv_pool + (((static_cast<size_t>(page_ok ? page : 0) * d.n_layer + layer) * 2 + 0) * hkv + g) *
-                          page_stride;
-      const uint16_t* vp = kp + static_cast<size_t>(hkv) * page_stride;
+    const int vdim = tid % HD, vpart = tid / HD;
+    for (int p = 0; p < npages; ++p) {
+      const int buf = p & 1;
+      const int ps = t0 + p * kPageTokens;
+      const int ntok = min(kPageTokens, t1 - ps);
+      if (!mbar_wait(&sm.bar[buf], phase[buf], d.err, d.wait_limit_ns)) return;
+      phase[buf] ^= 1u;
+      const uint16_t* ks = sm.kv[buf][0];
+      const uint16_t* vs = sm.kv[buf][1];
       // scores
       float s[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) s[h] = 0.f;
       if (tok < ntok) {
-        const uint4* k4 = reinterpret_cast<const uint4*>(kp + static_cast<size_t>(tok) * HD + qd * QD);
+        const bool isnew = newest && (ps + tok == ri.pos);
+        if (isnew) {
+#pragma unroll 4
+          for (int j = 0; j < QD; ++j) {
+            const float kf = sm.knew[qd * QD + j];
 #pragma unroll
-        for (int v8 = 0; v8 < QD / 8; ++v8) {
-          const uint4 w = k4[v8];
-          const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                               bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+            for (int h = 0; h < G; ++h) s[h] = fmaf(sm.qs[h][qd][j], kf, s[h]);
+          }
+        } else {
+          const uint4* k4 = reinterpret_cast<const uint4*>(ks + tok * HD + qd * QD);
 #pragma unroll
-          for (int h = 0; h < G; ++h)
+          for (int v8 = 0; v8 < QD / 8; ++v8) {
+            const uint4 w = k4[v8];
+            const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                                 bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s[h] = fmaf(qs[h][qd][v8 * 8 + j], kf[j], s[h]);
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) s[h] = fmaf(sm.qs[h][qd][v8 * 8 + jj], kf[jj], s[h]);
+          }
         }
       }
 #pragma unroll
@@ -550,51 +676,51 @@ __global__ void __launch_bounds__(kAttnThreads)
       }
       if (qd == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc[h][tok] = tok < ntok ? s[h] : -INFINITY;
+        for (int h = 0; h < G; ++h) sm.sc[h][tok] = tok < ntok ? s[h] : -INFINITY;
       }
       __syncthreads();
-      if (warp < G && ntok > 0) {
+      if (warp < G) {
         const int h = warp;
-        const float a0 = sc[h][lane], a1 = sc[h][lane + 32];
+        const float a0 = sm.sc[h][lane], a1 = sm.sc[h][lane + 32];
         const float mx = warp_max(fmaxf(a0, a1));
-        const float mold = msm[h];
+        const float mold = sm.msm[h];
         const float mnew = fmaxf(mold, mx);
         const float p0 = lane < ntok ? expf(a0 - mnew) : 0.f;
         const float p1 = lane + 32 < ntok ? expf(a1 - mnew) : 0.f;
-        sc[h][lane] = p0;
-        sc[h][lane + 32] = p1;
+        sm.sc[h][lane] = p0;
+        sm.sc[h][lane + 32] = p1;
         const float sum = warp_sum(p0 + p1);
         if (lane == 0) {
           const float f = expf(mold - mnew);   // 0 for the first page (mold = -inf)
-          scl[h] = f;
-          lsm[h] = lsm[h] * f + sum;
-          msm[h] = mnew;
+          sm.scl[h] = f;
+          sm.lsm[h] = sm.lsm[h] * f + sum;
+          sm.msm[h] = mnew;
         }
       }
       __syncthreads();
-      if (ntok > 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) o[h] *= scl[h];
-        const int tb = vpart * TPP, te = min(ntok, tb + TPP);
-        for (int t = tb; t < te; ++t) {
-          const float v = bf16bits_to_f32(vp[static_cast<size_t>(t) * HD + vd]);
+      for (int h = 0; h < G; ++h) o[h] *= sm.scl[h];
+      const int tb = vpart * TPP, te = min(ntok, tb + TPP);
+      for (int t = tb; t < te; ++t) {
+        const bool isnew = newest && (ps + t == ri.pos);
+        const float v = isnew ? sm.vnew[vdim] : bf16bits_to_f32(vs[t * HD + vdim]);
 #pragma unroll
-          for (int h = 0; h < G; ++h) o[h] = fmaf(sc[h][t], v, o[h]);
-        }
+        for (int h = 0; h < G; ++h) o[h] = fmaf(sm.sc[h][t], v, o[h]);
       }
-      __syncthreads();
+      __syncthreads();   // buffer `buf` is free again
+      if (tid == 0 && p + 2 < npages) issue(p + 2, buf);
     }
     // merge the token groups
 #pragma unroll
-    for (int h = 0; h < G; ++h) ored[vpart][h][vd] = o[h];
+    for (int h = 0; h < G; ++h) sm.ored[vpart][h][vdim] = o[h];
     __syncthreads();
     if (nch == 1) {
       for (int e = tid; e < G * HD; e += kAttnThreads) {
         const int h = e / HD, dd = e % HD;
         float t = 0.f;
 #pragma unroll
-        for (int p = 0; p < PARTS; ++p) t += ored[p][h][dd];
-        d.attn[static_cast<size_t>(r) * hq * HD + (g * G + h) * HD + dd] = t / lsm[h];
+        for (int p = 0; p < PARTS; ++p) t += sm.ored[p][h][dd];
+        d.attn[static_cast<size_t>(r) * hq * HD + (g * G + h) * HD + dd] = t / sm.lsm[h];
       }
       __syncthreads();
       continue;
@@ -604,21 +730,21 @@ __global__ void __launch_bounds__(kAttnThreads)
       const int h = e / HD, dd = e % HD;
       float t = 0.f;
 #pragma unroll
-      for (int p = 0; p < PARTS; ++p) t += ored[p][h][dd];
+      for (int p = 0; p < PARTS; ++p) t += sm.ored[p][h][dd];
       pw[h * (HD + 2) + dd] = t;
     }
     if (tid < G) {
-      pw[tid * (HD + 2) + HD] = msm[tid];
-      pw[tid * (HD + 2) + HD + 1] = lsm[tid];
+      pw[tid * (HD + 2) + HD] = sm.msm[tid];
+      pw[tid * (HD + 2) + HD + 1] = sm.lsm[tid];
     }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
       const uint32_t old = atomic_add_acq_rel_gpu(&d.arrive[r * hkv + g], 1u);
-      s_last = (old == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
+      sm.s_last = (old == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
     }
     __syncthreads();
-    if (s_last) {
+    if (sm.s_last) {
       __threadfence();
       const float* pb = d.part + (static_cast<size_t>(r) * hkv + g) * kMaxChunks * G * (HD + 2);
       for (int e = tid; e < G * HD; e += kAttnThreads) {
@@ -640,318 +766,379 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
 }
 
-template <int HD>
-static cudaError_t attn_paged_hd(const DevPtrs& d, int nrows, int layer, int units, int chunk,
-                                 int grid, cudaStream_t st) {
-  const int G = d.Hq / d.Hkv;
-  switch (G) {
-    case 1: attn_paged_kernel<HD, 1><<<grid, kAttnThreads, 0, st>>>(d, nrows, layer, units, chunk); break;
-    case 2: attn_paged_kernel<HD, 2><<<grid, kAttnThreads, 0, st>>>(d, nrows, layer, units, chunk); break;
-    case 4: attn_paged_kernel<HD, 4><<<grid, kAttnThreads, 0, st>>>(d, nrows, layer, units, chunk); break;
-    case 8: attn_paged_kernel<HD, 8><<<grid, kAttnThreads, 0, st>>>(d, nrows, layer, units, chunk); break;
-    default: return cudaErrorInvalidValue;
+template <int HD, int G>
+static cudaError_t attn_paged_launch(const DevPtrs& d, int nrows, int layer, int units, int chunk,
+                                     int grid, int fuse, const uint16_t* qn, const uint16_t* kn,
+                                     cudaStream_t st) {
+  static bool configured = false;
+  const int smem = static_cast<int>(sizeof(AttnSmem<HD, G>));
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_paged_kernel<HD, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
   }
+  attn_paged_kernel<HD, G><<<grid, kAttnThreads, smem, st>>>(d, nrows, layer, units, chunk, fuse, qn, kn);
   return cudaGetLastError();
 }
 
+template <int HD>
+static cudaError_t attn_paged_hd(const DevPtrs& d, int nrows, int layer, int units, int chunk,
+                                 int grid, int fuse, const uint16_t* qn, const uint16_t* kn,
+                                 cudaStream_t st) {
+  switch (d.Hq / d.Hkv) {
+    case 1: return attn_paged_launch<HD, 1>(d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
+    case 2: return attn_paged_launch<HD, 2>(d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
+    case 4: return attn_paged_launch<HD, 4>(d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
+    case 8: return attn_paged_launch<HD, 8>(d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,
-                              int chunk_tokens, int n_sm, cudaStream_t st) {
+                              int chunk_tokens, int n_sm, bool fuse_append, const uint16_t* q_norm,
+                              const uint16_t* k_norm, cudaStream_t st) {
   if (nrows <= 0 || total_units <= 0) return cudaSuccess;
   if (d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0) return cudaErrorInvalidValue;
   const int grid = total_units < 4 * n_sm ? total_units : 4 * n_sm;
-  if (d.hd == 128) return attn_paged_hd<128>(d, nrows, layer, total_units, chunk_tokens, grid, st);
-  if (d.hd == 64) return attn_paged_hd<64>(d, nrows, layer, total_units, chunk_tokens, grid, st);
+  const int f = fuse_append ? 1 : 0;
+  if (d.hd == 128) return attn_paged_hd<128>(d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st);
+  if (d.hd == 64) return attn_paged_hd<64>(d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st);
   return cudaErrorInvalidValue;
 }
 
 // ============================================================================
 // Fast-AR attention over the per-frame codebook cache (<= N positions)
 // ============================================================================
-// [P2] "Two autoregressions": the fast AR's KV cache is num_codebooks long
-// and is overwritten every frame.
-template <int EPL>
-__global__ void attn_fast_kernel(DevPtrs d, int nrows, int layer, int npos) {
+// One CTA per (row, KV head g): warp 0 computes the new position's K (norm if
+// configured, RoPE at the codebook index) and V and appends them; the K/V of
+// earlier positions (written by earlier passes of this frame) are staged in
+// shared memory; warp h < G then computes query head g*G+h.  [P2] "Two
+// autoregressions": the fast AR's KV cache is num_codebooks long and is
+// overwritten every frame.
+template <int EPL, int G>
+__global__ void attn_fast_kernel(DevPtrs d, int layer, int pos, const uint16_t* q_norm,
+                                 const uint16_t* k_norm) {
+  constexpr int HD = EPL * 32;
+  __shared__ float ks[kMaxCodebooks][HD], vs[kMaxCodebooks][HD];
+  const int r = blockIdx.x / d.Hkv, g = blockIdx.x % d.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x * (blockDim.x >> 5) + warp;
-  const int hq = d.Hq, hd = d.hd;
-  if (unit >= nrows * hq) return;
-  const int r = unit / hq, h = unit % hq;
-  const int g = h / (hq / d.Hkv);
-  const float* q = d.qrot + (static_cast<size_t>(r) * hq + h) * hd;
-  const float* kb = d.fast_kv +
-                    (((static_cast<size_t>(r) * d.fast_n_layer + layer) * 2 + 0) * d.Hkv + g) * d.N * hd;
-  const float* vb = kb + static_cast<size_t>(d.Hkv) * d.N * hd;
-  float s = -INFINITY;
-  if (lane < npos) {
-    float t = 0.f;
-    const float* kr = kb + static_cast<size_t>(lane) * hd;
-    for (int e = 0; e < hd; ++e) t = fmaf(q[e], kr[e], t);
-    s = t * (1.0f / sqrtf(static_cast<float>(hd)));
+  const int hq = d.Hq, hkv = d.Hkv, N = d.N;
+  const float* qkv = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
+  float* kb = d.fast_kv + (((static_cast<size_t>(r) * d.fast_n_layer + layer) * 2 + 0) * hkv + g) * N * HD;
+  float* vb = kb + static_cast<size_t>(hkv) * N * HD;
+  if (warp == 0) {
+    float kv[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) kv[j] = qkv[hq * HD + g * HD + lane * EPL + j];
+    head_norm_rope<EPL>(kv, k_norm, d.eps, pos, d, lane);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const float vv = qkv[hq * HD + hkv * HD + g * HD + lane * EPL + j];
+      kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
+      vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv;
+      ks[pos][lane * EPL + j] = kv[j];
+      vs[pos][lane * EPL + j] = vv;
+    }
+  } else {
+    for (int e = threadIdx.x - 32; e < pos * HD; e += blockDim.x - 32) {
+      ks[e / HD][e % HD] = kb[e];
+      vs[e / HD][e % HD] = vb[e];
+    }
   }
-  const float m = warp_max(s);
-  const float p = lane < npos ? expf(s - m) : 0.f;
-  const float l = warp_sum(p);
+  __syncthreads();
+  if (warp >= G) return;
+  const int h = g * G + warp;
+  float q[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) q[j] = qkv[h * HD + lane * EPL + j];
+  head_norm_rope<EPL>(q, q_norm, d.eps, pos, d, lane);
+  const float scale = 1.0f / sqrtf(static_cast<float>(HD));
+  float s[kMaxCodebooks];
+  float m = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < kMaxCodebooks; ++t) {
+    s[t] = -INFINITY;
+    if (t <= pos) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) a = fmaf(q[j], ks[t][lane * EPL + j], a);
+      s[t] = warp_sum(a) * scale;
+      m = fmaxf(m, s[t]);
+    }
+  }
+  float l = 0.f;
   float o[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) o[j] = 0.f;
-  for (int t = 0; t < npos; ++t) {
-    const float pt = __shfl_sync(0xFFFFFFFFu, p, t);
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) o[j] = fmaf(pt, vb[static_cast<size_t>(t) * hd + lane * EPL + j], o[j]);
+  for (int t = 0; t < kMaxCodebooks; ++t) {
+    if (t <= pos) {
+      const float p = expf(s[t] - m);
+      l += p;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, vs[t][lane * EPL + j], o[j]);
+    }
   }
-  float* dst = d.attn + static_cast<size_t>(r) * hq * hd + h * hd;
+  float* dst = d.attn + static_cast<size_t>(r) * hq * HD + h * HD;
 #pragma unroll
   for (int j = 0; j < EPL; ++j) dst[lane * EPL + j] = o[j] / l;
 }
 
-cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int npos, cudaStream_t st) {
-  if (nrows <= 0) return cudaSuccess;
-  const int units = nrows * d.Hq;
-  const int grid = (units + 7) / 8;
-  if (d.hd == 128) attn_fast_kernel<4><<<grid, 256, 0, st>>>(d, nrows, layer, npos);
-  else if (d.hd == 64) attn_fast_kernel<2><<<grid, 256, 0, st>>>(d, nrows, layer, npos);
-  else return cudaErrorInvalidValue;
+template <int EPL>
+static cudaError_t attn_fast_epl(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* qn,
+                                 const uint16_t* kn, cudaStream_t st) {
+  const int G = d.Hq / d.Hkv;
+  const int threads = 32 * (G > 1 ? G : 2);
+  const int grid = nrows * d.Hkv;
+  switch (G) {
+    case 1: attn_fast_kernel<EPL, 1><<<grid, threads, 0, st>>>(d, layer, pos, qn, kn); break;
+    case 2: attn_fast_kernel<EPL, 2><<<grid, threads, 0, st>>>(d, layer, pos, qn, kn); break;
+    case 4: attn_fast_kernel<EPL, 4><<<grid, threads, 0, st>>>(d, layer, pos, qn, kn); break;
+    case 8: attn_fast_kernel<EPL, 8><<<grid, threads, 0, st>>>(d, layer, pos, qn, kn); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* q_norm,
+                             const uint16_t* k_norm, cudaStream_t st) {
+  if (nrows <= 0) return cudaSuccess;
+  if (pos < 0 || pos >= d.N || pos >= d.rope_len) return cudaErrorInvalidValue;
+  if (d.hd == 128) return attn_fast_epl<4>(d, nrows, layer, pos, q_norm, k_norm, st);
+  if (d.hd == 64) return attn_fast_epl<2>(d, nrows, layer, pos, q_norm, k_norm, st);
+  return cudaErrorInvalidValue;
 }
 
 // ============================================================================
 // Sampler: temperature + top-p on caller uniforms, one CTA per row
 // ============================================================================
-// Candidates are ordered by (logit descending, token id ascending), encoded
-// as unique 64-bit keys.  Probability mass is integer fixed point
-// (exp((z - zmax) / T) * 2^40, rounded), so every sum is exact and the
-// result does not depend on the order of the atomics.  The top-p cut and the
-// draw are both "first candidate in key order whose cumulative mass reaches
-// a target", found by a radix descent over the key bytes with mass
-// histograms.  [P2] "Two autoregressions": sample(biased_logits, ...) for
-// q0, unmasked sample(logits, ...) for q1..q9.
+// Candidates are ordered by (logit descending, token id ascending): each gets
+// a unique 64-bit key (order-preserving bits of the logit, then the inverted
+// id), and the keys are sorted in shared memory (bitonic).  Probability mass
+// is integer fixed point, round(exp((z - zmax) / T) * 2^40), so prefix sums
+// are exact and independent of thread order.  The top-p cut is the first
+// candidate whose inclusive cumulative mass reaches ceil(top_p * Z); the draw
+// is the first kept candidate whose inclusive cumulative mass reaches
+// floor(u * Zk) + 1, i.e. exceeds u * Zk.  One sort serves the normal draw
+// and the repetition-aware resample.  A single extra candidate (<|im_end|>
+// for q0) is merged into the sorted order virtually.  [P2] "Two
+// autoregressions": sample(biased_logits, ...) for q0, unmasked
+// sample(logits, ...) for q1..q9.
 constexpr int kSampWarps = kSampThreads / 32;
+constexpr int kSortMax = 4096;
 
-struct SampShared {
-  unsigned long long hmass[256];
-  unsigned int hcnt[256];
-  unsigned long long red64[kSampWarps];
+struct SampSmem {
+  unsigned long long key[kSortMax];
+  unsigned long long cum[kSortMax];
+  unsigned long long wsum[kSampWarps];
   float redf[kSampWarps];
-  unsigned long long bc[6];
+  unsigned long long bc[4];
   int ibc[4];
 };
 
 struct Cands {
-  int n;          // number of candidates
-  int n_main;     // candidates 0..n_main-1 have ids id_base + i
+  int n_main;      // candidates 0..n_main-1 have ids id_base + i
   int id_base;
-  int extra_id;   // candidate n_main (when n > n_main)
+  int has_extra;   // candidate n_main with id extra_id
+  int extra_id;
 };
 
 DEVI uint32_t ord_f32(float f) {
   const uint32_t u = __float_as_uint(f + 0.0f);   // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-
-DEVI int cand_id(const Cands& c, int i) { return i < c.n_main ? c.id_base + i : c.extra_id; }
-
-DEVI int key_to_index(const Cands& c, unsigned long long key) {
-  const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
-  if (c.n > c.n_main && id == c.extra_id) return c.n_main;
-  return id - c.id_base;
+DEVI float unord_f32(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+DEVI unsigned long long make_key(float z, int id) {
+  return (static_cast<unsigned long long>(ord_f32(z)) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+DEVI int key_id(unsigned long long k) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+}
+DEVI unsigned long long fixed_mass(float z, float zmax, float inv_t) {
+  return __float2ull_rn(expf((z - zmax) * inv_t) * 1099511627776.0f);   // * 2^40
 }
 
-DEVI float block_max_f(float v, SampShared& sh) {
+DEVI float samp_block_max(float v, SampSmem& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_max(v);
-  if (lane == 0) sh.redf[warp] = v;
+  if (lane == 0) sm.redf[warp] = v;
   __syncthreads();
-  float t = sh.redf[0];
-  for (int w = 1; w < kSampWarps; ++w) t = fmaxf(t, sh.redf[w]);
-  __syncthreads();
-  return t;
-}
-
-DEVI unsigned long long block_sum_u64(unsigned long long v, SampShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  if (lane == 0) sh.red64[warp] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kSampWarps; ++w) t += sh.red64[w];
+  float t = sm.redf[0];
+  for (int w = 1; w < kSampWarps; ++w) t = fmaxf(t, sm.redf[w]);
   __syncthreads();
   return t;
 }
 
-DEVI unsigned long long block_max_u64(unsigned long long v, SampShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = w > v ? w : v;
+// Sorted candidate list shared by the draws of one row.
+struct SortedCands {
+  int np;                     // padded (power of two) length of key[]
+  int n_main;
+  unsigned long long ekey;    // extra candidate key (0 if none)
+  int ins;                    // sorted keys strictly greater than ekey
+  float zmax;
+};
+
+// Loads z[0..n_main) (+ extra at z[n_main]) and sorts.  All threads call.
+DEVI SortedCands samp_sort(const float* z, const Cands& c, SampSmem& sm) {
+  const int tid = threadIdx.x;
+  SortedCands sc;
+  sc.n_main = c.n_main;
+  int np = 1;
+  while (np < c.n_main) np <<= 1;
+  sc.np = np;
+  float zm = -INFINITY;
+  for (int i = tid; i < np; i += kSampThreads) {
+    unsigned long long k = 0;
+    if (i < c.n_main) {
+      const float v = z[i];
+      zm = fmaxf(zm, v);
+      k = make_key(v, c.id_base + i);
+    }
+    sm.key[i] = k;
   }
-  if (lane == 0) sh.red64[warp] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kSampWarps; ++w) t = sh.red64[w] > t ? sh.red64[w] : t;
-  __syncthreads();
-  return t;
-}
-
-// First key (descending) whose inclusive cumulative mass reaches target
-// (1 <= target <= total).  Also returns the mass strictly before it and its
-// own mass.
-DEVI unsigned long long select_by_mass(const unsigned long long (&key)[kSampPerThread],
-                                       const unsigned long long (&mass)[kSampPerThread], int n,
-                                       unsigned long long target, SampShared& sh,
-                                       unsigned long long* above_out,
-                                       unsigned long long* mass_out) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  unsigned long long prefix = 0, above = 0, result = 0;
-  for (int shift = 56;; shift -= 8) {
-    for (int i = tid; i < 256; i += kSampThreads) {
-      sh.hmass[i] = 0;
-      sh.hcnt[i] = 0;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int e = 0; e < kSampPerThread; ++e) {
-      const int i = tid + e * kSampThreads;
-      if (i < n) {
-        const unsigned long long k = key[e];
-        if (shift == 56 || (k >> (shift + 8)) == prefix) {
-          const int bin = static_cast<int>((k >> shift) & 255ull);
-          atomicAdd(&sh.hmass[bin], mass[e]);
-          atomicAdd(&sh.hcnt[bin], 1u);
-        }
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255-8l .. 248-8l (descending)
-      unsigned long long m8[8];
-      unsigned long long tot = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        m8[j] = sh.hmass[255 - 8 * lane - j];
-        tot += m8[j];
-      }
-      unsigned long long incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const unsigned long long excl = incl - tot;
-      const unsigned long long need = target - above;   // >= 1
-      if (excl < need && need <= incl) {
-        unsigned long long cc = excl;   // mass before bin jb
-        int jb = 7;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (cc + m8[j] >= need) {
-            jb = j;
-            break;
+  float ze = -INFINITY;
+  sc.ekey = 0;
+  if (c.has_extra) {
+    ze = z[c.n_main];
+    sc.ekey = make_key(ze, c.extra_id);
+    zm = fmaxf(zm, ze);
+  }
+  sc.zmax = samp_block_max(zm, sm);   // includes a __syncthreads after the key stores
+  // bitonic sort, descending
+  for (int k = 2; k <= np; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < np; i += kSampThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = sm.key[i], b = sm.key[l];
+          const bool desc = (i & k) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            sm.key[i] = b;
+            sm.key[l] = a;
           }
-          cc += m8[j];
         }
-        const int bin = 255 - 8 * lane - jb;
-        sh.ibc[0] = bin;
-        sh.bc[0] = above + cc;
-        sh.ibc[1] = static_cast<int>(sh.hcnt[bin]);
-        sh.bc[1] = sh.hmass[bin];
-      }
-    }
-    __syncthreads();
-    const int bin = sh.ibc[0];
-    const int cnt = sh.ibc[1];
-    above = sh.bc[0];
-    const unsigned long long mbin = sh.bc[1];
-    prefix = (shift == 56) ? static_cast<unsigned long long>(bin)
-                           : ((prefix << 8) | static_cast<unsigned long long>(bin));
-    if (shift == 0) {
-      result = prefix;
-      *mass_out = mbin;
-      break;
-    }
-    if (cnt == 1) {
-#pragma unroll
-      for (int e = 0; e < kSampPerThread; ++e) {
-        const int i = tid + e * kSampThreads;
-        if (i < n && (key[e] >> shift) == prefix) sh.bc[2] = key[e];
       }
       __syncthreads();
-      result = sh.bc[2];
-      *mass_out = mbin;
-      break;
     }
+  }
+  sc.ins = 0;
+  if (c.has_extra) {
+    int cnt = 0;
+    for (int i = tid; i < np; i += kSampThreads) cnt += sm.key[i] > sc.ekey ? 1 : 0;
+    cnt = static_cast<int>(warp_sum(static_cast<float>(cnt)));
+    if ((tid & 31) == 0) sm.redf[tid >> 5] = static_cast<float>(cnt);
+    __syncthreads();
+    float t = 0.f;
+    for (int w = 0; w < kSampWarps; ++w) t += sm.redf[w];
+    sc.ins = static_cast<int>(t);
     __syncthreads();
   }
-  __syncthreads();
-  *above_out = above;
-  return result;
+  return sc;
 }
 
-// One draw: returns the chosen candidate index.
-DEVI int sample_draw(const float (&z)[kSampPerThread], const unsigned long long (&key)[kSampPerThread],
-                     const Cands& c, float temperature, float top_p, float u, SampShared& sh) {
-  const int tid = threadIdx.x;
+// One draw over the sorted candidates.  Returns the candidate index
+// (0..n_main-1, or n_main for the extra candidate).
+DEVI int samp_draw(const SortedCands& sc, const Cands& c, float temperature, float top_p, float u,
+                   SampSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int np = sc.np;
   if (!(temperature > 0.f)) {
-    unsigned long long best = 0;
-#pragma unroll
-    for (int e = 0; e < kSampPerThread; ++e)
-      if (tid + e * kSampThreads < c.n && key[e] > best) best = key[e];
-    return key_to_index(c, block_max_u64(best, sh));
+    const unsigned long long best = sm.key[0] > sc.ekey ? sm.key[0] : sc.ekey;
+    const int id = key_id(best);
+    return (c.has_extra && best == sc.ekey) ? c.n_main : id - c.id_base;
   }
-  float zmax = -INFINITY;
-#pragma unroll
-  for (int e = 0; e < kSampPerThread; ++e)
-    if (tid + e * kSampThreads < c.n) zmax = fmaxf(zmax, z[e]);
-  zmax = block_max_f(zmax, sh);
-  unsigned long long mass[kSampPerThread];
+  const float inv_t = 1.0f / temperature;
+  // each thread owns a contiguous segment of the sorted order
+  const int ept = (np + kSampThreads - 1) / kSampThreads;
+  const int i0 = tid * ept;
+  const unsigned long long me = c.has_extra ? fixed_mass(unord_f32(static_cast<uint32_t>(sc.ekey >> 32)), sc.zmax, inv_t) : 0ull;
   unsigned long long local = 0;
-#pragma unroll
-  for (int e = 0; e < kSampPerThread; ++e) {
-    mass[e] = 0;
-    if (tid + e * kSampThreads < c.n) {
-      const float p = expf((z[e] - zmax) / temperature);
-      mass[e] = __float2ull_rn(p * 1099511627776.0f);   // * 2^40
-      local += mass[e];
+  for (int e = 0; e < ept; ++e) {
+    const int i = i0 + e;
+    if (i < np) {
+      const unsigned long long k = sm.key[i];
+      const unsigned long long m = k ? fixed_mass(unord_f32(static_cast<uint32_t>(k >> 32)), sc.zmax, inv_t) : 0ull;
+      local += m;
+      sm.cum[i] = local;        // inclusive within the segment, fixed below
     }
   }
-  const unsigned long long Z = block_sum_u64(local, sh);
+  // exclusive scan of the thread totals
+  unsigned long long incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm.wsum[warp] = incl;
+  __syncthreads();
+  unsigned long long wbase = 0, total = 0;
+  for (int w = 0; w < kSampWarps; ++w) {
+    if (w < warp) wbase += sm.wsum[w];
+    total += sm.wsum[w];
+  }
+  const unsigned long long base = wbase + incl - local;
+  for (int e = 0; e < ept; ++e) {
+    const int i = i0 + e;
+    if (i < np) sm.cum[i] += base + ((c.has_extra && i >= sc.ins) ? me : 0ull);
+  }
+  __syncthreads();
+  const unsigned long long Z = total + me;
+  // extra candidate's interval in the merged order
+  const unsigned long long e_excl = sc.ins > 0 ? sm.cum[sc.ins - 1] : 0ull;
+  const unsigned long long e_incl = e_excl + me;
+  // find the candidate whose (excl, incl] interval contains target; for a
+  // sorted element i, excl = cum[i-1], plus the extra mass when the extra
+  // candidate sits right before it (i == ins)
+  auto find = [&](unsigned long long target) -> void {
+    for (int e = 0; e < ept; ++e) {
+      const int i = i0 + e;
+      if (i < np) {
+        const unsigned long long hi = sm.cum[i];
+        const unsigned long long lo =
+            (i > 0 ? sm.cum[i - 1] : 0ull) + ((c.has_extra && i == sc.ins) ? me : 0ull);
+        if (lo < target && target <= hi) {
+          sm.ibc[0] = i;
+          sm.bc[0] = hi;
+        }
+      }
+    }
+    if (tid == 0 && c.has_extra && e_excl < target && target <= e_incl) {
+      sm.ibc[0] = -1;
+      sm.bc[0] = e_incl;
+    }
+    __syncthreads();
+  };
   unsigned long long tc = Z;
   if (top_p < 1.0f) {
     const double t = ceil(static_cast<double>(top_p) * static_cast<double>(Z));
     tc = t < 1.0 ? 1ull : static_cast<unsigned long long>(t);
     if (tc > Z) tc = Z;
   }
-  unsigned long long above, mk;
-  select_by_mass(key, mass, c.n, tc, sh, &above, &mk);
-  const unsigned long long zk = above + mk;
-  unsigned long long td = static_cast<unsigned long long>(floor(static_cast<double>(u) * static_cast<double>(zk))) + 1ull;
+  find(tc);
+  const unsigned long long zk = sm.bc[0];
+  __syncthreads();
+  unsigned long long td =
+      static_cast<unsigned long long>(floor(static_cast<double>(u) * static_cast<double>(zk))) + 1ull;
   if (td > zk) td = zk;
-  if (td < 1ull) td = 1ull;
-  const unsigned long long kd = select_by_mass(key, mass, c.n, td, sh, &above, &mk);
-  return key_to_index(c, kd);
-}
-
-DEVI void load_candidates(const float* src, const Cands& c, float (&z)[kSampPerThread],
-                          unsigned long long (&key)[kSampPerThread]) {
-#pragma unroll
-  for (int e = 0; e < kSampPerThread; ++e) {
-    const int i = threadIdx.x + e * kSampThreads;
-    z[e] = -INFINITY;
-    key[e] = 0;
-    if (i < c.n) {
-      z[e] = src[i];
-      key[e] = (static_cast<unsigned long long>(ord_f32(z[e])) << 32) |
-               static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(cand_id(c, i)));
-    }
-  }
+  find(td);
+  const int pick = sm.ibc[0];
+  int idx;
+  if (pick < 0) idx = c.n_main;
+  else idx = key_id(sm.key[pick]) - c.id_base;
+  __syncthreads();
+  return idx;
 }
 
 __global__ void __launch_bounds__(kSampThreads)
     sample_q0_kernel(DevPtrs d, const float* uniforms, int ldu, SamplingParams sp,
                      const int32_t* forced, int ldf, int32_t* codes_out, int32_t* status_out,
                      float* slow_logits_out, int32_t* draws_out, const uint16_t* fast_emb) {
-  __shared__ SampShared sh;
+  extern __shared__ __align__(16) unsigned char samp_smem_raw[];
+  SampSmem& sm = *reinterpret_cast<SampSmem*>(samp_smem_raw);
   __shared__ int s_commit, s_active;
   const int row = blockIdx.x, tid = threadIdx.x;
   const RowInfo ri = d.rows[row];
@@ -972,15 +1159,13 @@ __global__ void __launch_bounds__(kSampThreads)
     return;
   }
   // [P2] "Two autoregressions": the bias keeps the semantic ids and <|im_end|>.
-  Cands c{ns + (sp.allow_eos ? 1 : 0), ns, d.sem_begin, d.im_end};
-  float z[kSampPerThread];
-  unsigned long long key[kSampPerThread];
-  load_candidates(zsrc, c, z, key);
+  const Cands c{ns, d.sem_begin, sp.allow_eos ? 1 : 0, d.im_end};
+  const SortedCands sc = samp_sort(zsrc, c, sm);
   const float* u = uniforms + static_cast<size_t>(row) * ldu;
-  const int normal = sample_draw(z, key, c, sp.temperature, sp.top_p, u[0], sh);
+  const int normal = samp_draw(sc, c, sp.temperature, sp.top_p, u[0], sm);
   // [P2] "Two autoregressions": a second draw at temperature 1.0, top-p 0.9,
   // used when the normal draw repeats a semantic token of the last 10 frames.
-  const int ras = sample_draw(z, key, c, sp.ras_temperature, sp.ras_top_p, u[1], sh);
+  const int ras = samp_draw(sc, c, sp.ras_temperature, sp.ras_top_p, u[1], sm);
   if (tid == 0) {
     const int hn = d.hist_n[slot];
     const int w = min(sp.ras_win, hn);
@@ -1037,7 +1222,8 @@ __global__ void __launch_bounds__(kSampThreads)
     sample_fast_kernel(DevPtrs d, int k, const float* uniforms, int ldu, SamplingParams sp,
                        const int32_t* forced, int ldf, int32_t* codes_out, float* fast_logits_out,
                        int32_t* draws_out, const uint16_t* fast_emb) {
-  __shared__ SampShared sh;
+  extern __shared__ __align__(16) unsigned char samp_smem_raw[];
+  SampSmem& sm = *reinterpret_cast<SampSmem*>(samp_smem_raw);
   __shared__ int s_commit;
   const int row = blockIdx.x, tid = threadIdx.x;
   const int N = d.N, Cf = d.Cf;
@@ -1046,12 +1232,10 @@ __global__ void __launch_bounds__(kSampThreads)
     for (int i = tid; i < Cf; i += kSampThreads)
       fast_logits_out[(static_cast<size_t>(row) * (N - 1) + (k - 1)) * Cf + i] = zs[i];
   if (!d.rows[row].active) return;
-  Cands c{Cf, Cf, 0, -1};
-  float z[kSampPerThread];
-  unsigned long long key[kSampPerThread];
-  load_candidates(zs, c, z, key);
+  const Cands c{Cf, 0, 0, -1};
+  const SortedCands sc = samp_sort(zs, c, sm);
   const float* u = uniforms + static_cast<size_t>(row) * ldu;
-  const int draw = sample_draw(z, key, c, sp.temperature, sp.top_p, u[k + 1], sh);
+  const int draw = samp_draw(sc, c, sp.temperature, sp.top_p, u[k + 1], sm);
   if (tid == 0) {
     int commit = forced ? forced[static_cast<size_t>(row) * ldf + k] : draw;
     if (commit < 0 || commit >= Cf) {
@@ -1072,13 +1256,27 @@ __global__ void __launch_bounds__(kSampThreads)
   }
 }
 
+static cudaError_t samp_configure() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(sample_q0_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(SampSmem)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sample_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(SampSmem)));
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
 cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms, int ldu,
                              const SamplingParams& sp, const int32_t* forced, int ldf,
                              int32_t* codes_out, int32_t* status_out, float* slow_logits_out,
                              int32_t* draws_out, const uint16_t* fast_emb, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  sample_q0_kernel<<<nrows, kSampThreads, 0, st>>>(d, uniforms, ldu, sp, forced, ldf, codes_out,
-                                                   status_out, slow_logits_out, draws_out, fast_emb);
+  cudaError_t e = samp_configure();
+  if (e != cudaSuccess) return e;
+  sample_q0_kernel<<<nrows, kSampThreads, sizeof(SampSmem), st>>>(
+      d, uniforms, ldu, sp, forced, ldf, codes_out, status_out, slow_logits_out, draws_out, fast_emb);
   return cudaGetLastError();
 }
 
@@ -1087,8 +1285,10 @@ cudaError_t launch_sample_fast(const DevPtrs& d, int nrows, int k, const float* 
                                int32_t* codes_out, float* fast_logits_out, int32_t* draws_out,
                                const uint16_t* fast_emb, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  sample_fast_kernel<<<nrows, kSampThreads, 0, st>>>(d, k, uniforms, ldu, sp, forced, ldf, codes_out,
-                                                     fast_logits_out, draws_out, fast_emb);
+  cudaError_t e = samp_configure();
+  if (e != cudaSuccess) return e;
+  sample_fast_kernel<<<nrows, kSampThreads, sizeof(SampSmem), st>>>(
+      d, k, uniforms, ldu, sp, forced, ldf, codes_out, fast_logits_out, draws_out, fast_emb);
   return cudaGetLastError();
 }
 

@@ -62,8 +62,8 @@ enum {
  * the slow AR's width and heads (fast_dim = dim; no fast_project_in).
  * Requirements: dim % 8 == 0, ffn % 8 == 0, head_dim in {64, 128},
  * n_head % n_kv_head == 0 with n_head / n_kv_head in {1, 2, 4, 8},
- * page_tokens == 64, n_codebooks in [2, 16], n_sem + 1 <= 4608,
- * fast_vocab <= 4608, im_end_id outside [sem_begin, sem_begin + n_sem). */
+ * page_tokens == 64, n_codebooks in [2, 16], n_sem <= 4096,
+ * fast_vocab <= 4096, im_end_id outside [sem_begin, sem_begin + n_sem). */
 typedef struct dualar_config {
   int32_t dim;           /* model width D */
   int32_t n_layer;       /* slow-AR layers */
