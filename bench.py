@@ -40,6 +40,8 @@ WORKLOADS = {
     "s2pro_b1": dict(cfg="s2pro", batch=1, prompt=512, frames=256, temperature=0.8, top_p=0.8,
                      ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 1, 512-token prompt, 256 frames, "
                                        "T=0.8 top-p 0.8 RAS window 10"),
+    "s2pro_l1_b1": dict(cfg="s2pro_l1", batch=1, prompt=512, frames=16, temperature=0.8, top_p=0.8,
+                        ras_win=10, desc="one-layer S2-Pro-shaped profiling case, batch 1, 512-token prompt"),
     "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
                     desc="tiny Dual-AR, batch 1, 32-token prompt, 16 frames"),
 }
@@ -174,8 +176,8 @@ def main():
     config = {"workload": f"{args.workload}: {wl['desc']}", "batch": wl["batch"],
               "prompt_tokens": wl["prompt"], "frames": W + K,
               "l2": "inputs larger than L2 (9.1 GB of weights streamed per frame); no flush"}
-    if args.workload == "tiny_b1":
-        config["l2"] = "tiny weights fit in L2 (parity workload, not a bench line)"
+    if args.workload != "s2pro_b1":
+        config["l2"] = "small profiling/parity workload, not a bench line"
 
     if args.impl == "reference":
         if rank != 0:

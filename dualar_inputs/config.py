@@ -151,7 +151,15 @@ TINY = DualARConfig(
     ffn=768, vocab=1_024, sem_begin=512, n_sem=512, im_end_id=3,
     fast_n_layer=2, fast_vocab=128, n_codebooks=4)
 
-CONFIGS = {"tiny": TINY, "s2pro": S2PRO}
+# Profiling case: S2-Pro layer shapes (dim 2560, 32/8 heads of 128, FFN 9728,
+# 4,096 semantic ids, fast vocab 4,096, N = 10) with one slow and one fast
+# layer and an 8,192-id vocabulary, so one process holds well under 1 GB.
+S2PRO_L1 = DualARConfig(
+    name="s2pro_l1", dim=2560, n_layer=1, n_head=32, n_kv_head=8, head_dim=128,
+    ffn=9728, vocab=8_192, sem_begin=4_000, n_sem=4_096, im_end_id=3_999,
+    fast_n_layer=1, fast_vocab=4_096, n_codebooks=10)
+
+CONFIGS = {"tiny": TINY, "s2pro": S2PRO, "s2pro_l1": S2PRO_L1}
 
 # Audio frames per second of the codec: 44,100 Hz / hop 2,048.
 FRAMES_PER_AUDIO_SECOND = 44_100 / 2_048
