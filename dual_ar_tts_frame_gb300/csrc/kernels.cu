@@ -22,6 +22,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "gemv.cuh"
 #include "internal.h"
 
 namespace dualar {
@@ -69,239 +70,68 @@ cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t*
 }
 
 // ============================================================================
-// GEMV: y[b][n] = sum_k W[n][k] x'[b][k], x' = RMSNorm(x) (optional)
+// GEMV (standalone launch; device code in gemv.cuh)
 // ============================================================================
-// Each CTA owns a contiguous range of output rows (balanced to +-1 row) and
-// walks it in groups of 8 rows, one row per consumer warp.  K is cut into
-// chunks of at most kChunk elements; a ring stage holds one (group, chunk)
-// tile: up to 8 row-chunks per matrix (16 for the SwiGLU gate/up pair), each
-// fetched by one bulk copy.  A warp accumulates its row over the chunks and
-// reduces with shuffles only, so consumer warps never synchronise with each
-// other; the producer thread runs ahead by the ring depth.
-constexpr int kRowsPerGroup = kGemvConsumerWarps;   // 8
-constexpr int kChunk = 2560;                        // elements per row-chunk (one matrix)
 constexpr int kMaxStages = 8;
-constexpr int kSmemBudget = 225 * 1024;             // dynamic shared memory per CTA
-
-struct GemvPlan {
-  int kc;          // chunk length (elements, multiple of 8)
-  int n_chunks;
-  int nmat;        // 1, or 2 for SwiGLU
-  int tile_bytes;  // ring stage size
-  int stages;
-  int nbt;         // activation rows per launch (template)
-  size_t smem;
-};
+constexpr int kSmemBudget = 225 * 1024;   // dynamic shared memory per CTA
 
 // Shared-memory layout of gemv_kernel (offsets in bytes).
 __host__ __device__ inline size_t gemv_misc_off() { return 256; }
-__host__ __device__ inline size_t gemv_xs_off() { return 256 + 4 * 128; }
+__host__ __device__ inline size_t gemv_xs_off() { return 1024; }
 __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
   return (gemv_xs_off() + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
 }
 
 template <int NB>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-    gemv_kernel(const GemvArgs a, const int kc, const int n_chunks, const int stages,
-                const int tile_bytes) {
+__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a, const int stages) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
+  GemvRing ring;
+  ring.full = reinterpret_cast<uint64_t*>(smem);
+  ring.empty = ring.full + kMaxStages;
+  ring.base = smem + gemv_ring_off(NB, a.K);
+  ring.stages = stages;
   float* misc = reinterpret_cast<float*>(smem + gemv_misc_off());
   float* xs = reinterpret_cast<float*>(smem + gemv_xs_off());
-  unsigned char* ring = smem + gemv_ring_off(NB, a.K);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int K = a.K;
-  const bool swiglu = a.mode == GEMV_SWIGLU;
-  const int nmat = swiglu ? 2 : 1;
-  const int nv = swiglu ? a.n0 : a.n0 + a.n1;
-  const int v_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * nv) / gridDim.x);
-  const int v_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * nv) / gridDim.x);
-  const int n_groups = (v_end - v_begin + kRowsPerGroup - 1) / kRowsPerGroup;
-  const int n_tiles = n_groups * n_chunks;
-  const size_t slot_bytes = static_cast<size_t>(kc) * 2;   // one row-chunk in a stage
-
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGemvConsumerWarps);
+      mbar_init(&ring.full[s], 1);
+      mbar_init(&ring.empty[s], kGemvConsumerWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-
+  const GemvGeo g = gemv_geo(a, blockIdx.x, gridDim.x);
+  uint32_t t = 0;
   if (warp == kGemvConsumerWarps) {
-    // ---------------- producer: one thread streams the CTA's weight rows ---
-    if (lane != 0) return;
-    const uint64_t pol = policy_evict_first();
-    for (int t = 0; t < n_tiles; ++t) {
-      const int s = t % stages;
-      if (t >= stages) {
-        if (!mbar_wait(&empty[s], ((t / stages) - 1) & 1, a.err, a.wait_limit_ns)) return;
-      }
-      const int g = t / n_chunks, c = t % n_chunks;
-      const int v0 = v_begin + g * kRowsPerGroup;
-      const int rows = min(kRowsPerGroup, v_end - v0);
-      const int k0 = c * kc;
-      const int len = min(kc, K - k0);
-      const uint32_t bytes = static_cast<uint32_t>(len) * 2;
-      mbar_arrive_expect_tx(&full[s], bytes * rows * nmat);
-      unsigned char* st = ring + static_cast<size_t>(s) * tile_bytes;
-      for (int m = 0; m < nmat; ++m) {
-        for (int w = 0; w < rows; ++w) {
-          const int v = v0 + w;
-          const uint16_t* rowp;
-          if (swiglu) rowp = (m ? a.w1 : a.w0) + static_cast<size_t>(v) * K;
-          else rowp = v < a.n0 ? a.w0 + static_cast<size_t>(v) * K
-                               : a.w1 + static_cast<size_t>(v - a.n0) * K;
-          bulk_load_g2s(st + (m * kRowsPerGroup + w) * slot_bytes, rowp + k0, bytes, &full[s], pol);
-        }
-      }
+    if (lane == 0) {
+      gemv_produce(a, g, ring, t, policy_evict_first(), nullptr);
+      gemv_drain(ring, t, a.wait_limit_ns);
     }
     return;
   }
-
-  // ---------------- consumers ------------------------------------------------
-  constexpr int NCT = kGemvConsumerWarps * 32;
-  const int nb = a.nb;
-  // Stage x (and its RMSNorm) in shared memory.
-  float ss[NB];
-#pragma unroll
-  for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-  const int K4 = K >> 2;
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    if (b < nb) {
-      const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
-      float4* dst = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
-      for (int k = tid; k < K4; k += NCT) {
-        const float4 v = src[k];
-        dst[k] = v;
-        ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      }
-    }
-  }
-  if (a.norm_w != nullptr) {
-    // [P1] "Fast Transformer": RMSNorm(dim, eps=norm_eps), pre-norm blocks.
-    float* red = misc + 8;   // [8 warps][NB]
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float w = warp_sum(ss[b]);
-      if (lane == 0) red[warp * NB + b] = w;
-    }
-    named_barrier(1, NCT);
-    if (tid < NB) {
-      float t = 0.f;
-      for (int w = 0; w < kGemvConsumerWarps; ++w) t += red[w * NB + tid];
-      misc[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
-    }
-    named_barrier(1, NCT);
-    for (int b = 0; b < nb; ++b) {
-      const float sc = misc[b];
-      float* xb = xs + static_cast<size_t>(b) * K;
-      for (int k = tid; k < K; k += NCT) xb[k] = (xb[k] * sc) * bf16bits_to_f32(a.norm_w[k]);
-    }
-  }
-  named_barrier(1, NCT);
-  if (a.save_x != nullptr && blockIdx.x == 0) {
-    for (int b = 0; b < nb; ++b) {
-      const int row = a.save_map ? a.save_map[b] : b;
-      if (row < 0) continue;
-      for (int k = tid; k < K; k += NCT)
-        a.save_x[static_cast<size_t>(row) * a.lds + k] = xs[static_cast<size_t>(b) * K + k];
-    }
-  }
-
-  const float4* xs4 = reinterpret_cast<const float4*>(xs);
-  float acc[2][NB];
-  for (int t = 0; t < n_tiles; ++t) {
-    const int s = t % stages;
-    const int g = t / n_chunks, c = t % n_chunks;
-    const int v0 = v_begin + g * kRowsPerGroup;
-    const int rows = min(kRowsPerGroup, v_end - v0);
-    if (c == 0) {
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int b = 0; b < NB; ++b) acc[m][b] = 0.f;
-    }
-    if (!mbar_wait(&full[s], (t / stages) & 1, a.err, a.wait_limit_ns)) return;
-    if (warp < rows) {
-      const int k0 = c * kc;
-      const int nvec = min(kc, K - k0) >> 3;
-      const unsigned char* st = ring + static_cast<size_t>(s) * tile_bytes;
-      for (int m = 0; m < nmat; ++m) {
-        const uint4* wr = reinterpret_cast<const uint4*>(st + (m * kRowsPerGroup + warp) * slot_bytes);
-        float p0[NB], p1[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) p0[b] = p1[b] = 0.f;
-        int j = lane;
-#pragma unroll 2
-        for (; j + 32 < nvec; j += 64) {
-          const uint4 w0 = wr[j], w1 = wr[j + 32];
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            const size_t xb = (static_cast<size_t>(b) * K + k0) >> 2;
-            p0[b] = dot8(w0, xs4[xb + 2 * j], xs4[xb + 2 * j + 1], p0[b]);
-            p1[b] = dot8(w1, xs4[xb + 2 * (j + 32)], xs4[xb + 2 * (j + 32) + 1], p1[b]);
-          }
-        }
-        if (j < nvec) {
-          const uint4 w0 = wr[j];
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            const size_t xb = (static_cast<size_t>(b) * K + k0) >> 2;
-            p0[b] = dot8(w0, xs4[xb + 2 * j], xs4[xb + 2 * j + 1], p0[b]);
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < NB; ++b) acc[m][b] += p0[b] + p1[b];
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (c == n_chunks - 1 && warp < rows) {
-      const int n = v0 + warp;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        acc[0][b] = warp_sum(acc[0][b]);
-        if (swiglu) acc[1][b] = warp_sum(acc[1][b]);
-      }
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (lane == b && b < nb) {
-          const int orow = a.out_map ? a.out_map[b] : b;
-          if (orow >= 0) {
-            float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
-            if (a.mode == GEMV_STORE) *o = acc[0][b];
-            else if (a.mode == GEMV_ADD) *o = a.base[static_cast<size_t>(orow) * a.ldb + n] + acc[0][b];
-            // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
-            else *o = silu(acc[0][b]) * acc[1][b];
-          }
-        }
-      }
-    }
-  }
+  gemv_stage_x<NB>(a, xs, misc, misc + 16 * 8, blockIdx.x, false);
+  gemv_consume<NB>(a, g, ring, t, xs);
 }
 
-static GemvPlan plan_gemv(int K, int nb, int mode) {
+struct GemvPlan {
+  int stages;
+  int nbt;
+  size_t smem;
+};
+
+static GemvPlan plan_gemv(int K, int nb) {
   GemvPlan p;
-  p.nmat = mode == GEMV_SWIGLU ? 2 : 1;
-  const int kmax = kChunk / p.nmat;
-  p.n_chunks = (K + kmax - 1) / kmax;
-  p.kc = ((K + p.n_chunks - 1) / p.n_chunks + 7) & ~7;
-  p.tile_bytes = (kRowsPerGroup * p.nmat * p.kc * 2 + 127) & ~127;
   int nbt = nb >= 8 ? 8 : nb >= 4 ? 4 : nb >= 2 ? 2 : 1;
   while (true) {
     const size_t ring = gemv_ring_off(nbt, K);
     const long long room = static_cast<long long>(kSmemBudget) - static_cast<long long>(ring);
-    int st = room > 0 ? static_cast<int>(room / p.tile_bytes) : 0;
+    const int st = room > 0 ? static_cast<int>(room / kStageBytes) : 0;
     if (st >= 2 || nbt == 1) {
       p.nbt = nbt;
       p.stages = st > kMaxStages ? kMaxStages : st;
-      p.smem = ring + static_cast<size_t>(p.stages) * p.tile_bytes;
+      p.smem = ring + static_cast<size_t>(p.stages) * kStageBytes;
       return p;
     }
     nbt >>= 1;
@@ -317,14 +147,14 @@ static cudaError_t launch_gemv_nb(const GemvArgs& a, const GemvPlan& p, int grid
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  gemv_kernel<NB><<<grid, kGemvThreads, p.smem, st>>>(a, p.kc, p.n_chunks, p.stages, p.tile_bytes);
+  gemv_kernel<NB><<<grid, kGemvThreads, p.smem, st>>>(a, p.stages);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
   if (a.nb <= 0) return cudaSuccess;
   if (a.K % 8 != 0) return cudaErrorInvalidValue;
-  const GemvPlan p = plan_gemv(a.K, a.nb, a.mode);
+  const GemvPlan p = plan_gemv(a.K, a.nb);
   if (p.stages < 1 || p.smem > static_cast<size_t>(kSmemBudget)) return cudaErrorInvalidValue;
   const int nv = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
   const int grid = nv < n_sm ? nv : n_sm;
@@ -915,230 +745,248 @@ cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, co
 // ============================================================================
 // Candidates are ordered by (logit descending, token id ascending): each gets
 // a unique 64-bit key (order-preserving bits of the logit, then the inverted
-// id), and the keys are sorted in shared memory (bitonic).  Probability mass
-// is integer fixed point, round(exp((z - zmax) / T) * 2^40), so prefix sums
-// are exact and independent of thread order.  The top-p cut is the first
-// candidate whose inclusive cumulative mass reaches ceil(top_p * Z); the draw
-// is the first kept candidate whose inclusive cumulative mass reaches
-// floor(u * Zk) + 1, i.e. exceeds u * Zk.  One sort serves the normal draw
-// and the repetition-aware resample.  A single extra candidate (<|im_end|>
-// for q0) is merged into the sorted order virtually.  [P2] "Two
+// id).  Probability mass is integer fixed point, round(exp((z - zmax) / T) *
+// 2^24), so every sum is exact and independent of thread order.  The top-p
+// cut is the first candidate (in key order) whose inclusive cumulative mass
+// reaches ceil(top_p * Z); the draw is the first kept candidate whose
+// inclusive cumulative mass reaches floor(u * Zk) + 1, i.e. exceeds u * Zk.
+// Both are found by a most-significant-byte-first radix descent over the
+// keys with 256-bin mass histograms; lanes of a warp that hit the same bin
+// are combined (match + reduce) before one shared-memory atomic.  [P2] "Two
 // autoregressions": sample(biased_logits, ...) for q0, unmasked
 // sample(logits, ...) for q1..q9.
-constexpr int kSampWarps = kSampThreads / 32;
-constexpr int kSortMax = 4096;
+constexpr int kMaxCands = 4097;
 
+template <int NT>
 struct SampSmem {
-  unsigned long long key[kSortMax];
-  unsigned long long cum[kSortMax];
-  unsigned long long wsum[kSampWarps];
-  float redf[kSampWarps];
+  static constexpr int NW = NT / 32;
+  unsigned long long hmass[256];
+  unsigned int hcnt[256];
+  unsigned long long red64[NW];
+  float redf[NW];
   unsigned long long bc[4];
   int ibc[4];
 };
 
 struct Cands {
-  int n_main;      // candidates 0..n_main-1 have ids id_base + i
+  int n;          // candidates
+  int n_main;     // candidates 0..n_main-1 have ids id_base + i
   int id_base;
-  int has_extra;   // candidate n_main with id extra_id
-  int extra_id;
+  int extra_id;   // id of candidate n_main when n > n_main
 };
 
 DEVI uint32_t ord_f32(float f) {
   const uint32_t u = __float_as_uint(f + 0.0f);   // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-DEVI float unord_f32(uint32_t o) {
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
-DEVI unsigned long long make_key(float z, int id) {
-  return (static_cast<unsigned long long>(ord_f32(z)) << 32) |
-         static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(id));
-}
-DEVI int key_id(unsigned long long k) {
-  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
-}
-DEVI unsigned long long fixed_mass(float z, float zmax, float inv_t) {
-  return __float2ull_rn(expf((z - zmax) * inv_t) * 1099511627776.0f);   // * 2^40
+DEVI int cand_id(const Cands& c, int i) { return i < c.n_main ? c.id_base + i : c.extra_id; }
+DEVI int key_to_index(const Cands& c, unsigned long long key) {
+  const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+  if (c.n > c.n_main && id == c.extra_id) return c.n_main;
+  return id - c.id_base;
 }
 
-DEVI float samp_block_max(float v, SampSmem& sm) {
+template <int NT>
+DEVI float samp_block_max(float v, SampSmem<NT>& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_max(v);
   if (lane == 0) sm.redf[warp] = v;
   __syncthreads();
   float t = sm.redf[0];
-  for (int w = 1; w < kSampWarps; ++w) t = fmaxf(t, sm.redf[w]);
+  for (int w = 1; w < SampSmem<NT>::NW; ++w) t = fmaxf(t, sm.redf[w]);
   __syncthreads();
   return t;
 }
 
-// Sorted candidate list shared by the draws of one row.
-struct SortedCands {
-  int np;                     // padded (power of two) length of key[]
-  int n_main;
-  unsigned long long ekey;    // extra candidate key (0 if none)
-  int ins;                    // sorted keys strictly greater than ekey
-  float zmax;
-};
-
-// Loads z[0..n_main) (+ extra at z[n_main]) and sorts.  All threads call.
-DEVI SortedCands samp_sort(const float* z, const Cands& c, SampSmem& sm) {
-  const int tid = threadIdx.x;
-  SortedCands sc;
-  sc.n_main = c.n_main;
-  int np = 1;
-  while (np < c.n_main) np <<= 1;
-  sc.np = np;
-  float zm = -INFINITY;
-  for (int i = tid; i < np; i += kSampThreads) {
-    unsigned long long k = 0;
-    if (i < c.n_main) {
-      const float v = z[i];
-      zm = fmaxf(zm, v);
-      k = make_key(v, c.id_base + i);
-    }
-    sm.key[i] = k;
-  }
-  float ze = -INFINITY;
-  sc.ekey = 0;
-  if (c.has_extra) {
-    ze = z[c.n_main];
-    sc.ekey = make_key(ze, c.extra_id);
-    zm = fmaxf(zm, ze);
-  }
-  sc.zmax = samp_block_max(zm, sm);   // includes a __syncthreads after the key stores
-  // bitonic sort, descending
-  for (int k = 2; k <= np; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < np; i += kSampThreads) {
-        const int l = i ^ j;
-        if (l > i) {
-          const unsigned long long a = sm.key[i], b = sm.key[l];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            sm.key[i] = b;
-            sm.key[l] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  sc.ins = 0;
-  if (c.has_extra) {
-    int cnt = 0;
-    for (int i = tid; i < np; i += kSampThreads) cnt += sm.key[i] > sc.ekey ? 1 : 0;
-    cnt = static_cast<int>(warp_sum(static_cast<float>(cnt)));
-    if ((tid & 31) == 0) sm.redf[tid >> 5] = static_cast<float>(cnt);
-    __syncthreads();
-    float t = 0.f;
-    for (int w = 0; w < kSampWarps; ++w) t += sm.redf[w];
-    sc.ins = static_cast<int>(t);
-    __syncthreads();
-  }
-  return sc;
+template <int NT>
+DEVI unsigned long long samp_block_sum(unsigned long long v, SampSmem<NT>& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  if (lane == 0) sm.red64[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int w = 0; w < SampSmem<NT>::NW; ++w) t += sm.red64[w];
+  __syncthreads();
+  return t;
 }
 
-// One draw over the sorted candidates.  Returns the candidate index
-// (0..n_main-1, or n_main for the extra candidate).
-DEVI int samp_draw(const SortedCands& sc, const Cands& c, float temperature, float top_p, float u,
-                   SampSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int np = sc.np;
-  if (!(temperature > 0.f)) {
-    const unsigned long long best = sm.key[0] > sc.ekey ? sm.key[0] : sc.ekey;
-    const int id = key_id(best);
-    return (c.has_extra && best == sc.ekey) ? c.n_main : id - c.id_base;
-  }
-  const float inv_t = 1.0f / temperature;
-  // each thread owns a contiguous segment of the sorted order
-  const int ept = (np + kSampThreads - 1) / kSampThreads;
-  const int i0 = tid * ept;
-  const unsigned long long me = c.has_extra ? fixed_mass(unord_f32(static_cast<uint32_t>(sc.ekey >> 32)), sc.zmax, inv_t) : 0ull;
-  unsigned long long local = 0;
-  for (int e = 0; e < ept; ++e) {
-    const int i = i0 + e;
-    if (i < np) {
-      const unsigned long long k = sm.key[i];
-      const unsigned long long m = k ? fixed_mass(unord_f32(static_cast<uint32_t>(k >> 32)), sc.zmax, inv_t) : 0ull;
-      local += m;
-      sm.cum[i] = local;        // inclusive within the segment, fixed below
-    }
-  }
-  // exclusive scan of the thread totals
-  unsigned long long incl = local;
+template <int NT>
+DEVI unsigned long long samp_block_max_u64(unsigned long long v, SampSmem<NT>& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
   }
-  if (lane == 31) sm.wsum[warp] = incl;
+  if (lane == 0) sm.red64[warp] = v;
   __syncthreads();
-  unsigned long long wbase = 0, total = 0;
-  for (int w = 0; w < kSampWarps; ++w) {
-    if (w < warp) wbase += sm.wsum[w];
-    total += sm.wsum[w];
-  }
-  const unsigned long long base = wbase + incl - local;
-  for (int e = 0; e < ept; ++e) {
-    const int i = i0 + e;
-    if (i < np) sm.cum[i] += base + ((c.has_extra && i >= sc.ins) ? me : 0ull);
-  }
+  unsigned long long t = 0;
+  for (int w = 0; w < SampSmem<NT>::NW; ++w) t = sm.red64[w] > t ? sm.red64[w] : t;
   __syncthreads();
-  const unsigned long long Z = total + me;
-  // extra candidate's interval in the merged order
-  const unsigned long long e_excl = sc.ins > 0 ? sm.cum[sc.ins - 1] : 0ull;
-  const unsigned long long e_incl = e_excl + me;
-  // find the candidate whose (excl, incl] interval contains target; for a
-  // sorted element i, excl = cum[i-1], plus the extra mass when the extra
-  // candidate sits right before it (i == ins)
-  auto find = [&](unsigned long long target) -> void {
-    for (int e = 0; e < ept; ++e) {
-      const int i = i0 + e;
-      if (i < np) {
-        const unsigned long long hi = sm.cum[i];
-        const unsigned long long lo =
-            (i > 0 ? sm.cum[i - 1] : 0ull) + ((c.has_extra && i == sc.ins) ? me : 0ull);
-        if (lo < target && target <= hi) {
-          sm.ibc[0] = i;
-          sm.bc[0] = hi;
-        }
-      }
-    }
-    if (tid == 0 && c.has_extra && e_excl < target && target <= e_incl) {
-      sm.ibc[0] = -1;
-      sm.bc[0] = e_incl;
+  return t;
+}
+
+// First key (descending) whose inclusive cumulative mass reaches target
+// (1 <= target <= total).  *above_out: mass strictly before it; *mass_out:
+// its own mass.
+template <int NT, int EPT>
+DEVI unsigned long long samp_select(const unsigned long long (&key)[EPT], const uint32_t (&mass)[EPT],
+                                    int n, unsigned long long target, SampSmem<NT>& sm,
+                                    unsigned long long* above_out, unsigned long long* mass_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long prefix = 0, above = 0, result = 0;
+  for (int shift = 56;; shift -= 8) {
+    for (int b = tid; b < 256; b += NT) {
+      sm.hmass[b] = 0;
+      sm.hcnt[b] = 0;
     }
     __syncthreads();
-  };
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = tid + e * NT;
+      const bool valid = i < n && (shift == 56 || (key[e] >> (shift + 8)) == prefix);
+      const uint32_t bin = valid ? static_cast<uint32_t>((key[e] >> shift) & 255ull) : 256u;
+      const uint32_t grp = __match_any_sync(0xFFFFFFFFu, bin);
+      const uint32_t sum = __reduce_add_sync(grp, valid ? mass[e] : 0u);
+      if (valid && (__ffs(grp) - 1) == lane) {
+        atomicAdd(&sm.hmass[bin], static_cast<unsigned long long>(sum));
+        atomicAdd(&sm.hcnt[bin], static_cast<unsigned int>(__popc(grp)));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending)
+      unsigned long long m8[8];
+      unsigned long long tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        m8[j] = sm.hmass[255 - 8 * lane - j];
+        tot += m8[j];
+      }
+      unsigned long long incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned long long excl = incl - tot;
+      const unsigned long long need = target - above;   // >= 1
+      if (excl < need && need <= incl) {
+        unsigned long long cc = excl;
+        int jb = 7;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cc + m8[j] >= need) {
+            jb = j;
+            break;
+          }
+          cc += m8[j];
+        }
+        const int bin = 255 - 8 * lane - jb;
+        sm.ibc[0] = bin;
+        sm.ibc[1] = static_cast<int>(sm.hcnt[bin]);
+        sm.bc[0] = above + cc;
+        sm.bc[1] = sm.hmass[bin];
+      }
+    }
+    __syncthreads();
+    const int bin = sm.ibc[0];
+    const int cnt = sm.ibc[1];
+    above = sm.bc[0];
+    const unsigned long long mbin = sm.bc[1];
+    prefix = (shift == 56) ? static_cast<unsigned long long>(bin)
+                           : ((prefix << 8) | static_cast<unsigned long long>(bin));
+    if (shift == 0) {
+      result = prefix;
+      *mass_out = mbin;
+      break;
+    }
+    if (cnt == 1) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const int i = tid + e * NT;
+        if (i < n && (key[e] >> shift) == prefix) sm.bc[2] = key[e];
+      }
+      __syncthreads();
+      result = sm.bc[2];
+      *mass_out = mbin;
+      break;
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  *above_out = above;
+  return result;
+}
+
+// One draw: returns the chosen candidate index.
+template <int NT, int EPT>
+DEVI int samp_draw(const float (&z)[EPT], const unsigned long long (&key)[EPT], const Cands& c,
+                   float zmax, float temperature, float top_p, float u, SampSmem<NT>& sm) {
+  const int tid = threadIdx.x;
+  if (!(temperature > 0.f)) {
+    unsigned long long best = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (tid + e * NT < c.n && key[e] > best) best = key[e];
+    return key_to_index(c, samp_block_max_u64(best, sm));
+  }
+  const float inv_t = 1.0f / temperature;
+  uint32_t mass[EPT];
+  unsigned long long local = 0;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    mass[e] = 0;
+    if (tid + e * NT < c.n) {
+      mass[e] = __float2uint_rn(expf((z[e] - zmax) * inv_t) * 16777216.0f);   // * 2^24
+      local += mass[e];
+    }
+  }
+  const unsigned long long Z = samp_block_sum(local, sm);
   unsigned long long tc = Z;
   if (top_p < 1.0f) {
     const double t = ceil(static_cast<double>(top_p) * static_cast<double>(Z));
     tc = t < 1.0 ? 1ull : static_cast<unsigned long long>(t);
     if (tc > Z) tc = Z;
   }
-  find(tc);
-  const unsigned long long zk = sm.bc[0];
-  __syncthreads();
+  unsigned long long above, mk;
+  samp_select<NT, EPT>(key, mass, c.n, tc, sm, &above, &mk);
+  const unsigned long long zk = above + mk;
   unsigned long long td =
       static_cast<unsigned long long>(floor(static_cast<double>(u) * static_cast<double>(zk))) + 1ull;
   if (td > zk) td = zk;
-  find(td);
-  const int pick = sm.ibc[0];
-  int idx;
-  if (pick < 0) idx = c.n_main;
-  else idx = key_id(sm.key[pick]) - c.id_base;
-  __syncthreads();
-  return idx;
+  const unsigned long long kd = samp_select<NT, EPT>(key, mass, c.n, td, sm, &above, &mk);
+  return key_to_index(c, kd);
 }
+
+// Loads the candidates' logits and keys into registers; returns zmax.
+template <int NT, int EPT>
+DEVI float samp_load(const float* src, const Cands& c, float (&z)[EPT], unsigned long long (&key)[EPT],
+                     SampSmem<NT>& sm) {
+  float zm = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = threadIdx.x + e * NT;
+    z[e] = -INFINITY;
+    key[e] = 0;
+    if (i < c.n) {
+      z[e] = src[i];
+      zm = fmaxf(zm, z[e]);
+      key[e] = (static_cast<unsigned long long>(ord_f32(z[e])) << 32) |
+               static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(cand_id(c, i)));
+    }
+  }
+  return samp_block_max(zm, sm);
+}
+
+constexpr int kSampEPT = (kMaxCands + kSampThreads - 1) / kSampThreads;
 
 __global__ void __launch_bounds__(kSampThreads)
     sample_q0_kernel(DevPtrs d, const float* uniforms, int ldu, SamplingParams sp,
                      const int32_t* forced, int ldf, int32_t* codes_out, int32_t* status_out,
                      float* slow_logits_out, int32_t* draws_out, const uint16_t* fast_emb) {
-  extern __shared__ __align__(16) unsigned char samp_smem_raw[];
-  SampSmem& sm = *reinterpret_cast<SampSmem*>(samp_smem_raw);
+  __shared__ SampSmem<kSampThreads> sm;
   __shared__ int s_commit, s_active;
   const int row = blockIdx.x, tid = threadIdx.x;
   const RowInfo ri = d.rows[row];
@@ -1159,13 +1007,16 @@ __global__ void __launch_bounds__(kSampThreads)
     return;
   }
   // [P2] "Two autoregressions": the bias keeps the semantic ids and <|im_end|>.
-  const Cands c{ns, d.sem_begin, sp.allow_eos ? 1 : 0, d.im_end};
-  const SortedCands sc = samp_sort(zsrc, c, sm);
+  const Cands c{ns + (sp.allow_eos ? 1 : 0), ns, d.sem_begin, d.im_end};
+  float z[kSampEPT];
+  unsigned long long key[kSampEPT];
+  const float zmax = samp_load<kSampThreads, kSampEPT>(zsrc, c, z, key, sm);
   const float* u = uniforms + static_cast<size_t>(row) * ldu;
-  const int normal = samp_draw(sc, c, sp.temperature, sp.top_p, u[0], sm);
+  const int normal = samp_draw<kSampThreads, kSampEPT>(z, key, c, zmax, sp.temperature, sp.top_p, u[0], sm);
   // [P2] "Two autoregressions": a second draw at temperature 1.0, top-p 0.9,
   // used when the normal draw repeats a semantic token of the last 10 frames.
-  const int ras = samp_draw(sc, c, sp.ras_temperature, sp.ras_top_p, u[1], sm);
+  const int ras = samp_draw<kSampThreads, kSampEPT>(z, key, c, zmax, sp.ras_temperature, sp.ras_top_p,
+                                                   u[1], sm);
   if (tid == 0) {
     const int hn = d.hist_n[slot];
     const int w = min(sp.ras_win, hn);
@@ -1222,8 +1073,7 @@ __global__ void __launch_bounds__(kSampThreads)
     sample_fast_kernel(DevPtrs d, int k, const float* uniforms, int ldu, SamplingParams sp,
                        const int32_t* forced, int ldf, int32_t* codes_out, float* fast_logits_out,
                        int32_t* draws_out, const uint16_t* fast_emb) {
-  extern __shared__ __align__(16) unsigned char samp_smem_raw[];
-  SampSmem& sm = *reinterpret_cast<SampSmem*>(samp_smem_raw);
+  __shared__ SampSmem<kSampThreads> sm;
   __shared__ int s_commit;
   const int row = blockIdx.x, tid = threadIdx.x;
   const int N = d.N, Cf = d.Cf;
@@ -1232,10 +1082,12 @@ __global__ void __launch_bounds__(kSampThreads)
     for (int i = tid; i < Cf; i += kSampThreads)
       fast_logits_out[(static_cast<size_t>(row) * (N - 1) + (k - 1)) * Cf + i] = zs[i];
   if (!d.rows[row].active) return;
-  const Cands c{Cf, 0, 0, -1};
-  const SortedCands sc = samp_sort(zs, c, sm);
+  const Cands c{Cf, Cf, 0, -1};
+  float z[kSampEPT];
+  unsigned long long key[kSampEPT];
+  const float zmax = samp_load<kSampThreads, kSampEPT>(zs, c, z, key, sm);
   const float* u = uniforms + static_cast<size_t>(row) * ldu;
-  const int draw = samp_draw(sc, c, sp.temperature, sp.top_p, u[k + 1], sm);
+  const int draw = samp_draw<kSampThreads, kSampEPT>(z, key, c, zmax, sp.temperature, sp.top_p, u[k + 1], sm);
   if (tid == 0) {
     int commit = forced ? forced[static_cast<size_t>(row) * ldf + k] : draw;
     if (commit < 0 || commit >= Cf) {
@@ -1256,26 +1108,12 @@ __global__ void __launch_bounds__(kSampThreads)
   }
 }
 
-static cudaError_t samp_configure() {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(sample_q0_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(sizeof(SampSmem)));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sample_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(SampSmem)));
-  if (e == cudaSuccess) done = true;
-  return e;
-}
-
 cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms, int ldu,
                              const SamplingParams& sp, const int32_t* forced, int ldf,
                              int32_t* codes_out, int32_t* status_out, float* slow_logits_out,
                              int32_t* draws_out, const uint16_t* fast_emb, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  cudaError_t e = samp_configure();
-  if (e != cudaSuccess) return e;
-  sample_q0_kernel<<<nrows, kSampThreads, sizeof(SampSmem), st>>>(
+  sample_q0_kernel<<<nrows, kSampThreads, 0, st>>>(
       d, uniforms, ldu, sp, forced, ldf, codes_out, status_out, slow_logits_out, draws_out, fast_emb);
   return cudaGetLastError();
 }
@@ -1285,9 +1123,7 @@ cudaError_t launch_sample_fast(const DevPtrs& d, int nrows, int k, const float* 
                                int32_t* codes_out, float* fast_logits_out, int32_t* draws_out,
                                const uint16_t* fast_emb, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  cudaError_t e = samp_configure();
-  if (e != cudaSuccess) return e;
-  sample_fast_kernel<<<nrows, kSampThreads, sizeof(SampSmem), st>>>(
+  sample_fast_kernel<<<nrows, kSampThreads, 0, st>>>(
       d, k, uniforms, ldu, sp, forced, ldf, codes_out, fast_logits_out, draws_out, fast_emb);
   return cudaGetLastError();
 }
