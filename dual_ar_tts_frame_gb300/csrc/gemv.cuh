@@ -3,16 +3,18 @@
 //
 //   y[b][n] = sum_k W[n][k] x'[b][k],   x' = RMSNorm(x) * g   (optional)
 //
-// Each CTA owns a contiguous range of output rows (balanced to +-1 row) and
-// walks it in groups of kRowsPerGroup rows, one row per consumer warp.  K is
-// cut into chunks; a ring stage holds one (group, chunk) tile -- up to 16
-// row-chunks per matrix (two matrices for the SwiGLU gate/up pair), each
-// fetched by one bulk copy (cp.async.bulk) into shared memory.  A warp
-// accumulates its row over the chunks and reduces with shuffles only, so
-// consumer warps never synchronise with each other while streaming.  One
-// producer thread runs ahead by the ring depth; in the persistent kernel it
-// keeps streaming the next GEMV's weights while the consumers are still busy
-// with other work, since weights never depend on activations.
+// Each CTA owns a contiguous range of output rows (balanced to +-1 row).  A
+// ring stage holds one tile: R consecutive rows of one matrix, which are
+// contiguous in memory, fetched by ONE bulk copy (cp.async.bulk) of up to
+// 40 KB (R is a power of two with R*K*2 <= 40 KB).  The consumer warps split
+// the tile: S = warps / R warps per row, each taking a contiguous segment of
+// K, lane-strided 16-byte vectors.  A warp reduces its segment with shuffles,
+// stores the partial, and the last warp of the row to finish (shared-memory
+// counter) adds the S partials in segment order -- deterministic, and no
+// CTA-wide synchronisation while streaming.  The SwiGLU gate and up rows are
+// two consecutive tiles.  One producer thread runs ahead by the ring depth;
+// in the persistent kernel it keeps streaming the next GEMV's weights while
+// the consumers are still busy, since weights never depend on activations.
 #pragma once
 
 #include "common.cuh"
@@ -20,36 +22,78 @@
 
 namespace dualar {
 
-constexpr int kRowsPerGroup = kGemvConsumerWarps;   // one row per consumer warp
-constexpr int kStageBytes = 40960;                  // one ring stage
-constexpr int kMaxVecPerLane = 5;                   // 16-byte weight vectors per lane per row-chunk
+constexpr int kWarpsC = kGemvConsumerWarps;   // consumer warps (power of two)
+constexpr int kStageBytes = 40960;            // one ring stage
+constexpr int kMaxStagesRing = 8;
+constexpr int kMaxVecPerLane = 5;             // 16-byte vectors per lane per tile (unrolled)
 
-// Chunk length (elements) of one row-chunk: a tile of kRowsPerGroup rows x
-// nmat matrices x kc elements fits one stage, and kc/8 vectors spread over
-// 32 lanes give at most kMaxVecPerLane vectors per lane.
-__host__ __device__ inline int gemv_kc(int K, int nmat, int* n_chunks) {
-  const int kmax = kStageBytes / (kRowsPerGroup * nmat * 2);   // 1280 or 640
-  const int n = (K + kmax - 1) / kmax;
-  if (n_chunks) *n_chunks = n;
-  return ((K + n - 1) / n + 7) & ~7;
+// Rows per tile for K (power of two, <= kWarpsC).
+__host__ __device__ inline int gemv_rows_per_tile(int K) {
+  int r = kWarpsC;
+  while (r > 1 && r * K * 2 > kStageBytes) r >>= 1;
+  return r;
+}
+
+// Whether a K fits the unrolled inner loop (vectors per lane per tile).
+__host__ __device__ inline bool gemv_k_supported(int K) {
+  const int R = gemv_rows_per_tile(K);
+  if (R * K * 2 > kStageBytes) return false;
+  const int S = kWarpsC / R;
+  const int seg = (K / 8 + S - 1) / S;
+  return (seg + 31) / 32 <= kMaxVecPerLane;
 }
 
 struct GemvGeo {
-  int v_begin, v_end;   // rows of this CTA
-  int n_groups, n_chunks, kc, nmat, n_tiles;
+  int v_begin, v_end;   // rows of this CTA (virtual row space)
+  int R, S, seg;        // rows per tile, warps per row, vectors per segment
+  bool swiglu;
 };
 
 DEVI GemvGeo gemv_geo(const GemvArgs& a, int cta, int ncta) {
   GemvGeo g;
-  const bool swiglu = a.mode == GEMV_SWIGLU;
-  g.nmat = swiglu ? 2 : 1;
-  const int nv = swiglu ? a.n0 : a.n0 + a.n1;
+  g.swiglu = a.mode == GEMV_SWIGLU;
+  const int nv = g.swiglu ? a.n0 : a.n0 + a.n1;
   g.v_begin = static_cast<int>((static_cast<long long>(cta) * nv) / ncta);
   g.v_end = static_cast<int>((static_cast<long long>(cta + 1) * nv) / ncta);
-  g.n_groups = (g.v_end - g.v_begin + kRowsPerGroup - 1) / kRowsPerGroup;
-  g.kc = gemv_kc(a.K, g.nmat, &g.n_chunks);
-  g.n_tiles = g.n_groups * g.n_chunks;
+  g.R = gemv_rows_per_tile(a.K);
+  g.S = kWarpsC / g.R;
+  g.seg = (a.K / 8 + g.S - 1) / g.S;
   return g;
+}
+
+// Tile sequence of one CTA: R-row tiles that never cross a segment boundary
+// (restricted head: semantic block, then the <|im_end|> row); a SwiGLU tile
+// is two loads (gate rows, then up rows).
+struct TileIter {
+  int v, v_end, n0, n1, R;
+  bool swiglu;
+  int sub;
+  __device__ TileIter(const GemvArgs& a, const GemvGeo& g)
+      : v(g.v_begin), v_end(g.v_end), n0(a.n0), n1(a.n1), R(g.R), swiglu(g.swiglu), sub(0) {}
+  // row0, rows: rows of the tile; part: 0 gate / 1 up (SwiGLU)
+  __device__ bool next(int& row0, int& rows, int& part) {
+    if (v >= v_end) return false;
+    if (swiglu) {
+      rows = min(R, v_end - v);
+      row0 = v;
+      part = sub;
+      if (sub == 1) v += rows;
+      sub ^= 1;
+      return true;
+    }
+    const int seg_end = v < n0 ? n0 : n0 + n1;
+    rows = min(R, min(v_end, seg_end) - v);
+    row0 = v;
+    part = 0;
+    v += rows;
+    return true;
+  }
+};
+
+DEVI const uint16_t* gemv_tile_src(const GemvArgs& a, int row0, int part) {
+  if (a.mode == GEMV_SWIGLU) return (part ? a.w1 : a.w0) + static_cast<size_t>(row0) * a.K;
+  return row0 < a.n0 ? a.w0 + static_cast<size_t>(row0) * a.K
+                     : a.w1 + static_cast<size_t>(row0 - a.n0) * a.K;
 }
 
 struct GemvRing {
@@ -59,13 +103,23 @@ struct GemvRing {
   int stages;
 };
 
+// Shared scratch of the consumers: per-warp partials, per-row arrival
+// counters (one set per stage) and the SwiGLU gate outputs.
+template <int NB>
+struct GemvScratch {
+  float part[kMaxStagesRing][kWarpsC][NB];
+  int cnt[kMaxStagesRing][kWarpsC];
+  float gate[kWarpsC][NB];
+};
+
 // Producer side: issues the tiles of one GEMV for this CTA.  t is the ring's
-// running tile counter (shared convention with the consumers).  Returns false
-// if a wait gave up or the error word is set (then nothing more is issued).
+// running tile counter (same convention as the consumers).  Returns false if
+// a wait gave up or the abort word is set (then nothing more is issued).
 DEVI bool gemv_produce(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
                        uint64_t pol, const volatile uint32_t* abort_word) {
-  const size_t slot_bytes = static_cast<size_t>(g.kc) * 2;
-  for (int i = 0; i < g.n_tiles; ++i, ++t) {
+  TileIter it(a, g);
+  int row0, rows, part;
+  while (it.next(row0, rows, part)) {
     const int s = static_cast<int>(t % ring.stages);
     if (t >= static_cast<uint32_t>(ring.stages)) {
       const uint32_t parity = ((t / ring.stages) - 1) & 1;
@@ -79,24 +133,11 @@ DEVI bool gemv_produce(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
         }
       }
     }
-    const int grp = i / g.n_chunks, c = i % g.n_chunks;
-    const int v0 = g.v_begin + grp * kRowsPerGroup;
-    const int rows = min(kRowsPerGroup, g.v_end - v0);
-    const int k0 = c * g.kc;
-    const int len = min(g.kc, a.K - k0);
-    const uint32_t bytes = static_cast<uint32_t>(len) * 2;
-    mbar_arrive_expect_tx(&ring.full[s], bytes * rows * g.nmat);
-    unsigned char* st = ring.base + static_cast<size_t>(s) * kStageBytes;
-    for (int m = 0; m < g.nmat; ++m) {
-      for (int w = 0; w < rows; ++w) {
-        const int v = v0 + w;
-        const uint16_t* rowp;
-        if (g.nmat == 2) rowp = (m ? a.w1 : a.w0) + static_cast<size_t>(v) * a.K;
-        else rowp = v < a.n0 ? a.w0 + static_cast<size_t>(v) * a.K
-                             : a.w1 + static_cast<size_t>(v - a.n0) * a.K;
-        bulk_load_g2s(st + (m * kRowsPerGroup + w) * slot_bytes, rowp + k0, bytes, &ring.full[s], pol);
-      }
-    }
+    const uint32_t bytes = static_cast<uint32_t>(rows) * a.K * 2;
+    mbar_arrive_expect_tx(&ring.full[s], bytes);
+    bulk_load_g2s(ring.base + static_cast<size_t>(s) * kStageBytes, gemv_tile_src(a, row0, part), bytes,
+                  &ring.full[s], pol);
+    ++t;
   }
   return true;
 }
@@ -115,14 +156,16 @@ DEVI void gemv_drain(const GemvRing& ring, uint32_t t, uint64_t limit_ns) {
   }
 }
 
-// Consumer prologue: x rows into shared memory in a split layout (xa holds
-// elements 8j..8j+3, xb elements 8j+4..8j+7, so a warp's 16-byte reads are
-// conflict-free), RMSNorm applied if requested.  Uses named barrier 1 over the
-// consumer threads.  `red` needs 16 * NB floats, `scale` NB floats.
+// Consumer prologue: x rows into shared memory in a split layout (for each
+// 8-element vector j, elements 0..3 at xa[j], 4..7 at xb[j], so a warp's
+// 16-byte reads are conflict-free), RMSNorm applied if requested.  Uses
+// named barrier 1 over the consumer threads.  `red` holds kWarpsC * NB
+// floats, `scale` NB floats.  coherent: read x through L2 (data written by
+// other CTAs of the same grid).
 template <int NB>
 DEVI void gemv_stage_x(const GemvArgs& a, float* xs, float* red, float* scale, int cta,
                        bool coherent) {
-  constexpr int NCT = kGemvConsumerWarps * 32;
+  constexpr int NCT = kWarpsC * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, KV = K >> 3;
   float ss[NB];
@@ -154,7 +197,7 @@ DEVI void gemv_stage_x(const GemvArgs& a, float* xs, float* red, float* scale, i
     named_barrier(1, NCT);
     if (tid < NB) {
       float t = 0.f;
-      for (int w = 0; w < kGemvConsumerWarps; ++w) t += red[w * NB + tid];
+      for (int w = 0; w < kWarpsC; ++w) t += red[w * NB + tid];
       scale[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
     }
     named_barrier(1, NCT);
@@ -184,76 +227,99 @@ DEVI void gemv_stage_x(const GemvArgs& a, float* xs, float* red, float* scale, i
   }
 }
 
-// Consumer side: consumes the tiles of one GEMV, writes the epilogue.
+template <int NB>
+DEVI void gemv_epilogue(const GemvArgs& a, int n, int b, float y, float g) {
+  if (b >= a.nb) return;
+  const int orow = a.out_map ? a.out_map[b] : b;
+  if (orow < 0) return;
+  float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
+  if (a.mode == GEMV_STORE) *o = y;
+  else if (a.mode == GEMV_ADD) *o = __ldcg(a.base + static_cast<size_t>(orow) * a.ldb + n) + y;
+  // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
+  else *o = silu(g) * y;
+}
+
+// Consumer side: consumes the tiles of one GEMV and writes the epilogue.
 // Returns false if a wait gave up.
 template <int NB>
 DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
-                       const float* xs) {
+                       const float* xs, GemvScratch<NB>& sc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV = K >> 3;
-  const size_t slot_bytes = static_cast<size_t>(g.kc) * 2;
-  float acc[2][NB];
-  for (int i = 0; i < g.n_tiles; ++i, ++t) {
+  const int r = warp / g.S, sg = warp % g.S;
+  const int j0 = sg * g.seg;
+  const int nvec = max(0, min(g.seg, KV - j0));
+  TileIter it(a, g);
+  int row0, rows, part;
+  while (it.next(row0, rows, part)) {
     const int s = static_cast<int>(t % ring.stages);
-    const int grp = i / g.n_chunks, c = i % g.n_chunks;
-    const int v0 = g.v_begin + grp * kRowsPerGroup;
-    const int rows = min(kRowsPerGroup, g.v_end - v0);
-    if (c == 0) {
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int b = 0; b < NB; ++b) acc[m][b] = 0.f;
-    }
     if (!mbar_wait(&ring.full[s], (t / ring.stages) & 1, a.err, a.wait_limit_ns)) return false;
-    if (warp < rows) {
-      const int j0 = (c * g.kc) >> 3;                 // first vector of this chunk
-      const int nvec = min(g.kc, K - c * g.kc) >> 3;
-      const unsigned char* st = ring.base + static_cast<size_t>(s) * kStageBytes;
-      for (int m = 0; m < g.nmat; ++m) {
-        const uint4* wr = reinterpret_cast<const uint4*>(st + (m * kRowsPerGroup + warp) * slot_bytes);
-        uint4 w[kMaxVecPerLane];
+    if (r < rows) {
+      const uint4* wr = reinterpret_cast<const uint4*>(ring.base + static_cast<size_t>(s) * kStageBytes) +
+                        static_cast<size_t>(r) * KV + j0;
+      uint4 w[kMaxVecPerLane];
+#pragma unroll
+      for (int q = 0; q < kMaxVecPerLane; ++q) {
+        const int j = lane + 32 * q;
+        if (j < nvec) w[q] = wr[j];
+      }
+      float p[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const float4* xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K) + j0;
+        const float4* xb = xa + KV;
+        float acc = 0.f;
 #pragma unroll
         for (int q = 0; q < kMaxVecPerLane; ++q) {
           const int j = lane + 32 * q;
-          if (j < nvec) w[q] = wr[j];
+          if (j < nvec) acc = dot8(w[q], xa[j], xb[j], acc);
         }
+        p[b] = warp_sum(acc);
+      }
+      const int n = row0 + r;
+      if (g.S == 1) {
+        if (lane < NB) {
+          float y = p[0];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float4* xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K);
-          const float4* xb = xa + KV;
-          float p = 0.f;
+          for (int b = 1; b < NB; ++b)
+            if (lane == b) y = p[b];
+          if (g.swiglu && part == 0) sc.gate[warp][lane] = y;
+          else gemv_epilogue<NB>(a, n, lane, y, g.swiglu ? sc.gate[warp][lane] : 0.f);
+        }
+      } else {
+        if (lane < NB) {
+          float y = p[0];
 #pragma unroll
-          for (int q = 0; q < kMaxVecPerLane; ++q) {
-            const int j = lane + 32 * q;
-            if (j < nvec) p = dot8(w[q], xa[j0 + j], xb[j0 + j], p);
+          for (int b = 1; b < NB; ++b)
+            if (lane == b) y = p[b];
+          sc.part[s][warp][lane] = y;
+        }
+        __threadfence_block();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&sc.cnt[s][r], 1) == g.S - 1;
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (last) {
+          __threadfence_block();
+          if (lane < NB) {
+            float y = 0.f;
+            for (int q = 0; q < g.S; ++q) y += sc.part[s][r * g.S + q][lane];
+            if (g.swiglu && part == 0) sc.gate[r][lane] = y;
+            else gemv_epilogue<NB>(a, n, lane, y, g.swiglu ? sc.gate[r][lane] : 0.f);
           }
-          acc[m][b] += p;
+          if (lane == 0) sc.cnt[s][r] = 0;
+          __threadfence_block();
         }
       }
+      // release the stage only after this warp's partial/combine is done: the
+      // per-stage scratch is reused with the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ring.empty[s]);
-    if (c == g.n_chunks - 1 && warp < rows) {
-      const int n = v0 + warp;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        acc[0][b] = warp_sum(acc[0][b]);
-        if (g.nmat == 2) acc[1][b] = warp_sum(acc[1][b]);
-      }
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (lane == b && b < a.nb) {
-          const int orow = a.out_map ? a.out_map[b] : b;
-          if (orow >= 0) {
-            float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
-            if (a.mode == GEMV_STORE) *o = acc[0][b];
-            else if (a.mode == GEMV_ADD) *o = __ldcg(a.base + static_cast<size_t>(orow) * a.ldb + n) + acc[0][b];
-            // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
-            else *o = silu(acc[0][b]) * acc[1][b];
-          }
-        }
-      }
-    }
+    ++t;
   }
   return true;
 }

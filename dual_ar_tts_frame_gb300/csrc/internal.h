@@ -12,7 +12,10 @@ constexpr int kMaxCodebooks = 16;
 constexpr int kRasRing = 16;         // RAS history ring per slot (window <= 16)
 constexpr int kMaxChunks = 64;       // split-KV chunks per (row, KV head)
 constexpr int kMaxGroup = 8;         // query heads per KV head
-constexpr int kGemvConsumerWarps = 16;
+#ifndef DUALAR_GEMV_WARPS
+#define DUALAR_GEMV_WARPS 16
+#endif
+constexpr int kGemvConsumerWarps = DUALAR_GEMV_WARPS;
 constexpr int kGemvThreads = (kGemvConsumerWarps + 1) * 32;
 constexpr int kSampThreads = 512;
 

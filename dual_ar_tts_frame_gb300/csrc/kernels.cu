@@ -72,12 +72,13 @@ cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t*
 // ============================================================================
 // GEMV (standalone launch; device code in gemv.cuh)
 // ============================================================================
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = kMaxStagesRing;
 constexpr int kSmemBudget = 225 * 1024;   // dynamic shared memory per CTA
 
-// Shared-memory layout of gemv_kernel (offsets in bytes).
-__host__ __device__ inline size_t gemv_misc_off() { return 256; }
-__host__ __device__ inline size_t gemv_xs_off() { return 1024; }
+// Shared-memory layout of gemv_kernel (offsets in bytes): mbarriers, the
+// consumers' scratch, x rows, then the ring.
+__host__ __device__ inline size_t gemv_scratch_off() { return 256; }
+__host__ __device__ inline size_t gemv_xs_off() { return 256 + sizeof(GemvScratch<8>) + 4 * 160; }
 __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
   return (gemv_xs_off() + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
 }
@@ -87,10 +88,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   extern __shared__ __align__(128) unsigned char smem[];
   GemvRing ring;
   ring.full = reinterpret_cast<uint64_t*>(smem);
-  ring.empty = ring.full + kMaxStages;
+  ring.empty = ring.full + kMaxStagesRing;
   ring.base = smem + gemv_ring_off(NB, a.K);
   ring.stages = stages;
-  float* misc = reinterpret_cast<float*>(smem + gemv_misc_off());
+  GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + gemv_scratch_off());
+  float* misc = reinterpret_cast<float*>(smem + gemv_scratch_off() + sizeof(GemvScratch<8>));
   float* xs = reinterpret_cast<float*>(smem + gemv_xs_off());
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  for (int i = tid; i < kMaxStagesRing * kWarpsC; i += blockDim.x) (&scr.cnt[0][0])[i] = 0;
   __syncthreads();
   const GemvGeo g = gemv_geo(a, blockIdx.x, gridDim.x);
   uint32_t t = 0;
@@ -111,8 +114,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
     }
     return;
   }
-  gemv_stage_x<NB>(a, xs, misc, misc + 16 * 8, blockIdx.x, false);
-  gemv_consume<NB>(a, g, ring, t, xs);
+  gemv_stage_x<NB>(a, xs, misc, misc + kWarpsC * 8, blockIdx.x, false);
+  gemv_consume<NB>(a, g, ring, t, xs, scr);
 }
 
 struct GemvPlan {
@@ -153,7 +156,7 @@ static cudaError_t launch_gemv_nb(const GemvArgs& a, const GemvPlan& p, int grid
 
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
   if (a.nb <= 0) return cudaSuccess;
-  if (a.K % 8 != 0) return cudaErrorInvalidValue;
+  if (a.K % 8 != 0 || !gemv_k_supported(a.K)) return cudaErrorInvalidValue;
   const GemvPlan p = plan_gemv(a.K, a.nb);
   if (p.stages < 1 || p.smem > static_cast<size_t>(kSmemBudget)) return cudaErrorInvalidValue;
   const int nv = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
