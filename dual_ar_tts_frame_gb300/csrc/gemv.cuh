@@ -156,61 +156,91 @@ DEVI void gemv_drain(const GemvRing& ring, uint32_t t, uint64_t limit_ns) {
   }
 }
 
-// Consumer prologue: x rows into shared memory in a split layout (for each
-// 8-element vector j, elements 0..3 at xa[j], 4..7 at xb[j], so a warp's
-// 16-byte reads are conflict-free), RMSNorm applied if requested.  Uses
-// named barrier 1 over the consumer threads.  `red` holds kWarpsC * NB
-// floats, `scale` NB floats.  coherent: read x through L2 (data written by
-// other CTAs of the same grid).
+// Consumer prologue.  Stages x' = x * g (g the RMSNorm gain, 1 without norm)
+// in shared memory in a split layout (for each 8-element vector j, elements
+// 0..3 at xa[j], 4..7 at xb[j], so a warp's 16-byte reads are
+// conflict-free), and the RMSNorm scale s = 1/sqrt(mean(x^2) + eps) per row
+// b, so that W (s x*g) = s (W x') is applied in the epilogue.  x and g are
+// loaded in one pass (independent loads).  Also prefetches the residual base
+// values of this CTA's rows and the output row map.  Uses named barrier 1
+// over the consumer threads.  coherent: read x and base through L2 (data
+// written by other CTAs of the same grid).
+constexpr int kBaseRows = 64;   // residual rows prefetched per CTA
+
 template <int NB>
-DEVI void gemv_stage_x(const GemvArgs& a, float* xs, float* red, float* scale, int cta,
+struct GemvPro {
+  float red[kWarpsC][NB];
+  float scale[NB];
+  int orow[NB];
+  float base[kBaseRows][NB];
+};
+
+template <int NB>
+DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<NB>& pr, int cta,
                        bool coherent) {
   constexpr int NCT = kWarpsC * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, KV = K >> 3;
+  const bool norm = a.norm_w != nullptr;
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
+  for (int j = tid; j < KV; j += NCT) {
+    float gw[8];
+    if (norm) {
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.norm_w + 8 * j);
+      gw[0] = bf16lo(gv.x); gw[1] = bf16hi(gv.x); gw[2] = bf16lo(gv.y); gw[3] = bf16hi(gv.y);
+      gw[4] = bf16lo(gv.z); gw[5] = bf16hi(gv.z); gw[6] = bf16lo(gv.w); gw[7] = bf16hi(gv.w);
+    } else {
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    if (b < a.nb) {
-      const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
-      float4* xa = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
-      float4* xb = xa + KV;
-      for (int j = tid; j < KV; j += NCT) {
+      for (int e = 0; e < 8; ++e) gw[e] = 1.f;
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (b < a.nb) {
+        const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
         const float4 v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
         const float4 v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
-        xa[j] = v0;
-        xb[j] = v1;
+        float4* xa = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
+        xa[j] = make_float4(v0.x * gw[0], v0.y * gw[1], v0.z * gw[2], v0.w * gw[3]);
+        xa[KV + j] = make_float4(v1.x * gw[4], v1.y * gw[5], v1.z * gw[6], v1.w * gw[7]);
         ss[b] += v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w + v1.x * v1.x + v1.y * v1.y +
                  v1.z * v1.z + v1.w * v1.w;
       }
     }
   }
-  if (a.norm_w != nullptr) {
+  // residual base rows and output row map, fetched once
+  const int nrows = g.v_end - g.v_begin;
+  if (a.mode == GEMV_ADD && nrows <= kBaseRows) {
+    for (int e = tid; e < nrows * NB; e += NCT) {
+      const int rr = e / NB, b = e % NB;
+      if (b < a.nb) {
+        const int orow = a.out_map ? a.out_map[b] : b;
+        if (orow >= 0) {
+          const float* bp = a.base + static_cast<size_t>(orow) * a.ldb + g.v_begin + rr;
+          pr.base[rr][b] = coherent ? __ldcg(bp) : *bp;
+        }
+      }
+    }
+  }
+  if (tid < NB) pr.orow[tid] = tid < a.nb ? (a.out_map ? a.out_map[tid] : tid) : -1;
+  if (norm) {
     // [P1] "Fast Transformer": RMSNorm(dim, eps=norm_eps), pre-norm blocks.
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const float w = warp_sum(ss[b]);
-      if (lane == 0) red[warp * NB + b] = w;
+      if (lane == 0) pr.red[warp][b] = w;
     }
-    named_barrier(1, NCT);
-    if (tid < NB) {
+  }
+  named_barrier(1, NCT);
+  if (tid < NB) {
+    float sc = 1.f;
+    if (norm) {
       float t = 0.f;
-      for (int w = 0; w < kWarpsC; ++w) t += red[w * NB + tid];
-      scale[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
+      for (int w = 0; w < kWarpsC; ++w) t += pr.red[w][tid];
+      sc = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
     }
-    named_barrier(1, NCT);
-    for (int b = 0; b < a.nb; ++b) {
-      const float sc = scale[b];
-      float* xa = xs + static_cast<size_t>(b) * K;
-      float* xb = xa + 4 * KV;
-      for (int k = tid; k < K; k += NCT) {
-        const int j = k >> 3, e = k & 7;
-        float* p = e < 4 ? xa + 4 * j + e : xb + 4 * j + (e - 4);
-        *p = (*p * sc) * bf16bits_to_f32(a.norm_w[k]);
-      }
-    }
+    pr.scale[tid] = sc;
   }
   named_barrier(1, NCT);
   if (a.save_x != nullptr && cta == 0) {
@@ -219,31 +249,42 @@ DEVI void gemv_stage_x(const GemvArgs& a, float* xs, float* red, float* scale, i
       if (row < 0) continue;
       const float* xa = xs + static_cast<size_t>(b) * K;
       const float* xb = xa + 4 * KV;
+      const float sc = pr.scale[b];
       for (int k = tid; k < K; k += NCT) {
         const int j = k >> 3, e = k & 7;
-        a.save_x[static_cast<size_t>(row) * a.lds + k] = e < 4 ? xa[4 * j + e] : xb[4 * j + e - 4];
+        a.save_x[static_cast<size_t>(row) * a.lds + k] = sc * (e < 4 ? xa[4 * j + e] : xb[4 * j + e - 4]);
       }
     }
   }
 }
 
 template <int NB>
-DEVI void gemv_epilogue(const GemvArgs& a, int n, int b, float y, float g) {
+DEVI void gemv_epilogue(const GemvArgs& a, const GemvGeo& g, const GemvPro<NB>& pr, int n, int b,
+                        float y, float gate) {
   if (b >= a.nb) return;
-  const int orow = a.out_map ? a.out_map[b] : b;
+  const int orow = pr.orow[b];
   if (orow < 0) return;
   float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
-  if (a.mode == GEMV_STORE) *o = y;
-  else if (a.mode == GEMV_ADD) *o = __ldcg(a.base + static_cast<size_t>(orow) * a.ldb + n) + y;
-  // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
-  else *o = silu(g) * y;
+  y *= pr.scale[b];
+  if (a.mode == GEMV_STORE) {
+    *o = y;
+  } else if (a.mode == GEMV_ADD) {
+    const int rr = n - g.v_begin;
+    const float base = (g.v_end - g.v_begin <= kBaseRows)
+                           ? pr.base[rr][b]
+                           : __ldcg(a.base + static_cast<size_t>(orow) * a.ldb + n);
+    *o = base + y;
+  } else {
+    // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
+    *o = silu(gate * pr.scale[b]) * y;
+  }
 }
 
 // Consumer side: consumes the tiles of one GEMV and writes the epilogue.
 // Returns false if a wait gave up.
 template <int NB>
 DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
-                       const float* xs, GemvScratch<NB>& sc) {
+                       const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV = K >> 3;
   const int r = warp / g.S, sg = warp % g.S;
@@ -284,7 +325,7 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
           for (int b = 1; b < NB; ++b)
             if (lane == b) y = p[b];
           if (g.swiglu && part == 0) sc.gate[warp][lane] = y;
-          else gemv_epilogue<NB>(a, n, lane, y, g.swiglu ? sc.gate[warp][lane] : 0.f);
+          else gemv_epilogue<NB>(a, g, pr, n, lane, y, g.swiglu ? sc.gate[warp][lane] : 0.f);
         }
       } else {
         if (lane < NB) {
@@ -305,7 +346,7 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
             float y = 0.f;
             for (int q = 0; q < g.S; ++q) y += sc.part[s][r * g.S + q][lane];
             if (g.swiglu && part == 0) sc.gate[r][lane] = y;
-            else gemv_epilogue<NB>(a, n, lane, y, g.swiglu ? sc.gate[r][lane] : 0.f);
+            else gemv_epilogue<NB>(a, g, pr, n, lane, y, g.swiglu ? sc.gate[r][lane] : 0.f);
           }
           if (lane == 0) sc.cnt[s][r] = 0;
           __threadfence_block();

@@ -78,7 +78,9 @@ constexpr int kSmemBudget = 225 * 1024;   // dynamic shared memory per CTA
 // Shared-memory layout of gemv_kernel (offsets in bytes): mbarriers, the
 // consumers' scratch, x rows, then the ring.
 __host__ __device__ inline size_t gemv_scratch_off() { return 256; }
-__host__ __device__ inline size_t gemv_xs_off() { return 256 + sizeof(GemvScratch<8>) + 4 * 160; }
+__host__ __device__ inline size_t gemv_xs_off() {
+  return (256 + sizeof(GemvScratch<8>) + sizeof(GemvPro<8>) + 127) & ~size_t(127);
+}
 __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
   return (gemv_xs_off() + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
 }
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   ring.base = smem + gemv_ring_off(NB, a.K);
   ring.stages = stages;
   GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + gemv_scratch_off());
-  float* misc = reinterpret_cast<float*>(smem + gemv_scratch_off() + sizeof(GemvScratch<8>));
+  GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + gemv_scratch_off() + sizeof(GemvScratch<8>));
   float* xs = reinterpret_cast<float*>(smem + gemv_xs_off());
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -114,8 +116,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
     }
     return;
   }
-  gemv_stage_x<NB>(a, xs, misc, misc + kWarpsC * 8, blockIdx.x, false);
-  gemv_consume<NB>(a, g, ring, t, xs, scr);
+  gemv_stage_x<NB>(a, g, xs, pro, blockIdx.x, false);
+  gemv_consume<NB>(a, g, ring, t, xs, scr, pro);
 }
 
 struct GemvPlan {
