@@ -24,7 +24,8 @@ EXPORTED = [
     "dualar_create", "dualar_prefill", "dualar_decode_frame", "dualar_decode_frame_forced",
     "dualar_release", "dualar_sync", "dualar_get_error", "dualar_destroy",
     "dualar_get_page_table", "dualar_get_rope_table", "dualar_read_state", "dualar_slot_length",
-    "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_profile", "dualar_profile_read",
+    "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_set_persistent",
+    "dualar_debug_barrier_extra", "dualar_profile", "dualar_profile_read",
 ]
 
 c_i32 = ctypes.c_int32
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_set_wait_limit.argtypes = [H, ctypes.c_uint64]
     L.dualar_last_launch_count.argtypes = [H]
     L.dualar_last_launch_count.restype = c_i32
+    L.dualar_set_persistent.argtypes = [H, c_i32]
+    L.dualar_debug_barrier_extra.argtypes = [H, ctypes.c_uint32]
     L.dualar_profile.argtypes = [H, c_i32]
     L.dualar_profile_read.argtypes = [H, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]

@@ -14,6 +14,7 @@
 
 #include "dualar.h"
 #include "internal.h"
+#include "mega.h"
 
 using namespace dualar;
 
@@ -37,6 +38,13 @@ struct dualar_handle {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<double> prof_bytes;
+  // persistent frame kernel
+  bool use_mega = true;
+  uint32_t bar_extra = 0;
+  uint32_t* bar_counter = nullptr;
+  MegaOp* mega_ops[3] = {nullptr, nullptr, nullptr};   // programs for batch 1, 2
+  int mega_nops[3] = {0, 0, 0};
+  bool mega_unsupported[3] = {false, false, false};
 };
 
 namespace {
@@ -199,26 +207,120 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
 
 const uint16_t* U16(const void* p) { return static_cast<const uint16_t*>(p); }
 
+// GEMV arguments of the four projections of a block and of the heads.
+GemvArgs args_qkv(dualar_handle* h, const dualar_layer_weights& lw, int nrows, const float* xin) {
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(lw.wqkv);
+  a.n0 = h->d.qkv_dim;
+  a.K = h->cfg.dim;
+  a.mode = GEMV_STORE;
+  a.nb = nrows;
+  a.x = xin;
+  a.ldx = h->cfg.dim;
+  a.norm_w = U16(lw.attn_norm);
+  a.out = h->d.qkv;
+  a.ldo = h->d.qkv_dim;
+  return a;
+}
+
+GemvArgs args_o(dualar_handle* h, const dualar_layer_weights& lw, int nrows, const float* base, float* out) {
+  const int qd = h->cfg.n_head * h->cfg.head_dim;
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(lw.wo);
+  a.n0 = h->cfg.dim;
+  a.K = qd;
+  a.mode = GEMV_ADD;
+  a.nb = nrows;
+  a.x = h->d.attn;
+  a.ldx = qd;
+  a.base = base;
+  a.ldb = h->cfg.dim;
+  a.out = out;
+  a.ldo = h->cfg.dim;
+  return a;
+}
+
+GemvArgs args_gateup(dualar_handle* h, const dualar_layer_weights& lw, int nrows, const float* hres) {
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(lw.w_gate);
+  a.w1 = U16(lw.w_up);
+  a.n0 = h->cfg.ffn;
+  a.n1 = h->cfg.ffn;
+  a.K = h->cfg.dim;
+  a.mode = GEMV_SWIGLU;
+  a.nb = nrows;
+  a.x = hres;
+  a.ldx = h->cfg.dim;
+  a.norm_w = U16(lw.ffn_norm);
+  a.out = h->d.act;
+  a.ldo = h->cfg.ffn;
+  return a;
+}
+
+GemvArgs args_down(dualar_handle* h, const dualar_layer_weights& lw, int nrows, float* hres) {
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(lw.w_down);
+  a.n0 = h->cfg.dim;
+  a.K = h->cfg.ffn;
+  a.mode = GEMV_ADD;
+  a.nb = nrows;
+  a.x = h->d.act;
+  a.ldx = h->cfg.ffn;
+  a.base = hres;
+  a.ldb = h->cfg.dim;
+  a.out = hres;
+  a.ldo = h->cfg.dim;
+  return a;
+}
+
+GemvArgs args_fast_head(dualar_handle* h, int nrows) {
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(h->w.fast_out);
+  a.n0 = h->cfg.fast_vocab;
+  a.K = h->cfg.dim;
+  a.mode = GEMV_STORE;
+  a.nb = nrows;
+  a.x = h->d.hf;
+  a.ldx = h->cfg.dim;
+  a.norm_w = U16(h->w.fast_norm);
+  a.out = h->d.logits;
+  a.ldo = h->d.logit_ld;
+  return a;
+}
+
+// Final RMSNorm + restricted head for rows [r0, r0 + n): commits the normed
+// hidden state and the logits of rows whose commit_map entry is a slot.
+// [P2] "Two autoregressions" (bias keeps semantic ids + <|im_end|>) and "The
+// slow AR is Qwen3-4B" (tied head): only those 4,097 rows are computed.
+GemvArgs args_head(dualar_handle* h, int r0, int n) {
+  const dualar_config& c = h->cfg;
+  GemvArgs a = gemv_base(h);
+  a.w0 = U16(h->w.tok_emb) + static_cast<size_t>(c.sem_begin) * c.dim;
+  a.n0 = c.n_sem;
+  a.w1 = U16(h->w.tok_emb) + static_cast<size_t>(c.im_end_id) * c.dim;
+  a.n1 = 1;
+  a.K = c.dim;
+  a.mode = GEMV_STORE;
+  a.nb = n;
+  a.x = h->d.hs + static_cast<size_t>(r0) * c.dim;
+  a.ldx = c.dim;
+  a.norm_w = U16(h->w.final_norm);
+  a.out = h->d.z_last;
+  a.ldo = c.n_sem + 1;
+  a.out_map = h->d.commit_map + r0;
+  a.save_x = h->d.h_last;
+  a.save_map = h->d.commit_map + r0;
+  a.lds = c.dim;
+  return a;
+}
+
 // One transformer block over nrows rows.  Slow blocks attend over the paged
 // cache; fast blocks over the per-frame codebook cache.
 int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast, int nrows,
           const float* xin, float* hres, int fast_pos, int units, int chunk, bool fuse_append) {
   const dualar_config& c = h->cfg;
   const DevPtrs& d = h->d;
-  const int qd = c.n_head * c.head_dim;
-  // u = RMSNorm(x); qkv = Wqkv u
-  GemvArgs a = gemv_base(h);
-  a.w0 = U16(lw.wqkv);
-  a.n0 = d.qkv_dim;
-  a.K = c.dim;
-  a.mode = GEMV_STORE;
-  a.nb = nrows;
-  a.x = xin;
-  a.ldx = c.dim;
-  a.norm_w = U16(lw.attn_norm);
-  a.out = d.qkv;
-  a.ldo = d.qkv_dim;
-  TRY(run_gemv(h, a));
+  TRY(run_gemv(h, args_qkv(h, lw, nrows, xin)));
   const bool qk = fast ? c.fast_qk_norm : c.slow_qk_norm;
   const uint16_t* qn = qk ? U16(lw.q_norm) : nullptr;
   const uint16_t* kn = qk ? U16(lw.k_norm) : nullptr;
@@ -230,49 +332,69 @@ int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast
     LAUNCH(h, launch_append(d, nrows, layer, false, 0, qn, kn, h->stream));
     LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, false, nullptr, nullptr, h->stream));
   }
-  // h = x + Wo attn
-  a = gemv_base(h);
-  a.w0 = U16(lw.wo);
-  a.n0 = c.dim;
-  a.K = qd;
-  a.mode = GEMV_ADD;
-  a.nb = nrows;
-  a.x = d.attn;
-  a.ldx = qd;
-  a.base = xin;
-  a.ldb = c.dim;
-  a.out = hres;
-  a.ldo = c.dim;
-  TRY(run_gemv(h, a));
-  // act = SiLU(Wgate u) * (Wup u), u = RMSNorm(h)
-  a = gemv_base(h);
-  a.w0 = U16(lw.w_gate);
-  a.w1 = U16(lw.w_up);
-  a.n0 = c.ffn;
-  a.n1 = c.ffn;
-  a.K = c.dim;
-  a.mode = GEMV_SWIGLU;
-  a.nb = nrows;
-  a.x = hres;
-  a.ldx = c.dim;
-  a.norm_w = U16(lw.ffn_norm);
-  a.out = d.act;
-  a.ldo = c.ffn;
-  TRY(run_gemv(h, a));
-  // h += Wdown act
-  a = gemv_base(h);
-  a.w0 = U16(lw.w_down);
-  a.n0 = c.dim;
-  a.K = c.ffn;
-  a.mode = GEMV_ADD;
-  a.nb = nrows;
-  a.x = d.act;
-  a.ldx = c.ffn;
-  a.base = hres;
-  a.ldb = c.dim;
-  a.out = hres;
-  a.ldo = c.dim;
-  return run_gemv(h, a);
+  TRY(run_gemv(h, args_o(h, lw, nrows, xin, hres)));
+  TRY(run_gemv(h, args_gateup(h, lw, nrows, hres)));
+  return run_gemv(h, args_down(h, lw, nrows, hres));
+}
+
+// The frame program of the persistent kernel for batch nb (same op order as
+// the per-op path in decode_impl).
+int build_mega_program(dualar_handle* h, int nb) {
+  const dualar_config& c = h->cfg;
+  const DevPtrs& d = h->d;
+  std::vector<MegaOp> ops;
+  auto op = [&](int type, int layer, int pos) {
+    MegaOp o{};
+    o.type = type;
+    o.layer = layer;
+    o.pos = pos;
+    return o;
+  };
+  auto gemv = [&](const GemvArgs& a) {
+    MegaOp o = op(MOP_GEMV, 0, 0);
+    o.g = a;
+    ops.push_back(o);
+  };
+  ops.push_back(op(MOP_SAMPLE_Q0, 0, 0));
+  for (int p = 0; p < c.n_codebooks; ++p) {
+    const float* xin = d.fin + static_cast<size_t>(p & 1) * kMaxRows * c.dim;
+    for (int l = 0; l < c.fast_n_layer; ++l) {
+      const dualar_layer_weights& lw = h->fast[l];
+      const float* x = l == 0 ? xin : d.hf;
+      gemv(args_qkv(h, lw, nb, x));
+      MegaOp a = op(MOP_ATTN_FAST, l, p);
+      a.q_norm = c.fast_qk_norm ? U16(lw.q_norm) : nullptr;
+      a.k_norm = c.fast_qk_norm ? U16(lw.k_norm) : nullptr;
+      ops.push_back(a);
+      gemv(args_o(h, lw, nb, x, d.hf));
+      gemv(args_gateup(h, lw, nb, d.hf));
+      gemv(args_down(h, lw, nb, d.hf));
+    }
+    if (p == 0) continue;
+    gemv(args_fast_head(h, nb));
+    ops.push_back(op(MOP_SAMPLE_FAST, 0, p));
+  }
+  ops.push_back(op(MOP_FUSION, 0, 0));
+  for (int l = 0; l < c.n_layer; ++l) {
+    const dualar_layer_weights& lw = h->slow[l];
+    const float* x = l == 0 ? d.xs : d.hs;
+    gemv(args_qkv(h, lw, nb, x));
+    MegaOp a = op(MOP_ATTN_PAGED, l, 0);
+    a.q_norm = c.slow_qk_norm ? U16(lw.q_norm) : nullptr;
+    a.k_norm = c.slow_qk_norm ? U16(lw.k_norm) : nullptr;
+    ops.push_back(a);
+    gemv(args_o(h, lw, nb, x, d.hs));
+    gemv(args_gateup(h, lw, nb, d.hs));
+    gemv(args_down(h, lw, nb, d.hs));
+  }
+  gemv(args_head(h, 0, nb));
+  MegaOp* dev = nullptr;
+  CUDA_TRY(h, cudaMalloc(&dev, ops.size() * sizeof(MegaOp)));
+  h->allocs.push_back(dev);
+  CUDA_TRY(h, cudaMemcpy(dev, ops.data(), ops.size() * sizeof(MegaOp), cudaMemcpyHostToDevice));
+  h->mega_ops[nb] = dev;
+  h->mega_nops[nb] = static_cast<int>(ops.size());
+  return DUALAR_OK;
 }
 
 // Split-KV work list: chunk size and per-row first unit.
@@ -298,32 +420,6 @@ int slow_stack(dualar_handle* h, int nrows, int units, int chunk, bool decode) {
     TRY(block(h, h->slow[l], l, false, nrows, l == 0 ? h->d.xs : h->d.hs, h->d.hs, 0, units, chunk,
               decode));
   return DUALAR_OK;
-}
-
-// Final RMSNorm + restricted head for rows [r0, r0 + n): commits the normed
-// hidden state and the logits of rows whose commit_map entry is a slot.
-// [P2] "Two autoregressions" (bias keeps semantic ids + <|im_end|>) and "The
-// slow AR is Qwen3-4B" (tied head): only those 4,097 rows are computed.
-int restricted_head(dualar_handle* h, int r0, int n) {
-  const dualar_config& c = h->cfg;
-  GemvArgs a = gemv_base(h);
-  a.w0 = U16(h->w.tok_emb) + static_cast<size_t>(c.sem_begin) * c.dim;
-  a.n0 = c.n_sem;
-  a.w1 = U16(h->w.tok_emb) + static_cast<size_t>(c.im_end_id) * c.dim;
-  a.n1 = 1;
-  a.K = c.dim;
-  a.mode = GEMV_STORE;
-  a.nb = n;
-  a.x = h->d.hs + static_cast<size_t>(r0) * c.dim;
-  a.ldx = c.dim;
-  a.norm_w = U16(h->w.final_norm);
-  a.out = h->d.z_last;
-  a.ldo = c.n_sem + 1;
-  a.out_map = h->d.commit_map + r0;
-  a.save_x = h->d.h_last;
-  a.save_map = h->d.commit_map + r0;
-  a.lds = c.dim;
-  return run_gemv(h, a);
 }
 
 int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const float* uniforms,
@@ -395,6 +491,43 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
                     smp->ras_top_p, smp->allow_eos};
   const int N = c.n_codebooks;
   LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
+  if (h->use_mega && batch <= 2 && !h->mega_unsupported[batch]) {
+    if (!h->mega_ops[batch]) TRY(build_mega_program(h, batch));
+    MegaParams mp{};
+    mp.d = d;
+    mp.ops = h->mega_ops[batch];
+    mp.n_ops = h->mega_nops[batch];
+    mp.nrows = batch;
+    mp.units = units;
+    mp.chunk = chunk;
+    mp.kmax = std::max(std::max(c.dim, c.n_head * c.head_dim), c.ffn);
+    mp.io = SampIO{uniforms, N + 1, sp, forced, N, codes, status, slow_logits, fast_logits, draws,
+                   U16(h->w.fast_emb)};
+    mp.tok_emb = U16(h->w.tok_emb);
+    mp.fusion = U16(h->w.fusion);
+    mp.bar = h->bar_counter;
+    mp.bar_extra = h->bar_extra;
+    CUDA_TRY(h, cudaMemsetAsync(h->bar_counter, 0, 4, h->stream));
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (h->profiling) {
+      e0 = next_event(h);
+      e1 = next_event(h);
+      CUDA_TRY(h, cudaEventRecord(e0, h->stream));
+    }
+    bool unsupported = false;
+    LAUNCH(h, launch_mega(mp, batch, h->n_sm, h->stream, &unsupported));
+    if (!unsupported) {
+      if (h->profiling) {
+        CUDA_TRY(h, cudaEventRecord(e1, h->stream));
+        h->prof_bytes.push_back(0.0);
+      }
+      for (int r = 0; r < batch; ++r) h->length[slots[r]] += 1;
+      return DUALAR_OK;
+    }
+    if (h->profiling) h->ev_used -= 2;
+    --h->launches;
+    h->mega_unsupported[batch] = true;   // fall through to the per-op path
+  }
   // 1. q0 from the held restricted logits (+ repetition-aware resample)
   LAUNCH(h, launch_sample_q0(d, batch, uniforms, N + 1, sp, forced, N, codes, status, slow_logits,
                              draws, U16(h->w.fast_emb), h->stream));
@@ -422,7 +555,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
   // 3. fusion -> next slow input; 4. one slow position; restricted head
   LAUNCH(h, launch_fusion(d, batch, U16(h->w.tok_emb), U16(h->w.fusion), h->stream));
   TRY(slow_stack(h, batch, units, chunk, true));
-  TRY(restricted_head(h, 0, batch));
+  TRY(run_gemv(h, args_head(h, 0, batch)));
   for (int r = 0; r < batch; ++r) h->length[slots[r]] += 1;
   return DUALAR_OK;
 }
@@ -537,6 +670,7 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
   ALLOC(d.arrive, R * c.n_kv_head);
   ALLOC(d.codes_ws, R * kMaxCodebooks);
   ALLOC(d.err, 1);
+  ALLOC(h->bar_counter, 1);
 #undef ALLOC
 
   // RoPE tables: angle = pos * base^(-2i/head_dim) in double, cos/sin rounded
@@ -632,7 +766,7 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
     plan_attention(h, s, &units, &chunk);
     LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
     TRY(slow_stack(h, m, units, chunk, false));
-    if (c0 + m == n_tokens) TRY(restricted_head(h, m - 1, 1));
+    if (c0 + m == n_tokens) TRY(run_gemv(h, args_head(h, m - 1, 1)));
   }
   h->length[slot] = n_tokens;
   return DUALAR_OK;
@@ -745,6 +879,18 @@ int dualar_set_wait_limit(dualar_handle* h, uint64_t nanoseconds) {
 }
 
 int32_t dualar_last_launch_count(const dualar_handle* h) { return h ? h->launches : -1; }
+
+int dualar_set_persistent(dualar_handle* h, int32_t enable) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  h->use_mega = enable != 0;
+  return DUALAR_OK;
+}
+
+int dualar_debug_barrier_extra(dualar_handle* h, uint32_t extra) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  h->bar_extra = extra;
+  return DUALAR_OK;
+}
 
 int dualar_profile(dualar_handle* h, int32_t enable) {
   if (!h) return DUALAR_ERR_INVALID_ARG;

@@ -215,7 +215,7 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
     for (int e = tid; e < nrows * NB; e += NCT) {
       const int rr = e / NB, b = e % NB;
       if (b < a.nb) {
-        const int orow = a.out_map ? a.out_map[b] : b;
+        const int orow = a.out_map ? __ldcg(a.out_map + b) : b;
         if (orow >= 0) {
           const float* bp = a.base + static_cast<size_t>(orow) * a.ldb + g.v_begin + rr;
           pr.base[rr][b] = coherent ? __ldcg(bp) : *bp;
@@ -223,7 +223,7 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
       }
     }
   }
-  if (tid < NB) pr.orow[tid] = tid < a.nb ? (a.out_map ? a.out_map[tid] : tid) : -1;
+  if (tid < NB) pr.orow[tid] = tid < a.nb ? (a.out_map ? __ldcg(a.out_map + tid) : tid) : -1;
   if (norm) {
     // [P1] "Fast Transformer": RMSNorm(dim, eps=norm_eps), pre-norm blocks.
 #pragma unroll
@@ -245,7 +245,7 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
   named_barrier(1, NCT);
   if (a.save_x != nullptr && cta == 0) {
     for (int b = 0; b < a.nb; ++b) {
-      const int row = a.save_map ? a.save_map[b] : b;
+      const int row = a.save_map ? __ldcg(a.save_map + b) : b;
       if (row < 0) continue;
       const float* xa = xs + static_cast<size_t>(b) * K;
       const float* xb = xa + 4 * KV;

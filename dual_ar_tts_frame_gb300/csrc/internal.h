@@ -118,6 +118,21 @@ struct SamplingParams {
   int32_t allow_eos;
 };
 
+// Per-call sampler arguments (device pointers).
+struct SampIO {
+  const float* uniforms;
+  int ldu;
+  SamplingParams sp;
+  const int32_t* forced;
+  int ldf;
+  int32_t* codes_out;
+  int32_t* status_out;
+  float* slow_logits_out;
+  float* fast_logits_out;
+  int32_t* draws_out;
+  const uint16_t* fast_emb;
+};
+
 // ---- launchers (kernels.cu) -------------------------------------------------
 cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t* tok_emb,
                          cudaStream_t st);

@@ -1,0 +1,205 @@
+// Persistent frame kernel: one cooperative launch runs a whole Dual-AR frame
+// for a batch of 1-2 sequences -- q0 draw, the N fast-AR passes (all
+// codebooks, without returning to the host), fusion, the slow-AR position and
+// the restricted head.
+//
+// One CTA per SM: 16 consumer warps execute the ops of a fixed program in
+// order, separated by grid-wide barriers; one producer warp walks the same
+// program and streams the weight tiles of every GEMV into a shared-memory ring
+// with bulk copies.  Weights never depend on activations, so the producer
+// runs ahead across op boundaries (bounded by the ring depth) and HBM keeps
+// streaming while the consumers wait at a barrier, sample or attend.
+//
+// Every wait is bounded: a grid barrier that does not complete within the
+// handle's wait limit raises DEV_ERR_GRID_TIMEOUT, and once the error word is
+// set the remaining barriers return at once, so the kernel always finishes.
+//
+// [P2] "Two autoregressions" (decode_one_token_ar order, fast KV cache of
+// num_codebooks positions, Eq. 1 fusion); "The slow AR is Qwen3-4B".
+#include "common.cuh"
+#include "gemv.cuh"
+#include "internal.h"
+#include "mega.h"
+#include "ops.cuh"
+
+namespace dualar {
+
+constexpr int kMegaNCT = kWarpsC * 32;   // consumer threads
+constexpr int kMegaRingStages = 3;
+
+template <int NB, int HD, int G>
+struct MegaLayout {
+  // fixed area (offsets from the dynamic shared memory base)
+  static constexpr size_t bars = 0;   // full[8], empty[8], attn[2]
+  static constexpr size_t scratch = 256;
+  static constexpr size_t pro = (scratch + sizeof(GemvScratch<NB>) + 15) & ~size_t(15);
+  static constexpr size_t uni = (pro + sizeof(GemvPro<NB>) + 127) & ~size_t(127);
+  // union region: GEMV x rows | paged attention | fast attention | sampler
+  __host__ __device__ static size_t union_bytes(int kmax) {
+    size_t u = sizeof(float) * size_t(NB) * kmax;
+    u = u > sizeof(AttnSmem<HD, G, kMegaNCT>) ? u : sizeof(AttnSmem<HD, G, kMegaNCT>);
+    u = u > sizeof(FastAttnSmem<HD>) ? u : sizeof(FastAttnSmem<HD>);
+    u = u > sizeof(SampSmem<kMegaNCT>) ? u : sizeof(SampSmem<kMegaNCT>);
+    return u;
+  }
+  __host__ __device__ static size_t ring(int kmax) { return (uni + union_bytes(kmax) + 127) & ~size_t(127); }
+  __host__ __device__ static size_t total(int kmax) { return ring(kmax) + size_t(kMegaRingStages) * kStageBytes; }
+};
+
+DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64_t limit_ns) {
+  named_barrier(1, kMegaNCT);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(counter, 1u);
+    const volatile uint32_t* ev = err;
+    if (ld_acquire_gpu(counter) < target) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_gpu(counter) < target) {
+        if (*ev & (DEV_ERR_GRID_TIMEOUT | DEV_ERR_MBAR_TIMEOUT)) break;   // another CTA gave up
+        if (global_timer_ns() - t0 > limit_ns) {
+          raise_error(err, DEV_ERR_GRID_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  named_barrier(1, kMegaNCT);
+}
+
+template <int NB, int HD, int G>
+__global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams p) {
+  using Lay = MegaLayout<NB, HD, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::bars);
+  GemvRing ring;
+  ring.full = bars;
+  ring.empty = bars + kMaxStagesRing;
+  ring.base = smem + Lay::ring(p.kmax);
+  ring.stages = kMegaRingStages;
+  uint64_t* abars = bars + 2 * kMaxStagesRing;
+  GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + Lay::scratch);
+  GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + Lay::pro);
+  unsigned char* uni = smem + Lay::uni;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  const DevPtrs& d = p.d;
+
+  if (tid == 0) {
+    for (int s = 0; s < kMegaRingStages; ++s) {
+      mbar_init(&ring.full[s], 1);
+      mbar_init(&ring.empty[s], kWarpsC);
+    }
+    mbar_init(&abars[0], 1);
+    mbar_init(&abars[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  for (int i = tid; i < kMaxStagesRing * kWarpsC; i += blockDim.x) (&scr.cnt[0][0])[i] = 0;
+  __syncthreads();
+
+  if (warp == kWarpsC) {
+    // ---------------- producer: weights of every GEMV of the program -------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t t = 0;
+      for (int i = 0; i < p.n_ops; ++i) {
+        const MegaOp& op = p.ops[i];
+        if (op.type != MOP_GEMV) continue;
+        const GemvGeo g = gemv_geo(op.g, cta, ncta);
+        if (!gemv_produce(op.g, g, ring, t, pol, d.err)) break;
+      }
+      gemv_drain(ring, t, d.wait_limit_ns);
+    }
+    return;
+  }
+
+  // ---------------- consumers ------------------------------------------------
+  uint32_t t = 0;
+  uint32_t aphase[2] = {0u, 0u};
+  uint32_t epoch = 0;
+  const int hkv = d.Hkv;
+  for (int i = 0; i < p.n_ops; ++i) {
+    const MegaOp& op = p.ops[i];
+    switch (op.type) {
+      case MOP_GEMV: {
+        const GemvGeo g = gemv_geo(op.g, cta, ncta);
+        float* xs = reinterpret_cast<float*>(uni);
+        gemv_stage_x<NB>(op.g, g, xs, pro, cta, true);
+        if (!gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro)) {
+          // the ring protocol is broken: stop streaming (the error word is set)
+          return;
+        }
+        break;
+      }
+      case MOP_ATTN_PAGED:
+        attn_paged_units<HD, G, kMegaNCT>(d, p.nrows, op.layer, p.units, p.chunk, true, op.q_norm,
+                                          op.k_norm, *reinterpret_cast<AttnSmem<HD, G, kMegaNCT>*>(uni),
+                                          abars, aphase, cta, ncta);
+        break;
+      case MOP_ATTN_FAST:
+        for (int u = cta; u < p.nrows * hkv; u += ncta)
+          attn_fast_unit<HD / 32, G, kMegaNCT>(d, u, op.layer, op.pos, op.q_norm, op.k_norm,
+                                               *reinterpret_cast<FastAttnSmem<HD>*>(uni));
+        break;
+      case MOP_SAMPLE_Q0:
+        for (int r = cta; r < p.nrows; r += ncta)
+          sample_q0_row<kMegaNCT>(d, r, p.io, *reinterpret_cast<SampSmem<kMegaNCT>*>(uni));
+        break;
+      case MOP_SAMPLE_FAST:
+        for (int r = cta; r < p.nrows; r += ncta)
+          sample_fast_row<kMegaNCT>(d, r, op.pos, p.io, *reinterpret_cast<SampSmem<kMegaNCT>*>(uni));
+        break;
+      case MOP_FUSION:
+        for (int r = cta; r < p.nrows; r += ncta) fusion_row<kMegaNCT>(d, r, p.tok_emb, p.fusion);
+        break;
+      default:
+        break;
+    }
+    if (i + 1 < p.n_ops) {
+      ++epoch;
+      grid_barrier(p.bar, epoch * static_cast<uint32_t>(ncta) + p.bar_extra, d.err, d.wait_limit_ns);
+    }
+  }
+}
+
+template <int NB, int HD, int G>
+static cudaError_t mega_launch_t(const MegaParams& p, int n_sm, cudaStream_t st, bool* unsupported) {
+  using Lay = MegaLayout<NB, HD, G>;
+  const size_t smem = Lay::total(p.kmax);
+  if (smem > 227 * 1024) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  static int configured = 0;
+  if (configured != static_cast<int>(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(mega_kernel<NB, HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mega_kernel<NB, HD, G>, kGemvThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) {
+      *unsupported = true;
+      return cudaSuccess;
+    }
+    configured = static_cast<int>(smem);
+  }
+  MegaParams q = p;
+  void* args[] = {&q};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mega_kernel<NB, HD, G>), dim3(n_sm),
+                                     dim3(kGemvThreads), args, smem, st);
+}
+
+cudaError_t launch_mega(const MegaParams& p, int nb, int n_sm, cudaStream_t st, bool* unsupported) {
+  *unsupported = false;
+  const int hd = p.d.hd, G = p.d.Hq / p.d.Hkv;
+  if (nb == 1 && hd == 128 && G == 4) return mega_launch_t<1, 128, 4>(p, n_sm, st, unsupported);
+  if (nb == 2 && hd == 128 && G == 4) return mega_launch_t<2, 128, 4>(p, n_sm, st, unsupported);
+  if (nb == 1 && hd == 64 && G == 2) return mega_launch_t<1, 64, 2>(p, n_sm, st, unsupported);
+  if (nb == 2 && hd == 64 && G == 2) return mega_launch_t<2, 64, 2>(p, n_sm, st, unsupported);
+  *unsupported = true;
+  return cudaSuccess;
+}
+
+}  // namespace dualar

@@ -1,0 +1,50 @@
+// Program and parameters of the persistent frame kernel (mega.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace dualar {
+
+enum MegaOpType : int {
+  MOP_GEMV = 0,
+  MOP_ATTN_PAGED = 1,
+  MOP_ATTN_FAST = 2,
+  MOP_SAMPLE_Q0 = 3,
+  MOP_SAMPLE_FAST = 4,
+  MOP_FUSION = 5,
+};
+
+// One op of the frame program (device memory, built once per batch size).
+struct MegaOp {
+  int type;
+  int layer;
+  int pos;     // fast attention: codebook position; fast sample: codebook k
+  int pad;
+  const uint16_t* q_norm;
+  const uint16_t* k_norm;
+  GemvArgs g;  // MOP_GEMV
+};
+
+struct MegaParams {
+  DevPtrs d;
+  const MegaOp* ops;
+  int n_ops;
+  int nrows;
+  int units, chunk;         // paged-attention work list of this frame
+  int kmax;                 // largest GEMV K (shared-memory x rows)
+  SampIO io;
+  const uint16_t* tok_emb;
+  const uint16_t* fusion;
+  uint32_t* bar;            // grid-barrier counter, zero at launch
+  uint32_t bar_extra;       // test hook: arrivals a barrier waits for beyond the grid (0 normally)
+};
+
+// Launches the frame program as one cooperative kernel (grid = n_sm CTAs).
+// *unsupported is set (and nothing launched) when the batch or head shape has
+// no persistent instantiation or the shared-memory plan does not fit.
+cudaError_t launch_mega(const MegaParams& p, int nb, int n_sm, cudaStream_t st, bool* unsupported);
+
+}  // namespace dualar

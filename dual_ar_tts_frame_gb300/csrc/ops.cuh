@@ -1,0 +1,827 @@
+// Device-side ops of the Dual-AR frame other than the GEMV: QK-norm/RoPE,
+// paged split-KV attention (slow AR), attention over the per-frame codebook
+// cache (fast AR), the sampler, and the multi-codebook fusion.
+//
+// Every op is a device function over NT participating threads that
+// synchronise with named barrier 2 (never __syncthreads), so the same code
+// runs as a standalone kernel (NT = blockDim) and inside the persistent frame
+// kernel (NT = the consumer warps, while a producer warp streams weights).
+// Activations are read through L2 (ld.global.cg): inside the persistent
+// kernel they are rewritten by other CTAs between ops and L1 is not coherent.
+//
+// Pages cited (title, section):
+//   [P1] "How the Dual-Autoregressive Architecture Works in Fish Speech S2: A Deep Dive"
+//   [P2] "Fish Audio S2: a Qwen3-4B on the time axis, four layers on the codebook
+//        axis, and tags that are only text"
+#pragma once
+
+#include <cfloat>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dualar {
+
+template <int NT>
+DEVI void csync() {
+  named_barrier(2, NT);
+}
+
+DEVI float ldf(const float* p) { return __ldcg(p); }
+DEVI int ldi(const int32_t* p) { return __ldcg(p); }
+DEVI RowInfo ld_row(const RowInfo* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  return RowInfo{v.x, v.y, v.z, v.w};
+}
+
+// QK-norm (optional) + RoPE of one head vector held as EPL elements per lane.
+// [P2] "The slow AR is Qwen3-4B": qk-norm (slow AR only), rope_base 1e6;
+// "Streaming: whose numbers": bf16 tables.  Pairs (2i, 2i+1) rotate by
+// pos * base^(-2i/hd).
+template <int EPL>
+DEVI void head_norm_rope(float (&v)[EPL], const uint16_t* nw, float eps, int pos, const DevPtrs& d,
+                         int lane) {
+  const int hd = EPL * 32, half = hd / 2;
+  if (nw != nullptr) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s += v[j] * v[j];
+    s = warp_sum(s);
+    const float inv = 1.0f / sqrtf(s / static_cast<float>(hd) + eps);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) v[j] = (v[j] * inv) * bf16bits_to_f32(nw[lane * EPL + j]);
+  }
+#pragma unroll
+  for (int pp = 0; pp < EPL / 2; ++pp) {
+    const int i = (lane * EPL) / 2 + pp;
+    const float c = bf16bits_to_f32(d.rope_cos[static_cast<size_t>(pos) * half + i]);
+    const float sn = bf16bits_to_f32(d.rope_sin[static_cast<size_t>(pos) * half + i]);
+    const float x0 = v[2 * pp], x1 = v[2 * pp + 1];
+    v[2 * pp] = x0 * c - x1 * sn;
+    v[2 * pp + 1] = x1 * c + x0 * sn;
+  }
+}
+
+// ============================================================================
+// Paged split-KV decode attention (slow AR)
+// ============================================================================
+// A unit is (row, KV head g, chunk c of chunk_tokens positions).  The unit
+// computes softmax(q K^T / sqrt(hd)) V for the G query heads of g over its
+// chunk with a running max; K and V pages (64 positions x hd, bf16) are
+// staged in shared memory by double-buffered bulk copies.  The last unit of
+// (row, g) to finish merges the chunks in chunk order (deterministic).
+// With fuse_append (decode: one row per sequence) the unit applies QK-norm
+// and RoPE to its query heads itself, and the unit holding the newest
+// position also computes that position's K and V, writes them to the page
+// and uses them directly.  [P2] fact table: 32 query heads over 8 KV heads.
+constexpr int kPageTokens = 64;
+
+template <int HD, int G, int NT>
+struct AttnSmem {
+  static constexpr int TPT = NT / kPageTokens;   // threads per token (score pass)
+  static constexpr int QD = HD / TPT;            // dims per thread (score pass)
+  static constexpr int PARTS = NT / HD;          // token groups (value pass)
+  uint16_t kv[2][2][kPageTokens * HD];           // [buffer][K/V][tok][dim]
+  float qs[G][TPT][QD + 1];
+  float sc[G][kPageTokens];
+  float ored[PARTS][G][HD];
+  float knew[HD], vnew[HD];
+  float scl[G], msm[G], lsm[G];
+  int s_last;
+};
+
+template <int HD, int G, int NT>
+DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens,
+                           bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm,
+                           AttnSmem<HD, G, NT>& sm, uint64_t* bars, uint32_t (&phase)[2], int cta,
+                           int ncta) {
+  using S = AttnSmem<HD, G, NT>;
+  constexpr int EPL = HD / 32;
+  constexpr int TPT = S::TPT, QD = S::QD, PARTS = S::PARTS;
+  constexpr int TPP = kPageTokens / PARTS;
+  constexpr int NW = NT / 32;
+  constexpr uint32_t kPageBytes = kPageTokens * HD * 2;
+  static_assert(QD % 8 == 0, "score pass reads 16-byte vectors");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hq = d.Hq, hkv = d.Hkv;
+  const float qscale = 1.0f / sqrtf(static_cast<float>(HD));
+  const size_t page_stride = static_cast<size_t>(kPageTokens) * HD;
+
+  for (int u = cta; u < total_units; u += ncta) {
+    int lo = 0, hi = nrows - 1;   // rows are sorted by unit0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ldi(&d.rows[mid].unit0) <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    const int r = lo;
+    const RowInfo ri = ld_row(&d.rows[r]);
+    const int L = ri.pos + 1;
+    const int nch = (L + chunk_tokens - 1) / chunk_tokens;
+    const int local = u - ri.unit0;
+    const int g = local / nch, c = local % nch;
+    if (!ri.active || g >= hkv) continue;
+    const int t0 = c * chunk_tokens;
+    const int t1 = min(L, t0 + chunk_tokens);
+    const int npages = (t1 - t0 + kPageTokens - 1) / kPageTokens;
+    const bool newest = fuse_append && (c == nch - 1);
+    const int32_t* ptab = d.page_table + static_cast<size_t>(ri.slot) * d.pages_per_seq + t0 / kPageTokens;
+    bool ok = true;
+    for (int p = 0; p < npages; ++p) {
+      const int pg = ldi(ptab + p);
+      if (pg < 0 || pg >= d.max_pages) ok = false;
+    }
+    if (!ok) {
+      if (tid == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
+      continue;
+    }
+    auto issue = [&](int p, int buf) {
+      const uint16_t* kp = d.kv_pool +
+          (((static_cast<size_t>(ldi(ptab + p)) * d.n_layer + layer) * 2 + 0) * hkv + g) * page_stride;
+      const uint16_t* vp = kp + static_cast<size_t>(hkv) * page_stride;
+      mbar_arrive_expect_tx(&bars[buf], 2 * kPageBytes);
+      bulk_load_g2s_plain(sm.kv[buf][0], kp, kPageBytes, &bars[buf]);
+      bulk_load_g2s_plain(sm.kv[buf][1], vp, kPageBytes, &bars[buf]);
+    };
+    if (tid == 0) {
+      issue(0, 0);
+      if (npages > 1) issue(1, 1);
+    }
+
+    if (fuse_append) {
+      if (warp < G) {
+        const int h = g * G + warp;
+        const float* src = d.qkv + static_cast<size_t>(r) * d.qkv_dim + h * HD;
+        float v[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) v[j] = ldf(src + lane * EPL + j);
+        head_norm_rope<EPL>(v, q_norm, d.eps, ri.pos, d, lane);
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          const int dd = lane * EPL + j;
+          sm.qs[warp][dd / QD][dd % QD] = v[j] * qscale;
+        }
+      }
+      if (warp == (G % NW) && newest) {
+        const float* base = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
+        float kv[EPL], vv[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          kv[j] = ldf(base + hq * HD + g * HD + lane * EPL + j);
+          vv[j] = ldf(base + hq * HD + hkv * HD + g * HD + lane * EPL + j);
+        }
+        head_norm_rope<EPL>(kv, k_norm, d.eps, ri.pos, d, lane);
+        const int pg = ldi(d.page_table + static_cast<size_t>(ri.slot) * d.pages_per_seq + ri.pos / kPageTokens);
+        uint16_t* kd = d.kv_pool + (((static_cast<size_t>(pg) * d.n_layer + layer) * 2 + 0) * hkv + g) *
+                                       page_stride + static_cast<size_t>(ri.pos % kPageTokens) * HD;
+        uint16_t* vd = kd + static_cast<size_t>(hkv) * page_stride;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          const uint16_t kb = f32_to_bf16bits(kv[j]), vb = f32_to_bf16bits(vv[j]);
+          kd[lane * EPL + j] = kb;
+          vd[lane * EPL + j] = vb;
+          sm.knew[lane * EPL + j] = bf16bits_to_f32(kb);
+          sm.vnew[lane * EPL + j] = bf16bits_to_f32(vb);
+        }
+      }
+    } else {
+      for (int e = tid; e < G * HD; e += NT) {
+        const int h = e / HD, dd = e % HD;
+        sm.qs[h][dd / QD][dd % QD] = ldf(d.qrot + (static_cast<size_t>(r) * hq + g * G + h) * HD + dd) * qscale;
+      }
+    }
+    if (tid < G) {
+      sm.msm[tid] = -INFINITY;
+      sm.lsm[tid] = 0.f;
+    }
+    float o[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) o[h] = 0.f;
+    csync<NT>();
+
+    const int tok = tid / TPT, qd = tid % TPT;
+    const int vdim = tid % HD, vpart = tid / HD;
+    for (int p = 0; p < npages; ++p) {
+      const int buf = p & 1;
+      const int ps = t0 + p * kPageTokens;
+      const int ntok = min(kPageTokens, t1 - ps);
+      if (!mbar_wait(&bars[buf], phase[buf], d.err, d.wait_limit_ns)) return;
+      phase[buf] ^= 1u;
+      const uint16_t* ks = sm.kv[buf][0];
+      const uint16_t* vs = sm.kv[buf][1];
+      float s[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) s[h] = 0.f;
+      if (tok < ntok) {
+        if (newest && ps + tok == ri.pos) {
+#pragma unroll 4
+          for (int j = 0; j < QD; ++j) {
+            const float kf = sm.knew[qd * QD + j];
+#pragma unroll
+            for (int h = 0; h < G; ++h) s[h] = fmaf(sm.qs[h][qd][j], kf, s[h]);
+          }
+        } else {
+          const uint4* k4 = reinterpret_cast<const uint4*>(ks + tok * HD + qd * QD);
+#pragma unroll
+          for (int v8 = 0; v8 < QD / 8; ++v8) {
+            const uint4 w = k4[v8];
+            const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                                 bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) s[h] = fmaf(sm.qs[h][qd][v8 * 8 + jj], kf[jj], s[h]);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int o2 = 1; o2 < TPT; o2 <<= 1) s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], o2);
+      if (qd == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) sm.sc[h][tok] = tok < ntok ? s[h] : -INFINITY;
+      }
+      csync<NT>();
+      if (warp < G) {
+        const int h = warp;
+        const float a0 = sm.sc[h][lane], a1 = sm.sc[h][lane + 32];
+        const float mx = warp_max(fmaxf(a0, a1));
+        const float mold = sm.msm[h];
+        const float mnew = fmaxf(mold, mx);
+        const float p0 = lane < ntok ? expf(a0 - mnew) : 0.f;
+        const float p1 = lane + 32 < ntok ? expf(a1 - mnew) : 0.f;
+        sm.sc[h][lane] = p0;
+        sm.sc[h][lane + 32] = p1;
+        const float sum = warp_sum(p0 + p1);
+        if (lane == 0) {
+          const float f = expf(mold - mnew);   // 0 for the first page (mold = -inf)
+          sm.scl[h] = f;
+          sm.lsm[h] = sm.lsm[h] * f + sum;
+          sm.msm[h] = mnew;
+        }
+      }
+      csync<NT>();
+#pragma unroll
+      for (int h = 0; h < G; ++h) o[h] *= sm.scl[h];
+      const int tb = vpart * TPP, te = min(ntok, tb + TPP);
+      for (int t = tb; t < te; ++t) {
+        const float v = (newest && ps + t == ri.pos) ? sm.vnew[vdim] : bf16bits_to_f32(vs[t * HD + vdim]);
+#pragma unroll
+        for (int h = 0; h < G; ++h) o[h] = fmaf(sm.sc[h][t], v, o[h]);
+      }
+      csync<NT>();   // buffer `buf` is free again
+      if (tid == 0 && p + 2 < npages) issue(p + 2, buf);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) sm.ored[vpart][h][vdim] = o[h];
+    csync<NT>();
+    float* attn = d.attn + static_cast<size_t>(r) * hq * HD + g * G * HD;
+    if (nch == 1) {
+      for (int e = tid; e < G * HD; e += NT) {
+        const int h = e / HD, dd = e % HD;
+        float t = 0.f;
+#pragma unroll
+        for (int p = 0; p < PARTS; ++p) t += sm.ored[p][h][dd];
+        attn[h * HD + dd] = t / sm.lsm[h];
+      }
+      csync<NT>();
+      continue;
+    }
+    float* pw = d.part + ((static_cast<size_t>(r) * hkv + g) * kMaxChunks + c) * G * (HD + 2);
+    for (int e = tid; e < G * HD; e += NT) {
+      const int h = e / HD, dd = e % HD;
+      float t = 0.f;
+#pragma unroll
+      for (int p = 0; p < PARTS; ++p) t += sm.ored[p][h][dd];
+      pw[h * (HD + 2) + dd] = t;
+    }
+    if (tid < G) {
+      pw[tid * (HD + 2) + HD] = sm.msm[tid];
+      pw[tid * (HD + 2) + HD + 1] = sm.lsm[tid];
+    }
+    __threadfence();
+    csync<NT>();
+    if (tid == 0) {
+      const uint32_t old = atomic_add_acq_rel_gpu(&d.arrive[r * hkv + g], 1u);
+      sm.s_last = (old == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
+    }
+    csync<NT>();
+    if (sm.s_last) {
+      __threadfence();
+      const float* pb = d.part + (static_cast<size_t>(r) * hkv + g) * kMaxChunks * G * (HD + 2);
+      for (int e = tid; e < G * HD; e += NT) {
+        const int h = e / HD, dd = e % HD;
+        float M = -INFINITY;
+        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, ldf(pb + (cc * G + h) * (HD + 2) + HD));
+        float Ls = 0.f, Os = 0.f;
+        for (int cc = 0; cc < nch; ++cc) {
+          const float* q = pb + (cc * G + h) * (HD + 2);
+          const float f = expf(ldf(q + HD) - M);
+          Ls += ldf(q + HD + 1) * f;
+          Os += ldf(q + dd) * f;
+        }
+        attn[h * HD + dd] = Os / Ls;
+      }
+      if (tid == 0) d.arrive[r * hkv + g] = 0u;
+    }
+    csync<NT>();
+  }
+}
+
+// ============================================================================
+// Fast-AR attention over the per-frame codebook cache (<= N positions)
+// ============================================================================
+// One unit per (row, KV head g): warp 0 computes the new position's K (norm
+// if configured, RoPE at the codebook index) and V and appends them; the K/V
+// of earlier positions (written by earlier passes of this frame) are staged
+// in shared memory; warp h < G then computes query head g*G+h.  [P2] "Two
+// autoregressions": the fast AR's KV cache is num_codebooks long and is
+// overwritten every frame.
+template <int HD>
+struct FastAttnSmem {
+  float ks[kMaxCodebooks][HD], vs[kMaxCodebooks][HD];
+};
+
+template <int EPL, int G, int NT>
+DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const uint16_t* q_norm,
+                         const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm) {
+  constexpr int HD = EPL * 32;
+  static_assert(G <= NT / 32 && NT >= 64, "one warp per query head plus a K/V warp");
+  const int r = unit / d.Hkv, g = unit % d.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = d.Hq, hkv = d.Hkv, N = d.N;
+  const float* qkv = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
+  float* kb = d.fast_kv + (((static_cast<size_t>(r) * d.fast_n_layer + layer) * 2 + 0) * hkv + g) * N * HD;
+  float* vb = kb + static_cast<size_t>(hkv) * N * HD;
+  if (warp == 0) {
+    float kv[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) kv[j] = ldf(qkv + hq * HD + g * HD + lane * EPL + j);
+    head_norm_rope<EPL>(kv, k_norm, d.eps, pos, d, lane);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const float vv = ldf(qkv + hq * HD + hkv * HD + g * HD + lane * EPL + j);
+      kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
+      vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv;
+      sm.ks[pos][lane * EPL + j] = kv[j];
+      sm.vs[pos][lane * EPL + j] = vv;
+    }
+  } else {
+    for (int e = threadIdx.x - 32; e < pos * HD; e += NT - 32) {
+      sm.ks[e / HD][e % HD] = ldf(kb + e);
+      sm.vs[e / HD][e % HD] = ldf(vb + e);
+    }
+  }
+  csync<NT>();
+  if (warp < G) {
+    const int h = g * G + warp;
+    float q[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) q[j] = ldf(qkv + h * HD + lane * EPL + j);
+    head_norm_rope<EPL>(q, q_norm, d.eps, pos, d, lane);
+    const float scale = 1.0f / sqrtf(static_cast<float>(HD));
+    float s[kMaxCodebooks];
+    float m = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < kMaxCodebooks; ++t) {
+      s[t] = -INFINITY;
+      if (t <= pos) {
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) a = fmaf(q[j], sm.ks[t][lane * EPL + j], a);
+        s[t] = warp_sum(a) * scale;
+        m = fmaxf(m, s[t]);
+      }
+    }
+    float l = 0.f;
+    float o[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) o[j] = 0.f;
+#pragma unroll
+    for (int t = 0; t < kMaxCodebooks; ++t) {
+      if (t <= pos) {
+        const float p = expf(s[t] - m);
+        l += p;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, sm.vs[t][lane * EPL + j], o[j]);
+      }
+    }
+    float* dst = d.attn + static_cast<size_t>(r) * hq * HD + h * HD;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) dst[lane * EPL + j] = o[j] / l;
+  }
+  csync<NT>();   // shared buffers are reused by the next unit
+}
+
+// ============================================================================
+// Sampler: temperature + top-p on caller uniforms, one CTA per row
+// ============================================================================
+// Candidates are ordered by (logit descending, token id ascending): each gets
+// a unique 64-bit key (order-preserving bits of the logit, then the inverted
+// id).  Probability mass is integer fixed point, round(exp((z - zmax) / T) *
+// 2^24), so every sum is exact and independent of thread order.  The top-p
+// cut is the first candidate (in key order) whose inclusive cumulative mass
+// reaches ceil(top_p * Z); the draw is the first kept candidate whose
+// inclusive cumulative mass reaches floor(u * Zk) + 1, i.e. exceeds u * Zk.
+// Both are found by a most-significant-byte-first radix descent over the
+// keys with 256-bin mass histograms; lanes of a warp that hit the same bin
+// are combined (match + reduce) before one shared-memory atomic.  [P2] "Two
+// autoregressions": sample(biased_logits, ...) for q0, unmasked
+// sample(logits, ...) for q1..q9.
+constexpr int kMaxCands = 4097;
+
+template <int NT>
+struct SampSmem {
+  static constexpr int NW = NT / 32;
+  unsigned long long hmass[256];
+  unsigned int hcnt[256];
+  unsigned long long red64[NW];
+  float redf[NW];
+  unsigned long long bc[4];
+  int ibc[4];
+  int s_commit, s_active;
+};
+
+struct Cands {
+  int n;          // candidates
+  int n_main;     // candidates 0..n_main-1 have ids id_base + i
+  int id_base;
+  int extra_id;   // id of candidate n_main when n > n_main
+};
+
+DEVI uint32_t ord_f32(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);   // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+DEVI int cand_id(const Cands& c, int i) { return i < c.n_main ? c.id_base + i : c.extra_id; }
+DEVI int key_to_index(const Cands& c, unsigned long long key) {
+  const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+  if (c.n > c.n_main && id == c.extra_id) return c.n_main;
+  return id - c.id_base;
+}
+
+template <int NT>
+DEVI float samp_block_max(float v, SampSmem<NT>& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max(v);
+  if (lane == 0) sm.redf[warp] = v;
+  csync<NT>();
+  float t = sm.redf[0];
+  for (int w = 1; w < SampSmem<NT>::NW; ++w) t = fmaxf(t, sm.redf[w]);
+  csync<NT>();
+  return t;
+}
+
+template <int NT>
+DEVI unsigned long long samp_block_sum(unsigned long long v, SampSmem<NT>& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  if (lane == 0) sm.red64[warp] = v;
+  csync<NT>();
+  unsigned long long t = 0;
+  for (int w = 0; w < SampSmem<NT>::NW; ++w) t += sm.red64[w];
+  csync<NT>();
+  return t;
+}
+
+template <int NT>
+DEVI unsigned long long samp_block_max_u64(unsigned long long v, SampSmem<NT>& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
+  }
+  if (lane == 0) sm.red64[warp] = v;
+  csync<NT>();
+  unsigned long long t = 0;
+  for (int w = 0; w < SampSmem<NT>::NW; ++w) t = sm.red64[w] > t ? sm.red64[w] : t;
+  csync<NT>();
+  return t;
+}
+
+// First key (descending) whose inclusive cumulative mass reaches target
+// (1 <= target <= total).  *above_out: mass strictly before it; *mass_out:
+// its own mass.
+template <int NT, int EPT>
+DEVI unsigned long long samp_select(const unsigned long long (&key)[EPT], const uint32_t (&mass)[EPT],
+                                    int n, unsigned long long target, SampSmem<NT>& sm,
+                                    unsigned long long* above_out, unsigned long long* mass_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long prefix = 0, above = 0, result = 0;
+  for (int shift = 56;; shift -= 8) {
+    for (int b = tid; b < 256; b += NT) {
+      sm.hmass[b] = 0;
+      sm.hcnt[b] = 0;
+    }
+    csync<NT>();
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = tid + e * NT;
+      const bool valid = i < n && (shift == 56 || (key[e] >> (shift + 8)) == prefix);
+      const uint32_t bin = valid ? static_cast<uint32_t>((key[e] >> shift) & 255ull) : 256u;
+      const uint32_t grp = __match_any_sync(0xFFFFFFFFu, bin);
+      const uint32_t sum = __reduce_add_sync(grp, valid ? mass[e] : 0u);
+      if (valid && (__ffs(grp) - 1) == lane) {
+        atomicAdd(&sm.hmass[bin], static_cast<unsigned long long>(sum));
+        atomicAdd(&sm.hcnt[bin], static_cast<unsigned int>(__popc(grp)));
+      }
+    }
+    csync<NT>();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending)
+      unsigned long long m8[8];
+      unsigned long long tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        m8[j] = sm.hmass[255 - 8 * lane - j];
+        tot += m8[j];
+      }
+      unsigned long long incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned long long excl = incl - tot;
+      const unsigned long long need = target - above;   // >= 1
+      if (excl < need && need <= incl) {
+        unsigned long long cc = excl;
+        int jb = 7;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cc + m8[j] >= need) {
+            jb = j;
+            break;
+          }
+          cc += m8[j];
+        }
+        const int bin = 255 - 8 * lane - jb;
+        sm.ibc[0] = bin;
+        sm.ibc[1] = static_cast<int>(sm.hcnt[bin]);
+        sm.bc[0] = above + cc;
+        sm.bc[1] = sm.hmass[bin];
+      }
+    }
+    csync<NT>();
+    const int bin = sm.ibc[0];
+    const int cnt = sm.ibc[1];
+    above = sm.bc[0];
+    const unsigned long long mbin = sm.bc[1];
+    prefix = (shift == 56) ? static_cast<unsigned long long>(bin)
+                           : ((prefix << 8) | static_cast<unsigned long long>(bin));
+    if (shift == 0) {
+      result = prefix;
+      *mass_out = mbin;
+      break;
+    }
+    if (cnt == 1) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const int i = tid + e * NT;
+        if (i < n && (key[e] >> shift) == prefix) sm.bc[2] = key[e];
+      }
+      csync<NT>();
+      result = sm.bc[2];
+      *mass_out = mbin;
+      break;
+    }
+    csync<NT>();
+  }
+  csync<NT>();
+  *above_out = above;
+  return result;
+}
+
+// One draw: returns the chosen candidate index.
+template <int NT, int EPT>
+DEVI int samp_draw(const float (&z)[EPT], const unsigned long long (&key)[EPT], const Cands& c,
+                   float zmax, float temperature, float top_p, float u, SampSmem<NT>& sm) {
+  const int tid = threadIdx.x;
+  if (!(temperature > 0.f)) {
+    unsigned long long best = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (tid + e * NT < c.n && key[e] > best) best = key[e];
+    return key_to_index(c, samp_block_max_u64(best, sm));
+  }
+  const float inv_t = 1.0f / temperature;
+  uint32_t mass[EPT];
+  unsigned long long local = 0;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    mass[e] = 0;
+    if (tid + e * NT < c.n) {
+      mass[e] = __float2uint_rn(expf((z[e] - zmax) * inv_t) * 16777216.0f);   // * 2^24
+      local += mass[e];
+    }
+  }
+  const unsigned long long Z = samp_block_sum(local, sm);
+  if (Z == 0ull) {
+    // no finite mass (non-finite logits): take the largest key
+    unsigned long long best = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (tid + e * NT < c.n && key[e] > best) best = key[e];
+    return key_to_index(c, samp_block_max_u64(best, sm));
+  }
+  unsigned long long tc = Z;
+  if (top_p < 1.0f) {
+    const double t = ceil(static_cast<double>(top_p) * static_cast<double>(Z));
+    tc = t < 1.0 ? 1ull : static_cast<unsigned long long>(t);
+    if (tc > Z) tc = Z;
+  }
+  unsigned long long above, mk;
+  samp_select<NT, EPT>(key, mass, c.n, tc, sm, &above, &mk);
+  const unsigned long long zk = above + mk;
+  unsigned long long td =
+      static_cast<unsigned long long>(floor(static_cast<double>(u) * static_cast<double>(zk))) + 1ull;
+  if (td > zk) td = zk;
+  const unsigned long long kd = samp_select<NT, EPT>(key, mass, c.n, td, sm, &above, &mk);
+  return key_to_index(c, kd);
+}
+
+// Loads the candidates' logits and keys into registers; returns zmax.
+template <int NT, int EPT>
+DEVI float samp_load(const float* src, const Cands& c, float (&z)[EPT], unsigned long long (&key)[EPT],
+                     SampSmem<NT>& sm) {
+  float zm = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = threadIdx.x + e * NT;
+    z[e] = -INFINITY;
+    key[e] = 0;
+    if (i < c.n) {
+      z[e] = ldf(src + i);
+      zm = fmaxf(zm, z[e]);
+      key[e] = (static_cast<unsigned long long>(ord_f32(z[e])) << 32) |
+               static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(cand_id(c, i)));
+    }
+  }
+  return samp_block_max(zm, sm);
+}
+
+// q0 of one row: normal draw, repetition-aware resample, commit, and the
+// inputs of fast passes 0 and 1.
+template <int NT>
+DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT>& sm) {
+  constexpr int EPT = (kMaxCands + NT - 1) / NT;
+  const int tid = threadIdx.x;
+  const RowInfo ri = ld_row(&d.rows[row]);
+  const int slot = ri.slot;
+  const int ns = d.n_sem, N = d.N;
+  const float* zsrc = d.z_last + static_cast<size_t>(slot) * (ns + 1);
+  if (io.slow_logits_out)
+    for (int i = tid; i < ns + 1; i += NT) io.slow_logits_out[static_cast<size_t>(row) * (ns + 1) + i] = ldf(zsrc + i);
+  if (ldi(d.finished + slot)) {
+    // a finished slot stays finished: no codes, no state change
+    if (tid == 0) {
+      io.status_out[row] = 2;
+      d.rows[row].active = 0;
+      d.commit_map[row] = -1;
+    }
+    for (int k = tid; k < N; k += NT) io.codes_out[row * N + k] = -1;
+    csync<NT>();
+    return;
+  }
+  // [P2] "Two autoregressions": the bias keeps the semantic ids and <|im_end|>.
+  const Cands c{ns + (io.sp.allow_eos ? 1 : 0), ns, d.sem_begin, d.im_end};
+  float z[EPT];
+  unsigned long long key[EPT];
+  const float zmax = samp_load<NT, EPT>(zsrc, c, z, key, sm);
+  const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
+  const int normal = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u[0], sm);
+  // [P2] "Two autoregressions": a second draw at temperature 1.0, top-p 0.9,
+  // used when the normal draw repeats a semantic token of the last 10 frames.
+  const int ras = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.ras_temperature, io.sp.ras_top_p, u[1], sm);
+  if (tid == 0) {
+    const int hn = ldi(d.hist_n + slot);
+    const int w = min(io.sp.ras_win, hn);
+    bool repeat = false;
+    if (normal != ns)
+      for (int j = 0; j < w; ++j)
+        if (ldi(d.hist + slot * kRasRing + ((hn - 1 - j) % kRasRing)) == normal) repeat = true;
+    const int chosen = (io.sp.ras_win > 0 && repeat) ? ras : normal;
+    const int commit = io.forced ? io.forced[static_cast<size_t>(row) * io.ldf] : chosen;
+    if (io.draws_out) {
+      io.draws_out[row * (N + 2) + 0] = normal;
+      io.draws_out[row * (N + 2) + 1] = ras;
+      io.draws_out[row * (N + 2) + 2] = chosen;
+    }
+    int active = 1;
+    if (commit == ns || commit < 0 || commit > ns) {
+      if (commit != ns) raise_error(d.err, DEV_ERR_BAD_INDEX);
+      io.status_out[row] = 1;
+      d.finished[slot] = 1;
+      d.rows[row].active = 0;
+      d.commit_map[row] = -1;
+      active = 0;
+    } else {
+      io.status_out[row] = 0;
+      d.hist[slot * kRasRing + (hn % kRasRing)] = commit;
+      d.hist_n[slot] = hn + 1;
+      d.codes_ws[row * kMaxCodebooks] = commit;
+    }
+    sm.s_commit = commit;
+    sm.s_active = active;
+  }
+  csync<NT>();
+  const int commit = sm.s_commit;
+  if (!sm.s_active) {
+    for (int k = tid; k < N; k += NT) io.codes_out[row * N + k] = -1;
+    csync<NT>();
+    return;
+  }
+  if (tid == 0) io.codes_out[row * N] = commit;
+  // fast pass 0 reads the slow hidden state; pass 1 the embedding of q0
+  // ([P2] "Two autoregressions", decode_one_token_ar).  q0 indexes the fast
+  // embedding clamped to its rows (a no-op when n_sem == fast_vocab).
+  const int D = d.D;
+  const int e0 = min(commit, d.Cf - 1);
+  float* f0 = d.fin + static_cast<size_t>(row) * D;
+  float* f1 = d.fin + (static_cast<size_t>(kMaxRows) + row) * D;
+  const float* hl = d.h_last + static_cast<size_t>(slot) * D;
+  const uint16_t* er = io.fast_emb + static_cast<size_t>(e0) * D;
+  for (int k = tid; k < D; k += NT) {
+    f0[k] = ldf(hl + k);
+    f1[k] = bf16bits_to_f32(er[k]);
+  }
+  csync<NT>();
+}
+
+// q_k (k >= 1) of one row from the fast head's logits, and the input of pass k+1.
+template <int NT>
+DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, SampSmem<NT>& sm) {
+  constexpr int EPT = (kMaxCands + NT - 1) / NT;
+  const int tid = threadIdx.x;
+  const int N = d.N, Cf = d.Cf;
+  const float* zs = d.logits + static_cast<size_t>(row) * d.logit_ld;
+  if (io.fast_logits_out)
+    for (int i = tid; i < Cf; i += NT)
+      io.fast_logits_out[(static_cast<size_t>(row) * (N - 1) + (k - 1)) * Cf + i] = ldf(zs + i);
+  if (!ldi(&d.rows[row].active)) return;
+  const Cands c{Cf, Cf, 0, -1};
+  float z[EPT];
+  unsigned long long key[EPT];
+  const float zmax = samp_load<NT, EPT>(zs, c, z, key, sm);
+  const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
+  const int draw = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u[k + 1], sm);
+  if (tid == 0) {
+    int commit = io.forced ? io.forced[static_cast<size_t>(row) * io.ldf + k] : draw;
+    if (commit < 0 || commit >= Cf) {
+      raise_error(d.err, DEV_ERR_BAD_INDEX);
+      commit = 0;
+    }
+    if (io.draws_out) io.draws_out[row * (N + 2) + k + 2] = draw;
+    d.codes_ws[row * kMaxCodebooks + k] = commit;
+    io.codes_out[row * N + k] = commit;
+    sm.s_commit = commit;
+  }
+  csync<NT>();
+  if (k + 1 < N) {
+    const int D = d.D;
+    float* f = d.fin + (static_cast<size_t>((k + 1) & 1) * kMaxRows + row) * D;
+    const uint16_t* er = io.fast_emb + static_cast<size_t>(sm.s_commit) * D;
+    for (int j = tid; j < D; j += NT) f[j] = bf16bits_to_f32(er[j]);
+  }
+  csync<NT>();
+}
+
+// ============================================================================
+// Multi-codebook fusion
+// ============================================================================
+// [P2] "Two autoregressions", Eq. 1 and the code's scale:
+//   x_{t+1} = (e_LM[q0] + sum_{k<N} E^(k)[q_k]) / sqrt(N+1)
+// with E^(k) the block of the fusion table that starts at row
+// n_sem + (k-1) * fast_vocab (row 0 for k = 0).
+template <int NT>
+DEVI void fusion_row(const DevPtrs& d, int row, const uint16_t* tok_emb, const uint16_t* fusion) {
+  if (!ldi(&d.rows[row].active)) return;
+  const int D = d.D, N = d.N;
+  int q[kMaxCodebooks];
+  bool bad = false;
+  for (int k = 0; k < N; ++k) {
+    q[k] = ldi(d.codes_ws + row * kMaxCodebooks + k);
+    const int lim = k == 0 ? d.n_sem : d.Cf;
+    if (q[k] < 0 || q[k] >= lim) bad = true;
+  }
+  if (bad) {
+    if (threadIdx.x == 0) raise_error(d.err, DEV_ERR_BAD_INDEX);
+    return;
+  }
+  const float scale = 1.0f / sqrtf(static_cast<float>(N + 1));
+  const uint16_t* e0 = tok_emb + static_cast<size_t>(d.sem_begin + q[0]) * D;
+  for (int j = threadIdx.x; j < D; j += NT) {
+    float acc = bf16bits_to_f32(e0[j]);
+    for (int k = 0; k < N; ++k) {
+      const int off = k == 0 ? 0 : d.n_sem + (k - 1) * d.Cf;
+      acc += bf16bits_to_f32(fusion[static_cast<size_t>(off + q[k]) * D + j]);
+    }
+    d.xs[static_cast<size_t>(row) * D + j] = acc * scale;
+  }
+}
+
+}  // namespace dualar

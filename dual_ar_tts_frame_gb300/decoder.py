@@ -174,6 +174,12 @@ class DualARDecoder:
     def last_launch_count(self) -> int:
         return int(self.lib.dualar_last_launch_count(self.h))
 
+    def set_persistent(self, enable: bool) -> None:
+        self._check(self.lib.dualar_set_persistent(self.h, int(enable)))
+
+    def debug_barrier_extra(self, extra: int) -> None:
+        self._check(self.lib.dualar_debug_barrier_extra(self.h, extra))
+
     def profile(self, enable: bool) -> None:
         self._check(self.lib.dualar_profile(self.h, int(enable)))
 

@@ -222,10 +222,24 @@ int dualar_set_wait_limit(dualar_handle* h, uint64_t nanoseconds);
 /* Number of kernel launches queued by the last decode call. */
 int32_t dualar_last_launch_count(const dualar_handle* h);
 
-/* GEMV timing: with enable = 1, every weight-streaming GEMV launch queued from
- * now on is bracketed by CUDA events on the handle's stream and its
- * algorithmic bytes (weights read + activations read and written) are
- * recorded; enable = 0 stops recording. */
+/* Decode path for batches of 1-2 sequences: 1 (default) runs the whole frame
+ * as one persistent cooperative kernel (one CTA per SM; the N fast-AR passes
+ * and the slow step never return to the host); 0 queues one kernel per op.
+ * Both paths compute the same values. */
+int dualar_set_persistent(dualar_handle* h, int32_t enable);
+
+/* Test hook for the failure path of the persistent kernel's grid barrier:
+ * every barrier waits for `extra` arrivals beyond the grid, which never come,
+ * so each wait runs into the handle's wait limit (dualar_set_wait_limit), the
+ * kernel finishes with garbage outputs, and dualar_sync returns
+ * DUALAR_ERR_TIMEOUT.  0 (default) restores normal operation. */
+int dualar_debug_barrier_extra(dualar_handle* h, uint32_t extra);
+
+/* Kernel timing: with enable = 1, every weight-streaming GEMV launch and
+ * every persistent frame-kernel launch queued from now on is bracketed by
+ * CUDA events on the handle's stream; for GEMV launches the algorithmic bytes
+ * (weights read + activations read and written) are recorded as well (0 for
+ * the frame kernel).  enable = 0 stops recording. */
 int dualar_profile(dualar_handle* h, int32_t enable);
 
 /* Synchronises the stream, then reports the recorded GEMV launches: their

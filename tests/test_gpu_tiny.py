@@ -28,9 +28,11 @@ def dev_weights(tiny_bits):
     return upload_weights(tiny_bits)
 
 
-def make(dev_weights, max_pages=64, max_seqs=4, max_ctx=1024):
+def make(dev_weights, max_pages=64, max_seqs=4, max_ctx=1024, persistent=True):
     from dual_ar_tts_frame_gb300 import DualARDecoder
-    return DualARDecoder(TINY, dev_weights, max_pages=max_pages, max_seqs=max_seqs, max_ctx=max_ctx)
+    d = DualARDecoder(TINY, dev_weights, max_pages=max_pages, max_seqs=max_seqs, max_ctx=max_ctx)
+    d.set_persistent(persistent)
+    return d
 
 
 def gpu_sampling(o: OSampling):
@@ -115,9 +117,11 @@ def run_forced(d, o, slot_prompts, n_frames, smp, seed):
     return stats
 
 
-@pytest.fixture
-def dec(dev_weights):
-    d = make(dev_weights)
+@pytest.fixture(params=[True, False], ids=["persistent", "per-op"])
+def dec(dev_weights, request):
+    """Both decode paths: the persistent frame kernel (batches of 1-2) and one
+    kernel per op (any batch)."""
+    d = make(dev_weights, persistent=request.param)
     yield d
     d.close()
 
@@ -125,6 +129,36 @@ def dec(dev_weights):
 def test_teacher_forced_b1(dec, tiny_oracle):
     smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
     run_forced(dec, tiny_oracle, {0: g.make_prompt(TINY, 32, seed=0)}, 16, smp, seed=3)
+
+
+def test_teacher_forced_b2(dec, tiny_oracle):
+    """Two sequences (the persistent kernel's largest batch), contexts across
+    several pages and split-KV chunks."""
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
+    prompts = {3: g.make_prompt(TINY, 150, seed=14), 1: g.make_prompt(TINY, 60, seed=15)}
+    run_forced(dec, tiny_oracle, prompts, 8, smp, seed=16)
+
+
+def test_paths_bit_identical(dev_weights):
+    """The persistent kernel and the per-op path commit the same codes and
+    hold bit-identical state after sampled frames."""
+    p = g.make_prompt(TINY, 90, seed=17)
+    uni = g.make_uniforms(8, 1, TINY, seed=18)
+    smp = gpu_sampling(OSampling(temperature=0.8, top_p=0.8, ras_win=10))
+    out = []
+    for persistent in (True, False):
+        d = make(dev_weights, persistent=persistent)
+        d.prefill(0, p)
+        codes = []
+        for f in range(8):
+            c, s_ = d.decode_frame([0], dev(uni[f]), smp)
+            codes.append(c.cpu().numpy())
+        d.sync()
+        out.append((np.stack(codes), d.read_state(0)))
+        d.close()
+    np.testing.assert_array_equal(out[0][0], out[1][0])
+    np.testing.assert_array_equal(out[0][1][0], out[1][1][0])
+    np.testing.assert_array_equal(out[0][1][1], out[1][1][1])
 
 
 def test_teacher_forced_ragged_batch(dec, tiny_oracle):
@@ -256,6 +290,23 @@ def test_eos_excluded_when_disallowed(dec):
 
 
 # ------------------------------------------------------------ error paths --
+
+def test_grid_barrier_timeout_reports_error(dev_weights):
+    """A grid barrier of the persistent kernel that never completes (the test
+    hook asks for one arrival more than the grid has) gives up after the wait
+    limit; the kernel finishes and dualar_sync reports DUALAR_ERR_TIMEOUT."""
+    from dual_ar_tts_frame_gb300._lib import DualARError
+    d = make(dev_weights)
+    d.prefill(0, g.make_prompt(TINY, 20, seed=1))
+    d.sync()
+    d.set_wait_limit(20_000_000)          # 20 ms
+    d.debug_barrier_extra(1)
+    uni = dev(g.make_uniforms(1, 1, TINY, seed=2)[0])
+    d.decode_frame([0], uni, gpu_sampling(OSampling()))
+    with pytest.raises(DualARError) as e:
+        d.sync()
+    assert e.value.code == -6
+    d.close()
 
 def test_error_codes(dev_weights):
     from dual_ar_tts_frame_gb300._lib import DualARError
