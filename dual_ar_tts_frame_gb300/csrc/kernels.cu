@@ -295,7 +295,7 @@ cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int
 // ============================================================================
 // Standalone launches of the ops in ops.cuh
 // ============================================================================
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 512;   // same split as the persistent kernel (bit-identical paths)
 
 template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads)
