@@ -22,6 +22,7 @@ ERRORS = {
 # Every symbol include/dualar.h declares.
 EXPORTED = [
     "dualar_create", "dualar_prefill", "dualar_decode_frame", "dualar_decode_frame_forced",
+    "dualar_decode_frame_noalloc",
     "dualar_release", "dualar_sync", "dualar_get_error", "dualar_destroy",
     "dualar_get_page_table", "dualar_get_rope_table", "dualar_read_state", "dualar_slot_length",
     "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_set_persistent",
@@ -77,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_decode_frame_forced.argtypes = [H, c_i32, ctypes.POINTER(c_i32), c_vp,
                                              ctypes.POINTER(dualar_sampling), c_vp, c_vp, c_vp, c_vp,
                                              c_vp, c_vp]
+    L.dualar_decode_frame_noalloc.argtypes = [H, c_i32, ctypes.POINTER(c_i32), c_vp,
+                                              ctypes.POINTER(dualar_sampling), c_vp, c_vp]
     L.dualar_release.argtypes = [H, c_i32]
     L.dualar_sync.argtypes = [H]
     L.dualar_get_error.argtypes = [H, ctypes.c_char_p, ctypes.c_size_t]

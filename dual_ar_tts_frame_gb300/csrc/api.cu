@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <set>
 #include <string>
 #include <vector>
@@ -424,7 +425,7 @@ int slow_stack(dualar_handle* h, int nrows, int units, int chunk, bool decode) {
 
 int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const float* uniforms,
                 const dualar_sampling* smp, const int32_t* forced, int32_t* codes, int32_t* status,
-                float* slow_logits, float* fast_logits, int32_t* draws) {
+                float* slow_logits, float* fast_logits, int32_t* draws, bool per_op_only = false) {
   if (!h) return DUALAR_ERR_INVALID_ARG;
   const dualar_config& c = h->cfg;
   if (batch < 1 || batch > c.max_seqs) {
@@ -491,7 +492,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
                     smp->ras_top_p, smp->allow_eos};
   const int N = c.n_codebooks;
   LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
-  if (h->use_mega && batch <= 2 && !h->mega_unsupported[batch]) {
+  if (!per_op_only && h->use_mega && batch <= 2 && !h->mega_unsupported[batch]) {
     if (!h->mega_ops[batch]) TRY(build_mega_program(h, batch));
     MegaParams mp{};
     mp.d = d;
@@ -557,6 +558,38 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
   TRY(slow_stack(h, batch, units, chunk, true));
   TRY(run_gemv(h, args_head(h, 0, batch)));
   for (int r = 0; r < batch; ++r) h->length[slots[r]] += 1;
+  return DUALAR_OK;
+}
+
+// ---- decode without allocating ------------------------------------------------
+// dualar_decode_frame_noalloc keeps the split-KV attention's scratch (arrival
+// counters, then partial results) in this fixed array instead of the handle's
+// workspace.  It lives in every GPU that loads the library, until exit.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static void* g_noalloc_addr[kNoAllocMaxDevices] = {};   // device address of the array, per device
+static std::mutex g_noalloc_mutex;
+
+// Device address of the fixed scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+int noalloc_scratch(dualar_handle* h, int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) {
+    set_err(h, "decode_frame_noalloc: device %d beyond the %d supported", dev, kNoAllocMaxDevices);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      set_err(h, "cudaGetSymbolAddress(scratch) failed: %s", cudaGetErrorString(e));
+      return DUALAR_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
   return DUALAR_OK;
 }
 
@@ -785,6 +818,50 @@ int dualar_decode_frame_forced(dualar_handle* h, int32_t batch, const int32_t* s
                                float* slow_logits, float* fast_logits, int32_t* draws) {
   return decode_impl(h, batch, slots, uniforms, sampling, forced_codes, codes, status, slow_logits,
                      fast_logits, draws);
+}
+
+int dualar_decode_frame_noalloc(dualar_handle* h, int32_t batch, const int32_t* slots,
+                                const float* uniforms, const dualar_sampling* sampling,
+                                int32_t* codes, int32_t* status) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  const dualar_config& c = h->cfg;
+  const size_t G = static_cast<size_t>(c.n_head / c.n_kv_head);
+  const size_t cnt_bytes =
+      (static_cast<size_t>(batch > 0 ? batch : 0) * c.n_kv_head * sizeof(uint32_t) + 255) & ~size_t(255);
+  const size_t part_bytes = static_cast<size_t>(batch > 0 ? batch : 0) * c.n_kv_head * kMaxChunks * G *
+                            (c.head_dim + 2) * sizeof(float);
+  if (batch < 1 || cnt_bytes + part_bytes > kNoAllocScratchBytes) {
+    const size_t per_seq = 256 + static_cast<size_t>(c.n_kv_head) * kMaxChunks * G * (c.head_dim + 2) * 4;
+    set_err(h, "decode_frame_noalloc: batch %d needs %zu bytes of attention scratch; the fixed array holds "
+               "%zu bytes (at most %zu sequences per call for this model)",
+            batch, cnt_bytes + part_bytes, kNoAllocScratchBytes, kNoAllocScratchBytes / per_seq);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  CUDA_TRY(h, cudaGetDevice(&dev));
+  if (dev != h->device) {
+    set_err(h, "decode_frame_noalloc: device %d is current, the handle lives on device %d", dev, h->device);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  void* base = nullptr;
+  int rc = noalloc_scratch(h, dev, &base);
+  if (rc != DUALAR_OK) return rc;
+  uint32_t* cnt = static_cast<uint32_t*>(base);
+  float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + cnt_bytes);
+  // the last call's counters may be anything: they must start at zero
+  CUDA_TRY(h, cudaMemsetAsync(cnt, 0, cnt_bytes, h->stream));
+  uint32_t* saved_arrive = h->d.arrive;
+  float* saved_part = h->d.part;
+  const bool saved_prof = h->profiling;
+  h->d.arrive = cnt;
+  h->d.part = part;
+  h->profiling = false;   // timing events would be created on demand
+  rc = decode_impl(h, batch, slots, uniforms, sampling, nullptr, codes, status, nullptr, nullptr, nullptr,
+                   /*per_op_only=*/true);
+  h->d.arrive = saved_arrive;
+  h->d.part = saved_part;
+  h->profiling = saved_prof;
+  return rc;
 }
 
 int dualar_release(dualar_handle* h, int32_t slot) {

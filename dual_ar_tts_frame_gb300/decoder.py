@@ -120,6 +120,17 @@ class DualARDecoder:
             ctypes.byref(smp), _ptr(codes), _ptr(status)))
         return codes, status
 
+    def decode_frame_noalloc(self, slots, uniforms: torch.Tensor, sampling: Sampling,
+                             codes: torch.Tensor, status: torch.Tensor):
+        """dualar_decode_frame_noalloc: the caller passes every output buffer;
+        the call itself allocates nothing."""
+        s = np.ascontiguousarray(np.asarray(slots, np.int32))
+        smp = sampling.c()
+        self._check(self.lib.dualar_decode_frame_noalloc(
+            self.h, s.size, s.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(uniforms),
+            ctypes.byref(smp), _ptr(codes), _ptr(status)))
+        return codes, status
+
     def decode_frame_forced(self, slots, uniforms: torch.Tensor, sampling: Sampling,
                             forced: torch.Tensor | None, want_logits: bool = True):
         s = np.ascontiguousarray(np.asarray(slots, np.int32))

@@ -184,6 +184,35 @@ int dualar_decode_frame_forced(dualar_handle* h, int32_t batch, const int32_t* s
                                const int32_t* forced_codes, int32_t* codes, int32_t* status,
                                float* slow_logits, float* fast_logits, int32_t* draws);
 
+/* Decodes one frame like dualar_decode_frame, but allocates nothing during the
+ * call.  The pages have no counterpart of this call; it exists for callers
+ * that cannot allocate device memory once they are running -- for example a
+ * host that hands the library a fixed device budget at start-up and owns
+ * every remaining byte through its own arena, or a process where another
+ * framework has already reserved the rest of the GPU.  dualar_decode_frame
+ * may allocate on the first call with a new batch size (it uploads the
+ * persistent kernel's op program then) and while timing is on (events); this
+ * call never does: it runs one kernel per op, and the split-KV attention
+ * keeps its scratch (arrival counters and partial results) in a fixed 4 MiB
+ * array compiled into the library instead of the handle's workspace.
+ *   - Limit: batch * n_kv_head * 64 * (n_head/n_kv_head) * (head_dim+2) * 4
+ *     bytes of partials plus counters must fit in 4 MiB -- at most 3
+ *     sequences per call for the S2-Pro shape; larger batches return
+ *     DUALAR_ERR_INVALID_ARG with the sizes in the error message.
+ *   - Every GPU that loads the library holds the array until the process
+ *     exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.  The handle's device must be
+ *     current.
+ *   - All calls share the one array.  Each call clears the counters first;
+ *     calls whose GPU work overlaps (other streams, other handles on the same
+ *     device) race on the array and must not overlap.
+ * Arguments, outputs and errors as dualar_decode_frame. */
+int dualar_decode_frame_noalloc(dualar_handle* h, int32_t batch, const int32_t* slots,
+                                const float* uniforms, const dualar_sampling* sampling,
+                                int32_t* codes, int32_t* status);
+
 /* Ends the sequence in a slot and returns its KV pages to the pool (lowest
  * page numbers are handed out first).  Queues nothing on the GPU. */
 int dualar_release(dualar_handle* h, int32_t slot);
