@@ -43,6 +43,8 @@ struct dualar_handle {
   bool use_mega = true;
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
+  uint64_t* trace = nullptr;     // dualar_set_trace
+  int64_t trace_bytes = 0;
   MegaOp* mega_ops[3] = {nullptr, nullptr, nullptr};   // programs for batch 1, 2
   int mega_nops[3] = {0, 0, 0};
   bool mega_unsupported[3] = {false, false, false};
@@ -508,6 +510,8 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     mp.fusion = U16(h->w.fusion);
     mp.bar = h->bar_counter;
     mp.bar_extra = h->bar_extra;
+    const int64_t need = static_cast<int64_t>(h->n_sm) * mp.n_ops * 2 * 8;
+    mp.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
     CUDA_TRY(h, cudaMemsetAsync(h->bar_counter, 0, 4, h->stream));
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (h->profiling) {
@@ -960,6 +964,23 @@ int32_t dualar_last_launch_count(const dualar_handle* h) { return h ? h->launche
 int dualar_set_persistent(dualar_handle* h, int32_t enable) {
   if (!h) return DUALAR_ERR_INVALID_ARG;
   h->use_mega = enable != 0;
+  return DUALAR_OK;
+}
+
+int dualar_set_trace(dualar_handle* h, void* device_buffer, int64_t bytes, int32_t* n_ops,
+                     int32_t* n_ctas) {
+  if (!h || bytes < 0) return DUALAR_ERR_INVALID_ARG;
+  h->trace = static_cast<uint64_t*>(device_buffer);
+  h->trace_bytes = device_buffer ? bytes : 0;
+  if (n_ctas) *n_ctas = h->n_sm;
+  if (n_ops) {
+    // ops of the batch-1 program (built on demand)
+    if (!h->mega_ops[1]) {
+      const int rc = build_mega_program(h, 1);
+      if (rc != DUALAR_OK) return rc;
+    }
+    *n_ops = h->mega_nops[1];
+  }
   return DUALAR_OK;
 }
 

@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   const int hkv = d.Hkv;
   for (int i = 0; i < p.n_ops; ++i) {
     const MegaOp& op = p.ops[i];
+    uint64_t* tr = p.trace ? p.trace + (static_cast<size_t>(cta) * p.n_ops + i) * 2 : nullptr;
+    if (tr && tid == 0) tr[0] = global_timer_ns();
     switch (op.type) {
       case MOP_GEMV: {
         const GemvGeo g = gemv_geo(op.g, cta, ncta);
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       default:
         break;
     }
+    if (tr && tid == 0) tr[1] = global_timer_ns();
     if (i + 1 < p.n_ops) {
       ++epoch;
       grid_barrier(p.bar, epoch * static_cast<uint32_t>(ncta) + p.bar_extra, d.err, d.wait_limit_ns);

@@ -40,6 +40,7 @@ struct MegaParams {
   const uint16_t* fusion;
   uint32_t* bar;            // grid-barrier counter, zero at launch
   uint32_t bar_extra;       // test hook: arrivals a barrier waits for beyond the grid (0 normally)
+  uint64_t* trace;          // optional: [n_sm][n_ops][2] global-timer stamps (op start, op end)
 };
 
 // Launches the frame program as one cooperative kernel (grid = n_sm CTAs).

@@ -191,6 +191,14 @@ class DualARDecoder:
     def debug_barrier_extra(self, extra: int) -> None:
         self._check(self.lib.dualar_debug_barrier_extra(self.h, extra))
 
+    def set_trace(self, buf: torch.Tensor | None):
+        """Per-op timeline of the persistent kernel into buf (uint64 device
+        tensor); returns (n_ops, n_ctas) for a batch of 1."""
+        n_ops, n_ctas = ctypes.c_int32(), ctypes.c_int32()
+        self._check(self.lib.dualar_set_trace(self.h, _ptr(buf), buf.numel() * 8 if buf is not None else 0,
+                                              ctypes.byref(n_ops), ctypes.byref(n_ctas)))
+        return n_ops.value, n_ctas.value
+
     def profile(self, enable: bool) -> None:
         self._check(self.lib.dualar_profile(self.h, int(enable)))
 

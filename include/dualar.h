@@ -264,6 +264,15 @@ int dualar_set_persistent(dualar_handle* h, int32_t enable);
  * DUALAR_ERR_TIMEOUT.  0 (default) restores normal operation. */
 int dualar_debug_barrier_extra(dualar_handle* h, uint32_t extra);
 
+/* Per-op timeline of the persistent frame kernel.  device_buffer: device
+ * memory of `bytes` bytes (NULL stops tracing).  While set, every persistent
+ * launch whose program fits writes, per CTA and op, the global-timer stamps
+ * (ns) at the op's start and at its end before the grid barrier:
+ * uint64 [n_ctas][n_ops][2].  *n_ops / *n_ctas (optional) receive the sizes
+ * for a batch of 1 (n_ops builds that program if needed). */
+int dualar_set_trace(dualar_handle* h, void* device_buffer, int64_t bytes, int32_t* n_ops,
+                     int32_t* n_ctas);
+
 /* Kernel timing: with enable = 1, every weight-streaming GEMV launch and
  * every persistent frame-kernel launch queued from now on is bracketed by
  * CUDA events on the handle's stream; for GEMV launches the algorithmic bytes
