@@ -43,6 +43,7 @@ struct dualar_handle {
   bool use_mega = true;
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
+  uint64_t prefetch_bytes = 256 * 1024;   // dualar_set_prefetch
   uint64_t* trace = nullptr;     // dualar_set_trace
   int64_t trace_bytes = 0;
   MegaOp* mega_ops[3] = {nullptr, nullptr, nullptr};   // programs for batch 1, 2
@@ -512,6 +513,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     mp.bar_extra = h->bar_extra;
     const int64_t need = static_cast<int64_t>(h->n_sm) * mp.n_ops * 2 * 8;
     mp.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
+    mp.prefetch_bytes = h->prefetch_bytes;
     CUDA_TRY(h, cudaMemsetAsync(h->bar_counter, 0, 4, h->stream));
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (h->profiling) {
@@ -981,6 +983,12 @@ int dualar_set_trace(dualar_handle* h, void* device_buffer, int64_t bytes, int32
     }
     *n_ops = h->mega_nops[1];
   }
+  return DUALAR_OK;
+}
+
+int dualar_set_prefetch(dualar_handle* h, uint64_t bytes_per_sm) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  h->prefetch_bytes = bytes_per_sm;
   return DUALAR_OK;
 }
 

@@ -111,6 +111,18 @@ DEVI uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
+// Release-ordered add at GPU scope (cumulative: writes this thread observed
+// before it, e.g. through a CTA barrier, are ordered before the add).
+DEVI void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Prefetch [src, src+bytes) into L2 (bulk, asynchronous, no completion
+// tracking).  src 16-byte aligned, bytes a multiple of 16.
+DEVI void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 DEVI uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)

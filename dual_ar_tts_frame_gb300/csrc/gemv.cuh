@@ -169,11 +169,20 @@ constexpr int kBaseRows = 64;   // residual rows prefetched per CTA
 
 template <int NB>
 struct GemvPro {
-  float red[kWarpsC][NB];
-  float scale[NB];
+  float red[kWarpsC][NB];   // per-warp sums of x^2 (RMSNorm)
   int orow[NB];
   float base[kBaseRows][NB];
 };
+
+// RMSNorm scale of batch row b (1 without norm): 1/sqrt(mean(x^2) + eps).
+template <int NB>
+DEVI float gemv_scale(const GemvArgs& a, const GemvPro<NB>& pr, int b) {
+  if (a.norm_w == nullptr) return 1.f;
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarpsC; ++w) t += pr.red[w][b];
+  return 1.0f / sqrtf(t / static_cast<float>(a.K) + a.eps);
+}
 
 template <int NB>
 DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<NB>& pr, int cta,
@@ -224,23 +233,12 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
     }
   }
   if (tid < NB) pr.orow[tid] = tid < a.nb ? (a.out_map ? __ldcg(a.out_map + tid) : tid) : -1;
-  if (norm) {
-    // [P1] "Fast Transformer": RMSNorm(dim, eps=norm_eps), pre-norm blocks.
+  // RMSNorm partial sums per warp; the scale itself is finished where it is
+  // used (epilogue), so the prologue needs a single barrier
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float w = warp_sum(ss[b]);
-      if (lane == 0) pr.red[warp][b] = w;
-    }
-  }
-  named_barrier(1, NCT);
-  if (tid < NB) {
-    float sc = 1.f;
-    if (norm) {
-      float t = 0.f;
-      for (int w = 0; w < kWarpsC; ++w) t += pr.red[w][tid];
-      sc = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
-    }
-    pr.scale[tid] = sc;
+  for (int b = 0; b < NB; ++b) {
+    const float w = warp_sum(ss[b]);
+    if (lane == 0) pr.red[warp][b] = w;
   }
   named_barrier(1, NCT);
   if (a.save_x != nullptr && cta == 0) {
@@ -249,7 +247,7 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
       if (row < 0) continue;
       const float* xa = xs + static_cast<size_t>(b) * K;
       const float* xb = xa + 4 * KV;
-      const float sc = pr.scale[b];
+      const float sc = gemv_scale(a, pr, b);
       for (int k = tid; k < K; k += NCT) {
         const int j = k >> 3, e = k & 7;
         a.save_x[static_cast<size_t>(row) * a.lds + k] = sc * (e < 4 ? xa[4 * j + e] : xb[4 * j + e - 4]);
@@ -265,7 +263,8 @@ DEVI void gemv_epilogue(const GemvArgs& a, const GemvGeo& g, const GemvPro<NB>& 
   const int orow = pr.orow[b];
   if (orow < 0) return;
   float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
-  y *= pr.scale[b];
+  const float sc = gemv_scale(a, pr, b);
+  y *= sc;
   if (a.mode == GEMV_STORE) {
     *o = y;
   } else if (a.mode == GEMV_ADD) {
@@ -276,7 +275,7 @@ DEVI void gemv_epilogue(const GemvArgs& a, const GemvGeo& g, const GemvPro<NB>& 
     *o = base + y;
   } else {
     // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
-    *o = silu(gate * pr.scale[b]) * y;
+    *o = silu(gate * sc) * y;
   }
 }
 

@@ -49,8 +49,9 @@ struct MegaLayout {
 DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64_t limit_ns) {
   named_barrier(1, kMegaNCT);
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(counter, 1u);
+    // release: every write of this CTA's consumers (ordered before this
+    // thread by the CTA barrier) is visible before the arrival counts
+    red_release_gpu_add(counter, 1u);
     const volatile uint32_t* ev = err;
     if (ld_acquire_gpu(counter) < target) {
       const uint64_t t0 = global_timer_ns();
@@ -62,10 +63,46 @@ DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64
         }
       }
     }
-    __threadfence();
   }
   named_barrier(1, kMegaNCT);
 }
+
+// Position in the sequence of weight tiles of the frame program (all GEMV
+// ops, in order) for one CTA.
+struct TileCursor {
+  const MegaOp* ops;
+  int n_ops, cta, ncta;
+  int i;
+  bool open;
+  GemvArgs a;
+  GemvGeo g;
+  TileIter it;
+  __device__ TileCursor(const MegaOp* o, int n, int c, int nc)
+      : ops(o), n_ops(n), cta(c), ncta(nc), i(0), open(false), a(), g(), it(a, g) {}
+  __device__ bool next(const uint16_t*& src, uint32_t& bytes) {
+    while (i < n_ops) {
+      if (!open) {
+        if (ops[i].type != MOP_GEMV) {
+          ++i;
+          continue;
+        }
+        a = ops[i].g;
+        g = gemv_geo(a, cta, ncta);
+        it = TileIter(a, g);
+        open = true;
+      }
+      int row0, rows, part;
+      if (it.next(row0, rows, part)) {
+        src = gemv_tile_src(a, row0, part);
+        bytes = static_cast<uint32_t>(rows) * a.K * 2;
+        return true;
+      }
+      open = false;
+      ++i;
+    }
+    return false;
+  }
+};
 
 template <int NB, int HD, int G>
 __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams p) {
@@ -100,14 +137,46 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
 
   if (warp == kWarpsC) {
     // ---------------- producer: weights of every GEMV of the program -------
+    // Tiles go into the ring in program order; a second cursor keeps the next
+    // p.prefetch_bytes of tiles beyond the ring in flight into L2, so HBM
+    // keeps streaming while the consumers wait at a barrier, sample or attend.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      TileCursor lc(p.ops, p.n_ops, cta, ncta), pc(p.ops, p.n_ops, cta, ncta);
+      uint64_t loaded = 0, prefetched = 0;
+      const uint32_t* errp = d.err;
       uint32_t t = 0;
-      for (int i = 0; i < p.n_ops; ++i) {
-        const MegaOp& op = p.ops[i];
-        if (op.type != MOP_GEMV) continue;
-        const GemvGeo g = gemv_geo(op.g, cta, ncta);
-        if (!gemv_produce(op.g, g, ring, t, pol, d.err)) break;
+      const uint16_t* src;
+      uint32_t bytes;
+      bool ok = true;
+      while (ok && lc.next(src, bytes)) {
+        const int s = static_cast<int>(t % kMegaRingStages);
+        if (t >= static_cast<uint32_t>(kMegaRingStages)) {
+          const uint32_t parity = ((t / kMegaRingStages) - 1) & 1;
+          if (!mbar_try_wait(&ring.empty[s], parity)) {
+            // ring full: run the L2 prefetch ahead, then wait
+            const uint16_t* ps;
+            uint32_t pb;
+            while (prefetched < loaded + p.prefetch_bytes && pc.next(ps, pb)) {
+              if (prefetched + pb > loaded + bytes) bulk_prefetch_l2(ps, pb);
+              prefetched += pb;
+            }
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&ring.empty[s], parity)) {
+              if (*reinterpret_cast<const volatile uint32_t*>(errp) ||
+                  global_timer_ns() - t0 > d.wait_limit_ns) {
+                raise_error(d.err, DEV_ERR_MBAR_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+          }
+        }
+        mbar_arrive_expect_tx(&ring.full[s], bytes);
+        bulk_load_g2s(ring.base + static_cast<size_t>(s) * kStageBytes, src, bytes, &ring.full[s], pol);
+        loaded += bytes;
+        ++t;
       }
       gemv_drain(ring, t, d.wait_limit_ns);
     }

@@ -41,6 +41,7 @@ struct MegaParams {
   uint32_t* bar;            // grid-barrier counter, zero at launch
   uint32_t bar_extra;       // test hook: arrivals a barrier waits for beyond the grid (0 normally)
   uint64_t* trace;          // optional: [n_sm][n_ops][2] global-timer stamps (op start, op end)
+  uint64_t prefetch_bytes;  // weight bytes per CTA kept in flight into L2 beyond the ring
 };
 
 // Launches the frame program as one cooperative kernel (grid = n_sm CTAs).

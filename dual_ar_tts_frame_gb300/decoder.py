@@ -191,6 +191,9 @@ class DualARDecoder:
     def debug_barrier_extra(self, extra: int) -> None:
         self._check(self.lib.dualar_debug_barrier_extra(self.h, extra))
 
+    def set_prefetch(self, bytes_per_sm: int) -> None:
+        self._check(self.lib.dualar_set_prefetch(self.h, bytes_per_sm))
+
     def set_trace(self, buf: torch.Tensor | None):
         """Per-op timeline of the persistent kernel into buf (uint64 device
         tensor); returns (n_ops, n_ctas) for a batch of 1."""

@@ -257,6 +257,11 @@ int32_t dualar_last_launch_count(const dualar_handle* h);
  * Both paths compute the same values. */
 int dualar_set_persistent(dualar_handle* h, int32_t enable);
 
+/* Persistent frame kernel: weight bytes per SM that its producer keeps in
+ * flight into L2 ahead of the shared-memory ring (default 256 KiB; 0 turns
+ * the L2 prefetch off).  A tuning knob; results do not depend on it. */
+int dualar_set_prefetch(dualar_handle* h, uint64_t bytes_per_sm);
+
 /* Test hook for the failure path of the persistent kernel's grid barrier:
  * every barrier waits for `extra` arrivals beyond the grid, which never come,
  * so each wait runs into the handle's wait limit (dualar_set_wait_limit), the
