@@ -813,28 +813,23 @@ DEVI void fusion_row(const DevPtrs& d, int row, const uint16_t* tok_emb, const u
     return;
   }
   const float scale = 1.0f / sqrtf(static_cast<float>(N + 1));
-  // one 8-element vector per thread: the N+1 row reads are independent
+  // one 8-element vector per thread; the row reads are independent and the
+  // compiler keeps a few of them in flight (few live registers: this code is
+  // inlined into the persistent kernel)
   const int DV = D >> 3;
   for (int j = threadIdx.x; j < DV; j += NT) {
-    uint4 v[kMaxCodebooks + 1];
-    v[0] = *reinterpret_cast<const uint4*>(tok_emb + static_cast<size_t>(d.sem_begin + q[0]) * D + 8 * j);
-#pragma unroll
-    for (int k = 0; k < kMaxCodebooks; ++k) {
-      if (k < N) {
-        const int off = k == 0 ? 0 : d.n_sem + (k - 1) * d.Cf;
-        v[k + 1] = *reinterpret_cast<const uint4*>(fusion + static_cast<size_t>(off + q[k]) * D + 8 * j);
-      }
-    }
     float acc[8];
-    acc[0] = bf16lo(v[0].x); acc[1] = bf16hi(v[0].x); acc[2] = bf16lo(v[0].y); acc[3] = bf16hi(v[0].y);
-    acc[4] = bf16lo(v[0].z); acc[5] = bf16hi(v[0].z); acc[6] = bf16lo(v[0].w); acc[7] = bf16hi(v[0].w);
-#pragma unroll
-    for (int k = 0; k < kMaxCodebooks; ++k) {
-      if (k < N) {
-        const uint4 w = v[k + 1];
-        acc[0] += bf16lo(w.x); acc[1] += bf16hi(w.x); acc[2] += bf16lo(w.y); acc[3] += bf16hi(w.y);
-        acc[4] += bf16lo(w.z); acc[5] += bf16hi(w.z); acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
-      }
+    {
+      const uint4 v = *reinterpret_cast<const uint4*>(tok_emb + static_cast<size_t>(d.sem_begin + q[0]) * D + 8 * j);
+      acc[0] = bf16lo(v.x); acc[1] = bf16hi(v.x); acc[2] = bf16lo(v.y); acc[3] = bf16hi(v.y);
+      acc[4] = bf16lo(v.z); acc[5] = bf16hi(v.z); acc[6] = bf16lo(v.w); acc[7] = bf16hi(v.w);
+    }
+#pragma unroll 4
+    for (int k = 0; k < N; ++k) {
+      const int off = k == 0 ? 0 : d.n_sem + (k - 1) * d.Cf;
+      const uint4 w = *reinterpret_cast<const uint4*>(fusion + static_cast<size_t>(off + q[k]) * D + 8 * j);
+      acc[0] += bf16lo(w.x); acc[1] += bf16hi(w.x); acc[2] += bf16lo(w.y); acc[3] += bf16hi(w.y);
+      acc[4] += bf16lo(w.z); acc[5] += bf16hi(w.z); acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
     }
     float4* dst = reinterpret_cast<float4*>(d.xs + static_cast<size_t>(row) * D + 8 * j);
     dst[0] = make_float4(acc[0] * scale, acc[1] * scale, acc[2] * scale, acc[3] * scale);
