@@ -105,7 +105,7 @@ struct TileCursor {
 };
 
 template <int NB, int HD, int G>
-__global__ void __maxnreg__(120) mega_kernel(const MegaParams p) {   // 544 threads x 120 registers: one CTA per SM, no spills
+__global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams p) {
   using Lay = MegaLayout<NB, HD, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::bars);
