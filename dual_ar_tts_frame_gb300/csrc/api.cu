@@ -43,7 +43,7 @@ struct dualar_handle {
   bool use_mega = true;
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
-  uint64_t prefetch_bytes = 256 * 1024;   // dualar_set_prefetch
+  uint64_t prefetch_bytes = 0;   // dualar_set_prefetch
   uint64_t* trace = nullptr;     // dualar_set_trace
   int64_t trace_bytes = 0;
   MegaOp* mega_ops[3] = {nullptr, nullptr, nullptr};   // programs for batch 1, 2

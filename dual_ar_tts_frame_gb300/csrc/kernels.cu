@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     attn_paged_kernel(DevPtrs d, int nrows, int layer, int total_units, int chunk_tokens,
                       int fuse_append, const uint16_t* q_norm, const uint16_t* k_norm) {
   extern __shared__ __align__(128) unsigned char attn_smem_raw[];
-  auto& sm = *reinterpret_cast<AttnSmem<HD, G, kAttnThreads>*>(attn_smem_raw);
+  auto& sm = *reinterpret_cast<AttnSmem<HD, G, kAttnThreads, 2>*>(attn_smem_raw);
   __shared__ uint64_t bars[2];
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
   __syncthreads();
   uint32_t phase[2] = {0u, 0u};
-  attn_paged_units<HD, G, kAttnThreads>(d, nrows, layer, total_units, chunk_tokens, fuse_append != 0,
+  attn_paged_units<HD, G, kAttnThreads, 2>(d, nrows, layer, total_units, chunk_tokens, fuse_append != 0,
                                         q_norm, k_norm, sm, bars, phase, blockIdx.x, gridDim.x);
 }
 
@@ -320,7 +320,7 @@ static cudaError_t attn_paged_launch(const DevPtrs& d, int nrows, int layer, int
                                      int grid, int fuse, const uint16_t* qn, const uint16_t* kn,
                                      cudaStream_t st) {
   static bool configured = false;
-  const int smem = static_cast<int>(sizeof(AttnSmem<HD, G, kAttnThreads>));
+  const int smem = static_cast<int>(sizeof(AttnSmem<HD, G, kAttnThreads, 2>));
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_paged_kernel<HD, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

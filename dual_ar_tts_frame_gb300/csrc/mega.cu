@@ -25,7 +25,8 @@
 namespace dualar {
 
 constexpr int kMegaNCT = kWarpsC * 32;   // consumer threads
-constexpr int kMegaRingStages = 3;
+constexpr int kMegaMaxStages = 6;
+constexpr size_t kMegaSmemLimit = 227 * 1024;
 
 template <int NB, int HD, int G>
 struct MegaLayout {
@@ -37,13 +38,19 @@ struct MegaLayout {
   // union region: GEMV x rows | paged attention | fast attention | sampler
   __host__ __device__ static size_t union_bytes(int kmax) {
     size_t u = sizeof(float) * size_t(NB) * kmax;
-    u = u > sizeof(AttnSmem<HD, G, kMegaNCT>) ? u : sizeof(AttnSmem<HD, G, kMegaNCT>);
+    u = u > sizeof(AttnSmem<HD, G, kMegaNCT, 1>) ? u : sizeof(AttnSmem<HD, G, kMegaNCT, 1>);
     u = u > sizeof(FastAttnSmem<HD>) ? u : sizeof(FastAttnSmem<HD>);
     u = u > sizeof(SampSmem<kMegaNCT>) ? u : sizeof(SampSmem<kMegaNCT>);
     return u;
   }
   __host__ __device__ static size_t ring(int kmax) { return (uni + union_bytes(kmax) + 127) & ~size_t(127); }
-  __host__ __device__ static size_t total(int kmax) { return ring(kmax) + size_t(kMegaRingStages) * kStageBytes; }
+  // as many 40 KB ring stages as fit next to the fixed area and the union
+  __host__ __device__ static int stages(int kmax) {
+    const size_t room = kMegaSmemLimit > ring(kmax) ? kMegaSmemLimit - ring(kmax) : 0;
+    const int s = static_cast<int>(room / kStageBytes);
+    return s > kMegaMaxStages ? kMegaMaxStages : s;
+  }
+  __host__ __device__ static size_t total(int kmax) { return ring(kmax) + size_t(stages(kmax)) * kStageBytes; }
 };
 
 DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64_t limit_ns) {
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   ring.full = bars;
   ring.empty = bars + kMaxStagesRing;
   ring.base = smem + Lay::ring(p.kmax);
-  ring.stages = kMegaRingStages;
+  ring.stages = Lay::stages(p.kmax);
   uint64_t* abars = bars + 2 * kMaxStagesRing;
   GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + Lay::scratch);
   GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + Lay::pro);
@@ -123,7 +130,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   const DevPtrs& d = p.d;
 
   if (tid == 0) {
-    for (int s = 0; s < kMegaRingStages; ++s) {
+    for (int s = 0; s < ring.stages; ++s) {
       mbar_init(&ring.full[s], 1);
       mbar_init(&ring.empty[s], kWarpsC);
     }
@@ -150,9 +157,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       uint32_t bytes;
       bool ok = true;
       while (ok && lc.next(src, bytes)) {
-        const int s = static_cast<int>(t % kMegaRingStages);
-        if (t >= static_cast<uint32_t>(kMegaRingStages)) {
-          const uint32_t parity = ((t / kMegaRingStages) - 1) & 1;
+        const int s = static_cast<int>(t % ring.stages);
+        if (t >= static_cast<uint32_t>(ring.stages)) {
+          const uint32_t parity = ((t / ring.stages) - 1) & 1;
           if (!mbar_try_wait(&ring.empty[s], parity)) {
             // ring full: run the L2 prefetch ahead, then wait
             const uint16_t* ps;
@@ -204,8 +211,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         break;
       }
       case MOP_ATTN_PAGED:
-        attn_paged_units<HD, G, kMegaNCT>(d, p.nrows, op.layer, p.units, p.chunk, true, op.q_norm,
-                                          op.k_norm, *reinterpret_cast<AttnSmem<HD, G, kMegaNCT>*>(uni),
+        attn_paged_units<HD, G, kMegaNCT, 1>(d, p.nrows, op.layer, p.units, p.chunk, true, op.q_norm,
+                                          op.k_norm, *reinterpret_cast<AttnSmem<HD, G, kMegaNCT, 1>*>(uni),
                                           abars, aphase, cta, ncta);
         break;
       case MOP_ATTN_FAST:
@@ -239,7 +246,7 @@ template <int NB, int HD, int G>
 static cudaError_t mega_launch_t(const MegaParams& p, int n_sm, cudaStream_t st, bool* unsupported) {
   using Lay = MegaLayout<NB, HD, G>;
   const size_t smem = Lay::total(p.kmax);
-  if (smem > 227 * 1024) {
+  if (Lay::stages(p.kmax) < 2 || smem > kMegaSmemLimit) {
     *unsupported = true;
     return cudaSuccess;
   }

@@ -77,12 +77,13 @@ DEVI void head_norm_rope(float (&v)[EPL], const uint16_t* nw, float eps, int pos
 // and uses them directly.  [P2] fact table: 32 query heads over 8 KV heads.
 constexpr int kPageTokens = 64;
 
-template <int HD, int G, int NT>
+template <int HD, int G, int NT, int NBUF = 2>
 struct AttnSmem {
   static constexpr int TPT = NT / kPageTokens;   // threads per token (score pass)
   static constexpr int QD = HD / TPT;            // dims per thread (score pass)
   static constexpr int PARTS = NT / HD;          // token groups (value pass)
-  uint16_t kv[2][2][kPageTokens * HD];           // [buffer][K/V][tok][dim]
+  static constexpr int BUFS = NBUF;              // page buffers (2: double-buffered)
+  uint16_t kv[NBUF][2][kPageTokens * HD];        // [buffer][K/V][tok][dim]
   float qs[G][TPT][QD + 1];
   float sc[G][kPageTokens];
   float ored[PARTS][G][HD];
@@ -91,12 +92,12 @@ struct AttnSmem {
   int s_last;
 };
 
-template <int HD, int G, int NT>
+template <int HD, int G, int NT, int NBUF>
 DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens,
                            bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm,
-                           AttnSmem<HD, G, NT>& sm, uint64_t* bars, uint32_t (&phase)[2], int cta,
+                           AttnSmem<HD, G, NT, NBUF>& sm, uint64_t* bars, uint32_t (&phase)[2], int cta,
                            int ncta) {
-  using S = AttnSmem<HD, G, NT>;
+  using S = AttnSmem<HD, G, NT, NBUF>;
   constexpr int EPL = HD / 32;
   constexpr int TPT = S::TPT, QD = S::QD, PARTS = S::PARTS;
   constexpr int TPP = kPageTokens / PARTS;
@@ -146,7 +147,7 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     };
     if (tid == 0) {
       issue(0, 0);
-      if (npages > 1) issue(1, 1);
+      if (NBUF > 1 && npages > 1) issue(1, 1);
     }
 
     if (fuse_append) {
@@ -203,7 +204,7 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     const int tok = tid / TPT, qd = tid % TPT;
     const int vdim = tid % HD, vpart = tid / HD;
     for (int p = 0; p < npages; ++p) {
-      const int buf = p & 1;
+      const int buf = NBUF > 1 ? (p & 1) : 0;
       const int ps = t0 + p * kPageTokens;
       const int ntok = min(kPageTokens, t1 - ps);
       if (!mbar_wait(&bars[buf], phase[buf], d.err, d.wait_limit_ns)) return;
@@ -272,7 +273,7 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
         for (int h = 0; h < G; ++h) o[h] = fmaf(sm.sc[h][t], v, o[h]);
       }
       csync<NT>();   // buffer `buf` is free again
-      if (tid == 0 && p + 2 < npages) issue(p + 2, buf);
+      if (tid == 0 && p + NBUF < npages) issue(p + NBUF, buf);
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) sm.ored[vpart][h][vdim] = o[h];
