@@ -25,7 +25,7 @@
 namespace dualar {
 
 constexpr int kMegaNCT = kWarpsC * 32;   // consumer threads
-constexpr int kMegaMaxStages = 6;
+constexpr int kMegaMaxStages = 3;   // measured: a 4th stage does not help
 constexpr size_t kMegaSmemLimit = 227 * 1024;
 
 template <int NB, int HD, int G>
