@@ -289,6 +289,20 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
   const int r = warp / g.S, sg = warp % g.S;
   const int j0 = sg * g.seg;
   const int nvec = max(0, min(g.seg, KV - j0));
+  // Batch 1: this warp's x segment is the same for every row, so it is read
+  // from shared memory once per op and kept in registers.
+  constexpr int XR = NB == 1 ? kMaxVecPerLane : 1;
+  float4 xra[XR], xrb[XR];
+  if (NB == 1) {
+    const float4* xa = reinterpret_cast<const float4*>(xs) + j0;
+    const float4* xb = xa + KV;
+#pragma unroll
+    for (int q = 0; q < XR; ++q) {
+      const int j = lane + 32 * q;
+      xra[q] = j < nvec ? xa[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      xrb[q] = j < nvec ? xb[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   TileIter it(a, g);
   int row0, rows, part;
   while (it.next(row0, rows, part)) {
@@ -301,20 +315,29 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
 #pragma unroll
       for (int q = 0; q < kMaxVecPerLane; ++q) {
         const int j = lane + 32 * q;
-        if (j < nvec) w[q] = wr[j];
+        w[q] = j < nvec ? wr[j] : make_uint4(0u, 0u, 0u, 0u);
       }
       float p[NB];
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        const float4* xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K) + j0;
-        const float4* xb = xa + KV;
-        float acc = 0.f;
+        // one accumulator per vector: independent FMA chains
+        float acc[kMaxVecPerLane];
+        if (NB == 1) {
 #pragma unroll
-        for (int q = 0; q < kMaxVecPerLane; ++q) {
-          const int j = lane + 32 * q;
-          if (j < nvec) acc = dot8(w[q], xa[j], xb[j], acc);
+          for (int q = 0; q < kMaxVecPerLane; ++q) acc[q] = dot8(w[q], xra[q < XR ? q : 0], xrb[q < XR ? q : 0], 0.f);
+        } else {
+          const float4* xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K) + j0;
+          const float4* xb = xa + KV;
+#pragma unroll
+          for (int q = 0; q < kMaxVecPerLane; ++q) {
+            const int j = lane + 32 * q;
+            acc[q] = j < nvec ? dot8(w[q], xa[j], xb[j], 0.f) : 0.f;
+          }
         }
-        p[b] = warp_sum(acc);
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxVecPerLane; ++q) sum += acc[q];
+        p[b] = warp_sum(sum);
       }
       const int n = row0 + r;
       if (g.S == 1) {
