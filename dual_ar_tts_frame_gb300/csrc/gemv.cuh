@@ -8,11 +8,12 @@
 // contiguous in memory, fetched by ONE bulk copy (cp.async.bulk) of up to
 // 40 KB (R is a power of two with R*K*2 <= 40 KB).  The consumer warps split
 // the tile: S = warps / R warps per row, each taking a contiguous segment of
-// K, lane-strided 16-byte vectors.  A warp reduces its segment with shuffles,
-// stores the partial, and the last warp of the row to finish (shared-memory
-// counter) adds the S partials in segment order -- deterministic, and no
-// CTA-wide synchronisation while streaming.  The SwiGLU gate and up rows are
-// two consecutive tiles.  One producer thread runs ahead by the ring depth;
+// K, lane-strided 16-byte vectors.  A warp frees its ring stage as soon as its
+// dot products have consumed the tile, then reduces its segment with shuffles
+// and stores the partial in a per-tile buffer; no CTA-wide synchronisation
+// while streaming.  When the buffer is full, and at the end of the GEMV, the
+// consumers add each row's S partials in segment order (deterministic) and
+// write the epilogue.  The SwiGLU gate and up rows are two consecutive tiles.  One producer thread runs ahead by the ring depth;
 // in the persistent kernel it keeps streaming the next GEMV's weights while
 // the consumers are still busy, since weights never depend on activations.
 #pragma once
@@ -103,13 +104,14 @@ struct GemvRing {
   int stages;
 };
 
-// Shared scratch of the consumers: per-warp partials, per-row arrival
-// counters (one set per stage) and the SwiGLU gate outputs.
+// Shared scratch of the consumers: the per-warp partials of the last
+// kPartTiles tiles and where each of those tiles starts.  A SwiGLU pair (gate
+// tile, up tile) always sits in one window since kPartTiles is even.
 template <int NB>
 struct GemvScratch {
-  float part[kMaxStagesRing][kWarpsC][NB];
-  int cnt[kMaxStagesRing][kWarpsC];
-  float gate[kWarpsC][NB];
+  static constexpr int kPartTiles = NB <= 2 ? 32 : 16;
+  float part[kPartTiles][kWarpsC][NB];
+  int2 tile[kPartTiles];   // first row, rows
 };
 
 // Producer side: issues the tiles of one GEMV for this CTA.  t is the ring's
@@ -279,11 +281,41 @@ DEVI void gemv_epilogue(const GemvArgs& a, const GemvGeo& g, const GemvPro<NB>& 
   }
 }
 
+// Combines the partials of the ntiles tiles in the window (S partials per
+// row, added in segment order) and writes their epilogue.  Called by all
+// consumer threads; named barrier 1 before (partials visible) and, when more
+// tiles follow, after (window free again).
+template <int NB>
+DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, const GemvPro<NB>& pr,
+                     int ntiles, bool more) {
+  constexpr int NCT = kWarpsC * 32;
+  named_barrier(1, NCT);
+  const int step = g.swiglu ? 2 : 1;   // SwiGLU: gate tile, then up tile
+  const int per = g.R * NB;
+  const int n = (ntiles / step) * per;
+  for (int e = threadIdx.x; e < n; e += NCT) {
+    const int tt = (e / per) * step, r = (e % per) / NB, b = e % NB;
+    const int2 ti = sc.tile[tt];
+    if (r >= ti.y) continue;
+    float y = 0.f;
+    for (int q = 0; q < g.S; ++q) y += sc.part[tt][r * g.S + q][b];
+    float gate = 0.f;
+    if (g.swiglu) {
+      gate = y;
+      y = 0.f;
+      for (int q = 0; q < g.S; ++q) y += sc.part[tt + 1][r * g.S + q][b];
+    }
+    gemv_epilogue<NB>(a, g, pr, ti.x + r, b, y, gate);
+  }
+  if (more) named_barrier(1, NCT);
+}
+
 // Consumer side: consumes the tiles of one GEMV and writes the epilogue.
 // Returns false if a wait gave up.
 template <int NB>
 DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
                        const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr) {
+  constexpr int kWin = GemvScratch<NB>::kPartTiles;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV = K >> 3;
   const int r = warp / g.S, sg = warp % g.S;
@@ -305,10 +337,13 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
   }
   TileIter it(a, g);
   int row0, rows, part;
+  int tw = 0;   // tiles in the current window
   while (it.next(row0, rows, part)) {
     const int s = static_cast<int>(t % ring.stages);
     if (!mbar_wait(&ring.full[s], (t / ring.stages) & 1, a.err, a.wait_limit_ns)) return false;
-    if (r < rows) {
+    const bool mine = r < rows;
+    float p[NB];
+    if (mine) {
       const uint4* wr = reinterpret_cast<const uint4*>(ring.base + static_cast<size_t>(s) * kStageBytes) +
                         static_cast<size_t>(r) * KV + j0;
       uint4 w[kMaxVecPerLane];
@@ -317,7 +352,6 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
         const int j = lane + 32 * q;
         w[q] = j < nvec ? wr[j] : make_uint4(0u, 0u, 0u, 0u);
       }
-      float p[NB];
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         // one accumulator per vector: independent FMA chains
@@ -337,53 +371,33 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
         float sum = 0.f;
 #pragma unroll
         for (int q = 0; q < kMaxVecPerLane; ++q) sum += acc[q];
-        p[b] = warp_sum(sum);
+        p[b] = sum;
       }
-      const int n = row0 + r;
-      if (g.S == 1) {
-        if (lane < NB) {
-          float y = p[0];
-#pragma unroll
-          for (int b = 1; b < NB; ++b)
-            if (lane == b) y = p[b];
-          if (g.swiglu && part == 0) sc.gate[warp][lane] = y;
-          else gemv_epilogue<NB>(a, g, pr, n, lane, y, g.swiglu ? sc.gate[warp][lane] : 0.f);
-        }
-      } else {
-        if (lane < NB) {
-          float y = p[0];
-#pragma unroll
-          for (int b = 1; b < NB; ++b)
-            if (lane == b) y = p[b];
-          sc.part[s][warp][lane] = y;
-        }
-        __threadfence_block();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&sc.cnt[s][r], 1) == g.S - 1;
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last) {
-          __threadfence_block();
-          if (lane < NB) {
-            float y = 0.f;
-            for (int q = 0; q < g.S; ++q) y += sc.part[s][r * g.S + q][lane];
-            if (g.swiglu && part == 0) sc.gate[r][lane] = y;
-            else gemv_epilogue<NB>(a, g, pr, n, lane, y, g.swiglu ? sc.gate[r][lane] : 0.f);
-          }
-          if (lane == 0) sc.cnt[s][r] = 0;
-          __threadfence_block();
-        }
-      }
-      // release the stage only after this warp's partial/combine is done: the
-      // per-stage scratch is reused with the stage
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[s]);
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[s]);
     }
+    // The stage is free once every lane's reads of it are done (the sums
+    // above depend on them; the arrive is a release): the producer refills it
+    // while this warp still reduces its partial.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[s]);
     ++t;
+    if (mine) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) p[b] = warp_sum(p[b]);
+      if (lane < NB) {
+        float y = p[0];
+#pragma unroll
+        for (int b = 1; b < NB; ++b)
+          if (lane == b) y = p[b];
+        sc.part[tw][warp][lane] = y;
+      }
+    }
+    if (threadIdx.x == 0) sc.tile[tw] = make_int2(row0, rows);
+    if (++tw == kWin) {
+      gemv_flush<NB>(a, g, sc, pr, tw, true);
+      tw = 0;
+    }
   }
+  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false);
   return true;
 }
 

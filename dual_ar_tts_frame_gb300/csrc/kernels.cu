@@ -79,11 +79,22 @@ constexpr int kSmemBudget = 225 * 1024;   // dynamic shared memory per CTA
 // Shared-memory layout of gemv_kernel (offsets in bytes): mbarriers, the
 // consumers' scratch, x rows, then the ring.
 __host__ __device__ inline size_t gemv_scratch_off() { return 256; }
-__host__ __device__ inline size_t gemv_xs_off() {
-  return (256 + sizeof(GemvScratch<8>) + sizeof(GemvPro<8>) + 127) & ~size_t(127);
+__host__ __device__ inline size_t gemv_scratch_bytes(int nbt) {
+  switch (nbt) {
+    case 8: return sizeof(GemvScratch<8>);
+    case 4: return sizeof(GemvScratch<4>);
+    case 2: return sizeof(GemvScratch<2>);
+    default: return sizeof(GemvScratch<1>);
+  }
+}
+__host__ __device__ inline size_t gemv_pro_off(int nbt) {
+  return (gemv_scratch_off() + gemv_scratch_bytes(nbt) + 15) & ~size_t(15);
+}
+__host__ __device__ inline size_t gemv_xs_off(int nbt) {
+  return (gemv_pro_off(nbt) + sizeof(GemvPro<8>) + 127) & ~size_t(127);
 }
 __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
-  return (gemv_xs_off() + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
+  return (gemv_xs_off(nbt) + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
 }
 
 template <int NB>
@@ -95,8 +106,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   ring.base = smem + gemv_ring_off(NB, a.K);
   ring.stages = stages;
   GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + gemv_scratch_off());
-  GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + gemv_scratch_off() + sizeof(GemvScratch<8>));
-  float* xs = reinterpret_cast<float*>(smem + gemv_xs_off());
+  GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + gemv_pro_off(NB));
+  float* xs = reinterpret_cast<float*>(smem + gemv_xs_off(NB));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -106,7 +117,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  for (int i = tid; i < kMaxStagesRing * kWarpsC; i += blockDim.x) (&scr.cnt[0][0])[i] = 0;
   __syncthreads();
   const GemvGeo g = gemv_geo(a, blockIdx.x, gridDim.x);
   uint32_t t = 0;

@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  for (int i = tid; i < kMaxStagesRing * kWarpsC; i += blockDim.x) (&scr.cnt[0][0])[i] = 0;
   __syncthreads();
 
   if (warp == kWarpsC) {
