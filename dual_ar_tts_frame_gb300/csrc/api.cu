@@ -43,6 +43,9 @@ struct dualar_handle {
   bool use_mega = true;
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
+  uint64_t* tagged = nullptr;    // the tagged work buffers (one region)
+  size_t tagged_words = 0;
+  uint32_t epoch = 0;            // tag epoch of the last persistent launch
   uint64_t prefetch_bytes = 0;   // dualar_set_prefetch
   uint64_t* trace = nullptr;     // dualar_set_trace
   int64_t trace_bytes = 0;
@@ -161,6 +164,7 @@ GemvArgs gemv_base(dualar_handle* h) {
   a.eps = h->cfg.norm_eps;
   a.err = h->d.err;
   a.wait_limit_ns = h->d.wait_limit_ns;
+  a.x_src = a.base_src = a.out_src = -1;
   return a;
 }
 
@@ -342,56 +346,87 @@ int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast
 }
 
 // The frame program of the persistent kernel for batch nb (same op order as
-// the per-op path in decode_impl).
+// the per-op path in decode_impl).  Activations go through the tagged
+// buffers; each read names the op that wrote the version it needs.
 int build_mega_program(dualar_handle* h, int nb) {
   const dualar_config& c = h->cfg;
   const DevPtrs& d = h->d;
   std::vector<MegaOp> ops;
-  auto op = [&](int type, int layer, int pos) {
+  auto F = [](uint64_t* p) { return reinterpret_cast<float*>(p); };
+  auto op = [&](int type, int layer, int pos, int in_src) {
     MegaOp o{};
     o.type = type;
     o.layer = layer;
     o.pos = pos;
+    o.in_src = in_src;
     return o;
   };
-  auto gemv = [&](const GemvArgs& a) {
-    MegaOp o = op(MOP_GEMV, 0, 0);
-    o.g = a;
+  // appends op o and returns its index (the tag its outputs carry)
+  auto push = [&](const MegaOp& o) {
     ops.push_back(o);
+    return static_cast<int>(ops.size()) - 1;
   };
-  ops.push_back(op(MOP_SAMPLE_Q0, 0, 0));
+  auto gemv = [&](GemvArgs a, float* x, int x_src, float* base, int base_src, float* out, bool tagged_out) {
+    a.x = x;
+    a.x_src = x_src;
+    if (a.mode == GEMV_ADD) {
+      a.base = base;
+      a.base_src = base_src;
+    }
+    const int idx = static_cast<int>(ops.size());
+    if (tagged_out) {
+      a.out = out;
+      a.out_src = idx;
+    }
+    MegaOp o = op(MOP_GEMV, 0, 0, -1);
+    o.g = a;
+    return push(o);
+  };
+  auto attn_op = [&](int type, int layer, int pos, int qkv_src, bool qk, const dualar_layer_weights& lw) {
+    MegaOp a = op(type, layer, pos, qkv_src);
+    a.q_norm = qk ? U16(lw.q_norm) : nullptr;
+    a.k_norm = qk ? U16(lw.k_norm) : nullptr;
+    return push(a);
+  };
+  const size_t D = c.dim;
+  int fin_src[kMaxCodebooks];
+  fin_src[0] = fin_src[1] = push(op(MOP_SAMPLE_Q0, 0, 0, -1));   // writes the inputs of passes 0 and 1
+  int hf_src = -1;
   for (int p = 0; p < c.n_codebooks; ++p) {
-    const float* xin = d.fin + static_cast<size_t>(p & 1) * kMaxRows * c.dim;
+    float* xin = F(d.fin_t + static_cast<size_t>(p) * kTaggedRows * D);
     for (int l = 0; l < c.fast_n_layer; ++l) {
       const dualar_layer_weights& lw = h->fast[l];
-      const float* x = l == 0 ? xin : d.hf;
-      gemv(args_qkv(h, lw, nb, x));
-      MegaOp a = op(MOP_ATTN_FAST, l, p);
-      a.q_norm = c.fast_qk_norm ? U16(lw.q_norm) : nullptr;
-      a.k_norm = c.fast_qk_norm ? U16(lw.k_norm) : nullptr;
-      ops.push_back(a);
-      gemv(args_o(h, lw, nb, x, d.hf));
-      gemv(args_gateup(h, lw, nb, d.hf));
-      gemv(args_down(h, lw, nb, d.hf));
+      float* x = l == 0 ? xin : F(d.hf_t);
+      const int x_src = l == 0 ? fin_src[p] : hf_src;
+      const int qkv = gemv(args_qkv(h, lw, nb, nullptr), x, x_src, nullptr, -1, F(d.qkv_t), true);
+      const int at = attn_op(MOP_ATTN_FAST, l, p, qkv, c.fast_qk_norm, lw);
+      hf_src = gemv(args_o(h, lw, nb, nullptr, nullptr), F(d.attn_t), at, x, x_src, F(d.hf_t), true);
+      const int act = gemv(args_gateup(h, lw, nb, nullptr), F(d.hf_t), hf_src, nullptr, -1, F(d.act_t), true);
+      hf_src = gemv(args_down(h, lw, nb, nullptr), F(d.act_t), act, F(d.hf_t), hf_src, F(d.hf_t), true);
     }
     if (p == 0) continue;
-    gemv(args_fast_head(h, nb));
-    ops.push_back(op(MOP_SAMPLE_FAST, 0, p));
+    const int head = gemv(args_fast_head(h, nb), F(d.hf_t), hf_src, nullptr, -1, F(d.logits_t), true);
+    const int smp = push(op(MOP_SAMPLE_FAST, 0, p, head));
+    if (p + 1 < c.n_codebooks) fin_src[p + 1] = smp;
   }
-  ops.push_back(op(MOP_FUSION, 0, 0));
+  int hs_src = push(op(MOP_FUSION, 0, 0, -1));
   for (int l = 0; l < c.n_layer; ++l) {
     const dualar_layer_weights& lw = h->slow[l];
-    const float* x = l == 0 ? d.xs : d.hs;
-    gemv(args_qkv(h, lw, nb, x));
-    MegaOp a = op(MOP_ATTN_PAGED, l, 0);
-    a.q_norm = c.slow_qk_norm ? U16(lw.q_norm) : nullptr;
-    a.k_norm = c.slow_qk_norm ? U16(lw.k_norm) : nullptr;
-    ops.push_back(a);
-    gemv(args_o(h, lw, nb, x, d.hs));
-    gemv(args_gateup(h, lw, nb, d.hs));
-    gemv(args_down(h, lw, nb, d.hs));
+    float* x = l == 0 ? F(d.xs_t) : F(d.hs_t);
+    const int x_src = hs_src;
+    const int qkv = gemv(args_qkv(h, lw, nb, nullptr), x, x_src, nullptr, -1, F(d.qkv_t), true);
+    const int at = attn_op(MOP_ATTN_PAGED, l, 0, qkv, c.slow_qk_norm, lw);
+    hs_src = gemv(args_o(h, lw, nb, nullptr, nullptr), F(d.attn_t), at, x, x_src, F(d.hs_t), true);
+    const int act = gemv(args_gateup(h, lw, nb, nullptr), F(d.hs_t), hs_src, nullptr, -1, F(d.act_t), true);
+    hs_src = gemv(args_down(h, lw, nb, nullptr), F(d.act_t), act, F(d.hs_t), hs_src, F(d.hs_t), true);
   }
-  gemv(args_head(h, 0, nb));
+  // the head writes the held state (plain buffers, read by the host and the
+  // next launch)
+  gemv(args_head(h, 0, nb), F(d.hs_t), hs_src, nullptr, -1, nullptr, false);
+  if (ops.size() >= (1u << kTagOpBits)) {
+    h->mega_unsupported[nb] = true;   // op indices do not fit the tag
+    return DUALAR_OK;
+  }
   MegaOp* dev = nullptr;
   CUDA_TRY(h, cudaMalloc(&dev, ops.size() * sizeof(MegaOp)));
   h->allocs.push_back(dev);
@@ -495,9 +530,18 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
                     smp->ras_top_p, smp->allow_eos};
   const int N = c.n_codebooks;
   LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
-  if (!per_op_only && h->use_mega && batch <= 2 && !h->mega_unsupported[batch]) {
-    if (!h->mega_ops[batch]) TRY(build_mega_program(h, batch));
+  if (!per_op_only && h->use_mega && batch <= kTaggedRows && !h->mega_unsupported[batch] && !h->mega_ops[batch])
+    TRY(build_mega_program(h, batch));
+  if (!per_op_only && h->use_mega && batch <= kTaggedRows && !h->mega_unsupported[batch]) {
+    // a new tag epoch per launch; when it would no longer fit its bits the
+    // tagged buffers are cleared and the count starts again
+    if (h->epoch + 1 >= (1u << (32 - kTagOpBits))) {
+      CUDA_TRY(h, cudaMemsetAsync(h->tagged, 0, h->tagged_words * sizeof(uint64_t), h->stream));
+      h->epoch = 0;
+    }
+    h->epoch += 1;
     MegaParams mp{};
+    mp.epoch = h->epoch;
     mp.d = d;
     mp.ops = h->mega_ops[batch];
     mp.n_ops = h->mega_nops[batch];
@@ -710,6 +754,28 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
   ALLOC(d.codes_ws, R * kMaxCodebooks);
   ALLOC(d.err, 1);
   ALLOC(h->bar_counter, 1);
+  {
+    // tagged work buffers of the persistent frame kernel, one region (cleared
+    // together when the tag epoch wraps); every buffer starts on 64 bytes
+    const size_t TR = kTaggedRows;
+    const size_t sizes[8] = {TR * d.qkv_dim, TR * c.n_head * c.head_dim, TR * c.ffn, TR * c.dim,
+                             TR * c.dim, TR * c.dim, kMaxCodebooks * TR * c.dim, TR * d.logit_ld};
+    size_t offs[8], total = 0;
+    for (int i = 0; i < 8; ++i) {
+      offs[i] = total;
+      total += (sizes[i] + 7) / 8 * 8;
+    }
+    ALLOC(h->tagged, total);
+    h->tagged_words = total;
+    d.qkv_t = h->tagged + offs[0];
+    d.attn_t = h->tagged + offs[1];
+    d.act_t = h->tagged + offs[2];
+    d.hs_t = h->tagged + offs[3];
+    d.hf_t = h->tagged + offs[4];
+    d.xs_t = h->tagged + offs[5];
+    d.fin_t = h->tagged + offs[6];
+    d.logits_t = h->tagged + offs[7];
+  }
 #undef ALLOC
 
   // RoPE tables: angle = pos * base^(-2i/head_dim) in double, cos/sin rounded

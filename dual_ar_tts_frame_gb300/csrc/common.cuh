@@ -26,6 +26,96 @@ DEVI uint64_t global_timer_ns() {
   return t;
 }
 
+// ---- tagged activations ----------------------------------------------------
+// Inside the persistent frame kernel an activation value travels with the tag
+// of the op that wrote it: one 64-bit word, the float in the low half and the
+// tag in the high half, written and read as a single 8-byte access (so value
+// and tag are seen together).  A reader spins on its own words until they
+// carry the tag it expects; no grid-wide barrier and no fence is needed
+// between the writer and the reader.  A tag is (launch epoch << 12) | index
+// of the writing op, never 0.
+constexpr uint64_t kAbortCheckNs = 20000;   // waits look at the error word after this long
+
+DEVI uint32_t op_tag(uint32_t epoch, int op) { return (epoch << kTagOpBits) | static_cast<uint32_t>(op); }
+DEVI uint64_t tag_pack(float v, uint32_t tag) {
+  return (static_cast<uint64_t>(tag) << 32) | static_cast<uint64_t>(__float_as_uint(v));
+}
+DEVI uint32_t tag_of(uint64_t w) { return static_cast<uint32_t>(w >> 32); }
+DEVI float tag_val(uint64_t w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+
+DEVI void tag_store(uint64_t* p, float v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(tag_pack(v, tag)) : "memory");
+}
+// two consecutive words (16-byte aligned)
+DEVI void tag_store2(uint64_t* p, float a, float b, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(tag_pack(a, tag)),
+               "l"(tag_pack(b, tag))
+               : "memory");
+}
+DEVI uint64_t tag_load(const uint64_t* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+// two consecutive words (16-byte aligned); each word is read as one access
+DEVI void tag_load2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// Bounded wait on n <= 8 tagged words: returns their values once every word
+// carries `tag`.  Gives up (zeros, false) when the error word shows that
+// another wait gave up, or after limit_ns, raising DEV_ERR_GRID_TIMEOUT.
+template <int n>
+DEVI bool tag_wait(const uint64_t* p, uint32_t tag, float (&v)[n], uint32_t* err, uint64_t limit_ns) {
+  static_assert(n >= 1 && n <= 8, "tag_wait reads at most 8 words");
+  uint64_t w[n];
+  if (n % 2 == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+    for (int q = 0; q < n / 2; ++q) tag_load2(p + 2 * q, w[2 * q], w[2 * q + 1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < n; ++q) w[q] = tag_load(p + q);
+  }
+  bool ok = true;
+#pragma unroll
+  for (int q = 0; q < n; ++q) ok = ok && tag_of(w[q]) == tag;
+  if (!ok) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      ok = true;
+#pragma unroll
+      for (int q = 0; q < n; ++q) {
+        if (tag_of(w[q]) != tag) w[q] = tag_load(p + q);
+        ok = ok && tag_of(w[q]) == tag;
+      }
+      if (ok) break;
+      const uint64_t dt = global_timer_ns() - t0;
+      if (dt > kAbortCheckNs &&
+          (*reinterpret_cast<const volatile uint32_t*>(err) & (DEV_ERR_GRID_TIMEOUT | DEV_ERR_MBAR_TIMEOUT))) {
+        break;
+      }
+      if (dt > limit_ns) {
+        raise_error(err, DEV_ERR_GRID_TIMEOUT);
+        break;
+      }
+    }
+    if (!ok) {
+#pragma unroll
+      for (int q = 0; q < n; ++q) v[q] = 0.f;
+      return false;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < n; ++q) v[q] = tag_val(w[q]);
+  return true;
+}
+
+DEVI float tag_wait1(const uint64_t* p, uint32_t tag, uint32_t* err, uint64_t limit_ns) {
+  float v[1];
+  tag_wait<1>(p, tag, v, err, limit_ns);
+  return v[0];
+}
+
 // ---- shared-memory addresses and mbarriers ---------------------------------
 DEVI uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

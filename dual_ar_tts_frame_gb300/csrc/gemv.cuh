@@ -188,14 +188,42 @@ DEVI float gemv_scale(const GemvArgs& a, const GemvPro<NB>& pr, int b) {
 
 template <int NB>
 DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<NB>& pr, int cta,
-                       bool coherent) {
+                       bool coherent, uint32_t epoch = 0) {
   constexpr int NCT = kWarpsC * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, KV = K >> 3;
   const bool norm = a.norm_w != nullptr;
+  // residual base of this CTA's rows (one value per thread at most): the load
+  // is issued before the x loop and its result taken after it, so the two
+  // round trips overlap
+  const int nrows = g.v_end - g.v_begin;
+  const bool pre_base = a.mode == GEMV_ADD && nrows <= kBaseRows;
+  const int nbase = pre_base ? nrows * NB : 0;
+  static_assert(kBaseRows * NB <= NCT, "one base value per thread");
+  int my_rr = -1, my_b = 0;
+  uint64_t wb = 0;
+  float fb = 0.f;
+  const uint64_t* pb = nullptr;
+  if (tid < nbase) {
+    my_rr = tid / NB;
+    my_b = tid % NB;
+    const int orow = my_b < a.nb ? (a.out_map ? __ldcg(a.out_map + my_b) : my_b) : -1;
+    if (orow < 0) {
+      my_rr = -1;
+    } else {
+      const size_t off = static_cast<size_t>(orow) * a.ldb + g.v_begin + my_rr;
+      if (a.base_src >= 0) {
+        pb = reinterpret_cast<const uint64_t*>(a.base) + off;
+        wb = tag_load(pb);
+      } else {
+        fb = coherent ? __ldcg(a.base + off) : a.base[off];
+      }
+    }
+  }
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
+  const uint32_t xtag = a.x_src >= 0 ? op_tag(epoch, a.x_src) : 0u;
   for (int j = tid; j < KV; j += NCT) {
     float gw[8];
     if (norm) {
@@ -209,30 +237,31 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       if (b < a.nb) {
-        const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
-        const float4 v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
-        const float4 v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
+        float v[8];
+        if (a.x_src >= 0) {
+          tag_wait<8>(reinterpret_cast<const uint64_t*>(a.x) + static_cast<size_t>(b) * a.ldx + 8 * j, xtag, v,
+                      a.err, a.wait_limit_ns);
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
+          const float4 v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
+          const float4 v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
+          v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+          v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+        }
         float4* xa = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
-        xa[j] = make_float4(v0.x * gw[0], v0.y * gw[1], v0.z * gw[2], v0.w * gw[3]);
-        xa[KV + j] = make_float4(v1.x * gw[4], v1.y * gw[5], v1.z * gw[6], v1.w * gw[7]);
-        ss[b] += v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w + v1.x * v1.x + v1.y * v1.y +
-                 v1.z * v1.z + v1.w * v1.w;
+        xa[j] = make_float4(v[0] * gw[0], v[1] * gw[1], v[2] * gw[2], v[3] * gw[3]);
+        xa[KV + j] = make_float4(v[4] * gw[4], v[5] * gw[5], v[6] * gw[6], v[7] * gw[7]);
+        ss[b] += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3] + v[4] * v[4] + v[5] * v[5] +
+                 v[6] * v[6] + v[7] * v[7];
       }
     }
   }
-  // residual base rows and output row map, fetched once
-  const int nrows = g.v_end - g.v_begin;
-  if (a.mode == GEMV_ADD && nrows <= kBaseRows) {
-    for (int e = tid; e < nrows * NB; e += NCT) {
-      const int rr = e / NB, b = e % NB;
-      if (b < a.nb) {
-        const int orow = a.out_map ? __ldcg(a.out_map + b) : b;
-        if (orow >= 0) {
-          const float* bp = a.base + static_cast<size_t>(orow) * a.ldb + g.v_begin + rr;
-          pr.base[rr][b] = coherent ? __ldcg(bp) : *bp;
-        }
-      }
+  if (my_rr >= 0) {
+    if (pb != nullptr) {
+      const uint32_t btag = op_tag(epoch, a.base_src);
+      fb = tag_of(wb) == btag ? tag_val(wb) : tag_wait1(pb, btag, a.err, a.wait_limit_ns);
     }
+    pr.base[my_rr][my_b] = fb;
   }
   if (tid < NB) pr.orow[tid] = tid < a.nb ? (a.out_map ? __ldcg(a.out_map + tid) : tid) : -1;
   // RMSNorm partial sums per warp; the scale itself is finished where it is
@@ -260,34 +289,45 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
 
 template <int NB>
 DEVI void gemv_epilogue(const GemvArgs& a, const GemvGeo& g, const GemvPro<NB>& pr, int n, int b,
-                        float y, float gate) {
+                        float y, float gate, uint32_t epoch) {
   if (b >= a.nb) return;
   const int orow = pr.orow[b];
   if (orow < 0) return;
-  float* o = a.out + static_cast<size_t>(orow) * a.ldo + n;
+  const size_t oi = static_cast<size_t>(orow) * a.ldo + n;
   const float sc = gemv_scale(a, pr, b);
   y *= sc;
+  float r;
   if (a.mode == GEMV_STORE) {
-    *o = y;
+    r = y;
   } else if (a.mode == GEMV_ADD) {
     const int rr = n - g.v_begin;
-    const float base = (g.v_end - g.v_begin <= kBaseRows)
-                           ? pr.base[rr][b]
-                           : __ldcg(a.base + static_cast<size_t>(orow) * a.ldb + n);
-    *o = base + y;
+    float base;
+    if (g.v_end - g.v_begin <= kBaseRows) {
+      base = pr.base[rr][b];
+    } else {
+      const size_t bi = static_cast<size_t>(orow) * a.ldb + n;
+      base = a.base_src >= 0
+                 ? tag_wait1(reinterpret_cast<const uint64_t*>(a.base) + bi, op_tag(epoch, a.base_src), a.err,
+                             a.wait_limit_ns)
+                 : __ldcg(a.base + bi);
+    }
+    r = base + y;
   } else {
     // [P2] "The slow AR is Qwen3-4B": SwiGLU FFN, down(SiLU(gate) * up).
-    *o = silu(gate * sc) * y;
+    r = silu(gate * sc) * y;
   }
+  if (a.out_src >= 0) tag_store(reinterpret_cast<uint64_t*>(a.out) + oi, r, op_tag(epoch, a.out_src));
+  else a.out[oi] = r;
 }
 
+// Consumer side: consumes the tiles of one GEMV and writes the epilogue.
 // Combines the partials of the ntiles tiles in the window (S partials per
 // row, added in segment order) and writes their epilogue.  Called by all
 // consumer threads; named barrier 1 before (partials visible) and, when more
 // tiles follow, after (window free again).
 template <int NB>
 DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, const GemvPro<NB>& pr,
-                     int ntiles, bool more) {
+                     int ntiles, bool more, uint32_t epoch) {
   constexpr int NCT = kWarpsC * 32;
   named_barrier(1, NCT);
   const int step = g.swiglu ? 2 : 1;   // SwiGLU: gate tile, then up tile
@@ -305,7 +345,7 @@ DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, c
       y = 0.f;
       for (int q = 0; q < g.S; ++q) y += sc.part[tt + 1][r * g.S + q][b];
     }
-    gemv_epilogue<NB>(a, g, pr, ti.x + r, b, y, gate);
+    gemv_epilogue<NB>(a, g, pr, ti.x + r, b, y, gate, epoch);
   }
   if (more) named_barrier(1, NCT);
 }
@@ -314,7 +354,7 @@ DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, c
 // Returns false if a wait gave up.
 template <int NB>
 DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
-                       const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr) {
+                       const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr, uint32_t epoch = 0) {
   constexpr int kWin = GemvScratch<NB>::kPartTiles;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV = K >> 3;
@@ -393,11 +433,11 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
     }
     if (threadIdx.x == 0) sc.tile[tw] = make_int2(row0, rows);
     if (++tw == kWin) {
-      gemv_flush<NB>(a, g, sc, pr, tw, true);
+      gemv_flush<NB>(a, g, sc, pr, tw, true, epoch);
       tw = 0;
     }
   }
-  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false);
+  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch);
   return true;
 }
 

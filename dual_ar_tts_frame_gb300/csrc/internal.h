@@ -71,6 +71,11 @@ struct GemvArgs {
   int lds;
   uint32_t* err;
   uint64_t wait_limit_ns;
+  // Persistent frame kernel only: index of the op that wrote x / base, and of
+  // this op (written into out); -1 means a plain fp32 buffer.  With an index
+  // the pointer is a tagged 64-bit buffer (common.cuh, "tagged activations")
+  // with the same element strides.
+  int x_src, base_src, out_src;
 };
 
 // Device buffers of one handle that kernels need (plain pointers).
@@ -109,7 +114,19 @@ struct DevPtrs {
   int32_t* codes_ws;          // [kMaxRows][kMaxCodebooks] codes of the current frame
   uint32_t* err;              // device error word
   uint64_t wait_limit_ns;
+  // tagged copies of the work buffers, used by the persistent frame kernel
+  // (kTaggedRows rows each, same strides as the fp32 buffers)
+  uint64_t* qkv_t;            // [kTaggedRows][qkv_dim]
+  uint64_t* attn_t;           // [kTaggedRows][Hq*hd]
+  uint64_t* act_t;            // [kTaggedRows][F]
+  uint64_t* hs_t;             // [kTaggedRows][D]
+  uint64_t* hf_t;             // [kTaggedRows][D]
+  uint64_t* xs_t;             // [kTaggedRows][D]
+  uint64_t* fin_t;            // [kMaxCodebooks][kTaggedRows][D] input of fast pass p
+  uint64_t* logits_t;         // [kTaggedRows][logit_ld]
 };
+constexpr int kTaggedRows = 2;   // batch rows of the persistent frame kernel
+constexpr int kTagOpBits = 12;   // low bits of an activation tag: index of the writing op
 
 struct SamplingParams {
   float temperature, top_p;

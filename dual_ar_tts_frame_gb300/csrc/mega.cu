@@ -10,9 +10,18 @@
 // runs ahead across op boundaries (bounded by the ring depth) and HBM keeps
 // streaming while the consumers wait at a barrier, sample or attend.
 //
-// Every wait is bounded: a grid barrier that does not complete within the
-// handle's wait limit raises DEV_ERR_GRID_TIMEOUT, and once the error word is
-// set the remaining barriers return at once, so the kernel always finishes.
+// Ops hand activations to each other as tagged words (common.cuh): a reader
+// spins on the words it needs until they carry the tag of the op that writes
+// them, so consecutive ops need no grid-wide barrier -- a CTA moves on as soon
+// as its own inputs are there.  Every activation buffer is rewritten in place
+// only by an op that (directly or through earlier ops) has read outputs of
+// every reader of the previous contents, so a word is never overwritten while
+// someone still waits for its old tag.  One grid barrier remains, after the
+// q0 draw, which may deactivate a row (read by attention units anywhere).
+//
+// Every wait is bounded: a wait that does not complete within the handle's
+// wait limit raises DEV_ERR_GRID_TIMEOUT, and once the error word is set the
+// remaining waits give up quickly, so the kernel always finishes.
 //
 // [P2] "Two autoregressions" (decode_one_token_ar order, fast KV cache of
 // num_codebooks positions, Eq. 1 fusion); "The slow AR is Qwen3-4B".
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   // ---------------- consumers ------------------------------------------------
   uint32_t t = 0;
   uint32_t aphase[2] = {0u, 0u};
-  uint32_t epoch = 0;
+  const uint32_t ep = p.epoch;
   const int hkv = d.Hkv;
   for (int i = 0; i < p.n_ops; ++i) {
     const MegaOp& op = p.ops[i];
@@ -202,8 +211,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       case MOP_GEMV: {
         const GemvGeo g = gemv_geo(op.g, cta, ncta);
         float* xs = reinterpret_cast<float*>(uni);
-        gemv_stage_x<NB>(op.g, g, xs, pro, cta, true);
-        if (!gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro)) {
+        gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
+        if (!gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep)) {
           // the ring protocol is broken: stop streaming (the error word is set)
           return;
         }
@@ -212,31 +221,39 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       case MOP_ATTN_PAGED:
         attn_paged_units<HD, G, kMegaNCT, 1>(d, p.nrows, op.layer, p.units, p.chunk, true, op.q_norm,
                                           op.k_norm, *reinterpret_cast<AttnSmem<HD, G, kMegaNCT, 1>*>(uni),
-                                          abars, aphase, cta, ncta);
+                                          abars, aphase, cta, ncta, OpTags{op_tag(ep, op.in_src), op_tag(ep, i)});
         break;
       case MOP_ATTN_FAST:
+        // unit u always runs on CTA u % ncta, so the fast KV written by one
+        // pass is read by the same CTA in later passes
         for (int u = cta; u < p.nrows * hkv; u += ncta)
           attn_fast_unit<HD / 32, G, kMegaNCT>(d, u, op.layer, op.pos, op.q_norm, op.k_norm,
-                                               *reinterpret_cast<FastAttnSmem<HD>*>(uni));
+                                               *reinterpret_cast<FastAttnSmem<HD>*>(uni),
+                                               OpTags{op_tag(ep, op.in_src), op_tag(ep, i)});
         break;
       case MOP_SAMPLE_Q0:
         for (int r = cta; r < p.nrows; r += ncta)
-          sample_q0_row<kMegaNCT>(d, r, p.io, *reinterpret_cast<SampSmem<kMegaNCT>*>(uni));
+          sample_q0_row<kMegaNCT>(d, r, p.io, *reinterpret_cast<SampSmem<kMegaNCT>*>(uni),
+                                  OpTags{0u, op_tag(ep, i)});
         break;
       case MOP_SAMPLE_FAST:
+        // row r always runs on CTA r: the codes of the frame (codes_ws) are
+        // written and read (fusion) by one CTA
         for (int r = cta; r < p.nrows; r += ncta)
-          sample_fast_row<kMegaNCT>(d, r, op.pos, p.io, *reinterpret_cast<SampSmem<kMegaNCT>*>(uni));
+          sample_fast_row<kMegaNCT>(d, r, op.pos, p.io, *reinterpret_cast<SampSmem<kMegaNCT>*>(uni),
+                                    OpTags{op_tag(ep, op.in_src), op_tag(ep, i)});
         break;
       case MOP_FUSION:
-        for (int r = cta; r < p.nrows; r += ncta) fusion_row<kMegaNCT>(d, r, p.tok_emb, p.fusion);
+        for (int r = cta; r < p.nrows; r += ncta)
+          fusion_row<kMegaNCT>(d, r, p.tok_emb, p.fusion, OpTags{0u, op_tag(ep, i)});
         break;
       default:
         break;
     }
     if (tr && tid == 0) tr[1] = global_timer_ns();
     if (i + 1 < p.n_ops) {
-      ++epoch;
-      grid_barrier(p.bar, epoch * static_cast<uint32_t>(ncta) + p.bar_extra, d.err, d.wait_limit_ns);
+      if (i == 0) grid_barrier(p.bar, static_cast<uint32_t>(ncta) + p.bar_extra, d.err, d.wait_limit_ns);
+      else named_barrier(1, kMegaNCT);   // shared memory is reused by the next op
     }
   }
 }

@@ -22,7 +22,7 @@ struct MegaOp {
   int type;
   int layer;
   int pos;     // fast attention: codebook position; fast sample: codebook k
-  int pad;
+  int in_src;  // attention, fast sample: index of the op that wrote the input
   const uint16_t* q_norm;
   const uint16_t* k_norm;
   GemvArgs g;  // MOP_GEMV
@@ -42,6 +42,7 @@ struct MegaParams {
   uint32_t bar_extra;       // test hook: arrivals a barrier waits for beyond the grid (0 normally)
   uint64_t* trace;          // optional: [n_sm][n_ops][2] global-timer stamps (op start, op end)
   uint64_t prefetch_bytes;  // weight bytes per CTA kept in flight into L2 beyond the ring
+  uint32_t epoch;           // launch epoch of the activation tags (1 .. 2^20 - 1)
 };
 
 // Launches the frame program as one cooperative kernel (grid = n_sm CTAs).

@@ -35,6 +35,29 @@ DEVI RowInfo ld_row(const RowInfo* p) {
   return RowInfo{v.x, v.y, v.z, v.w};
 }
 
+// Tags of an op's activation input and output inside the persistent frame
+// kernel (common.cuh, "tagged activations"); 0 selects the plain fp32
+// buffers (standalone kernels).
+struct OpTags {
+  uint32_t in, out;
+};
+
+// EPL consecutive activation values at element offset off.
+template <int EPL>
+DEVI void act_load(const float* plain, const uint64_t* tagged, size_t off, uint32_t tag, float (&v)[EPL],
+                   const DevPtrs& d) {
+  if (tag != 0u) {
+    tag_wait<EPL>(tagged + off, tag, v, d.err, d.wait_limit_ns);
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) v[j] = ldf(plain + off + j);
+  }
+}
+DEVI void act_store(float* plain, uint64_t* tagged, size_t off, uint32_t tag, float v) {
+  if (tag != 0u) tag_store(tagged + off, v, tag);
+  else plain[off] = v;
+}
+
 // QK-norm (optional) + RoPE of one head vector held as EPL elements per lane.
 // [P2] "The slow AR is Qwen3-4B": qk-norm (slow AR only), rope_base 1e6;
 // "Streaming: whose numbers": bf16 tables.  Pairs (2i, 2i+1) rotate by
@@ -96,7 +119,7 @@ template <int HD, int G, int NT, int NBUF>
 DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens,
                            bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm,
                            AttnSmem<HD, G, NT, NBUF>& sm, uint64_t* bars, uint32_t (&phase)[2], int cta,
-                           int ncta) {
+                           int ncta, OpTags tg = OpTags{0u, 0u}) {
   using S = AttnSmem<HD, G, NT, NBUF>;
   constexpr int EPL = HD / 32;
   constexpr int TPT = S::TPT, QD = S::QD, PARTS = S::PARTS;
@@ -122,7 +145,14 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     const int nch = (L + chunk_tokens - 1) / chunk_tokens;
     const int local = u - ri.unit0;
     const int g = local / nch, c = local % nch;
-    if (!ri.active || g >= hkv) continue;
+    if (!ri.active || g >= hkv) {
+      // tagged output: the readers wait for every row, so an inactive row
+      // still writes (zeros) once per KV head
+      if (tg.out != 0u && c == 0 && g < hkv)
+        for (int e = tid; e < G * HD; e += NT)
+          tag_store(d.attn_t + static_cast<size_t>(r) * hq * HD + g * G * HD + e, 0.f, tg.out);
+      continue;
+    }
     const int t0 = c * chunk_tokens;
     const int t1 = min(L, t0 + chunk_tokens);
     const int npages = (t1 - t0 + kPageTokens - 1) / kPageTokens;
@@ -153,10 +183,8 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     if (fuse_append) {
       if (warp < G) {
         const int h = g * G + warp;
-        const float* src = d.qkv + static_cast<size_t>(r) * d.qkv_dim + h * HD;
         float v[EPL];
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) v[j] = ldf(src + lane * EPL + j);
+        act_load<EPL>(d.qkv, d.qkv_t, static_cast<size_t>(r) * d.qkv_dim + h * HD + lane * EPL, tg.in, v, d);
         head_norm_rope<EPL>(v, q_norm, d.eps, ri.pos, d, lane);
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
@@ -165,13 +193,10 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
         }
       }
       if (warp == (G % NW) && newest) {
-        const float* base = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
+        const size_t base = static_cast<size_t>(r) * d.qkv_dim;
         float kv[EPL], vv[EPL];
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-          kv[j] = ldf(base + hq * HD + g * HD + lane * EPL + j);
-          vv[j] = ldf(base + hq * HD + hkv * HD + g * HD + lane * EPL + j);
-        }
+        act_load<EPL>(d.qkv, d.qkv_t, base + hq * HD + g * HD + lane * EPL, tg.in, kv, d);
+        act_load<EPL>(d.qkv, d.qkv_t, base + hq * HD + hkv * HD + g * HD + lane * EPL, tg.in, vv, d);
         head_norm_rope<EPL>(kv, k_norm, d.eps, ri.pos, d, lane);
         const int pg = ldi(d.page_table + static_cast<size_t>(ri.slot) * d.pages_per_seq + ri.pos / kPageTokens);
         uint16_t* kd = d.kv_pool + (((static_cast<size_t>(pg) * d.n_layer + layer) * 2 + 0) * hkv + g) *
@@ -278,14 +303,14 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
 #pragma unroll
     for (int h = 0; h < G; ++h) sm.ored[vpart][h][vdim] = o[h];
     csync<NT>();
-    float* attn = d.attn + static_cast<size_t>(r) * hq * HD + g * G * HD;
+    const size_t attn_off = static_cast<size_t>(r) * hq * HD + g * G * HD;
     if (nch == 1) {
       for (int e = tid; e < G * HD; e += NT) {
         const int h = e / HD, dd = e % HD;
         float t = 0.f;
 #pragma unroll
         for (int p = 0; p < PARTS; ++p) t += sm.ored[p][h][dd];
-        attn[h * HD + dd] = t / sm.lsm[h];
+        act_store(d.attn, d.attn_t, attn_off + h * HD + dd, tg.out, t / sm.lsm[h]);
       }
       csync<NT>();
       continue;
@@ -306,7 +331,15 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     csync<NT>();
     if (tid == 0) {
       const uint32_t old = atomic_add_acq_rel_gpu(&d.arrive[r * hkv + g], 1u);
-      sm.s_last = (old == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
+      int last = 0;
+      if (old == static_cast<uint32_t>(nch - 1)) {
+        // the counter is reset before any output of this (row, head) is
+        // written: whoever uses it next (the next layer) reads that output
+        // first, directly or through later ops
+        const uint32_t prev = atomicExch(&d.arrive[r * hkv + g], 0u);
+        last = prev == 0xFFFFFFFFu ? 2 : 1;
+      }
+      sm.s_last = last;
     }
     csync<NT>();
     if (sm.s_last) {
@@ -323,9 +356,8 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
           Ls += ldf(q + HD + 1) * f;
           Os += ldf(q + dd) * f;
         }
-        attn[h * HD + dd] = Os / Ls;
+        act_store(d.attn, d.attn_t, attn_off + h * HD + dd, tg.out, Os / Ls);
       }
-      if (tid == 0) d.arrive[r * hkv + g] = 0u;
     }
     csync<NT>();
   }
@@ -347,27 +379,26 @@ struct FastAttnSmem {
 
 template <int EPL, int G, int NT>
 DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const uint16_t* q_norm,
-                         const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm) {
+                         const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm, OpTags tg = OpTags{0u, 0u}) {
   constexpr int HD = EPL * 32;
   static_assert(G <= NT / 32 && NT >= 64, "one warp per query head plus a K/V warp");
   const int r = unit / d.Hkv, g = unit % d.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = d.Hq, hkv = d.Hkv, N = d.N;
-  const float* qkv = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
+  const size_t qkv = static_cast<size_t>(r) * d.qkv_dim;
   float* kb = d.fast_kv + (((static_cast<size_t>(r) * d.fast_n_layer + layer) * 2 + 0) * hkv + g) * N * HD;
   float* vb = kb + static_cast<size_t>(hkv) * N * HD;
   if (warp == 0) {
-    float kv[EPL];
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) kv[j] = ldf(qkv + hq * HD + g * HD + lane * EPL + j);
+    float kv[EPL], vv[EPL];
+    act_load<EPL>(d.qkv, d.qkv_t, qkv + hq * HD + g * HD + lane * EPL, tg.in, kv, d);
+    act_load<EPL>(d.qkv, d.qkv_t, qkv + hq * HD + hkv * HD + g * HD + lane * EPL, tg.in, vv, d);
     head_norm_rope<EPL>(kv, k_norm, d.eps, pos, d, lane);
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      const float vv = ldf(qkv + hq * HD + hkv * HD + g * HD + lane * EPL + j);
       kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
-      vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv;
+      vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv[j];
       sm.ks[pos][lane * EPL + j] = kv[j];
-      sm.vs[pos][lane * EPL + j] = vv;
+      sm.vs[pos][lane * EPL + j] = vv[j];
     }
   } else {
     for (int e = threadIdx.x - 32; e < pos * HD; e += NT - 32) {
@@ -379,8 +410,7 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
   if (warp < G) {
     const int h = g * G + warp;
     float q[EPL];
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) q[j] = ldf(qkv + h * HD + lane * EPL + j);
+    act_load<EPL>(d.qkv, d.qkv_t, qkv + h * HD + lane * EPL, tg.in, q, d);
     head_norm_rope<EPL>(q, q_norm, d.eps, pos, d, lane);
     const float scale = 1.0f / sqrtf(static_cast<float>(HD));
     float s[kMaxCodebooks];
@@ -409,9 +439,9 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
         for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, sm.vs[t][lane * EPL + j], o[j]);
       }
     }
-    float* dst = d.attn + static_cast<size_t>(r) * hq * HD + h * HD;
+    const size_t dst = static_cast<size_t>(r) * hq * HD + h * HD;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) dst[lane * EPL + j] = o[j] / l;
+    for (int j = 0; j < EPL; ++j) act_store(d.attn, d.attn_t, dst + lane * EPL + j, tg.out, o[j] / l);
   }
   csync<NT>();   // shared buffers are reused by the next unit
 }
@@ -646,17 +676,39 @@ DEVI int samp_draw(const float (&z)[EPT], const unsigned long long (&key)[EPT], 
 }
 
 // Loads the candidates' logits and keys into registers; returns zmax.
+// With tag != 0 the logits are tagged words at tsrc (all loads are issued
+// before the first tag is checked).
 template <int NT, int EPT>
 DEVI float samp_load(const float* src, const Cands& c, float (&z)[EPT], unsigned long long (&key)[EPT],
-                     SampSmem<NT>& sm) {
+                     SampSmem<NT>& sm, const uint64_t* tsrc = nullptr, uint32_t tag = 0u,
+                     const DevPtrs* d = nullptr) {
+  static_assert(EPT <= 32, "one bit per candidate slot");
   float zm = -INFINITY;
+  uint32_t late = 0;   // tagged: words that did not carry the tag yet
 #pragma unroll
   for (int e = 0; e < EPT; ++e) {
     const int i = threadIdx.x + e * NT;
     z[e] = -INFINITY;
+    if (i < c.n) {
+      if (tag != 0u) {
+        const uint64_t w = tag_load(tsrc + i);
+        z[e] = tag_val(w);
+        late |= (tag_of(w) != tag ? 1u : 0u) << e;
+      } else {
+        z[e] = ldf(src + i);
+      }
+    }
+  }
+  if (late != 0u) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if ((late >> e) & 1u) z[e] = tag_wait1(tsrc + threadIdx.x + e * NT, tag, d->err, d->wait_limit_ns);
+  }
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = threadIdx.x + e * NT;
     key[e] = 0;
     if (i < c.n) {
-      z[e] = ldf(src + i);
       zm = fmaxf(zm, z[e]);
       key[e] = (static_cast<unsigned long long>(ord_f32(z[e])) << 32) |
                static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(cand_id(c, i)));
@@ -667,8 +719,23 @@ DEVI float samp_load(const float* src, const Cands& c, float (&z)[EPT], unsigned
 
 // q0 of one row: normal draw, repetition-aware resample, commit, and the
 // inputs of fast passes 0 and 1.
+// Fast-pass inputs written by the samplers: pass p of batch row `row`.
+DEVI size_t fin_plain_off(int p, int row, int D) {
+  return (static_cast<size_t>(p & 1) * kMaxRows + row) * D;
+}
+DEVI size_t fin_tagged_off(int p, int row, int D) {
+  return (static_cast<size_t>(p) * kTaggedRows + row) * D;
+}
 template <int NT>
-DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT>& sm) {
+DEVI void fin_zero(const DevPtrs& d, int p, int row, uint32_t tag) {
+  if (tag == 0u) return;   // plain buffers: nothing waits for an inactive row
+  uint64_t* f = d.fin_t + fin_tagged_off(p, row, d.D);
+  for (int k = threadIdx.x; k < d.D; k += NT) tag_store(f + k, 0.f, tag);
+}
+
+template <int NT>
+DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT>& sm,
+                        OpTags tg = OpTags{0u, 0u}) {
   constexpr int EPT = (kMaxCands + NT - 1) / NT;
   const int tid = threadIdx.x;
   const RowInfo ri = ld_row(&d.rows[row]);
@@ -685,6 +752,8 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
       d.commit_map[row] = -1;
     }
     for (int k = tid; k < N; k += NT) io.codes_out[row * N + k] = -1;
+    fin_zero<NT>(d, 0, row, tg.out);
+    fin_zero<NT>(d, 1, row, tg.out);
     csync<NT>();
     return;
   }
@@ -733,6 +802,8 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
   const int commit = sm.s_commit;
   if (!sm.s_active) {
     for (int k = tid; k < N; k += NT) io.codes_out[row * N + k] = -1;
+    fin_zero<NT>(d, 0, row, tg.out);
+    fin_zero<NT>(d, 1, row, tg.out);
     csync<NT>();
     return;
   }
@@ -742,32 +813,41 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
   // embedding clamped to its rows (a no-op when n_sem == fast_vocab).
   const int D = d.D;
   const int e0 = min(commit, d.Cf - 1);
-  float* f0 = d.fin + static_cast<size_t>(row) * D;
-  float* f1 = d.fin + (static_cast<size_t>(kMaxRows) + row) * D;
   const float* hl = d.h_last + static_cast<size_t>(slot) * D;
   const uint16_t* er = io.fast_emb + static_cast<size_t>(e0) * D;
   for (int k = tid; k < D; k += NT) {
-    f0[k] = ldf(hl + k);
-    f1[k] = bf16bits_to_f32(er[k]);
+    act_store(d.fin, d.fin_t, (tg.out ? fin_tagged_off(0, row, D) : fin_plain_off(0, row, D)) + k, tg.out,
+              ldf(hl + k));
+    act_store(d.fin, d.fin_t, (tg.out ? fin_tagged_off(1, row, D) : fin_plain_off(1, row, D)) + k, tg.out,
+              bf16bits_to_f32(er[k]));
   }
   csync<NT>();
 }
 
 // q_k (k >= 1) of one row from the fast head's logits, and the input of pass k+1.
 template <int NT>
-DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, SampSmem<NT>& sm) {
+DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, SampSmem<NT>& sm,
+                          OpTags tg = OpTags{0u, 0u}) {
   constexpr int EPT = (kMaxCands + NT - 1) / NT;
   const int tid = threadIdx.x;
   const int N = d.N, Cf = d.Cf;
-  const float* zs = d.logits + static_cast<size_t>(row) * d.logit_ld;
-  if (io.fast_logits_out)
-    for (int i = tid; i < Cf; i += NT)
-      io.fast_logits_out[(static_cast<size_t>(row) * (N - 1) + (k - 1)) * Cf + i] = ldf(zs + i);
-  if (!ldi(&d.rows[row].active)) return;
+  const size_t zoff = static_cast<size_t>(row) * d.logit_ld;
   const Cands c{Cf, Cf, 0, -1};
   float z[EPT];
   unsigned long long key[EPT];
-  const float zmax = samp_load<NT, EPT>(zs, c, z, key, sm);
+  const float zmax = samp_load<NT, EPT>(d.logits + zoff, c, z, key, sm, d.logits_t + zoff, tg.in, &d);
+  if (io.fast_logits_out) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = tid + e * NT;
+      if (i < Cf) io.fast_logits_out[(static_cast<size_t>(row) * (N - 1) + (k - 1)) * Cf + i] = z[e];
+    }
+  }
+  if (!ldi(&d.rows[row].active)) {
+    if (k + 1 < N) fin_zero<NT>(d, k + 1, row, tg.out);
+    csync<NT>();
+    return;
+  }
   const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
   const int draw = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u[k + 1], sm);
   if (tid == 0) {
@@ -784,9 +864,9 @@ DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, Sa
   csync<NT>();
   if (k + 1 < N) {
     const int D = d.D;
-    float* f = d.fin + (static_cast<size_t>((k + 1) & 1) * kMaxRows + row) * D;
+    const size_t f = tg.out ? fin_tagged_off(k + 1, row, D) : fin_plain_off(k + 1, row, D);
     const uint16_t* er = io.fast_emb + static_cast<size_t>(sm.s_commit) * D;
-    for (int j = tid; j < D; j += NT) f[j] = bf16bits_to_f32(er[j]);
+    for (int j = tid; j < D; j += NT) act_store(d.fin, d.fin_t, f + j, tg.out, bf16bits_to_f32(er[j]));
   }
   csync<NT>();
 }
@@ -799,9 +879,14 @@ DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, Sa
 // with E^(k) the block of the fusion table that starts at row
 // n_sem + (k-1) * fast_vocab (row 0 for k = 0).
 template <int NT>
-DEVI void fusion_row(const DevPtrs& d, int row, const uint16_t* tok_emb, const uint16_t* fusion) {
-  if (!ldi(&d.rows[row].active)) return;
+DEVI void fusion_row(const DevPtrs& d, int row, const uint16_t* tok_emb, const uint16_t* fusion,
+                     OpTags tg = OpTags{0u, 0u}) {
   const int D = d.D, N = d.N;
+  if (!ldi(&d.rows[row].active)) {
+    if (tg.out != 0u)
+      for (int k = threadIdx.x; k < D; k += NT) tag_store(d.xs_t + static_cast<size_t>(row) * D + k, 0.f, tg.out);
+    return;
+  }
   int q[kMaxCodebooks];
   bool bad = false;
   for (int k = 0; k < N; ++k) {
@@ -811,6 +896,8 @@ DEVI void fusion_row(const DevPtrs& d, int row, const uint16_t* tok_emb, const u
   }
   if (bad) {
     if (threadIdx.x == 0) raise_error(d.err, DEV_ERR_BAD_INDEX);
+    if (tg.out != 0u)
+      for (int k = threadIdx.x; k < D; k += NT) tag_store(d.xs_t + static_cast<size_t>(row) * D + k, 0.f, tg.out);
     return;
   }
   const float scale = 1.0f / sqrtf(static_cast<float>(N + 1));
@@ -832,9 +919,15 @@ DEVI void fusion_row(const DevPtrs& d, int row, const uint16_t* tok_emb, const u
       acc[0] += bf16lo(w.x); acc[1] += bf16hi(w.x); acc[2] += bf16lo(w.y); acc[3] += bf16hi(w.y);
       acc[4] += bf16lo(w.z); acc[5] += bf16hi(w.z); acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
     }
-    float4* dst = reinterpret_cast<float4*>(d.xs + static_cast<size_t>(row) * D + 8 * j);
-    dst[0] = make_float4(acc[0] * scale, acc[1] * scale, acc[2] * scale, acc[3] * scale);
-    dst[1] = make_float4(acc[4] * scale, acc[5] * scale, acc[6] * scale, acc[7] * scale);
+    if (tg.out != 0u) {
+      uint64_t* dst = d.xs_t + static_cast<size_t>(row) * D + 8 * j;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) tag_store2(dst + e, acc[e] * scale, acc[e + 1] * scale, tg.out);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(d.xs + static_cast<size_t>(row) * D + 8 * j);
+      dst[0] = make_float4(acc[0] * scale, acc[1] * scale, acc[2] * scale, acc[3] * scale);
+      dst[1] = make_float4(acc[4] * scale, acc[5] * scale, acc[6] * scale, acc[7] * scale);
+    }
   }
 }
 
