@@ -542,6 +542,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     h->epoch += 1;
     MegaParams mp{};
     mp.epoch = h->epoch;
+    mp.fkv_floats = 2 * c.n_codebooks * c.head_dim;
     mp.d = d;
     mp.ops = h->mega_ops[batch];
     mp.n_ops = h->mega_nops[batch];
@@ -758,10 +759,11 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
     // tagged work buffers of the persistent frame kernel, one region (cleared
     // together when the tag epoch wraps); every buffer starts on 64 bytes
     const size_t TR = kTaggedRows;
-    const size_t sizes[8] = {TR * d.qkv_dim, TR * c.n_head * c.head_dim, TR * c.ffn, TR * c.dim,
-                             TR * c.dim, TR * c.dim, kMaxCodebooks * TR * c.dim, TR * d.logit_ld};
-    size_t offs[8], total = 0;
-    for (int i = 0; i < 8; ++i) {
+    const size_t sizes[9] = {TR * d.qkv_dim, TR * c.n_head * c.head_dim, TR * c.ffn, TR * c.dim,
+                             TR * c.dim, TR * c.dim, kMaxCodebooks * TR * c.dim, TR * d.logit_ld,
+                             TR * c.n_kv_head * kMaxChunks * G * (c.head_dim + 2)};
+    size_t offs[9], total = 0;
+    for (int i = 0; i < 9; ++i) {
       offs[i] = total;
       total += (sizes[i] + 7) / 8 * 8;
     }
@@ -775,6 +777,7 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
     d.xs_t = h->tagged + offs[5];
     d.fin_t = h->tagged + offs[6];
     d.logits_t = h->tagged + offs[7];
+    d.part_t = h->tagged + offs[8];
   }
 #undef ALLOC
 

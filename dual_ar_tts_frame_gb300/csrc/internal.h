@@ -124,6 +124,7 @@ struct DevPtrs {
   uint64_t* xs_t;             // [kTaggedRows][D]
   uint64_t* fin_t;            // [kMaxCodebooks][kTaggedRows][D] input of fast pass p
   uint64_t* logits_t;         // [kTaggedRows][logit_ld]
+  uint64_t* part_t;           // split-KV partials [kTaggedRows][Hkv][kMaxChunks][G][hd+2]
 };
 constexpr int kTaggedRows = 2;   // batch rows of the persistent frame kernel
 constexpr int kTagOpBits = 12;   // low bits of an activation tag: index of the writing op

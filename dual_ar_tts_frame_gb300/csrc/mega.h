@@ -43,6 +43,7 @@ struct MegaParams {
   uint64_t* trace;          // optional: [n_sm][n_ops][2] global-timer stamps (op start, op end)
   uint64_t prefetch_bytes;  // weight bytes per CTA kept in flight into L2 beyond the ring
   uint32_t epoch;           // launch epoch of the activation tags (1 .. 2^20 - 1)
+  int fkv_floats;           // fast K/V per layer kept in shared memory: 2 * N * head_dim
 };
 
 // Launches the frame program as one cooperative kernel (grid = n_sm CTAs).

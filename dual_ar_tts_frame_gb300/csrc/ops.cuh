@@ -112,6 +112,7 @@ struct AttnSmem {
   float ored[PARTS][G][HD];
   float knew[HD], vnew[HD];
   float scl[G], msm[G], lsm[G];
+  float cm[kMaxChunks][G], cl[kMaxChunks][G];   // tagged combine: (m, l) of every chunk
   int s_last;
 };
 
@@ -315,6 +316,64 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
       csync<NT>();
       continue;
     }
+    if (tg.out != 0u) {
+      // Tagged partials: the unit of the last chunk combines them.  It waits
+      // only for units with smaller indices, and every CTA runs its units in
+      // increasing order, so the waits always end.
+      const size_t pbase = (static_cast<size_t>(r) * hkv + g) * kMaxChunks * G * (HD + 2);
+      uint64_t* pt = d.part_t + pbase + static_cast<size_t>(c) * G * (HD + 2);
+      for (int e = tid; e < G * HD; e += NT) {
+        const int h = e / HD, dd = e % HD;
+        float t = 0.f;
+#pragma unroll
+        for (int p = 0; p < PARTS; ++p) t += sm.ored[p][h][dd];
+        tag_store(pt + h * (HD + 2) + dd, t, tg.out);
+      }
+      if (tid < G) {
+        tag_store(pt + tid * (HD + 2) + HD, sm.msm[tid], tg.out);
+        tag_store(pt + tid * (HD + 2) + HD + 1, sm.lsm[tid], tg.out);
+      }
+      csync<NT>();
+      if (c != nch - 1) continue;
+      const uint64_t* pb = d.part_t + pbase;
+      for (int idx = tid; idx < nch * G; idx += NT) {
+        const int cc = idx / G, h = idx % G;
+        float ml[2];
+        tag_wait<2>(pb + static_cast<size_t>(cc * G + h) * (HD + 2) + HD, tg.out, ml, d.err, d.wait_limit_ns);
+        sm.cm[cc][h] = ml[0];
+        sm.cl[cc][h] = ml[1];
+      }
+      csync<NT>();
+      // same arithmetic and order as the last-arriver combine below
+      for (int e = tid; e < G * HD; e += NT) {
+        const int h = e / HD, dd = e % HD;
+        float M = -INFINITY;
+        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, sm.cm[cc][h]);
+        float Ls = 0.f, Os = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += 8) {
+          uint64_t w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            w[k] = c0 + k < nch ? tag_load(pb + static_cast<size_t>((c0 + k) * G + h) * (HD + 2) + dd) : 0ull;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int cc = c0 + k;
+            if (cc < nch) {
+              const float o = tag_of(w[k]) == tg.out
+                                  ? tag_val(w[k])
+                                  : tag_wait1(pb + static_cast<size_t>(cc * G + h) * (HD + 2) + dd, tg.out, d.err,
+                                              d.wait_limit_ns);
+              const float f = expf(sm.cm[cc][h] - M);
+              Ls += sm.cl[cc][h] * f;
+              Os += o * f;
+            }
+          }
+        }
+        tag_store(d.attn_t + attn_off + h * HD + dd, Os / Ls, tg.out);
+      }
+      csync<NT>();
+      continue;
+    }
     float* pw = d.part + ((static_cast<size_t>(r) * hkv + g) * kMaxChunks + c) * G * (HD + 2);
     for (int e = tid; e < G * HD; e += NT) {
       const int h = e / HD, dd = e % HD;
@@ -366,10 +425,10 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
 // ============================================================================
 // Fast-AR attention over the per-frame codebook cache (<= N positions)
 // ============================================================================
-// One unit per (row, KV head g): warp 0 computes the new position's K (norm
-// if configured, RoPE at the codebook index) and V and appends them; the K/V
-// of earlier positions (written by earlier passes of this frame) are staged
-// in shared memory; warp h < G then computes query head g*G+h.  [P2] "Two
+// One unit per (row, KV head g): warp G computes the new position's K (norm
+// if configured, RoPE at the codebook index) and V and appends them, while
+// warp h < G loads query head g*G+h; the K/V of earlier positions (written by
+// earlier passes of this frame) are read from shared memory.  [P2] "Two
 // autoregressions": the fast AR's KV cache is num_codebooks long and is
 // overwritten every frame.
 template <int HD>
@@ -379,39 +438,48 @@ struct FastAttnSmem {
 
 template <int EPL, int G, int NT>
 DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const uint16_t* q_norm,
-                         const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm, OpTags tg = OpTags{0u, 0u}) {
+                         const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm, OpTags tg = OpTags{0u, 0u},
+                         float* res = nullptr) {
+  // res (persistent frame kernel): this layer's K and V rows [2][N][HD], kept
+  // in shared memory for the whole frame by the one CTA that runs this unit;
+  // otherwise earlier positions come from the global fast cache
   constexpr int HD = EPL * 32;
-  static_assert(G <= NT / 32 && NT >= 64, "one warp per query head plus a K/V warp");
+  static_assert(G + 1 <= NT / 32, "one warp per query head plus a K/V warp");
   const int r = unit / d.Hkv, g = unit % d.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = d.Hq, hkv = d.Hkv, N = d.N;
   const size_t qkv = static_cast<size_t>(r) * d.qkv_dim;
   float* kb = d.fast_kv + (((static_cast<size_t>(r) * d.fast_n_layer + layer) * 2 + 0) * hkv + g) * N * HD;
   float* vb = kb + static_cast<size_t>(hkv) * N * HD;
-  if (warp == 0) {
+  float (*ks)[HD] = res ? reinterpret_cast<float (*)[HD]>(res) : sm.ks;
+  float (*vs)[HD] = res ? reinterpret_cast<float (*)[HD]>(res + static_cast<size_t>(N) * HD) : sm.vs;
+  if (res == nullptr)
+    for (int e = threadIdx.x; e < pos * HD; e += NT) {
+      ks[e / HD][e % HD] = ldf(kb + e);
+      vs[e / HD][e % HD] = ldf(vb + e);
+    }
+  float q[EPL];
+  if (warp < G) {
+    act_load<EPL>(d.qkv, d.qkv_t, qkv + (g * G + warp) * HD + lane * EPL, tg.in, q, d);
+    head_norm_rope<EPL>(q, q_norm, d.eps, pos, d, lane);
+  } else if (warp == G) {
     float kv[EPL], vv[EPL];
     act_load<EPL>(d.qkv, d.qkv_t, qkv + hq * HD + g * HD + lane * EPL, tg.in, kv, d);
     act_load<EPL>(d.qkv, d.qkv_t, qkv + hq * HD + hkv * HD + g * HD + lane * EPL, tg.in, vv, d);
     head_norm_rope<EPL>(kv, k_norm, d.eps, pos, d, lane);
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
-      vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv[j];
-      sm.ks[pos][lane * EPL + j] = kv[j];
-      sm.vs[pos][lane * EPL + j] = vv[j];
-    }
-  } else {
-    for (int e = threadIdx.x - 32; e < pos * HD; e += NT - 32) {
-      sm.ks[e / HD][e % HD] = ldf(kb + e);
-      sm.vs[e / HD][e % HD] = ldf(vb + e);
+      if (res == nullptr) {
+        kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
+        vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv[j];
+      }
+      ks[pos][lane * EPL + j] = kv[j];
+      vs[pos][lane * EPL + j] = vv[j];
     }
   }
   csync<NT>();
   if (warp < G) {
     const int h = g * G + warp;
-    float q[EPL];
-    act_load<EPL>(d.qkv, d.qkv_t, qkv + h * HD + lane * EPL, tg.in, q, d);
-    head_norm_rope<EPL>(q, q_norm, d.eps, pos, d, lane);
     const float scale = 1.0f / sqrtf(static_cast<float>(HD));
     float s[kMaxCodebooks];
     float m = -INFINITY;
@@ -421,7 +489,7 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
       if (t <= pos) {
         float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) a = fmaf(q[j], sm.ks[t][lane * EPL + j], a);
+        for (int j = 0; j < EPL; ++j) a = fmaf(q[j], ks[t][lane * EPL + j], a);
         s[t] = warp_sum(a) * scale;
         m = fmaxf(m, s[t]);
       }
@@ -436,7 +504,7 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
         const float p = expf(s[t] - m);
         l += p;
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, sm.vs[t][lane * EPL + j], o[j]);
+        for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, vs[t][lane * EPL + j], o[j]);
       }
     }
     const size_t dst = static_cast<size_t>(r) * hq * HD + h * HD;
@@ -456,18 +524,30 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
 // cut is the first candidate (in key order) whose inclusive cumulative mass
 // reaches ceil(top_p * Z); the draw is the first kept candidate whose
 // inclusive cumulative mass reaches floor(u * Zk) + 1, i.e. exceeds u * Zk.
-// Both are found by a most-significant-byte-first radix descent over the
-// keys with 256-bin mass histograms; lanes of a warp that hit the same bin
-// are combined (match + reduce) before one shared-memory atomic.  [P2] "Two
+// Both are found from one histogram of mass over kSampBins bins of
+// (zmax - z) / T (a bin index never increases with the key, so the bins
+// partition the key order): an inclusive scan over the bins locates the bin
+// holding a target, and only the candidates of that bin are ranked by key.
+// A bin with more than kBinCap candidates (near-equal logits) falls back to a
+// most-significant-byte-first radix descent over the keys.  [P2] "Two
 // autoregressions": sample(biased_logits, ...) for q0, unmasked
 // sample(logits, ...) for q1..q9.
 constexpr int kMaxCands = 4097;
 
+constexpr int kSampBins = 2048;
+constexpr int kBinCap = 512;
+// Candidates with (zmax - z) / T above ln(2^25) have zero mass and are never
+// selected; the bins cover [0, 17.5) of that distance.
+constexpr float kBinScale = static_cast<float>(kSampBins) / 17.5f;
+
 template <int NT>
 struct SampSmem {
   static constexpr int NW = NT / 32;
-  unsigned long long hmass[256];
-  unsigned int hcnt[256];
+  unsigned long long hmass[kSampBins];   // per-bin mass, then its inclusive scan
+  unsigned int hcnt[kSampBins];
+  unsigned long long lkey[kBinCap];      // candidates of the target bin
+  unsigned int lmass[kBinCap];
+  int nlist;
   unsigned long long red64[NW];
   float redf[NW];
   unsigned long long bc[4];
@@ -627,6 +707,116 @@ DEVI unsigned long long samp_select(const unsigned long long (&key)[EPT], const 
   return result;
 }
 
+// Bin of a candidate with positive mass (monotone: never increases with z).
+DEVI int samp_bin(float z, float zmax, float inv_t) {
+  const float t = (zmax - z) * inv_t * kBinScale;
+  return t < static_cast<float>(kSampBins - 1) ? static_cast<int>(t) : kSampBins - 1;
+}
+
+// Histogram of mass per bin, then its inclusive scan (hmass[b] = mass of
+// bins 0..b).  hcnt keeps the per-bin counts.
+template <int NT, int EPT>
+DEVI void samp_hist(const float (&z)[EPT], const uint32_t (&mass)[EPT], int n, float zmax, float inv_t,
+                    SampSmem<NT>& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int BPT = kSampBins / NT;   // bins per thread (contiguous)
+  static_assert(kSampBins % NT == 0 && BPT >= 1, "bins split evenly over the threads");
+  for (int b = tid; b < kSampBins; b += NT) {
+    sm.hmass[b] = 0;
+    sm.hcnt[b] = 0;
+  }
+  csync<NT>();
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = tid + e * NT;
+    if (i < n && mass[e] != 0u) {
+      const int b = samp_bin(z[e], zmax, inv_t);
+      atomicAdd(&sm.hmass[b], static_cast<unsigned long long>(mass[e]));
+      atomicAdd(&sm.hcnt[b], 1u);
+    }
+  }
+  csync<NT>();
+  unsigned long long c[BPT];
+  unsigned long long run = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    run += sm.hmass[tid * BPT + j];
+    c[j] = run;
+  }
+  unsigned long long incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm.red64[warp] = incl;
+  csync<NT>();
+  unsigned long long off = incl - run;
+  for (int w = 0; w < warp; ++w) off += sm.red64[w];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) sm.hmass[tid * BPT + j] = off + c[j];
+  csync<NT>();
+}
+
+// First key (descending) whose inclusive cumulative mass reaches target
+// (1 <= target <= total), using the scanned histogram; *incl_out is that
+// inclusive cumulative mass.
+template <int NT, int EPT>
+DEVI unsigned long long samp_resolve(const float (&z)[EPT], const unsigned long long (&key)[EPT],
+                                     const uint32_t (&mass)[EPT], int n, float zmax, float inv_t,
+                                     unsigned long long target, SampSmem<NT>& sm,
+                                     unsigned long long* incl_out, bool* radix) {
+  const int tid = threadIdx.x;
+  // the bin holding the target: excl(b) < target <= incl(b) (exactly one)
+  for (int b = tid; b < kSampBins; b += NT) {
+    const unsigned long long hi = sm.hmass[b];
+    const unsigned long long lo = b == 0 ? 0ull : sm.hmass[b - 1];
+    if (lo < target && target <= hi) {
+      sm.ibc[0] = b;
+      sm.bc[0] = lo;
+    }
+  }
+  if (tid == 0) sm.nlist = 0;
+  csync<NT>();
+  const int bin = sm.ibc[0];
+  const unsigned long long above = sm.bc[0];
+  const int cnt = static_cast<int>(sm.hcnt[bin]);
+  if (cnt > kBinCap) {
+    // near-equal logits crowd one bin: radix descent over all keys
+    unsigned long long ab, mk;
+    const unsigned long long k = samp_select<NT, EPT>(key, mass, n, target, sm, &ab, &mk);
+    *incl_out = ab + mk;
+    *radix = true;   // the descent reused the bin arrays
+    return k;
+  }
+  *radix = false;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = tid + e * NT;
+    if (i < n && mass[e] != 0u && samp_bin(z[e], zmax, inv_t) == bin) {
+      const int slot = atomicAdd(&sm.nlist, 1);
+      sm.lkey[slot] = key[e];
+      sm.lmass[slot] = mass[e];
+    }
+  }
+  csync<NT>();
+  for (int i = tid; i < cnt; i += NT) {
+    const unsigned long long ki = sm.lkey[i];
+    unsigned long long cum = above;
+    for (int j = 0; j < cnt; ++j)
+      if (sm.lkey[j] >= ki) cum += sm.lmass[j];
+    if (cum >= target && cum - sm.lmass[i] < target) {
+      sm.bc[1] = ki;
+      sm.bc[2] = cum;
+    }
+  }
+  csync<NT>();
+  *incl_out = sm.bc[2];
+  const unsigned long long k = sm.bc[1];
+  csync<NT>();
+  return k;
+}
+
 // One draw: returns the chosen candidate index.
 template <int NT, int EPT>
 DEVI int samp_draw(const float (&z)[EPT], const unsigned long long (&key)[EPT], const Cands& c,
@@ -665,13 +855,15 @@ DEVI int samp_draw(const float (&z)[EPT], const unsigned long long (&key)[EPT], 
     tc = t < 1.0 ? 1ull : static_cast<unsigned long long>(t);
     if (tc > Z) tc = Z;
   }
-  unsigned long long above, mk;
-  samp_select<NT, EPT>(key, mass, c.n, tc, sm, &above, &mk);
-  const unsigned long long zk = above + mk;
+  samp_hist<NT, EPT>(z, mass, c.n, zmax, inv_t, sm);
+  unsigned long long zk, zd;
+  bool radix = false;
+  samp_resolve<NT, EPT>(z, key, mass, c.n, zmax, inv_t, tc, sm, &zk, &radix);
   unsigned long long td =
       static_cast<unsigned long long>(floor(static_cast<double>(u) * static_cast<double>(zk))) + 1ull;
   if (td > zk) td = zk;
-  const unsigned long long kd = samp_select<NT, EPT>(key, mass, c.n, td, sm, &above, &mk);
+  if (radix) samp_hist<NT, EPT>(z, mass, c.n, zmax, inv_t, sm);
+  const unsigned long long kd = samp_resolve<NT, EPT>(z, key, mass, c.n, zmax, inv_t, td, sm, &zd, &radix);
   return key_to_index(c, kd);
 }
 
