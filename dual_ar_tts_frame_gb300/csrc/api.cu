@@ -46,10 +46,12 @@ struct dualar_handle {
   uint64_t* tagged = nullptr;    // the tagged work buffers (one region)
   size_t tagged_words = 0;
   uint32_t epoch = 0;            // tag epoch of the last persistent launch
-  uint64_t prefetch_bytes = 0;   // dualar_set_prefetch
+  uint64_t prefetch_bytes = 65536;   // dualar_set_prefetch
   uint64_t* trace = nullptr;     // dualar_set_trace
   int64_t trace_bytes = 0;
-  MegaOp* mega_ops[3] = {nullptr, nullptr, nullptr};   // programs for batch 1, 2
+  MegaOp* mega_ops[3] = {nullptr, nullptr, nullptr};
+  ProdOp* mega_prod[3] = {nullptr, nullptr, nullptr};   // GEMV ops of each program, for the producer
+  int mega_nprod[3] = {0, 0, 0};   // programs for batch 1, 2
   int mega_nops[3] = {0, 0, 0};
   bool mega_unsupported[3] = {false, false, false};
 };
@@ -427,12 +429,21 @@ int build_mega_program(dualar_handle* h, int nb) {
     h->mega_unsupported[nb] = true;   // op indices do not fit the tag
     return DUALAR_OK;
   }
+  std::vector<ProdOp> prod;
+  for (const MegaOp& o : ops)
+    if (o.type == MOP_GEMV) prod.push_back(ProdOp{o.g.w0, o.g.w1, o.g.n0, o.g.n1, o.g.K, o.g.mode});
   MegaOp* dev = nullptr;
   CUDA_TRY(h, cudaMalloc(&dev, ops.size() * sizeof(MegaOp)));
   h->allocs.push_back(dev);
   CUDA_TRY(h, cudaMemcpy(dev, ops.data(), ops.size() * sizeof(MegaOp), cudaMemcpyHostToDevice));
+  ProdOp* pdev = nullptr;
+  CUDA_TRY(h, cudaMalloc(&pdev, std::max<size_t>(prod.size(), 1) * sizeof(ProdOp)));
+  h->allocs.push_back(pdev);
+  CUDA_TRY(h, cudaMemcpy(pdev, prod.data(), prod.size() * sizeof(ProdOp), cudaMemcpyHostToDevice));
   h->mega_ops[nb] = dev;
   h->mega_nops[nb] = static_cast<int>(ops.size());
+  h->mega_prod[nb] = pdev;
+  h->mega_nprod[nb] = static_cast<int>(prod.size());
   return DUALAR_OK;
 }
 
@@ -546,6 +557,8 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     mp.d = d;
     mp.ops = h->mega_ops[batch];
     mp.n_ops = h->mega_nops[batch];
+    mp.prod = h->mega_prod[batch];
+    mp.n_prod = h->mega_nprod[batch];
     mp.nrows = batch;
     mp.units = units;
     mp.chunk = chunk;

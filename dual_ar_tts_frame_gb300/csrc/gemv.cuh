@@ -225,6 +225,7 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
   const uint32_t xtag = a.x_src >= 0 ? op_tag(epoch, a.x_src) : 0u;
   for (int j = tid; j < KV; j += NCT) {
+    // the gain is loaded before x is polled: the two round trips overlap
     float gw[8];
     if (norm) {
       const uint4 gv = *reinterpret_cast<const uint4*>(a.norm_w + 8 * j);

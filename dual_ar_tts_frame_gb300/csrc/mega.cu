@@ -43,7 +43,8 @@ struct MegaLayout {
   static constexpr size_t bars = 0;   // full[8], empty[8], attn[2]
   static constexpr size_t scratch = 256;
   static constexpr size_t pro = (scratch + sizeof(GemvScratch<NB>) + 15) & ~size_t(15);
-  static constexpr size_t uni = (pro + sizeof(GemvPro<NB>) + 127) & ~size_t(127);
+  static constexpr size_t opbuf = (pro + sizeof(GemvPro<NB>) + 15) & ~size_t(15);   // MegaOp[2]
+  static constexpr size_t uni = (opbuf + 2 * sizeof(MegaOp) + 127) & ~size_t(127);
   // union region: GEMV x rows | paged attention | fast attention | sampler
   __host__ __device__ static size_t union_bytes(int kmax) {
     size_t u = sizeof(float) * size_t(NB) * kmax;
@@ -92,37 +93,48 @@ DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64
 }
 
 // Position in the sequence of weight tiles of the frame program (all GEMV
-// ops, in order) for one CTA.
+// ops, in order) for one CTA.  The descriptor of the next GEMV is loaded one
+// op ahead, so moving to it costs no memory round trip.
 struct TileCursor {
-  const MegaOp* ops;
-  int n_ops, cta, ncta;
-  int i;
-  bool open;
+  const ProdOp* prod;
+  int n, cta, ncta;
+  int j;
+  ProdOp nxt;
   GemvArgs a;
   GemvGeo g;
   TileIter it;
-  __device__ TileCursor(const MegaOp* o, int n, int c, int nc)
-      : ops(o), n_ops(n), cta(c), ncta(nc), i(0), open(false), a(), g(), it(a, g) {}
+  __device__ static GemvArgs args_of(const ProdOp& q) {
+    GemvArgs a{};
+    a.w0 = q.w0;
+    a.w1 = q.w1;
+    a.n0 = q.n0;
+    a.n1 = q.n1;
+    a.K = q.K;
+    a.mode = q.mode;
+    return a;
+  }
+  __device__ TileCursor(const ProdOp* pr, int np, int c, int nc)
+      : prod(pr), n(np), cta(c), ncta(nc), j(0), nxt(), a(), g(), it(a, g) {
+    if (n > 0) {
+      a = args_of(prod[0]);
+      g = gemv_geo(a, cta, ncta);
+      it = TileIter(a, g);
+    }
+    if (n > 1) nxt = prod[1];
+  }
   __device__ bool next(const uint16_t*& src, uint32_t& bytes) {
-    while (i < n_ops) {
-      if (!open) {
-        if (ops[i].type != MOP_GEMV) {
-          ++i;
-          continue;
-        }
-        a = ops[i].g;
-        g = gemv_geo(a, cta, ncta);
-        it = TileIter(a, g);
-        open = true;
-      }
+    while (j < n) {
       int row0, rows, part;
       if (it.next(row0, rows, part)) {
         src = gemv_tile_src(a, row0, part);
         bytes = static_cast<uint32_t>(rows) * a.K * 2;
         return true;
       }
-      open = false;
-      ++i;
+      if (++j >= n) break;
+      a = args_of(nxt);
+      g = gemv_geo(a, cta, ncta);
+      it = TileIter(a, g);
+      if (j + 1 < n) nxt = prod[j + 1];
     }
     return false;
   }
@@ -144,6 +156,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + Lay::scratch);
   GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + Lay::pro);
   unsigned char* uni = smem + Lay::uni;
+  MegaOp* opb = reinterpret_cast<MegaOp*>(smem + Lay::opbuf);   // ops i and i+1 (slot i & 1)
+  constexpr int kOpChunks = static_cast<int>(sizeof(MegaOp) / 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x, ncta = gridDim.x;
   const DevPtrs& d = p.d;
@@ -158,6 +172,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  if (tid < kOpChunks && p.n_ops > 0)
+    reinterpret_cast<uint4*>(opb)[tid] = reinterpret_cast<const uint4*>(p.ops)[tid];
   __syncthreads();
 
   if (warp == kWarpsC) {
@@ -167,7 +183,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
     // keeps streaming while the consumers wait at a barrier, sample or attend.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      TileCursor lc(p.ops, p.n_ops, cta, ncta), pc(p.ops, p.n_ops, cta, ncta);
+      TileCursor lc(p.prod, p.n_prod, cta, ncta), pc(p.prod, p.n_prod, cta, ncta);
       uint64_t loaded = 0, prefetched = 0;
       const uint32_t* errp = d.err;
       uint32_t t = 0;
@@ -214,7 +230,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   const uint32_t ep = p.epoch;
   const int hkv = d.Hkv;
   for (int i = 0; i < p.n_ops; ++i) {
-    const MegaOp& op = p.ops[i];
+    const MegaOp& op = opb[i & 1];
+    // the next op's descriptor arrives while this op runs
+    const bool fetch = i + 1 < p.n_ops && tid < kOpChunks;
+    if (fetch) {
+      cp_async16(reinterpret_cast<uint4*>(&opb[(i + 1) & 1]) + tid, reinterpret_cast<const uint4*>(p.ops + i + 1) + tid);
+      cp_async_commit();
+    }
     uint64_t* tr = p.trace ? p.trace + (static_cast<size_t>(cta) * p.n_ops + i) * 2 : nullptr;
     if (tr && tid == 0) tr[0] = global_timer_ns();
     switch (op.type) {
@@ -224,6 +246,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
         if (!gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep)) {
           // the ring protocol is broken: stop streaming (the error word is set)
+          if (fetch) cp_async_wait_all();
           return;
         }
         break;
@@ -262,6 +285,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         break;
     }
     if (tr && tid == 0) tr[1] = global_timer_ns();
+    if (fetch) cp_async_wait_all();
     if (i + 1 < p.n_ops) {
       if (i == 0) grid_barrier(p.bar, static_cast<uint32_t>(ncta) + p.bar_extra, d.err, d.wait_limit_ns);
       else named_barrier(1, kMegaNCT);   // shared memory is reused by the next op

@@ -18,7 +18,8 @@ enum MegaOpType : int {
 };
 
 // One op of the frame program (device memory, built once per batch size).
-struct MegaOp {
+// Consumers copy the next op into shared memory in 16-byte pieces.
+struct alignas(16) MegaOp {
   int type;
   int layer;
   int pos;     // fast attention: codebook position; fast sample: codebook k
@@ -28,10 +29,22 @@ struct MegaOp {
   GemvArgs g;  // MOP_GEMV
 };
 
+static_assert(sizeof(MegaOp) % 16 == 0, "copied in 16-byte pieces");
+
+// What the producer needs of one GEMV of the program (GEMV ops only, in
+// program order): the weight matrices and their shape.
+struct ProdOp {
+  const uint16_t* w0;
+  const uint16_t* w1;
+  int n0, n1, K, mode;
+};
+
 struct MegaParams {
   DevPtrs d;
   const MegaOp* ops;
   int n_ops;
+  const ProdOp* prod;       // the GEMV ops of the program, for the producer
+  int n_prod;
   int nrows;
   int units, chunk;         // paged-attention work list of this frame
   int kmax;                 // largest GEMV K (shared-memory x rows)

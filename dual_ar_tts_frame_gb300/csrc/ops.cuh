@@ -552,6 +552,7 @@ struct SampSmem {
   float redf[NW];
   unsigned long long bc[4];
   int ibc[4];
+  int hist[kRasRing];   // q0: the slot's RAS history ring
   int s_commit, s_active;
 };
 
@@ -933,10 +934,28 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
   const RowInfo ri = ld_row(&d.rows[row]);
   const int slot = ri.slot;
   const int ns = d.n_sem, N = d.N;
+  // the slot's state, loaded once and in parallel: finished flag, RAS
+  // history length and ring
+  if (tid == 0) {
+    sm.ibc[2] = ldi(d.finished + slot);
+    sm.ibc[3] = ldi(d.hist_n + slot);
+  } else if (tid >= 32 && tid < 32 + kRasRing) {
+    sm.hist[tid - 32] = ldi(d.hist + slot * kRasRing + (tid - 32));
+  }
   const float* zsrc = d.z_last + static_cast<size_t>(slot) * (ns + 1);
-  if (io.slow_logits_out)
-    for (int i = tid; i < ns + 1; i += NT) io.slow_logits_out[static_cast<size_t>(row) * (ns + 1) + i] = ldf(zsrc + i);
-  if (ldi(d.finished + slot)) {
+  // [P2] "Two autoregressions": the bias keeps the semantic ids and <|im_end|>.
+  const Cands c{ns + (io.sp.allow_eos ? 1 : 0), ns, d.sem_begin, d.im_end};
+  float z[EPT];
+  unsigned long long key[EPT];
+  const float zmax = samp_load<NT, EPT>(zsrc, c, z, key, sm);   // (its block reduction orders the state loads)
+  if (io.slow_logits_out) {
+    float* so = io.slow_logits_out + static_cast<size_t>(row) * (ns + 1);
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (tid + e * NT < c.n) so[tid + e * NT] = z[e];
+    if (c.n < ns + 1 && tid == 0) so[ns] = ldf(zsrc + ns);
+  }
+  if (sm.ibc[2]) {
     // a finished slot stays finished: no codes, no state change
     if (tid == 0) {
       io.status_out[row] = 2;
@@ -949,23 +968,18 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
     csync<NT>();
     return;
   }
-  // [P2] "Two autoregressions": the bias keeps the semantic ids and <|im_end|>.
-  const Cands c{ns + (io.sp.allow_eos ? 1 : 0), ns, d.sem_begin, d.im_end};
-  float z[EPT];
-  unsigned long long key[EPT];
-  const float zmax = samp_load<NT, EPT>(zsrc, c, z, key, sm);
   const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
   const int normal = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u[0], sm);
   // [P2] "Two autoregressions": a second draw at temperature 1.0, top-p 0.9,
   // used when the normal draw repeats a semantic token of the last 10 frames.
   const int ras = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.ras_temperature, io.sp.ras_top_p, u[1], sm);
   if (tid == 0) {
-    const int hn = ldi(d.hist_n + slot);
+    const int hn = sm.ibc[3];
     const int w = min(io.sp.ras_win, hn);
     bool repeat = false;
     if (normal != ns)
       for (int j = 0; j < w; ++j)
-        if (ldi(d.hist + slot * kRasRing + ((hn - 1 - j) % kRasRing)) == normal) repeat = true;
+        if (sm.hist[(hn - 1 - j) % kRasRing] == normal) repeat = true;
     const int chosen = (io.sp.ras_win > 0 && repeat) ? ras : normal;
     const int commit = io.forced ? io.forced[static_cast<size_t>(row) * io.ldf] : chosen;
     if (io.draws_out) {

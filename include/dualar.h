@@ -258,8 +258,10 @@ int32_t dualar_last_launch_count(const dualar_handle* h);
 int dualar_set_persistent(dualar_handle* h, int32_t enable);
 
 /* Persistent frame kernel: weight bytes per SM that its producer keeps in
- * flight into L2 ahead of the shared-memory ring (default 0: off; on GB300
- * the extra prefetch requests cost more than they hide).  A tuning knob; results do not depend on it. */
+ * flight into L2 ahead of the shared-memory ring while the ring is full
+ * (default 65536; on GB300 64 KiB hides part of the refill at op boundaries,
+ * 128 KiB and more cost more than they hide; 0 turns it off).  A tuning knob;
+ * results do not depend on it. */
 int dualar_set_prefetch(dualar_handle* h, uint64_t bytes_per_sm);
 
 /* Test hook for the failure path of the persistent kernel's grid barrier:
