@@ -34,7 +34,7 @@ DEVI uint64_t global_timer_ns() {
 // carry the tag it expects; no grid-wide barrier and no fence is needed
 // between the writer and the reader.  A tag is (launch epoch << 12) | index
 // of the writing op, never 0.
-constexpr uint64_t kAbortCheckNs = 20000;   // waits look at the error word after this long
+constexpr uint64_t kAbortCheckNs = 10000;   // how often a long wait looks at the error word
 
 DEVI uint32_t op_tag(uint32_t epoch, int op) { return (epoch << kTagOpBits) | static_cast<uint32_t>(op); }
 DEVI uint64_t tag_pack(float v, uint32_t tag) {
@@ -81,6 +81,7 @@ DEVI bool tag_wait(const uint64_t* p, uint32_t tag, float (&v)[n], uint32_t* err
   for (int q = 0; q < n; ++q) ok = ok && tag_of(w[q]) == tag;
   if (!ok) {
     const uint64_t t0 = global_timer_ns();
+    uint64_t next_chk = kAbortCheckNs;
     while (true) {
       ok = true;
 #pragma unroll
@@ -90,9 +91,10 @@ DEVI bool tag_wait(const uint64_t* p, uint32_t tag, float (&v)[n], uint32_t* err
       }
       if (ok) break;
       const uint64_t dt = global_timer_ns() - t0;
-      if (dt > kAbortCheckNs &&
-          (*reinterpret_cast<const volatile uint32_t*>(err) & (DEV_ERR_GRID_TIMEOUT | DEV_ERR_MBAR_TIMEOUT))) {
-        break;
+      if (dt > next_chk) {
+        // another wait gave up: give up too (looked at every kAbortCheckNs)
+        next_chk = dt + kAbortCheckNs;
+        if (*reinterpret_cast<const volatile uint32_t*>(err) & (DEV_ERR_GRID_TIMEOUT | DEV_ERR_MBAR_TIMEOUT)) break;
       }
       if (dt > limit_ns) {
         raise_error(err, DEV_ERR_GRID_TIMEOUT);

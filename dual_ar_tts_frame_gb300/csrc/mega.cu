@@ -36,6 +36,11 @@ namespace dualar {
 constexpr int kMegaNCT = kWarpsC * 32;   // consumer threads
 constexpr int kMegaMaxStages = 3;   // measured: a 4th stage does not help
 constexpr size_t kMegaSmemLimit = 227 * 1024;
+// producer timing, in SM cycles (about 2 GHz)
+constexpr long long kIdleCycles = 3000;        // a wait this long: the consumers are not streaming
+constexpr long long kTileCycles = 1600;        // one 40 KB tile per SM at its share of HBM bandwidth
+constexpr long long kAbortCheckCycles = 20000; // how often a long wait looks at the error word
+constexpr uint64_t kIdlePrefetchBytes = 512 * 1024;   // prefetch window growth while the consumers idle
 
 template <int NB, int HD, int G>
 struct MegaLayout {
@@ -80,9 +85,14 @@ DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64
     const volatile uint32_t* ev = err;
     if (ld_acquire_gpu(counter) < target) {
       const uint64_t t0 = global_timer_ns();
+      uint64_t next_chk = kAbortCheckNs;
       while (ld_acquire_gpu(counter) < target) {
-        if (*ev & (DEV_ERR_GRID_TIMEOUT | DEV_ERR_MBAR_TIMEOUT)) break;   // another CTA gave up
-        if (global_timer_ns() - t0 > limit_ns) {
+        const uint64_t dt = global_timer_ns() - t0;
+        if (dt > next_chk) {
+          next_chk = dt + kAbortCheckNs;
+          if (*ev & (DEV_ERR_GRID_TIMEOUT | DEV_ERR_MBAR_TIMEOUT)) break;   // another CTA gave up
+        }
+        if (dt > limit_ns) {
           raise_error(err, DEV_ERR_GRID_TIMEOUT);
           break;
         }
@@ -195,20 +205,46 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         if (t >= static_cast<uint32_t>(ring.stages)) {
           const uint32_t parity = ((t / ring.stages) - 1) & 1;
           if (!mbar_try_wait(&ring.empty[s], parity)) {
-            // ring full: run the L2 prefetch ahead, then wait
-            const uint16_t* ps;
-            uint32_t pb;
-            while (prefetched < loaded + p.prefetch_bytes && pc.next(ps, pb)) {
-              if (prefetched + pb > loaded + bytes) bulk_prefetch_l2(ps, pb);
-              prefetched += pb;
+            // Ring full: keep the next p.prefetch_bytes of tiles beyond the
+            // ring in flight into L2.  A wait longer than a tile interval
+            // means the consumers are not streaming (they wait for
+            // activations, attend or sample): the window then grows by one
+            // tile per tile interval, up to kIdlePrefetchBytes more, so HBM
+            // keeps working.
+            {
+              const uint16_t* ps;
+              uint32_t pb;
+              while (prefetched < loaded + p.prefetch_bytes && pc.next(ps, pb)) {
+                if (prefetched + pb > loaded + bytes) bulk_prefetch_l2(ps, pb);
+                prefetched += pb;
+              }
             }
-            const uint64_t t0 = global_timer_ns();
+            const long long c0 = clock64();
+            long long next_pf = c0 + kIdleCycles, next_chk = c0 + kAbortCheckCycles;
+            const uint64_t g0 = global_timer_ns();
             while (!mbar_try_wait(&ring.empty[s], parity)) {
-              if (*reinterpret_cast<const volatile uint32_t*>(errp) ||
-                  global_timer_ns() - t0 > d.wait_limit_ns) {
-                raise_error(d.err, DEV_ERR_MBAR_TIMEOUT);
-                ok = false;
-                break;
+              const long long now = clock64();
+              if (now >= next_pf) {
+                next_pf = now + kTileCycles;
+                const uint16_t* ps;
+                uint32_t pb;
+                bool issued = false;
+                while (!issued && prefetched < loaded + p.prefetch_bytes + kIdlePrefetchBytes && pc.next(ps, pb)) {
+                  if (prefetched + pb > loaded + bytes) {
+                    bulk_prefetch_l2(ps, pb);
+                    issued = true;
+                  }
+                  prefetched += pb;
+                }
+              }
+              if (now >= next_chk) {
+                next_chk = now + kAbortCheckCycles;
+                const uint64_t dt = global_timer_ns() - g0;
+                if (*reinterpret_cast<const volatile uint32_t*>(errp) || dt > d.wait_limit_ns) {
+                  raise_error(d.err, DEV_ERR_MBAR_TIMEOUT);
+                  ok = false;
+                  break;
+                }
               }
             }
             if (!ok) break;
