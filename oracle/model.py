@@ -28,10 +28,16 @@ its reason, in the design notes):
   * after prefill the sequence holds the final hidden state and restricted
     logits of its last prompt position; a frame samples q0 from them, runs
     the fast AR, fuses the codes and runs one slow position on the fused
-    vector.
+    vector;
+  * the slow AR's KV cache holds bf16 values: K (after QK-norm and RoPE) and
+    V are rounded to bf16 (nearest even) when appended, as in a model whose
+    checkpoint and serving are all bf16 ([P2] "Two autoregressions", the fact
+    table: all parameters BF16; "Streaming: whose numbers": the model runs
+    on bf16 tables).  The fast AR's per-frame cache stays float32.
 
 Precision: every activation is float32; weights are bf16 widened exactly to
-float32; the KV cache is float32; sampling probabilities are float64.
+float32; the slow KV cache holds bf16 values (widened to float32), the fast
+KV cache is float32; sampling probabilities are float64.
 """
 from __future__ import annotations
 
@@ -161,13 +167,20 @@ class Weights:
 # One transformer block over Tq new rows, with a contiguous KV cache
 # --------------------------------------------------------------------------
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bf16 (ties to even), as float32."""
+    return bf16_bits_to_f32(f32_to_bf16_bits(np.asarray(x, np.float32)))
+
+
 def block(cfg: DualARConfig, w: LayerW, h: np.ndarray, pos0: int,
           kcache: np.ndarray, vcache: np.ndarray, cos, sin,
-          qk_norm: bool) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+          qk_norm: bool, kv_bf16: bool = False) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """Pre-norm block: h += Wo attn(RoPE(QKnorm(q,k)), v); h += down(SiLU(gate) * up).
 
     h: [Tq, D] rows at positions pos0..pos0+Tq-1; kcache/vcache: [Tk, Hkv, hd]
-    holding positions 0..pos0-1.  Returns (h_out, kcache', vcache').
+    holding positions 0..pos0-1.  With kv_bf16 the new K and V rows are
+    rounded to bf16 before they join the cache (and the attention reads them
+    from it).  Returns (h_out, kcache', vcache').
     [P1] "Fast Transformer": TransformerBlock; [P2] "The slow AR is
     Qwen3-4B" (Qwen3 layer: GQA, SwiGLU FFN 9728, qk-norm)."""
     hd, hq, hkv = cfg.head_dim, cfg.n_head, cfg.n_kv_head
@@ -183,6 +196,8 @@ def block(cfg: DualARConfig, w: LayerW, h: np.ndarray, pos0: int,
     pos = np.arange(pos0, pos0 + tq)
     q = apply_rope(q, pos, cos, sin)
     k = apply_rope(k, pos, cos, sin)
+    if kv_bf16:
+        k, v = bf16_round(k), bf16_round(v)
     kc = np.concatenate([kcache, k.astype(np.float32)], axis=0)
     vc = np.concatenate([vcache, v.astype(np.float32)], axis=0)
     a = gqa_attention(q, kc, vc, hq // hkv, causal_offset=pos0)
@@ -250,7 +265,7 @@ class DualAROracle:
         h = np.asarray(x, np.float32)
         for i, lw in enumerate(self.w.slow):
             k, v = seq.kv[i]
-            h, k, v = block(cfg, lw, h, seq.pos, k, v, self.cos, self.sin, cfg.slow_qk_norm)
+            h, k, v = block(cfg, lw, h, seq.pos, k, v, self.cos, self.sin, cfg.slow_qk_norm, kv_bf16=True)
             seq.kv[i] = [k, v]
         seq.pos += h.shape[0]
         return rmsnorm(h, self.w.final_norm, cfg.norm_eps)
@@ -382,7 +397,8 @@ class DualAROracle:
         h = np.asarray(x_rows, np.float32)
         kv = empty_kv(cfg, cfg.n_layer)
         for i, lw in enumerate(self.w.slow):
-            h, _, _ = block(cfg, lw, h, 0, kv[i][0], kv[i][1], self.cos, self.sin, cfg.slow_qk_norm)
+            h, _, _ = block(cfg, lw, h, 0, kv[i][0], kv[i][1], self.cos, self.sin, cfg.slow_qk_norm,
+                            kv_bf16=True)
         return rmsnorm(h, self.w.final_norm, cfg.norm_eps)
 
     def fast_full_recompute(self, h_slow: np.ndarray, codes: np.ndarray) -> np.ndarray:

@@ -3,9 +3,10 @@
 Tolerances (teacher-forced logits): max |gpu - oracle| <= 0.05 and relative
 L2 <= 1e-2.  Sampled ids are compared through replay: the oracle follows the
 GPU's committed codes and each GPU draw must equal the oracle's draw from the
-oracle's logits unless the draw lies within 1e-3 (of the kept mass) of a CDF
-boundary or the top-p cut lies within 1e-3 of top_p; greedy draws must agree
-wherever the oracle's top-1/top-2 gap exceeds 0.1.
+oracle's logits unless the draw lies, within what the logit difference and
+the GPU sampler's fixed-point arithmetic can move, at a CDF boundary or at
+the top-p cut; greedy draws must agree wherever the oracle's top-1/top-2 gap
+exceeds 0.1.
 """
 from __future__ import annotations
 
@@ -13,9 +14,27 @@ import numpy as np
 
 MAX_ABS = 0.05
 REL_L2 = 1e-2
-CDF_DELTA = 1e-3
-CUT_DELTA = 1e-3
 GREEDY_GAP = 0.1
+# The GPU sampler's arithmetic: mass = round(expf((z - zmax) * (1/T)) * 2^24)
+# in fp32, exact integer sums, integer targets ceil(top_p * Z) and
+# floor(u * Zk) + 1.  One mass is off the exact exp(.) * 2^24 by at most
+# 0.5 (the rounding) plus MASS_REL of itself (the fp32 exponent argument,
+# |a| <= 17.5 where masses are non-zero, and expf).
+MASS_UNIT = float(2 ** 24)
+MASS_REL = 4e-6
+
+
+def arith_margins(r, temperature: float) -> tuple[float, float]:
+    """(cut, cdf) distances the fixed-point arithmetic can move the
+    normalised cumulative masses (the cut over all candidates, the draw over
+    the kept ones): relative errors twice (numerator and normaliser) plus
+    n/2 rounding units in each of the two sums and one unit for the target."""
+    zs = np.asarray(r.z_sorted, np.float64)
+    e = np.exp((zs - zs.max()) / temperature)
+    n = zs.size
+    z_all = MASS_UNIT * e.sum()
+    z_kept = MASS_UNIT * e[:r.kept].sum()
+    return 2 * MASS_REL + (n + 2) / z_all, 4 * MASS_REL + (n + 2) / z_kept
 
 
 def assert_logits_close(gpu, ref, what=""):
@@ -42,12 +61,14 @@ def draw_decidable(r, temperature: float, eps: float = 0.0) -> bool:
     boundaries by at most exp(4 eps / T) - 1 (the draw); adjacent candidates
     whose logits are within 2 eps may swap order.  The draw is decidable when
     the CDF boundaries, the cut, and the logit gaps next to the chosen
-    candidate and at the cut all clear those bounds (and the fixed 1e-3
-    margins)."""
+    candidate and at the cut all clear those bounds, and the boundaries and
+    the cut clear what the GPU's fixed-point arithmetic can move them
+    (arith_margins) on top."""
     if temperature <= 0:
         return r.gap > max(GREEDY_GAP, 2 * eps)
-    if not (r.cdf_margin > max(CDF_DELTA, np.expm1(4 * eps / temperature))
-            and r.cut_margin > max(CUT_DELTA, np.expm1(2 * eps / temperature))):
+    cut_a, cdf_a = arith_margins(r, temperature)
+    if not (r.cdf_margin > cdf_a + np.expm1(4 * eps / temperature)
+            and r.cut_margin > cut_a + np.expm1(2 * eps / temperature)):
         return False
     if eps > 0 and r.z_sorted is not None:
         zs = r.z_sorted

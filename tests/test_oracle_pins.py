@@ -227,6 +227,39 @@ def test_fast_incremental_equals_full_recompute(tiny_oracle):
     np.testing.assert_allclose(logits, full, rtol=1e-4, atol=1e-5)
 
 
+def _rne_8bit(x: np.ndarray) -> np.ndarray:
+    """Round to 8 significant bits, ties to even, via frexp (normal numbers)."""
+    m, e = np.frexp(np.asarray(x, np.float64))
+    return (np.rint(m * 256.0) / 256.0 * np.exp2(e)).astype(np.float32)
+
+
+def test_slow_kv_cache_holds_bf16_values(tiny_oracle):
+    """The slow cache stores K (after QK-norm and RoPE) and V rounded to bf16;
+    the first prompt position's K and V, recomputed here in fp32 from the
+    weights, round (ties to even) to exactly what the cache holds.  The fast
+    AR's per-frame cache is not rounded."""
+    o = tiny_oracle
+    cfg = TINY
+    prompt = g.make_prompt(cfg, 9, seed=31)
+    seq = o.prefill(prompt)
+    for k, v in seq.kv:
+        for t in (k, v):
+            assert not np.any(t.view(np.uint32) & np.uint32(0xFFFF))
+    lw = o.w.slow[0]
+    # the same product as the prefill's (all prompt rows at once), so the fp32
+    # values are bit-identical before rounding
+    u = om.rmsnorm(o.w.tok_emb[prompt], lw.attn_norm, cfg.norm_eps)
+    qkv = (u @ lw.wqkv.T)[0]
+    k0 = qkv[cfg.q_dim:cfg.q_dim + cfg.kv_dim].reshape(cfg.n_kv_head, cfg.head_dim)
+    v0 = qkv[cfg.q_dim + cfg.kv_dim:].reshape(cfg.n_kv_head, cfg.head_dim)
+    k0 = om.rmsnorm(k0, lw.k_norm, cfg.norm_eps)    # position 0: RoPE is the identity
+    np.testing.assert_array_equal(seq.kv[0][0][0], _rne_8bit(k0))
+    np.testing.assert_array_equal(seq.kv[0][1][0], _rne_8bit(v0))
+    kv = om.empty_kv(cfg, cfg.fast_n_layer)
+    o.fast_forward(np.ones(cfg.dim, np.float32), 0, kv)
+    assert np.any(kv[0][0].view(np.uint32) & np.uint32(0xFFFF))
+
+
 def test_fast_kv_overwritten_each_frame(tiny_oracle):
     """The fast AR starts every frame from an empty num_codebooks-long cache:
     the same slow state and codes give the same logits whatever ran before."""
