@@ -42,6 +42,8 @@ WORKLOADS = {
                                        "T=0.8 top-p 0.8 RAS window 10"),
     "s2pro_l1_b1": dict(cfg="s2pro_l1", batch=1, prompt=512, frames=16, temperature=0.8, top_p=0.8,
                         ras_win=10, desc="one-layer S2-Pro-shaped profiling case, batch 1, 512-token prompt"),
+    "s2pro_b64": dict(cfg="s2pro", batch=64, prompt=0, frames=28, temperature=0.8, top_p=0.8, ras_win=10,
+                      desc="full S2-Pro-shaped Dual-AR, batch 64, contexts uniform in [1024, 4096]"),
     "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
                     desc="tiny Dual-AR, batch 1, 32-token prompt, 16 frames"),
 }
@@ -56,6 +58,7 @@ def parse():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="s2pro_b1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-b64", action="store_true", help="skip the batch-64 measurement")
     return ap.parse_args()
 
 
@@ -163,6 +166,55 @@ def time_oracle(cfg, bits, wl, prompt, uniforms, n_frames, budget_s):
 
 # ---------------------------------------------------------------------------
 
+def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
+    """Batch 64 (the full-size batch-64 workload): 64 sequences with contexts
+    uniform in [1,024, 4,096] (seed 3) set up by the synthetic-context hook
+    (seeded K/V and held state, no prefill), then `warmup` + `frames` decode
+    steps with seeded uniforms (seed 1), T 0.8, top-p 0.8, resample window 10,
+    <|im_end|> excluded.  Device-timed with CUDA events."""
+    import torch
+    from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling
+    from dual_ar_tts_frame_gb300 import bytemodel
+    b = 64
+    ctx = gen.make_lengths(b, 1024, 4096, seed=3, stream="ctx_b64")
+    max_ctx = int(ctx.max()) + warmup + frames + 8
+    pages = sum(-(-(int(c) + warmup + frames + 1) // cfg.page_tokens) for c in ctx) + 8
+    dec = DualARDecoder(cfg, w, max_pages=pages, max_seqs=b, max_ctx=max_ctx)
+    for s in range(b):
+        dec.synthetic_context(s, int(ctx[s]), seed=1000 + s)
+    dec.sync()
+    smp = Sampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
+    uni = torch.from_numpy(gen.make_uniforms(warmup + frames, b, cfg, seed=1)).cuda()
+    codes = torch.empty((b, cfg.n_codebooks), dtype=torch.int32, device="cuda")
+    status = torch.empty((b,), dtype=torch.int32, device="cuda")
+    slots = list(range(b))
+    stream = torch.cuda.current_stream()
+    for f in range(warmup):
+        dec.decode_frame(slots, uni[f], smp, codes, status)
+    dec.sync()
+    launches = dec.last_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for f in range(warmup, warmup + frames):
+        dec.decode_frame(slots, uni[f], smp, codes, status)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dec.sync()
+    ms = ev0.elapsed_time(ev1)
+    assert int(status.max().item()) == 0
+    bytes_total = sum(bytemodel.frame_bytes(cfg, [int(c) + f + 1 for c in ctx]) for f in range(warmup, warmup + frames))
+    gbs = bytes_total / (ms / 1000.0) / 1e9
+    dec.close()
+    return {"workload": "full S2-Pro-shaped Dual-AR, batch 64, contexts uniform in [1024, 4096] (seed 3, "
+                        "synthetic K/V and held state, no prefill), T=0.8 top-p 0.8 RAS window 10",
+            "value": b * frames / (ms / 1000.0), "unit": "frames/s", "steps": frames, "warmup": warmup,
+            "ms_per_step": ms / frames, "rtf": FRAMES_PER_AUDIO_SECOND / (frames / (ms / 1000.0)),
+            "frame_bytes_per_step": bytes_total / frames,
+            "frame_roofline": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
+            "gpu_launches_per_step": launches}
+
+
 def main():
     args = parse()
     wl = WORKLOADS[args.workload]
@@ -178,6 +230,18 @@ def main():
               "l2": "inputs larger than L2 (9.1 GB of weights streamed per frame); no flush"}
     if args.workload != "s2pro_b1":
         config["l2"] = "small profiling/parity workload, not a bench line"
+
+    if args.workload == "s2pro_b64":
+        # the batch-64 measurement alone (also part of the default line)
+        import torch
+        from dual_ar_tts_frame_gb300 import build, upload_weights
+        torch.cuda.set_device(local)
+        build()
+        w = upload_weights(gen.make_weights(cfg, seed=0))
+        peak, _ = peaks()
+        r = measure_batch64(cfg, w, frames=K, warmup=W, peak=peak)
+        print(json.dumps({"metric": METRIC, "impl": "ours", "config": {"workload": r["workload"]}, **r}), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -303,6 +367,11 @@ def main():
         e2e = {"value": b * K * ws / el, "unit": "frames/s", "h2d_bytes_per_step": hu[0].numel() * 4,
                "d2h_bytes_per_step": hc.numel() * 4 + hs.numel() * 4}
 
+    dec.close()
+    b64 = None
+    if args.workload == "s2pro_b1" and not args.no_b64:
+        b64 = measure_batch64(cfg, w, frames=24, warmup=4, peak=peak)
+
     cpu = None
     if rank == 0 and ws == 1 and bits is not None:
         n_or = 8 if cfg.name == "s2pro" else 16
@@ -335,9 +404,9 @@ def main():
             "gpu_launches": launches_per_frame * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "batch64": b64,
         }
         print(json.dumps(line), flush=True)
-    dec.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
 

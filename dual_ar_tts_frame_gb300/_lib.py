@@ -26,7 +26,7 @@ EXPORTED = [
     "dualar_release", "dualar_sync", "dualar_get_error", "dualar_destroy",
     "dualar_get_page_table", "dualar_get_rope_table", "dualar_read_state", "dualar_slot_length",
     "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_set_persistent",
-    "dualar_debug_barrier_extra", "dualar_set_trace", "dualar_set_prefetch", "dualar_profile", "dualar_profile_read",
+    "dualar_debug_barrier_extra", "dualar_debug_synthetic_context", "dualar_set_trace", "dualar_set_prefetch", "dualar_profile", "dualar_profile_read",
 ]
 
 c_i32 = ctypes.c_int32
@@ -95,6 +95,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_last_launch_count.restype = c_i32
     L.dualar_set_persistent.argtypes = [H, c_i32]
     L.dualar_debug_barrier_extra.argtypes = [H, ctypes.c_uint32]
+    L.dualar_debug_synthetic_context.argtypes = [H, c_i32, c_i32, ctypes.c_uint32]
     L.dualar_set_prefetch.argtypes = [H, ctypes.c_uint64]
     L.dualar_set_trace.argtypes = [H, c_vp, ctypes.c_int64, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32)]
     L.dualar_profile.argtypes = [H, c_i32]

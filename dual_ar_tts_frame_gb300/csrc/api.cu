@@ -448,12 +448,23 @@ int build_mega_program(dualar_handle* h, int nb) {
 }
 
 // Split-KV work list: chunk size and per-row first unit.
+// Chunks are as short as possible (one page) while the batch's (row, KV
+// head, page) count is small -- a decode step of one or two sequences needs
+// every unit it can get -- and grow once there are more pages than about
+// eight units per SM, so that a unit streams several pages (double-buffered)
+// instead of paying a page's latency per unit.
 void plan_attention(dualar_handle* h, LaunchSetup& s, int* units, int* chunk) {
   int max_len = 0;
-  for (int r = 0; r < s.n_rows; ++r) max_len = std::max(max_len, s.rows[r].pos + 1);
+  long long page_units = 0;
   const int pt = h->cfg.page_tokens;
+  for (int r = 0; r < s.n_rows; ++r) {
+    max_len = std::max(max_len, s.rows[r].pos + 1);
+    page_units += static_cast<long long>(h->cfg.n_kv_head) * ((s.rows[r].pos + 1 + pt - 1) / pt);
+  }
   const int pages = (max_len + pt - 1) / pt;
-  const int ppc = std::max(1, (pages + kMaxChunks - 1) / kMaxChunks);
+  const long long target = 8LL * h->n_sm;
+  const int ppc = std::max(std::max(1, (pages + kMaxChunks - 1) / kMaxChunks),
+                           static_cast<int>(page_units / target));
   *chunk = ppc * pt;
   int u = 0;
   for (int r = 0; r < s.n_rows; ++r) {
@@ -889,6 +900,50 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
     TRY(slow_stack(h, m, units, chunk, false));
     if (c0 + m == n_tokens) TRY(run_gemv(h, args_head(h, m - 1, 1)));
   }
+  h->length[slot] = n_tokens;
+  return DUALAR_OK;
+}
+
+int dualar_debug_synthetic_context(dualar_handle* h, int32_t slot, int32_t n_tokens, uint32_t seed) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  const dualar_config& c = h->cfg;
+  if (slot < 0 || slot >= c.max_seqs || n_tokens <= 0) {
+    set_err(h, "synthetic context: bad slot or length");
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  if (h->length[slot] >= 0) {
+    set_err(h, "synthetic context: slot %d holds a sequence", slot);
+    return DUALAR_ERR_SLOT_BUSY;
+  }
+  if (n_tokens > c.max_ctx) {
+    set_err(h, "synthetic context: %d tokens exceed max_ctx %d", n_tokens, c.max_ctx);
+    return DUALAR_ERR_CONTEXT_FULL;
+  }
+  const int need = (n_tokens + c.page_tokens - 1) / c.page_tokens;
+  if (need > static_cast<int>(h->free_pages.size())) {
+    set_err(h, "synthetic context: %d pages needed, %zu free", need, h->free_pages.size());
+    return DUALAR_ERR_OOM_PAGES;
+  }
+  const DevPtrs& d = h->d;
+  CUDA_TRY(h, cudaMemsetAsync(d.hist_n + slot, 0, 4, h->stream));
+  CUDA_TRY(h, cudaMemsetAsync(d.finished + slot, 0, 4, h->stream));
+  h->launches = 0;
+  static LaunchSetup s;
+  // pages in the order prefill takes them (lowest free first)
+  for (int p0 = 0; p0 < need; p0 += kMaxRows) {
+    std::memset(&s, 0, sizeof(s));
+    for (int p = p0; p < std::min(need, p0 + kMaxRows); ++p) {
+      const int pg = *h->free_pages.begin();
+      h->free_pages.erase(h->free_pages.begin());
+      h->pages[slot].push_back(pg);
+      s.upd_slot[s.n_updates] = slot;
+      s.upd_index[s.n_updates] = p;
+      s.upd_page[s.n_updates] = pg;
+      ++s.n_updates;
+    }
+    LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
+  }
+  LAUNCH(h, launch_synthetic_fill(d, slot, need, seed, h->n_sm, h->stream));
   h->length[slot] = n_tokens;
   return DUALAR_OK;
 }

@@ -172,6 +172,8 @@ cudaError_t launch_sample_fast(const DevPtrs& d, int nrows, int k, const float* 
                                const uint16_t* fast_emb, cudaStream_t st);
 cudaError_t launch_fusion(const DevPtrs& d, int nrows, const uint16_t* tok_emb,
                           const uint16_t* fusion, cudaStream_t st);
+cudaError_t launch_synthetic_fill(const DevPtrs& d, int slot, int n_pages, uint32_t seed, int n_sm,
+                                  cudaStream_t st);
 
 
 }  // namespace dualar

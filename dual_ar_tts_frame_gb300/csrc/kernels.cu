@@ -71,6 +71,63 @@ cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t*
 }
 
 // ============================================================================
+// Synthetic context (benchmark / test hook)
+// ============================================================================
+// Fills the KV pages of a slot (all layers), its held hidden state and its
+// held logits with seeded values in [-1, 1) (hidden) and [-3, 3) (logits),
+// from a counter hash of (seed, element).  Not part of the decode path.
+DEVI uint32_t synth_hash(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7FEB352Du;
+  x ^= x >> 15;
+  x *= 0x846CA68Bu;
+  x ^= x >> 16;
+  return x;
+}
+DEVI float synth_unit(uint32_t seed, uint64_t i) {
+  const uint32_t h = synth_hash(synth_hash(static_cast<uint32_t>(i) ^ seed) + static_cast<uint32_t>(i >> 32));
+  return static_cast<float>(h >> 8) * (2.0f / 16777216.0f) - 1.0f;
+}
+// grid: (x, n_pages); each thread writes 8 bf16 values per step
+__global__ void synthetic_fill_kernel(DevPtrs d, int slot, uint32_t seed) {
+  const size_t page_elems = static_cast<size_t>(d.n_layer) * 2 * d.Hkv * d.page_tokens * d.hd;
+  const int p = blockIdx.y;
+  const int pg = d.page_table[static_cast<size_t>(slot) * d.pages_per_seq + p];
+  if (pg < 0 || pg >= d.max_pages) {
+    if (threadIdx.x == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
+    return;
+  }
+  const size_t base = static_cast<size_t>(pg) * page_elems;
+  uint4* dst = reinterpret_cast<uint4*>(d.kv_pool + base);
+  const size_t nv = page_elems / 8;
+  for (size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nv;
+       v += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t e = base + 8 * v + 2 * q;
+      w[q] = static_cast<uint32_t>(f32_to_bf16bits(synth_unit(seed, e))) |
+             (static_cast<uint32_t>(f32_to_bf16bits(synth_unit(seed, e + 1))) << 16);
+    }
+    dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int k = threadIdx.x; k < d.D; k += blockDim.x)
+      d.h_last[static_cast<size_t>(slot) * d.D + k] = synth_unit(seed ^ 0x9E3779B9u, k);
+    for (int k = threadIdx.x; k < d.n_sem + 1; k += blockDim.x)
+      d.z_last[static_cast<size_t>(slot) * (d.n_sem + 1) + k] = 3.0f * synth_unit(seed ^ 0x85EBCA6Bu, k);
+  }
+}
+
+cudaError_t launch_synthetic_fill(const DevPtrs& d, int slot, int n_pages, uint32_t seed, int n_sm,
+                                  cudaStream_t st) {
+  (void)n_sm;
+  if (n_pages <= 0) return cudaSuccess;
+  synthetic_fill_kernel<<<dim3(64, n_pages), 256, 0, st>>>(d, slot, seed);
+  return cudaGetLastError();
+}
+
+// ============================================================================
 // GEMV (standalone launch; device code in gemv.cuh)
 // ============================================================================
 constexpr int kMaxStages = kMaxStagesRing;

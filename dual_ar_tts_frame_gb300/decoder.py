@@ -191,6 +191,10 @@ class DualARDecoder:
     def debug_barrier_extra(self, extra: int) -> None:
         self._check(self.lib.dualar_debug_barrier_extra(self.h, extra))
 
+    def synthetic_context(self, slot: int, n_tokens: int, seed: int = 0) -> None:
+        """Benchmark/test hook: a context of n_tokens seeded positions, no prefill."""
+        self._check(self.lib.dualar_debug_synthetic_context(self.h, slot, n_tokens, seed & 0xFFFFFFFF))
+
     def set_prefetch(self, bytes_per_sm: int) -> None:
         self._check(self.lib.dualar_set_prefetch(self.h, bytes_per_sm))
 

@@ -271,6 +271,18 @@ int dualar_set_prefetch(dualar_handle* h, uint64_t bytes_per_sm);
  * DUALAR_ERR_TIMEOUT.  0 (default) restores normal operation. */
 int dualar_debug_barrier_extra(dualar_handle* h, uint32_t extra);
 
+/* Benchmark and test hook (no counterpart on the pages): gives a free slot a
+ * context of n_tokens positions without running the model.  Pages are taken
+ * exactly as dualar_prefill takes them (lowest free first); every K/V value of
+ * those pages (all layers) is set to a seeded value in [-1, 1) (bf16), the
+ * held hidden state to seeded values in [-1, 1) and the held restricted
+ * logits to seeded values in [-3, 3); the resample history is empty.  The
+ * slot then decodes like a prefilled one.  Used to set up long batched
+ * contexts (e.g. 64 sequences of 1-4K tokens) whose prefill would dominate a
+ * decode benchmark.  Errors: INVALID_ARG (slot or length), SLOT_BUSY,
+ * CONTEXT_FULL, OOM_PAGES, CUDA.  Asynchronous on the handle's stream. */
+int dualar_debug_synthetic_context(dualar_handle* h, int32_t slot, int32_t n_tokens, uint32_t seed);
+
 /* Per-op timeline of the persistent frame kernel.  device_buffer: device
  * memory of `bytes` bytes (NULL stops tracing).  While set, every persistent
  * launch whose program fits writes, per CTA and op, the global-timer stamps

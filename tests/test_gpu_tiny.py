@@ -335,3 +335,30 @@ def test_error_codes(dev_weights):
     assert d.page_table(0) == [0, 1, 2]
     d.release(0)
     d.close()
+
+
+# ------------------------------------------------------ synthetic context --
+
+def test_synthetic_context_hook(dev_weights):
+    """The benchmark's context hook takes pages like prefill (lowest free
+    first), sets the length, and the slot decodes (both paths)."""
+    d = make(dev_weights, max_pages=32)
+    pages = PageOracle(32, TINY.page_tokens)
+    d.synthetic_context(2, 300, seed=5)
+    pages.append(2, 300)
+    p = g.make_prompt(TINY, 70, seed=6)
+    d.prefill(0, p)
+    pages.append(0, 70)
+    assert d.slot_length(2) == 300 and d.slot_length(0) == 70
+    assert d.page_table(2) == pages.table[2] and d.page_table(0) == pages.table[0]
+    smp = gpu_sampling(OSampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False))
+    uni = dev(g.make_uniforms(2, 2, TINY, seed=7))
+    for f, persistent in enumerate((True, False)):
+        d.set_persistent(persistent)
+        codes, status = d.decode_frame([2, 0], uni[f], smp)
+        d.sync()
+        assert status.cpu().tolist() == [0, 0]
+        c = codes.cpu().numpy()
+        assert np.all((c[:, 0] >= 0) & (c[:, 0] < TINY.n_sem)) and np.all((c[:, 1:] >= 0) & (c[:, 1:] < TINY.fast_vocab))
+    assert d.slot_length(2) == 302
+    d.close()
