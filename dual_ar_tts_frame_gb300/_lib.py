@@ -25,7 +25,7 @@ EXPORTED = [
     "dualar_decode_frame_noalloc",
     "dualar_release", "dualar_sync", "dualar_get_error", "dualar_destroy",
     "dualar_get_page_table", "dualar_get_rope_table", "dualar_read_state", "dualar_slot_length",
-    "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_set_persistent",
+    "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_set_persistent", "dualar_set_tensor_cores",
     "dualar_debug_barrier_extra", "dualar_debug_synthetic_context", "dualar_set_trace", "dualar_set_prefetch", "dualar_profile", "dualar_profile_read",
 ]
 
@@ -94,6 +94,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_last_launch_count.argtypes = [H]
     L.dualar_last_launch_count.restype = c_i32
     L.dualar_set_persistent.argtypes = [H, c_i32]
+    L.dualar_set_tensor_cores.argtypes = [H, c_i32]
     L.dualar_debug_barrier_extra.argtypes = [H, ctypes.c_uint32]
     L.dualar_debug_synthetic_context.argtypes = [H, c_i32, c_i32, ctypes.c_uint32]
     L.dualar_set_prefetch.argtypes = [H, ctypes.c_uint64]

@@ -16,6 +16,7 @@
 #include "dualar.h"
 #include "internal.h"
 #include "mega.h"
+#include "tcgemm.h"
 
 using namespace dualar;
 
@@ -41,6 +42,8 @@ struct dualar_handle {
   std::vector<double> prof_bytes;
   // persistent frame kernel
   bool use_mega = true;
+  bool use_tc = true;            // dualar_set_tensor_cores
+  TcBuffers tc{};                // tensor-core projection buffers
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
   uint64_t* tagged = nullptr;    // the tagged work buffers (one region)
@@ -201,7 +204,18 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
     }
     CUDA_TRY(h, cudaEventRecord(e0, h->stream));
   }
-  LAUNCH(h, launch_gemv(a, h->n_sm, h->stream));
+  if (h->use_tc && tc_eligible(a, h->tc.ldx)) {
+    // 9..128 rows: one pass over the weights on the tensor cores
+    int n = 0;
+    const cudaError_t e = launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n);
+    h->launches += n;
+    if (e != cudaSuccess) {
+      set_err(h, "tensor-core projection failed: %s", cudaGetErrorString(e));
+      return DUALAR_ERR_CUDA;
+    }
+  } else {
+    LAUNCH(h, launch_gemv(a, h->n_sm, h->stream));
+  }
   if (h->profiling) {
     CUDA_TRY(h, cudaEventRecord(e1, h->stream));
     h->prof_bytes.push_back(gemv_bytes(a));
@@ -780,6 +794,17 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
   ALLOC(d.err, 1);
   ALLOC(h->bar_counter, 1);
   {
+    // tensor-core projections: x' halves for up to 128 rows and the split-K
+    // partial sums
+    const int kmax = std::max(std::max(c.dim, c.n_head * c.head_dim), c.ffn);
+    const int nmax = std::max(std::max(d.qkv_dim, 2 * c.ffn), std::max(c.n_sem + 1, std::max(c.fast_vocab, c.dim)));
+    h->tc.ldx = kmax;
+    h->tc.part_floats = static_cast<size_t>(kTcMaxSlices) * kTcMaxRows * nmax;
+    ALLOC(h->tc.xh, static_cast<size_t>(kTcMaxRows) * kmax);
+    ALLOC(h->tc.xl, static_cast<size_t>(kTcMaxRows) * kmax);
+    ALLOC(h->tc.part, h->tc.part_floats);
+  }
+  {
     // tagged work buffers of the persistent frame kernel, one region (cleared
     // together when the tag epoch wraps); every buffer starts on 64 bytes
     const size_t TR = kTaggedRows;
@@ -1103,6 +1128,12 @@ int32_t dualar_last_launch_count(const dualar_handle* h) { return h ? h->launche
 int dualar_set_persistent(dualar_handle* h, int32_t enable) {
   if (!h) return DUALAR_ERR_INVALID_ARG;
   h->use_mega = enable != 0;
+  return DUALAR_OK;
+}
+
+int dualar_set_tensor_cores(dualar_handle* h, int32_t enable) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  h->use_tc = enable != 0;
   return DUALAR_OK;
 }
 

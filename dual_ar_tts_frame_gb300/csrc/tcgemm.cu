@@ -1,0 +1,366 @@
+// Batched projections on the tensor cores (tcgen05), for decode batches and
+// prefill chunks of 9..128 rows:
+//
+//   y[m][n] = sum_k x'[m][k] W[n][k],   x' = RMSNorm(x) * g (optional)
+//
+// At these batch sizes a projection is still bound by the weight bytes (2*M
+// FLOP per weight byte, below the ridge), but it is a dense contraction: the
+// weights are read ONCE per launch instead of once per 8 rows.
+//
+// Three kernels per projection:
+//  1. tc_split_kernel: x' per row (RMSNorm scale and gain applied), written as
+//     two bf16 halves x' = hi + lo (lo = bf16(x' - hi)), so the bf16 tensor
+//     cores see x' to ~16 significant bits;
+//  2. tc_gemm_kernel: the weights are the MMA's M side (128 rows per
+//     instruction, two instructions per CTA tile of 256 rows), the batch its N
+//     side (padded to 16/32/64/128), K = 16 per instruction.  TMA copies
+//     weight and activation tiles (64 K wide, 128-byte swizzle) into a ring of
+//     shared-memory stages; one thread issues tcgen05.mma (hi and lo halves
+//     into the same fp32 accumulator in tensor memory); four warps read the
+//     accumulators back (tcgen05.ld) and store this CTA's split-K partial sums;
+//  3. tc_reduce_kernel: adds the partial sums of the K slices in slice order
+//     (deterministic) and applies the epilogue: store / residual add / SwiGLU,
+//     with the optional output row map.
+// [P2] "The slow AR is Qwen3-4B" (the projections of a Qwen3 layer) and "Two
+// autoregressions" (the fast AR's layers and head).
+#include <cuda.h>
+
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+#include "tcgemm.h"
+
+namespace dualar {
+
+constexpr int kTcThreads = 192;     // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: read-back
+constexpr int kTcWTile = 128 * 64 * 2;   // one 128-row x 64-K weight tile (bytes)
+constexpr size_t kTcSmemBudget = 200 * 1024;
+
+__host__ __device__ constexpr int tc_stage_bytes(int nbp) { return 2 * kTcWTile + 2 * nbp * 128; }
+__host__ __device__ constexpr int tc_stages(int nbp) {
+  return static_cast<int>(kTcSmemBudget / tc_stage_bytes(nbp)) > 6 ? 6
+                                                                     : static_cast<int>(kTcSmemBudget / tc_stage_bytes(nbp));
+}
+__host__ __device__ constexpr size_t tc_smem_bytes(int nbp) {
+  // stages, then full/empty/accumulator mbarriers and the TMEM address, plus
+  // up to 1 KB to align the stages on 1024 bytes (128-byte swizzle atoms)
+  return static_cast<size_t>(tc_stages(nbp)) * tc_stage_bytes(nbp) + 256 + 1024;
+}
+
+struct TcArgs {
+  int n0, n1;          // weight rows of segment 0 (map 0) and segment 1 (map 1)
+  int K;
+  int nb;              // batch rows written back (<= NBP)
+  int kc_per_slice;    // 64-wide K chunks per split-K slice
+  float* part;         // [slices][nb][ldp] partial sums
+  int ldp;             // n0 + n1
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+};
+
+template <int NBP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tw0, const __grid_constant__ CUtensorMap tw1,
+                   const __grid_constant__ CUtensorMap txh, const __grid_constant__ CUtensorMap txl,
+                   const TcArgs a) {
+  constexpr int S = tc_stages(NBP);
+  constexpr int SB = tc_stage_bytes(NBP);
+  constexpr int XT = NBP * 128;                                   // one activation tile (bytes)
+  constexpr uint32_t kCols = 2 * NBP < 32 ? 32u : static_cast<uint32_t>(2 * NBP);   // power of two
+  static_assert(S >= 2, "at least two stages");
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned stages
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(accf + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, slice = blockIdx.y;
+  const int kc_total = a.K / 64;
+  const int c0 = slice * a.kc_per_slice;
+  const int nch = min(kc_total, c0 + a.kc_per_slice) - c0;   // >= 1 (host)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&accf[0], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % S;
+        if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, a.err, a.wait_limit_ns)) break;
+        unsigned char* st = smem + s * SB;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(SB));
+        const int kx = (c0 + i) * 64;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int r0 = tile * 256 + t * 128;
+          if (r0 < a.n0) tma_load_2d_hint(st + t * kTcWTile, &tw0, kx, r0, &full[s], pol);
+          else tma_load_2d_hint(st + t * kTcWTile, &tw1, kx, r0 - a.n0, &full[s], pol);
+        }
+        tma_load_2d(st + 2 * kTcWTile, &txh, kx, 0, &full[s]);
+        tma_load_2d(st + 2 * kTcWTile + XT, &txl, kx, 0, &full[s]);
+        ++issued;
+      }
+      // every copy issued here has landed before the CTA may exit (bounded)
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&full[i % S], (i / S) & 1))
+          if (global_timer_ns() - t0 > a.wait_limit_ns) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NBP);
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&full[s], (i / S) & 1, a.err, a.wait_limit_ns)) break;
+        tc_fence_after();
+        unsigned char* st = smem + s * SB;
+        const uint64_t dxh = smem_desc_sw128(st + 2 * kTcWTile);
+        const uint64_t dxl = smem_desc_sw128(st + 2 * kTcWTile + XT);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint64_t dw = smem_desc_sw128(st + t * kTcWTile);
+          const uint32_t dt = tbase + static_cast<uint32_t>(t * NBP);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ko = static_cast<uint64_t>(k * 32) >> 4;   // +32 bytes per 16-wide K step
+            tc_mma_bf16(dt, dw + ko, dxh + ko, idesc, i > 0 || k > 0);
+            tc_mma_bf16(dt, dw + ko, dxl + ko, idesc, true);
+          }
+        }
+        tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+      }
+      tc_commit(&accf[0]);      // all MMAs above complete (also after an early stop)
+    }
+  } else {
+    // ---- read-back: warp w may access TMEM lanes 32*(w%4) .. +31
+    const int q = warp & 3;
+    if (mbar_wait(&accf[0], 0, a.err, a.wait_limit_ns)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        const int n = tile * 256 + t * 128 + q * 32 + lane;   // weight row of this lane
+#pragma unroll 1
+        for (int c = 0; c < NBP / 16; ++c) {
+          float v[16];
+          tmem_ld16(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(t * NBP + c * 16), v);
+          if (n < a.ldp) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int m = c * 16 + j;
+              if (m < a.nb) a.part[(static_cast<size_t>(slice) * a.nb + m) * a.ldp + n] = v[j];
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kCols);
+  }
+}
+
+// x' rows as bf16 hi/lo: one CTA per row.
+__global__ void tc_split_kernel(const float* x, int ldx, int K, const uint16_t* norm_w, float eps, uint16_t* xh,
+                                uint16_t* xl, int ldxh, float* save_x, const int32_t* save_map, int lds) {
+  const int m = blockIdx.x;
+  const float* xr = x + static_cast<size_t>(m) * ldx;
+  __shared__ float red[32];
+  __shared__ float s_scale;
+  float sc = 1.f;
+  if (norm_w != nullptr) {
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) ss += xr[k] * xr[k];
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+      s_scale = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
+    }
+    __syncthreads();
+    sc = s_scale;
+  }
+  const int row = save_x ? (save_map ? save_map[m] : m) : -1;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const float v = norm_w ? (xr[k] * bf16bits_to_f32(norm_w[k])) * sc : xr[k];
+    const uint16_t hi = f32_to_bf16bits(v);
+    xh[static_cast<size_t>(m) * ldxh + k] = hi;
+    xl[static_cast<size_t>(m) * ldxh + k] = f32_to_bf16bits(v - bf16bits_to_f32(hi));
+    if (row >= 0) save_x[static_cast<size_t>(row) * lds + k] = v;
+  }
+}
+
+// Sum of the K-slice partials (slice order) and the epilogue.
+__global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
+                                 int ldo, const float* base, int ldb, const int32_t* out_map, int n0) {
+  const size_t total = static_cast<size_t>(nb) * n_out;
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(e / n_out), n = static_cast<int>(e % n_out);
+    float y = 0.f;
+    for (int s = 0; s < slices; ++s) y += part[(static_cast<size_t>(s) * nb + m) * ldp + n];
+    const int orow = out_map ? out_map[m] : m;
+    if (orow < 0) continue;
+    float r;
+    if (mode == GEMV_SWIGLU) {
+      float u = 0.f;
+      for (int s = 0; s < slices; ++s) u += part[(static_cast<size_t>(s) * nb + m) * ldp + n0 + n];
+      r = silu(y) * u;   // [P2] "The slow AR is Qwen3-4B": down(SiLU(gate) * up)
+    } else if (mode == GEMV_ADD) {
+      r = base[static_cast<size_t>(orow) * ldb + n] + y;
+    } else {
+      r = y;
+    }
+    out[static_cast<size_t>(orow) * ldo + n] = r;
+  }
+}
+
+// ---- host side ------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool tc_available() { return encode_fn() != nullptr; }
+
+// bf16 matrix [rows][K] (row stride ld elements), tiles of box_rows x 64,
+// 128-byte swizzle; rows beyond `rows` read as zeros.
+static bool make_map(CUtensorMap* m, const void* base, int K, int rows, int ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps are built once per (address, K, rows, box) and kept.
+static bool cached_map(CUtensorMap* out, const void* base, int K, int rows, int ld, int box_rows) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int, int>, CUtensorMap> cache;
+  std::lock_guard<std::mutex> g(mu);
+  const auto key = std::make_tuple(base, K, rows, ld, box_rows);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return true;
+  }
+  CUtensorMap m;
+  if (!make_map(&m, base, K, rows, ld, box_rows)) return false;
+  cache.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+bool tc_eligible(const GemvArgs& a, int ldx) {
+  if (!tc_available()) return false;
+  if (a.nb < kTcMinRows || a.nb > kTcMaxRows || a.K % 64 != 0 || a.K > ldx) return false;
+  if (a.x_src >= 0 || a.base_src >= 0 || a.out_src >= 0) return false;   // plain buffers only
+  if (a.mode == GEMV_SWIGLU) return a.n0 % 128 == 0 && a.n1 == a.n0;
+  return a.n1 == 0 || a.n0 % 128 == 0;
+}
+
+template <int NBP>
+static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& xh,
+                                   const CUtensorMap& xl, const TcArgs& t, dim3 grid, cudaStream_t st) {
+  static bool configured = false;
+  const size_t smem = tc_smem_bytes(NBP);
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  tc_gemm_kernel<NBP><<<grid, kTcThreads, smem, st>>>(w0, w1, xh, xl, t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches) {
+  const int nbp = a.nb <= 16 ? 16 : a.nb <= 32 ? 32 : a.nb <= 64 ? 64 : 128;
+  const int n_rows = a.n0 + a.n1;   // virtual weight rows (SwiGLU: gate then up)
+  const int tiles = (n_rows + 255) / 256;
+  const int kc = a.K / 64;
+  int slices = (n_sm + tiles / 2) / tiles;
+  slices = slices < 1 ? 1 : slices > kTcMaxSlices ? kTcMaxSlices : slices;
+  if (slices > kc) slices = kc;
+  const int kcps = (kc + slices - 1) / slices;
+  slices = (kc + kcps - 1) / kcps;   // no empty slice
+  if (static_cast<size_t>(slices) * a.nb * n_rows > b.part_floats) return cudaErrorInvalidValue;
+
+  CUtensorMap m0, m1, mh, ml;
+  const int seg1 = a.n1 > 0 ? a.n1 : 1;
+  if (!cached_map(&m0, a.w0, a.K, a.n0, a.K, 128) ||
+      !cached_map(&m1, a.n1 > 0 ? a.w1 : a.w0, a.K, seg1, a.K, 128) ||
+      !cached_map(&mh, b.xh, a.K, kTcMaxRows, b.ldx, nbp) || !cached_map(&ml, b.xl, a.K, kTcMaxRows, b.ldx, nbp))
+    return cudaErrorInvalidValue;
+
+  tc_split_kernel<<<a.nb, 256, 0, st>>>(a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh, b.xl, b.ldx, a.save_x, a.save_map,
+                                        a.lds);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  TcArgs t{a.n0, a.n1, a.K, a.nb, kcps, b.part, n_rows, a.err, a.wait_limit_ns};
+  const dim3 grid(tiles, slices);
+  switch (nbp) {
+    case 16: e = launch_gemm_nbp<16>(m0, m1, mh, ml, t, grid, st); break;
+    case 32: e = launch_gemm_nbp<32>(m0, m1, mh, ml, t, grid, st); break;
+    case 64: e = launch_gemm_nbp<64>(m0, m1, mh, ml, t, grid, st); break;
+    default: e = launch_gemm_nbp<128>(m0, m1, mh, ml, t, grid, st); break;
+  }
+  if (e != cudaSuccess) return e;
+  const int n_out = a.mode == GEMV_SWIGLU ? a.n0 : n_rows;
+  const size_t total = static_cast<size_t>(a.nb) * n_out;
+  int rgrid = static_cast<int>((total + 255) / 256);
+  rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
+  tc_reduce_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb,
+                                          a.out_map, a.n0);
+  if (launches) *launches += 3;
+  return cudaGetLastError();
+}
+
+}  // namespace dualar

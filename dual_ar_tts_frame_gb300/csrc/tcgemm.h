@@ -1,0 +1,33 @@
+// Batched projections on the tensor cores (tcgemm.cu): host interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace dualar {
+
+constexpr int kTcMinRows = 9;      // below this the weight-streaming GEMV (<= 8 rows per pass) is used
+constexpr int kTcMaxRows = 128;    // activation rows per launch (the MMA's N <= 128)
+constexpr int kTcMaxSlices = 16;   // split-K slices
+
+// Work buffers of one handle.
+struct TcBuffers {
+  uint16_t* xh;          // [kTcMaxRows][ldx] bf16: high half of x'
+  uint16_t* xl;          // [kTcMaxRows][ldx] bf16: low half
+  int ldx;               // >= every projection's K
+  float* part;           // split-K partial sums
+  size_t part_floats;
+};
+
+// Whether the driver offers tensor-map encoding (checked once).
+bool tc_available();
+// Whether a projection can take the tensor-core path: 9..128 plain-buffer
+// rows, K a multiple of 64 and <= ldx, segment boundaries on 128 rows.
+bool tc_eligible(const GemvArgs& a, int ldx);
+// Queues split, GEMM and reduce kernels; *launches += 3.
+cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches);
+
+}  // namespace dualar

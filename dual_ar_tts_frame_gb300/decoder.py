@@ -188,6 +188,9 @@ class DualARDecoder:
     def set_persistent(self, enable: bool) -> None:
         self._check(self.lib.dualar_set_persistent(self.h, int(enable)))
 
+    def set_tensor_cores(self, enable: bool) -> None:
+        self._check(self.lib.dualar_set_tensor_cores(self.h, int(enable)))
+
     def debug_barrier_extra(self, extra: int) -> None:
         self._check(self.lib.dualar_debug_barrier_extra(self.h, extra))
 

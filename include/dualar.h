@@ -257,6 +257,14 @@ int32_t dualar_last_launch_count(const dualar_handle* h);
  * Both paths compute the same values. */
 int dualar_set_persistent(dualar_handle* h, int32_t enable);
 
+/* Projections of 9..128 rows (decode batches above 8 sequences, prefill
+ * chunks) run on the tensor cores: 1 (default) one tcgen05 GEMM per
+ * projection that reads the weights once (activations as two bf16 halves,
+ * fp32 accumulation, split-K partials added in a fixed order); 0 the
+ * weight-streaming GEMV in passes of <= 8 rows.  Both compute the same
+ * projection to fp32 rounding (not bit-identically).  Errors: INVALID_ARG. */
+int dualar_set_tensor_cores(dualar_handle* h, int32_t enable);
+
 /* Persistent frame kernel: weight bytes per SM that its producer keeps in
  * flight into L2 ahead of the shared-memory ring while the ring is full
  * (default 65536; on GB300 64 KiB hides part of the refill at op boundaries,

@@ -362,3 +362,33 @@ def test_synthetic_context_hook(dev_weights):
         assert np.all((c[:, 0] >= 0) & (c[:, 0] < TINY.n_sem)) and np.all((c[:, 1:] >= 0) & (c[:, 1:] < TINY.fast_vocab))
     assert d.slot_length(2) == 302
     d.close()
+
+
+# ----------------------------------------------------- tensor-core batches --
+
+def test_teacher_forced_batch12_tensor_cores(dev_weights, tiny_oracle):
+    """Twelve sequences (ragged contexts, several pages and chunks): every
+    projection runs on the tensor cores (tcgen05, 9..128 rows), against the
+    oracle; the same frames with the tensor cores off (GEMV passes of <= 8
+    rows) agree to fp32 rounding."""
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
+    prompts = {s: g.make_prompt(TINY, int(n), seed=40 + s)
+               for s, n in enumerate(g.make_lengths(12, 20, 200, seed=41, stream="tc_b12"))}
+    d = make(dev_weights, max_pages=128, max_seqs=16)
+    run_forced(d, tiny_oracle, prompts, 3, smp, seed=42)
+    d.close()
+    # the two projection paths on identical inputs
+    outs = []
+    for tc in (True, False):
+        d = make(dev_weights, max_pages=128, max_seqs=16)
+        d.set_tensor_cores(tc)
+        for s, p in prompts.items():
+            d.prefill(s, p)
+        forced = g.make_forced_codes(1, 12, TINY, seed=43)[0]
+        uni = g.make_uniforms(1, 12, TINY, seed=44)[0]
+        _, _, slow, fast, _ = d.decode_frame_forced(list(prompts), dev(uni), gpu_sampling(smp), dev(forced))
+        d.sync()
+        outs.append((slow.cpu().numpy(), fast.cpu().numpy()))
+        d.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert np.abs(a - b).max() <= 2e-3 * max(1.0, float(np.abs(b).max()))
