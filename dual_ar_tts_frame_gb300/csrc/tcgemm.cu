@@ -188,54 +188,116 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// x' rows as bf16 hi/lo: one CTA per row.
-__global__ void tc_split_kernel(const float* x, int ldx, int K, const uint16_t* norm_w, float eps, uint16_t* xh,
-                                uint16_t* xl, int ldxh, float* save_x, const int32_t* save_map, int lds) {
+// x' rows as bf16 hi/lo: one CTA of 1024 threads per row; the row is read
+// once (float4, kept in registers: K <= 12288) and written as 4 bf16 per
+// 8-byte store.
+constexpr int kSplitThreads = 1024;
+constexpr int kSplitVec = 3;   // float4 per thread
+
+__global__ void __launch_bounds__(kSplitThreads, 1)
+    tc_split_kernel(const float* x, int ldx, int K, const uint16_t* norm_w, float eps, uint16_t* xh, uint16_t* xl,
+                    int ldxh, float* save_x, const int32_t* save_map, int lds) {
   const int m = blockIdx.x;
-  const float* xr = x + static_cast<size_t>(m) * ldx;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * ldx);
+  const int KV = K >> 2;
   __shared__ float red[32];
-  __shared__ float s_scale;
+  float4 v[kSplitVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < kSplitVec; ++q) {
+    const int j = threadIdx.x + q * kSplitThreads;
+    v[q] = j < KV ? xr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+  }
   float sc = 1.f;
   if (norm_w != nullptr) {
-    float ss = 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) ss += xr[k] * xr[k];
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      float t = 0.f;
-      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
-      s_scale = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
-    }
-    __syncthreads();
-    sc = s_scale;
+    float t = 0.f;
+#pragma unroll 8
+    for (int w = 0; w < kSplitThreads / 32; ++w) t += red[w];
+    sc = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
   }
   const int row = save_x ? (save_map ? save_map[m] : m) : -1;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    const float v = norm_w ? (xr[k] * bf16bits_to_f32(norm_w[k])) * sc : xr[k];
-    const uint16_t hi = f32_to_bf16bits(v);
-    xh[static_cast<size_t>(m) * ldxh + k] = hi;
-    xl[static_cast<size_t>(m) * ldxh + k] = f32_to_bf16bits(v - bf16bits_to_f32(hi));
-    if (row >= 0) save_x[static_cast<size_t>(row) * lds + k] = v;
+#pragma unroll
+  for (int q = 0; q < kSplitVec; ++q) {
+    const int j = threadIdx.x + q * kSplitThreads;
+    if (j >= KV) continue;
+    float e[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+    if (norm_w != nullptr) {
+      const uint2 gw = *reinterpret_cast<const uint2*>(norm_w + 4 * j);
+      e[0] = (e[0] * bf16lo(gw.x)) * sc;
+      e[1] = (e[1] * bf16hi(gw.x)) * sc;
+      e[2] = (e[2] * bf16lo(gw.y)) * sc;
+      e[3] = (e[3] * bf16hi(gw.y)) * sc;
+    }
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint16_t hb = f32_to_bf16bits(e[c]);
+      h[c] = hb;
+      l[c] = f32_to_bf16bits(e[c] - bf16bits_to_f32(hb));
+    }
+    *reinterpret_cast<uint2*>(xh + static_cast<size_t>(m) * ldxh + 4 * j) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    *reinterpret_cast<uint2*>(xl + static_cast<size_t>(m) * ldxh + 4 * j) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    if (row >= 0)
+      *reinterpret_cast<float4*>(save_x + static_cast<size_t>(row) * lds + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
   }
 }
 
-// Sum of the K-slice partials (slice order) and the epilogue.
+// Sum of the K-slice partials (slice order) and the epilogue, 4 columns per
+// thread (all row strides multiples of 4 floats).
 __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
                                  int ldo, const float* base, int ldb, const int32_t* out_map, int n0) {
+  const int nq = n_out >> 2;   // n_out % 4 == 0 (host)
+  const size_t total = static_cast<size_t>(nb) * nq;
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(e / nq), n = 4 * static_cast<int>(e % nq);
+    const int orow = out_map ? out_map[m] : m;
+    if (orow < 0) continue;
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < slices; ++s) {
+      const float4 p = *reinterpret_cast<const float4*>(part + (static_cast<size_t>(s) * nb + m) * ldp + n);
+      y.x += p.x; y.y += p.y; y.z += p.z; y.w += p.w;
+    }
+    float4 r;
+    if (mode == GEMV_SWIGLU) {
+      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < slices; ++s) {
+        const float4 p = *reinterpret_cast<const float4*>(part + (static_cast<size_t>(s) * nb + m) * ldp + n0 + n);
+        u.x += p.x; u.y += p.y; u.z += p.z; u.w += p.w;
+      }
+      // [P2] "The slow AR is Qwen3-4B": down(SiLU(gate) * up)
+      r = make_float4(silu(y.x) * u.x, silu(y.y) * u.y, silu(y.z) * u.z, silu(y.w) * u.w);
+    } else if (mode == GEMV_ADD) {
+      const float4 b = *reinterpret_cast<const float4*>(base + static_cast<size_t>(orow) * ldb + n);
+      r = make_float4(b.x + y.x, b.y + y.y, b.z + y.z, b.w + y.w);
+    } else {
+      r = y;
+    }
+    *reinterpret_cast<float4*>(out + static_cast<size_t>(orow) * ldo + n) = r;
+  }
+}
+
+// The same, one column per thread (rows not 16-byte aligned: the head's 4,097).
+__global__ void tc_reduce_scalar_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode,
+                                        float* out, int ldo, const float* base, int ldb, const int32_t* out_map,
+                                        int n0) {
   const size_t total = static_cast<size_t>(nb) * n_out;
   for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(e / n_out), n = static_cast<int>(e % n_out);
-    float y = 0.f;
-    for (int s = 0; s < slices; ++s) y += part[(static_cast<size_t>(s) * nb + m) * ldp + n];
     const int orow = out_map ? out_map[m] : m;
     if (orow < 0) continue;
+    float y = 0.f;
+    for (int s = 0; s < slices; ++s) y += part[(static_cast<size_t>(s) * nb + m) * ldp + n];
     float r;
     if (mode == GEMV_SWIGLU) {
       float u = 0.f;
       for (int s = 0; s < slices; ++s) u += part[(static_cast<size_t>(s) * nb + m) * ldp + n0 + n];
-      r = silu(y) * u;   // [P2] "The slow AR is Qwen3-4B": down(SiLU(gate) * up)
+      r = silu(y) * u;
     } else if (mode == GEMV_ADD) {
       r = base[static_cast<size_t>(orow) * ldb + n] + y;
     } else {
@@ -301,6 +363,8 @@ static bool cached_map(CUtensorMap* out, const void* base, int K, int rows, int 
 bool tc_eligible(const GemvArgs& a, int ldx) {
   if (!tc_available()) return false;
   if (a.nb < kTcMinRows || a.nb > kTcMaxRows || a.K % 64 != 0 || a.K > ldx) return false;
+  if (a.K > 4 * kSplitThreads * kSplitVec) return false;          // one row in registers
+  if (a.ldx % 4 != 0 || (a.save_x && a.lds % 4 != 0)) return false;   // float4 rows in the split
   if (a.x_src >= 0 || a.base_src >= 0 || a.out_src >= 0) return false;   // plain buffers only
   if (a.mode == GEMV_SWIGLU) return a.n0 % 128 == 0 && a.n1 == a.n0;
   return a.n1 == 0 || a.n0 % 128 == 0;
@@ -340,8 +404,8 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
       !cached_map(&mh, b.xh, a.K, kTcMaxRows, b.ldx, nbp) || !cached_map(&ml, b.xl, a.K, kTcMaxRows, b.ldx, nbp))
     return cudaErrorInvalidValue;
 
-  tc_split_kernel<<<a.nb, 256, 0, st>>>(a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh, b.xl, b.ldx, a.save_x, a.save_map,
-                                        a.lds);
+  tc_split_kernel<<<a.nb, kSplitThreads, 0, st>>>(a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh, b.xl, b.ldx, a.save_x,
+                                                  a.save_map, a.lds);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   TcArgs t{a.n0, a.n1, a.K, a.nb, kcps, b.part, n_rows, a.err, a.wait_limit_ns};
@@ -354,11 +418,16 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
   }
   if (e != cudaSuccess) return e;
   const int n_out = a.mode == GEMV_SWIGLU ? a.n0 : n_rows;
-  const size_t total = static_cast<size_t>(a.nb) * n_out;
+  const bool vec = n_out % 4 == 0 && n_rows % 4 == 0 && a.ldo % 4 == 0 && (a.mode != GEMV_ADD || a.ldb % 4 == 0);
+  const size_t total = static_cast<size_t>(a.nb) * (vec ? n_out / 4 : n_out);
   int rgrid = static_cast<int>((total + 255) / 256);
   rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
-  tc_reduce_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb,
-                                          a.out_map, a.n0);
+  if (vec)
+    tc_reduce_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb,
+                                            a.out_map, a.n0);
+  else
+    tc_reduce_scalar_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base,
+                                                   a.ldb, a.out_map, a.n0);
   if (launches) *launches += 3;
   return cudaGetLastError();
 }
