@@ -44,6 +44,8 @@ WORKLOADS = {
                         ras_win=10, desc="one-layer S2-Pro-shaped profiling case, batch 1, 512-token prompt"),
     "s2pro_b64": dict(cfg="s2pro", batch=64, prompt=0, frames=28, temperature=0.8, top_p=0.8, ras_win=10,
                       desc="full S2-Pro-shaped Dual-AR, batch 64, contexts uniform in [1024, 4096]"),
+    "s2pro_l1_b64": dict(cfg="s2pro_l1", batch=64, prompt=0, frames=8, temperature=0.8, top_p=0.8, ras_win=10,
+                         desc="one-layer S2-Pro-shaped profiling case, batch 64, contexts uniform in [1024, 4096]"),
     "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
                     desc="tiny Dual-AR, batch 1, 32-token prompt, 16 frames"),
 }
@@ -231,7 +233,7 @@ def main():
     if args.workload != "s2pro_b1":
         config["l2"] = "small profiling/parity workload, not a bench line"
 
-    if args.workload == "s2pro_b64":
+    if args.workload in ("s2pro_b64", "s2pro_l1_b64"):
         # the batch-64 measurement alone (also part of the default line)
         import torch
         from dual_ar_tts_frame_gb300 import build, upload_weights

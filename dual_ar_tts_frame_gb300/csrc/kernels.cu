@@ -363,23 +363,24 @@ cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int
 // Standalone launches of the ops in ops.cuh
 // ============================================================================
 constexpr int kAttnThreads = 512;   // same split as the persistent kernel (bit-identical paths)
+constexpr int kAttnBufs = 2;        // pages in flight per CTA (measured: a third does not help)
 
 template <int HD, int G>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __launch_bounds__(kAttnThreads, 2)
     attn_paged_kernel(DevPtrs d, int nrows, int layer, int total_units, int chunk_tokens,
                       int fuse_append, const uint16_t* q_norm, const uint16_t* k_norm) {
   extern __shared__ __align__(128) unsigned char attn_smem_raw[];
-  auto& sm = *reinterpret_cast<AttnSmem<HD, G, kAttnThreads, 2>*>(attn_smem_raw);
-  __shared__ uint64_t bars[2];
+  auto& sm = *reinterpret_cast<AttnSmem<HD, G, kAttnThreads, kAttnBufs>*>(attn_smem_raw);
+  __shared__ uint64_t bars[kAttnBufs];
   if (threadIdx.x == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int b = 0; b < kAttnBufs; ++b) mbar_init(&bars[b], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  uint32_t phase[2] = {0u, 0u};
-  attn_paged_units<HD, G, kAttnThreads, 2>(d, nrows, layer, total_units, chunk_tokens, fuse_append != 0,
-                                        q_norm, k_norm, sm, bars, phase, blockIdx.x, gridDim.x);
+  uint32_t phase[kAttnBufs];
+  for (int b = 0; b < kAttnBufs; ++b) phase[b] = 0u;
+  attn_paged_units<HD, G, kAttnThreads, kAttnBufs>(d, nrows, layer, total_units, chunk_tokens, fuse_append != 0,
+                                                   q_norm, k_norm, sm, bars, phase, blockIdx.x, gridDim.x);
 }
 
 template <int HD, int G>
@@ -387,7 +388,7 @@ static cudaError_t attn_paged_launch(const DevPtrs& d, int nrows, int layer, int
                                      int grid, int fuse, const uint16_t* qn, const uint16_t* kn,
                                      cudaStream_t st) {
   static bool configured = false;
-  const int smem = static_cast<int>(sizeof(AttnSmem<HD, G, kAttnThreads, 2>));
+  const int smem = static_cast<int>(sizeof(AttnSmem<HD, G, kAttnThreads, kAttnBufs>));
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_paged_kernel<HD, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

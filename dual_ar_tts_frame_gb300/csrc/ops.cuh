@@ -105,7 +105,7 @@ struct AttnSmem {
   static constexpr int TPT = NT / kPageTokens;   // threads per token (score pass)
   static constexpr int QD = HD / TPT;            // dims per thread (score pass)
   static constexpr int PARTS = NT / HD;          // token groups (value pass)
-  static constexpr int BUFS = NBUF;              // page buffers (2: double-buffered)
+  static constexpr int BUFS = NBUF;              // page buffers (a ring of NBUF pages in flight)
   uint16_t kv[NBUF][2][kPageTokens * HD];        // [buffer][K/V][tok][dim]
   float qs[G][TPT][QD + 1];
   float sc[G][kPageTokens];
@@ -119,7 +119,7 @@ struct AttnSmem {
 template <int HD, int G, int NT, int NBUF>
 DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens,
                            bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm,
-                           AttnSmem<HD, G, NT, NBUF>& sm, uint64_t* bars, uint32_t (&phase)[2], int cta,
+                           AttnSmem<HD, G, NT, NBUF>& sm, uint64_t* bars, uint32_t* phase, int cta,
                            int ncta, OpTags tg = OpTags{0u, 0u}) {
   using S = AttnSmem<HD, G, NT, NBUF>;
   constexpr int EPL = HD / 32;
@@ -177,8 +177,7 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
       bulk_load_g2s_plain(sm.kv[buf][1], vp, kPageBytes, &bars[buf]);
     };
     if (tid == 0) {
-      issue(0, 0);
-      if (NBUF > 1 && npages > 1) issue(1, 1);
+      for (int p = 0; p < NBUF && p < npages; ++p) issue(p, p);
     }
 
     if (fuse_append) {
@@ -230,7 +229,7 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     const int tok = tid / TPT, qd = tid % TPT;
     const int vdim = tid % HD, vpart = tid / HD;
     for (int p = 0; p < npages; ++p) {
-      const int buf = NBUF > 1 ? (p & 1) : 0;
+      const int buf = p % NBUF;
       const int ps = t0 + p * kPageTokens;
       const int ntok = min(kPageTokens, t1 - ps);
       if (!mbar_wait(&bars[buf], phase[buf], d.err, d.wait_limit_ns)) return;
