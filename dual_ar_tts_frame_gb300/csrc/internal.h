@@ -160,6 +160,12 @@ cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,
                               int chunk_tokens, int n_sm, bool fuse_append, const uint16_t* q_norm,
                               const uint16_t* k_norm, cudaStream_t st);
+// Tensor-core variant for launches of >= kAttnMmaMinRows rows (attn_mma.cu);
+// *used is false (nothing launched) when the shape or the driver rules it out.
+constexpr int kAttnMmaMinRows = 3;
+cudaError_t launch_attn_mma(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens, int n_sm,
+                            bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st,
+                            bool* used);
 cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* q_norm,
                              const uint16_t* k_norm, cudaStream_t st);
 cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms, int ldu,

@@ -417,6 +417,14 @@ cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_
                               const uint16_t* k_norm, cudaStream_t st) {
   if (nrows <= 0 || total_units <= 0) return cudaSuccess;
   if (d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0) return cudaErrorInvalidValue;
+  {
+    // 3+ rows: the tensor-core variant; 1-2 rows keep this kernel, the same
+    // device code as the persistent frame kernel (bit-identical paths)
+    bool used = false;
+    const cudaError_t e = launch_attn_mma(d, nrows, layer, total_units, chunk_tokens, n_sm, fuse_append, q_norm,
+                                          k_norm, st, &used);
+    if (e != cudaSuccess || used) return e;
+  }
   const int grid = total_units < 4 * n_sm ? total_units : 4 * n_sm;
   const int f = fuse_append ? 1 : 0;
   if (d.hd == 128) return attn_paged_hd<128>(d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st);

@@ -360,6 +360,10 @@ static bool cached_map(CUtensorMap* out, const void* base, int K, int rows, int 
   return true;
 }
 
+bool tc_bf16_map(CUtensorMap* out, const void* base, int K, int rows, int ld, int box_rows) {
+  return cached_map(out, base, K, rows, ld, box_rows);
+}
+
 bool tc_eligible(const GemvArgs& a, int ldx) {
   if (!tc_available()) return false;
   if (a.nb < kTcMinRows || a.nb > kTcMaxRows || a.K % 64 != 0 || a.K > ldx) return false;

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -27,6 +28,9 @@ bool tc_available();
 // Whether a projection can take the tensor-core path: 9..128 plain-buffer
 // rows, K a multiple of 64 and <= ldx, segment boundaries on 128 rows.
 bool tc_eligible(const GemvArgs& a, int ldx);
+// Tensor map of a bf16 matrix [rows][K] (row stride ld elements), tiles of
+// box_rows x 64 with 128-byte swizzle; built once per argument set and kept.
+bool tc_bf16_map(CUtensorMap* out, const void* base, int K, int rows, int ld, int box_rows);
 // Queues split, GEMM and reduce kernels; *launches += 3.
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches);
 
