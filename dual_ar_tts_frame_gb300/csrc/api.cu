@@ -478,7 +478,7 @@ void plan_attention(dualar_handle* h, LaunchSetup& s, int* units, int* chunk) {
   const int pages = (max_len + pt - 1) / pt;
   const long long target = 8LL * h->n_sm;
   const int ppc = std::max(std::max(1, (pages + kMaxChunks - 1) / kMaxChunks),
-                           static_cast<int>(page_units / target));
+                           std::min(kMaxChunkPages, static_cast<int>(page_units / target)));
   *chunk = ppc * pt;
   int u = 0;
   for (int r = 0; r < s.n_rows; ++r) {

@@ -48,8 +48,9 @@ struct AmSmem {
   float cm[kAmWarps][8], cl[kAmWarps][8];
   float co[kAmWarps][G][HD];
   float knew[HD], vnew[HD];
+  RowInfo rows[kMaxRows];   // the launch's rows (read once)
   uint64_t full[AmCfg<HD>::NBUF], empty[AmCfg<HD>::NBUF];
-  int abort_flag, s_last;
+  int abort_flag, s_last, unit_ok;
 };
 
 template <int HD, int G>
@@ -110,15 +111,17 @@ struct AmUnit {
   const int32_t* ptab;
 };
 
-DEVI bool am_unit(const DevPtrs& d, int nrows, int u, int chunk_tokens, AmUnit& un) {
+// Unit u's row and chunk (from the launch's rows in shared memory); false for
+// an inactive row.
+DEVI bool am_unit(const DevPtrs& d, const RowInfo* rows, int nrows, int u, int chunk_tokens, AmUnit& un) {
   int lo = 0, hi = nrows - 1;   // rows are sorted by unit0
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (ldi(&d.rows[mid].unit0) <= u) lo = mid;
+    if (rows[mid].unit0 <= u) lo = mid;
     else hi = mid - 1;
   }
   un.r = lo;
-  un.ri = ld_row(&d.rows[lo]);
+  un.ri = rows[lo];
   const int L = un.ri.pos + 1;
   un.nch = (L + chunk_tokens - 1) / chunk_tokens;
   const int local = u - un.ri.unit0;
@@ -129,12 +132,23 @@ DEVI bool am_unit(const DevPtrs& d, int nrows, int u, int chunk_tokens, AmUnit& 
   un.t1 = min(L, un.t0 + chunk_tokens);
   un.npages = (un.t1 - un.t0 + kPageTokens - 1) / kPageTokens;
   un.ptab = d.page_table + static_cast<size_t>(un.ri.slot) * d.pages_per_seq + un.t0 / kPageTokens;
-  for (int p = 0; p < un.npages; ++p) {
-    const int pg = ldi(un.ptab + p);
-    if (pg < 0 || pg >= d.max_pages) return false;
-  }
   return true;
 }
+
+// Whole warp: page p's index for p = lane + 32 * i in pg[i] (-1 beyond the
+// unit); false if any index is out of range.  One round trip.
+template <int NPG>
+DEVI bool am_pages(const DevPtrs& d, const AmUnit& un, int lane, int (&pg)[NPG]) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < NPG; ++i) {
+    const int p = lane + 32 * i;
+    pg[i] = p < un.npages ? ldi(un.ptab + p) : -1;
+    if (p < un.npages && (pg[i] < 0 || pg[i] >= d.max_pages)) ok = false;
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+constexpr int kAmPageRegs = (kMaxChunkPages + 31) / 32;
 
 template <int HD, int G>
 __global__ void __launch_bounds__(kAmThreads, 1)
@@ -159,36 +173,49 @@ __global__ void __launch_bounds__(kAmThreads, 1)
     sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  for (int i = tid; i < nrows; i += kAmThreads) sm.rows[i] = ld_row(&d.rows[i]);
   __syncthreads();
   const volatile int* abort_flag = &sm.abort_flag;
 
   if (warp == kAmWarps) {
-    // ---- producer: the K/V pages of this CTA's units, in order
-    if (lane == 0) {
-      uint32_t gs = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        AmUnit un;
-        if (!am_unit(d, nrows, u, chunk_tokens, un)) continue;
-        for (int p = 0; p < un.npages; ++p) {
-          const int s = static_cast<int>(gs % NB);
+    // ---- producer (the whole warp; lane 0 issues): the K/V pages of this
+    // CTA's units, in order
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      AmUnit un;
+      if (!am_unit(d, sm.rows, nrows, u, chunk_tokens, un)) continue;
+      int pg[kAmPageRegs];
+      if (!am_pages(d, un, lane, pg)) continue;
+      for (int p = 0; p < un.npages; ++p) {
+        int pgp = 0;
+#pragma unroll
+        for (int i = 0; i < kAmPageRegs; ++i) {
+          const int v = __shfl_sync(0xFFFFFFFFu, pg[i], p & 31);
+          if ((p >> 5) == i) pgp = v;
+        }
+        const int s = static_cast<int>(gs % NB);
+        if (lane == 0) {
           if (gs >= static_cast<uint32_t>(NB) && !am_wait(&sm.empty[s], ((gs / NB) - 1) & 1, abort_flag, d)) {
             sm.abort_flag = 1;
             ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::PAGE));
-          const int pg = ldi(un.ptab + p);
-          const int rowk = static_cast<int>(((static_cast<long long>(pg) * d.n_layer + layer) * 2 * hkv + un.g) * 64);
-          const int rowv = rowk + hkv * 64;
+          } else {
+            mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::PAGE));
+            const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + un.g) * 64);
+            const int rowv = rowk + hkv * 64;
 #pragma unroll
-          for (int hh = 0; hh < C::HALVES; ++hh) {
-            tma_load_2d(ring + s * C::PAGE + hh * kAmBox, &tkv, hh * 64, rowk, &sm.full[s]);
-            tma_load_2d(ring + s * C::PAGE + (C::HALVES + hh) * kAmBox, &tkv, hh * 64, rowv, &sm.full[s]);
+            for (int hh = 0; hh < C::HALVES; ++hh) {
+              tma_load_2d(ring + s * C::PAGE + hh * kAmBox, &tkv, hh * 64, rowk, &sm.full[s]);
+              tma_load_2d(ring + s * C::PAGE + (C::HALVES + hh) * kAmBox, &tkv, hh * 64, rowv, &sm.full[s]);
+            }
           }
-          ++gs;
         }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        ++gs;
       }
+    }
+    if (lane == 0) {
       // every copy issued here lands before the CTA exits (bounded)
       for (uint32_t i = gs > static_cast<uint32_t>(NB) ? gs - NB : 0; i < gs; ++i) {
         const uint64_t t0 = global_timer_ns();
@@ -205,9 +232,14 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   uint32_t gs_base = 0;
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     AmUnit un;
-    if (!am_unit(d, nrows, u, chunk_tokens, un)) {
-      if (un.ri.active && un.g < hkv && tid == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
-      continue;
+    if (!am_unit(d, sm.rows, nrows, u, chunk_tokens, un)) continue;
+    if (warp == 0) {
+      int pg[kAmPageRegs];
+      const bool pages_ok = am_pages(d, un, lane, pg);
+      if (lane == 0) {
+        sm.unit_ok = pages_ok ? 1 : 0;
+        if (!pages_ok) raise_error(d.err, DEV_ERR_BAD_PAGE);
+      }
     }
     const int r = un.r;
     const bool newest = fuse && un.c == un.nch - 1;
@@ -250,6 +282,10 @@ __global__ void __launch_bounds__(kAmThreads, 1)
       }
     }
     named_barrier(1, kAmWarps * 32);
+    if (!sm.unit_ok) {
+      named_barrier(1, kAmWarps * 32);   // (the producer skipped it too)
+      continue;
+    }
     // Q fragments (rows gr < G real; rows gr + 8 are zero)
     uint32_t qh[HD / 16][2], ql[HD / 16][2];
 #pragma unroll
@@ -473,7 +509,8 @@ cudaError_t launch_attn_mma(const DevPtrs& d, int nrows, int layer, int total_un
                             bool* used) {
   *used = false;
   if (nrows < kAttnMmaMinRows || total_units <= 0 || !tc_available()) return cudaSuccess;
-  if ((d.hd != 64 && d.hd != 128) || d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0)
+  if ((d.hd != 64 && d.hd != 128) || d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0 ||
+      chunk_tokens / kPageTokens > kMaxChunkPages || nrows > kMaxRows)
     return cudaSuccess;
   const long long rows = static_cast<long long>(d.max_pages) * d.n_layer * 2 * d.Hkv * kPageTokens;
   if (rows >= (1LL << 31)) return cudaSuccess;

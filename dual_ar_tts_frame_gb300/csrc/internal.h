@@ -11,6 +11,7 @@ constexpr int kMaxRows = 128;        // rows per launch: decode batch or prefill
 constexpr int kMaxCodebooks = 16;
 constexpr int kRasRing = 16;         // RAS history ring per slot (window <= 16)
 constexpr int kMaxChunks = 64;       // split-KV chunks per (row, KV head)
+constexpr int kMaxChunkPages = 64;   // pages per split-KV chunk
 constexpr int kMaxGroup = 8;         // query heads per KV head
 #ifndef DUALAR_GEMV_WARPS
 #define DUALAR_GEMV_WARPS 16
