@@ -44,6 +44,8 @@ struct dualar_handle {
   bool use_mega = true;
   bool use_tc = true;            // dualar_set_tensor_cores
   TcBuffers tc{};                // tensor-core projection buffers
+  const float* tc_ready_x = nullptr;   // the tc buffers hold the halves of this [nb][K] input
+  int tc_ready_k = 0, tc_ready_nb = 0;
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
   uint64_t* tagged = nullptr;    // the tagged work buffers (one region)
@@ -205,15 +207,27 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
     CUDA_TRY(h, cudaEventRecord(e0, h->stream));
   }
   if (h->use_tc && tc_eligible(a, h->tc.ldx)) {
-    // 9..128 rows: one pass over the weights on the tensor cores
+    // 9..128 rows: one pass over the weights on the tensor cores.  The
+    // SwiGLU output feeds the down projection without norm: its reduce
+    // writes the halves the next GEMM reads, and that split is skipped.
     int n = 0;
-    const cudaError_t e = launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n);
+    const bool ready = h->tc_ready_x == a.x && h->tc_ready_k == a.K && h->tc_ready_nb == a.nb &&
+                       a.ldx == a.K && a.norm_w == nullptr && a.save_x == nullptr;
+    const bool split_out = a.mode == GEMV_SWIGLU && a.out_map == nullptr && a.ldo == a.n0;
+    h->tc_ready_x = nullptr;
+    const cudaError_t e = launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n, ready, split_out);
+    if (e == cudaSuccess && split_out) {
+      h->tc_ready_x = a.out;
+      h->tc_ready_k = a.n0;
+      h->tc_ready_nb = a.nb;
+    }
     h->launches += n;
     if (e != cudaSuccess) {
       set_err(h, "tensor-core projection failed: %s", cudaGetErrorString(e));
       return DUALAR_ERR_CUDA;
     }
   } else {
+    h->tc_ready_x = nullptr;
     LAUNCH(h, launch_gemv(a, h->n_sm, h->stream));
   }
   if (h->profiling) {

@@ -249,26 +249,39 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // Sum of the K-slice partials (slice order) and the epilogue, 4 columns per
 // thread (all row strides multiples of 4 floats).
 __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
-                                 int ldo, const float* base, int ldb, const int32_t* out_map, int n0) {
+                                 int ldo, const float* base, int ldb, const int32_t* out_map, int n0, uint16_t* xh,
+                                 uint16_t* xl, int ldxh) {
   const int nq = n_out >> 2;   // n_out % 4 == 0 (host)
   const size_t total = static_cast<size_t>(nb) * nq;
+  // the slices' partials, four loads in flight, added in slice order
+  auto sum = [&](const float* p0, size_t stride) {
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= slices; s += 4) {
+      float4 q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const float4*>(p0 + (s + k) * stride);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        y.x += q[k].x; y.y += q[k].y; y.z += q[k].z; y.w += q[k].w;
+      }
+    }
+    for (; s < slices; ++s) {
+      const float4 q = *reinterpret_cast<const float4*>(p0 + s * stride);
+      y.x += q.x; y.y += q.y; y.z += q.z; y.w += q.w;
+    }
+    return y;
+  };
   for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(e / nq), n = 4 * static_cast<int>(e % nq);
     const int orow = out_map ? out_map[m] : m;
     if (orow < 0) continue;
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < slices; ++s) {
-      const float4 p = *reinterpret_cast<const float4*>(part + (static_cast<size_t>(s) * nb + m) * ldp + n);
-      y.x += p.x; y.y += p.y; y.z += p.z; y.w += p.w;
-    }
+    const size_t stride = static_cast<size_t>(nb) * ldp;
+    const float4 y = sum(part + static_cast<size_t>(m) * ldp + n, stride);
     float4 r;
     if (mode == GEMV_SWIGLU) {
-      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < slices; ++s) {
-        const float4 p = *reinterpret_cast<const float4*>(part + (static_cast<size_t>(s) * nb + m) * ldp + n0 + n);
-        u.x += p.x; u.y += p.y; u.z += p.z; u.w += p.w;
-      }
+      const float4 u = sum(part + static_cast<size_t>(m) * ldp + n0 + n, stride);
       // [P2] "The slow AR is Qwen3-4B": down(SiLU(gate) * up)
       r = make_float4(silu(y.x) * u.x, silu(y.y) * u.y, silu(y.z) * u.z, silu(y.w) * u.w);
     } else if (mode == GEMV_ADD) {
@@ -278,6 +291,19 @@ __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp,
       r = y;
     }
     *reinterpret_cast<float4*>(out + static_cast<size_t>(orow) * ldo + n) = r;
+    if (xh != nullptr) {
+      // the output is the next projection's input (no norm): its bf16 halves
+      const float e4[4] = {r.x, r.y, r.z, r.w};
+      uint32_t hh[4], ll[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint16_t hb = f32_to_bf16bits(e4[c]);
+        hh[c] = hb;
+        ll[c] = f32_to_bf16bits(e4[c] - bf16bits_to_f32(hb));
+      }
+      *reinterpret_cast<uint2*>(xh + static_cast<size_t>(m) * ldxh + n) = make_uint2(hh[0] | (hh[1] << 16), hh[2] | (hh[3] << 16));
+      *reinterpret_cast<uint2*>(xl + static_cast<size_t>(m) * ldxh + n) = make_uint2(ll[0] | (ll[1] << 16), ll[2] | (ll[3] << 16));
+    }
   }
 }
 
@@ -389,7 +415,8 @@ static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1,
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches) {
+cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
+                           bool x_ready, bool split_out) {
   const int nbp = a.nb <= 16 ? 16 : a.nb <= 32 ? 32 : a.nb <= 64 ? 64 : 128;
   const int n_rows = a.n0 + a.n1;   // virtual weight rows (SwiGLU: gate then up)
   const int tiles = (n_rows + 255) / 256;
@@ -408,10 +435,14 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
       !cached_map(&mh, b.xh, a.K, kTcMaxRows, b.ldx, nbp) || !cached_map(&ml, b.xl, a.K, kTcMaxRows, b.ldx, nbp))
     return cudaErrorInvalidValue;
 
-  tc_split_kernel<<<a.nb, kSplitThreads, 0, st>>>(a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh, b.xl, b.ldx, a.save_x,
-                                                  a.save_map, a.lds);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!x_ready) {
+    tc_split_kernel<<<a.nb, kSplitThreads, 0, st>>>(a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh, b.xl, b.ldx, a.save_x,
+                                                    a.save_map, a.lds);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (launches) *launches += 1;
+  }
   TcArgs t{a.n0, a.n1, a.K, a.nb, kcps, b.part, n_rows, a.err, a.wait_limit_ns};
   const dim3 grid(tiles, slices);
   switch (nbp) {
@@ -423,16 +454,18 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
   if (e != cudaSuccess) return e;
   const int n_out = a.mode == GEMV_SWIGLU ? a.n0 : n_rows;
   const bool vec = n_out % 4 == 0 && n_rows % 4 == 0 && a.ldo % 4 == 0 && (a.mode != GEMV_ADD || a.ldb % 4 == 0);
+  if (split_out && (!vec || a.out_map != nullptr || n_out > b.ldx)) return cudaErrorInvalidValue;
   const size_t total = static_cast<size_t>(a.nb) * (vec ? n_out / 4 : n_out);
   int rgrid = static_cast<int>((total + 255) / 256);
   rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
   if (vec)
     tc_reduce_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb,
-                                            a.out_map, a.n0);
+                                            a.out_map, a.n0, split_out ? b.xh : nullptr, split_out ? b.xl : nullptr,
+                                            b.ldx);
   else
     tc_reduce_scalar_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base,
                                                    a.ldb, a.out_map, a.n0);
-  if (launches) *launches += 3;
+  if (launches) *launches += 2;
   return cudaGetLastError();
 }
 

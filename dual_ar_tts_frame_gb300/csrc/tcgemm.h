@@ -31,7 +31,10 @@ bool tc_eligible(const GemvArgs& a, int ldx);
 // Tensor map of a bf16 matrix [rows][K] (row stride ld elements), tiles of
 // box_rows x 64 with 128-byte swizzle; built once per argument set and kept.
 bool tc_bf16_map(CUtensorMap* out, const void* base, int K, int rows, int ld, int box_rows);
-// Queues split, GEMM and reduce kernels; *launches += 3.
-cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches);
+// Queues split (unless x_ready: the buffers already hold x's halves), GEMM
+// and reduce kernels; split_out: the reduce also writes the output's halves
+// (it is the next projection's input, without norm).  *launches += count.
+cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
+                           bool x_ready = false, bool split_out = false);
 
 }  // namespace dualar
