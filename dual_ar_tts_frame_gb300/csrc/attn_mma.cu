@@ -11,9 +11,12 @@
 //   online softmax over the page on the fragment rows,
 //   O += P V   (P as bf16 hi + lo halves built from the S fragments).
 // Pages arrive by TMA (128-byte swizzle, so ldmatrix reads are conflict-free)
-// into a ring of shared-memory stages fed by a producer warp that walks the
-// CTA's pages across units; four compute warps take a unit's pages
-// round-robin and merge their (m, l, O) in warp order.  Decode (fuse): the
+// from a producer warp that walks the CTA's pages across units.  Page number
+// n (counted over the CTA's whole launch) belongs to compute warp n % 4, which
+// owns a small ring of slots (each the K or the V block of a page) and takes
+// them in order: every slot has a single consumer, so an mbarrier wait is
+// never more than one phase ahead of its barrier (a parity wait cannot tell
+// phases two apart).  The warps merge their (m, l, O) in warp order.  Decode (fuse): the
 // unit holding the newest position computes its K/V (QK-norm, RoPE), writes
 // them to the cache and patches the page's row in shared memory, since the
 // page copy may predate the write.
@@ -37,8 +40,9 @@ constexpr int kAmBox = 64 * 64 * 2;                // one TMA box: 64 tokens x 6
 template <int HD>
 struct AmCfg {
   static constexpr int HALVES = HD / 64;                  // boxes per 64-token K (or V) block
-  static constexpr int PAGE = 2 * HALVES * kAmBox;        // K and V of one page
-  static constexpr int NBUF = HD == 128 ? 6 : 8;          // ring stages
+  static constexpr int SLOT = HALVES * kAmBox;            // a slot: the K or the V block of one page
+  static constexpr int SLOTS = HD == 128 ? 3 : 4;         // slots of each compute warp
+  static constexpr int NBUF = kAmWarps * SLOTS;
 };
 
 template <int HD, int G>
@@ -55,7 +59,7 @@ struct AmSmem {
 
 template <int HD, int G>
 constexpr size_t am_smem_bytes() {
-  return static_cast<size_t>(AmCfg<HD>::NBUF) * AmCfg<HD>::PAGE + sizeof(AmSmem<HD, G>) + 1024;
+  return static_cast<size_t>(AmCfg<HD>::NBUF) * AmCfg<HD>::SLOT + sizeof(AmSmem<HD, G>) + 1024;
 }
 
 DEVI void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -98,7 +102,7 @@ DEVI bool am_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > d.wait_limit_ns) {
-      raise_error(d.err, DEV_ERR_MBAR_TIMEOUT);
+      raise_error(d.err, DEV_ERR_MBAR_TIMEOUT | DEV_ERR_ATTN_WAIT);
       return false;
     }
   }
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   static_assert(G >= 1 && G <= 8, "query heads per KV head: the MMA rows 0..7");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  AmSmem<HD, G>& sm = *reinterpret_cast<AmSmem<HD, G>*>(ring + NB * C::PAGE);
+  AmSmem<HD, G>& sm = *reinterpret_cast<AmSmem<HD, G>*>(ring + NB * C::SLOT);
   const uint32_t ring_s = smem_addr(ring);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hkv = d.Hkv, hq = d.Hq;
@@ -181,6 +185,10 @@ __global__ void __launch_bounds__(kAmThreads, 1)
     // ---- producer (the whole warp; lane 0 issues): the K/V pages of this
     // CTA's units, in order
     uint32_t gs = 0;
+    uint32_t cnt[kAmWarps];   // slot fills given to each compute warp so far
+    uint32_t iss[kAmWarps];   // ... and actually issued (lane 0)
+#pragma unroll
+    for (int w = 0; w < kAmWarps; ++w) cnt[w] = iss[w] = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       AmUnit un;
@@ -194,19 +202,28 @@ __global__ void __launch_bounds__(kAmThreads, 1)
           const int v = __shfl_sync(0xFFFFFFFFu, pg[i], p & 31);
           if ((p >> 5) == i) pgp = v;
         }
-        const int s = static_cast<int>(gs % NB);
-        if (lane == 0) {
-          if (gs >= static_cast<uint32_t>(NB) && !am_wait(&sm.empty[s], ((gs / NB) - 1) & 1, abort_flag, d)) {
-            sm.abort_flag = 1;
-            ok = false;
-          } else {
-            mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::PAGE));
-            const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + un.g) * 64);
-            const int rowv = rowk + hkv * 64;
+        const int w = static_cast<int>(gs % kAmWarps);
+        const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + un.g) * 64);
 #pragma unroll
-            for (int hh = 0; hh < C::HALVES; ++hh) {
-              tma_load_2d(ring + s * C::PAGE + hh * kAmBox, &tkv, hh * 64, rowk, &sm.full[s]);
-              tma_load_2d(ring + s * C::PAGE + (C::HALVES + hh) * kAmBox, &tkv, hh * 64, rowv, &sm.full[s]);
+        for (int kv = 0; kv < 2; ++kv) {
+          uint32_t j = 0;
+#pragma unroll
+          for (int ww = 0; ww < kAmWarps; ++ww)
+            if (ww == w) j = cnt[ww]++;
+          const int s = w * C::SLOTS + static_cast<int>(j % C::SLOTS);
+          if (lane == 0 && ok) {
+            if (j >= static_cast<uint32_t>(C::SLOTS) &&
+                !am_wait(&sm.empty[s], ((j / C::SLOTS) - 1) & 1, abort_flag, d)) {
+              sm.abort_flag = 1;
+              ok = false;
+            } else {
+              mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::SLOT));
+#pragma unroll
+              for (int hh = 0; hh < C::HALVES; ++hh)
+                tma_load_2d(ring + s * C::SLOT + hh * kAmBox, &tkv, hh * 64, rowk + kv * hkv * 64, &sm.full[s]);
+#pragma unroll
+              for (int ww = 0; ww < kAmWarps; ++ww)
+                if (ww == w) ++iss[ww];
             }
           }
         }
@@ -217,11 +234,12 @@ __global__ void __launch_bounds__(kAmThreads, 1)
     }
     if (lane == 0) {
       // every copy issued here lands before the CTA exits (bounded)
-      for (uint32_t i = gs > static_cast<uint32_t>(NB) ? gs - NB : 0; i < gs; ++i) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&sm.full[i % NB], (i / NB) & 1))
-          if (global_timer_ns() - t0 > d.wait_limit_ns) break;
-      }
+      for (int w = 0; w < kAmWarps; ++w)
+        for (uint32_t j = iss[w] > static_cast<uint32_t>(C::SLOTS) ? iss[w] - C::SLOTS : 0; j < iss[w]; ++j) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(&sm.full[w * C::SLOTS + j % C::SLOTS], (j / C::SLOTS) & 1))
+            if (global_timer_ns() - t0 > d.wait_limit_ns) break;
+        }
     }
     return;
   }
@@ -230,6 +248,7 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   const float qscale = 1.0f / sqrtf(static_cast<float>(HD));
   const int gr = lane >> 2, tq = lane & 3;   // fragment row (head) and column pair
   uint32_t gs_base = 0;
+  uint32_t mine = 0;   // pages this warp has taken so far (its slot sequence)
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     AmUnit un;
     if (!am_unit(d, sm.rows, nrows, u, chunk_tokens, un)) continue;
@@ -302,14 +321,17 @@ __global__ void __launch_bounds__(kAmThreads, 1)
 #pragma unroll
     for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-    for (int p = warp; p < un.npages; p += kAmWarps) {
-      const uint32_t gs = gs_base + p;
-      const int s = static_cast<int>(gs % NB);
-      const bool got = am_wait(&sm.full[s], (gs / NB) & 1, abort_flag, d);
+    const int p0 = static_cast<int>((warp - static_cast<int>(gs_base % kAmWarps) + kAmWarps) % kAmWarps);
+    for (int p = p0; p < un.npages; p += kAmWarps) {
+      const uint32_t jk = mine++, jv = mine++;
+      const int sk = warp * C::SLOTS + static_cast<int>(jk % C::SLOTS);
+      const int sv = warp * C::SLOTS + static_cast<int>(jv % C::SLOTS);
+      bool got = am_wait(&sm.full[sk], (jk / C::SLOTS) & 1, abort_flag, d);
+      got = am_wait(&sm.full[sv], (jv / C::SLOTS) & 1, abort_flag, d) && got;
       if (!got) sm.abort_flag = 1;   // the others stop waiting too
       const int ps = un.t0 + p * kPageTokens;
       const int ntok = min(kPageTokens, un.t1 - ps);
-      const uint32_t kb = ring_s + s * C::PAGE, vb = kb + C::HALVES * kAmBox;
+      const uint32_t kb = ring_s + sk * C::SLOT, vb = ring_s + sv * C::SLOT;
       if (got && newest && ps <= un.ri.pos && un.ri.pos < ps + kPageTokens) {
         // the newest row (its copy may predate the cache write)
         const int rr = un.ri.pos - ps;
@@ -401,7 +423,10 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[s]);   // the stage is free (reads done: values used above)
+      if (lane == 0) {   // both slots are free (reads done: their values were used above)
+        mbar_arrive(&sm.empty[sk]);
+        mbar_arrive(&sm.empty[sv]);
+      }
     }
     gs_base += un.npages;
 

@@ -26,6 +26,8 @@ enum : uint32_t {
   DEV_ERR_GRID_TIMEOUT = 1u << 1,   // a grid-wide barrier gave up
   DEV_ERR_BAD_INDEX = 1u << 2,      // an index failed its bounds check (access skipped)
   DEV_ERR_BAD_PAGE = 1u << 3,       // a page-table entry was out of range (access skipped)
+  DEV_ERR_TC_WAIT = 1u << 4,        // with MBAR_TIMEOUT: in the tensor-core projection (tcgemm.cu)
+  DEV_ERR_ATTN_WAIT = 1u << 5,      // with MBAR_TIMEOUT: in the tensor-core attention (attn_mma.cu)
 };
 
 // One row of a launch: a sequence (slot) writing one position.

@@ -110,7 +110,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int issued = 0;
       for (int i = 0; i < nch; ++i) {
         const int s = i % S;
-        if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, a.err, a.wait_limit_ns)) break;
+        if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, a.err, a.wait_limit_ns)) {
+          raise_error(a.err, DEV_ERR_TC_WAIT);
+          break;
+        }
         unsigned char* st = smem + s * SB;
         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(SB));
         const int kx = (c0 + i) * 64;
@@ -137,7 +140,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, NBP);
       for (int i = 0; i < nch; ++i) {
         const int s = i % S;
-        if (!mbar_wait(&full[s], (i / S) & 1, a.err, a.wait_limit_ns)) break;
+        if (!mbar_wait(&full[s], (i / S) & 1, a.err, a.wait_limit_ns)) {
+          raise_error(a.err, DEV_ERR_TC_WAIT | (1u << 6));
+          break;
+        }
         tc_fence_after();
         unsigned char* st = smem + s * SB;
         const uint64_t dxh = smem_desc_sw128(st + 2 * kTcWTile);
@@ -160,7 +166,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ---- read-back: warp w may access TMEM lanes 32*(w%4) .. +31
     const int q = warp & 3;
-    if (mbar_wait(&accf[0], 0, a.err, a.wait_limit_ns)) {
+    const bool accd = mbar_wait(&accf[0], 0, a.err, a.wait_limit_ns);
+    if (!accd && lane == 0) raise_error(a.err, DEV_ERR_TC_WAIT | (1u << 7));
+    if (accd) {
       tc_fence_after();
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
