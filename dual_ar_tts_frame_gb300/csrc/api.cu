@@ -445,6 +445,7 @@ int build_mega_program(dualar_handle* h, int nb) {
     float* x = l == 0 ? F(d.xs_t) : F(d.hs_t);
     const int x_src = hs_src;
     const int qkv = gemv(args_qkv(h, lw, nb, nullptr), x, x_src, nullptr, -1, F(d.qkv_t), true);
+    ops[qkv].pos = l + 1;   // its attention's first pages are fetched during it
     const int at = attn_op(MOP_ATTN_PAGED, l, 0, qkv, c.slow_qk_norm, lw);
     hs_src = gemv(args_o(h, lw, nb, nullptr, nullptr), F(d.attn_t), at, x, x_src, F(d.hs_t), true);
     const int act = gemv(args_gateup(h, lw, nb, nullptr), F(d.hs_t), hs_src, nullptr, -1, F(d.act_t), true);

@@ -22,7 +22,8 @@ enum MegaOpType : int {
 struct alignas(16) MegaOp {
   int type;
   int layer;
-  int pos;     // fast attention: codebook position; fast sample: codebook k
+  int pos;     // fast attention: codebook position; fast sample: codebook k;
+               // GEMV: 1 + layer of the paged attention that follows it (0: none)
   int in_src;  // attention, fast sample: index of the op that wrote the input
   const uint16_t* q_norm;
   const uint16_t* k_norm;
