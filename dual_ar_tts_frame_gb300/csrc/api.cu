@@ -805,6 +805,7 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
   ALLOC(d.logits, R * d.logit_ld);
   ALLOC(d.part, R * c.n_kv_head * kMaxChunks * G * (c.head_dim + 2));
   ALLOC(d.arrive, R * c.n_kv_head);
+  ALLOC(d.sched, c.n_layer);
   ALLOC(d.codes_ws, R * kMaxCodebooks);
   ALLOC(d.err, 1);
   ALLOC(h->bar_counter, 1);

@@ -4,22 +4,38 @@
 // Same work units as attn_paged_units (row, KV head, chunk of pages), the
 // same partial-sum format and the same deterministic last-arriver combine.
 // Inside a unit the G query heads of the KV head are the rows of warp-level
-// MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulators; G <= 8 of the 16
-// rows are real -- tcgen05's M >= 64 would waste far more):
-//   S = Q K^T  (Q: the unit's query heads, 1/sqrt(hd) folded in, as bf16
-//               hi + lo halves; K: a 64-token page),
+// MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulators; tcgen05's
+// M >= 64 would waste far more):
+//   S = Q K^T  (Q: the unit's query heads, 1/sqrt(hd) folded in, split into
+//               bf16 hi + lo halves that sit in different rows of the same
+//               MMA: rows h and h + 4 for G <= 4, rows h and h + 8 for G = 8;
+//               the two row results are added afterwards),
 //   online softmax over the page on the fragment rows,
-//   O += P V   (P as bf16 hi + lo halves built from the S fragments).
-// Pages arrive by TMA (128-byte swizzle, so ldmatrix reads are conflict-free)
-// from a producer warp that walks the CTA's pages across units.  Page number
-// n (counted over the CTA's whole launch) belongs to compute warp n % 4, which
-// owns a small ring of slots (each the K or the V block of a page) and takes
-// them in order: every slot has a single consumer, so an mbarrier wait is
-// never more than one phase ahead of its barrier (a parity wait cannot tell
-// phases two apart).  The warps merge their (m, l, O) in warp order.  Decode (fuse): the
-// unit holding the newest position computes its K/V (QK-norm, RoPE), writes
-// them to the cache and patches the page's row in shared memory, since the
-// page copy may predate the write.
+//   O += P V   (P split into hi + lo rows the same way).
+// A CTA has seven warps with fixed roles, chained by mbarriers:
+//  * prep (warp 5) takes units from a per-layer counter shared by all CTAs
+//    (a CTA that finishes early takes more): first every full chunk, row
+//    by row, then every row's last (partial) chunk, rows ordered by that
+//    chunk's page count, largest first.  For each it loads the page
+//    indices, the query rows (QK-norm and RoPE when fused), and for the
+//    unit holding the newest position that position's K/V, which it writes
+//    to the cache; it publishes the unit in one of two shared-memory
+//    descriptors;
+//  * producer (warp 4, one lane) copies the units' K and V pages by TMA
+//    (128-byte swizzle, so ldmatrix reads are conflict-free).  Page p of
+//    unit u goes to compute warp (p + u) % 4 (a function of the unit alone,
+//    so the rounding of the result does not depend on the schedule), which
+//    owns a small ring of slots (each the K or the V block of a page) and
+//    takes them in order: every slot has a single consumer, so an mbarrier
+//    wait is never more than one phase ahead of its barrier (a parity wait
+//    cannot tell phases two apart);
+//  * compute (warps 0-3) run the MMAs and hand their (m, l, O) to
+//  * finalize (warp 6), which merges the four in warp order, writes the
+//    partial (or the output), and for the last chunk of a (row, KV head) to
+//    arrive combines the chunks in chunk order.
+// The compute warps thus never wait on global memory between units.  The
+// page copy of the newest position may predate its cache write; the compute
+// warp patches that row in shared memory from the descriptor.
 // [P2] "The slow AR is Qwen3-4B" (GQA: 32 query heads over 8 KV heads,
 // qk-norm, RoPE) and "Streaming: whose numbers" (bf16 RoPE tables).
 #include <cuda.h>
@@ -34,8 +50,12 @@
 namespace dualar {
 
 constexpr int kAmWarps = 4;                        // compute warps
-constexpr int kAmThreads = (kAmWarps + 1) * 32;    // + the producer warp
+constexpr int kAmProducer = kAmWarps;              // page copies
+constexpr int kAmPrep = kAmWarps + 1;              // unit set-up
+constexpr int kAmFinal = kAmWarps + 2;             // merge and combine
+constexpr int kAmThreads = (kAmWarps + 3) * 32;
 constexpr int kAmBox = 64 * 64 * 2;                // one TMA box: 64 tokens x 64 dims (bf16)
+constexpr uint32_t kAmUnitUsers = 1 + kAmWarps + 1;   // producer, compute warps, finalize
 
 template <int HD>
 struct AmCfg {
@@ -45,16 +65,35 @@ struct AmCfg {
   static constexpr int NBUF = kAmWarps * SLOTS;
 };
 
+// One unit as the prep warp publishes it.
+template <int HD, int G>
+struct AmUnitDesc {
+  float q[G][HD];                         // query rows, 1/sqrt(hd) folded in
+  uint32_t knew[HD / 2], vnew[HD / 2];    // newest position's K and V (bf16 pairs)
+  int32_t pages[kMaxChunkPages];
+  int32_t r, g, c, nch, t0, t1, npages, pos, newest, rot, last;
+};
+
+// The launch's rows and the unit order built from them.
+struct AmSmemRows {
+  RowInfo rows[kMaxRows];    // read once at the start
+  int32_t fpre[kMaxRows];    // full-chunk units before each row
+  int32_t lorder[kMaxRows];  // active rows by last-chunk page count, largest first
+  int32_t lcur[kMaxChunkPages + 1];
+};
+static_assert(kMaxRows == 4 * 32, "the prep warp's row scan: four rows per lane");
+
 template <int HD, int G>
 struct AmSmem {
-  // after the ring (offsets in floats / elements from the end of the ring)
-  float qs[G][HD];
-  float cm[kAmWarps][8], cl[kAmWarps][8];
+  // after the ring
+  AmUnitDesc<HD, G> unit[2];
   float co[kAmWarps][G][HD];
-  float knew[HD], vnew[HD];
-  RowInfo rows[kMaxRows];   // the launch's rows (read once)
+  float cm[kAmWarps][8], cl[kAmWarps][8];
+  float fc[8][kMaxChunks];   // finalize: chunk weights of each head
+  AmSmemRows t;
   uint64_t full[AmCfg<HD>::NBUF], empty[AmCfg<HD>::NBUF];
-  int abort_flag, s_last, unit_ok;
+  uint64_t ufull[2], uempty[2], cfull, cempty;
+  int abort_flag;
 };
 
 template <int HD, int G>
@@ -74,7 +113,8 @@ DEVI void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr)
                : "memory");
 }
-// C += A B: A 16x16 (rows g, g+8 of the fragment layout), B 16x8, fp32 C.
+// C += A B: A 16x16 (a0/a2: row g, a1/a3: row g + 8 of the fragment layout),
+// B 16x8, fp32 C (c0/c1: row g, c2/c3: row g + 8).
 DEVI void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -88,6 +128,9 @@ DEVI void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+DEVI uint32_t pack_bf16(float x, float y) {
+  return static_cast<uint32_t>(f32_to_bf16bits(x)) | (static_cast<uint32_t>(f32_to_bf16bits(y)) << 16);
 }
 // shared address of (token, dim) in a K or V block of 64 tokens stored as
 // HD/64 swizzled boxes of [64 tokens][128 bytes]
@@ -115,28 +158,35 @@ struct AmUnit {
   const int32_t* ptab;
 };
 
-// Unit u's row and chunk (from the launch's rows in shared memory); false for
-// an inactive row.
-DEVI bool am_unit(const DevPtrs& d, const RowInfo* rows, int nrows, int u, int chunk_tokens, AmUnit& un) {
-  int lo = 0, hi = nrows - 1;   // rows are sorted by unit0
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (rows[mid].unit0 <= u) lo = mid;
-    else hi = mid - 1;
+// Unit v of the launch's order (full chunks row by row, then the last
+// chunks in lorder): its row, KV head and chunk.
+DEVI void am_unit(const DevPtrs& d, const AmSmemRows& t, int nrows, int ftot, int v, int chunk_tokens, AmUnit& un) {
+  if (v < ftot) {
+    int lo = 0, hi = nrows - 1;   // the last row with fpre <= v
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (t.fpre[mid] <= v) lo = mid;
+      else hi = mid - 1;
+    }
+    un.r = lo;
+    un.ri = t.rows[lo];
+    un.nch = (un.ri.pos + chunk_tokens) / chunk_tokens;
+    const int local = v - t.fpre[lo];
+    un.g = local / (un.nch - 1);
+    un.c = local % (un.nch - 1);
+  } else {
+    const int w = v - ftot;
+    un.r = t.lorder[w / d.Hkv];
+    un.ri = t.rows[un.r];
+    un.nch = (un.ri.pos + chunk_tokens) / chunk_tokens;
+    un.g = w % d.Hkv;
+    un.c = un.nch - 1;
   }
-  un.r = lo;
-  un.ri = rows[lo];
   const int L = un.ri.pos + 1;
-  un.nch = (L + chunk_tokens - 1) / chunk_tokens;
-  const int local = u - un.ri.unit0;
-  un.g = local / un.nch;
-  un.c = local % un.nch;
-  if (!un.ri.active || un.g >= d.Hkv) return false;
   un.t0 = un.c * chunk_tokens;
   un.t1 = min(L, un.t0 + chunk_tokens);
   un.npages = (un.t1 - un.t0 + kPageTokens - 1) / kPageTokens;
   un.ptab = d.page_table + static_cast<size_t>(un.ri.slot) * d.pages_per_seq + un.t0 / kPageTokens;
-  return true;
 }
 
 // Whole warp: page p's index for p = lane + 32 * i in pg[i] (-1 beyond the
@@ -154,13 +204,37 @@ DEVI bool am_pages(const DevPtrs& d, const AmUnit& un, int lane, int (&pg)[NPG])
 }
 constexpr int kAmPageRegs = (kMaxChunkPages + 31) / 32;
 
+// RMS norm over the head (gains nw, or none) then RoPE on adjacent pairs,
+// with the position's cos/sin already loaded; lane holds dims lane*EPL ...
+template <int EPL>
+DEVI void am_norm_rope(float (&v)[EPL], const float (&nw)[EPL], bool norm, float eps, const float (&cs)[EPL / 2],
+                       const float (&sn)[EPL / 2]) {
+  if (norm) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s += v[j] * v[j];
+    s = warp_sum(s);
+    const float inv = 1.0f / sqrtf(s / static_cast<float>(EPL * 32) + eps);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) v[j] = (v[j] * inv) * nw[j];
+  }
+#pragma unroll
+  for (int pp = 0; pp < EPL / 2; ++pp) {
+    const float x0 = v[2 * pp], x1 = v[2 * pp + 1];
+    v[2 * pp] = x0 * cs[pp] - x1 * sn[pp];
+    v[2 * pp + 1] = x1 * cs[pp] + x0 * sn[pp];
+  }
+}
+
 template <int HD, int G>
 __global__ void __launch_bounds__(kAmThreads, 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tkv, const DevPtrs d, int nrows, int layer, int total_units,
                     int chunk_tokens, int fuse, const uint16_t* q_norm, const uint16_t* k_norm) {
   using C = AmCfg<HD>;
+  using Desc = AmUnitDesc<HD, G>;
   constexpr int NB = C::NBUF;
   constexpr int EPL = HD / 32;
+  constexpr bool ROWS8 = G > 4;   // lo halves in rows 8..15 (else rows 4..7)
   static_assert(G >= 1 && G <= 8, "query heads per KV head: the MMA rows 0..7");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -168,42 +242,224 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   const uint32_t ring_s = smem_addr(ring);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hkv = d.Hkv, hq = d.Hq;
-  const size_t page_stride = static_cast<size_t>(kPageTokens) * HD;
   if (tid == 0) {
     for (int b = 0; b < NB; ++b) {
       mbar_init(&sm.full[b], 1);
       mbar_init(&sm.empty[b], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.ufull[b], 1);
+      mbar_init(&sm.uempty[b], kAmUnitUsers);
+    }
+    mbar_init(&sm.cfull, kAmWarps);
+    mbar_init(&sm.cempty, 1);
     sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int i = tid; i < nrows; i += kAmThreads) sm.rows[i] = ld_row(&d.rows[i]);
+  for (int i = tid; i < nrows; i += kAmThreads) sm.t.rows[i] = ld_row(&d.rows[i]);
   __syncthreads();
-  const volatile int* abort_flag = &sm.abort_flag;
+  volatile int* abort_flag = &sm.abort_flag;
 
-  if (warp == kAmWarps) {
-    // ---- producer (the whole warp; lane 0 issues): the K/V pages of this
-    // CTA's units, in order
-    uint32_t gs = 0;
+  if (warp == kAmPrep) {
+    // ---- prep: publish the CTA's units in order, then an end marker
+    const float qscale = 1.0f / sqrtf(static_cast<float>(HD));
+    const bool qnorm = fuse && q_norm != nullptr, knorm = fuse && k_norm != nullptr;
+    float qw[EPL], kw[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      qw[j] = qnorm ? bf16bits_to_f32(q_norm[lane * EPL + j]) : 1.f;
+      kw[j] = knorm ? bf16bits_to_f32(k_norm[lane * EPL + j]) : 1.f;
+    }
+    // the unit order: per-row full-chunk counts (prefix sums), and the
+    // active rows sorted by their last chunk's page count (counting sort)
+    AmSmemRows& t = sm.t;
+    for (int i = lane; i <= kMaxChunkPages; i += 32) t.lcur[i] = 0;
+    __syncwarp();
+    int fl[4], lp[4], fs = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane * 4 + i;
+      fl[i] = lp[i] = 0;
+      if (r < nrows && t.rows[r].active) {
+        const int L = t.rows[r].pos + 1, nch = (L + chunk_tokens - 1) / chunk_tokens;
+        fl[i] = (nch - 1) * hkv;
+        lp[i] = (L - (nch - 1) * chunk_tokens + kPageTokens - 1) / kPageTokens;   // 1 .. chunk pages
+        atomicAdd(&t.lcur[lp[i]], 1);
+      }
+      fs += fl[i];
+    }
+    int fx = fs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, fx, o);
+      if (lane >= o) fx += y;
+    }
+    const int ftot = __shfl_sync(0xFFFFFFFFu, fx, 31);
+    {
+      int fe = fx - fs;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        t.fpre[lane * 4 + i] = fe;
+        fe += fl[i];
+      }
+    }
+    __syncwarp();
+    // bins in descending page count: lane takes counts 64 - 2 lane and 63 - 2 lane
+    const int s0 = kMaxChunkPages - 2 * lane, s1 = s0 - 1;
+    const int h0 = t.lcur[s0], h1 = s1 >= 1 ? t.lcur[s1] : 0;
+    int hx = h0 + h1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, hx, o);
+      if (lane >= o) hx += y;
+    }
+    const int nact = __shfl_sync(0xFFFFFFFFu, hx, 31);
+    __syncwarp();
+    t.lcur[s0] = hx - h0 - h1;
+    if (s1 >= 1) t.lcur[s1] = hx - h1;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (lp[i] > 0) t.lorder[atomicAdd(&t.lcur[lp[i]], 1)] = lane * 4 + i;
+    __syncwarp();
+    const int total = ftot + nact * hkv;
+
+    uint32_t k = 0;
+    bool ok = true;
+    uint32_t* counter = d.sched + layer;
+    int next = 0;
+    if (lane == 0) next = static_cast<int>(atomicAdd(counter, 1u));
+    for (;;) {
+      const int v = __shfl_sync(0xFFFFFFFFu, next, 0);
+      if (v >= total) break;
+      if (lane == 0) next = static_cast<int>(atomicAdd(counter, 1u));   // the one after (its latency overlaps)
+      AmUnit un;
+      am_unit(d, t, nrows, ftot, v, chunk_tokens, un);
+      int pg[kAmPageRegs];
+      if (!am_pages(d, un, lane, pg)) {
+        if (lane == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
+        continue;
+      }
+      const int r = un.r, pos = un.ri.pos;
+      const bool newest = fuse && un.c == un.nch - 1;
+      // loads first (they touch no shared memory)
+      float qv[G][EPL];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float* src = fuse ? d.qkv + static_cast<size_t>(r) * d.qkv_dim + (un.g * G + h) * HD
+                                : d.qrot + (static_cast<size_t>(r) * hq + un.g * G + h) * HD;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) qv[h][j] = ldf(src + lane * EPL + j);
+      }
+      float cs[EPL / 2], sn[EPL / 2];
+      if (fuse) {
+#pragma unroll
+        for (int pp = 0; pp < EPL / 2; ++pp) {
+          const size_t i = static_cast<size_t>(pos) * (HD / 2) + (lane * EPL) / 2 + pp;
+          cs[pp] = bf16bits_to_f32(d.rope_cos[i]);
+          sn[pp] = bf16bits_to_f32(d.rope_sin[i]);
+        }
+      }
+      float kv[EPL], vv[EPL];
+      if (newest) {
+        const float* base = d.qkv + static_cast<size_t>(r) * d.qkv_dim + hq * HD + un.g * HD + lane * EPL;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          kv[j] = ldf(base + j);
+          vv[j] = ldf(base + hkv * HD + j);
+        }
+      }
+      const int b = static_cast<int>(k & 1);
+      if (k >= 2 && !am_wait(&sm.uempty[b], ((k >> 1) - 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      Desc& un_d = sm.unit[b];
+#pragma unroll
+      for (int i = 0; i < kAmPageRegs; ++i)
+        if (lane + 32 * i < un.npages) un_d.pages[lane + 32 * i] = pg[i];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (fuse) am_norm_rope<EPL>(qv[h], qw, qnorm, d.eps, cs, sn);
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) un_d.q[h][lane * EPL + j] = qv[h][j] * qscale;
+      }
+      if (newest) {
+        am_norm_rope<EPL>(kv, kw, knorm, d.eps, cs, sn);
+        // the newest position's page: the unit's page (pos - t0) / 64
+        const int pl = (pos - un.t0) / kPageTokens;
+        int pgn = 0;
+#pragma unroll
+        for (int i = 0; i < kAmPageRegs; ++i) {
+          const int x = __shfl_sync(0xFFFFFFFFu, pg[i], pl & 31);
+          if ((pl >> 5) == i) pgn = x;
+        }
+        const size_t page_stride = static_cast<size_t>(kPageTokens) * HD;
+        uint16_t* kd = d.kv_pool + (((static_cast<size_t>(pgn) * d.n_layer + layer) * 2 + 0) * hkv + un.g) * page_stride +
+                       static_cast<size_t>(pos % kPageTokens) * HD + lane * EPL;
+        uint16_t* vd = kd + static_cast<size_t>(hkv) * page_stride;
+#pragma unroll
+        for (int j = 0; j < EPL; j += 2) {
+          const uint32_t kp = pack_bf16(kv[j], kv[j + 1]), vp = pack_bf16(vv[j], vv[j + 1]);
+          *reinterpret_cast<uint32_t*>(kd + j) = kp;
+          *reinterpret_cast<uint32_t*>(vd + j) = vp;
+          un_d.knew[(lane * EPL + j) / 2] = kp;
+          un_d.vnew[(lane * EPL + j) / 2] = vp;
+        }
+      }
+      if (lane == 0) {
+        un_d.r = r;
+        un_d.g = un.g;
+        un_d.c = un.c;
+        un_d.nch = un.nch;
+        un_d.t0 = un.t0;
+        un_d.t1 = un.t1;
+        un_d.npages = un.npages;
+        un_d.pos = pos;
+        un_d.newest = newest ? 1 : 0;
+        un_d.rot = v & (kAmWarps - 1);
+        un_d.last = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ufull[b]);
+      ++k;
+    }
+    if (ok) {
+      const int b = static_cast<int>(k & 1);
+      if (k >= 2 && !am_wait(&sm.uempty[b], ((k >> 1) - 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      if (lane == 0) {
+        sm.unit[b].last = 1;
+        mbar_arrive(&sm.ufull[b]);
+      }
+    }
+    return;
+  }
+
+  if (warp == kAmProducer) {
+    // ---- producer (lane 0): the K/V pages of the published units, in order
+    if (lane != 0) return;
     uint32_t cnt[kAmWarps];   // slot fills given to each compute warp so far
-    uint32_t iss[kAmWarps];   // ... and actually issued (lane 0)
+    uint32_t iss[kAmWarps];   // ... and actually issued
 #pragma unroll
     for (int w = 0; w < kAmWarps; ++w) cnt[w] = iss[w] = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      AmUnit un;
-      if (!am_unit(d, sm.rows, nrows, u, chunk_tokens, un)) continue;
-      int pg[kAmPageRegs];
-      if (!am_pages(d, un, lane, pg)) continue;
-      for (int p = 0; p < un.npages; ++p) {
-        int pgp = 0;
-#pragma unroll
-        for (int i = 0; i < kAmPageRegs; ++i) {
-          const int v = __shfl_sync(0xFFFFFFFFu, pg[i], p & 31);
-          if ((p >> 5) == i) pgp = v;
-        }
-        const int w = static_cast<int>(gs % kAmWarps);
-        const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + un.g) * 64);
+    for (uint32_t k = 0; ok; ++k) {
+      const int b = static_cast<int>(k & 1);
+      if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        break;
+      }
+      const Desc& un_d = sm.unit[b];
+      if (un_d.last) break;
+      const int npages = un_d.npages, g = un_d.g, rot = un_d.rot;
+      for (int p = 0; ok && p < npages; ++p) {
+        const int pgp = un_d.pages[p];
+        const int w = (p + rot) & (kAmWarps - 1);
+        const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + g) * 64);
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           uint32_t j = 0;
@@ -211,109 +467,153 @@ __global__ void __launch_bounds__(kAmThreads, 1)
           for (int ww = 0; ww < kAmWarps; ++ww)
             if (ww == w) j = cnt[ww]++;
           const int s = w * C::SLOTS + static_cast<int>(j % C::SLOTS);
-          if (lane == 0 && ok) {
-            if (j >= static_cast<uint32_t>(C::SLOTS) &&
-                !am_wait(&sm.empty[s], ((j / C::SLOTS) - 1) & 1, abort_flag, d)) {
-              sm.abort_flag = 1;
-              ok = false;
-            } else {
-              mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::SLOT));
-#pragma unroll
-              for (int hh = 0; hh < C::HALVES; ++hh)
-                tma_load_2d(ring + s * C::SLOT + hh * kAmBox, &tkv, hh * 64, rowk + kv * hkv * 64, &sm.full[s]);
-#pragma unroll
-              for (int ww = 0; ww < kAmWarps; ++ww)
-                if (ww == w) ++iss[ww];
-            }
+          if (!ok) continue;
+          if (j >= static_cast<uint32_t>(C::SLOTS) &&
+              !am_wait(&sm.empty[s], ((j / C::SLOTS) - 1) & 1, abort_flag, d)) {
+            *abort_flag = 1;
+            ok = false;
+            continue;
           }
+          mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::SLOT));
+#pragma unroll
+          for (int hh = 0; hh < C::HALVES; ++hh)
+            tma_load_2d(ring + s * C::SLOT + hh * kAmBox, &tkv, hh * 64, rowk + kv * hkv * 64, &sm.full[s]);
+#pragma unroll
+          for (int ww = 0; ww < kAmWarps; ++ww)
+            if (ww == w) ++iss[ww];
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok) break;
-        ++gs;
       }
+      if (ok) mbar_arrive(&sm.uempty[b]);
     }
-    if (lane == 0) {
-      // every copy issued here lands before the CTA exits (bounded)
-      for (int w = 0; w < kAmWarps; ++w)
-        for (uint32_t j = iss[w] > static_cast<uint32_t>(C::SLOTS) ? iss[w] - C::SLOTS : 0; j < iss[w]; ++j) {
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(&sm.full[w * C::SLOTS + j % C::SLOTS], (j / C::SLOTS) & 1))
-            if (global_timer_ns() - t0 > d.wait_limit_ns) break;
-        }
-    }
+    // every copy issued here lands before the CTA exits (bounded)
+    for (int w = 0; w < kAmWarps; ++w)
+      for (uint32_t j = iss[w] > static_cast<uint32_t>(C::SLOTS) ? iss[w] - C::SLOTS : 0; j < iss[w]; ++j) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&sm.full[w * C::SLOTS + j % C::SLOTS], (j / C::SLOTS) & 1))
+          if (global_timer_ns() - t0 > d.wait_limit_ns) break;
+      }
     return;
   }
 
+  if (warp == kAmFinal) {
+    // ---- finalize: merge the compute warps' states, write, combine chunks
+    for (uint32_t k = 0;; ++k) {
+      const int b = static_cast<int>(k & 1);
+      if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      const Desc& un_d = sm.unit[b];
+      if (un_d.last) return;
+      if (!am_wait(&sm.cfull, k & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      const int r = un_d.r, g = un_d.g, c = un_d.c, nch = un_d.nch;
+      const size_t attn_off = static_cast<size_t>(r) * hq * HD + g * G * HD;
+      float* pw = d.part + ((static_cast<size_t>(r) * hkv + g) * kMaxChunks + c) * G * (HD + 2);
+      for (int e = lane; e < G * HD; e += 32) {
+        const int h = e / HD, dd = e % HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAmWarps; ++w) M = fmaxf(M, sm.cm[w][h]);
+        float Ls = 0.f, Os = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAmWarps; ++w) {
+          const float fw = sm.cm[w][h] == -INFINITY ? 0.f : expf(sm.cm[w][h] - M);
+          Ls += sm.cl[w][h] * fw;
+          Os += sm.co[w][h][dd] * fw;
+        }
+        if (nch == 1) {
+          d.attn[attn_off + h * HD + dd] = Os / Ls;
+        } else {
+          pw[h * (HD + 2) + dd] = Os;
+          if (dd == 0) {
+            pw[h * (HD + 2) + HD] = M;
+            pw[h * (HD + 2) + HD + 1] = Ls;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.cempty);
+      if (nch > 1) {
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const uint32_t old = atomic_add_acq_rel_gpu(&d.arrive[r * hkv + g], 1u);
+          if (old == static_cast<uint32_t>(nch - 1)) {
+            // reset before any output of this (row, head) is written
+            atomicExch(&d.arrive[r * hkv + g], 0u);
+            last = 1;
+          }
+        }
+        if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+          __threadfence();
+          const float* pb = d.part + (static_cast<size_t>(r) * hkv + g) * kMaxChunks * G * (HD + 2);
+          for (int h = 0; h < G; ++h) {
+            float mx = -INFINITY;
+            for (int cc = lane; cc < nch; cc += 32) mx = fmaxf(mx, ldf(pb + (cc * G + h) * (HD + 2) + HD));
+            const float M = warp_max(mx);
+            float ls = 0.f;
+            for (int cc = lane; cc < nch; cc += 32) {
+              const float* q = pb + (cc * G + h) * (HD + 2);
+              const float f = expf(ldf(q + HD) - M);
+              sm.fc[h][cc] = f;
+              ls += ldf(q + HD + 1) * f;
+            }
+            const float Ls = warp_sum(ls);
+            __syncwarp();
+            float os[EPL];
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) os[j] = 0.f;
+#pragma unroll 4
+            for (int cc = 0; cc < nch; ++cc) {
+              const float* q = pb + (cc * G + h) * (HD + 2) + lane * EPL;
+              const float f = sm.fc[h][cc];
+#pragma unroll
+              for (int j = 0; j < EPL; ++j) os[j] += ldf(q + j) * f;
+            }
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) d.attn[attn_off + h * HD + lane * EPL + j] = os[j] / Ls;
+            __syncwarp();
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.uempty[b]);
+    }
+  }
+
   // ---- compute warps
-  const float qscale = 1.0f / sqrtf(static_cast<float>(HD));
-  const int gr = lane >> 2, tq = lane & 3;   // fragment row (head) and column pair
-  uint32_t gs_base = 0;
+  const int gr = lane >> 2, tq = lane & 3;          // fragment row and column pair
+  const int head = ROWS8 ? gr : (gr & 3);           // the query head of this lane's rows
+  const bool lo_row = !ROWS8 && gr >= 4;            // rows 4..7 carry the lo halves (G <= 4)
+  const bool writer = (ROWS8 || gr < 4) && head < G;
   uint32_t mine = 0;   // pages this warp has taken so far (its slot sequence)
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    AmUnit un;
-    if (!am_unit(d, sm.rows, nrows, u, chunk_tokens, un)) continue;
-    if (warp == 0) {
-      int pg[kAmPageRegs];
-      const bool pages_ok = am_pages(d, un, lane, pg);
-      if (lane == 0) {
-        sm.unit_ok = pages_ok ? 1 : 0;
-        if (!pages_ok) raise_error(d.err, DEV_ERR_BAD_PAGE);
-      }
+  for (uint32_t k = 0;; ++k) {
+    const int b = static_cast<int>(k & 1);
+    if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
+      *abort_flag = 1;
+      return;
     }
-    const int r = un.r;
-    const bool newest = fuse && un.c == un.nch - 1;
-    // query heads of this unit (and the newest position's K/V)
-    for (int h = warp; h < G; h += kAmWarps) {
-      float v[EPL];
-      if (fuse) {
-        const float* src = d.qkv + static_cast<size_t>(r) * d.qkv_dim + (un.g * G + h) * HD;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) v[j] = ldf(src + lane * EPL + j);
-        head_norm_rope<EPL>(v, q_norm, d.eps, un.ri.pos, d, lane);
-      } else {
-        const float* src = d.qrot + (static_cast<size_t>(r) * hq + un.g * G + h) * HD;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) v[j] = ldf(src + lane * EPL + j);
-      }
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) sm.qs[h][lane * EPL + j] = v[j] * qscale;
-    }
-    if (newest && warp == kAmWarps - 1) {
-      const float* base = d.qkv + static_cast<size_t>(r) * d.qkv_dim;
-      float kv[EPL], vv[EPL];
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        kv[j] = ldf(base + hq * HD + un.g * HD + lane * EPL + j);
-        vv[j] = ldf(base + hq * HD + hkv * HD + un.g * HD + lane * EPL + j);
-      }
-      head_norm_rope<EPL>(kv, k_norm, d.eps, un.ri.pos, d, lane);
-      const int pg = ldi(d.page_table + static_cast<size_t>(un.ri.slot) * d.pages_per_seq + un.ri.pos / kPageTokens);
-      uint16_t* kd = d.kv_pool + (((static_cast<size_t>(pg) * d.n_layer + layer) * 2 + 0) * hkv + un.g) * page_stride +
-                     static_cast<size_t>(un.ri.pos % kPageTokens) * HD;
-      uint16_t* vd = kd + static_cast<size_t>(hkv) * page_stride;
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        const uint16_t kb = f32_to_bf16bits(kv[j]), vb = f32_to_bf16bits(vv[j]);
-        kd[lane * EPL + j] = kb;
-        vd[lane * EPL + j] = vb;
-        sm.knew[lane * EPL + j] = bf16bits_to_f32(kb);
-        sm.vnew[lane * EPL + j] = bf16bits_to_f32(vb);
-      }
-    }
-    named_barrier(1, kAmWarps * 32);
-    if (!sm.unit_ok) {
-      named_barrier(1, kAmWarps * 32);   // (the producer skipped it too)
-      continue;
-    }
-    // Q fragments (rows gr < G real; rows gr + 8 are zero)
-    uint32_t qh[HD / 16][2], ql[HD / 16][2];
+    const Desc& un_d = sm.unit[b];
+    if (un_d.last) return;
+    const int t0 = un_d.t0, t1 = un_d.t1, npages = un_d.npages, pos = un_d.pos;
+    const bool newest = un_d.newest != 0;
+    // Q fragments: row gr holds the hi half of head gr; the lo half sits in
+    // row gr + 4 (G <= 4: another lane) or row gr + 8 (G = 8: a1/a3)
+    uint32_t qa[HD / 16][2], qb[HD / 16][2];
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int dd = ks * 16 + half * 8 + 2 * tq;
-        const float x = gr < G ? sm.qs[gr][dd] : 0.f, y = gr < G ? sm.qs[gr][dd + 1] : 0.f;
-        split2(x, y, qh[ks][half], ql[ks][half]);
+        const float x = head < G ? un_d.q[head][dd] : 0.f, y = head < G ? un_d.q[head][dd + 1] : 0.f;
+        uint32_t hi, lo;
+        split2(x, y, hi, lo);
+        qa[ks][half] = lo_row ? lo : hi;
+        qb[ks][half] = ROWS8 ? lo : 0u;
       }
     }
     float m_run = -INFINITY, l_run = 0.f;
@@ -321,105 +621,112 @@ __global__ void __launch_bounds__(kAmThreads, 1)
 #pragma unroll
     for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-    const int p0 = static_cast<int>((warp - static_cast<int>(gs_base % kAmWarps) + kAmWarps) % kAmWarps);
-    for (int p = p0; p < un.npages; p += kAmWarps) {
+    const int p0 = (warp - un_d.rot) & (kAmWarps - 1);
+    for (int p = p0; p < npages; p += kAmWarps) {
       const uint32_t jk = mine++, jv = mine++;
       const int sk = warp * C::SLOTS + static_cast<int>(jk % C::SLOTS);
       const int sv = warp * C::SLOTS + static_cast<int>(jv % C::SLOTS);
       bool got = am_wait(&sm.full[sk], (jk / C::SLOTS) & 1, abort_flag, d);
-      got = am_wait(&sm.full[sv], (jv / C::SLOTS) & 1, abort_flag, d) && got;
-      if (!got) sm.abort_flag = 1;   // the others stop waiting too
-      const int ps = un.t0 + p * kPageTokens;
-      const int ntok = min(kPageTokens, un.t1 - ps);
+      got = got && am_wait(&sm.full[sv], (jv / C::SLOTS) & 1, abort_flag, d);
+      if (!got) {
+        *abort_flag = 1;
+        return;
+      }
+      const int ps = t0 + p * kPageTokens;
+      const int ntok = min(kPageTokens, t1 - ps);
       const uint32_t kb = ring_s + sk * C::SLOT, vb = ring_s + sv * C::SLOT;
-      if (got && newest && ps <= un.ri.pos && un.ri.pos < ps + kPageTokens) {
+      if (newest && ps <= pos && pos < ps + kPageTokens) {
         // the newest row (its copy may predate the cache write)
-        const int rr = un.ri.pos - ps;
+        const int rr = pos - ps;
         if (lane < HD / 8) {
-          uint32_t wk[4], wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            wk[e] = static_cast<uint32_t>(f32_to_bf16bits(sm.knew[lane * 8 + 2 * e])) |
-                    (static_cast<uint32_t>(f32_to_bf16bits(sm.knew[lane * 8 + 2 * e + 1])) << 16);
-            wv[e] = static_cast<uint32_t>(f32_to_bf16bits(sm.vnew[lane * 8 + 2 * e])) |
-                    (static_cast<uint32_t>(f32_to_bf16bits(sm.vnew[lane * 8 + 2 * e + 1])) << 16);
-          }
           const uint32_t ak = sw_addr(kb, rr, lane * 8), av = sw_addr(vb, rr, lane * 8);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ak), "r"(wk[0]), "r"(wk[1]), "r"(wk[2]),
-                       "r"(wk[3])
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ak), "r"(un_d.knew[lane * 4]),
+                       "r"(un_d.knew[lane * 4 + 1]), "r"(un_d.knew[lane * 4 + 2]), "r"(un_d.knew[lane * 4 + 3])
                        : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(av), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]),
-                       "r"(wv[3])
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(av), "r"(un_d.vnew[lane * 4]),
+                       "r"(un_d.vnew[lane * 4 + 1]), "r"(un_d.vnew[lane * 4 + 2]), "r"(un_d.vnew[lane * 4 + 3])
                        : "memory");
         }
+        // (the slot is refilled by TMA later: order these writes before it)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
-      if (got) {
-        // S = Q K^T over the page: 8 tiles of 8 tokens
-        float sc[8][4];
+      // S = Q K^T over the page: 8 tiles of 8 tokens
+      float sc[8][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
+      for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
-          for (int jp = 0; jp < 4; ++jp) {
-            uint32_t b[4];
-            const int tok = jp * 16 + (lane >> 4) * 8 + (lane & 7);
-            const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
-            ldsm_x4(b, sw_addr(kb, tok, dim));
-            mma16816(sc[2 * jp], qh[ks][0], 0u, qh[ks][1], 0u, b[0], b[1]);
-            mma16816(sc[2 * jp], ql[ks][0], 0u, ql[ks][1], 0u, b[0], b[1]);
-            mma16816(sc[2 * jp + 1], qh[ks][0], 0u, qh[ks][1], 0u, b[2], b[3]);
-            mma16816(sc[2 * jp + 1], ql[ks][0], 0u, ql[ks][1], 0u, b[2], b[3]);
-          }
+        for (int jp = 0; jp < 4; ++jp) {
+          uint32_t bb[4];
+          const int tok = jp * 16 + (lane >> 4) * 8 + (lane & 7);
+          const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
+          ldsm_x4(bb, sw_addr(kb, tok, dim));
+          mma16816(sc[2 * jp], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[0], bb[1]);
+          mma16816(sc[2 * jp + 1], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[2], bb[3]);
         }
-        // online softmax on row gr (tokens 8j + 2tq, +1)
-        float mx = -INFINITY;
+      }
+      // hi + lo rows -> the head's scores (tokens 8j + 2tq, +1)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int t = 8 * j + 2 * tq;
-          if (t >= ntok) sc[j][0] = -INFINITY;
-          if (t + 1 >= ntok) sc[j][1] = -INFINITY;
-          mx = fmaxf(mx, fmaxf(sc[j][0], sc[j][1]));
+      for (int j = 0; j < 8; ++j) {
+        if (ROWS8) {
+          sc[j][0] += sc[j][2];
+          sc[j][1] += sc[j][3];
+        } else {
+          sc[j][0] += __shfl_xor_sync(0xFFFFFFFFu, sc[j][0], 16);
+          sc[j][1] += __shfl_xor_sync(0xFFFFFFFFu, sc[j][1], 16);
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float f = expf(m_run - m_new);   // 0 on the first page (m_run = -inf)
-        float ps_sum = 0.f;
+      }
+      // online softmax on the head's row
+      float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sc[j][0] = expf(sc[j][0] - m_new);
-          sc[j][1] = expf(sc[j][1] - m_new);
-          ps_sum += sc[j][0] + sc[j][1];
+      for (int j = 0; j < 8; ++j) {
+        const int t = 8 * j + 2 * tq;
+        if (t >= ntok) sc[j][0] = -INFINITY;
+        if (t + 1 >= ntok) sc[j][1] = -INFINITY;
+        mx = fmaxf(mx, fmaxf(sc[j][0], sc[j][1]));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float f = expf(m_run - m_new);   // 0 on the first page (m_run = -inf)
+      float ps_sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc[j][0] = expf(sc[j][0] - m_new);
+        sc[j][1] = expf(sc[j][1] - m_new);
+        ps_sum += sc[j][0] + sc[j][1];
+      }
+      ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 1);
+      ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 2);
+      l_run = l_run * f + ps_sum;
+      m_run = m_new;
+#pragma unroll
+      for (int n = 0; n < HD / 8; ++n) {
+        o[n][0] *= f;
+        o[n][1] *= f;
+        if (ROWS8) {
+          o[n][2] *= f;
+          o[n][3] *= f;
         }
-        ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 1);
-        ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 2);
-        l_run = l_run * f + ps_sum;
-        m_run = m_new;
+      }
+      // O += P V: 4 steps of 16 tokens
 #pragma unroll
-        for (int n = 0; n < HD / 8; ++n) {
-          o[n][0] *= f;
-          o[n][1] *= f;
-        }
-        // O += P V: 4 steps of 16 tokens
+      for (int kt = 0; kt < 4; ++kt) {
+        uint32_t ph0, pl0, ph2, pl2;
+        split2(sc[2 * kt][0], sc[2 * kt][1], ph0, pl0);
+        split2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], ph2, pl2);
+        const uint32_t a0 = lo_row ? pl0 : ph0, a2 = lo_row ? pl2 : ph2;
+        const uint32_t a1 = ROWS8 ? pl0 : 0u, a3 = ROWS8 ? pl2 : 0u;
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-          uint32_t ph0, pl0, ph2, pl2;
-          split2(sc[2 * kt][0], sc[2 * kt][1], ph0, pl0);
-          split2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], ph2, pl2);
-#pragma unroll
-          for (int np = 0; np < HD / 16; ++np) {
-            uint32_t b[4];
-            const int tok = kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-            const int dim = np * 16 + (lane >> 4) * 8;
-            ldsm_x4_t(b, sw_addr(vb, tok, dim));
-            mma16816(o[2 * np], ph0, 0u, ph2, 0u, b[0], b[1]);
-            mma16816(o[2 * np], pl0, 0u, pl2, 0u, b[0], b[1]);
-            mma16816(o[2 * np + 1], ph0, 0u, ph2, 0u, b[2], b[3]);
-            mma16816(o[2 * np + 1], pl0, 0u, pl2, 0u, b[2], b[3]);
-          }
+        for (int np = 0; np < HD / 16; ++np) {
+          uint32_t bb[4];
+          const int tok = kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int dim = np * 16 + (lane >> 4) * 8;
+          ldsm_x4_t(bb, sw_addr(vb, tok, dim));
+          mma16816(o[2 * np], a0, a1, a2, a3, bb[0], bb[1]);
+          mma16816(o[2 * np + 1], a0, a1, a2, a3, bb[2], bb[3]);
         }
       }
       __syncwarp();
@@ -428,77 +735,38 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         mbar_arrive(&sm.empty[sv]);
       }
     }
-    gs_base += un.npages;
 
-    // merge the warps' (m, l, O) (warp order: deterministic)
-    if (gr < G) {
+    // hand (m, l, O) to the finalize warp
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) {
+      if (ROWS8) {
+        o[n][0] += o[n][2];
+        o[n][1] += o[n][3];
+      } else {
+        o[n][0] += __shfl_xor_sync(0xFFFFFFFFu, o[n][0], 16);
+        o[n][1] += __shfl_xor_sync(0xFFFFFFFFu, o[n][1], 16);
+      }
+    }
+    if (k >= 1 && !am_wait(&sm.cempty, (k - 1) & 1, abort_flag, d)) {
+      *abort_flag = 1;
+      return;
+    }
+    if (writer) {
       if (tq == 0) {
-        sm.cm[warp][gr] = m_run;
-        sm.cl[warp][gr] = l_run;
+        sm.cm[warp][head] = m_run;
+        sm.cl[warp][head] = l_run;
       }
 #pragma unroll
       for (int n = 0; n < HD / 8; ++n) {
-        sm.co[warp][gr][8 * n + 2 * tq] = o[n][0];
-        sm.co[warp][gr][8 * n + 2 * tq + 1] = o[n][1];
+        sm.co[warp][head][8 * n + 2 * tq] = o[n][0];
+        sm.co[warp][head][8 * n + 2 * tq + 1] = o[n][1];
       }
     }
-    named_barrier(1, kAmWarps * 32);
-    const size_t attn_off = static_cast<size_t>(r) * hq * HD + un.g * G * HD;
-    float* pw = d.part + ((static_cast<size_t>(r) * hkv + un.g) * kMaxChunks + un.c) * G * (HD + 2);
-    for (int e = tid; e < G * HD; e += kAmWarps * 32) {
-      const int h = e / HD, dd = e % HD;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kAmWarps; ++w) M = fmaxf(M, sm.cm[w][h]);
-      float Ls = 0.f, Os = 0.f;
-#pragma unroll
-      for (int w = 0; w < kAmWarps; ++w) {
-        const float fw = sm.cm[w][h] == -INFINITY ? 0.f : expf(sm.cm[w][h] - M);
-        Ls += sm.cl[w][h] * fw;
-        Os += sm.co[w][h][dd] * fw;
-      }
-      if (un.nch == 1) {
-        d.attn[attn_off + h * HD + dd] = Os / Ls;
-      } else {
-        pw[h * (HD + 2) + dd] = Os;
-        if (dd == 0) {
-          pw[h * (HD + 2) + HD] = M;
-          pw[h * (HD + 2) + HD + 1] = Ls;
-        }
-      }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&sm.cfull);
+      mbar_arrive(&sm.uempty[b]);
     }
-    if (un.nch > 1) {
-      __threadfence();
-      named_barrier(1, kAmWarps * 32);
-      if (tid == 0) {
-        const uint32_t old = atomic_add_acq_rel_gpu(&d.arrive[r * hkv + un.g], 1u);
-        int last = 0;
-        if (old == static_cast<uint32_t>(un.nch - 1)) {
-          const uint32_t prev = atomicExch(&d.arrive[r * hkv + un.g], 0u);
-          last = prev == 0xFFFFFFFFu ? 2 : 1;
-        }
-        sm.s_last = last;
-      }
-      named_barrier(1, kAmWarps * 32);
-      if (sm.s_last) {
-        __threadfence();
-        const float* pb = d.part + (static_cast<size_t>(r) * hkv + un.g) * kMaxChunks * G * (HD + 2);
-        for (int e = tid; e < G * HD; e += kAmWarps * 32) {
-          const int h = e / HD, dd = e % HD;
-          float M = -INFINITY;
-          for (int cc = 0; cc < un.nch; ++cc) M = fmaxf(M, ldf(pb + (cc * G + h) * (HD + 2) + HD));
-          float Ls = 0.f, Os = 0.f;
-          for (int cc = 0; cc < un.nch; ++cc) {
-            const float* q = pb + (cc * G + h) * (HD + 2);
-            const float fc = expf(ldf(q + HD) - M);
-            Ls += ldf(q + HD + 1) * fc;
-            Os += ldf(q + dd) * fc;
-          }
-          d.attn[attn_off + h * HD + dd] = Os / Ls;
-        }
-      }
-    }
-    named_barrier(1, kAmWarps * 32);   // shared buffers are reused by the next unit
   }
 }
 

@@ -114,6 +114,7 @@ struct DevPtrs {
   float* logits;              // [kMaxRows][logit_ld]
   float* part;                // split-KV partials [kMaxRows][Hkv][kMaxChunks][G][hd+2]
   uint32_t* arrive;           // [kMaxRows][Hkv] last-arriver counters
+  uint32_t* sched;            // [n_layer] unit counters of the tensor-core attention (zeroed by setup)
   int32_t* codes_ws;          // [kMaxRows][kMaxCodebooks] codes of the current frame
   uint32_t* err;              // device error word
   uint64_t wait_limit_ns;

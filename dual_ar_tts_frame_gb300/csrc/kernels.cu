@@ -40,6 +40,7 @@ __global__ void setup_kernel(const LaunchSetup s, DevPtrs d, const uint16_t* tok
     d.commit_map[r] = commit ? ri.slot : -1;
   }
   if (r == 0) {
+    for (int i = threadIdx.x; i < d.n_layer; i += blockDim.x) d.sched[i] = 0;
     for (int i = threadIdx.x; i < s.n_updates; i += blockDim.x) {
       const int sl = s.upd_slot[i], ix = s.upd_index[i], pg = s.upd_page[i];
       if (sl < 0 || sl >= d.max_seqs || ix < 0 || ix >= d.pages_per_seq || pg < 0 ||

@@ -370,7 +370,9 @@ def test_teacher_forced_batch12_tensor_cores(dev_weights, tiny_oracle):
     """Twelve sequences (ragged contexts, several pages and chunks): every
     projection runs on the tensor cores (tcgen05, 9..128 rows), against the
     oracle; the same frames with the tensor cores off (GEMV passes of <= 8
-    rows) agree to fp32 rounding."""
+    rows) agree to fp32 rounding, and two runs of the tensor-core path are
+    bit-identical (the attention's dynamic unit schedule must not change
+    the rounding)."""
     smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
     prompts = {s: g.make_prompt(TINY, int(n), seed=40 + s)
                for s, n in enumerate(g.make_lengths(12, 20, 200, seed=41, stream="tc_b12"))}
@@ -379,7 +381,7 @@ def test_teacher_forced_batch12_tensor_cores(dev_weights, tiny_oracle):
     d.close()
     # the two projection paths on identical inputs
     outs = []
-    for tc in (True, False):
+    for tc in (True, True, False):
         d = make(dev_weights, max_pages=128, max_seqs=16)
         d.set_tensor_cores(tc)
         for s, p in prompts.items():
@@ -391,4 +393,6 @@ def test_teacher_forced_batch12_tensor_cores(dev_weights, tiny_oracle):
         outs.append((slow.cpu().numpy(), fast.cpu().numpy()))
         d.close()
     for a, b in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(outs[0], outs[2]):
         assert np.abs(a - b).max() <= 2e-3 * max(1.0, float(np.abs(b).max()))
