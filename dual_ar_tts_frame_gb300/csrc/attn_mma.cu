@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(kAmThreads, 1)
     sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  pdl_wait();
+  pdl_launch();
   for (int i = tid; i < nrows; i += kAmThreads) sm.t.rows[i] = ld_row(&d.rows[i]);
   __syncthreads();
   volatile int* abort_flag = &sm.abort_flag;
@@ -781,8 +783,8 @@ static cudaError_t am_launch(const CUtensorMap& m, const DevPtrs& d, int nrows, 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_mma_kernel<HD, G><<<grid, kAmThreads, smem, st>>>(m, d, nrows, layer, units, chunk, fuse, qn, kn);
-  return cudaGetLastError();
+  return launch_pdl(attn_mma_kernel<HD, G>, dim3(grid), dim3(kAmThreads), smem, st, m, d, nrows, layer, units, chunk,
+                    fuse, qn, kn);
 }
 
 template <int HD>

@@ -131,6 +131,16 @@ DEVI void cp_async16(void* smem_dst, const void* gsrc) {
 DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 DEVI void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization (launch_pdl) may start while the kernel before it in the
+// stream still runs: pdl_wait() blocks until that kernel has completed and
+// its writes are visible (a no-op after a normal launch), so every kernel
+// calls it before touching memory that an earlier kernel writes or reads,
+// and every CTA calls it before it exits (so that a kernel's completion
+// implies its predecessor's).  pdl_launch() lets the next kernel start.
+DEVI void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DEVI void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 DEVI void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                : "memory");

@@ -7,6 +7,25 @@
 
 namespace dualar {
 
+// Launches kern with programmatic stream serialization: it may begin (its
+// prologue, loads of constant data) while the previous kernel in the stream
+// runs; the kernel calls pdl_wait() before anything that kernel produces.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kMaxRows = 128;        // rows per launch: decode batch or prefill chunk
 constexpr int kMaxCodebooks = 16;
 constexpr int kRasRing = 16;         // RAS history ring per slot (window <= 16)

@@ -32,6 +32,8 @@ namespace dualar {
 // setup: rows, page tables, prompt embeddings
 // ============================================================================
 __global__ void setup_kernel(const LaunchSetup s, DevPtrs d, const uint16_t* tok_emb) {
+  pdl_wait();
+  pdl_launch();
   const int r = blockIdx.x;
   if (r < s.n_rows && threadIdx.x == 0) {
     const RowInfo ri = s.rows[r];
@@ -67,8 +69,7 @@ __global__ void setup_kernel(const LaunchSetup s, DevPtrs d, const uint16_t* tok
 
 cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t* tok_emb,
                          cudaStream_t st) {
-  setup_kernel<<<s.n_rows > 0 ? s.n_rows : 1, 256, 0, st>>>(s, d, tok_emb);
-  return cudaGetLastError();
+  return launch_pdl(setup_kernel, dim3(s.n_rows > 0 ? s.n_rows : 1), dim3(256), 0, st, s, d, tok_emb);
 }
 
 // ============================================================================
@@ -157,6 +158,8 @@ __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
 
 template <int NB>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a, const int stages) {
+  pdl_wait();
+  pdl_launch();
   extern __shared__ __align__(128) unsigned char smem[];
   GemvRing ring;
   ring.full = reinterpret_cast<uint64_t*>(smem);
@@ -221,8 +224,7 @@ static cudaError_t launch_gemv_nb(const GemvArgs& a, const GemvPlan& p, int grid
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  gemv_kernel<NB><<<grid, kGemvThreads, p.smem, st>>>(a, p.stages);
-  return cudaGetLastError();
+  return launch_pdl(gemv_kernel<NB>, dim3(grid), dim3(kGemvThreads), p.smem, st, a, p.stages);
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
@@ -267,6 +269,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
 template <int EPL>
 __global__ void append_kernel(DevPtrs d, int layer, int fast, int fast_pos, const uint16_t* q_norm,
                               const uint16_t* k_norm) {
+  pdl_wait();
+  pdl_launch();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowInfo ri = d.rows[row];
@@ -351,13 +355,14 @@ __global__ void append_kernel(DevPtrs d, int layer, int fast, int fast_pos, cons
 cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int fast_pos,
                           const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
+  cudaError_t e;
   if (d.hd == 128)
-    append_kernel<4><<<nrows, 256, 0, st>>>(d, layer, fast ? 1 : 0, fast_pos, q_norm, k_norm);
+    e = launch_pdl(append_kernel<4>, dim3(nrows), dim3(256), 0, st, d, layer, fast ? 1 : 0, fast_pos, q_norm, k_norm);
   else if (d.hd == 64)
-    append_kernel<2><<<nrows, 256, 0, st>>>(d, layer, fast ? 1 : 0, fast_pos, q_norm, k_norm);
+    e = launch_pdl(append_kernel<2>, dim3(nrows), dim3(256), 0, st, d, layer, fast ? 1 : 0, fast_pos, q_norm, k_norm);
   else
     return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  return e;
 }
 
 // ============================================================================
@@ -370,6 +375,8 @@ template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2)
     attn_paged_kernel(DevPtrs d, int nrows, int layer, int total_units, int chunk_tokens,
                       int fuse_append, const uint16_t* q_norm, const uint16_t* k_norm) {
+  pdl_wait();
+  pdl_launch();
   extern __shared__ __align__(128) unsigned char attn_smem_raw[];
   auto& sm = *reinterpret_cast<AttnSmem<HD, G, kAttnThreads, kAttnBufs>*>(attn_smem_raw);
   __shared__ uint64_t bars[kAttnBufs];
@@ -396,8 +403,8 @@ static cudaError_t attn_paged_launch(const DevPtrs& d, int nrows, int layer, int
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_paged_kernel<HD, G><<<grid, kAttnThreads, smem, st>>>(d, nrows, layer, units, chunk, fuse, qn, kn);
-  return cudaGetLastError();
+  return launch_pdl(attn_paged_kernel<HD, G>, dim3(grid), dim3(kAttnThreads), smem, st, d, nrows, layer, units,
+                    chunk, fuse, qn, kn);
 }
 
 template <int HD>
@@ -436,6 +443,8 @@ cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_
 template <int EPL, int G>
 __global__ void attn_fast_kernel(DevPtrs d, int layer, int pos, const uint16_t* q_norm,
                                  const uint16_t* k_norm) {
+  pdl_wait();
+  pdl_launch();
   constexpr int NT = 32 * (G + 1 > 2 ? G + 1 : 2);
   __shared__ FastAttnSmem<EPL * 32> sm;
   attn_fast_unit<EPL, G, NT>(d, blockIdx.x, layer, pos, q_norm, k_norm, sm);
@@ -447,13 +456,12 @@ static cudaError_t attn_fast_epl(const DevPtrs& d, int nrows, int layer, int pos
   const int G = d.Hq / d.Hkv;
   const int grid = nrows * d.Hkv;
   switch (G) {
-    case 1: attn_fast_kernel<EPL, 1><<<grid, 64, 0, st>>>(d, layer, pos, qn, kn); break;
-    case 2: attn_fast_kernel<EPL, 2><<<grid, 96, 0, st>>>(d, layer, pos, qn, kn); break;
-    case 4: attn_fast_kernel<EPL, 4><<<grid, 160, 0, st>>>(d, layer, pos, qn, kn); break;
-    case 8: attn_fast_kernel<EPL, 8><<<grid, 288, 0, st>>>(d, layer, pos, qn, kn); break;
+    case 1: return launch_pdl(attn_fast_kernel<EPL, 1>, dim3(grid), dim3(64), 0, st, d, layer, pos, qn, kn);
+    case 2: return launch_pdl(attn_fast_kernel<EPL, 2>, dim3(grid), dim3(96), 0, st, d, layer, pos, qn, kn);
+    case 4: return launch_pdl(attn_fast_kernel<EPL, 4>, dim3(grid), dim3(160), 0, st, d, layer, pos, qn, kn);
+    case 8: return launch_pdl(attn_fast_kernel<EPL, 8>, dim3(grid), dim3(288), 0, st, d, layer, pos, qn, kn);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* q_norm,
@@ -466,11 +474,15 @@ cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, co
 }
 
 __global__ void __launch_bounds__(kSampThreads) sample_q0_kernel(DevPtrs d, SampIO io) {
+  pdl_wait();
+  pdl_launch();
   __shared__ SampSmem<kSampThreads> sm;
   sample_q0_row<kSampThreads>(d, blockIdx.x, io, sm);
 }
 
 __global__ void __launch_bounds__(kSampThreads) sample_fast_kernel(DevPtrs d, int k, SampIO io) {
+  pdl_wait();
+  pdl_launch();
   __shared__ SampSmem<kSampThreads> sm;
   sample_fast_row<kSampThreads>(d, blockIdx.x, k, io, sm);
 }
@@ -498,10 +510,9 @@ cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms,
                              int32_t* codes_out, int32_t* status_out, float* slow_logits_out,
                              int32_t* draws_out, const uint16_t* fast_emb, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  sample_q0_kernel<<<nrows, kSampThreads, 0, st>>>(
-      d, make_io(uniforms, ldu, sp, forced, ldf, codes_out, status_out, slow_logits_out, nullptr,
-                 draws_out, fast_emb));
-  return cudaGetLastError();
+  return launch_pdl(sample_q0_kernel, dim3(nrows), dim3(kSampThreads), 0, st, d,
+                    make_io(uniforms, ldu, sp, forced, ldf, codes_out, status_out, slow_logits_out, nullptr,
+                            draws_out, fast_emb));
 }
 
 cudaError_t launch_sample_fast(const DevPtrs& d, int nrows, int k, const float* uniforms, int ldu,
@@ -509,21 +520,21 @@ cudaError_t launch_sample_fast(const DevPtrs& d, int nrows, int k, const float* 
                                int32_t* codes_out, float* fast_logits_out, int32_t* draws_out,
                                const uint16_t* fast_emb, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  sample_fast_kernel<<<nrows, kSampThreads, 0, st>>>(
-      d, k, make_io(uniforms, ldu, sp, forced, ldf, codes_out, nullptr, nullptr, fast_logits_out,
-                    draws_out, fast_emb));
-  return cudaGetLastError();
+  return launch_pdl(sample_fast_kernel, dim3(nrows), dim3(kSampThreads), 0, st, d, k,
+                    make_io(uniforms, ldu, sp, forced, ldf, codes_out, nullptr, nullptr, fast_logits_out,
+                            draws_out, fast_emb));
 }
 
 __global__ void fusion_kernel(DevPtrs d, const uint16_t* tok_emb, const uint16_t* fusion) {
+  pdl_wait();
+  pdl_launch();
   fusion_row<256>(d, blockIdx.x, tok_emb, fusion);
 }
 
 cudaError_t launch_fusion(const DevPtrs& d, int nrows, const uint16_t* tok_emb,
                           const uint16_t* fusion, cudaStream_t st) {
   if (nrows <= 0) return cudaSuccess;
-  fusion_kernel<<<nrows, 256, 0, st>>>(d, tok_emb, fusion);
-  return cudaGetLastError();
+  return launch_pdl(fusion_kernel, dim3(nrows), dim3(256), 0, st, d, tok_emb, fusion);
 }
 
 }  // namespace dualar

@@ -105,26 +105,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- TMA producer
+      // ---- TMA producer.  The weights are constant: the first stages' weight
+      // tiles are requested before waiting for the kernel that writes x.
       const uint64_t pol = policy_evict_first();
-      int issued = 0;
-      for (int i = 0; i < nch; ++i) {
-        const int s = i % S;
-        if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, a.err, a.wait_limit_ns)) {
-          raise_error(a.err, DEV_ERR_TC_WAIT);
-          break;
-        }
-        unsigned char* st = smem + s * SB;
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(SB));
+      auto load_w = [&](int i) {
+        unsigned char* st = smem + (i % S) * SB;
         const int kx = (c0 + i) * 64;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int r0 = tile * 256 + t * 128;
-          if (r0 < a.n0) tma_load_2d_hint(st + t * kTcWTile, &tw0, kx, r0, &full[s], pol);
-          else tma_load_2d_hint(st + t * kTcWTile, &tw1, kx, r0 - a.n0, &full[s], pol);
+          if (r0 < a.n0) tma_load_2d_hint(st + t * kTcWTile, &tw0, kx, r0, &full[i % S], pol);
+          else tma_load_2d_hint(st + t * kTcWTile, &tw1, kx, r0 - a.n0, &full[i % S], pol);
         }
-        tma_load_2d(st + 2 * kTcWTile, &txh, kx, 0, &full[s]);
-        tma_load_2d(st + 2 * kTcWTile + XT, &txl, kx, 0, &full[s]);
+      };
+      auto load_x = [&](int i) {
+        unsigned char* st = smem + (i % S) * SB;
+        const int kx = (c0 + i) * 64;
+        tma_load_2d(st + 2 * kTcWTile, &txh, kx, 0, &full[i % S]);
+        tma_load_2d(st + 2 * kTcWTile + XT, &txl, kx, 0, &full[i % S]);
+      };
+      const int pre = nch < S ? nch : S;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], static_cast<uint32_t>(SB));
+        load_w(i);
+      }
+      pdl_wait();
+      pdl_launch();
+      for (int i = 0; i < pre; ++i) load_x(i);
+      int issued = pre;
+      for (int i = pre; i < nch; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&empty[s], ((i / S) - 1) & 1, a.err, a.wait_limit_ns)) {
+          raise_error(a.err, DEV_ERR_TC_WAIT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(SB));
+        load_w(i);
+        load_x(i);
         ++issued;
       }
       // every copy issued here has landed before the CTA may exit (bounded)
@@ -165,6 +182,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ---- read-back: warp w may access TMEM lanes 32*(w%4) .. +31
+    pdl_wait();   // (the partial sums' buffer is read by the previous reduce)
     const int q = warp & 3;
     const bool accd = mbar_wait(&accf[0], 0, a.err, a.wait_limit_ns);
     if (!accd && lane == 0) raise_error(a.err, DEV_ERR_TC_WAIT | (1u << 7));
@@ -205,6 +223,8 @@ constexpr int kSplitVec = 3;   // float4 per thread
 __global__ void __launch_bounds__(kSplitThreads, 1)
     tc_split_kernel(const float* x, int ldx, int K, const uint16_t* norm_w, float eps, uint16_t* xh, uint16_t* xl,
                     int ldxh, float* save_x, const int32_t* save_map, int lds) {
+  pdl_wait();
+  pdl_launch();
   const int m = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * ldx);
   const int KV = K >> 2;
@@ -259,6 +279,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
                                  int ldo, const float* base, int ldb, const int32_t* out_map, int n0, uint16_t* xh,
                                  uint16_t* xl, int ldxh) {
+  pdl_wait();
+  pdl_launch();
   const int nq = n_out >> 2;   // n_out % 4 == 0 (host)
   const size_t total = static_cast<size_t>(nb) * nq;
   // the slices' partials, four loads in flight, added in slice order
@@ -319,6 +341,8 @@ __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp,
 __global__ void tc_reduce_scalar_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode,
                                         float* out, int ldo, const float* base, int ldb, const int32_t* out_map,
                                         int n0) {
+  pdl_wait();
+  pdl_launch();
   const size_t total = static_cast<size_t>(nb) * n_out;
   for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -419,8 +443,7 @@ static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  tc_gemm_kernel<NBP><<<grid, kTcThreads, smem, st>>>(w0, w1, xh, xl, t);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<NBP>, grid, dim3(kTcThreads), smem, st, w0, w1, xh, xl, t);
 }
 
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
@@ -445,9 +468,8 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
 
   cudaError_t e = cudaSuccess;
   if (!x_ready) {
-    tc_split_kernel<<<a.nb, kSplitThreads, 0, st>>>(a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh, b.xl, b.ldx, a.save_x,
-                                                    a.save_map, a.lds);
-    e = cudaGetLastError();
+    e = launch_pdl(tc_split_kernel, dim3(a.nb), dim3(kSplitThreads), 0, st, a.x, a.ldx, a.K, a.norm_w, a.eps, b.xh,
+                   b.xl, b.ldx, a.save_x, a.save_map, a.lds);
     if (e != cudaSuccess) return e;
     if (launches) *launches += 1;
   }
@@ -467,14 +489,15 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
   int rgrid = static_cast<int>((total + 255) / 256);
   rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
   if (vec)
-    tc_reduce_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb,
-                                            a.out_map, a.n0, split_out ? b.xh : nullptr, split_out ? b.xl : nullptr,
-                                            b.ldx);
+    e = launch_pdl(tc_reduce_kernel, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), slices, a.nb,
+                   n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb, a.out_map, a.n0,
+                   split_out ? b.xh : static_cast<uint16_t*>(nullptr), split_out ? b.xl : static_cast<uint16_t*>(nullptr),
+                   b.ldx);
   else
-    tc_reduce_scalar_kernel<<<rgrid, 256, 0, st>>>(b.part, slices, a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base,
-                                                   a.ldb, a.out_map, a.n0);
+    e = launch_pdl(tc_reduce_scalar_kernel, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), slices,
+                   a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb, a.out_map, a.n0);
   if (launches) *launches += 2;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dualar
