@@ -46,6 +46,7 @@ struct dualar_handle {
   TcBuffers tc{};                // tensor-core projection buffers
   const float* tc_ready_x = nullptr;   // the tc buffers hold the halves of this [nb][K] input
   int tc_ready_k = 0, tc_ready_nb = 0;
+  TcPending tc_pend;             // a residual-add reduce not yet queued (see run_gemv)
   uint32_t bar_extra = 0;
   uint32_t* bar_counter = nullptr;
   uint64_t* tagged = nullptr;    // the tagged work buffers (one region)
@@ -73,8 +74,24 @@ void set_err(dualar_handle* h, const char* fmt, ...) {
   h->err = buf;
 }
 
+// Queues the deferred residual-add reduce, if any.
+int flush_tc(dualar_handle* h) {
+  if (!h->tc_pend.on) return DUALAR_OK;
+  h->tc_pend.on = false;
+  ++h->launches;
+  const cudaError_t e = launch_tc_pending(h->tc_pend, h->tc, h->n_sm, h->stream);
+  if (e != cudaSuccess) {
+    set_err(h, "tensor-core reduce failed: %s", cudaGetErrorString(e));
+    return DUALAR_ERR_CUDA;
+  }
+  return DUALAR_OK;
+}
+
+// Every stream operation first queues a deferred reduce (flush_tc), so that
+// nothing can read the residual stream before it is written.
 #define CUDA_TRY(h, call)                                                               \
   do {                                                                                  \
+    if (const int frc_ = flush_tc(h)) return frc_;                                      \
     cudaError_t e_ = (call);                                                            \
     if (e_ != cudaSuccess) {                                                            \
       set_err(h, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
@@ -84,6 +101,7 @@ void set_err(dualar_handle* h, const char* fmt, ...) {
 
 #define LAUNCH(h, call)                                                                 \
   do {                                                                                  \
+    if (const int frc_ = flush_tc(h)) return frc_;                                      \
     cudaError_t e_ = (call);                                                            \
     ++(h)->launches;                                                                    \
     if (e_ != cudaSuccess) {                                                            \
@@ -210,12 +228,28 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
     // 9..128 rows: one pass over the weights on the tensor cores.  The
     // SwiGLU output feeds the down projection without norm: its reduce
     // writes the halves the next GEMM reads, and that split is skipped.
+    // A residual-add projection's reduce waits for the next projection: if
+    // that one normalises the residual stream, reduce, norm and split run
+    // as one kernel.
     int n = 0;
-    const bool ready = h->tc_ready_x == a.x && h->tc_ready_k == a.K && h->tc_ready_nb == a.nb &&
-                       a.ldx == a.K && a.norm_w == nullptr && a.save_x == nullptr;
+    bool fused = false;
+    if (h->tc_pend.on && tc_can_fuse(h->tc_pend, a)) {
+      h->tc_pend.on = false;
+      ++n;
+      const cudaError_t ef = launch_tc_reduce_norm(h->tc_pend, a, h->tc, h->stream);
+      if (ef != cudaSuccess) {
+        set_err(h, "tensor-core reduce failed: %s", cudaGetErrorString(ef));
+        return DUALAR_ERR_CUDA;
+      }
+      fused = true;
+    } else if (const int frc = flush_tc(h)) {
+      return frc;
+    }
+    const bool ready = fused || (h->tc_ready_x == a.x && h->tc_ready_k == a.K && h->tc_ready_nb == a.nb &&
+                                 a.ldx == a.K && a.norm_w == nullptr && a.save_x == nullptr);
     const bool split_out = a.mode == GEMV_SWIGLU && a.out_map == nullptr && a.ldo == a.n0;
     h->tc_ready_x = nullptr;
-    const cudaError_t e = launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n, ready, split_out);
+    const cudaError_t e = launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n, ready, split_out, &h->tc_pend);
     if (e == cudaSuccess && split_out) {
       h->tc_ready_x = a.out;
       h->tc_ready_k = a.n0;
@@ -661,6 +695,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
   LAUNCH(h, launch_fusion(d, batch, U16(h->w.tok_emb), U16(h->w.fusion), h->stream));
   TRY(slow_stack(h, batch, units, chunk, true));
   TRY(run_gemv(h, args_head(h, 0, batch)));
+  TRY(flush_tc(h));
   for (int r = 0; r < batch; ++r) h->length[slots[r]] += 1;
   return DUALAR_OK;
 }
@@ -941,6 +976,7 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
     TRY(slow_stack(h, m, units, chunk, false));
     if (c0 + m == n_tokens) TRY(run_gemv(h, args_head(h, m - 1, 1)));
   }
+  TRY(flush_tc(h));
   h->length[slot] = n_tokens;
   return DUALAR_OK;
 }

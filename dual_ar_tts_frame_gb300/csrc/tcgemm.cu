@@ -21,6 +21,10 @@
 //  3. tc_reduce_kernel: adds the partial sums of the K slices in slice order
 //     (deterministic) and applies the epilogue: store / residual add / SwiGLU,
 //     with the optional output row map.
+// A residual-add projection's reduce is usually fused with the next
+// projection's split (tc_reduce_norm_kernel: the same sums and the same norm
+// arithmetic, one CTA per row), since that projection reads the residual
+// stream it writes.
 // [P2] "The slow AR is Qwen3-4B" (the projections of a Qwen3 layer) and "Two
 // autoregressions" (the fast AR's layers and head).
 #include <cuda.h>
@@ -274,6 +278,77 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   }
 }
 
+// Residual add of the K-slice partials (slice order, as tc_reduce_kernel),
+// then the split of the result as tc_split_kernel does it (the same thread
+// mapping, so the same sums): out = base + sum, x' = RMSNorm(out) * g.
+__global__ void __launch_bounds__(kSplitThreads, 1)
+    tc_reduce_norm_kernel(const float* part, int slices, int nb, int ldp, int K, const float* base, int ldb,
+                          float* out, int ldo, const uint16_t* norm_w, float eps, uint16_t* xh, uint16_t* xl,
+                          int ldxh, float* save_x, const int32_t* save_map, int lds) {
+  pdl_wait();
+  pdl_launch();
+  const int m = blockIdx.x;
+  const int KV = K >> 2;
+  const size_t stride = static_cast<size_t>(nb) * ldp;
+  __shared__ float red[32];
+  float4 v[kSplitVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < kSplitVec; ++q) {
+    const int j = threadIdx.x + q * kSplitThreads;
+    v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < KV) {
+      const float* p0 = part + static_cast<size_t>(m) * ldp + 4 * j;
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      int sl = 0;
+      for (; sl + 8 <= slices; sl += 8) {
+        float4 t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = *reinterpret_cast<const float4*>(p0 + (sl + k) * stride);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          y.x += t[k].x; y.y += t[k].y; y.z += t[k].z; y.w += t[k].w;
+        }
+      }
+      for (; sl < slices; ++sl) {
+        const float4 t = *reinterpret_cast<const float4*>(p0 + sl * stride);
+        y.x += t.x; y.y += t.y; y.z += t.z; y.w += t.w;
+      }
+      const float4 bb = *reinterpret_cast<const float4*>(base + static_cast<size_t>(m) * ldb + 4 * j);
+      v[q] = make_float4(bb.x + y.x, bb.y + y.y, bb.z + y.z, bb.w + y.w);
+      *reinterpret_cast<float4*>(out + static_cast<size_t>(m) * ldo + 4 * j) = v[q];
+    }
+    ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll 8
+  for (int w = 0; w < kSplitThreads / 32; ++w) t += red[w];
+  const float sc = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
+  const int row = save_x ? (save_map ? save_map[m] : m) : -1;
+#pragma unroll
+  for (int q = 0; q < kSplitVec; ++q) {
+    const int j = threadIdx.x + q * kSplitThreads;
+    if (j >= KV) continue;
+    const uint2 gw = *reinterpret_cast<const uint2*>(norm_w + 4 * j);
+    float e[4] = {(v[q].x * bf16lo(gw.x)) * sc, (v[q].y * bf16hi(gw.x)) * sc, (v[q].z * bf16lo(gw.y)) * sc,
+                  (v[q].w * bf16hi(gw.y)) * sc};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint16_t hb = f32_to_bf16bits(e[c]);
+      h[c] = hb;
+      l[c] = f32_to_bf16bits(e[c] - bf16bits_to_f32(hb));
+    }
+    *reinterpret_cast<uint2*>(xh + static_cast<size_t>(m) * ldxh + 4 * j) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    *reinterpret_cast<uint2*>(xl + static_cast<size_t>(m) * ldxh + 4 * j) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    if (row >= 0)
+      *reinterpret_cast<float4*>(save_x + static_cast<size_t>(row) * lds + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
+  }
+}
+
 // Sum of the K-slice partials (slice order) and the epilogue, 4 columns per
 // thread (all row strides multiples of 4 floats).
 __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
@@ -287,12 +362,12 @@ __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp,
   auto sum = [&](const float* p0, size_t stride) {
     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = 0;
-    for (; s + 4 <= slices; s += 4) {
-      float4 q[4];
+    for (; s + 8 <= slices; s += 8) {
+      float4 q[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const float4*>(p0 + (s + k) * stride);
+      for (int k = 0; k < 8; ++k) q[k] = *reinterpret_cast<const float4*>(p0 + (s + k) * stride);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         y.x += q[k].x; y.y += q[k].y; y.z += q[k].z; y.w += q[k].w;
       }
     }
@@ -447,7 +522,7 @@ static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1,
 }
 
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
-                           bool x_ready, bool split_out) {
+                           bool x_ready, bool split_out, TcPending* defer) {
   const int nbp = a.nb <= 16 ? 16 : a.nb <= 32 ? 32 : a.nb <= 64 ? 64 : 128;
   const int n_rows = a.n0 + a.n1;   // virtual weight rows (SwiGLU: gate then up)
   const int tiles = (n_rows + 255) / 256;
@@ -485,6 +560,19 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
   const int n_out = a.mode == GEMV_SWIGLU ? a.n0 : n_rows;
   const bool vec = n_out % 4 == 0 && n_rows % 4 == 0 && a.ldo % 4 == 0 && (a.mode != GEMV_ADD || a.ldb % 4 == 0);
   if (split_out && (!vec || a.out_map != nullptr || n_out > b.ldx)) return cudaErrorInvalidValue;
+  if (defer != nullptr && a.mode == GEMV_ADD && vec && a.out_map == nullptr && !split_out) {
+    defer->on = true;
+    defer->slices = slices;
+    defer->nb = a.nb;
+    defer->ldp = n_rows;
+    defer->n_out = n_out;
+    defer->out = a.out;
+    defer->ldo = a.ldo;
+    defer->base = a.base;
+    defer->ldb = a.ldb;
+    if (launches) *launches += 1;
+    return cudaSuccess;
+  }
   const size_t total = static_cast<size_t>(a.nb) * (vec ? n_out / 4 : n_out);
   int rgrid = static_cast<int>((total + 255) / 256);
   rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
@@ -498,6 +586,27 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
                    a.nb, n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb, a.out_map, a.n0);
   if (launches) *launches += 2;
   return e;
+}
+
+bool tc_can_fuse(const TcPending& p, const GemvArgs& a) {
+  return p.on && a.x == p.out && a.ldx == p.ldo && a.K == p.n_out && a.nb == p.nb && a.norm_w != nullptr &&
+         a.K <= 4 * kSplitThreads * kSplitVec && (a.save_x == nullptr || a.lds % 4 == 0);
+}
+
+cudaError_t launch_tc_pending(const TcPending& p, const TcBuffers& b, int n_sm, cudaStream_t st) {
+  const size_t total = static_cast<size_t>(p.nb) * (p.n_out / 4);
+  int rgrid = static_cast<int>((total + 255) / 256);
+  rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
+  return launch_pdl(tc_reduce_kernel, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), p.slices,
+                    p.nb, p.ldp, p.n_out, static_cast<int>(GEMV_ADD), p.out, p.ldo, p.base, p.ldb,
+                    static_cast<const int32_t*>(nullptr), 0, static_cast<uint16_t*>(nullptr),
+                    static_cast<uint16_t*>(nullptr), b.ldx);
+}
+
+cudaError_t launch_tc_reduce_norm(const TcPending& p, const GemvArgs& a, const TcBuffers& b, cudaStream_t st) {
+  return launch_pdl(tc_reduce_norm_kernel, dim3(p.nb), dim3(kSplitThreads), 0, st, static_cast<const float*>(b.part),
+                    p.slices, p.nb, p.ldp, p.n_out, p.base, p.ldb, p.out, p.ldo, a.norm_w, a.eps, b.xh, b.xl, b.ldx,
+                    a.save_x, a.save_map, a.lds);
 }
 
 }  // namespace dualar

@@ -31,10 +31,33 @@ bool tc_eligible(const GemvArgs& a, int ldx);
 // Tensor map of a bf16 matrix [rows][K] (row stride ld elements), tiles of
 // box_rows x 64 with 128-byte swizzle; built once per argument set and kept.
 bool tc_bf16_map(CUtensorMap* out, const void* base, int K, int rows, int ld, int box_rows);
+// A residual-add reduce that has not been queued yet: the split-K partial
+// sums of the last projection, to be added to base and stored to out.
+struct TcPending {
+  bool on = false;
+  int slices = 0, nb = 0, ldp = 0, n_out = 0;
+  float* out = nullptr;
+  int ldo = 0;
+  const float* base = nullptr;
+  int ldb = 0;
+};
+
 // Queues split (unless x_ready: the buffers already hold x's halves), GEMM
 // and reduce kernels; split_out: the reduce also writes the output's halves
-// (it is the next projection's input, without norm).  *launches += count.
+// (it is the next projection's input, without norm).  With defer (a
+// residual-add projection whose output is one of the buffers' row blocks)
+// the reduce is not queued but described in *defer: the caller queues it
+// later, alone (launch_tc_pending) or fused with the next projection's
+// norm and split (launch_tc_reduce_norm).  *launches += count.
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
-                           bool x_ready = false, bool split_out = false);
+                           bool x_ready = false, bool split_out = false, TcPending* defer = nullptr);
+// Whether a deferred reduce can be fused into the split of projection a
+// (its input is the pending output, with a norm).
+bool tc_can_fuse(const TcPending& p, const GemvArgs& a);
+// The pending reduce on its own.
+cudaError_t launch_tc_pending(const TcPending& p, const TcBuffers& b, int n_sm, cudaStream_t st);
+// The pending reduce, then a's RMSNorm and bf16 halves (and save_x) in the
+// same kernel, one CTA per row; a's GEMM then runs with x_ready.
+cudaError_t launch_tc_reduce_norm(const TcPending& p, const GemvArgs& a, const TcBuffers& b, cudaStream_t st);
 
 }  // namespace dualar
