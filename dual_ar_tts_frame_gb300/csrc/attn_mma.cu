@@ -12,7 +12,7 @@
 //               the two row results are added afterwards),
 //   online softmax over the page on the fragment rows,
 //   O += P V   (P split into hi + lo rows the same way).
-// A CTA has seven warps with fixed roles, chained by mbarriers:
+// A CTA has eight warps with fixed roles, chained by mbarriers:
 //  * prep (warp 5) takes units from a per-layer counter shared by all CTAs
 //    (a CTA that finishes early takes more): first every full chunk, row
 //    by row, then every row's last (partial) chunk, rows ordered by that
@@ -22,17 +22,18 @@
 //    to the cache; it publishes the unit in one of two shared-memory
 //    descriptors;
 //  * producer (warp 4, one lane) copies the units' K and V pages by TMA
-//    (128-byte swizzle, so ldmatrix reads are conflict-free).  Page p of
-//    unit u goes to compute warp (p + u) % 4 (a function of the unit alone,
-//    so the rounding of the result does not depend on the schedule), which
-//    owns a small ring of slots (each the K or the V block of a page) and
-//    takes them in order: every slot has a single consumer, so an mbarrier
-//    wait is never more than one phase ahead of its barrier (a parity wait
-//    cannot tell phases two apart);
-//  * compute (warps 0-3) run the MMAs and hand their (m, l, O) to
-//  * finalize (warp 6), which merges the four in warp order, writes the
-//    partial (or the output), and for the last chunk of a (row, KV head) to
-//    arrive combines the chunks in chunk order.
+//    (128-byte swizzle, so ldmatrix reads are conflict-free) into a ring of
+//    page slots (K then V) that every compute warp reads in order (so an
+//    mbarrier wait is never more than one phase ahead of its barrier: a
+//    parity wait cannot tell phases two apart); the ring holds 160-192 KB
+//    (five or six pages at hd 128), all lookahead for the four warps;
+//  * compute warp w takes tokens 16 w .. 16 w + 15 of every page (a
+//    function of the page alone, so the rounding does not depend on the
+//    schedule), with its own running (m, l, O);
+//  * compute warps hand their (m, l, O) to
+//  * finalize (warps 6 and 7, alternate units), which merges the four in
+//    warp order, writes the partial (or the output), and for the last chunk
+//    of a (row, KV head) to arrive combines the chunks in chunk order.
 // The compute warps thus never wait on global memory between units.  The
 // page copy of the newest position may predate its cache write; the compute
 // warp patches that row in shared memory from the descriptor.
@@ -52,17 +53,19 @@ namespace dualar {
 constexpr int kAmWarps = 4;                        // compute warps
 constexpr int kAmProducer = kAmWarps;              // page copies
 constexpr int kAmPrep = kAmWarps + 1;              // unit set-up
-constexpr int kAmFinal = kAmWarps + 2;             // merge and combine
-constexpr int kAmThreads = (kAmWarps + 3) * 32;
+constexpr int kAmFinal = kAmWarps + 2;             // merge and combine: two warps, alternate units
+constexpr int kAmFinalWarps = 2;
+constexpr int kAmThreads = (kAmWarps + 2 + kAmFinalWarps) * 32;
 constexpr int kAmBox = 64 * 64 * 2;                // one TMA box: 64 tokens x 64 dims (bf16)
 constexpr uint32_t kAmUnitUsers = 1 + kAmWarps + 1;   // producer, compute warps, finalize
 
-template <int HD>
+template <int HD, int G>
 struct AmCfg {
   static constexpr int HALVES = HD / 64;                  // boxes per 64-token K (or V) block
-  static constexpr int SLOT = HALVES * kAmBox;            // a slot: the K or the V block of one page
-  static constexpr int SLOTS = HD == 128 ? 3 : 4;         // slots of each compute warp
-  static constexpr int NBUF = kAmWarps * SLOTS;
+  static constexpr int HALF = HALVES * kAmBox;            // the K (or the V) block of one page
+  static constexpr int SLOT = 2 * HALF;                   // a slot: one page, K then V
+  // pages in the ring: 192 KB, 160 KB where the merge buffers are largest
+  static constexpr int NBUF = ((HD == 128 && G > 4 ? 160 : 192) * 1024) / SLOT;
 };
 
 // One unit as the prep warp publishes it.
@@ -71,7 +74,7 @@ struct AmUnitDesc {
   float q[G][HD];                         // query rows, 1/sqrt(hd) folded in
   uint32_t knew[HD / 2], vnew[HD / 2];    // newest position's K and V (bf16 pairs)
   int32_t pages[kMaxChunkPages];
-  int32_t r, g, c, nch, t0, t1, npages, pos, newest, rot, last;
+  int32_t r, g, c, nch, t0, t1, npages, pos, newest, last;
 };
 
 // The launch's rows and the unit order built from them.
@@ -87,18 +90,23 @@ template <int HD, int G>
 struct AmSmem {
   // after the ring
   AmUnitDesc<HD, G> unit[2];
-  float co[kAmWarps][G][HD];
-  float cm[kAmWarps][8], cl[kAmWarps][8];
-  float fc[8][kMaxChunks];   // finalize: chunk weights of each head
+  // the compute warps' states of units k (buffer k % 2), for finalize warp k % 2
+  float co[2][kAmWarps][G][HD];
+  float cm[2][kAmWarps][8], cl[2][kAmWarps][8];
+  struct Fin {
+    float fw[kAmWarps][8];              // merge weight of each warp's state, per head
+    float m[8], ls[8];                  // merged max and sum, per head
+    float fm[8][kMaxChunks], fl[8][kMaxChunks];   // chunk combine: max (then weight) and sum
+  } fin[kAmFinalWarps];
   AmSmemRows t;
-  uint64_t full[AmCfg<HD>::NBUF], empty[AmCfg<HD>::NBUF];
-  uint64_t ufull[2], uempty[2], cfull, cempty;
+  uint64_t full[AmCfg<HD, G>::NBUF], empty[AmCfg<HD, G>::NBUF];
+  uint64_t ufull[2], uempty[2], cfull[2], cempty[2];
   int abort_flag;
 };
 
 template <int HD, int G>
 constexpr size_t am_smem_bytes() {
-  return static_cast<size_t>(AmCfg<HD>::NBUF) * AmCfg<HD>::SLOT + sizeof(AmSmem<HD, G>) + 1024;
+  return static_cast<size_t>(AmCfg<HD, G>::NBUF) * AmCfg<HD, G>::SLOT + sizeof(AmSmem<HD, G>) + 1024;
 }
 
 DEVI void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -230,7 +238,7 @@ template <int HD, int G>
 __global__ void __launch_bounds__(kAmThreads, 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tkv, const DevPtrs d, int nrows, int layer, int total_units,
                     int chunk_tokens, int fuse, const uint16_t* q_norm, const uint16_t* k_norm) {
-  using C = AmCfg<HD>;
+  using C = AmCfg<HD, G>;
   using Desc = AmUnitDesc<HD, G>;
   constexpr int NB = C::NBUF;
   constexpr int EPL = HD / 32;
@@ -245,14 +253,16 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   if (tid == 0) {
     for (int b = 0; b < NB; ++b) {
       mbar_init(&sm.full[b], 1);
-      mbar_init(&sm.empty[b], 1);
+      mbar_init(&sm.empty[b], kAmWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.ufull[b], 1);
       mbar_init(&sm.uempty[b], kAmUnitUsers);
     }
-    mbar_init(&sm.cfull, kAmWarps);
-    mbar_init(&sm.cempty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.cfull[b], kAmWarps);
+      mbar_init(&sm.cempty[b], 1);
+    }
     sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -420,14 +430,15 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         un_d.npages = un.npages;
         un_d.pos = pos;
         un_d.newest = newest ? 1 : 0;
-        un_d.rot = v & (kAmWarps - 1);
         un_d.last = 0;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.ufull[b]);
       ++k;
     }
-    if (ok) {
+    // end markers: one for every reader, and one more for the finalize warp
+    // that takes the next unit number
+    for (int e = 0; ok && e < 2; ++e, ++k) {
       const int b = static_cast<int>(k & 1);
       if (k >= 2 && !am_wait(&sm.uempty[b], ((k >> 1) - 1) & 1, abort_flag, d)) {
         *abort_flag = 1;
@@ -437,17 +448,16 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         sm.unit[b].last = 1;
         mbar_arrive(&sm.ufull[b]);
       }
+      __syncwarp();
     }
     return;
   }
 
   if (warp == kAmProducer) {
-    // ---- producer (lane 0): the K/V pages of the published units, in order
+    // ---- producer (lane 0): the K/V pages of the published units, in order,
+    // into a ring of page slots that every compute warp reads
     if (lane != 0) return;
-    uint32_t cnt[kAmWarps];   // slot fills given to each compute warp so far
-    uint32_t iss[kAmWarps];   // ... and actually issued
-#pragma unroll
-    for (int w = 0; w < kAmWarps; ++w) cnt[w] = iss[w] = 0;
+    uint32_t gp = 0;   // pages issued
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
       const int b = static_cast<int>(k & 1);
@@ -457,87 +467,89 @@ __global__ void __launch_bounds__(kAmThreads, 1)
       }
       const Desc& un_d = sm.unit[b];
       if (un_d.last) break;
-      const int npages = un_d.npages, g = un_d.g, rot = un_d.rot;
-      for (int p = 0; ok && p < npages; ++p) {
+      const int npages = un_d.npages, g = un_d.g;
+      for (int p = 0; p < npages; ++p, ++gp) {
         const int pgp = un_d.pages[p];
-        const int w = (p + rot) & (kAmWarps - 1);
+        const int s = static_cast<int>(gp % NB);
+        if (gp >= static_cast<uint32_t>(NB) && !am_wait(&sm.empty[s], ((gp / NB) - 1) & 1, abort_flag, d)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
         const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + g) * 64);
+        mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::SLOT));
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          uint32_t j = 0;
-#pragma unroll
-          for (int ww = 0; ww < kAmWarps; ++ww)
-            if (ww == w) j = cnt[ww]++;
-          const int s = w * C::SLOTS + static_cast<int>(j % C::SLOTS);
-          if (!ok) continue;
-          if (j >= static_cast<uint32_t>(C::SLOTS) &&
-              !am_wait(&sm.empty[s], ((j / C::SLOTS) - 1) & 1, abort_flag, d)) {
-            *abort_flag = 1;
-            ok = false;
-            continue;
-          }
-          mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::SLOT));
+        for (int kv = 0; kv < 2; ++kv)
 #pragma unroll
           for (int hh = 0; hh < C::HALVES; ++hh)
-            tma_load_2d(ring + s * C::SLOT + hh * kAmBox, &tkv, hh * 64, rowk + kv * hkv * 64, &sm.full[s]);
-#pragma unroll
-          for (int ww = 0; ww < kAmWarps; ++ww)
-            if (ww == w) ++iss[ww];
-        }
+            tma_load_2d(ring + s * C::SLOT + kv * C::HALF + hh * kAmBox, &tkv, hh * 64, rowk + kv * hkv * 64,
+                        &sm.full[s]);
       }
       if (ok) mbar_arrive(&sm.uempty[b]);
     }
     // every copy issued here lands before the CTA exits (bounded)
-    for (int w = 0; w < kAmWarps; ++w)
-      for (uint32_t j = iss[w] > static_cast<uint32_t>(C::SLOTS) ? iss[w] - C::SLOTS : 0; j < iss[w]; ++j) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&sm.full[w * C::SLOTS + j % C::SLOTS], (j / C::SLOTS) & 1))
-          if (global_timer_ns() - t0 > d.wait_limit_ns) break;
-      }
+    for (uint32_t j = gp > static_cast<uint32_t>(NB) ? gp - NB : 0; j < gp; ++j) {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&sm.full[j % NB], (j / NB) & 1))
+        if (global_timer_ns() - t0 > d.wait_limit_ns) break;
+    }
     return;
   }
 
-  if (warp == kAmFinal) {
-    // ---- finalize: merge the compute warps' states, write, combine chunks
-    for (uint32_t k = 0;; ++k) {
-      const int b = static_cast<int>(k & 1);
+  if (warp >= kAmFinal) {
+    // ---- finalize warp fi: units fi, fi + 2, ... (descriptor and state
+    // buffers fi); merge the compute warps' states, write, combine chunks
+    constexpr int EPLF = HD / 32;
+    const int fi = warp - kAmFinal;
+    auto& fz = sm.fin[fi];
+    for (uint32_t k = static_cast<uint32_t>(fi);; k += 2) {
+      const int b = fi;
       if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
         *abort_flag = 1;
         return;
       }
       const Desc& un_d = sm.unit[b];
       if (un_d.last) return;
-      if (!am_wait(&sm.cfull, k & 1, abort_flag, d)) {
+      if (!am_wait(&sm.cfull[b], (k >> 1) & 1, abort_flag, d)) {
         *abort_flag = 1;
         return;
       }
       const int r = un_d.r, g = un_d.g, c = un_d.c, nch = un_d.nch;
       const size_t attn_off = static_cast<size_t>(r) * hq * HD + g * G * HD;
       float* pw = d.part + ((static_cast<size_t>(r) * hkv + g) * kMaxChunks + c) * G * (HD + 2);
-      for (int e = lane; e < G * HD; e += 32) {
-        const int h = e / HD, dd = e % HD;
+      if (lane < G) {
+        const int h = lane;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kAmWarps; ++w) M = fmaxf(M, sm.cm[w][h]);
-        float Ls = 0.f, Os = 0.f;
+        for (int w = 0; w < kAmWarps; ++w) M = fmaxf(M, sm.cm[b][w][h]);
+        float Ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kAmWarps; ++w) {
-          const float fw = sm.cm[w][h] == -INFINITY ? 0.f : expf(sm.cm[w][h] - M);
-          Ls += sm.cl[w][h] * fw;
-          Os += sm.co[w][h][dd] * fw;
+          const float fw = sm.cm[b][w][h] == -INFINITY ? 0.f : expf(sm.cm[b][w][h] - M);
+          fz.fw[w][h] = fw;
+          Ls += sm.cl[b][w][h] * fw;
         }
+        fz.m[h] = M;
+        fz.ls[h] = Ls;
+      }
+      __syncwarp();
+      for (int e = lane; e < G * HD; e += 32) {
+        const int h = e / HD, dd = e % HD;
+        float Os = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAmWarps; ++w) Os += sm.co[b][w][h][dd] * fz.fw[w][h];
         if (nch == 1) {
-          d.attn[attn_off + h * HD + dd] = Os / Ls;
+          d.attn[attn_off + h * HD + dd] = Os / fz.ls[h];
         } else {
           pw[h * (HD + 2) + dd] = Os;
           if (dd == 0) {
-            pw[h * (HD + 2) + HD] = M;
-            pw[h * (HD + 2) + HD + 1] = Ls;
+            pw[h * (HD + 2) + HD] = fz.m[h];
+            pw[h * (HD + 2) + HD + 1] = fz.ls[h];
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.cempty);
+      if (lane == 0) mbar_arrive(&sm.cempty[b]);
       if (nch > 1) {
         __threadfence();
         __syncwarp();
@@ -551,35 +563,50 @@ __global__ void __launch_bounds__(kAmThreads, 1)
           }
         }
         if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+          // the chunks in chunk order: every chunk's (m, l) first (one
+          // round of loads), the weights per head, then O with all heads'
+          // loads of a chunk in flight together
           __threadfence();
           const float* pb = d.part + (static_cast<size_t>(r) * hkv + g) * kMaxChunks * G * (HD + 2);
-          for (int h = 0; h < G; ++h) {
-            float mx = -INFINITY;
-            for (int cc = lane; cc < nch; cc += 32) mx = fmaxf(mx, ldf(pb + (cc * G + h) * (HD + 2) + HD));
-            const float M = warp_max(mx);
-            float ls = 0.f;
-            for (int cc = lane; cc < nch; cc += 32) {
-              const float* q = pb + (cc * G + h) * (HD + 2);
-              const float f = expf(ldf(q + HD) - M);
-              sm.fc[h][cc] = f;
-              ls += ldf(q + HD + 1) * f;
-            }
-            const float Ls = warp_sum(ls);
-            __syncwarp();
-            float os[EPL];
-#pragma unroll
-            for (int j = 0; j < EPL; ++j) os[j] = 0.f;
-#pragma unroll 4
-            for (int cc = 0; cc < nch; ++cc) {
-              const float* q = pb + (cc * G + h) * (HD + 2) + lane * EPL;
-              const float f = sm.fc[h][cc];
-#pragma unroll
-              for (int j = 0; j < EPL; ++j) os[j] += ldf(q + j) * f;
-            }
-#pragma unroll
-            for (int j = 0; j < EPL; ++j) d.attn[attn_off + h * HD + lane * EPL + j] = os[j] / Ls;
-            __syncwarp();
+          for (int i = lane; i < nch * G; i += 32) {
+            const int cc = i / G, h = i % G;
+            const float* q = pb + (cc * G + h) * (HD + 2);
+            fz.fm[h][cc] = ldf(q + HD);
+            fz.fl[h][cc] = ldf(q + HD + 1);
           }
+          __syncwarp();
+          if (lane < G) {
+            const int h = lane;
+            float M = -INFINITY;
+            for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, fz.fm[h][cc]);
+            float Ls = 0.f;
+            for (int cc = 0; cc < nch; ++cc) {
+              const float f = expf(fz.fm[h][cc] - M);
+              fz.fm[h][cc] = f;
+              Ls += fz.fl[h][cc] * f;
+            }
+            fz.ls[h] = Ls;
+          }
+          __syncwarp();
+          float os[G][EPLF];
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < EPLF; ++j) os[h][j] = 0.f;
+#pragma unroll 2
+          for (int cc = 0; cc < nch; ++cc) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float* q = pb + (cc * G + h) * (HD + 2) + lane * EPLF;
+              const float f = fz.fm[h][cc];
+#pragma unroll
+              for (int j = 0; j < EPLF; ++j) os[h][j] += ldf(q + j) * f;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < EPLF; ++j) d.attn[attn_off + h * HD + lane * EPLF + j] = os[h][j] / fz.ls[h];
         }
       }
       __syncwarp();
@@ -592,7 +619,7 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   const int head = ROWS8 ? gr : (gr & 3);           // the query head of this lane's rows
   const bool lo_row = !ROWS8 && gr >= 4;            // rows 4..7 carry the lo halves (G <= 4)
   const bool writer = (ROWS8 || gr < 4) && head < G;
-  uint32_t mine = 0;   // pages this warp has taken so far (its slot sequence)
+  uint32_t gp = 0;   // pages taken so far (the ring position)
   for (uint32_t k = 0;; ++k) {
     const int b = static_cast<int>(k & 1);
     if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
@@ -623,21 +650,18 @@ __global__ void __launch_bounds__(kAmThreads, 1)
 #pragma unroll
     for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-    const int p0 = (warp - un_d.rot) & (kAmWarps - 1);
-    for (int p = p0; p < npages; p += kAmWarps) {
-      const uint32_t jk = mine++, jv = mine++;
-      const int sk = warp * C::SLOTS + static_cast<int>(jk % C::SLOTS);
-      const int sv = warp * C::SLOTS + static_cast<int>(jv % C::SLOTS);
-      bool got = am_wait(&sm.full[sk], (jk / C::SLOTS) & 1, abort_flag, d);
-      got = got && am_wait(&sm.full[sv], (jv / C::SLOTS) & 1, abort_flag, d);
-      if (!got) {
+    // every page of the unit; this warp takes its tokens 16 warp .. +15
+    const int tw = 16 * warp;
+    for (int p = 0; p < npages; ++p, ++gp) {
+      const int s = static_cast<int>(gp % NB);
+      if (!am_wait(&sm.full[s], (gp / NB) & 1, abort_flag, d)) {
         *abort_flag = 1;
         return;
       }
       const int ps = t0 + p * kPageTokens;
       const int ntok = min(kPageTokens, t1 - ps);
-      const uint32_t kb = ring_s + sk * C::SLOT, vb = ring_s + sv * C::SLOT;
-      if (newest && ps <= pos && pos < ps + kPageTokens) {
+      const uint32_t kb = ring_s + s * C::SLOT, vb = kb + C::HALF;
+      if (newest && ps + tw <= pos && pos < ps + tw + 16) {
         // the newest row (its copy may predate the cache write)
         const int rr = pos - ps;
         if (lane < HD / 8) {
@@ -653,78 +677,74 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
-      // S = Q K^T over the page: 8 tiles of 8 tokens
-      float sc[8][4];
+      if (tw < ntok) {
+        // S = Q K^T over the warp's 16 tokens: 2 tiles of 8
+        float sc[2][4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+        for (int j = 0; j < 2; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks) {
-#pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
+        for (int ks = 0; ks < HD / 16; ++ks) {
           uint32_t bb[4];
-          const int tok = jp * 16 + (lane >> 4) * 8 + (lane & 7);
+          const int tok = tw + (lane >> 4) * 8 + (lane & 7);
           const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
           ldsm_x4(bb, sw_addr(kb, tok, dim));
-          mma16816(sc[2 * jp], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[0], bb[1]);
-          mma16816(sc[2 * jp + 1], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[2], bb[3]);
+          mma16816(sc[0], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[0], bb[1]);
+          mma16816(sc[1], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[2], bb[3]);
         }
-      }
-      // hi + lo rows -> the head's scores (tokens 8j + 2tq, +1)
+        // hi + lo rows -> the head's scores (tokens tw + 8j + 2tq, +1)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (ROWS8) {
-          sc[j][0] += sc[j][2];
-          sc[j][1] += sc[j][3];
-        } else {
-          sc[j][0] += __shfl_xor_sync(0xFFFFFFFFu, sc[j][0], 16);
-          sc[j][1] += __shfl_xor_sync(0xFFFFFFFFu, sc[j][1], 16);
+        for (int j = 0; j < 2; ++j) {
+          if (ROWS8) {
+            sc[j][0] += sc[j][2];
+            sc[j][1] += sc[j][3];
+          } else {
+            sc[j][0] += __shfl_xor_sync(0xFFFFFFFFu, sc[j][0], 16);
+            sc[j][1] += __shfl_xor_sync(0xFFFFFFFFu, sc[j][1], 16);
+          }
         }
-      }
-      // online softmax on the head's row
-      float mx = -INFINITY;
+        // online softmax on the head's row
+        float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int t = 8 * j + 2 * tq;
-        if (t >= ntok) sc[j][0] = -INFINITY;
-        if (t + 1 >= ntok) sc[j][1] = -INFINITY;
-        mx = fmaxf(mx, fmaxf(sc[j][0], sc[j][1]));
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float f = expf(m_run - m_new);   // 0 on the first page (m_run = -inf)
-      float ps_sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sc[j][0] = expf(sc[j][0] - m_new);
-        sc[j][1] = expf(sc[j][1] - m_new);
-        ps_sum += sc[j][0] + sc[j][1];
-      }
-      ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 1);
-      ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 2);
-      l_run = l_run * f + ps_sum;
-      m_run = m_new;
-#pragma unroll
-      for (int n = 0; n < HD / 8; ++n) {
-        o[n][0] *= f;
-        o[n][1] *= f;
-        if (ROWS8) {
-          o[n][2] *= f;
-          o[n][3] *= f;
+        for (int j = 0; j < 2; ++j) {
+          const int t = tw + 8 * j + 2 * tq;
+          if (t >= ntok) sc[j][0] = -INFINITY;
+          if (t + 1 >= ntok) sc[j][1] = -INFINITY;
+          mx = fmaxf(mx, fmaxf(sc[j][0], sc[j][1]));
         }
-      }
-      // O += P V: 4 steps of 16 tokens
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);   // finite: token tw is valid
+        const float f = expf(m_run - m_new);     // 0 while m_run = -inf
+        float ps_sum = 0.f;
 #pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
+        for (int j = 0; j < 2; ++j) {
+          sc[j][0] = expf(sc[j][0] - m_new);
+          sc[j][1] = expf(sc[j][1] - m_new);
+          ps_sum += sc[j][0] + sc[j][1];
+        }
+        ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 1);
+        ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 2);
+        l_run = l_run * f + ps_sum;
+        m_run = m_new;
+#pragma unroll
+        for (int n = 0; n < HD / 8; ++n) {
+          o[n][0] *= f;
+          o[n][1] *= f;
+          if (ROWS8) {
+            o[n][2] *= f;
+            o[n][3] *= f;
+          }
+        }
+        // O += P V over the 16 tokens
         uint32_t ph0, pl0, ph2, pl2;
-        split2(sc[2 * kt][0], sc[2 * kt][1], ph0, pl0);
-        split2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], ph2, pl2);
+        split2(sc[0][0], sc[0][1], ph0, pl0);
+        split2(sc[1][0], sc[1][1], ph2, pl2);
         const uint32_t a0 = lo_row ? pl0 : ph0, a2 = lo_row ? pl2 : ph2;
         const uint32_t a1 = ROWS8 ? pl0 : 0u, a3 = ROWS8 ? pl2 : 0u;
 #pragma unroll
         for (int np = 0; np < HD / 16; ++np) {
           uint32_t bb[4];
-          const int tok = kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int tok = tw + ((lane >> 3) & 1) * 8 + (lane & 7);
           const int dim = np * 16 + (lane >> 4) * 8;
           ldsm_x4_t(bb, sw_addr(vb, tok, dim));
           mma16816(o[2 * np], a0, a1, a2, a3, bb[0], bb[1]);
@@ -732,10 +752,7 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) {   // both slots are free (reads done: their values were used above)
-        mbar_arrive(&sm.empty[sk]);
-        mbar_arrive(&sm.empty[sv]);
-      }
+      if (lane == 0) mbar_arrive(&sm.empty[s]);   // this warp's reads of the slot are done
     }
 
     // hand (m, l, O) to the finalize warp
@@ -749,24 +766,25 @@ __global__ void __launch_bounds__(kAmThreads, 1)
         o[n][1] += __shfl_xor_sync(0xFFFFFFFFu, o[n][1], 16);
       }
     }
-    if (k >= 1 && !am_wait(&sm.cempty, (k - 1) & 1, abort_flag, d)) {
+    // (state buffer b was last used by unit k - 2)
+    if (k >= 2 && !am_wait(&sm.cempty[b], ((k >> 1) - 1) & 1, abort_flag, d)) {
       *abort_flag = 1;
       return;
     }
     if (writer) {
       if (tq == 0) {
-        sm.cm[warp][head] = m_run;
-        sm.cl[warp][head] = l_run;
+        sm.cm[b][warp][head] = m_run;
+        sm.cl[b][warp][head] = l_run;
       }
 #pragma unroll
       for (int n = 0; n < HD / 8; ++n) {
-        sm.co[warp][head][8 * n + 2 * tq] = o[n][0];
-        sm.co[warp][head][8 * n + 2 * tq + 1] = o[n][1];
+        sm.co[b][warp][head][8 * n + 2 * tq] = o[n][0];
+        sm.co[b][warp][head][8 * n + 2 * tq + 1] = o[n][1];
       }
     }
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(&sm.cfull);
+      mbar_arrive(&sm.cfull[b]);
       mbar_arrive(&sm.uempty[b]);
     }
   }
