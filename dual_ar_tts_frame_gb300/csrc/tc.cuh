@@ -83,6 +83,17 @@ DEVI void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// The same without the wait: registers are valid after tmem_wait_ld().
+DEVI void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+DEVI void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // ---- tiled tensor copies (TMA) -----------------------------------------------------
 // 2-D tile global -> shared, completing on an mbarrier.  x (innermost, in
 // elements) must keep x * element size a multiple of 16 bytes.
@@ -99,6 +110,23 @@ DEVI void tma_load_2d_hint(void* dst, const void* tmap, int x, int y, uint64_t* 
       "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// 3-D tile shared -> global (bulk async group); the source must stay
+// untouched until the group has been waited for.
+DEVI void tma_store_3d(const void* tmap, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+               "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+DEVI void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until this thread's committed bulk stores have completed (written).
+DEVI void tma_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Request a 2-D tile of the tensor into L2 only (no completion to wait for).
+DEVI void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+               : "memory");
 }
 
 }  // namespace dualar

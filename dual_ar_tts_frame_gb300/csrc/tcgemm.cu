@@ -44,6 +44,7 @@ namespace dualar {
 constexpr int kTcThreads = 192;     // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: read-back
 constexpr int kTcWTile = 128 * 64 * 2;   // one 128-row x 64-K weight tile (bytes)
 constexpr size_t kTcSmemBudget = 200 * 1024;
+constexpr int kTcPrefetchChunks = 8;   // weight chunks (32 KB each) requested into L2 ahead of the ring
 
 __host__ __device__ constexpr int tc_stage_bytes(int nbp) { return 2 * kTcWTile + 2 * nbp * 128; }
 __host__ __device__ constexpr int tc_stages(int nbp) {
@@ -63,6 +64,7 @@ struct TcArgs {
   int kc_per_slice;    // 64-wide K chunks per split-K slice
   float* part;         // [slices][nb][ldp] partial sums
   int ldp;             // n0 + n1
+  int tma_store;       // the partial tile goes out through the tensor map tp (else plain stores)
   uint32_t* err;
   uint64_t wait_limit_ns;
 };
@@ -71,7 +73,7 @@ template <int NBP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tw0, const __grid_constant__ CUtensorMap tw1,
                    const __grid_constant__ CUtensorMap txh, const __grid_constant__ CUtensorMap txl,
-                   const TcArgs a) {
+                   const __grid_constant__ CUtensorMap tp, const TcArgs a) {
   constexpr int S = tc_stages(NBP);
   constexpr int SB = tc_stage_bytes(NBP);
   constexpr int XT = NBP * 128;                                   // one activation tile (bytes)
@@ -133,6 +135,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive_expect_tx(&full[i], static_cast<uint32_t>(SB));
         load_w(i);
       }
+      // and the next kTcPrefetchChunks chunks' weights into L2, so that the
+      // memory keeps streaming while the kernels before this one finish
+      for (int i = pre; i < nch && i < pre + kTcPrefetchChunks; ++i) {
+        const int kx = (c0 + i) * 64;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int r0 = tile * 256 + t * 128;
+          if (r0 < a.n0) tma_prefetch_l2_2d(&tw0, kx, r0);
+          else tma_prefetch_l2_2d(&tw1, kx, r0 - a.n0);
+        }
+      }
       pdl_wait();
       pdl_launch();
       for (int i = 0; i < pre; ++i) load_x(i);
@@ -190,21 +203,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;
     const bool accd = mbar_wait(&accf[0], 0, a.err, a.wait_limit_ns);
     if (!accd && lane == 0) raise_error(a.err, DEV_ERR_TC_WAIT | (1u << 7));
-    if (accd) {
+    if (accd && a.tma_store) {
+      // this warp's 32 weight rows of each 128-row half, for all NBP batch
+      // rows, are staged in the (now idle) stage ring as [NBP][32] blocks
+      // and leave in two tensor stores (no other warp involved)
       tc_fence_after();
+      constexpr int CW = NBP < 64 ? NBP : 64;
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        float* blk = reinterpret_cast<float*>(smem) + ((warp - 2) * 2 + t) * (NBP * 32);
+#pragma unroll 1
+        for (int c0 = 0; c0 < NBP; c0 += CW) {
+          uint32_t v[CW / 16][16];
+#pragma unroll
+          for (int c = 0; c < CW / 16; ++c)
+            tmem_ld16_async(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(t * NBP + c0 + c * 16),
+                            v[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < CW / 16; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) blk[(c0 + c * 16 + j) * 32 + lane] = __uint_as_float(v[c][j]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) tma_store_3d(&tp, blk, tile * 256 + t * 128 + q * 32, 0, slice);
+      }
+      if (lane == 0) {
+        tma_store_commit();
+        tma_store_wait();
+      }
+      __syncwarp();
+    } else if (accd) {
+      tc_fence_after();
+      // up to 64 accumulator columns per round: their loads issued together,
+      // one wait, then the stores (lane = weight row: 128-byte rows per store)
+      constexpr int CW = NBP < 64 ? NBP : 64;
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
         const int n = tile * 256 + t * 128 + q * 32 + lane;   // weight row of this lane
 #pragma unroll 1
-        for (int c = 0; c < NBP / 16; ++c) {
-          float v[16];
-          tmem_ld16(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(t * NBP + c * 16), v);
-          if (n < a.ldp) {
+        for (int c0 = 0; c0 < NBP; c0 += CW) {
+          uint32_t v[CW / 16][16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int m = c * 16 + j;
-              if (m < a.nb) a.part[(static_cast<size_t>(slice) * a.nb + m) * a.ldp + n] = v[j];
-            }
+          for (int c = 0; c < CW / 16; ++c)
+            tmem_ld16_async(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(t * NBP + c0 + c * 16),
+                            v[c]);
+          tmem_wait_ld();
+          if (n < a.ldp) {
+            float* dst = a.part + (static_cast<size_t>(slice) * a.nb + c0) * a.ldp + n;
+#pragma unroll
+            for (int c = 0; c < CW / 16; ++c)
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + c * 16 + j < a.nb) dst[static_cast<size_t>(c * 16 + j) * a.ldp] = __uint_as_float(v[c][j]);
           }
         }
       }
@@ -227,8 +279,8 @@ constexpr int kSplitVec = 3;   // float4 per thread
 __global__ void __launch_bounds__(kSplitThreads, 1)
     tc_split_kernel(const float* x, int ldx, int K, const uint16_t* norm_w, float eps, uint16_t* xh, uint16_t* xl,
                     int ldxh, float* save_x, const int32_t* save_map, int lds) {
+  pdl_launch();   // the next projection may start fetching its weights
   pdl_wait();
-  pdl_launch();
   const int m = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * ldx);
   const int KV = K >> 2;
@@ -285,8 +337,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     tc_reduce_norm_kernel(const float* part, int slices, int nb, int ldp, int K, const float* base, int ldb,
                           float* out, int ldo, const uint16_t* norm_w, float eps, uint16_t* xh, uint16_t* xl,
                           int ldxh, float* save_x, const int32_t* save_map, int lds) {
+  pdl_launch();   // the next projection may start fetching its weights
   pdl_wait();
-  pdl_launch();
   const int m = blockIdx.x;
   const int KV = K >> 2;
   const size_t stride = static_cast<size_t>(nb) * ldp;
@@ -354,8 +406,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
                                  int ldo, const float* base, int ldb, const int32_t* out_map, int n0, uint16_t* xh,
                                  uint16_t* xl, int ldxh) {
+  pdl_launch();   // the next projection may start fetching its weights
   pdl_wait();
-  pdl_launch();
   const int nq = n_out >> 2;   // n_out % 4 == 0 (host)
   const size_t total = static_cast<size_t>(nb) * nq;
   // the slices' partials, four loads in flight, added in slice order
@@ -416,8 +468,8 @@ __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp,
 __global__ void tc_reduce_scalar_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode,
                                         float* out, int ldo, const float* base, int ldb, const int32_t* out_map,
                                         int n0) {
+  pdl_launch();   // the next projection may start fetching its weights
   pdl_wait();
-  pdl_launch();
   const size_t total = static_cast<size_t>(nb) * n_out;
   for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -493,6 +545,35 @@ static bool cached_map(CUtensorMap* out, const void* base, int K, int rows, int 
   return true;
 }
 
+// fp32 [slices][nb][ldp] (rows of ldp floats), boxes of 32 x box_nb x 1;
+// built once per argument set and kept.
+static bool part_map(CUtensorMap* out, const float* base, int ldp, int nb, int slices, int box_nb) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int, int>, CUtensorMap> cache;
+  std::lock_guard<std::mutex> g(mu);
+  const auto key = std::make_tuple(static_cast<const void*>(base), ldp, nb, slices, box_nb);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return true;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(ldp), static_cast<cuuint64_t>(nb),
+                              static_cast<cuuint64_t>(slices)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldp) * 4, static_cast<cuuint64_t>(ldp) * nb * 4};
+  const cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_nb), 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  CUtensorMap m;
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache.emplace(key, m);
+  *out = m;
+  return true;
+}
+
 bool tc_bf16_map(CUtensorMap* out, const void* base, int K, int rows, int ld, int box_rows) {
   return cached_map(out, base, K, rows, ld, box_rows);
 }
@@ -509,7 +590,8 @@ bool tc_eligible(const GemvArgs& a, int ldx) {
 
 template <int NBP>
 static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& xh,
-                                   const CUtensorMap& xl, const TcArgs& t, dim3 grid, cudaStream_t st) {
+                                   const CUtensorMap& xl, const CUtensorMap& tp, const TcArgs& t, dim3 grid,
+                                   cudaStream_t st) {
   static bool configured = false;
   const size_t smem = tc_smem_bytes(NBP);
   if (!configured) {
@@ -518,7 +600,7 @@ static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(tc_gemm_kernel<NBP>, grid, dim3(kTcThreads), smem, st, w0, w1, xh, xl, t);
+  return launch_pdl(tc_gemm_kernel<NBP>, grid, dim3(kTcThreads), smem, st, w0, w1, xh, xl, tp, t);
 }
 
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
@@ -548,13 +630,17 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
     if (e != cudaSuccess) return e;
     if (launches) *launches += 1;
   }
-  TcArgs t{a.n0, a.n1, a.K, a.nb, kcps, b.part, n_rows, a.err, a.wait_limit_ns};
+  // the partial sums as a [slices][nb][ldp] fp32 tensor, boxes of 32 x NBP x 1
+  CUtensorMap mp;
+  const bool tstore = n_rows % 4 == 0 && part_map(&mp, b.part, n_rows, a.nb, slices, nbp);
+  if (!tstore) mp = m0;   // unused
+  TcArgs t{a.n0, a.n1, a.K, a.nb, kcps, b.part, n_rows, tstore ? 1 : 0, a.err, a.wait_limit_ns};
   const dim3 grid(tiles, slices);
   switch (nbp) {
-    case 16: e = launch_gemm_nbp<16>(m0, m1, mh, ml, t, grid, st); break;
-    case 32: e = launch_gemm_nbp<32>(m0, m1, mh, ml, t, grid, st); break;
-    case 64: e = launch_gemm_nbp<64>(m0, m1, mh, ml, t, grid, st); break;
-    default: e = launch_gemm_nbp<128>(m0, m1, mh, ml, t, grid, st); break;
+    case 16: e = launch_gemm_nbp<16>(m0, m1, mh, ml, mp, t, grid, st); break;
+    case 32: e = launch_gemm_nbp<32>(m0, m1, mh, ml, mp, t, grid, st); break;
+    case 64: e = launch_gemm_nbp<64>(m0, m1, mh, ml, mp, t, grid, st); break;
+    default: e = launch_gemm_nbp<128>(m0, m1, mh, ml, mp, t, grid, st); break;
   }
   if (e != cudaSuccess) return e;
   const int n_out = a.mode == GEMV_SWIGLU ? a.n0 : n_rows;
