@@ -209,6 +209,11 @@ DEVI uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+DEVI uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 // Named barrier over a subset of the block's warps (the consumer warps).
 DEVI void named_barrier(uint32_t id, uint32_t nthreads) {

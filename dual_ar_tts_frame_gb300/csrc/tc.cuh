@@ -119,6 +119,12 @@ DEVI void tma_store_3d(const void* tmap, const void* src, int x, int y, int z) {
                "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+DEVI void tma_store_3d_hint(const void* tmap, const void* src, int x, int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(tmap),
+      "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
 DEVI void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until this thread's committed bulk stores have completed (written).
 DEVI void tma_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -126,6 +132,12 @@ DEVI void tma_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "mem
 // Request a 2-D tile of the tensor into L2 only (no completion to wait for).
 DEVI void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+               : "memory");
+}
+
+DEVI void tma_prefetch_l2_2d_hint(const void* tmap, int x, int y, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(tmap),
+               "r"(x), "r"(y), "l"(policy)
                : "memory");
 }
 

@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int r0 = tile * 256 + t * 128;
-          if (r0 < a.n0) tma_prefetch_l2_2d(&tw0, kx, r0);
-          else tma_prefetch_l2_2d(&tw1, kx, r0 - a.n0);
+          if (r0 < a.n0) tma_prefetch_l2_2d_hint(&tw0, kx, r0, pol);
+          else tma_prefetch_l2_2d_hint(&tw1, kx, r0 - a.n0, pol);
         }
       }
       pdl_wait();
@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) tma_store_3d(&tp, blk, tile * 256 + t * 128 + q * 32, 0, slice);
+        // (kept in L2 until the reduce reads them: the weight streams are evict-first)
+        if (lane == 0) tma_store_3d_hint(&tp, blk, tile * 256 + t * 128 + q * 32, 0, slice, policy_evict_last());
       }
       if (lane == 0) {
         tma_store_commit();
@@ -330,6 +331,23 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   }
 }
 
+// Split-K sum at offset off of the partials: every slice's float4 in
+// flight at once (slices <= MAXS), added in slice order.
+template <int MAXS>
+DEVI float4 tc_slice_sum(const float* part, int slices, size_t stride, size_t off) {
+  float4 t[MAXS];
+#pragma unroll
+  for (int k = 0; k < MAXS; ++k)
+    if (k < slices) t[k] = *reinterpret_cast<const float4*>(part + off + k * stride);
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < MAXS; ++k)
+    if (k < slices) {
+      y.x += t[k].x; y.y += t[k].y; y.z += t[k].z; y.w += t[k].w;
+    }
+  return y;
+}
+
 // Residual add of the K-slice partials (slice order, as tc_reduce_kernel),
 // then the split of the result as tc_split_kernel does it (the same thread
 // mapping, so the same sums): out = base + sum, x' = RMSNorm(out) * g.
@@ -403,6 +421,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
 // Sum of the K-slice partials (slice order) and the epilogue, 4 columns per
 // thread (all row strides multiples of 4 floats).
+template <int MAXS>
 __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp, int n_out, int mode, float* out,
                                  int ldo, const float* base, int ldb, const int32_t* out_map, int n0, uint16_t* xh,
                                  uint16_t* xl, int ldxh) {
@@ -410,25 +429,8 @@ __global__ void tc_reduce_kernel(const float* part, int slices, int nb, int ldp,
   pdl_wait();
   const int nq = n_out >> 2;   // n_out % 4 == 0 (host)
   const size_t total = static_cast<size_t>(nb) * nq;
-  // the slices' partials, four loads in flight, added in slice order
-  auto sum = [&](const float* p0, size_t stride) {
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 8 <= slices; s += 8) {
-      float4 q[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) q[k] = *reinterpret_cast<const float4*>(p0 + (s + k) * stride);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        y.x += q[k].x; y.y += q[k].y; y.z += q[k].z; y.w += q[k].w;
-      }
-    }
-    for (; s < slices; ++s) {
-      const float4 q = *reinterpret_cast<const float4*>(p0 + s * stride);
-      y.x += q.x; y.y += q.y; y.z += q.z; y.w += q.w;
-    }
-    return y;
-  };
+  // the slices' partials, all loads in flight, added in slice order
+  auto sum = [&](const float* p0, size_t stride) { return tc_slice_sum<MAXS>(p0, slices, stride, 0); };
   for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(e / nq), n = 4 * static_cast<int>(e % nq);
@@ -663,7 +665,7 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
   int rgrid = static_cast<int>((total + 255) / 256);
   rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
   if (vec)
-    e = launch_pdl(tc_reduce_kernel, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), slices, a.nb,
+    e = launch_pdl(slices <= 4 ? tc_reduce_kernel<4> : slices <= 8 ? tc_reduce_kernel<8> : tc_reduce_kernel<16>, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), slices, a.nb,
                    n_rows, n_out, a.mode, a.out, a.ldo, a.base, a.ldb, a.out_map, a.n0,
                    split_out ? b.xh : static_cast<uint16_t*>(nullptr), split_out ? b.xl : static_cast<uint16_t*>(nullptr),
                    b.ldx);
@@ -683,7 +685,7 @@ cudaError_t launch_tc_pending(const TcPending& p, const TcBuffers& b, int n_sm, 
   const size_t total = static_cast<size_t>(p.nb) * (p.n_out / 4);
   int rgrid = static_cast<int>((total + 255) / 256);
   rgrid = rgrid > 8 * n_sm ? 8 * n_sm : rgrid;
-  return launch_pdl(tc_reduce_kernel, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), p.slices,
+  return launch_pdl(p.slices <= 4 ? tc_reduce_kernel<4> : p.slices <= 8 ? tc_reduce_kernel<8> : tc_reduce_kernel<16>, dim3(rgrid), dim3(256), 0, st, static_cast<const float*>(b.part), p.slices,
                     p.nb, p.ldp, p.n_out, static_cast<int>(GEMV_ADD), p.out, p.ldo, p.base, p.ldb,
                     static_cast<const int32_t*>(nullptr), 0, static_cast<uint16_t*>(nullptr),
                     static_cast<uint16_t*>(nullptr), b.ldx);
