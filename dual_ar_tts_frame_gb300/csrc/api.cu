@@ -392,19 +392,34 @@ int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast
           const float* xin, float* hres, int fast_pos, int units, int chunk, bool fuse_append) {
   const dualar_config& c = h->cfg;
   const DevPtrs& d = h->d;
+  // decode: the attention writes the bf16 halves of its output for the o
+  // projection (no split kernel between them)
   TRY(run_gemv(h, args_qkv(h, lw, nrows, xin)));
+  AttnHalves hv{nullptr, nullptr, 0};
+  const GemvArgs ao = args_o(h, lw, nrows, xin, hres);
+  const bool o_halves = (fast || fuse_append) && h->use_tc && !h->profiling && tc_eligible(ao, h->tc.ldx);
+  if (o_halves) hv = AttnHalves{h->tc.xh, h->tc.xl, h->tc.ldx};
+  bool halves_written = false;
   const bool qk = fast ? c.fast_qk_norm : c.slow_qk_norm;
   const uint16_t* qn = qk ? U16(lw.q_norm) : nullptr;
   const uint16_t* kn = qk ? U16(lw.k_norm) : nullptr;
   if (fast) {
-    LAUNCH(h, launch_attn_fast(d, nrows, layer, fast_pos, qn, kn, h->stream));
+    LAUNCH(h, launch_attn_fast(d, nrows, layer, fast_pos, qn, kn, h->stream, hv));
+    halves_written = o_halves;
   } else if (fuse_append) {
-    LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, true, qn, kn, h->stream));
+    bool mma = false;
+    LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, true, qn, kn, h->stream, &mma, hv));
+    halves_written = o_halves && mma;   // (the SIMT kernel writes no halves)
   } else {
     LAUNCH(h, launch_append(d, nrows, layer, false, 0, qn, kn, h->stream));
     LAUNCH(h, launch_attn_paged(d, nrows, layer, units, chunk, h->n_sm, false, nullptr, nullptr, h->stream));
   }
-  TRY(run_gemv(h, args_o(h, lw, nrows, xin, hres)));
+  if (halves_written) {
+    h->tc_ready_x = ao.x;
+    h->tc_ready_k = ao.K;
+    h->tc_ready_nb = ao.nb;
+  }
+  TRY(run_gemv(h, ao));
   TRY(run_gemv(h, args_gateup(h, lw, nrows, hres)));
   return run_gemv(h, args_down(h, lw, nrows, hres));
 }

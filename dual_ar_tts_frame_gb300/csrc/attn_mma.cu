@@ -237,7 +237,7 @@ DEVI void am_norm_rope(float (&v)[EPL], const float (&nw)[EPL], bool norm, float
 template <int HD, int G>
 __global__ void __launch_bounds__(kAmThreads, 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tkv, const DevPtrs d, int nrows, int layer, int total_units,
-                    int chunk_tokens, int fuse, const uint16_t* q_norm, const uint16_t* k_norm) {
+                    int chunk_tokens, int fuse, const uint16_t* q_norm, const uint16_t* k_norm, const AttnHalves hv) {
   using C = AmCfg<HD, G>;
   using Desc = AmUnitDesc<HD, G>;
   constexpr int NB = C::NBUF;
@@ -539,7 +539,9 @@ __global__ void __launch_bounds__(kAmThreads, 1)
 #pragma unroll
         for (int w = 0; w < kAmWarps; ++w) Os += sm.co[b][w][h][dd] * fz.fw[w][h];
         if (nch == 1) {
-          d.attn[attn_off + h * HD + dd] = Os / fz.ls[h];
+          const float o1[1] = {Os / fz.ls[h]};
+          d.attn[attn_off + h * HD + dd] = o1[0];
+          if (hv.xh != nullptr) attn_halves<1>(hv, r, (g * G + h) * HD + dd, o1);
         } else {
           pw[h * (HD + 2) + dd] = Os;
           if (dd == 0) {
@@ -604,9 +606,14 @@ __global__ void __launch_bounds__(kAmThreads, 1)
             }
           }
 #pragma unroll
-          for (int h = 0; h < G; ++h)
+          for (int h = 0; h < G; ++h) {
 #pragma unroll
-            for (int j = 0; j < EPLF; ++j) d.attn[attn_off + h * HD + lane * EPLF + j] = os[h][j] / fz.ls[h];
+            for (int j = 0; j < EPLF; ++j) {
+              os[h][j] = os[h][j] / fz.ls[h];
+              d.attn[attn_off + h * HD + lane * EPLF + j] = os[h][j];
+            }
+            if (hv.xh != nullptr) attn_halves<EPLF>(hv, r, (g * G + h) * HD + lane * EPLF, os[h]);
+          }
         }
       }
       __syncwarp();
@@ -792,7 +799,8 @@ __global__ void __launch_bounds__(kAmThreads, 1)
 
 template <int HD, int G>
 static cudaError_t am_launch(const CUtensorMap& m, const DevPtrs& d, int nrows, int layer, int units, int chunk,
-                             int grid, int fuse, const uint16_t* qn, const uint16_t* kn, cudaStream_t st) {
+                             int grid, int fuse, const uint16_t* qn, const uint16_t* kn, cudaStream_t st,
+                             AttnHalves hv) {
   static bool configured = false;
   const size_t smem = am_smem_bytes<HD, G>();
   if (!configured) {
@@ -802,24 +810,24 @@ static cudaError_t am_launch(const CUtensorMap& m, const DevPtrs& d, int nrows, 
     configured = true;
   }
   return launch_pdl(attn_mma_kernel<HD, G>, dim3(grid), dim3(kAmThreads), smem, st, m, d, nrows, layer, units, chunk,
-                    fuse, qn, kn);
+                    fuse, qn, kn, hv);
 }
 
 template <int HD>
 static cudaError_t am_hd(const CUtensorMap& m, const DevPtrs& d, int nrows, int layer, int units, int chunk, int grid,
-                         int fuse, const uint16_t* qn, const uint16_t* kn, cudaStream_t st) {
+                         int fuse, const uint16_t* qn, const uint16_t* kn, cudaStream_t st, AttnHalves hv) {
   switch (d.Hq / d.Hkv) {
-    case 1: return am_launch<HD, 1>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
-    case 2: return am_launch<HD, 2>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
-    case 4: return am_launch<HD, 4>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
-    case 8: return am_launch<HD, 8>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st);
+    case 1: return am_launch<HD, 1>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st, hv);
+    case 2: return am_launch<HD, 2>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st, hv);
+    case 4: return am_launch<HD, 4>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st, hv);
+    case 8: return am_launch<HD, 8>(m, d, nrows, layer, units, chunk, grid, fuse, qn, kn, st, hv);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_attn_mma(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens, int n_sm,
                             bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st,
-                            bool* used) {
+                            bool* used, AttnHalves hv) {
   *used = false;
   if (nrows < kAttnMmaMinRows || total_units <= 0 || !tc_available()) return cudaSuccess;
   if ((d.hd != 64 && d.hd != 128) || d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0 ||
@@ -831,8 +839,8 @@ cudaError_t launch_attn_mma(const DevPtrs& d, int nrows, int layer, int total_un
   if (!tc_bf16_map(&m, d.kv_pool, d.hd, static_cast<int>(rows), d.hd, 64)) return cudaSuccess;
   const int grid = total_units < n_sm ? total_units : n_sm;
   const int f = fuse_append ? 1 : 0;
-  cudaError_t e = d.hd == 128 ? am_hd<128>(m, d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st)
-                              : am_hd<64>(m, d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st);
+  cudaError_t e = d.hd == 128 ? am_hd<128>(m, d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st, hv)
+                              : am_hd<64>(m, d, nrows, layer, total_units, chunk_tokens, grid, f, q_norm, k_norm, st, hv);
   if (e == cudaSuccess) *used = true;
   return e;
 }

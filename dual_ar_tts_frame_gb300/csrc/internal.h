@@ -174,6 +174,14 @@ struct SampIO {
   const uint16_t* fast_emb;
 };
 
+// Per-op decode path: where the attention also writes the bf16 halves of its
+// output for the o projection ([rows][ld]; xh null: nowhere).
+struct AttnHalves {
+  uint16_t* xh;
+  uint16_t* xl;
+  int ld;
+};
+
 // ---- launchers (kernels.cu) -------------------------------------------------
 cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t* tok_emb,
                          cudaStream_t st);
@@ -182,15 +190,17 @@ cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int
                           const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st);
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,
                               int chunk_tokens, int n_sm, bool fuse_append, const uint16_t* q_norm,
-                              const uint16_t* k_norm, cudaStream_t st);
+                              const uint16_t* k_norm, cudaStream_t st, bool* mma_used = nullptr,
+                              AttnHalves hv = AttnHalves{nullptr, nullptr, 0});
 // Tensor-core variant for launches of >= kAttnMmaMinRows rows (attn_mma.cu);
 // *used is false (nothing launched) when the shape or the driver rules it out.
 constexpr int kAttnMmaMinRows = 3;
 cudaError_t launch_attn_mma(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens, int n_sm,
                             bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st,
-                            bool* used);
+                            bool* used,
+                            AttnHalves hv = AttnHalves{nullptr, nullptr, 0});
 cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* q_norm,
-                             const uint16_t* k_norm, cudaStream_t st);
+                             const uint16_t* k_norm, cudaStream_t st, AttnHalves hv = AttnHalves{nullptr, nullptr, 0});
 cudaError_t launch_sample_q0(const DevPtrs& d, int nrows, const float* uniforms, int ldu,
                              const SamplingParams& sp, const int32_t* forced, int ldf,
                              int32_t* codes_out, int32_t* status_out, float* slow_logits_out,

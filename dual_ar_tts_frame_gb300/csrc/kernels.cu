@@ -422,7 +422,8 @@ static cudaError_t attn_paged_hd(const DevPtrs& d, int nrows, int layer, int uni
 
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,
                               int chunk_tokens, int n_sm, bool fuse_append, const uint16_t* q_norm,
-                              const uint16_t* k_norm, cudaStream_t st) {
+                              const uint16_t* k_norm, cudaStream_t st, bool* mma_used, AttnHalves hv) {
+  if (mma_used) *mma_used = false;
   if (nrows <= 0 || total_units <= 0) return cudaSuccess;
   if (d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0) return cudaErrorInvalidValue;
   {
@@ -430,7 +431,8 @@ cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_
     // device code as the persistent frame kernel (bit-identical paths)
     bool used = false;
     const cudaError_t e = launch_attn_mma(d, nrows, layer, total_units, chunk_tokens, n_sm, fuse_append, q_norm,
-                                          k_norm, st, &used);
+                                          k_norm, st, &used, hv);
+    if (mma_used) *mma_used = used;
     if (e != cudaSuccess || used) return e;
   }
   const int grid = total_units < 4 * n_sm ? total_units : 4 * n_sm;
@@ -442,34 +444,34 @@ cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_
 
 template <int EPL, int G>
 __global__ void attn_fast_kernel(DevPtrs d, int layer, int pos, const uint16_t* q_norm,
-                                 const uint16_t* k_norm) {
+                                 const uint16_t* k_norm, AttnHalves hv) {
   pdl_wait();
   pdl_launch();
   constexpr int NT = 32 * (G + 1 > 2 ? G + 1 : 2);
   __shared__ FastAttnSmem<EPL * 32> sm;
-  attn_fast_unit<EPL, G, NT>(d, blockIdx.x, layer, pos, q_norm, k_norm, sm);
+  attn_fast_unit<EPL, G, NT, true>(d, blockIdx.x, layer, pos, q_norm, k_norm, sm, OpTags{0u, 0u}, nullptr, hv);
 }
 
 template <int EPL>
 static cudaError_t attn_fast_epl(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* qn,
-                                 const uint16_t* kn, cudaStream_t st) {
+                                 const uint16_t* kn, cudaStream_t st, AttnHalves hv) {
   const int G = d.Hq / d.Hkv;
   const int grid = nrows * d.Hkv;
   switch (G) {
-    case 1: return launch_pdl(attn_fast_kernel<EPL, 1>, dim3(grid), dim3(64), 0, st, d, layer, pos, qn, kn);
-    case 2: return launch_pdl(attn_fast_kernel<EPL, 2>, dim3(grid), dim3(96), 0, st, d, layer, pos, qn, kn);
-    case 4: return launch_pdl(attn_fast_kernel<EPL, 4>, dim3(grid), dim3(160), 0, st, d, layer, pos, qn, kn);
-    case 8: return launch_pdl(attn_fast_kernel<EPL, 8>, dim3(grid), dim3(288), 0, st, d, layer, pos, qn, kn);
+    case 1: return launch_pdl(attn_fast_kernel<EPL, 1>, dim3(grid), dim3(64), 0, st, d, layer, pos, qn, kn, hv);
+    case 2: return launch_pdl(attn_fast_kernel<EPL, 2>, dim3(grid), dim3(96), 0, st, d, layer, pos, qn, kn, hv);
+    case 4: return launch_pdl(attn_fast_kernel<EPL, 4>, dim3(grid), dim3(160), 0, st, d, layer, pos, qn, kn, hv);
+    case 8: return launch_pdl(attn_fast_kernel<EPL, 8>, dim3(grid), dim3(288), 0, st, d, layer, pos, qn, kn, hv);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_attn_fast(const DevPtrs& d, int nrows, int layer, int pos, const uint16_t* q_norm,
-                             const uint16_t* k_norm, cudaStream_t st) {
+                             const uint16_t* k_norm, cudaStream_t st, AttnHalves hv) {
   if (nrows <= 0) return cudaSuccess;
   if (pos < 0 || pos >= d.N || pos >= d.rope_len) return cudaErrorInvalidValue;
-  if (d.hd == 128) return attn_fast_epl<4>(d, nrows, layer, pos, q_norm, k_norm, st);
-  if (d.hd == 64) return attn_fast_epl<2>(d, nrows, layer, pos, q_norm, k_norm, st);
+  if (d.hd == 128) return attn_fast_epl<4>(d, nrows, layer, pos, q_norm, k_norm, st, hv);
+  if (d.hd == 64) return attn_fast_epl<2>(d, nrows, layer, pos, q_norm, k_norm, st, hv);
   return cudaErrorInvalidValue;
 }
 

@@ -53,6 +53,33 @@ DEVI void act_load(const float* plain, const uint64_t* tagged, size_t off, uint3
     for (int j = 0; j < EPL; ++j) v[j] = ldf(plain + off + j);
   }
 }
+// The bf16 halves (hi, lo = bf16(v - hi)) of EPL attention-output values at
+// row r, column col, for the o projection (per-op path).
+template <int EPL>
+DEVI void attn_halves(const AttnHalves& hv, int r, int col, const float (&v)[EPL]) {
+  uint16_t h[EPL], l[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    h[j] = f32_to_bf16bits(v[j]);
+    l[j] = f32_to_bf16bits(v[j] - bf16bits_to_f32(h[j]));
+  }
+  const size_t o = static_cast<size_t>(r) * hv.ld + col;
+  if constexpr (EPL % 2 == 0) {
+    // pairs in 32-bit words (col and ld even)
+#pragma unroll
+    for (int j = 0; j < EPL; j += 2) {
+      *reinterpret_cast<uint32_t*>(hv.xh + o + j) = static_cast<uint32_t>(h[j]) | (static_cast<uint32_t>(h[j + 1]) << 16);
+      *reinterpret_cast<uint32_t*>(hv.xl + o + j) = static_cast<uint32_t>(l[j]) | (static_cast<uint32_t>(l[j + 1]) << 16);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      hv.xh[o + j] = h[j];
+      hv.xl[o + j] = l[j];
+    }
+  }
+}
+
 DEVI void act_store(float* plain, uint64_t* tagged, size_t off, uint32_t tag, float v) {
   if (tag != 0u) tag_store(tagged + off, v, tag);
   else plain[off] = v;
@@ -501,10 +528,11 @@ struct FastAttnSmem {
   float ks[kMaxCodebooks][HD], vs[kMaxCodebooks][HD];
 };
 
-template <int EPL, int G, int NT>
+// HALVES (per-op path): also the bf16 halves of the output into hv.
+template <int EPL, int G, int NT, bool HALVES = false>
 DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const uint16_t* q_norm,
                          const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm, OpTags tg = OpTags{0u, 0u},
-                         float* res = nullptr) {
+                         float* res = nullptr, AttnHalves hv = AttnHalves{nullptr, nullptr, 0}) {
   // res (persistent frame kernel): this layer's K and V rows [2][N][HD], kept
   // in shared memory for the whole frame by the one CTA that runs this unit;
   // otherwise earlier positions come from the global fast cache
@@ -574,7 +602,11 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
     }
     const size_t dst = static_cast<size_t>(r) * hq * HD + h * HD;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) act_store(d.attn, d.attn_t, dst + lane * EPL + j, tg.out, o[j] / l);
+    for (int j = 0; j < EPL; ++j) {
+      o[j] = o[j] / l;
+      act_store(d.attn, d.attn_t, dst + lane * EPL + j, tg.out, o[j]);
+    }
+    if (HALVES && hv.xh != nullptr) attn_halves<EPL>(hv, r, h * HD + lane * EPL, o);
   }
   csync<NT>();   // shared buffers are reused by the next unit
 }
