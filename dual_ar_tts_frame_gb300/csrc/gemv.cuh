@@ -144,6 +144,27 @@ DEVI bool gemv_produce(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
   return true;
 }
 
+// This CTA's weight rows (contiguous per segment) requested into L2, in 32 KB
+// pieces (rows of 2 K bytes: 16-byte multiples).
+DEVI void gemv_prefetch_rows(const GemvArgs& a, const GemvGeo& g) {
+  auto range = [&](const uint16_t* base, int r0, int r1) {
+    if (r1 <= r0) return;
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(base + static_cast<size_t>(r0) * a.K);
+    const size_t bytes = static_cast<size_t>(r1 - r0) * a.K * 2;
+    for (size_t o = 0; o < bytes; o += 32768) {
+      const size_t n = bytes - o < 32768 ? bytes - o : 32768;
+      bulk_prefetch_l2(p + o, static_cast<uint32_t>(n));
+    }
+  };
+  if (g.swiglu) {
+    range(a.w0, g.v_begin, g.v_end);
+    range(a.w1, g.v_begin, g.v_end);
+  } else {
+    range(a.w0, g.v_begin, min(g.v_end, a.n0));
+    range(a.w1, max(g.v_begin, a.n0) - a.n0, g.v_end - a.n0);
+  }
+}
+
 // Waits (bounded) for every copy this producer may still have in flight, so
 // the CTA never exits with bulk copies writing into its shared memory.
 DEVI void gemv_drain(const GemvRing& ring, uint32_t t, uint64_t limit_ns) {

@@ -158,8 +158,6 @@ __host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
 
 template <int NB>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a, const int stages) {
-  pdl_wait();
-  pdl_launch();
   extern __shared__ __align__(128) unsigned char smem[];
   GemvRing ring;
   ring.full = reinterpret_cast<uint64_t*>(smem);
@@ -182,12 +180,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   const GemvGeo g = gemv_geo(a, blockIdx.x, gridDim.x);
   uint32_t t = 0;
   if (warp == kGemvConsumerWarps) {
+    // the weights are constant: this CTA's rows are requested into L2 and
+    // streamed into the ring while the previous kernel may still run (the
+    // consumers wait for it before reading x)
     if (lane == 0) {
+      gemv_prefetch_rows(a, g);
       gemv_produce(a, g, ring, t, policy_evict_first(), nullptr);
       gemv_drain(ring, t, a.wait_limit_ns);
     }
+    pdl_wait();
     return;
   }
+  pdl_wait();
+  pdl_launch();
   gemv_stage_x<NB>(a, g, xs, pro, blockIdx.x, false);
   gemv_consume<NB>(a, g, ring, t, xs, scr, pro);
 }
