@@ -334,13 +334,21 @@ def main():
     avg_us = 1000.0 * prof["total_ms"] / max(1, prof["launches"])
     kgbs = kbytes / (avg_us * 1e-6) / 1e9 if avg_us > 0 else None
     e2e = None
+    prefill = None
     if not args.no_e2e:
         # end to end through the public API: pinned host uniforms in, codes and
         # status out, the host reading each frame's result before the next
         eslots = [b + s for s in slots]
+        pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pe0.record(stream)
         for s in eslots:
             dec.prefill(s, prompt)
+        pe1.record(stream)
         dec.sync()
+        prefill = {"prompt_tokens": wl["prompt"], "ms_per_sequence": pe0.elapsed_time(pe1) / len(eslots),
+                   "note": "the prompt's prefill (chunks of up to 128 rows on the tensor cores), device-timed; "
+                           "the first audio frame follows one decode step later"}
+        prefill["tokens_per_s"] = wl["prompt"] / (prefill["ms_per_sequence"] / 1000.0)
         hu = torch.from_numpy(uni_all).pin_memory()
         du = torch.empty((b, cfg.n_codebooks + 1), dtype=torch.float32, device="cuda")
         hc = torch.empty((b, cfg.n_codebooks), dtype=torch.int32).pin_memory()
@@ -403,6 +411,7 @@ def main():
                          "launches": prof["launches"], "share_of_step": prof["total_ms"] / ms,
                          "peak_source": peak_src},
             "e2e": e2e,
+            "prefill": prefill,
             "gpu_launches": launches_per_frame * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
