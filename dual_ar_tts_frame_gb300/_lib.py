@@ -21,7 +21,8 @@ ERRORS = {
 
 # Every symbol include/dualar.h declares.
 EXPORTED = [
-    "dualar_create", "dualar_prefill", "dualar_decode_frame", "dualar_decode_frame_forced",
+    "dualar_create", "dualar_prefill", "dualar_prefill_append", "dualar_share_prefix",
+    "dualar_decode_frame", "dualar_decode_frame_forced",
     "dualar_decode_frame_noalloc",
     "dualar_release", "dualar_sync", "dualar_get_error", "dualar_destroy",
     "dualar_get_page_table", "dualar_get_rope_table", "dualar_read_state", "dualar_slot_length",
@@ -73,6 +74,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_create.argtypes = [ctypes.POINTER(dualar_config), ctypes.POINTER(dualar_weights), c_vp,
                                 ctypes.POINTER(H)]
     L.dualar_prefill.argtypes = [H, c_i32, ctypes.POINTER(c_i32), c_i32]
+    L.dualar_prefill_append.argtypes = [H, c_i32, ctypes.POINTER(c_i32), c_i32]
+    L.dualar_share_prefix.argtypes = [H, c_i32, c_i32, c_i32]
     L.dualar_decode_frame.argtypes = [H, c_i32, ctypes.POINTER(c_i32), c_vp,
                                       ctypes.POINTER(dualar_sampling), c_vp, c_vp]
     L.dualar_decode_frame_forced.argtypes = [H, c_i32, ctypes.POINTER(c_i32), c_vp,

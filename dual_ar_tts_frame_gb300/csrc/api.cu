@@ -33,6 +33,8 @@ struct dualar_handle {
   std::vector<int> length;               // next position per slot, -1 = empty
   std::vector<std::vector<int>> pages;   // pages per slot
   std::set<int> free_pages;
+  std::vector<int> page_refs;            // slots whose page table holds each page (shared prefixes)
+  std::vector<char> prefix_only;         // slot holds a shared prefix without its prompt's end
   std::string err;
   int launches = 0;
   // GEMV timing (dualar_profile)
@@ -72,6 +74,19 @@ void set_err(dualar_handle* h, const char* fmt, ...) {
   vsnprintf(buf, sizeof(buf), fmt, ap);
   va_end(ap);
   h->err = buf;
+}
+
+// The lowest free page, now held by one slot.
+int take_page(dualar_handle* h) {
+  const int pg = *h->free_pages.begin();
+  h->free_pages.erase(h->free_pages.begin());
+  h->page_refs[pg] = 1;
+  return pg;
+}
+
+// One slot fewer holds the page; the last one returns it to the pool.
+void drop_page(dualar_handle* h, int pg) {
+  if (--h->page_refs[pg] == 0) h->free_pages.insert(pg);
 }
 
 // Queues the deferred residual-add reduce, if any.
@@ -593,6 +608,10 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
       set_err(h, "decode: slot %d is empty", s);
       return DUALAR_ERR_SLOT_EMPTY;
     }
+    if (h->prefix_only[s]) {
+      set_err(h, "decode: slot %d holds a shared prefix; append the rest of its prompt first", s);
+      return DUALAR_ERR_INVALID_ARG;
+    }
     if (h->length[s] >= c.max_ctx) {
       set_err(h, "decode: slot %d reached max_ctx %d", s, c.max_ctx);
       return DUALAR_ERR_CONTEXT_FULL;
@@ -613,8 +632,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     const int pos = h->length[sl];
     s.rows[r] = RowInfo{sl, pos, 1, 0};
     if (pos % c.page_tokens == 0) {
-      const int pg = *h->free_pages.begin();
-      h->free_pages.erase(h->free_pages.begin());
+      const int pg = take_page(h);
       h->pages[sl].push_back(pg);
       s.upd_slot[s.n_updates] = sl;
       s.upd_index[s.n_updates] = pos / c.page_tokens;
@@ -929,24 +947,35 @@ int dualar_create(const dualar_config* cfg, const dualar_weights* w, void* cuda_
   }
   h->length.assign(c.max_seqs, -1);
   h->pages.assign(c.max_seqs, {});
+  h->page_refs.assign(c.max_pages, 0);
+  h->prefix_only.assign(c.max_seqs, 0);
   for (int p = 0; p < c.max_pages; ++p) h->free_pages.insert(p);
   *out = h;
   return DUALAR_OK;
 }
 
-int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens) {
+namespace {
+
+// Prompt positions [p0, p0 + n_tokens) of a slot: p0 = 0 starts a sequence in
+// an empty slot; p0 > 0 continues one (after a shared prefix).
+int prefill_impl(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens, bool append) {
   if (!h) return DUALAR_ERR_INVALID_ARG;
   const dualar_config& c = h->cfg;
   if (slot < 0 || slot >= c.max_seqs || !tokens || n_tokens <= 0) {
     set_err(h, "prefill: bad slot or tokens");
     return DUALAR_ERR_INVALID_ARG;
   }
-  if (h->length[slot] >= 0) {
+  if (!append && h->length[slot] >= 0) {
     set_err(h, "prefill: slot %d holds a sequence", slot);
     return DUALAR_ERR_SLOT_BUSY;
   }
-  if (n_tokens > c.max_ctx) {
-    set_err(h, "prefill: %d tokens exceed max_ctx %d", n_tokens, c.max_ctx);
+  if (append && h->length[slot] < 0) {
+    set_err(h, "prefill: slot %d is empty", slot);
+    return DUALAR_ERR_SLOT_EMPTY;
+  }
+  const int p0 = append ? h->length[slot] : 0;
+  if (p0 + n_tokens > c.max_ctx) {
+    set_err(h, "prefill: %d tokens exceed max_ctx %d", p0 + n_tokens, c.max_ctx);
     return DUALAR_ERR_CONTEXT_FULL;
   }
   for (int i = 0; i < n_tokens; ++i)
@@ -954,15 +983,17 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
       set_err(h, "prefill: token %d out of range", tokens[i]);
       return DUALAR_ERR_INVALID_ARG;
     }
-  const int need = (n_tokens + c.page_tokens - 1) / c.page_tokens;
+  const int need = (p0 + n_tokens + c.page_tokens - 1) / c.page_tokens - (p0 + c.page_tokens - 1) / c.page_tokens;
   if (need > static_cast<int>(h->free_pages.size())) {
     set_err(h, "prefill: %d pages needed, %zu free", need, h->free_pages.size());
     return DUALAR_ERR_OOM_PAGES;
   }
   const DevPtrs& d = h->d;
-  CUDA_TRY(h, cudaMemsetAsync(d.hist_n + slot, 0, 4, h->stream));
-  CUDA_TRY(h, cudaMemsetAsync(d.finished + slot, 0, 4, h->stream));
-  h->length[slot] = 0;
+  if (!append) {
+    CUDA_TRY(h, cudaMemsetAsync(d.hist_n + slot, 0, 4, h->stream));
+    CUDA_TRY(h, cudaMemsetAsync(d.finished + slot, 0, 4, h->stream));
+    h->length[slot] = 0;
+  }
   h->launches = 0;
   static LaunchSetup s;
   for (int c0 = 0; c0 < n_tokens; c0 += kMaxRows) {
@@ -972,12 +1003,11 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
     s.commit_last_only = 1;
     s.embed = 1;
     for (int r = 0; r < m; ++r) {
-      const int pos = c0 + r;
+      const int pos = p0 + c0 + r;
       s.rows[r] = RowInfo{slot, pos, 1, 0};
-      s.tokens[r] = tokens[pos];
+      s.tokens[r] = tokens[c0 + r];
       if (pos % c.page_tokens == 0) {
-        const int pg = *h->free_pages.begin();
-        h->free_pages.erase(h->free_pages.begin());
+        const int pg = take_page(h);
         h->pages[slot].push_back(pg);
         s.upd_slot[s.n_updates] = slot;
         s.upd_index[s.n_updates] = pos / c.page_tokens;
@@ -992,7 +1022,95 @@ int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_
     if (c0 + m == n_tokens) TRY(run_gemv(h, args_head(h, m - 1, 1)));
   }
   TRY(flush_tc(h));
-  h->length[slot] = n_tokens;
+  h->length[slot] = p0 + n_tokens;
+  h->prefix_only[slot] = 0;
+  return DUALAR_OK;
+}
+
+}  // namespace
+
+int dualar_prefill(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens) {
+  return prefill_impl(h, slot, tokens, n_tokens, false);
+}
+
+int dualar_prefill_append(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens) {
+  return prefill_impl(h, slot, tokens, n_tokens, true);
+}
+
+int dualar_share_prefix(dualar_handle* h, int32_t src, int32_t dst, int32_t n_tokens) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  const dualar_config& c = h->cfg;
+  if (src < 0 || src >= c.max_seqs || dst < 0 || dst >= c.max_seqs || src == dst || n_tokens <= 0) {
+    set_err(h, "share_prefix: bad slots or length");
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  if (h->length[src] < 0) {
+    set_err(h, "share_prefix: slot %d is empty", src);
+    return DUALAR_ERR_SLOT_EMPTY;
+  }
+  if (h->length[dst] >= 0) {
+    set_err(h, "share_prefix: slot %d holds a sequence", dst);
+    return DUALAR_ERR_SLOT_BUSY;
+  }
+  if (n_tokens > h->length[src]) {
+    set_err(h, "share_prefix: %d tokens exceed slot %d's %d", n_tokens, src, h->length[src]);
+    return DUALAR_ERR_INVALID_ARG;
+  }
+  const int pt = c.page_tokens;
+  const int nfull = n_tokens / pt;
+  const bool partial = n_tokens % pt != 0;
+  if (partial && h->free_pages.empty()) {
+    set_err(h, "share_prefix: no free page for the partly filled last page");
+    return DUALAR_ERR_OOM_PAGES;
+  }
+  const DevPtrs& d = h->d;
+  h->launches = 0;
+  // full pages by reference; the partly filled one as a copy (both sequences
+  // will write its remaining rows)
+  for (int i = 0; i < nfull; ++i) {
+    const int pg = h->pages[src][i];
+    ++h->page_refs[pg];
+    h->pages[dst].push_back(pg);
+  }
+  if (partial) {
+    const int from = h->pages[src][nfull];
+    const int pg = take_page(h);
+    h->pages[dst].push_back(pg);
+    const size_t page_elems = static_cast<size_t>(d.n_layer) * 2 * d.Hkv * pt * d.hd;
+    CUDA_TRY(h, cudaMemcpyAsync(d.kv_pool + static_cast<size_t>(pg) * page_elems,
+                                d.kv_pool + static_cast<size_t>(from) * page_elems, page_elems * 2,
+                                cudaMemcpyDeviceToDevice, h->stream));
+  }
+  static LaunchSetup s;
+  const int np = static_cast<int>(h->pages[dst].size());
+  for (int p0 = 0; p0 < np; p0 += kMaxRows) {
+    std::memset(&s, 0, sizeof(s));
+    for (int p = p0; p < std::min(np, p0 + kMaxRows); ++p) {
+      s.upd_slot[s.n_updates] = dst;
+      s.upd_index[s.n_updates] = p;
+      s.upd_page[s.n_updates] = h->pages[dst][p];
+      ++s.n_updates;
+    }
+    LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
+  }
+  if (n_tokens == h->length[src]) {
+    // the whole sequence: its held state too (the next frame starts from it)
+    CUDA_TRY(h, cudaMemcpyAsync(d.h_last + static_cast<size_t>(dst) * d.D, d.h_last + static_cast<size_t>(src) * d.D,
+                                sizeof(float) * d.D, cudaMemcpyDeviceToDevice, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(d.z_last + static_cast<size_t>(dst) * (d.n_sem + 1),
+                                d.z_last + static_cast<size_t>(src) * (d.n_sem + 1), sizeof(float) * (d.n_sem + 1),
+                                cudaMemcpyDeviceToDevice, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(d.hist + static_cast<size_t>(dst) * kRasRing, d.hist + static_cast<size_t>(src) * kRasRing,
+                                sizeof(int32_t) * kRasRing, cudaMemcpyDeviceToDevice, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(d.hist_n + dst, d.hist_n + src, 4, cudaMemcpyDeviceToDevice, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(d.finished + dst, d.finished + src, 4, cudaMemcpyDeviceToDevice, h->stream));
+    h->prefix_only[dst] = h->prefix_only[src];
+  } else {
+    CUDA_TRY(h, cudaMemsetAsync(d.hist_n + dst, 0, 4, h->stream));
+    CUDA_TRY(h, cudaMemsetAsync(d.finished + dst, 0, 4, h->stream));
+    h->prefix_only[dst] = 1;
+  }
+  h->length[dst] = n_tokens;
   return DUALAR_OK;
 }
 
@@ -1025,8 +1143,7 @@ int dualar_debug_synthetic_context(dualar_handle* h, int32_t slot, int32_t n_tok
   for (int p0 = 0; p0 < need; p0 += kMaxRows) {
     std::memset(&s, 0, sizeof(s));
     for (int p = p0; p < std::min(need, p0 + kMaxRows); ++p) {
-      const int pg = *h->free_pages.begin();
-      h->free_pages.erase(h->free_pages.begin());
+      const int pg = take_page(h);
       h->pages[slot].push_back(pg);
       s.upd_slot[s.n_updates] = slot;
       s.upd_index[s.n_updates] = p;
@@ -1105,9 +1222,10 @@ int dualar_release(dualar_handle* h, int32_t slot) {
     set_err(h, "release: bad slot %d", slot);
     return DUALAR_ERR_INVALID_ARG;
   }
-  for (int p : h->pages[slot]) h->free_pages.insert(p);
+  for (int p : h->pages[slot]) drop_page(h, p);
   h->pages[slot].clear();
   h->length[slot] = -1;
+  h->prefix_only[slot] = 0;
   return DUALAR_OK;
 }
 

@@ -105,6 +105,16 @@ class DualARDecoder:
         self._check(self.lib.dualar_prefill(self.h, slot, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                             t.size))
 
+    def prefill_append(self, slot: int, tokens) -> None:
+        """Continues the prompt of a slot (after share_prefix)."""
+        t = np.ascontiguousarray(np.asarray(tokens, np.int32))
+        self._check(self.lib.dualar_prefill_append(self.h, slot, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                                   t.size))
+
+    def share_prefix(self, src: int, dst: int, n_tokens: int) -> None:
+        """Starts slot dst from the first n_tokens positions of slot src (shared pages)."""
+        self._check(self.lib.dualar_share_prefix(self.h, src, dst, n_tokens))
+
     def decode_frame(self, slots, uniforms: torch.Tensor, sampling: Sampling,
                      codes: torch.Tensor | None = None, status: torch.Tensor | None = None):
         s = np.ascontiguousarray(np.asarray(slots, np.int32))

@@ -214,8 +214,32 @@ int dualar_decode_frame_noalloc(dualar_handle* h, int32_t batch, const int32_t* 
                                 int32_t* codes, int32_t* status);
 
 /* Ends the sequence in a slot and returns its KV pages to the pool (lowest
- * page numbers are handed out first).  Queues nothing on the GPU. */
+ * page numbers are handed out first); a page shared with other slots
+ * (dualar_share_prefix) returns only when the last of them releases it.
+ * Queues nothing on the GPU. */
 int dualar_release(dualar_handle* h, int32_t slot);
+
+/* Starts a sequence in the empty slot dst from the first n_tokens positions
+ * of slot src: a common prompt prefix such as a reference voice, which
+ * [P2] "Tags are text" places in the system prompt so that requests with the
+ * same voice share it, and whose cache hits [P2] "Streaming: whose numbers"
+ * reports.  dst's page table takes src's full pages of those positions by
+ * reference (each page counts the slots holding it); a partly filled last
+ * page is copied (one page of every layer's K/V), so neither sequence ever
+ * writes a shared page.  With n_tokens equal to src's length dst also takes
+ * src's held state (final hidden, restricted logits, resample history) and
+ * can decode at once; with fewer, dst holds only the prefix and must be
+ * continued with dualar_prefill_append before decoding (decode rejects it).
+ * 1 <= n_tokens <= src's length.  Errors: INVALID_ARG, SLOT_EMPTY (src),
+ * SLOT_BUSY (dst), OOM_PAGES, CUDA. */
+int dualar_share_prefix(dualar_handle* h, int32_t src, int32_t dst, int32_t n_tokens);
+
+/* Continues the prompt of a slot that holds a sequence (typically a shared
+ * prefix): positions length .. length + n_tokens - 1, exactly as
+ * dualar_prefill computes a prompt, and the slot then holds the state of the
+ * last of them.  tokens: host int32[n_tokens].  Errors: INVALID_ARG,
+ * SLOT_EMPTY, OOM_PAGES, CONTEXT_FULL, CUDA. */
+int dualar_prefill_append(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens);
 
 /* Synchronises the handle's stream and reports device-side errors:
  * DUALAR_ERR_TIMEOUT if a bounded wait gave up, DUALAR_ERR_DEVICE if a bounds

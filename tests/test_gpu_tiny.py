@@ -396,3 +396,81 @@ def test_teacher_forced_batch12_tensor_cores(dev_weights, tiny_oracle):
         np.testing.assert_array_equal(a, b)
     for a, b in zip(outs[0], outs[2]):
         assert np.abs(a - b).max() <= 2e-3 * max(1.0, float(np.abs(b).max()))
+
+
+# ---------------------------------------------------------- shared prefix --
+
+def test_shared_prefix_matches_full_prompts(dev_weights, tiny_oracle):
+    """A common prompt prefix (a reference voice) shared between slots: the
+    full pages by reference, the partly filled one copied; each slot then
+    continues its own prompt.  Every slot's state and teacher-forced frames
+    equal the oracle's run of its whole prompt; a whole-sequence share equals
+    its source bit for bit; page tables follow the oracle's allocator with
+    shared pages, also after the source is released."""
+    prefix = g.make_prompt(TINY, 150, seed=60)
+    rest = {1: g.make_prompt(TINY, 40, seed=61), 2: g.make_prompt(TINY, 90, seed=62)}
+    n_shared = 100                       # page 0 (positions 0..63) shared, page 1 copied
+    d = make(dev_weights, max_pages=64, max_seqs=4)
+    pages = PageOracle(d.max_pages, TINY.page_tokens)
+    d.prefill(0, prefix)
+    pages.append(0, len(prefix))
+    for s, r in rest.items():
+        d.share_prefix(0, s, n_shared)
+        pages.share(0, s, n_shared)
+        with pytest.raises(Exception):   # a bare prefix cannot decode
+            d.decode_frame_forced([s], dev(np.full((1, TINY.n_codebooks + 1), 0.5, np.float32)),
+                                  gpu_sampling(OSampling()), dev(np.zeros((1, TINY.n_codebooks), np.int32)))
+        d.prefill_append(s, r)
+        pages.append(s, len(r))
+    d.share_prefix(0, 3, len(prefix))    # the whole sequence, held state included
+    pages.share(0, 3, len(prefix))
+    d.sync()
+    for s in range(4):
+        assert d.page_table(s) == pages.table[s], f"slot {s}"
+    assert d.page_table(1)[0] == d.page_table(0)[0] and d.page_table(1)[1] != d.page_table(0)[1]
+    prompts = {0: prefix, 1: np.concatenate([prefix[:n_shared], rest[1]]),
+               2: np.concatenate([prefix[:n_shared], rest[2]]), 3: prefix}
+    seqs = {s: tiny_oracle.prefill(p) for s, p in prompts.items()}
+    states = {s: d.read_state(s) for s in range(4)}
+    for s in range(4):
+        assert_logits_close(states[s][0], seqs[s].h_last, f"hidden, slot {s}")
+        assert_logits_close(states[s][1], seqs[s].z_last, f"logits, slot {s}")
+    np.testing.assert_array_equal(states[3][0], states[0][0])
+    np.testing.assert_array_equal(states[3][1], states[0][1])
+    # the source goes away; its shared pages stay with the other slots
+    d.release(0)
+    pages.release(0)
+    slots = [1, 2, 3]
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
+    forced = g.make_forced_codes(2, 3, TINY, seed=63)
+    uni = g.make_uniforms(2, 3, TINY, seed=64)
+    for f in range(2):
+        codes, status, slow, fast, _ = d.decode_frame_forced(slots, dev(uni[f]), gpu_sampling(smp), dev(forced[f]))
+        d.sync()
+        slow, fast = slow.cpu().numpy(), fast.cpu().numpy()
+        np.testing.assert_array_equal(status.cpu().numpy(), 0)
+        for i, s in enumerate(slots):
+            r = tiny_oracle.decode_frame(seqs[s], uni[f, i], smp, forced=forced[f, i])
+            assert_logits_close(slow[i], r.slow_logits, f"slow logits f{f} slot {s}")
+            assert_logits_close(fast[i], r.fast_logits, f"fast logits f{f} slot {s}")
+            pages.append(s, 1)
+    for s in slots:
+        assert d.page_table(s) == pages.table[s], f"slot {s} after frames"
+    d.close()
+
+
+def test_shared_prefix_rejects_bad_arguments(dev_weights):
+    d = make(dev_weights, max_pages=64, max_seqs=4)
+    d.prefill(0, g.make_prompt(TINY, 20, seed=65))
+    with pytest.raises(Exception):
+        d.share_prefix(1, 2, 5)          # empty source
+    with pytest.raises(Exception):
+        d.share_prefix(0, 0, 5)          # same slot
+    with pytest.raises(Exception):
+        d.share_prefix(0, 1, 21)         # longer than the source
+    d.share_prefix(0, 1, 20)
+    with pytest.raises(Exception):
+        d.share_prefix(0, 1, 5)          # busy destination
+    with pytest.raises(Exception):
+        d.prefill_append(2, g.make_prompt(TINY, 4, seed=66))   # empty slot
+    d.close()

@@ -470,6 +470,30 @@ def test_page_oracle_lowest_free_first():
         p.append(3, 4 * 5)
 
 
+def test_page_oracle_shared_prefix():
+    p = oracle.PageOracle(8, 4)
+    p.append(0, 6)          # positions 0..5 -> pages 0, 1
+    p.share(0, 1, 5)        # page 0 by reference, the partly filled page copied: lowest free = 2
+    assert p.table[1] == [0, 2] and p.length[1] == 5
+    p.append(1, 4)          # positions 5..7 stay in page 2; position 8 -> page 3
+    assert p.table[1] == [0, 2, 3]
+    p.release(0)            # page 0 is still held by slot 1; page 1 returns
+    p.append(2, 1)
+    assert p.table[2] == [1]
+    p.share(1, 3, 8)        # whole pages only: no copy
+    assert p.table[3] == [0, 2]
+    p.release(1)            # pages 0 and 2 still held by slot 3; page 3 returns
+    p.append(4, 1)
+    assert p.table[4] == [3]
+    p.release(3)
+    p.append(5, 9)          # pages 0, 2 and then the lowest free (4)
+    assert p.table[5] == [0, 2, 4]
+    with pytest.raises(ValueError):
+        p.share(5, 2, 3)    # busy destination
+    with pytest.raises(ValueError):
+        p.share(5, 6, 10)   # longer than the source
+
+
 # ------------------------------------------------------ planted mistakes --
 
 def _expect_pin_failure(monkeypatch, target, name, bad, pin, *args):
