@@ -797,6 +797,507 @@ __global__ void __launch_bounds__(kAmThreads, 1)
   }
 }
 
+// ============================================================================
+// Prefill: query blocks
+// ============================================================================
+// A prefill launch holds consecutive positions of one sequence, whose K/V
+// the append kernel has already written.  Here a unit is (a block of
+// QB = 32 / G consecutive rows, KV head g, chunk c of the block's last row),
+// so every page is read once for QB rows instead of once per row.  Compute
+// warp w owns rows w RW .. w RW + RW - 1 (RW = 8 / G) over all 64 tokens of
+// every page: its 8 (row, head) pairs are MMA rows 0..7 with the bf16 hi
+// halves of Q and P and rows 8..15 with the lo halves, and each row masks
+// the positions after its own.  No merge between warps (each owns whole
+// rows); the finalize warps write every row's partial (or output) and
+// combine a row's chunks, in chunk order, when its last chunk arrives.  The
+// prep, producer and finalize roles, the page ring and the dynamic schedule
+// are those of the decode kernel above.
+template <int HD, int G>
+struct ApCfg {
+  static constexpr int RW = 8 / G;                        // rows per compute warp
+  static constexpr int QB = kAmWarps * RW;                // rows per unit
+  static constexpr int SLOT = AmCfg<HD, G>::SLOT;
+  static constexpr int NBUF = ((HD == 128 ? 160 : 192) * 1024) / SLOT;
+};
+
+struct ApDesc {
+  int32_t pages[kMaxChunkPages];
+  int32_t r0, nr, g, c, nch, t0, t1, npages, last;
+};
+
+template <int HD, int G>
+struct ApSmem {
+  ApDesc unit[2];
+  float co[2][kAmWarps][8][HD];           // each warp's 8 (row, head) states of unit k (buffer k % 2)
+  float cm[2][kAmWarps][8], cl[2][kAmWarps][8];
+  struct Fin {
+    float fm[8][kMaxChunks], fl[8][kMaxChunks];
+  } fin[kAmFinalWarps];
+  RowInfo rows[kMaxRows];
+  int32_t bpre[kMaxRows + 1];             // units before each block
+  uint64_t full[ApCfg<HD, G>::NBUF], empty[ApCfg<HD, G>::NBUF];
+  uint64_t ufull[2], uempty[2], cfull[2], cempty[2];
+  int abort_flag;
+};
+
+template <int HD, int G>
+constexpr size_t ap_smem_bytes() {
+  return static_cast<size_t>(ApCfg<HD, G>::NBUF) * ApCfg<HD, G>::SLOT + sizeof(ApSmem<HD, G>) + 1024;
+}
+
+template <int HD, int G>
+__global__ void __launch_bounds__(kAmThreads, 1)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap tkv, const DevPtrs d, int nrows, int layer,
+                        int chunk_tokens) {
+  using C = ApCfg<HD, G>;
+  constexpr int NB = C::NBUF, RW = C::RW, QB = C::QB;
+  constexpr int HALF = AmCfg<HD, G>::HALF, HALVES = AmCfg<HD, G>::HALVES;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  ApSmem<HD, G>& sm = *reinterpret_cast<ApSmem<HD, G>*>(ring + NB * C::SLOT);
+  const uint32_t ring_s = smem_addr(ring);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hkv = d.Hkv, hq = d.Hq;
+  if (tid == 0) {
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(&sm.full[b], 1);
+      mbar_init(&sm.empty[b], kAmWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.ufull[b], 1);
+      mbar_init(&sm.uempty[b], kAmUnitUsers);
+      mbar_init(&sm.cfull[b], kAmWarps);
+      mbar_init(&sm.cempty[b], 1);
+    }
+    sm.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_launch();
+  for (int i = tid; i < nrows; i += kAmThreads) sm.rows[i] = ld_row(&d.rows[i]);
+  __syncthreads();
+  volatile int* abort_flag = &sm.abort_flag;
+  const int nblk = (nrows + QB - 1) / QB;
+
+  if (warp == kAmPrep) {
+    // ---- prep: units from the shared counter; pages and row range per unit
+    if (lane == 0) {
+      int acc = 0;
+      for (int b = 0; b < nblk; ++b) {
+        sm.bpre[b] = acc;
+        const int rl = min(nrows, (b + 1) * QB) - 1;
+        acc += hkv * ((sm.rows[rl].pos + chunk_tokens) / chunk_tokens);
+      }
+      sm.bpre[nblk] = acc;
+    }
+    __syncwarp();
+    const int total = sm.bpre[nblk];
+    uint32_t k = 0;
+    bool ok = true;
+    uint32_t* counter = d.sched + layer;
+    int next = 0;
+    if (lane == 0) next = static_cast<int>(atomicAdd(counter, 1u));
+    for (;;) {
+      const int v = __shfl_sync(0xFFFFFFFFu, next, 0);
+      if (v >= total) break;
+      if (lane == 0) next = static_cast<int>(atomicAdd(counter, 1u));
+      int b = 0;
+      while (b + 1 < nblk && sm.bpre[b + 1] <= v) ++b;
+      const int r0 = b * QB, nr = min(nrows, r0 + QB) - r0;
+      const RowInfo first = sm.rows[r0], lastr = sm.rows[r0 + nr - 1];
+      // the block's rows must be consecutive positions of one sequence
+      bool rows_ok = lane >= nr || (sm.rows[r0 + lane].slot == first.slot && sm.rows[r0 + lane].pos == first.pos + lane &&
+                                    sm.rows[r0 + lane].active);
+      if (!__all_sync(0xFFFFFFFFu, rows_ok)) {
+        if (lane == 0) raise_error(d.err, DEV_ERR_BAD_INDEX);
+        continue;
+      }
+      const int L = lastr.pos + 1;
+      AmUnit un;
+      un.nch = (L + chunk_tokens - 1) / chunk_tokens;
+      const int local = v - sm.bpre[b];
+      un.g = local / un.nch;
+      un.c = local % un.nch;
+      un.t0 = un.c * chunk_tokens;
+      un.t1 = min(L, un.t0 + chunk_tokens);
+      un.npages = (un.t1 - un.t0 + kPageTokens - 1) / kPageTokens;
+      un.ptab = d.page_table + static_cast<size_t>(first.slot) * d.pages_per_seq + un.t0 / kPageTokens;
+      int pg[kAmPageRegs];
+      if (!am_pages(d, un, lane, pg)) {
+        if (lane == 0) raise_error(d.err, DEV_ERR_BAD_PAGE);
+        continue;
+      }
+      const int bb = static_cast<int>(k & 1);
+      if (k >= 2 && !am_wait(&sm.uempty[bb], ((k >> 1) - 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      ApDesc& ud = sm.unit[bb];
+#pragma unroll
+      for (int i = 0; i < kAmPageRegs; ++i)
+        if (lane + 32 * i < un.npages) ud.pages[lane + 32 * i] = pg[i];
+      if (lane == 0) {
+        ud.r0 = r0;
+        ud.nr = nr;
+        ud.g = un.g;
+        ud.c = un.c;
+        ud.nch = un.nch;
+        ud.t0 = un.t0;
+        ud.t1 = un.t1;
+        ud.npages = un.npages;
+        ud.last = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ufull[bb]);
+      ++k;
+    }
+    for (int e = 0; ok && e < 2; ++e, ++k) {
+      const int bb = static_cast<int>(k & 1);
+      if (k >= 2 && !am_wait(&sm.uempty[bb], ((k >> 1) - 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      if (lane == 0) {
+        sm.unit[bb].last = 1;
+        mbar_arrive(&sm.ufull[bb]);
+      }
+      __syncwarp();
+    }
+    return;
+  }
+
+  if (warp == kAmProducer) {
+    // ---- producer (lane 0): every unit's pages into the ring
+    if (lane != 0) return;
+    uint32_t gp = 0;
+    bool ok = true;
+    for (uint32_t k = 0; ok; ++k) {
+      const int b = static_cast<int>(k & 1);
+      if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        break;
+      }
+      const ApDesc& ud = sm.unit[b];
+      if (ud.last) break;
+      for (int p = 0; p < ud.npages; ++p, ++gp) {
+        const int pgp = ud.pages[p];
+        const int s = static_cast<int>(gp % NB);
+        if (gp >= static_cast<uint32_t>(NB) && !am_wait(&sm.empty[s], ((gp / NB) - 1) & 1, abort_flag, d)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const int rowk = static_cast<int>(((static_cast<long long>(pgp) * d.n_layer + layer) * 2 * hkv + ud.g) * 64);
+        mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(C::SLOT));
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int hh = 0; hh < HALVES; ++hh)
+            tma_load_2d(ring + s * C::SLOT + kv * HALF + hh * kAmBox, &tkv, hh * 64, rowk + kv * hkv * 64,
+                        &sm.full[s]);
+      }
+      if (ok) mbar_arrive(&sm.uempty[b]);
+    }
+    for (uint32_t j = gp > static_cast<uint32_t>(NB) ? gp - NB : 0; j < gp; ++j) {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&sm.full[j % NB], (j / NB) & 1))
+        if (global_timer_ns() - t0 > d.wait_limit_ns) break;
+    }
+    return;
+  }
+
+  if (warp >= kAmFinal) {
+    // ---- finalize warp fi: units fi, fi + 2, ...
+    constexpr int EPLF = HD / 32;
+    const int fi = warp - kAmFinal;
+    auto& fz = sm.fin[fi];
+    for (uint32_t k = static_cast<uint32_t>(fi);; k += 2) {
+      const int b = fi;
+      if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      const ApDesc& ud = sm.unit[b];
+      if (ud.last) return;
+      if (!am_wait(&sm.cfull[b], (k >> 1) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      const int r0 = ud.r0, nr = ud.nr, g = ud.g, c = ud.c, nch = ud.nch;
+      // every (warp, pair) -> (row, head): output, or this chunk's partial
+      for (int e = lane; e < kAmWarps * 8 * HD; e += 32) {
+        const int w = e / (8 * HD), vv = (e / HD) % 8, dd = e % HD;
+        const int jr = w * RW + vv / G, h = vv % G;
+        if (jr >= nr) continue;
+        const int r = r0 + jr;
+        const float O = sm.co[b][w][vv][dd];
+        if (nch == 1) {
+          d.attn[static_cast<size_t>(r) * hq * HD + (g * G + h) * HD + dd] = O / sm.cl[b][w][vv];
+        } else {
+          float* pw = d.part + ((static_cast<size_t>(r) * hkv + g) * kMaxChunks + c) * G * (HD + 2) + h * (HD + 2);
+          pw[dd] = O;
+          if (dd == 0) {
+            pw[HD] = sm.cm[b][w][vv];
+            pw[HD + 1] = sm.cl[b][w][vv];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.cempty[b]);
+      if (nch > 1) {
+        __threadfence();
+        __syncwarp();
+        // every row's arrival at once (lane = row), then the rows this unit completes
+        int last = 0;
+        if (lane < nr) {
+          const int r = r0 + lane;
+          const uint32_t old = atomic_add_acq_rel_gpu(&d.arrive[r * hkv + g], 1u);
+          if (old == static_cast<uint32_t>(nch - 1)) {
+            atomicExch(&d.arrive[r * hkv + g], 0u);
+            last = 1;
+          }
+        }
+        const uint32_t lastmask = __ballot_sync(0xFFFFFFFFu, last);
+        for (int jr = 0; jr < nr; ++jr) {
+          const int r = r0 + jr;
+          if (!((lastmask >> jr) & 1u)) continue;
+          // row r's chunks in chunk order
+          __threadfence();
+          const float* pb = d.part + (static_cast<size_t>(r) * hkv + g) * kMaxChunks * G * (HD + 2);
+          for (int i = lane; i < nch * G; i += 32) {
+            const int cc = i / G, h = i % G;
+            const float* q = pb + (cc * G + h) * (HD + 2);
+            fz.fm[h][cc] = ldf(q + HD);
+            fz.fl[h][cc] = ldf(q + HD + 1);
+          }
+          __syncwarp();
+          if (lane < G) {
+            const int h = lane;
+            float M = -INFINITY;
+            for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, fz.fm[h][cc]);
+            float Ls = 0.f;
+            for (int cc = 0; cc < nch; ++cc) {
+              const float f = fz.fm[h][cc] == -INFINITY ? 0.f : expf(fz.fm[h][cc] - M);
+              fz.fm[h][cc] = f;
+              Ls += fz.fl[h][cc] * f;
+            }
+            fz.fl[h][0] = Ls;   // (fl is not read again for this row)
+          }
+          __syncwarp();
+          float os[G][EPLF];
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < EPLF; ++j) os[h][j] = 0.f;
+#pragma unroll 2
+          for (int cc = 0; cc < nch; ++cc) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float* q = pb + (cc * G + h) * (HD + 2) + lane * EPLF;
+              const float f = fz.fm[h][cc];
+#pragma unroll
+              for (int j = 0; j < EPLF; ++j) os[h][j] += ldf(q + j) * f;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < EPLF; ++j)
+              d.attn[static_cast<size_t>(r) * hq * HD + (g * G + h) * HD + lane * EPLF + j] = os[h][j] / fz.fl[h][0];
+          __syncwarp();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.uempty[b]);
+    }
+  }
+
+  // ---- compute warps
+  const int gr = lane >> 2, tq = lane & 3;
+  const float qscale = 1.0f / sqrtf(static_cast<float>(HD));
+  uint32_t gp = 0;
+  for (uint32_t k = 0;; ++k) {
+    const int b = static_cast<int>(k & 1);
+    if (!am_wait(&sm.ufull[b], (k >> 1) & 1, abort_flag, d)) {
+      *abort_flag = 1;
+      return;
+    }
+    const ApDesc& ud = sm.unit[b];
+    if (ud.last) return;
+    const int t0 = ud.t0, t1 = ud.t1, npages = ud.npages, g = ud.g;
+    // this lane's (row, head): row rw0 + gr / G, head gr % G
+    const int jr = warp * RW + gr / G, h = gr % G;
+    const bool valid = jr < ud.nr;
+    const int r = ud.r0 + (valid ? jr : 0);
+    const int plim = valid ? sm.rows[r].pos : -1;   // the last position this row sees
+    uint32_t qa[HD / 16][2], qb[HD / 16][2];
+    const float* qsrc = d.qrot + (static_cast<size_t>(r) * hq + g * G + h) * HD;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int dd = ks * 16 + half * 8 + 2 * tq;
+        const float x = valid ? ldf(qsrc + dd) * qscale : 0.f, y = valid ? ldf(qsrc + dd + 1) * qscale : 0.f;
+        split2(x, y, qa[ks][half], qb[ks][half]);
+      }
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[HD / 8][4];
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int p = 0; p < npages; ++p, ++gp) {
+      const int s = static_cast<int>(gp % NB);
+      if (!am_wait(&sm.full[s], (gp / NB) & 1, abort_flag, d)) {
+        *abort_flag = 1;
+        return;
+      }
+      const int ps = t0 + p * kPageTokens;
+      const uint32_t kb = ring_s + s * C::SLOT, vb = kb + HALF;
+      float sc[8][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks) {
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp) {
+          uint32_t bb[4];
+          const int tok = jp * 16 + (lane >> 4) * 8 + (lane & 7);
+          const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
+          ldsm_x4(bb, sw_addr(kb, tok, dim));
+          mma16816(sc[2 * jp], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[0], bb[1]);
+          mma16816(sc[2 * jp + 1], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], bb[2], bb[3]);
+        }
+      }
+      // hi + lo rows -> scores; positions after the row's own, or past the chunk, masked
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc[j][0] += sc[j][2];
+        sc[j][1] += sc[j][3];
+        const int t = ps + 8 * j + 2 * tq;
+        if (t > plim || t >= t1) sc[j][0] = -INFINITY;
+        if (t + 1 > plim || t + 1 >= t1) sc[j][1] = -INFINITY;
+        mx = fmaxf(mx, fmaxf(sc[j][0], sc[j][1]));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const bool none = m_new == -INFINITY;   // nothing visible to this row yet
+      const float f = none ? 1.f : expf(m_run - m_new);
+      float ps_sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc[j][0] = none ? 0.f : expf(sc[j][0] - m_new);
+        sc[j][1] = none ? 0.f : expf(sc[j][1] - m_new);
+        ps_sum += sc[j][0] + sc[j][1];
+      }
+      ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 1);
+      ps_sum += __shfl_xor_sync(0xFFFFFFFFu, ps_sum, 2);
+      l_run = l_run * f + ps_sum;
+      m_run = m_new;
+#pragma unroll
+      for (int n = 0; n < HD / 8; ++n) {
+        o[n][0] *= f;
+        o[n][1] *= f;
+        o[n][2] *= f;
+        o[n][3] *= f;
+      }
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        uint32_t ph0, pl0, ph2, pl2;
+        split2(sc[2 * kt][0], sc[2 * kt][1], ph0, pl0);
+        split2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], ph2, pl2);
+#pragma unroll
+        for (int np = 0; np < HD / 16; ++np) {
+          uint32_t bb[4];
+          const int tok = kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int dim = np * 16 + (lane >> 4) * 8;
+          ldsm_x4_t(bb, sw_addr(vb, tok, dim));
+          mma16816(o[2 * np], ph0, pl0, ph2, pl2, bb[0], bb[1]);
+          mma16816(o[2 * np + 1], ph0, pl0, ph2, pl2, bb[2], bb[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+    }
+    // hand the rows' (m, l, O) to the finalize warp
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) {
+      o[n][0] += o[n][2];
+      o[n][1] += o[n][3];
+    }
+    if (k >= 2 && !am_wait(&sm.cempty[b], ((k >> 1) - 1) & 1, abort_flag, d)) {
+      *abort_flag = 1;
+      return;
+    }
+    if (tq == 0) {
+      sm.cm[b][warp][gr] = m_run;
+      sm.cl[b][warp][gr] = l_run;
+    }
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) {
+      sm.co[b][warp][gr][8 * n + 2 * tq] = o[n][0];
+      sm.co[b][warp][gr][8 * n + 2 * tq + 1] = o[n][1];
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&sm.cfull[b]);
+      mbar_arrive(&sm.uempty[b]);
+    }
+  }
+}
+
+template <int HD, int G>
+static cudaError_t ap_launch(const CUtensorMap& m, const DevPtrs& d, int nrows, int layer, int chunk, int grid,
+                             cudaStream_t st) {
+  static bool configured = false;
+  const size_t smem = ap_smem_bytes<HD, G>();
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_pdl(attn_prefill_kernel<HD, G>, dim3(grid), dim3(kAmThreads), smem, st, m, d, nrows, layer, chunk);
+}
+
+template <int HD>
+static cudaError_t ap_hd(const CUtensorMap& m, const DevPtrs& d, int nrows, int layer, int chunk, int grid,
+                         cudaStream_t st) {
+  switch (d.Hq / d.Hkv) {
+    case 1: return ap_launch<HD, 1>(m, d, nrows, layer, chunk, grid, st);
+    case 2: return ap_launch<HD, 2>(m, d, nrows, layer, chunk, grid, st);
+    case 4: return ap_launch<HD, 4>(m, d, nrows, layer, chunk, grid, st);
+    case 8: return ap_launch<HD, 8>(m, d, nrows, layer, chunk, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_attn_prefill(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens, int n_sm,
+                                cudaStream_t st, bool* used) {
+  *used = false;
+  if (nrows < 2 || total_units <= 0 || !tc_available()) return cudaSuccess;
+  if ((d.hd != 64 && d.hd != 128) || d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0 ||
+      chunk_tokens / kPageTokens > kMaxChunkPages || nrows > kMaxRows)
+    return cudaSuccess;
+  const long long rows = static_cast<long long>(d.max_pages) * d.n_layer * 2 * d.Hkv * kPageTokens;
+  if (rows >= (1LL << 31)) return cudaSuccess;
+  CUtensorMap m;
+  if (!tc_bf16_map(&m, d.kv_pool, d.hd, static_cast<int>(rows), d.hd, 64)) return cudaSuccess;
+  // chunks as long as a block of rows makes the units fewer: the split that
+  // suits one row per unit, times the rows of a block (at most kMaxChunkPages)
+  const int qb = 32 / (d.Hq / d.Hkv);
+  int cp = chunk_tokens / kPageTokens * qb;
+  cp = cp > kMaxChunkPages ? kMaxChunkPages : cp;
+  chunk_tokens = cp * kPageTokens;
+  const int grid = total_units < n_sm ? total_units : n_sm;
+  cudaError_t e = d.hd == 128 ? ap_hd<128>(m, d, nrows, layer, chunk_tokens, grid, st)
+                              : ap_hd<64>(m, d, nrows, layer, chunk_tokens, grid, st);
+  if (e == cudaSuccess) *used = true;
+  return e;
+}
+
 template <int HD, int G>
 static cudaError_t am_launch(const CUtensorMap& m, const DevPtrs& d, int nrows, int layer, int units, int chunk,
                              int grid, int fuse, const uint16_t* qn, const uint16_t* kn, cudaStream_t st,

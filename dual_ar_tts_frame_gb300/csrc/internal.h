@@ -195,6 +195,11 @@ cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_
 // Tensor-core variant for launches of >= kAttnMmaMinRows rows (attn_mma.cu);
 // *used is false (nothing launched) when the shape or the driver rules it out.
 constexpr int kAttnMmaMinRows = 3;
+// Prefill (rows: consecutive positions of one sequence, K/V already
+// appended): blocks of rows share every page read (attn_mma.cu).  *used is
+// false when the shape or the driver rules it out.
+cudaError_t launch_attn_prefill(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens, int n_sm,
+                                cudaStream_t st, bool* used);
 cudaError_t launch_attn_mma(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens, int n_sm,
                             bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st,
                             bool* used,

@@ -431,6 +431,12 @@ cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_
   if (mma_used) *mma_used = false;
   if (nrows <= 0 || total_units <= 0) return cudaSuccess;
   if (d.page_tokens != kPageTokens || chunk_tokens % kPageTokens != 0) return cudaErrorInvalidValue;
+  if (!fuse_append) {
+    // prefill: blocks of consecutive rows read each page once
+    bool used = false;
+    const cudaError_t e = launch_attn_prefill(d, nrows, layer, total_units, chunk_tokens, n_sm, st, &used);
+    if (e != cudaSuccess || used) return e;
+  }
   {
     // 3+ rows: the tensor-core variant; 1-2 rows keep this kernel, the same
     // device code as the persistent frame kernel (bit-identical paths)
