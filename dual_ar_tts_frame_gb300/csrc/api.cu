@@ -34,6 +34,7 @@ struct dualar_handle {
   std::vector<std::vector<int>> pages;   // pages per slot
   std::set<int> free_pages;
   std::vector<int> page_refs;            // slots whose page table holds each page (shared prefixes)
+  LaunchSetup setup{};                   // the setup kernel's argument, filled per launch sequence
   std::vector<char> prefix_only;         // slot holds a shared prefix without its prompt's end
   std::string err;
   int launches = 0;
@@ -622,7 +623,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     set_err(h, "decode: %d pages needed, %zu free", need, h->free_pages.size());
     return DUALAR_ERR_OOM_PAGES;
   }
-  static LaunchSetup s;   // large; filled per call, copied into the launch
+  LaunchSetup& s = h->setup;   // large; filled per call, copied into the launch
   std::memset(&s, 0, sizeof(s));
   s.n_rows = batch;
   s.commit_last_only = 0;
@@ -995,7 +996,7 @@ int prefill_impl(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t 
     h->length[slot] = 0;
   }
   h->launches = 0;
-  static LaunchSetup s;
+  LaunchSetup& s = h->setup;
   for (int c0 = 0; c0 < n_tokens; c0 += kMaxRows) {
     const int m = std::min(kMaxRows, n_tokens - c0);
     std::memset(&s, 0, sizeof(s));
@@ -1081,7 +1082,7 @@ int dualar_share_prefix(dualar_handle* h, int32_t src, int32_t dst, int32_t n_to
                                 d.kv_pool + static_cast<size_t>(from) * page_elems, page_elems * 2,
                                 cudaMemcpyDeviceToDevice, h->stream));
   }
-  static LaunchSetup s;
+  LaunchSetup& s = h->setup;
   const int np = static_cast<int>(h->pages[dst].size());
   for (int p0 = 0; p0 < np; p0 += kMaxRows) {
     std::memset(&s, 0, sizeof(s));
@@ -1138,7 +1139,7 @@ int dualar_debug_synthetic_context(dualar_handle* h, int32_t slot, int32_t n_tok
   CUDA_TRY(h, cudaMemsetAsync(d.hist_n + slot, 0, 4, h->stream));
   CUDA_TRY(h, cudaMemsetAsync(d.finished + slot, 0, 4, h->stream));
   h->launches = 0;
-  static LaunchSetup s;
+  LaunchSetup& s = h->setup;
   // pages in the order prefill takes them (lowest free first)
   for (int p0 = 0; p0 < need; p0 += kMaxRows) {
     std::memset(&s, 0, sizeof(s));
