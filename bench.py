@@ -61,6 +61,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-b64", action="store_true", help="skip the batch-64 measurement")
+    ap.add_argument("--no-w4a16", action="store_true", help="skip the 4-bit-weight measurement")
     return ap.parse_args()
 
 
@@ -215,6 +216,76 @@ def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
             "frame_bytes_per_step": bytes_total / frames,
             "frame_roofline": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
             "gpu_launches_per_step": launches}
+
+
+def measure_w4a16(cfg, w, prompt, frames: int, warmup: int, peak: float) -> dict:
+    """Batch 1 with 4-bit weights: the "late12attn" plan (every projection
+    packed except the query/key/value and output projections of the last 12
+    slow layers; embeddings, norms and heads bf16), packed on the GPU from
+    the same bf16 weights.  The benchmark's 512-token prompt is prefilled
+    through the packed weights, then `warmup` + `frames` frames (seed-1
+    uniforms, T 0.8, top-p 0.8, RAS 10, <|im_end|> excluded), device-timed;
+    then a few frames with every GEMV launch bracketed by events for the
+    GEMV kernel's own roofline."""
+    import torch
+    from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling, late_attn_keys, pack_w4a16
+    from dual_ar_tts_frame_gb300 import bytemodel
+    keys = late_attn_keys(cfg.n_layer, cfg.fast_n_layer, 12)
+    packed = {k: pack_w4a16(w[k]) for k in keys}
+    max_ctx = len(prompt) + warmup + frames + 16
+    dec = DualARDecoder(cfg, w, max_pages=(max_ctx + 63) // 64 + 2, max_seqs=1, max_ctx=max_ctx)
+    dec.set_w4a16(packed)
+    stream = torch.cuda.current_stream()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    dec.prefill(0, prompt)
+    p1.record(stream)
+    dec.sync()
+    prefill_ms = p0.elapsed_time(p1)
+    smp = Sampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
+    n_prof = 4
+    uni = torch.from_numpy(gen.make_uniforms(warmup + frames + n_prof, 1, cfg, seed=1)).cuda()
+    codes = torch.empty((1, cfg.n_codebooks), dtype=torch.int32, device="cuda")
+    status = torch.empty((1,), dtype=torch.int32, device="cuda")
+    for f in range(warmup):
+        dec.decode_frame([0], uni[f], smp, codes, status)
+    dec.sync()
+    launches = dec.last_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for f in range(warmup, warmup + frames):
+        dec.decode_frame([0], uni[f], smp, codes, status)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dec.sync()
+    ms = ev0.elapsed_time(ev1)
+    assert int(status.item()) == 0
+    dec.profile(True)
+    for f in range(warmup + frames, warmup + frames + n_prof):
+        dec.decode_frame([0], uni[f], smp, codes, status)
+    dec.profile(False)
+    prof = dec.profile_read()
+    dec.close()
+    att = [len(prompt) + f + 1 for f in range(warmup, warmup + frames)]
+    bytes_total = sum(bytemodel.frame_bytes(cfg, [a], keys) for a in att)
+    gbs = bytes_total / (ms / 1000.0) / 1e9
+    g_gbs = prof["total_bytes"] / (prof["total_ms"] / 1000.0) / 1e9 if prof["total_ms"] > 0 else None
+    return {"workload": f"full S2-Pro-shaped Dual-AR, batch 1, {len(prompt)}-token prompt, 4-bit weights "
+                        f"(late12attn plan: {len(keys)} of {5 * (cfg.n_layer + cfg.fast_n_layer)} block projections packed, "
+                        "group 128, bf16 scales), "
+                        "T=0.8 top-p 0.8 RAS window 10",
+            "value": frames / (ms / 1000.0), "unit": "frames/s", "steps": frames, "warmup": warmup,
+            "ms_per_step": ms / frames, "rtf": FRAMES_PER_AUDIO_SECOND / (frames / (ms / 1000.0)),
+            "packed_projections": len(keys), "frame_bytes_per_step": bytes_total / frames,
+            "frame_roofline": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
+            "gemv_roofline": {"kernel": "gemv_kernel (4-bit and bf16 weight-streaming GEMV)",
+                              "achieved": g_gbs, "peak": peak, "unit": "GB/s",
+                              "frac": (g_gbs / peak) if g_gbs else None,
+                              "launches": prof["launches"], "frames": n_prof,
+                              "bytes_per_frame": prof["total_bytes"] / n_prof,
+                              "ms_per_frame": prof["total_ms"] / n_prof},
+            "prefill_ms": prefill_ms, "gpu_launches_per_step": launches}
 
 
 def main():
@@ -381,6 +452,9 @@ def main():
     b64 = None
     if args.workload == "s2pro_b1" and not args.no_b64:
         b64 = measure_batch64(cfg, w, frames=24, warmup=4, peak=peak)
+    w4 = None
+    if args.workload in ("s2pro_b1", "s2pro_l1_b1") and not args.no_w4a16:
+        w4 = measure_w4a16(cfg, w, prompt, frames=64, warmup=8, peak=peak)
 
     cpu = None
     if rank == 0 and ws == 1 and bits is not None:
@@ -416,6 +490,7 @@ def main():
             "clocks": clocks,
             "cpu_baseline": cpu,
             "batch64": b64,
+            "w4a16": w4,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

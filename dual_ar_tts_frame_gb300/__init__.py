@@ -9,7 +9,7 @@ from .build import build  # noqa: F401
 
 def __getattr__(name):
     # the torch-based wrapper is imported on first use
-    if name in ("DualARDecoder", "Sampling", "upload_weights"):
+    if name in ("DualARDecoder", "Sampling", "upload_weights", "pack_w4a16", "late_attn_keys"):
         from . import decoder
         return getattr(decoder, name)
     raise AttributeError(name)

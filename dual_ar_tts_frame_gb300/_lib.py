@@ -28,6 +28,7 @@ EXPORTED = [
     "dualar_get_page_table", "dualar_get_rope_table", "dualar_read_state", "dualar_slot_length",
     "dualar_set_wait_limit", "dualar_last_launch_count", "dualar_set_persistent", "dualar_set_tensor_cores",
     "dualar_debug_barrier_extra", "dualar_debug_synthetic_context", "dualar_set_trace", "dualar_set_prefetch", "dualar_profile", "dualar_profile_read",
+    "dualar_w4a16_bytes", "dualar_quantize_w4a16", "dualar_set_w4a16",
 ]
 
 c_i32 = ctypes.c_int32
@@ -51,6 +52,10 @@ class dualar_weights(ctypes.Structure):
     _fields_ = [("tok_emb", c_vp), ("final_norm", c_vp), ("slow", ctypes.POINTER(dualar_layer_weights)),
                 ("fast_emb", c_vp), ("fast", ctypes.POINTER(dualar_layer_weights)),
                 ("fast_norm", c_vp), ("fast_out", c_vp), ("fusion", c_vp)]
+
+
+class dualar_w4a16_layer(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("wqkv", "wo", "w_gate", "w_up", "w_down")]
 
 
 class dualar_sampling(ctypes.Structure):
@@ -105,6 +110,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_profile.argtypes = [H, c_i32]
     L.dualar_profile_read.argtypes = [H, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    L.dualar_w4a16_bytes.argtypes = [c_i32, c_i32]
+    L.dualar_w4a16_bytes.restype = ctypes.c_int64
+    L.dualar_quantize_w4a16.argtypes = [c_vp, c_i32, c_i32, c_vp, c_vp]
+    L.dualar_set_w4a16.argtypes = [H, ctypes.POINTER(dualar_w4a16_layer), ctypes.POINTER(dualar_w4a16_layer)]
     for n in EXPORTED:
         getattr(L, n)
     _lib = L

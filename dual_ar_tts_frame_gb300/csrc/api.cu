@@ -63,6 +63,9 @@ struct dualar_handle {
   int mega_nprod[3] = {0, 0, 0};   // programs for batch 1, 2
   int mega_nops[3] = {0, 0, 0};
   bool mega_unsupported[3] = {false, false, false};
+  // packed 4-bit projections (dualar_set_w4a16); empty: all bf16
+  std::vector<dualar_w4a16_layer> slow_q, fast_q;
+  bool any_w4 = false;
 };
 
 namespace {
@@ -212,7 +215,7 @@ GemvArgs gemv_base(dualar_handle* h) {
 double gemv_bytes(const GemvArgs& a) {
   const double rows = (a.mode == GEMV_SWIGLU) ? 2.0 * a.n0 : static_cast<double>(a.n0 + a.n1);
   const double out_rows = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
-  double b = rows * a.K * 2.0;                       // weights
+  double b = rows * (a.w4 ? static_cast<double>(w4_row_bytes(a.K)) : a.K * 2.0);   // weights
   b += static_cast<double>(a.nb) * a.K * 4.0;        // x
   if (a.norm_w) b += a.K * 2.0;                      // norm gain
   b += static_cast<double>(a.nb) * out_rows * 4.0;   // y
@@ -240,7 +243,7 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
     }
     CUDA_TRY(h, cudaEventRecord(e0, h->stream));
   }
-  if (h->use_tc && tc_eligible(a, h->tc.ldx)) {
+  if (!a.w4 && h->use_tc && tc_eligible(a, h->tc.ldx)) {
     // 9..128 rows: one pass over the weights on the tensor cores.  The
     // SwiGLU output feeds the down projection without norm: its reduce
     // writes the halves the next GEMM reads, and that split is skipped.
@@ -404,16 +407,34 @@ GemvArgs args_head(dualar_handle* h, int r0, int n) {
 
 // One transformer block over nrows rows.  Slow blocks attend over the paged
 // cache; fast blocks over the per-frame codebook cache.
+// The packed 4-bit form of a projection, when dualar_set_w4a16 gave one.
+GemvArgs packed(GemvArgs a, const void* q0, const void* q1 = nullptr) {
+  if (q0 != nullptr) {
+    a.w0 = U16(q0);
+    if (q1 != nullptr) a.w1 = U16(q1);
+    a.w4 = 1;
+  }
+  return a;
+}
+
+const dualar_w4a16_layer* packed_layer(const dualar_handle* h, bool fast, int layer) {
+  const std::vector<dualar_w4a16_layer>& v = fast ? h->fast_q : h->slow_q;
+  return v.empty() ? nullptr : &v[layer];
+}
+
 int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast, int nrows,
           const float* xin, float* hres, int fast_pos, int units, int chunk, bool fuse_append) {
   const dualar_config& c = h->cfg;
   const DevPtrs& d = h->d;
+  static const dualar_w4a16_layer kNone{};
+  const dualar_w4a16_layer& lq = packed_layer(h, fast, layer) ? *packed_layer(h, fast, layer) : kNone;
   // decode: the attention writes the bf16 halves of its output for the o
   // projection (no split kernel between them)
-  TRY(run_gemv(h, args_qkv(h, lw, nrows, xin)));
+  TRY(run_gemv(h, packed(args_qkv(h, lw, nrows, xin), lq.wqkv)));
   AttnHalves hv{nullptr, nullptr, 0};
-  const GemvArgs ao = args_o(h, lw, nrows, xin, hres);
-  const bool o_halves = (fast || fuse_append) && h->use_tc && !h->profiling && tc_eligible(ao, h->tc.ldx);
+  const GemvArgs ao = packed(args_o(h, lw, nrows, xin, hres), lq.wo);
+  const bool o_halves =
+      (fast || fuse_append) && h->use_tc && !h->profiling && !ao.w4 && tc_eligible(ao, h->tc.ldx);
   if (o_halves) hv = AttnHalves{h->tc.xh, h->tc.xl, h->tc.ldx};
   bool halves_written = false;
   const bool qk = fast ? c.fast_qk_norm : c.slow_qk_norm;
@@ -436,8 +457,8 @@ int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast
     h->tc_ready_nb = ao.nb;
   }
   TRY(run_gemv(h, ao));
-  TRY(run_gemv(h, args_gateup(h, lw, nrows, hres)));
-  return run_gemv(h, args_down(h, lw, nrows, hres));
+  TRY(run_gemv(h, packed(args_gateup(h, lw, nrows, hres), lq.w_gate, lq.w_up)));
+  return run_gemv(h, packed(args_down(h, lw, nrows, hres), lq.w_down));
 }
 
 // The frame program of the persistent kernel for batch nb (same op order as
@@ -649,9 +670,10 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
                     smp->ras_top_p, smp->allow_eos};
   const int N = c.n_codebooks;
   LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
-  if (!per_op_only && h->use_mega && batch <= kTaggedRows && !h->mega_unsupported[batch] && !h->mega_ops[batch])
+  if (!per_op_only && h->use_mega && !h->any_w4 && batch <= kTaggedRows && !h->mega_unsupported[batch] &&
+      !h->mega_ops[batch])
     TRY(build_mega_program(h, batch));
-  if (!per_op_only && h->use_mega && batch <= kTaggedRows && !h->mega_unsupported[batch]) {
+  if (!per_op_only && h->use_mega && !h->any_w4 && batch <= kTaggedRows && !h->mega_unsupported[batch]) {
     // a new tag epoch per launch; when it would no longer fit its bits the
     // tagged buffers are cleared and the count starts again
     if (h->epoch + 1 >= (1u << (32 - kTagOpBits))) {
@@ -1314,6 +1336,59 @@ int32_t dualar_last_launch_count(const dualar_handle* h) { return h ? h->launche
 int dualar_set_persistent(dualar_handle* h, int32_t enable) {
   if (!h) return DUALAR_ERR_INVALID_ARG;
   h->use_mega = enable != 0;
+  return DUALAR_OK;
+}
+
+int64_t dualar_w4a16_bytes(int32_t n, int32_t k) {
+  if (n < 0 || k <= 0 || k % kW4Group) return -1;
+  return static_cast<int64_t>(n) * w4_row_bytes(k);
+}
+
+int dualar_quantize_w4a16(const void* w, int32_t n, int32_t k, void* out, void* cuda_stream) {
+  if (n < 0 || k <= 0 || k % kW4Group || (n > 0 && (!w || !out || !aligned16(w) || !aligned16(out))))
+    return DUALAR_ERR_INVALID_ARG;
+  const cudaError_t e = launch_quantize_w4(static_cast<const uint16_t*>(w), n, k, static_cast<unsigned char*>(out),
+                                           static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? DUALAR_OK : DUALAR_ERR_CUDA;
+}
+
+int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dualar_w4a16_layer* fast) {
+  if (!h) return DUALAR_ERR_INVALID_ARG;
+  const dualar_config& c = h->cfg;
+  const int qd = c.n_head * c.head_dim;
+  auto check = [&](const dualar_w4a16_layer* v, int n, const char* which) {
+    for (int i = 0; v && i < n; ++i) {
+      const dualar_w4a16_layer& l = v[i];
+      const void* ptrs[] = {l.wqkv, l.wo, l.w_gate, l.w_up, l.w_down};
+      for (const void* p : ptrs)
+        if (p && !aligned16(p)) {
+          set_err(h, "%s layer %d: a packed weight pointer is not 16-byte aligned", which, i);
+          return DUALAR_ERR_INVALID_ARG;
+        }
+      if ((l.w_gate == nullptr) != (l.w_up == nullptr)) {
+        set_err(h, "%s layer %d: w_gate and w_up must be packed together", which, i);
+        return DUALAR_ERR_INVALID_ARG;
+      }
+      const bool in_dim_ok = ((l.wqkv || l.w_gate) ? c.dim % kW4Group == 0 : true) &&
+                             (l.wo ? qd % kW4Group == 0 : true) && (l.w_down ? c.ffn % kW4Group == 0 : true);
+      if (!in_dim_ok) {
+        set_err(h, "%s layer %d: a packed projection's in-dimension is not a multiple of %d", which, i, kW4Group);
+        return DUALAR_ERR_INVALID_ARG;
+      }
+    }
+    return DUALAR_OK;
+  };
+  if (int rc = check(slow, c.n_layer, "slow")) return rc;
+  if (int rc = check(fast, c.fast_n_layer, "fast")) return rc;
+  if (const int frc = flush_tc(h)) return frc;
+  h->slow_q.clear();
+  h->fast_q.clear();
+  if (slow) h->slow_q.assign(slow, slow + c.n_layer);
+  if (fast) h->fast_q.assign(fast, fast + c.fast_n_layer);
+  h->any_w4 = false;
+  for (const auto* v : {&h->slow_q, &h->fast_q})
+    for (const dualar_w4a16_layer& l : *v)
+      if (l.wqkv || l.wo || l.w_gate || l.w_down) h->any_w4 = true;
   return DUALAR_OK;
 }
 

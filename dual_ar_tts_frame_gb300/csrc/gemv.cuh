@@ -44,21 +44,51 @@ __host__ __device__ inline bool gemv_k_supported(int K) {
   return (seg + 31) / 32 <= kMaxVecPerLane;
 }
 
+// ---- 4-bit weights (w4a16) ------------------------------------------------------
+// A packed matrix [n][K] (K a multiple of 128) is one record per output row,
+// records back to back:
+//   bytes [0, K/2)          byte i holds the codes of elements 2i (low nibble)
+//                           and 2i+1 (high nibble), each stored as u = q + 8
+//                           (q in [-8, 7]);
+//   bytes [K/2, K/2 + K/64) the bf16 scales of the K/128 groups of 128
+//                           consecutive elements;
+//   zero bytes up to a 16-byte multiple.
+// Element k of the row is (u_k - 8) * scale[k / 128].  A tile is R whole
+// records (one bulk copy); a lane reads 16-byte vectors of 32 elements, all
+// in one group.
+__host__ __device__ inline int w4_rows_per_tile(int K) {
+  int r = kWarpsC;
+  while (r > 1 && r * w4_row_bytes(K) > kStageBytes) r >>= 1;
+  return r;
+}
+
+__host__ __device__ inline bool w4_k_supported(int K) {
+  if (K <= 0 || K % kW4Group) return false;
+  const int R = w4_rows_per_tile(K);
+  if (R * w4_row_bytes(K) > kStageBytes) return false;
+  const int S = kWarpsC / R;
+  const int seg = (K / 32 + S - 1) / S;
+  return (seg + 31) / 32 <= kMaxVecPerLane;
+}
+
 struct GemvGeo {
   int v_begin, v_end;   // rows of this CTA (virtual row space)
   int R, S, seg;        // rows per tile, warps per row, vectors per segment
   bool swiglu;
 };
 
+// seg: 16-byte vectors per warp segment (8 bf16 elements, or 32 packed
+// 4-bit elements with W4).
+template <bool W4 = false>
 DEVI GemvGeo gemv_geo(const GemvArgs& a, int cta, int ncta) {
   GemvGeo g;
   g.swiglu = a.mode == GEMV_SWIGLU;
   const int nv = g.swiglu ? a.n0 : a.n0 + a.n1;
   g.v_begin = static_cast<int>((static_cast<long long>(cta) * nv) / ncta);
   g.v_end = static_cast<int>((static_cast<long long>(cta + 1) * nv) / ncta);
-  g.R = gemv_rows_per_tile(a.K);
+  g.R = W4 ? w4_rows_per_tile(a.K) : gemv_rows_per_tile(a.K);
   g.S = kWarpsC / g.R;
-  g.seg = (a.K / 8 + g.S - 1) / g.S;
+  g.seg = ((W4 ? a.K / 32 : a.K / 8) + g.S - 1) / g.S;
   return g;
 }
 
@@ -97,6 +127,21 @@ DEVI const uint16_t* gemv_tile_src(const GemvArgs& a, int row0, int part) {
                      : a.w1 + static_cast<size_t>(row0 - a.n0) * a.K;
 }
 
+// Bytes of one weight row, and where a tile starts (bf16 or packed 4-bit).
+template <bool W4>
+DEVI uint32_t gemv_row_bytes(int K) {
+  return W4 ? static_cast<uint32_t>(w4_row_bytes(K)) : static_cast<uint32_t>(K) * 2u;
+}
+template <bool W4>
+DEVI const void* gemv_tile_ptr(const GemvArgs& a, int row0, int part) {
+  if (!W4) return gemv_tile_src(a, row0, part);
+  const size_t rb = static_cast<size_t>(w4_row_bytes(a.K));
+  const unsigned char* w0 = reinterpret_cast<const unsigned char*>(a.w0);
+  const unsigned char* w1 = reinterpret_cast<const unsigned char*>(a.w1);
+  if (a.mode == GEMV_SWIGLU) return (part ? w1 : w0) + static_cast<size_t>(row0) * rb;
+  return row0 < a.n0 ? w0 + static_cast<size_t>(row0) * rb : w1 + static_cast<size_t>(row0 - a.n0) * rb;
+}
+
 struct GemvRing {
   uint64_t* full;
   uint64_t* empty;
@@ -117,6 +162,7 @@ struct GemvScratch {
 // Producer side: issues the tiles of one GEMV for this CTA.  t is the ring's
 // running tile counter (same convention as the consumers).  Returns false if
 // a wait gave up or the abort word is set (then nothing more is issued).
+template <bool W4 = false>
 DEVI bool gemv_produce(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
                        uint64_t pol, const volatile uint32_t* abort_word) {
   TileIter it(a, g);
@@ -135,9 +181,9 @@ DEVI bool gemv_produce(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
         }
       }
     }
-    const uint32_t bytes = static_cast<uint32_t>(rows) * a.K * 2;
+    const uint32_t bytes = static_cast<uint32_t>(rows) * gemv_row_bytes<W4>(a.K);
     mbar_arrive_expect_tx(&ring.full[s], bytes);
-    bulk_load_g2s(ring.base + static_cast<size_t>(s) * kStageBytes, gemv_tile_src(a, row0, part), bytes,
+    bulk_load_g2s(ring.base + static_cast<size_t>(s) * kStageBytes, gemv_tile_ptr<W4>(a, row0, part), bytes,
                   &ring.full[s], pol);
     ++t;
   }
@@ -146,11 +192,13 @@ DEVI bool gemv_produce(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
 
 // This CTA's weight rows (contiguous per segment) requested into L2, in 32 KB
 // pieces (rows of 2 K bytes: 16-byte multiples).
+template <bool W4 = false>
 DEVI void gemv_prefetch_rows(const GemvArgs& a, const GemvGeo& g) {
+  const size_t rb = gemv_row_bytes<W4>(a.K);
   auto range = [&](const uint16_t* base, int r0, int r1) {
     if (r1 <= r0) return;
-    const unsigned char* p = reinterpret_cast<const unsigned char*>(base + static_cast<size_t>(r0) * a.K);
-    const size_t bytes = static_cast<size_t>(r1 - r0) * a.K * 2;
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(base) + static_cast<size_t>(r0) * rb;
+    const size_t bytes = static_cast<size_t>(r1 - r0) * rb;
     for (size_t o = 0; o < bytes; o += 32768) {
       const size_t n = bytes - o < 32768 ? bytes - o : 32768;
       bulk_prefetch_l2(p + o, static_cast<uint32_t>(n));
@@ -207,9 +255,13 @@ DEVI float gemv_scale(const GemvArgs& a, const GemvPro<NB>& pr, int b) {
   return 1.0f / sqrtf(t / static_cast<float>(a.K) + a.eps);
 }
 
-template <int NB>
+// W4: x' goes to a split-32 layout instead (float4 t, elements 4t..4t+3, of
+// the 32-element vector v at float4 index t * (K/32) + v of the row), and
+// gsum[b][v] receives the sum of vector v's 32 values of x'; plain fp32 x
+// only (no tagged input).
+template <int NB, bool W4 = false>
 DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<NB>& pr, int cta,
-                       bool coherent, uint32_t epoch = 0) {
+                       bool coherent, uint32_t epoch = 0, float* gsum = nullptr) {
   constexpr int NCT = kWarpsC * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, KV = K >> 3;
@@ -245,36 +297,76 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
   const uint32_t xtag = a.x_src >= 0 ? op_tag(epoch, a.x_src) : 0u;
-  for (int j = tid; j < KV; j += NCT) {
-    // the gain is loaded before x is polled: the two round trips overlap
-    float gw[8];
-    if (norm) {
-      const uint4 gv = *reinterpret_cast<const uint4*>(a.norm_w + 8 * j);
-      gw[0] = bf16lo(gv.x); gw[1] = bf16hi(gv.x); gw[2] = bf16lo(gv.y); gw[3] = bf16hi(gv.y);
-      gw[4] = bf16lo(gv.z); gw[5] = bf16hi(gv.z); gw[6] = bf16lo(gv.w); gw[7] = bf16hi(gv.w);
-    } else {
+  if constexpr (W4) {
+    const int KV32 = K >> 5;
+    for (int j0 = 0; j0 < KV; j0 += NCT) {   // uniform trip count: the quad shuffles below
+      const int j = j0 + tid;
+      const bool act = j < KV;
+      float gw[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) gw[e] = 1.f;
-    }
+      if (norm && act) {
+        const uint4 gv = *reinterpret_cast<const uint4*>(a.norm_w + 8 * j);
+        gw[0] = bf16lo(gv.x); gw[1] = bf16hi(gv.x); gw[2] = bf16lo(gv.y); gw[3] = bf16hi(gv.y);
+        gw[4] = bf16lo(gv.z); gw[5] = bf16hi(gv.z); gw[6] = bf16lo(gv.w); gw[7] = bf16hi(gv.w);
+      }
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      if (b < a.nb) {
-        float v[8];
-        if (a.x_src >= 0) {
-          tag_wait<8>(reinterpret_cast<const uint64_t*>(a.x) + static_cast<size_t>(b) * a.ldx + 8 * j, xtag, v,
-                      a.err, a.wait_limit_ns);
-        } else {
+      for (int b = 0; b < NB; ++b) {
+        if (b >= a.nb) continue;   // uniform
+        float part = 0.f;
+        if (act) {
           const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
           const float4 v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
           const float4 v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
-          v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
-          v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+          const float4 p0 = make_float4(v0.x * gw[0], v0.y * gw[1], v0.z * gw[2], v0.w * gw[3]);
+          const float4 p1 = make_float4(v1.x * gw[4], v1.y * gw[5], v1.z * gw[6], v1.w * gw[7]);
+          // 8-vector j is quarter (j & 3) of 32-vector j >> 2: float4s 2(j&3), 2(j&3)+1
+          float4* x4 = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
+          const int t0 = 2 * (j & 3);
+          x4[t0 * KV32 + (j >> 2)] = p0;
+          x4[(t0 + 1) * KV32 + (j >> 2)] = p1;
+          ss[b] += v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w + v1.x * v1.x + v1.y * v1.y +
+                   v1.z * v1.z + v1.w * v1.w;
+          part = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w));
         }
-        float4* xa = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
-        xa[j] = make_float4(v[0] * gw[0], v[1] * gw[1], v[2] * gw[2], v[3] * gw[3]);
-        xa[KV + j] = make_float4(v[4] * gw[4], v[5] * gw[5], v[6] * gw[6], v[7] * gw[7]);
-        ss[b] += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3] + v[4] * v[4] + v[5] * v[5] +
-                 v[6] * v[6] + v[7] * v[7];
+        // the four 8-vectors of a 32-vector sit in lanes 4m .. 4m+3
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (act && (j & 3) == 0) gsum[b * KV32 + (j >> 2)] = part;
+      }
+    }
+  } else {
+    for (int j = tid; j < KV; j += NCT) {
+      // the gain is loaded before x is polled: the two round trips overlap
+      float gw[8];
+      if (norm) {
+        const uint4 gv = *reinterpret_cast<const uint4*>(a.norm_w + 8 * j);
+        gw[0] = bf16lo(gv.x); gw[1] = bf16hi(gv.x); gw[2] = bf16lo(gv.y); gw[3] = bf16hi(gv.y);
+        gw[4] = bf16lo(gv.z); gw[5] = bf16hi(gv.z); gw[6] = bf16lo(gv.w); gw[7] = bf16hi(gv.w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gw[e] = 1.f;
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < a.nb) {
+          float v[8];
+          if (a.x_src >= 0) {
+            tag_wait<8>(reinterpret_cast<const uint64_t*>(a.x) + static_cast<size_t>(b) * a.ldx + 8 * j, xtag, v,
+                        a.err, a.wait_limit_ns);
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
+            const float4 v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
+            const float4 v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
+            v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+            v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+          }
+          float4* xa = reinterpret_cast<float4*>(xs + static_cast<size_t>(b) * K);
+          xa[j] = make_float4(v[0] * gw[0], v[1] * gw[1], v[2] * gw[2], v[3] * gw[3]);
+          xa[KV + j] = make_float4(v[4] * gw[4], v[5] * gw[5], v[6] * gw[6], v[7] * gw[7]);
+          ss[b] += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3] + v[4] * v[4] + v[5] * v[5] +
+                   v[6] * v[6] + v[7] * v[7];
+        }
       }
     }
   }
@@ -460,6 +552,115 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
     }
   }
   if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch);
+  return true;
+}
+
+// ---- 4-bit consumer ------------------------------------------------------------
+// Element k of a packed row as the float 128 + u_k (u_k its stored nibble,
+// 0..15): the nibble is moved to bits 16..19 and the exponent and mantissa of
+// 128.0f (0x43000000) are OR-ed in, so no integer-to-float conversion is
+// needed.  e is the element's place in its 32-bit word (8 elements).
+template <int E>
+DEVI float w4_val128(uint32_t word) {
+  const uint32_t s = E <= 4 ? (word << (16 - 4 * E)) : (word >> (4 * E - 16));
+  return __uint_as_float((s & 0x000F0000u) | 0x43000000u);
+}
+
+// Sum over the 8 elements of one word: (128 + u_e) * x_e.
+DEVI float w4_dot8(uint32_t word, const float4 xa, const float4 xb) {
+  float s = w4_val128<0>(word) * xa.x;
+  s = fmaf(w4_val128<1>(word), xa.y, s);
+  s = fmaf(w4_val128<2>(word), xa.z, s);
+  s = fmaf(w4_val128<3>(word), xa.w, s);
+  s = fmaf(w4_val128<4>(word), xb.x, s);
+  s = fmaf(w4_val128<5>(word), xb.y, s);
+  s = fmaf(w4_val128<6>(word), xb.z, s);
+  s = fmaf(w4_val128<7>(word), xb.w, s);
+  return s;
+}
+
+// Consumer side of a GEMV over packed 4-bit rows: like gemv_consume, with a
+// lane's 16-byte vector holding 32 elements of one 128-element group.  For
+// vector v of row n and batch row b,
+//   sum_k (u_k - 8) s x'_k = s (sum_k (128 + u_k) x'_k - 136 gsum[b][v]),
+// with the 32-term sum in fp32 (its terms are at most 143 |x'_k|, and the
+// difference keeps about 2^-24 * 143 * 32 of relative error -- far below the
+// bf16 rounding of the weights themselves).  x' in the split-32 layout of
+// gemv_stage_x<NB, true>.
+template <int NB>
+DEVI bool gemv_consume_w4(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
+                          const float* xs, const float* gsum, GemvScratch<NB>& sc, const GemvPro<NB>& pr) {
+  constexpr int kWin = GemvScratch<NB>::kPartTiles;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = a.K, KV32 = K >> 5;
+  const int rb = w4_row_bytes(K);
+  const int r = warp / g.S, sg = warp % g.S;
+  const int v0 = sg * g.seg;
+  const int nvec = max(0, min(g.seg, KV32 - v0));
+  TileIter it(a, g);
+  int row0, rows, part;
+  int tw = 0;
+  while (it.next(row0, rows, part)) {
+    const int s = static_cast<int>(t % ring.stages);
+    if (!mbar_wait(&ring.full[s], (t / ring.stages) & 1, a.err, a.wait_limit_ns)) return false;
+    const bool mine = r < rows;
+    float p[NB];
+    if (mine) {
+      const unsigned char* rec = ring.base + static_cast<size_t>(s) * kStageBytes + static_cast<size_t>(r) * rb;
+      const uint4* wr = reinterpret_cast<const uint4*>(rec) + v0;
+      const uint16_t* scl = reinterpret_cast<const uint16_t*>(rec + K / 2);
+      uint4 w[kMaxVecPerLane];
+      float sv[kMaxVecPerLane];
+#pragma unroll
+      for (int q = 0; q < kMaxVecPerLane; ++q) {
+        const int j = lane + 32 * q;
+        w[q] = j < nvec ? wr[j] : make_uint4(0u, 0u, 0u, 0u);
+        sv[q] = j < nvec ? bf16bits_to_f32(scl[(v0 + j) >> 2]) : 0.f;
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        p[b] = 0.f;
+        if (b >= a.nb) continue;
+        const float4* x4 = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K);
+        const float* gs = gsum + static_cast<size_t>(b) * KV32;
+#pragma unroll
+        for (int q = 0; q < kMaxVecPerLane; ++q) {
+          const int j = lane + 32 * q;
+          if (j < nvec) {
+            const int v = v0 + j;
+            // four independent 8-term chains, then the group correction
+            const float d0 = w4_dot8(w[q].x, x4[0 * KV32 + v], x4[1 * KV32 + v]);
+            const float d1 = w4_dot8(w[q].y, x4[2 * KV32 + v], x4[3 * KV32 + v]);
+            const float d2 = w4_dot8(w[q].z, x4[4 * KV32 + v], x4[5 * KV32 + v]);
+            const float d3 = w4_dot8(w[q].w, x4[6 * KV32 + v], x4[7 * KV32 + v]);
+            const float dv = fmaf(-136.f, gs[v], (d0 + d1) + (d2 + d3));
+            p[b] = fmaf(sv[q], dv, p[b]);
+          }
+        }
+      }
+    }
+    // the stage is free once every lane's reads of it are done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[s]);
+    ++t;
+    if (mine) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) p[b] = warp_sum(p[b]);
+      if (lane < NB) {
+        float y = p[0];
+#pragma unroll
+        for (int b = 1; b < NB; ++b)
+          if (lane == b) y = p[b];
+        sc.part[tw][warp][lane] = y;
+      }
+    }
+    if (threadIdx.x == 0) sc.tile[tw] = make_int2(row0, rows);
+    if (++tw == kWin) {
+      gemv_flush<NB>(a, g, sc, pr, tw, true, 0);
+      tw = 0;
+    }
+  }
+  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, 0);
   return true;
 }
 

@@ -70,6 +70,12 @@ struct LaunchSetup {
   int32_t tokens[kMaxRows];          // prefill ids (unused in decode)
 };
 
+// 4-bit weights: elements per scale group, and bytes of one packed row of K
+// elements (K/2 code bytes, K/128 bf16 scales, zero padding to 16 bytes; the
+// layout is described in gemv.cuh, "4-bit weights").
+constexpr int kW4Group = 128;
+__host__ __device__ inline int w4_row_bytes(int K) { return K / 2 + ((K / 64 + 15) & ~15); }
+
 enum GemvMode : int { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2 };
 
 struct GemvArgs {
@@ -98,6 +104,9 @@ struct GemvArgs {
   // the pointer is a tagged 64-bit buffer (common.cuh, "tagged activations")
   // with the same element strides.
   int x_src, base_src, out_src;
+  // 1: w0 / w1 hold 4-bit packed weights (gemv.cuh, "4-bit weights")
+  // instead of bf16; standalone GEMV only.
+  int w4;
 };
 
 // Device buffers of one handle that kernels need (plain pointers).
@@ -186,6 +195,8 @@ struct AttnHalves {
 cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t* tok_emb,
                          cudaStream_t st);
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st);
+// Packs a bf16 matrix [n][K] (K % 128 == 0) into 4-bit records (gemv.cuh).
+cudaError_t launch_quantize_w4(const uint16_t* w, int n, int K, unsigned char* out, cudaStream_t st);
 cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int fast_pos,
                           const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st);
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,

@@ -152,21 +152,24 @@ __host__ __device__ inline size_t gemv_pro_off(int nbt) {
 __host__ __device__ inline size_t gemv_xs_off(int nbt) {
   return (gemv_pro_off(nbt) + sizeof(GemvPro<8>) + 127) & ~size_t(127);
 }
-__host__ __device__ inline size_t gemv_ring_off(int nbt, int K) {
-  return (gemv_xs_off(nbt) + sizeof(float) * size_t(nbt) * K + 127) & ~size_t(127);
+// W4: the x rows are followed by the 32-element sums of x' ([nbt][K/32]).
+__host__ __device__ inline size_t gemv_ring_off(int nbt, int K, bool w4 = false) {
+  const size_t xf = size_t(nbt) * K + (w4 ? size_t(nbt) * (K / 32) : 0);
+  return (gemv_xs_off(nbt) + sizeof(float) * xf + 127) & ~size_t(127);
 }
 
-template <int NB>
+template <int NB, bool W4>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a, const int stages) {
   extern __shared__ __align__(128) unsigned char smem[];
   GemvRing ring;
   ring.full = reinterpret_cast<uint64_t*>(smem);
   ring.empty = ring.full + kMaxStagesRing;
-  ring.base = smem + gemv_ring_off(NB, a.K);
+  ring.base = smem + gemv_ring_off(NB, a.K, W4);
   ring.stages = stages;
   GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + gemv_scratch_off());
   GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + gemv_pro_off(NB));
   float* xs = reinterpret_cast<float*>(smem + gemv_xs_off(NB));
+  float* gsum = xs + static_cast<size_t>(NB) * a.K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -177,15 +180,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  const GemvGeo g = gemv_geo(a, blockIdx.x, gridDim.x);
+  const GemvGeo g = gemv_geo<W4>(a, blockIdx.x, gridDim.x);
   uint32_t t = 0;
   if (warp == kGemvConsumerWarps) {
     // the weights are constant: this CTA's rows are requested into L2 and
     // streamed into the ring while the previous kernel may still run (the
     // consumers wait for it before reading x)
     if (lane == 0) {
-      gemv_prefetch_rows(a, g);
-      gemv_produce(a, g, ring, t, policy_evict_first(), nullptr);
+      gemv_prefetch_rows<W4>(a, g);
+      gemv_produce<W4>(a, g, ring, t, policy_evict_first(), nullptr);
       gemv_drain(ring, t, a.wait_limit_ns);
     }
     pdl_wait();
@@ -193,8 +196,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   }
   pdl_wait();
   pdl_launch();
-  gemv_stage_x<NB>(a, g, xs, pro, blockIdx.x, false);
-  gemv_consume<NB>(a, g, ring, t, xs, scr, pro);
+  if constexpr (W4) {
+    gemv_stage_x<NB, true>(a, g, xs, pro, blockIdx.x, false, 0, gsum);
+    gemv_consume_w4<NB>(a, g, ring, t, xs, gsum, scr, pro);
+  } else {
+    gemv_stage_x<NB>(a, g, xs, pro, blockIdx.x, false);
+    gemv_consume<NB>(a, g, ring, t, xs, scr, pro);
+  }
 }
 
 struct GemvPlan {
@@ -203,11 +211,11 @@ struct GemvPlan {
   size_t smem;
 };
 
-static GemvPlan plan_gemv(int K, int nb) {
+static GemvPlan plan_gemv(int K, int nb, bool w4) {
   GemvPlan p;
   int nbt = nb >= 8 ? 8 : nb >= 4 ? 4 : nb >= 2 ? 2 : 1;
   while (true) {
-    const size_t ring = gemv_ring_off(nbt, K);
+    const size_t ring = gemv_ring_off(nbt, K, w4);
     const long long room = static_cast<long long>(kSmemBudget) - static_cast<long long>(ring);
     const int st = room > 0 ? static_cast<int>(room / kStageBytes) : 0;
     if (st >= 2 || nbt == 1) {
@@ -220,22 +228,39 @@ static GemvPlan plan_gemv(int K, int nb) {
   }
 }
 
-template <int NB>
+template <int NB, bool W4>
 static cudaError_t launch_gemv_nb(const GemvArgs& a, const GemvPlan& p, int grid, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, W4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBudget);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(gemv_kernel<NB>, dim3(grid), dim3(kGemvThreads), p.smem, st, a, p.stages);
+  return launch_pdl(gemv_kernel<NB, W4>, dim3(grid), dim3(kGemvThreads), p.smem, st, a, p.stages);
+}
+
+template <bool W4>
+static cudaError_t launch_gemv_fmt(const GemvArgs& s, const GemvPlan& p, int grid, cudaStream_t st) {
+  switch (p.nbt) {
+    case 8: return launch_gemv_nb<8, W4>(s, p, grid, st);
+    case 4: return launch_gemv_nb<4, W4>(s, p, grid, st);
+    case 2: return launch_gemv_nb<2, W4>(s, p, grid, st);
+    default: return launch_gemv_nb<1, W4>(s, p, grid, st);
+  }
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
   if (a.nb <= 0) return cudaSuccess;
-  if (a.K % 8 != 0 || !gemv_k_supported(a.K)) return cudaErrorInvalidValue;
-  const GemvPlan p = plan_gemv(a.K, a.nb);
+  const bool w4 = a.w4 != 0;
+  if (w4) {
+    // packed 4-bit rows: plain fp32 input, no saved x (gemv_stage_x<NB, true>)
+    if (!w4_k_supported(a.K) || a.x_src >= 0 || a.base_src >= 0 || a.out_src >= 0 || a.save_x != nullptr)
+      return cudaErrorInvalidValue;
+  } else if (a.K % 8 != 0 || !gemv_k_supported(a.K)) {
+    return cudaErrorInvalidValue;
+  }
+  const GemvPlan p = plan_gemv(a.K, a.nb, w4);
   if (p.stages < 1 || p.smem > static_cast<size_t>(kSmemBudget)) return cudaErrorInvalidValue;
   const int nv = (a.mode == GEMV_SWIGLU) ? a.n0 : a.n0 + a.n1;
   const int grid = nv < n_sm ? nv : n_sm;
@@ -253,16 +278,59 @@ cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
       if (a.save_map) s.save_map = a.save_map + g0;
       else s.save_x = a.save_x + static_cast<size_t>(g0) * a.lds;
     }
-    cudaError_t e;
-    switch (p.nbt) {
-      case 8: e = launch_gemv_nb<8>(s, p, grid, st); break;
-      case 4: e = launch_gemv_nb<4>(s, p, grid, st); break;
-      case 2: e = launch_gemv_nb<2>(s, p, grid, st); break;
-      default: e = launch_gemv_nb<1>(s, p, grid, st); break;
-    }
+    const cudaError_t e = w4 ? launch_gemv_fmt<true>(s, p, grid, st) : launch_gemv_fmt<false>(s, p, grid, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// ============================================================================
+// 4-bit weight packing (w4a16; record layout in gemv.cuh, "4-bit weights")
+// ============================================================================
+// One warp per (row, group of 128 elements); lane l quantizes elements
+// 4l .. 4l+3 of the group.  Symmetric absolute-maximum rule: m = max |w| over
+// the group, scale s = bf16(m / 7) (fp32 division, round to nearest even),
+// q = clamp(rint(w / s), -8, 7) (q = 0 when s = 0), stored as q + 8.
+__global__ void quantize_w4_kernel(const uint16_t* w, int n, int K, unsigned char* out) {
+  const int gpr = K / kW4Group;
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<long long>(n) * gpr) return;   // whole warps leave together
+  const int row = static_cast<int>(wid / gpr), grp = static_cast<int>(wid % gpr);
+  const uint2 raw =
+      *reinterpret_cast<const uint2*>(w + static_cast<size_t>(row) * K + static_cast<size_t>(grp) * kW4Group + 4 * lane);
+  const float v[4] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y)};
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const uint16_t sbits = f32_to_bf16bits(m / 7.0f);
+  const float sc = bf16bits_to_f32(sbits);
+  uint32_t u[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float qf = sc > 0.f ? rintf(v[e] / sc) : 0.f;
+    qf = fminf(fmaxf(qf, -8.f), 7.f);
+    u[e] = static_cast<uint32_t>(static_cast<int>(qf) + 8);
+  }
+  const size_t rb = static_cast<size_t>(w4_row_bytes(K));
+  unsigned char* rec = out + static_cast<size_t>(row) * rb;
+  const uint16_t packed = static_cast<uint16_t>(u[0] | (u[1] << 4) | (u[2] << 8) | (u[3] << 12));
+  *reinterpret_cast<uint16_t*>(rec + grp * (kW4Group / 2) + 2 * lane) = packed;
+  if (lane == 0) *reinterpret_cast<uint16_t*>(rec + K / 2 + 2 * grp) = sbits;
+  if (grp == 0) {
+    const int pad0 = K / 2 + 2 * gpr;
+    for (int i = pad0 + lane; i < static_cast<int>(rb); i += 32) rec[i] = 0;
+  }
+}
+
+cudaError_t launch_quantize_w4(const uint16_t* w, int n, int K, unsigned char* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (K <= 0 || K % kW4Group) return cudaErrorInvalidValue;
+  const long long warps = static_cast<long long>(n) * (K / kW4Group);
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  quantize_w4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(w, n, K, out);
+  return cudaGetLastError();
 }
 
 // ============================================================================

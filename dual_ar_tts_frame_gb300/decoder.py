@@ -37,6 +37,38 @@ def upload_weights(bits: dict[str, np.ndarray], device="cuda") -> dict[str, torc
     return out
 
 
+PROJECTIONS = ("wqkv", "wo", "w_gate", "w_up", "w_down")
+
+
+def late_attn_keys(n_layer: int, fast_n_layer: int, n_bf16_attn: int = 12) -> list[str]:
+    """Weight names packed in the "late12attn" 4-bit variant (the model card
+    "s2-pro-w4a16-late12attn"): every projection except the query/key/value
+    and output projections of the last n_bf16_attn slow layers."""
+    out = []
+    for i in range(n_layer):
+        late = i >= n_layer - n_bf16_attn
+        out += [f"slow.{i}.{m}" for m in PROJECTIONS if not (late and m in ("wqkv", "wo"))]
+    out += [f"fast.{i}.{m}" for i in range(fast_n_layer) for m in PROJECTIONS]
+    return out
+
+
+def pack_w4a16(w: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """bf16 device matrix [n][k] -> its packed 4-bit records (uint8 [n][record
+    bytes]) via dualar_quantize_w4a16, queued on the stream."""
+    lib = L.lib()
+    n, k = w.shape
+    nbytes = lib.dualar_w4a16_bytes(n, k)
+    if nbytes < 0:
+        raise L.DualARError(-1, f"dualar_w4a16_bytes({n}, {k}): k must be a positive multiple of 128")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    st = stream or torch.cuda.current_stream()
+    rc = lib.dualar_quantize_w4a16(ctypes.c_void_p(w.contiguous().data_ptr()), n, k,
+                                   ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(st.cuda_stream))
+    if rc != L.DUALAR_OK:
+        raise L.DualARError(rc, "dualar_quantize_w4a16 failed")
+    return out.view(n, nbytes // max(n, 1)) if n else out
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
@@ -80,6 +112,28 @@ class DualARDecoder:
         if rc != L.DUALAR_OK:
             raise L.DualARError(rc, "dualar_create failed (message on stderr)")
         self.h = h
+
+    def set_w4a16(self, packed: dict[str, torch.Tensor] | None) -> None:
+        """Reads the named projections ("slow.3.w_down", ...) from their packed
+        4-bit records (pack_w4a16) from now on; None or {} restores bf16."""
+        packed = packed or {}
+        cfg = self.cfg
+
+        def layers(stack, n):
+            arr = (L.dualar_w4a16_layer * n)()
+            for i in range(n):
+                for m in PROJECTIONS:
+                    t = packed.get(f"{stack}.{i}.{m}")
+                    if t is not None:
+                        setattr(arr[i], m, t.data_ptr())
+            return arr
+
+        any_slow = any(k.startswith("slow.") for k in packed)
+        any_fast = any(k.startswith("fast.") for k in packed)
+        slow = layers("slow", cfg.n_layer) if any_slow else None
+        fast = layers("fast", cfg.fast_n_layer) if any_fast else None
+        self._check(self.lib.dualar_set_w4a16(self.h, slow, fast))
+        self.packed = dict(packed)    # keeps the device memory alive
 
     # ---- helpers ----------------------------------------------------------
     def _check(self, rc: int):

@@ -22,6 +22,8 @@
  *        1/sqrt(N+1) scale), "The slow AR is Qwen3-4B" (Qwen3 layer,
  *        qk-norm, rope_base, tied head, semantic id range), "Streaming"
  *        (bf16 RoPE tables).
+ *   [P3] "s2-pro-w4a16-late12attn" (model card) -- its opening line: the
+ *        4-bit-weight variant that keeps the late 12 attention layers bf16.
  *
  * Conventions for every call:
  *   - Return value: DUALAR_OK (0) or a negative DUALAR_ERR_* code.  Nothing
@@ -240,6 +242,59 @@ int dualar_share_prefix(dualar_handle* h, int32_t src, int32_t dst, int32_t n_to
  * last of them.  tokens: host int32[n_tokens].  Errors: INVALID_ARG,
  * SLOT_EMPTY, OOM_PAGES, CONTEXT_FULL, CUDA. */
 int dualar_prefill_append(dualar_handle* h, int32_t slot, const int32_t* tokens, int32_t n_tokens);
+
+/* ---- 4-bit weights (w4a16) --------------------------------------------
+ * [P3] "s2-pro-w4a16-late12attn" (model card): the S2-Pro checkpoint with
+ * 4-bit weights and 16-bit activations, keeping the attention of the late 12
+ * slow layers in bf16.  The card gives no packing format; this library's:
+ * a matrix [n][k] (k a positive multiple of 128) becomes n records, one per
+ * output row, of k/2 + roundup(k/64, 16) bytes:
+ *   bytes [0, k/2)            byte i holds the codes of elements 2i (low
+ *                             nibble) and 2i+1 (high nibble), each stored as
+ *                             u = q + 8 with q in [-8, 7];
+ *   bytes [k/2, k/2 + k/64)   the bf16 scale of each group of 128 consecutive
+ *                             elements (little-endian);
+ *   the rest                  zero.
+ * Element j of a row stands for (u_j - 8) * scale[j / 128].  Activations
+ * stay fp32 (at least the 16 bits the name asks for). */
+
+/* Bytes of the packed form of a [n][k] matrix; -1 if n < 0 or k is not a
+ * positive multiple of 128. */
+int64_t dualar_w4a16_bytes(int32_t n, int32_t k);
+
+/* Packs a bf16 matrix into the format above, on cuda_stream (a cudaStream_t,
+ * NULL = legacy default stream), asynchronously.  Each group of 128 takes
+ * scale s = bf16(m / 7) with m its largest |w| (fp32 division, round to
+ * nearest even) and q = clamp(rint(w / s), -8, 7) (0 when s = 0).
+ *   w:   device bf16 [n][k], 16-byte aligned
+ *   out: device, dualar_w4a16_bytes(n, k) bytes, 16-byte aligned
+ * Finite weights only.  Errors: INVALID_ARG (sizes, NULL or unaligned
+ * pointers), CUDA. */
+int dualar_quantize_w4a16(const void* w, int32_t n, int32_t k, void* out, void* cuda_stream);
+
+/* Packed projections of one transformer block (device pointers from
+ * dualar_quantize_w4a16 of the bf16 matrix of the same name, which keeps its
+ * shape [out][in]); NULL keeps that projection in bf16.  w_gate and w_up are
+ * both packed or both NULL. */
+typedef struct dualar_w4a16_layer {
+  const void* wqkv;
+  const void* wo;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+} dualar_w4a16_layer;
+
+/* Makes the decoder read the given projections from their packed form from
+ * the next call on (the caller keeps them valid until they are replaced or
+ * the handle is destroyed).  slow: host array [n_layer] or NULL (all bf16);
+ * fast: host array [fast_n_layer] or NULL.  Embeddings, norms and both heads
+ * stay bf16.  While any projection is packed, decode runs one kernel per op
+ * (not the persistent frame kernel) and packed projections use the
+ * weight-streaming GEMV at every batch size, in passes of at most 8 rows.
+ * Both arrays NULL restores the all-bf16 decoder.  Errors: INVALID_ARG (an
+ * unaligned pointer, a gate without its up matrix, an in-dimension that is
+ * not a multiple of 128). */
+int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dualar_w4a16_layer* fast);
 
 /* Synchronises the handle's stream and reports device-side errors:
  * DUALAR_ERR_TIMEOUT if a bounded wait gave up, DUALAR_ERR_DEVICE if a bounds

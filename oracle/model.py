@@ -251,9 +251,19 @@ class FrameResult:
 
 class DualAROracle:
     def __init__(self, cfg: DualARConfig, weight_bits: dict[str, np.ndarray],
-                 max_pos: int = 20_000):
+                 max_pos: int = 20_000, w4a16_keys: list[str] | None = None):
+        """w4a16_keys: projections (generator keys such as "slow.0.wqkv") that
+        the model reads through the 4-bit rule of oracle.w4a16 ([P3]
+        "s2-pro-w4a16-late12attn", opening line): each such matrix is
+        replaced by its quantised-then-dequantised float32 values."""
         self.cfg = cfg
         self.w = Weights(cfg, weight_bits)
+        if w4a16_keys:
+            from .w4a16 import dequantize, quantize
+            for key in w4a16_keys:
+                stack, i, name = key.split(".")
+                layer = (self.w.slow if stack == "slow" else self.w.fast)[int(i)]
+                setattr(layer, name, dequantize(*quantize(weight_bits[key])))
         self.cos, self.sin = rope_table(max(max_pos, cfg.n_codebooks), cfg.head_dim, cfg.rope_base)
         self.rep = cfg.n_head // cfg.n_kv_head
 

@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dualar_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dualar_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_names():
@@ -91,3 +91,27 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.dualar_sync(None) == -1
     assert lib.dualar_slot_length(None, 0) == -1
     lib.dualar_destroy(None)
+
+
+def test_w4a16_layout_and_argument_checks_without_gpu(lib):
+    """Packed 4-bit records: k/2 code bytes + k/128 bf16 scales padded to 16
+    bytes per row; sizes and pointers are checked before any GPU work."""
+    assert lib.dualar_w4a16_bytes(1, 128) == 80
+    assert lib.dualar_w4a16_bytes(2560, 9728) == 2560 * (4864 + 160)
+    assert lib.dualar_w4a16_bytes(6144, 2560) == 6144 * (1280 + 48)
+    assert lib.dualar_w4a16_bytes(0, 256) == 0
+    for n, k in ((1, 100), (1, 0), (-1, 128), (3, 192)):
+        assert lib.dualar_w4a16_bytes(n, k) == -1
+    assert lib.dualar_quantize_w4a16(None, 4, 100, None, None) == -1     # k not a multiple of 128
+    assert lib.dualar_quantize_w4a16(None, 4, 128, None, None) == -1     # NULL pointers
+    assert lib.dualar_quantize_w4a16(16, 4, 128, 40, None) == -1         # unaligned output
+    assert lib.dualar_quantize_w4a16(None, 0, 128, None, None) == 0      # nothing to do
+    assert lib.dualar_set_w4a16(None, None, None) == -1
+    assert ctypes.sizeof(L.dualar_w4a16_layer) == 5 * ctypes.sizeof(ctypes.c_void_p)
+
+
+def test_late_attn_keys_agree_with_oracle():
+    from dual_ar_tts_frame_gb300.decoder import late_attn_keys
+    from oracle import w4a16
+    for n, f, b in ((36, 4, 12), (2, 2, 1), (2, 2, 0), (2, 2, 2)):
+        assert sorted(late_attn_keys(n, f, b)) == sorted(w4a16.late_attn_keys(n, f, b))
