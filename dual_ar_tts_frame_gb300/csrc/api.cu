@@ -417,17 +417,18 @@ GemvArgs packed(GemvArgs a, const void* q0, const void* q1 = nullptr) {
   return a;
 }
 
-const dualar_w4a16_layer* packed_layer(const dualar_handle* h, bool fast, int layer) {
+// The packed projections of a block (all NULL when none were given).
+const dualar_w4a16_layer& packed_or_none(const dualar_handle* h, bool fast, int layer) {
+  static const dualar_w4a16_layer kNone{};
   const std::vector<dualar_w4a16_layer>& v = fast ? h->fast_q : h->slow_q;
-  return v.empty() ? nullptr : &v[layer];
+  return v.empty() ? kNone : v[layer];
 }
 
 int block(dualar_handle* h, const dualar_layer_weights& lw, int layer, bool fast, int nrows,
           const float* xin, float* hres, int fast_pos, int units, int chunk, bool fuse_append) {
   const dualar_config& c = h->cfg;
   const DevPtrs& d = h->d;
-  static const dualar_w4a16_layer kNone{};
-  const dualar_w4a16_layer& lq = packed_layer(h, fast, layer) ? *packed_layer(h, fast, layer) : kNone;
+  const dualar_w4a16_layer& lq = packed_or_none(h, fast, layer);
   // decode: the attention writes the bf16 halves of its output for the o
   // projection (no split kernel between them)
   TRY(run_gemv(h, packed(args_qkv(h, lw, nrows, xin), lq.wqkv)));
@@ -512,13 +513,16 @@ int build_mega_program(dualar_handle* h, int nb) {
     float* xin = F(d.fin_t + static_cast<size_t>(p) * kTaggedRows * D);
     for (int l = 0; l < c.fast_n_layer; ++l) {
       const dualar_layer_weights& lw = h->fast[l];
+      const dualar_w4a16_layer& lq = packed_or_none(h, true, l);
       float* x = l == 0 ? xin : F(d.hf_t);
       const int x_src = l == 0 ? fin_src[p] : hf_src;
-      const int qkv = gemv(args_qkv(h, lw, nb, nullptr), x, x_src, nullptr, -1, F(d.qkv_t), true);
+      const int qkv = gemv(packed(args_qkv(h, lw, nb, nullptr), lq.wqkv), x, x_src, nullptr, -1, F(d.qkv_t), true);
       const int at = attn_op(MOP_ATTN_FAST, l, p, qkv, c.fast_qk_norm, lw);
-      hf_src = gemv(args_o(h, lw, nb, nullptr, nullptr), F(d.attn_t), at, x, x_src, F(d.hf_t), true);
-      const int act = gemv(args_gateup(h, lw, nb, nullptr), F(d.hf_t), hf_src, nullptr, -1, F(d.act_t), true);
-      hf_src = gemv(args_down(h, lw, nb, nullptr), F(d.act_t), act, F(d.hf_t), hf_src, F(d.hf_t), true);
+      hf_src = gemv(packed(args_o(h, lw, nb, nullptr, nullptr), lq.wo), F(d.attn_t), at, x, x_src, F(d.hf_t), true);
+      const int act = gemv(packed(args_gateup(h, lw, nb, nullptr), lq.w_gate, lq.w_up), F(d.hf_t), hf_src,
+                           nullptr, -1, F(d.act_t), true);
+      hf_src = gemv(packed(args_down(h, lw, nb, nullptr), lq.w_down), F(d.act_t), act, F(d.hf_t), hf_src,
+                    F(d.hf_t), true);
     }
     if (p == 0) continue;
     const int head = gemv(args_fast_head(h, nb), F(d.hf_t), hf_src, nullptr, -1, F(d.logits_t), true);
@@ -528,14 +532,17 @@ int build_mega_program(dualar_handle* h, int nb) {
   int hs_src = push(op(MOP_FUSION, 0, 0, -1));
   for (int l = 0; l < c.n_layer; ++l) {
     const dualar_layer_weights& lw = h->slow[l];
+    const dualar_w4a16_layer& lq = packed_or_none(h, false, l);
     float* x = l == 0 ? F(d.xs_t) : F(d.hs_t);
     const int x_src = hs_src;
-    const int qkv = gemv(args_qkv(h, lw, nb, nullptr), x, x_src, nullptr, -1, F(d.qkv_t), true);
+    const int qkv = gemv(packed(args_qkv(h, lw, nb, nullptr), lq.wqkv), x, x_src, nullptr, -1, F(d.qkv_t), true);
     ops[qkv].pos = l + 1;   // its attention's first pages are fetched during it
     const int at = attn_op(MOP_ATTN_PAGED, l, 0, qkv, c.slow_qk_norm, lw);
-    hs_src = gemv(args_o(h, lw, nb, nullptr, nullptr), F(d.attn_t), at, x, x_src, F(d.hs_t), true);
-    const int act = gemv(args_gateup(h, lw, nb, nullptr), F(d.hs_t), hs_src, nullptr, -1, F(d.act_t), true);
-    hs_src = gemv(args_down(h, lw, nb, nullptr), F(d.act_t), act, F(d.hs_t), hs_src, F(d.hs_t), true);
+    hs_src = gemv(packed(args_o(h, lw, nb, nullptr, nullptr), lq.wo), F(d.attn_t), at, x, x_src, F(d.hs_t), true);
+    const int act = gemv(packed(args_gateup(h, lw, nb, nullptr), lq.w_gate, lq.w_up), F(d.hs_t), hs_src, nullptr,
+                         -1, F(d.act_t), true);
+    hs_src = gemv(packed(args_down(h, lw, nb, nullptr), lq.w_down), F(d.act_t), act, F(d.hs_t), hs_src, F(d.hs_t),
+                  true);
   }
   // the head writes the held state (plain buffers, read by the host and the
   // next launch)
@@ -546,7 +553,7 @@ int build_mega_program(dualar_handle* h, int nb) {
   }
   std::vector<ProdOp> prod;
   for (const MegaOp& o : ops)
-    if (o.type == MOP_GEMV) prod.push_back(ProdOp{o.g.w0, o.g.w1, o.g.n0, o.g.n1, o.g.K, o.g.mode});
+    if (o.type == MOP_GEMV) prod.push_back(ProdOp{o.g.w0, o.g.w1, o.g.n0, o.g.n1, o.g.K, o.g.mode, o.g.w4});
   MegaOp* dev = nullptr;
   CUDA_TRY(h, cudaMalloc(&dev, ops.size() * sizeof(MegaOp)));
   h->allocs.push_back(dev);
@@ -670,10 +677,9 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
                     smp->ras_top_p, smp->allow_eos};
   const int N = c.n_codebooks;
   LAUNCH(h, launch_setup(s, d, U16(h->w.tok_emb), h->stream));
-  if (!per_op_only && h->use_mega && !h->any_w4 && batch <= kTaggedRows && !h->mega_unsupported[batch] &&
-      !h->mega_ops[batch])
+  if (!per_op_only && h->use_mega && batch <= kTaggedRows && !h->mega_unsupported[batch] && !h->mega_ops[batch])
     TRY(build_mega_program(h, batch));
-  if (!per_op_only && h->use_mega && !h->any_w4 && batch <= kTaggedRows && !h->mega_unsupported[batch]) {
+  if (!per_op_only && h->use_mega && batch <= kTaggedRows && !h->mega_unsupported[batch]) {
     // a new tag epoch per launch; when it would no longer fit its bits the
     // tagged buffers are cleared and the count starts again
     if (h->epoch + 1 >= (1u << (32 - kTagOpBits))) {
@@ -702,6 +708,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     const int64_t need = static_cast<int64_t>(h->n_sm) * mp.n_ops * 2 * 8;
     mp.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
     mp.prefetch_bytes = h->prefetch_bytes;
+    mp.w4 = h->any_w4 ? 1 : 0;
     CUDA_TRY(h, cudaMemsetAsync(h->bar_counter, 0, 4, h->stream));
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (h->profiling) {
@@ -1381,6 +1388,22 @@ int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dua
   if (int rc = check(slow, c.n_layer, "slow")) return rc;
   if (int rc = check(fast, c.fast_n_layer, "fast")) return rc;
   if (const int frc = flush_tc(h)) return frc;
+  // the persistent kernel's programs name the old weights: built again on use
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) {
+    set_err(h, "stream synchronisation failed");
+    return DUALAR_ERR_CUDA;
+  }
+  for (int b = 0; b < 3; ++b) {
+    for (void* p : {static_cast<void*>(h->mega_ops[b]), static_cast<void*>(h->mega_prod[b])}) {
+      if (!p) continue;
+      h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), p), h->allocs.end());
+      cudaFree(p);
+    }
+    h->mega_ops[b] = nullptr;
+    h->mega_prod[b] = nullptr;
+    h->mega_nops[b] = h->mega_nprod[b] = 0;
+    h->mega_unsupported[b] = false;
+  }
   h->slow_q.clear();
   h->fast_q.clear();
   if (slow) h->slow_q.assign(slow, slow + c.n_layer);

@@ -257,8 +257,7 @@ DEVI float gemv_scale(const GemvArgs& a, const GemvPro<NB>& pr, int b) {
 
 // W4: x' goes to a split-32 layout instead (float4 t, elements 4t..4t+3, of
 // the 32-element vector v at float4 index t * (K/32) + v of the row), and
-// gsum[b][v] receives the sum of vector v's 32 values of x'; plain fp32 x
-// only (no tagged input).
+// gsum[b][v] receives the sum of vector v's 32 values of x'.
 template <int NB, bool W4 = false>
 DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<NB>& pr, int cta,
                        bool coherent, uint32_t epoch = 0, float* gsum = nullptr) {
@@ -315,9 +314,18 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
         if (b >= a.nb) continue;   // uniform
         float part = 0.f;
         if (act) {
-          const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
-          const float4 v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
-          const float4 v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
+          float4 v0, v1;
+          if (a.x_src >= 0) {
+            float v[8];
+            tag_wait<8>(reinterpret_cast<const uint64_t*>(a.x) + static_cast<size_t>(b) * a.ldx + 8 * j, xtag, v,
+                        a.err, a.wait_limit_ns);
+            v0 = make_float4(v[0], v[1], v[2], v[3]);
+            v1 = make_float4(v[4], v[5], v[6], v[7]);
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.ldx);
+            v0 = coherent ? __ldcg(src + 2 * j) : src[2 * j];
+            v1 = coherent ? __ldcg(src + 2 * j + 1) : src[2 * j + 1];
+          }
           const float4 p0 = make_float4(v0.x * gw[0], v0.y * gw[1], v0.z * gw[2], v0.w * gw[3]);
           const float4 p1 = make_float4(v1.x * gw[4], v1.y * gw[5], v1.z * gw[6], v1.w * gw[7]);
           // 8-vector j is quarter (j & 3) of 32-vector j >> 2: float4s 2(j&3), 2(j&3)+1
@@ -589,7 +597,8 @@ DEVI float w4_dot8(uint32_t word, const float4 xa, const float4 xb) {
 // gemv_stage_x<NB, true>.
 template <int NB>
 DEVI bool gemv_consume_w4(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
-                          const float* xs, const float* gsum, GemvScratch<NB>& sc, const GemvPro<NB>& pr) {
+                          const float* xs, const float* gsum, GemvScratch<NB>& sc, const GemvPro<NB>& pr,
+                          uint32_t epoch = 0) {
   constexpr int kWin = GemvScratch<NB>::kPartTiles;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV32 = K >> 5;
@@ -656,11 +665,11 @@ DEVI bool gemv_consume_w4(const GemvArgs& a, const GemvGeo& g, const GemvRing& r
     }
     if (threadIdx.x == 0) sc.tile[tw] = make_int2(row0, rows);
     if (++tw == kWin) {
-      gemv_flush<NB>(a, g, sc, pr, tw, true, 0);
+      gemv_flush<NB>(a, g, sc, pr, tw, true, epoch);
       tw = 0;
     }
   }
-  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, 0);
+  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch);
   return true;
 }
 

@@ -105,7 +105,7 @@ struct GemvArgs {
   // with the same element strides.
   int x_src, base_src, out_src;
   // 1: w0 / w1 hold 4-bit packed weights (gemv.cuh, "4-bit weights")
-  // instead of bf16; standalone GEMV only.
+  // instead of bf16.
   int w4;
 };
 

@@ -254,7 +254,7 @@ cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st) {
   if (a.nb <= 0) return cudaSuccess;
   const bool w4 = a.w4 != 0;
   if (w4) {
-    // packed 4-bit rows: plain fp32 input, no saved x (gemv_stage_x<NB, true>)
+    // packed 4-bit rows: plain fp32 buffers, no saved x (gemv_stage_x<NB, true>)
     if (!w4_k_supported(a.K) || a.x_src >= 0 || a.base_src >= 0 || a.out_src >= 0 || a.save_x != nullptr)
       return cudaErrorInvalidValue;
   } else if (a.K % 8 != 0 || !gemv_k_supported(a.K)) {

@@ -42,7 +42,9 @@ constexpr long long kTileCycles = 1600;        // one 40 KB tile per SM at its s
 constexpr long long kAbortCheckCycles = 20000; // how often a long wait looks at the error word
 constexpr uint64_t kIdlePrefetchBytes = 512 * 1024;   // prefetch window growth while the consumers idle
 
-template <int NB, int HD, int G>
+// W4: the program has packed 4-bit GEMVs, whose x rows are followed by
+// their 32-element sums (gemv_stage_x<NB, true>).
+template <int NB, int HD, int G, bool W4>
 struct MegaLayout {
   // fixed area (offsets from the dynamic shared memory base)
   static constexpr size_t bars = 0;   // full[8], empty[8], attn[2]
@@ -52,7 +54,7 @@ struct MegaLayout {
   static constexpr size_t uni = (opbuf + 2 * sizeof(MegaOp) + 127) & ~size_t(127);
   // union region: GEMV x rows | paged attention | fast attention | sampler
   __host__ __device__ static size_t union_bytes(int kmax) {
-    size_t u = sizeof(float) * size_t(NB) * kmax;
+    size_t u = sizeof(float) * size_t(NB) * (kmax + (W4 ? kmax / 32 : 0));
     u = u > sizeof(AttnSmem<HD, G, kMegaNCT, 1>) ? u : sizeof(AttnSmem<HD, G, kMegaNCT, 1>);
     u = u > sizeof(FastAttnSmem<HD>) ? u : sizeof(FastAttnSmem<HD>);
     u = u > sizeof(SampSmem<kMegaNCT>) ? u : sizeof(SampSmem<kMegaNCT>);
@@ -105,6 +107,7 @@ DEVI void grid_barrier(uint32_t* counter, uint32_t target, uint32_t* err, uint64
 // Position in the sequence of weight tiles of the frame program (all GEMV
 // ops, in order) for one CTA.  The descriptor of the next GEMV is loaded one
 // op ahead, so moving to it costs no memory round trip.
+template <bool W4>
 struct TileCursor {
   const ProdOp* prod;
   int n, cta, ncta;
@@ -121,13 +124,20 @@ struct TileCursor {
     a.n1 = q.n1;
     a.K = q.K;
     a.mode = q.mode;
+    a.w4 = W4 ? q.w4 : 0;
     return a;
+  }
+  __device__ GemvGeo geo(const GemvArgs& x) const {
+    if constexpr (W4) {
+      if (x.w4) return gemv_geo<true>(x, cta, ncta);
+    }
+    return gemv_geo(x, cta, ncta);
   }
   __device__ TileCursor(const ProdOp* pr, int np, int c, int nc)
       : prod(pr), n(np), cta(c), ncta(nc), j(0), nxt(), a(), g(), it(a, g) {
     if (n > 0) {
       a = args_of(prod[0]);
-      g = gemv_geo(a, cta, ncta);
+      g = geo(a);
       it = TileIter(a, g);
     }
     if (n > 1) nxt = prod[1];
@@ -136,13 +146,20 @@ struct TileCursor {
     while (j < n) {
       int row0, rows, part;
       if (it.next(row0, rows, part)) {
+        if constexpr (W4) {
+          if (a.w4) {
+            src = static_cast<const uint16_t*>(gemv_tile_ptr<true>(a, row0, part));
+            bytes = static_cast<uint32_t>(rows) * gemv_row_bytes<true>(a.K);
+            return true;
+          }
+        }
         src = gemv_tile_src(a, row0, part);
         bytes = static_cast<uint32_t>(rows) * a.K * 2;
         return true;
       }
       if (++j >= n) break;
       a = args_of(nxt);
-      g = gemv_geo(a, cta, ncta);
+      g = geo(a);
       it = TileIter(a, g);
       if (j + 1 < n) nxt = prod[j + 1];
     }
@@ -150,9 +167,9 @@ struct TileCursor {
   }
 };
 
-template <int NB, int HD, int G>
+template <int NB, int HD, int G, bool W4>
 __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams p) {
-  using Lay = MegaLayout<NB, HD, G>;
+  using Lay = MegaLayout<NB, HD, G, W4>;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::bars);
   GemvRing ring;
@@ -193,7 +210,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
     // keeps streaming while the consumers wait at a barrier, sample or attend.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      TileCursor lc(p.prod, p.n_prod, cta, ncta), pc(p.prod, p.n_prod, cta, ncta);
+      TileCursor<W4> lc(p.prod, p.n_prod, cta, ncta), pc(p.prod, p.n_prod, cta, ncta);
       uint64_t loaded = 0, prefetched = 0;
       const uint32_t* errp = d.err;
       uint32_t t = 0;
@@ -282,10 +299,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
     if (tr && tid == 0) tr[0] = global_timer_ns();
     switch (op.type) {
       case MOP_GEMV: {
-        const GemvGeo g = gemv_geo(op.g, cta, ncta);
+        const bool w4op = W4 && op.g.w4;
+        const GemvGeo g = w4op ? gemv_geo<true>(op.g, cta, ncta) : gemv_geo(op.g, cta, ncta);
         float* xs = reinterpret_cast<float*>(uni);
-        if (op.pos > 0 && tid == 0 &&
-            static_cast<size_t>(NB) * op.g.K * sizeof(float) <= kAttnPageOffset) {
+        float* gsum = xs + static_cast<size_t>(NB) * op.g.K;   // packed rows: the 32-element sums of x
+        const size_t xbytes = sizeof(float) * static_cast<size_t>(NB) * (op.g.K + (w4op ? op.g.K / 32 : 0));
+        if (op.pos > 0 && tid == 0 && xbytes <= kAttnPageOffset) {
           if (!pre_known) {
             pre = attn_paged_first(d, p.nrows, p.units, p.chunk, cta);
             pre_known = true;
@@ -296,8 +315,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
             att_pre = pre.unit;
           }
         }
-        gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
-        if (!gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep)) {
+        bool ok;
+        if constexpr (W4) {
+          if (w4op) {
+            gemv_stage_x<NB, true>(op.g, g, xs, pro, cta, true, ep, gsum);
+            ok = gemv_consume_w4<NB>(op.g, g, ring, t, xs, gsum, scr, pro, ep);
+          } else {
+            gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
+            ok = gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep);
+          }
+        } else {
+          gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
+          ok = gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep);
+        }
+        if (!ok) {
           // the ring protocol is broken: stop streaming (the error word is set)
           if (fetch) cp_async_wait_all();
           return;
@@ -348,9 +379,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   }
 }
 
-template <int NB, int HD, int G>
+template <int NB, int HD, int G, bool W4>
 static cudaError_t mega_launch_t(const MegaParams& p, int n_sm, cudaStream_t st, bool* unsupported) {
-  using Lay = MegaLayout<NB, HD, G>;
+  using Lay = MegaLayout<NB, HD, G, W4>;
   const size_t fkv_bytes = sizeof(float) * static_cast<size_t>(p.fkv_floats) * p.d.fast_n_layer;
   const size_t smem = Lay::total(p.kmax, fkv_bytes);
   // one fast-attention unit per CTA (its K/V stay in that CTA's shared memory)
@@ -360,11 +391,11 @@ static cudaError_t mega_launch_t(const MegaParams& p, int n_sm, cudaStream_t st,
   }
   static int configured = 0;
   if (configured != static_cast<int>(smem)) {
-    cudaError_t e = cudaFuncSetAttribute(mega_kernel<NB, HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(mega_kernel<NB, HD, G, W4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mega_kernel<NB, HD, G>, kGemvThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mega_kernel<NB, HD, G, W4>, kGemvThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) {
       *unsupported = true;
@@ -374,17 +405,25 @@ static cudaError_t mega_launch_t(const MegaParams& p, int n_sm, cudaStream_t st,
   }
   MegaParams q = p;
   void* args[] = {&q};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mega_kernel<NB, HD, G>), dim3(n_sm),
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mega_kernel<NB, HD, G, W4>), dim3(n_sm),
                                      dim3(kGemvThreads), args, smem, st);
 }
 
 cudaError_t launch_mega(const MegaParams& p, int nb, int n_sm, cudaStream_t st, bool* unsupported) {
   *unsupported = false;
   const int hd = p.d.hd, G = p.d.Hq / p.d.Hkv;
-  if (nb == 1 && hd == 128 && G == 4) return mega_launch_t<1, 128, 4>(p, n_sm, st, unsupported);
-  if (nb == 2 && hd == 128 && G == 4) return mega_launch_t<2, 128, 4>(p, n_sm, st, unsupported);
-  if (nb == 1 && hd == 64 && G == 2) return mega_launch_t<1, 64, 2>(p, n_sm, st, unsupported);
-  if (nb == 2 && hd == 64 && G == 2) return mega_launch_t<2, 64, 2>(p, n_sm, st, unsupported);
+  if (p.w4) {
+    if (nb == 1 && hd == 128 && G == 4) return mega_launch_t<1, 128, 4, true>(p, n_sm, st, unsupported);
+    if (nb == 2 && hd == 128 && G == 4) return mega_launch_t<2, 128, 4, true>(p, n_sm, st, unsupported);
+    if (nb == 1 && hd == 64 && G == 2) return mega_launch_t<1, 64, 2, true>(p, n_sm, st, unsupported);
+    if (nb == 2 && hd == 64 && G == 2) return mega_launch_t<2, 64, 2, true>(p, n_sm, st, unsupported);
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  if (nb == 1 && hd == 128 && G == 4) return mega_launch_t<1, 128, 4, false>(p, n_sm, st, unsupported);
+  if (nb == 2 && hd == 128 && G == 4) return mega_launch_t<2, 128, 4, false>(p, n_sm, st, unsupported);
+  if (nb == 1 && hd == 64 && G == 2) return mega_launch_t<1, 64, 2, false>(p, n_sm, st, unsupported);
+  if (nb == 2 && hd == 64 && G == 2) return mega_launch_t<2, 64, 2, false>(p, n_sm, st, unsupported);
   *unsupported = true;
   return cudaSuccess;
 }

@@ -38,6 +38,7 @@ struct ProdOp {
   const uint16_t* w0;
   const uint16_t* w1;
   int n0, n1, K, mode;
+  int w4;   // packed 4-bit rows (gemv.cuh, "4-bit weights")
 };
 
 struct MegaParams {
@@ -58,6 +59,7 @@ struct MegaParams {
   uint64_t prefetch_bytes;  // weight bytes per CTA kept in flight into L2 beyond the ring
   uint32_t epoch;           // launch epoch of the activation tags (1 .. 2^20 - 1)
   int fkv_floats;           // fast K/V per layer kept in shared memory: 2 * N * head_dim
+  int w4;                   // some GEMV of the program reads packed 4-bit rows
 };
 
 // Launches the frame program as one cooperative kernel (grid = n_sm CTAs).

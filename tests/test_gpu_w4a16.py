@@ -9,12 +9,14 @@ weights.
 
 - packing: the GPU's bytes equal the oracle's record bytes exactly (tiny
   shapes, the full-size 2560 x 9728 down projection, exact rounding ties);
-- decode: teacher-forced frames of the tiny model (batches 1, 2 and 12; the
-  late slow layer's attention in bf16) and of the one-layer full-width model
+- decode: teacher-forced frames of the tiny model (batches 1 and 2 through
+  both decode paths, 12 per op; the late slow layer's attention in bf16) and
+  of the one-layer full-width model
   (every projection packed, K = 2560 / 4096 / 9728) against the oracle on
   the same packed plan: logits within the tolerance, draws of the oracle's
   sampler on the GPU's logits equal to the GPU's;
-- restoring bf16 gives the persistent frame kernel back.
+- batches of 1-2 run packed and bf16 GEMVs in one persistent-kernel
+  program, whose cached program follows every change of weights.
 """
 import numpy as np
 import pytest
@@ -97,7 +99,9 @@ def gpu_sampling(o):
     return Sampling(o.temperature, o.top_p, o.ras_win, o.allow_eos, o.ras_temperature, o.ras_top_p)
 
 
-def run_forced(cfg, d, o, prompts, n_frames, smp, seed, max_launch=None):
+def run_forced(cfg, d, o, prompts, n_frames, smp, seed, persistent=None):
+    """persistent: True -- every frame is one persistent-kernel launch (plus
+    setup); False -- one kernel per op; None -- not checked."""
     slots = list(prompts)
     seqs = {}
     pages = PageOracle(d.max_pages, cfg.page_tokens)
@@ -116,8 +120,8 @@ def run_forced(cfg, d, o, prompts, n_frames, smp, seed, max_launch=None):
         codes, status, slow, fast, draws = d.decode_frame_forced(slots, dev(uni[f]), gpu_sampling(smp),
                                                                  dev(forced[f]))
         d.sync()
-        if max_launch is not None:
-            assert d.last_launch_count() > max_launch
+        if persistent is not None:
+            assert (d.last_launch_count() <= 2) == persistent, d.last_launch_count()
         codes, status = codes.cpu().numpy(), status.cpu().numpy()
         slow, fast, draws = slow.cpu().numpy(), fast.cpu().numpy(), draws.cpu().numpy()
         np.testing.assert_array_equal(codes, forced[f])
@@ -146,42 +150,54 @@ def tiny_packed(lib_built, tiny_bits):
     return keys, DualAROracle(TINY, tiny_bits, max_pos=4096, w4a16_keys=keys)
 
 
-@pytest.mark.parametrize("nseq", [1, 2, 12])
-def test_tiny_forced_frames(tiny_bits, tiny_packed, nseq):
-    """Batch 1 and 2 (no persistent kernel while weights are packed: more
-    than two launches per frame) and 12 (the bf16 late attention on the
-    tensor cores, packed projections in GEMV passes of <= 8 rows)."""
+@pytest.mark.parametrize("nseq,persistent", [(1, True), (1, False), (2, True), (2, False), (12, False)])
+def test_tiny_forced_frames(tiny_bits, tiny_packed, nseq, persistent):
+    """Batches 1 and 2 through the persistent frame kernel (packed and bf16
+    GEMVs in one program) and one kernel per op, and batch 12 (the bf16 late
+    attention on the tensor cores, packed projections in GEMV passes of <= 8
+    rows)."""
     keys, o = tiny_packed
     smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
     lens = g.make_lengths(nseq, 20, 200, seed=50 + nseq, stream="w4_tiny")
     prompts = {s: g.make_prompt(TINY, int(n), seed=60 + s) for s, n in enumerate(lens)}
     d = packed_decoder(TINY, tiny_bits, keys, max_pages=128, max_seqs=16, max_ctx=1024)
-    run_forced(TINY, d, o, prompts, 4, smp, seed=70 + nseq, max_launch=2 if nseq <= 2 else None)
+    d.set_persistent(persistent)
+    run_forced(TINY, d, o, prompts, 4, smp, seed=70 + nseq, persistent=persistent and nseq <= 2)
     d.close()
 
 
 def test_one_layer_full_width_forced_frames(lib_built):
     """Full widths (K = 2560, 4096, 9728: several records per tile, two
     warps per row for the down projection), every projection packed;
-    batches 1 and 3 with ragged contexts across pages."""
+    batches 1 and 2 through the persistent frame kernel, 3 per op, ragged
+    contexts across pages."""
     cfg = S2PRO_L1
     bits = g.make_weights(cfg, seed=0)
     keys = OW.late_attn_keys(cfg.n_layer, cfg.fast_n_layer, 0)
     o = DualAROracle(cfg, bits, max_pos=1024, w4a16_keys=keys)
     smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
-    for nseq, lens in ((1, [70]), (3, [64, 130, 9])):
+    for nseq, lens, pers in ((1, [70], True), (2, [200, 33], True), (3, [64, 130, 9], False)):
         prompts = {s: g.make_prompt(cfg, n, seed=80 + s) for s, n in enumerate(lens)}
         d = packed_decoder(cfg, bits, keys, max_pages=32, max_seqs=4, max_ctx=512)
-        run_forced(cfg, d, o, prompts, 2, smp, seed=90 + nseq)
+        run_forced(cfg, d, o, prompts, 2, smp, seed=90 + nseq, persistent=pers)
         d.close()
     torch.cuda.empty_cache()
 
 
-def test_restoring_bf16_restores_persistent_kernel(lib_built, tiny_bits, tiny_oracle):
-    keys = OW.late_attn_keys(TINY.n_layer, TINY.fast_n_layer, 1)
-    d = packed_decoder(TINY, tiny_bits, keys, max_pages=64, max_seqs=4, max_ctx=1024)
-    d.set_w4a16(None)
+def test_switching_weights_rebuilds_the_persistent_program(lib_built, tiny_bits, tiny_oracle, tiny_packed):
+    """One decoder: bf16 frames, then packed frames, then bf16 again; the
+    persistent kernel's program follows each switch (each segment against
+    its own oracle; each slot is released before the next one starts, so
+    page numbers start from the bottom again)."""
+    from dual_ar_tts_frame_gb300 import DualARDecoder, pack_w4a16, upload_weights
+    keys, o4 = tiny_packed
+    w = upload_weights(tiny_bits)
+    packed = {k: pack_w4a16(w[k]) for k in keys}
     smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10)
-    run_forced(TINY, d, tiny_oracle, {0: g.make_prompt(TINY, 40, seed=7)}, 3, smp, seed=8)
-    assert d.last_launch_count() <= 2
+    d = DualARDecoder(TINY, w, max_pages=64, max_seqs=4, max_ctx=1024)
+    for slot, (pk, o) in enumerate(((None, tiny_oracle), (packed, o4), (None, tiny_oracle))):
+        d.set_w4a16(pk)
+        run_forced(TINY, d, o, {slot: g.make_prompt(TINY, 40, seed=7 + slot)}, 3, smp, seed=8 + slot,
+                   persistent=True)
+        d.release(slot)
     d.close()
