@@ -564,27 +564,38 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
 }
 
 // ---- 4-bit consumer ------------------------------------------------------------
-// Element k of a packed row as the float 128 + u_k (u_k its stored nibble,
-// 0..15): the nibble is moved to bits 16..19 and the exponent and mantissa of
-// 128.0f (0x43000000) are OR-ed in, so no integer-to-float conversion is
-// needed.  e is the element's place in its 32-bit word (8 elements).
-template <int E>
-DEVI float w4_val128(uint32_t word) {
-  const uint32_t s = E <= 4 ? (word << (16 - 4 * E)) : (word >> (4 * E - 16));
-  return __uint_as_float((s & 0x000F0000u) | 0x43000000u);
+// Element of a packed row as the float 128 + u (u its stored nibble, 0..15):
+// src holds one nibble per byte (the even or the odd elements of a word);
+// byte I is moved to bits 16..23 under the exponent byte of 128.0f
+// (0x43000000), so no integer-to-float conversion is needed.
+template <int I>
+DEVI float w4_val128(uint32_t src) {
+  return __uint_as_float(__byte_perm(src, 0x43000000u, 0x7054u | (I << 8)));
 }
 
-// Sum over the 8 elements of one word: (128 + u_e) * x_e.
-DEVI float w4_dot8(uint32_t word, const float4 xa, const float4 xb) {
-  float s = w4_val128<0>(word) * xa.x;
-  s = fmaf(w4_val128<1>(word), xa.y, s);
-  s = fmaf(w4_val128<2>(word), xa.z, s);
-  s = fmaf(w4_val128<3>(word), xa.w, s);
-  s = fmaf(w4_val128<4>(word), xb.x, s);
-  s = fmaf(w4_val128<5>(word), xb.y, s);
-  s = fmaf(w4_val128<6>(word), xb.z, s);
-  s = fmaf(w4_val128<7>(word), xb.w, s);
-  return s;
+// c.x += a0 * b0, c.y += a1 * b1 in one packed fp32 instruction (two
+// independent round-to-nearest FMAs).
+DEVI void ffma2(float2& c, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(c.x), "+f"(c.y)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// The 8 elements of one 32-bit word of codes (element e in bits 4e..4e+3)
+// against x elements xa (0..3) and xb (4..7): c gets (128 + u_e) * x_e, even
+// elements in c.x, odd ones in c.y.
+DEVI float2 w4_word(uint32_t wd, const float4 xa, const float4 xb) {
+  const uint32_t ev = wd & 0x0F0F0F0Fu, od = (wd >> 4) & 0x0F0F0F0Fu;
+  float2 c = make_float2(w4_val128<0>(ev) * xa.x, w4_val128<0>(od) * xa.y);
+  ffma2(c, w4_val128<1>(ev), w4_val128<1>(od), xa.z, xa.w);
+  ffma2(c, w4_val128<2>(ev), w4_val128<2>(od), xb.x, xb.y);
+  ffma2(c, w4_val128<3>(ev), w4_val128<3>(od), xb.z, xb.w);
+  return c;
 }
 
 // Consumer side of a GEMV over packed 4-bit rows: like gemv_consume, with a
@@ -637,12 +648,13 @@ DEVI bool gemv_consume_w4(const GemvArgs& a, const GemvGeo& g, const GemvRing& r
           const int j = lane + 32 * q;
           if (j < nvec) {
             const int v = v0 + j;
-            // four independent 8-term chains, then the group correction
-            const float d0 = w4_dot8(w[q].x, x4[0 * KV32 + v], x4[1 * KV32 + v]);
-            const float d1 = w4_dot8(w[q].y, x4[2 * KV32 + v], x4[3 * KV32 + v]);
-            const float d2 = w4_dot8(w[q].z, x4[4 * KV32 + v], x4[5 * KV32 + v]);
-            const float d3 = w4_dot8(w[q].w, x4[6 * KV32 + v], x4[7 * KV32 + v]);
-            const float dv = fmaf(-136.f, gs[v], (d0 + d1) + (d2 + d3));
+            // four independent chains (one per word), then the group correction
+            const float2 d0 = w4_word(w[q].x, x4[0 * KV32 + v], x4[1 * KV32 + v]);
+            const float2 d1 = w4_word(w[q].y, x4[2 * KV32 + v], x4[3 * KV32 + v]);
+            const float2 d2 = w4_word(w[q].z, x4[4 * KV32 + v], x4[5 * KV32 + v]);
+            const float2 d3 = w4_word(w[q].w, x4[6 * KV32 + v], x4[7 * KV32 + v]);
+            const float dv =
+                fmaf(-136.f, gs[v], ((d0.x + d0.y) + (d1.x + d1.y)) + ((d2.x + d2.y) + (d3.x + d3.y)));
             p[b] = fmaf(sv[q], dv, p[b]);
           }
         }
