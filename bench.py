@@ -147,6 +147,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x of all ranks of the initialised process group (the
+    slowest replica's time); device: where the group's collectives run
+    ("cuda" for NCCL, "cpu" for gloo)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world_size: int, slowest_s: float) -> float:
+    """Whole-job throughput of independent replicas: the units all ranks
+    processed over the slowest rank's time."""
+    return units_per_rank * world_size / slowest_s
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -389,11 +406,8 @@ def main():
     prof = dec.profile_read()
     ms = ev0.elapsed_time(ev1)
     if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    frames = b * K * ws
-    value = frames / (ms / 1000.0)
+        ms = max_over_ranks(ms, "cuda")
+    value = replica_throughput(b * K, ws, ms / 1000.0)
     ms_per_step = ms / K
     # byte model over the timed frames: contexts grow by one per frame
     att = [wl["prompt"] + f + 1 for f in range(W, W + K)]
@@ -451,10 +465,8 @@ def main():
             assert int(hs[0]) == 0
         el = time.perf_counter() - t0
         if ws > 1:
-            t = torch.tensor([el], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            el = float(t.item())
-        e2e = {"value": b * K * ws / el, "unit": "frames/s", "h2d_bytes_per_step": hu[0].numel() * 4,
+            el = max_over_ranks(el, "cuda")
+        e2e = {"value": replica_throughput(b * K, ws, el), "unit": "frames/s", "h2d_bytes_per_step": hu[0].numel() * 4,
                "d2h_bytes_per_step": hc.numel() * 4 + hs.numel() * 4}
 
     dec.close()

@@ -115,3 +115,22 @@ def test_late_attn_keys_agree_with_oracle():
     from oracle import w4a16
     for n, f, b in ((36, 4, 12), (2, 2, 1), (2, 2, 0), (2, 2, 2)):
         assert sorted(late_attn_keys(n, f, b)) == sorted(w4a16.late_attn_keys(n, f, b))
+
+
+def test_byte_model_counts_packed_records_like_the_library(lib):
+    """The 4-bit frame bytes of the byte model use the same record size as
+    dualar_w4a16_bytes, and every packed projection is read once per slow
+    step and once per fast pass."""
+    from dualar_inputs import S2PRO
+    from dual_ar_tts_frame_gb300 import bytemodel
+    from dual_ar_tts_frame_gb300.decoder import late_attn_keys
+    keys = late_attn_keys(S2PRO.n_layer, S2PRO.fast_n_layer, 12)
+    shapes = bytemodel.projection_shapes(S2PRO)
+    saved = 0
+    for k in keys:
+        stack, _, name = k.split(".")
+        n, kk = shapes[name]
+        reads = 1 if stack == "slow" else S2PRO.n_codebooks
+        saved += reads * (2 * n * kk - lib.dualar_w4a16_bytes(n, kk))
+    assert bytemodel.weight_bytes_per_step(S2PRO) - bytemodel.weight_bytes_per_step(S2PRO, keys) == saved
+    assert bytemodel.weight_bytes_per_step(S2PRO, keys) == 4_649_059_328

@@ -11,6 +11,7 @@ whole model on weights the rule leaves unchanged.
 import os
 
 import numpy as np
+import pytest
 
 from dualar_inputs import S2PRO, TINY
 from dualar_inputs import generators as g
@@ -181,3 +182,57 @@ def test_model_changes_off_grid():
         z.append(o.prefill(prompt).z_last)
     d = np.abs(z[0] - z[1]).max()
     assert 1e-3 < d < 0.5 * np.abs(z[0]).max()
+
+
+# ------------------------------------------------------ planted mistakes --
+# Each plants a plausible mistake in the oracle's 4-bit rule (on the CPU) and
+# checks that one of the pins above fails.
+
+def _expect_failure(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(W, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
+    monkeypatch.undo()
+
+
+def test_planted_nibble_order_swap_is_caught(monkeypatch):
+    orig = W.pack
+
+    def bad(q, s_bits):
+        p = orig(q, s_bits)
+        k = q.shape[1]
+        p[:, :k // 2] = (p[:, :k // 2] >> 4) | ((p[:, :k // 2] & 15) << 4)
+        return p
+    _expect_failure(monkeypatch, "pack", bad, test_pack_matches_hand_worked_row)
+
+
+def test_planted_scale_divisor_is_caught(monkeypatch):
+    def bad(w_bits):
+        n, k = w_bits.shape
+        w = bf16_bits_to_f32(w_bits).reshape(n, k // 128, 128)
+        s_bits = f32_to_bf16_bits(np.abs(w).max(axis=2) / np.float32(8.0))   # /8 instead of /7
+        s = bf16_bits_to_f32(s_bits)
+        q = np.clip(np.rint(w / np.where(s > 0, s, 1)[:, :, None]), -8, 7)
+        return q.astype(np.int8).reshape(n, k), s_bits
+    _expect_failure(monkeypatch, "quantize", bad, test_on_grid_weights_round_trip_exactly)
+
+
+def test_planted_row_scale_is_caught(monkeypatch):
+    def bad(w_bits):
+        # one scale per row (its largest |w|) instead of one per group of 128
+        n, k = w_bits.shape
+        w = bf16_bits_to_f32(w_bits)
+        s_bits = f32_to_bf16_bits(np.abs(w).max(axis=1) / np.float32(7.0))
+        s = bf16_bits_to_f32(s_bits)
+        q = np.clip(np.rint(w / np.where(s > 0, s, 1)[:, None]), -8, 7)
+        return q.astype(np.int8), np.repeat(s_bits[:, None], k // 128, axis=1)
+    _expect_failure(monkeypatch, "quantize", bad, test_group_rounding_bound_and_scale)
+
+
+def test_planted_offset_sign_is_caught(monkeypatch):
+    orig = W.pack
+
+    def bad(q, s_bits):
+        return orig((-q.astype(np.int16)).clip(-8, 7).astype(np.int8), s_bits)   # stores 8 - q
+    _expect_failure(monkeypatch, "pack", bad, test_pack_matches_hand_worked_row)
+
