@@ -288,12 +288,15 @@ typedef struct dualar_w4a16_layer {
  * the next call on (the caller keeps them valid until they are replaced or
  * the handle is destroyed).  slow: host array [n_layer] or NULL (all bf16);
  * fast: host array [fast_n_layer] or NULL.  Embeddings, norms and both heads
- * stay bf16.  While any projection is packed, decode runs one kernel per op
- * (not the persistent frame kernel) and packed projections use the
- * weight-streaming GEMV at every batch size, in passes of at most 8 rows.
- * Both arrays NULL restores the all-bf16 decoder.  Errors: INVALID_ARG (an
- * unaligned pointer, a gate without its up matrix, an in-dimension that is
- * not a multiple of 128). */
+ * stay bf16.  Packed projections always run in the weight-streaming GEMV
+ * (never on the tensor cores): inside the persistent frame kernel for
+ * batches of 1-2 (dualar_set_persistent), otherwise one launch per
+ * projection in passes of at most 8 rows (prefill chunks included).  The
+ * call synchronises the handle's stream and drops the persistent kernel's
+ * cached frame programs, which are built again for the new weights on the
+ * next decode.  Both arrays NULL restores the all-bf16 decoder.  Errors:
+ * INVALID_ARG (an unaligned pointer, a gate without its up matrix, an
+ * in-dimension that is not a multiple of 128), CUDA. */
 int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dualar_w4a16_layer* fast);
 
 /* Synchronises the handle's stream and reports device-side errors:

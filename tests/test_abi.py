@@ -134,3 +134,10 @@ def test_byte_model_counts_packed_records_like_the_library(lib):
         saved += reads * (2 * n * kk - lib.dualar_w4a16_bytes(n, kk))
     assert bytemodel.weight_bytes_per_step(S2PRO) - bytemodel.weight_bytes_per_step(S2PRO, keys) == saved
     assert bytemodel.weight_bytes_per_step(S2PRO, keys) == 4_649_059_328
+
+
+def test_pack_w4a16_rejects_bad_shapes_before_any_gpu_work(lib):
+    torch = pytest.importorskip("torch")
+    from dual_ar_tts_frame_gb300 import pack_w4a16
+    with pytest.raises(L.DualARError):
+        pack_w4a16(torch.zeros((4, 100), dtype=torch.bfloat16))
