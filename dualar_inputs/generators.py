@@ -170,3 +170,18 @@ def make_forced_codes(n_frames: int, batch: int, cfg: DualARConfig, seed: int,
 def make_lengths(n: int, lo: int, hi_inclusive: int, seed: int, stream: str) -> np.ndarray:
     """Context/prompt lengths uniform on [lo, hi] (int64)."""
     return gen_randint((n,), lo, hi_inclusive + 1, seed, stream)
+
+
+def make_replacement_workload(batch: int, n_long: int, n_queue: int, seed: int) -> dict:
+    """The batch-128 replacement workload: `batch - n_long` contexts uniform
+    on [2,048, 4,096], `n_long` contexts of 16,384 that stay resident, a
+    finish frame uniform on [1, 64] for every sequence (the long ones never
+    finish), and a queue of `n_queue` replacement contexts uniform on
+    [2,048, 4,096] with their own finish frames, taken in order."""
+    short = make_lengths(batch - n_long, 2048, 4096, seed, "repl_ctx")
+    ctx = np.concatenate([short, np.full(n_long, 16384, np.int64)])
+    finish = np.concatenate([make_lengths(batch - n_long, 1, 64, seed, "repl_finish"),
+                             np.full(n_long, -1, np.int64)])
+    return {"ctx": ctx, "finish": finish,
+            "queue_ctx": make_lengths(n_queue, 2048, 4096, seed, "repl_queue_ctx"),
+            "queue_finish": make_lengths(n_queue, 1, 64, seed, "repl_queue_finish")}

@@ -580,3 +580,56 @@ def _tp_check(seed, fn):
     for i in range(n):
         expect = p[i] / zk if i in kept else 0.0
         assert abs(counts[i] / m - expect) <= 1.5 / m
+
+
+def test_page_oracle_under_replacement_churn():
+    """The batch-128 replacement workload's page traffic (124 contexts of
+    2-4K that finish at seeded frames and are replaced from a queue, 4
+    resident contexts of 16K), 64 steps: the page oracle agrees step by step
+    with a naive allocator (a sorted free list, lowest page first), every page
+    is held by at most one slot, and releasing everything frees the pool."""
+    wl = g.make_replacement_workload(128, 4, 256, seed=4)
+    pt = 64
+    need = sum(-(-int(c + 64) // pt) for c in wl["ctx"]) + 512
+    po = oracle.PageOracle(need, pt)
+    naive_free = list(range(need))
+    naive = {}
+
+    def naive_append(slot, old_len, n):
+        tab = naive.setdefault(slot, [])
+        for p in range(old_len, old_len + n):
+            if p % pt == 0:
+                tab.append(naive_free.pop(0))
+
+    def naive_release(slot):
+        naive_free.extend(naive.pop(slot))
+        naive_free.sort()
+
+    length, finish = {}, {}
+    for s in range(128):
+        po.append(s, int(wl["ctx"][s]))
+        naive_append(s, 0, int(wl["ctx"][s]))
+        length[s], finish[s] = int(wl["ctx"][s]), int(wl["finish"][s])
+    q = 0
+    for step in range(1, 65):
+        for s in range(128):
+            po.append(s, 1)
+            naive_append(s, length[s], 1)
+            length[s] += 1
+        for s in range(128):
+            if finish[s] == step:
+                po.release(s)
+                naive_release(s)
+                n = int(wl["queue_ctx"][q])
+                po.append(s, n)
+                naive_append(s, 0, n)
+                length[s], finish[s] = n, step + int(wl["queue_finish"][q])
+                q += 1
+        assert po.table == naive
+        held = [pg for tab in po.table.values() for pg in tab]
+        assert len(held) == len(set(held))
+        assert sorted(po.free) == naive_free
+    assert q > 100                                  # most short sequences were replaced, some twice
+    for s in list(po.table):
+        po.release(s)
+    assert sorted(po.free) == list(range(need)) and not any(po.holders)
