@@ -46,6 +46,10 @@ WORKLOADS = {
                       desc="full S2-Pro-shaped Dual-AR, batch 64, contexts uniform in [1024, 4096]"),
     "s2pro_l1_b64": dict(cfg="s2pro_l1", batch=64, prompt=0, frames=8, temperature=0.8, top_p=0.8, ras_win=10,
                          desc="one-layer S2-Pro-shaped profiling case, batch 64, contexts uniform in [1024, 4096]"),
+    "s2pro_b128_replace": dict(cfg="s2pro", batch=128, prompt=0, frames=64, temperature=0.8, top_p=0.8,
+                               ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 128: 124 contexts uniform in "
+                                                "[2048, 4096] that finish at seeded frames (uniform in [1, 64]) and "
+                                                "are replaced from a seeded queue, plus 4 resident contexts of 16384"),
     "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
                     desc="tiny Dual-AR, batch 1, 32-token prompt, 16 frames"),
 }
@@ -235,6 +239,85 @@ def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
             "gpu_launches_per_step": launches}
 
 
+def measure_replacement(cfg, w, frames: int, peak: float, with_prefill: bool) -> dict:
+    """Batch 128 with replacement: 124 contexts uniform in [2,048, 4,096] and
+    4 of 16,384 (seed 4), set up by the synthetic-context hook; every step
+    decodes all 128 slots, then each sequence whose seeded finish frame has
+    come is released and its slot restarted from the queue.  The decode steps
+    are device-timed one by one (CUDA events around each call), so the
+    replacements' set-up is excluded; with_prefill restarts slots with a real
+    prefill of a seeded prompt of the queued length and also reports the
+    wall time of the whole loop, prefill included."""
+    import torch
+    from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling
+    from dual_ar_tts_frame_gb300 import bytemodel
+    b = 128
+    wl = gen.make_replacement_workload(b, 4, 4 * b, seed=4)
+    ctx = [int(c) for c in wl["ctx"]]
+    max_ctx = max(ctx) + frames + 16
+    # every short slot may hold a 4,096-token context plus its growth at any time
+    per = lambda n: -(-(n + frames + 4) // cfg.page_tokens)  # noqa: E731
+    pages = (b - 4) * per(4096) + sum(per(c) for c in ctx[-4:]) + 8
+    dec = DualARDecoder(cfg, w, max_pages=pages, max_seqs=b, max_ctx=max_ctx)
+    for s in range(b):
+        dec.synthetic_context(s, ctx[s], seed=3000 + s)
+    dec.sync()
+    smp = Sampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
+    uni = torch.from_numpy(gen.make_uniforms(frames, b, cfg, seed=1)).cuda()
+    codes = torch.empty((b, cfg.n_codebooks), dtype=torch.int32, device="cuda")
+    status = torch.empty((b,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    slots = list(range(b))
+    length = list(ctx)
+    finish = [int(f) for f in wl["finish"]]
+    q = 0
+    step_ms = 0.0
+    step_bytes = 0
+    replaced = 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(frames)]
+    for f in range(3):   # untimed warm-up steps before the schedule starts
+        dec.decode_frame(slots, uni[f], smp, codes, status)
+        length = [n + 1 for n in length]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for f in range(frames):
+        step_bytes += bytemodel.frame_bytes(cfg, [n + 1 for n in length])
+        evs[f][0].record(stream)
+        dec.decode_frame(slots, uni[f], smp, codes, status)
+        evs[f][1].record(stream)
+        for s in slots:
+            length[s] += 1
+            if finish[s] == f + 1:
+                dec.release(s)
+                n = int(wl["queue_ctx"][q])
+                if with_prefill:
+                    dec.prefill(s, gen.make_prompt(cfg, n, seed=5000 + q))
+                else:
+                    dec.synthetic_context(s, n, seed=5000 + q)
+                length[s] = n
+                finish[s] = f + 1 + int(wl["queue_finish"][q])
+                q += 1
+                replaced += 1
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    dec.sync()
+    step_ms = sum(a.elapsed_time(z) for a, z in evs)
+    dec.close()
+    gbs = step_bytes / (step_ms / 1000.0) / 1e9
+    r = {"workload": WORKLOADS["s2pro_b128_replace"]["desc"] + " (synthetic K/V and held state for the "
+                     "initial contexts" + ("; replacements prefilled" if with_prefill else "; replacements "
+                     "set up by the synthetic-context hook") + ")",
+         "value": b * frames / (step_ms / 1000.0), "unit": "frames/s", "steps": frames,
+         "ms_per_step": step_ms / frames, "replaced_sequences": replaced,
+         "frame_bytes_per_step": step_bytes / frames,
+         "frame_roofline": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}}
+    if with_prefill:
+        r["prefill_included"] = {"value": b * frames / wall, "unit": "frames/s", "wall_s": wall,
+                                 "note": "host wall clock of the whole loop: decode steps plus the "
+                                         "replacements' prefills"}
+    return r
+
+
 def measure_w4a16(cfg, w, prompt, frames: int, warmup: int, peak: float) -> dict:
     """Batch 1 with 4-bit weights: the "late12attn" plan (every projection
     packed except the query/key/value and output projections of the last 12
@@ -329,6 +412,20 @@ def main():
               "l2": "inputs larger than L2 (9.1 GB of weights streamed per frame); no flush"}
     if args.workload != "s2pro_b1":
         config["l2"] = "small profiling/parity workload, not a bench line"
+
+    if args.workload == "s2pro_b128_replace":
+        # the batch-128 replacement workload alone (not part of the default line)
+        import torch
+        from dual_ar_tts_frame_gb300 import build, upload_weights
+        torch.cuda.set_device(local)
+        build()
+        w = upload_weights(gen.make_weights(cfg, seed=0))
+        peak, _ = peaks()
+        for with_prefill in (False, True):
+            r = measure_replacement(cfg, w, frames=W + K, peak=peak, with_prefill=with_prefill)
+            print(json.dumps({"metric": METRIC, "impl": "ours", "config": {"workload": r["workload"]}, **r}),
+                  flush=True)
+        return
 
     if args.workload in ("s2pro_b64", "s2pro_l1_b64"):
         # the batch-64 measurement alone (also part of the default line)
