@@ -7,8 +7,9 @@ must decode exactly what the ordinary call decodes: the same codes and the
 same held logits and hidden state, call after call -- the fixed scratch array
 it shares between calls has to be cleared and reused correctly.
 
-This file is collected last on purpose, so a run that stops at the first
-failure has already run every other test.
+This file is collected after the other parity files on purpose (only the
+full-size 4-bit file comes later), so a run that stops at the first failure
+has already run them.
 """
 import numpy as np
 import pytest
