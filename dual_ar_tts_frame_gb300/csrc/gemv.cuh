@@ -13,9 +13,14 @@
 // and stores the partial in a per-tile buffer; no CTA-wide synchronisation
 // while streaming.  When the buffer is full, and at the end of the GEMV, the
 // consumers add each row's S partials in segment order (deterministic) and
-// write the epilogue.  The SwiGLU gate and up rows are two consecutive tiles.  One producer thread runs ahead by the ring depth;
-// in the persistent kernel it keeps streaming the next GEMV's weights while
-// the consumers are still busy, since weights never depend on activations.
+// write the epilogue.  The SwiGLU gate and up rows are two consecutive
+// tiles.  One producer thread runs ahead by the ring depth; in the persistent
+// kernel it keeps streaming the next GEMV's weights while the consumers are
+// still busy, since weights never depend on activations.
+//
+// Packed 4-bit rows ("4-bit weights" below) use the same ring, tiles and
+// epilogue: a tile is R packed row records, a lane's 16-byte vector holds 32
+// elements of one scale group (gemv_consume_w4).
 #pragma once
 
 #include "common.cuh"
