@@ -74,7 +74,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with dual_ar_tts_frame_gb300.build.build() "
                            "(nvcc, sm_103a); there is no CPU fallback")
-    L = ctypes.CDLL(path)
+    _lib = bind(ctypes.CDLL(path))
+    return _lib
+
+
+def bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declares the argument and result types of every entry point."""
     H = c_vp
     L.dualar_create.argtypes = [ctypes.POINTER(dualar_config), ctypes.POINTER(dualar_weights), c_vp,
                                 ctypes.POINTER(H)]
@@ -116,7 +121,6 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.dualar_set_w4a16.argtypes = [H, ctypes.POINTER(dualar_w4a16_layer), ctypes.POINTER(dualar_w4a16_layer)]
     for n in EXPORTED:
         getattr(L, n)
-    _lib = L
     return L
 
 
