@@ -217,3 +217,22 @@ def test_w4a16_selection_checks(hl):
     assert h.prefill(0, 70) == OK and h.decode([0]) == OK     # packed weights drive the same bookkeeping
     assert hl.dualar_set_w4a16(h.h, None, None) == OK
     h.close()
+
+
+def test_decode_dispatch(hl):
+    """Batches of 1-2 run as one setup plus one persistent-kernel launch
+    (also with packed projections); batch 3, or the persistent kernel turned
+    off, queues one kernel per op."""
+    h = Host(hl, max_pages=16, max_seqs=4, max_ctx=300)
+    for s in range(3):
+        assert h.prefill(s, 20 + s) == OK
+    assert h.decode([0]) == OK and hl.dualar_last_launch_count(h.h) == 2
+    assert h.decode([1, 0]) == OK and hl.dualar_last_launch_count(h.h) == 2
+    assert h.decode([2, 1, 0]) == OK and hl.dualar_last_launch_count(h.h) > 2
+    slow = (L.dualar_w4a16_layer * TINY.n_layer)()
+    slow[0].w_down = 0x40000
+    assert hl.dualar_set_w4a16(h.h, slow, None) == OK
+    assert h.decode([0]) == OK and hl.dualar_last_launch_count(h.h) == 2
+    assert hl.dualar_set_persistent(h.h, 0) == OK
+    assert h.decode([0]) == OK and hl.dualar_last_launch_count(h.h) > 2
+    h.close()
