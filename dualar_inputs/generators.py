@@ -89,7 +89,9 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     """Widen bf16 bits (uint16) to float32 exactly."""
-    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    u = np.asarray(b, dtype=np.uint16).astype(np.uint32)
+    u <<= np.uint32(16)          # in place: one new array, not two
+    return u.view(np.float32)
 
 
 _tables: dict[str, np.ndarray] = {}
