@@ -55,15 +55,16 @@ class Host:
     """A tiny-config handle on the host stand-in, with fake (never read)
     16-byte-aligned weight addresses."""
 
-    def __init__(self, lib, max_pages=12, max_seqs=4, max_ctx=400):
+    def __init__(self, lib, max_pages=12, max_seqs=4, max_ctx=400, **shape):
         self.lib, self.max_pages, self.max_seqs = lib, max_pages, max_seqs
         c = TINY
-        cfg = L.dualar_config(
-            dim=c.dim, n_layer=c.n_layer, n_head=c.n_head, n_kv_head=c.n_kv_head, head_dim=c.head_dim,
-            ffn=c.ffn, vocab=c.vocab, sem_begin=c.sem_begin, n_sem=c.n_sem, im_end_id=c.im_end_id,
-            fast_n_layer=c.fast_n_layer, fast_vocab=c.fast_vocab, n_codebooks=c.n_codebooks,
-            slow_qk_norm=1, fast_qk_norm=0, page_tokens=64, max_pages=max_pages, max_seqs=max_seqs,
-            max_ctx=max_ctx, rope_base=1e6, norm_eps=1e-6)
+        kw = dict(dim=c.dim, n_layer=c.n_layer, n_head=c.n_head, n_kv_head=c.n_kv_head, head_dim=c.head_dim,
+                  ffn=c.ffn, vocab=c.vocab, sem_begin=c.sem_begin, n_sem=c.n_sem, im_end_id=c.im_end_id,
+                  fast_n_layer=c.fast_n_layer, fast_vocab=c.fast_vocab, n_codebooks=c.n_codebooks,
+                  slow_qk_norm=1, fast_qk_norm=0, page_tokens=64, max_pages=max_pages, max_seqs=max_seqs,
+                  max_ctx=max_ctx, rope_base=1e6, norm_eps=1e-6)
+        kw.update(shape)
+        cfg = L.dualar_config(**kw)
         addr = iter(range(0x10000, 0x10000 + 4096 * 4096, 4096))
 
         def layer():
@@ -235,4 +236,28 @@ def test_decode_dispatch(hl):
     assert h.decode([0]) == OK and hl.dualar_last_launch_count(h.h) == 2
     assert hl.dualar_set_persistent(h.h, 0) == OK
     assert h.decode([0]) == OK and hl.dualar_last_launch_count(h.h) > 2
+    h.close()
+
+
+def test_noalloc_batch_limit_at_the_s2pro_attention_shape(hl):
+    """The no-allocation call keeps the split-KV scratch in a fixed 4 MiB
+    array: at the S2-Pro attention shape (32 query heads, 8 KV heads of 128)
+    that holds 3 sequences per call, as the header states."""
+    h = Host(hl, max_pages=16, max_seqs=4, max_ctx=300, n_head=32, n_kv_head=8, head_dim=128)
+    for sl in range(4):
+        assert h.prefill(sl, 10) == OK
+    s = np.arange(4, dtype=np.int32)
+
+    def noalloc(n):
+        return hl.dualar_decode_frame_noalloc(h.h, n, s.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                              h.uni.ctypes.data, ctypes.byref(h.smp), h.codes.ctypes.data,
+                                              h.status.ctypes.data)
+    before = h.state()
+    assert noalloc(4) == INVALID
+    buf = ctypes.create_string_buffer(512)
+    hl.dualar_get_error(h.h, buf, 512)
+    assert b"at most 3 sequences" in buf.value
+    assert h.state() == before
+    assert noalloc(3) == OK
+    assert [h.length(i) for i in range(4)] == [11, 11, 11, 10]
     h.close()
