@@ -261,3 +261,25 @@ def test_noalloc_batch_limit_at_the_s2pro_attention_shape(hl):
     assert noalloc(3) == OK
     assert [h.length(i) for i in range(4)] == [11, 11, 11, 10]
     h.close()
+
+
+def test_whole_sequence_share_and_synthetic_context(hl):
+    """Sharing a slot's whole length hands over its held state, so the new
+    slot decodes at once; the synthetic-context hook takes pages exactly as
+    a prefill of the same length."""
+    h = Host(hl, max_pages=20, max_seqs=4, max_ctx=400)
+    po = PageOracle(20, 64)
+    assert h.prefill(0, 150) == OK
+    po.append(0, 150)
+    assert hl.dualar_share_prefix(h.h, 0, 1, 150) == OK
+    po.share(0, 1, 150)
+    assert h.decode([1, 0]) == OK
+    po.append(1, 1)
+    po.append(0, 1)
+    assert hl.dualar_debug_synthetic_context(h.h, 2, 130, 7) == OK
+    po.append(2, 130)
+    check_tables(h, po)
+    assert hl.dualar_debug_synthetic_context(h.h, 2, 10, 7) == BUSY
+    assert hl.dualar_debug_synthetic_context(h.h, 3, 401, 7) == FULL
+    check_tables(h, po)
+    h.close()
