@@ -13,7 +13,7 @@ the host-side bookkeeping the GPU tests also cover, now on the CPU:
   SLOT_EMPTY, OOM_PAGES and CONTEXT_FULL, each leaving the state unchanged;
 - the 4-bit weight selection's argument checks.
 
-This build never ships: the library itself is built only by nvcc for
+The stand-in library never ships: the library itself is built only by nvcc for
 sm_103a and has no CPU path.
 """
 import ctypes
