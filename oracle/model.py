@@ -30,10 +30,15 @@ its reason, in the design notes):
     the fast AR, fuses the codes and runs one slow position on the fused
     vector;
   * the slow AR's KV cache holds bf16 values: K (after QK-norm and RoPE) and
-    V are rounded to bf16 (nearest even) when appended, as in a model whose
-    checkpoint and serving are all bf16 ([P2] "Two autoregressions", the fact
-    table: all parameters BF16; "Streaming: whose numbers": the model runs
-    on bf16 tables).  The fast AR's per-frame cache stays float32.
+    V are rounded to bf16 (nearest even) when appended.  The pages do not say
+    what precision the cache has: their fact table ([P2] "Two
+    autoregressions") gives the checkpoint's parameters as BF16, and [P2]
+    "Streaming: whose numbers" says the model runs on bf16 tables, which
+    suggests, without stating it, a model served in bf16 throughout.  This is
+    a departure from a pure "fp32 activations over bf16 weights" oracle, taken
+    for the cache only; slow_kv_bf16=False gives that pure form, and the
+    full-size parity test reports how far the two lie apart.  The fast AR's
+    per-frame cache stays float32.
 
 Precision: every activation is float32; weights are bf16 widened exactly to
 float32; the slow KV cache holds bf16 values (widened to float32), the fast
@@ -251,12 +256,17 @@ class FrameResult:
 
 class DualAROracle:
     def __init__(self, cfg: DualARConfig, weight_bits: dict[str, np.ndarray],
-                 max_pos: int = 20_000, w4a16_keys: list[str] | None = None):
-        """w4a16_keys: projections (generator keys such as "slow.0.wqkv") that
+                 max_pos: int = 20_000, w4a16_keys: list[str] | None = None,
+                 slow_kv_bf16: bool = True):
+        """slow_kv_bf16: whether the slow AR's cache holds bf16 values (the
+        reading this oracle takes); False keeps it in float32, so a test can
+        show how far that reading moves the results.
+        w4a16_keys: projections (generator keys such as "slow.0.wqkv") that
         the model reads through the 4-bit rule of oracle.w4a16 ([P3]
         "s2-pro-w4a16-late12attn", opening line): each such matrix is
         replaced by its quantised-then-dequantised float32 values."""
         self.cfg = cfg
+        self.slow_kv_bf16 = slow_kv_bf16
         self.w = Weights(cfg, weight_bits)
         if w4a16_keys:
             from .w4a16 import dequantize, quantize
@@ -275,7 +285,8 @@ class DualAROracle:
         h = np.asarray(x, np.float32)
         for i, lw in enumerate(self.w.slow):
             k, v = seq.kv[i]
-            h, k, v = block(cfg, lw, h, seq.pos, k, v, self.cos, self.sin, cfg.slow_qk_norm, kv_bf16=True)
+            h, k, v = block(cfg, lw, h, seq.pos, k, v, self.cos, self.sin, cfg.slow_qk_norm,
+                            kv_bf16=self.slow_kv_bf16)
             seq.kv[i] = [k, v]
         seq.pos += h.shape[0]
         return rmsnorm(h, self.w.final_norm, cfg.norm_eps)
@@ -408,7 +419,7 @@ class DualAROracle:
         kv = empty_kv(cfg, cfg.n_layer)
         for i, lw in enumerate(self.w.slow):
             h, _, _ = block(cfg, lw, h, 0, kv[i][0], kv[i][1], self.cos, self.sin, cfg.slow_qk_norm,
-                            kv_bf16=True)
+                            kv_bf16=self.slow_kv_bf16)
         return rmsnorm(h, self.w.final_norm, cfg.norm_eps)
 
     def fast_full_recompute(self, h_slow: np.ndarray, codes: np.ndarray) -> np.ndarray:

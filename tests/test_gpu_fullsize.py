@@ -6,7 +6,9 @@ the persistent frame kernel, with the benchmark's weights (seed 0), its
 top-p 0.8, repetition-aware window 10, <|im_end|> excluded).  The oracle
 computes the same frames one by one on the host:
 
-- the state left by the prefill (final-normed hidden, restricted logits);
+- the state left by the prefill (final-normed hidden, restricted logits),
+  and, printed beside it, the distance of the GPU's prefill logits from an
+  oracle whose slow cache stays float32 instead of bf16;
 - three sampled frames, then two greedy ones (T = 0, no resample),
   replayed in the oracle along the GPU's trajectory:
   slow and fast logits within the tolerance; every GPU draw equal to the
@@ -75,6 +77,16 @@ def test_s2pro_b1_prefill_sampled_and_greedy_frames_match_oracle():
     seq = o.prefill(prompt)
     assert_logits_close(gh, seq.h_last, "prefill hidden")
     assert_logits_close(gz, seq.z_last, "prefill logits")
+    # What the bf16 slow-cache reading is worth: the same prefill with a
+    # float32 cache, reported (not asserted) against the GPU.
+    o.slow_kv_bf16 = False
+    z32 = o.prefill(prompt).z_last
+    o.slow_kv_bf16 = True
+    d32 = np.asarray(gz, np.float64) - z32
+    dbf = np.asarray(gz, np.float64) - seq.z_last
+    print(f"prefill logits vs oracle: bf16 cache max abs {np.abs(dbf).max():.4g} rel L2 "
+          f"{np.linalg.norm(dbf) / np.linalg.norm(seq.z_last):.3g}; float32 cache max abs "
+          f"{np.abs(d32).max():.4g} rel L2 {np.linalg.norm(d32) / np.linalg.norm(z32):.3g}")
     stats = DrawStats()      # oracle logits, draws stable under the measured eps
     samp = DrawStats()       # oracle sampler on the GPU's own logits
     greedy_compared = 0

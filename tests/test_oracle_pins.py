@@ -5,6 +5,7 @@ figures the pages print (tests/golden/pages_facts.txt), closed forms,
 invariants, or brute-force enumeration.  Tests at the end plant mistakes in
 the oracle (on the CPU) and check that a pin catches each of them.
 """
+import dataclasses
 import itertools
 import math
 import os
@@ -184,6 +185,108 @@ def test_silu_values():
     assert y[0] == 0.0
     assert abs(y[1] - 0.7310585786300049) < 1e-7       # logistic(1)
     assert abs(y[2] - 30.0) < 1e-5 and abs(y[3]) < 1e-10
+
+
+# ------------------------------------------------- one transformer block --
+#
+# A block on hand-set weights small enough to work out by hand: width 4,
+# four query heads over two KV heads of size 2, FFN width 4.  Every expected
+# number below is the closed form written beside it, not a call into the
+# oracle.  [P1] "Fast Transformer: The Codebook Decoder" (pre-norm
+# TransformerBlock: attention then SwiGLU FFN, each added to the residual);
+# [P2] "The slow AR is Qwen3-4B" (fused q/k/v projection in q, k, v order;
+# GQA; qk-norm).
+
+BLOCK_CFG = dataclasses.replace(TINY, name="block_pin", dim=4, n_head=4, n_kv_head=2, head_dim=2, ffn=4)
+
+
+def _block_weights_a(qk_norm: bool) -> om.LayerW:
+    """Attention with one key returns its value row unchanged, whatever q
+    and k are; the weights route one value component into the residual and
+    drive the SwiGLU gate to the closed-form points SiLU(0), SiLU(2), SiLU(+-20)."""
+    f = np.float32
+    wqkv = np.zeros((16, 4), f)
+    wqkv[0:8] = np.random.default_rng(3).standard_normal((8, 4))   # q: irrelevant with one key
+    wqkv[8, 0], wqkv[9, 2], wqkv[10, 0], wqkv[11, 2] = -5, 7, 1, 3    # k_h0 = (-5, 7), k_h1 = (1, 3)
+    wqkv[12, 0], wqkv[13, 3], wqkv[14, 0], wqkv[15, 0] = 2, -0.25, -1, 3   # v_h0 = (2, .5), v_h1 = (-1, 3)
+    wo = np.zeros((4, 8), f)
+    wo[1, 2], wo[1, 3] = 1, 4          # head 1's output (= v_h0) -> 2 + 4 * 0.5 = 4 into h[1]
+    return om.LayerW(
+        attn_norm=np.array([1, 1, 1, 2], f), wqkv=wqkv,
+        q_norm=np.array([0.5, 3], f) if qk_norm else None,
+        k_norm=np.array([2, 0.5], f) if qk_norm else None,
+        wo=wo, ffn_norm=np.array([1, 2, 1, 1], f),
+        w_gate=np.diag([0, 1, 20, 20]).astype(f), w_up=np.diag([5, 3, 2, -7]).astype(f),
+        w_down=np.eye(4, dtype=f))
+
+
+def test_block_single_position_closed_form():
+    """h = (2,-2,2,-2): RMSNorm gives u = (1,-1,1,-2) (rms 2, gain (1,1,1,2)),
+    so k = (-5,7 | 1,3) and v = (2,.5 | -1,3).  One key: every query head
+    outputs its KV head's v, so heads are (v_h0, v_h0, v_h1, v_h1) and wo adds
+    4 to h[1]: h' = (2,2,2,-2).  RMSNorm(h') with gain (1,2,1,1) is
+    (1,2,1,-1); gate = (0,2,20,-20), up = (5,6,2,7), down = I:
+    h_out = h' + (0, 12 L(2), 40 L(20), -140 L(-20)), L the logistic."""
+    cfg = BLOCK_CFG
+    cos, sin = om.rope_table(4, cfg.head_dim, cfg.rope_base)
+    h = np.array([[2, -2, 2, -2]], np.float32)
+    empty = np.zeros((0, 2, 2), np.float32)
+    expect = np.array([2.0, 12.569564935734588, 41.99999991755385, -2.0000002885615067])
+    for kv_bf16 in (False, True):
+        out, kc, vc = om.block(cfg, _block_weights_a(False), h, 0, empty, empty, cos, sin,
+                               qk_norm=False, kv_bf16=kv_bf16)
+        np.testing.assert_allclose(out[0], expect, rtol=1e-6, atol=2e-6)
+        np.testing.assert_allclose(kc[0], [[-5, 7], [1, 3]], rtol=1e-6)
+        np.testing.assert_allclose(vc[0], [[2, 0.5], [-1, 3]], rtol=1e-6)
+    # the rounded cache holds the bf16 neighbours exactly: 5 * (1 - 1.25e-7) -> 5
+    assert kc[0].tolist() == [[-5, 7], [1, 3]] and vc[0].tolist() == [[2, 0.5], [-1, 3]]
+
+
+def test_block_qk_norm_is_per_head_before_the_cache():
+    """With qk-norm, each K head is RMS-normalised over head_dim and scaled by
+    the k_norm gain (2, .5) before it is cached (position 0: RoPE is the
+    identity): (-5,7)/sqrt(37) * (2,.5) and (1,3)/sqrt(5) * (2,.5).  V and,
+    with one key, the block output are unchanged."""
+    cfg = BLOCK_CFG
+    cos, sin = om.rope_table(4, cfg.head_dim, cfg.rope_base)
+    h = np.array([[2, -2, 2, -2]], np.float32)
+    empty = np.zeros((0, 2, 2), np.float32)
+    out, kc, vc = om.block(cfg, _block_weights_a(True), h, 0, empty, empty, cos, sin, qk_norm=True)
+    np.testing.assert_allclose(kc[0], [[-1.643989873053573, 0.5753964555687505],
+                                       [0.8944271909999159, 0.6708203932499369]], rtol=2e-6)
+    np.testing.assert_allclose(vc[0], [[2, 0.5], [-1, 3]], rtol=1e-6)
+    np.testing.assert_allclose(out[0], [2.0, 12.569564935734588, 41.99999991755385, -2.0000002885615067],
+                               rtol=1e-6, atol=2e-6)
+
+
+def test_block_two_positions_attention_weights():
+    """Two positions, RoPE tables set to the identity, gate = 0 (so the FFN
+    adds SiLU(0) * up = 0 exactly).  Row 0 sees only key 0; row 1 sees keys 0
+    and 1 with scores q.k / sqrt(2).  k = (u[1], 0) per KV head, so the keys
+    are (-1,0) then (1,0); query head 0 is (b, 0) with b = ln 3 / sqrt(2),
+    giving weights (1/4, 3/4); head 3 is (-b, 0): (3/4, 1/4); heads 1, 2 are 0:
+    (1/2, 1/2).  v_h0 = (u[1], 0), v_h1 = (0, 2 u[3]).  wo picks one output
+    component of each head: (a0[0], a3[1], a1[0], a2[1])."""
+    cfg = BLOCK_CFG
+    f = np.float32
+    b = f(0.7768361992120932)
+    wqkv = np.zeros((16, 4), f)
+    wqkv[0, 0], wqkv[6, 0] = b, -b
+    wqkv[8, 1], wqkv[10, 1] = 1, 1
+    wqkv[12, 1], wqkv[15, 3] = 1, 2
+    wo = np.zeros((4, 8), f)
+    wo[0, 0], wo[1, 7], wo[2, 2], wo[3, 5] = 1, 1, 1, 1
+    rng = np.random.default_rng(4)
+    lw = om.LayerW(attn_norm=np.ones(4, f), wqkv=wqkv, q_norm=None, k_norm=None, wo=wo,
+                   ffn_norm=np.ones(4, f), w_gate=np.zeros((4, 4), f),
+                   w_up=rng.standard_normal((4, 4)).astype(f), w_down=rng.standard_normal((4, 4)).astype(f))
+    cos, sin = np.ones((2, 1), f), np.zeros((2, 1), f)
+    h = np.array([[2, -2, 2, -2], [2, 2, 2, 2]], f)
+    empty = np.zeros((0, 2, 2), f)
+    out, kc, vc = om.block(cfg, lw, h, 0, empty, empty, cos, sin, qk_norm=False)
+    # row 0: heads (v_h0, v_h0, v_h1, v_h1) at position 0 = ((-1,0), (-1,0), (0,-2), (0,-2))
+    # row 1: head 0 (-1/4 + 3/4, 0), head 1 (0, 0), head 2 (0, 0), head 3 (0, -3/2 + 1/2)
+    np.testing.assert_allclose(out, [[1, -4, 1, -4], [2.5, 1, 2, 2]], rtol=1e-6, atol=2e-6)
 
 
 # ------------------------------------------------ incremental == recompute --
@@ -546,6 +649,92 @@ def test_planted_fusion_scale_error_is_caught(monkeypatch):
     def bad(self, codes):
         return orig(self, codes) * math.sqrt(self.cfg.n_codebooks + 1) / math.sqrt(self.cfg.n_codebooks)
     _expect_pin_failure(monkeypatch, om.DualAROracle, "fuse", bad, test_fusion_unit_rows_closed_form)
+
+
+_BLOCK_PINS = (test_block_single_position_closed_form, test_block_qk_norm_is_per_head_before_the_cache,
+               test_block_two_positions_attention_weights)
+
+
+def _expect_block_pins_fail(monkeypatch, bad):
+    """A mistaken block must fail at least one of the block pins."""
+    monkeypatch.setattr(om, "block", bad)
+    failed = 0
+    for pin in _BLOCK_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    monkeypatch.undo()
+    assert failed, "no block pin caught the planted mistake"
+
+
+def _with(w, **kw):
+    return dataclasses.replace(w, **kw)
+
+
+def _qkv_rows(cfg, order):
+    """Row permutation of wqkv that makes a correct block read it in another
+    layout: "kv" swaps the k and v row blocks; "grouped" reads each KV group
+    as [its query heads, its k, its v] in turn."""
+    q, kv = cfg.q_dim, cfg.kv_dim
+    if order == "kv":
+        return list(range(q)) + list(range(q + kv, q + 2 * kv)) + list(range(q, q + kv))
+    g = cfg.n_head // cfg.n_kv_head
+    hd = cfg.head_dim
+    per = (g + 2) * hd
+    qs, ks, vs = [], [], []
+    for j in range(cfg.n_kv_head):
+        base = j * per
+        qs += list(range(base, base + g * hd))
+        ks += list(range(base + g * hd, base + (g + 1) * hd))
+        vs += list(range(base + (g + 1) * hd, base + per))
+    return qs + ks + vs
+
+
+def test_planted_block_gate_up_swap_is_caught(monkeypatch):
+    orig = om.block
+
+    def bad(cfg, w, *a, **k):          # SiLU(up) * gate
+        return orig(cfg, _with(w, w_gate=w.w_up, w_up=w.w_gate), *a, **k)
+    _expect_block_pins_fail(monkeypatch, bad)
+
+
+def test_planted_block_ffn_reads_pre_attention_state_is_caught(monkeypatch):
+    orig = om.block
+
+    def bad(cfg, w, h, *a, **k):       # h + attn(h) + FFN(RMSNorm(h))
+        ha, kc, vc = orig(cfg, _with(w, w_gate=np.zeros_like(w.w_gate)), h, *a, **k)
+        hf, _, _ = orig(cfg, _with(w, wo=np.zeros_like(w.wo)), h, *a, **k)
+        return ha + hf - h, kc, vc
+    _expect_block_pins_fail(monkeypatch, bad)
+
+
+def test_planted_block_ffn_norm_gain_mixup_is_caught(monkeypatch):
+    orig = om.block
+
+    def bad(cfg, w, *a, **k):          # the FFN normalised with the attention gain
+        return orig(cfg, _with(w, ffn_norm=w.attn_norm), *a, **k)
+    _expect_block_pins_fail(monkeypatch, bad)
+
+
+@pytest.mark.parametrize("order", ["kv", "grouped"])
+def test_planted_block_qkv_row_order_is_caught(monkeypatch, order):
+    orig = om.block
+
+    def bad(cfg, w, *a, **k):
+        return orig(cfg, _with(w, wqkv=w.wqkv[_qkv_rows(cfg, order)]), *a, **k)
+    _expect_block_pins_fail(monkeypatch, bad)
+
+
+def test_planted_block_missing_attention_scale_is_caught(monkeypatch):
+    orig_attn = om.gqa_attention
+
+    def bad(q, k, v, n_rep, causal_offset=None):
+        return orig_attn(q * np.float32(math.sqrt(q.shape[-1])), k, v, n_rep, causal_offset)
+    monkeypatch.setattr(om, "gqa_attention", bad)
+    with pytest.raises(AssertionError):
+        test_block_two_positions_attention_weights()
+    monkeypatch.undo()
 
 
 def test_planted_top_p_off_by_one_is_caught(monkeypatch):
