@@ -328,6 +328,49 @@ class DualAROracle:
         seq.z_last = self.restricted_logits(hn[-1])
         return seq
 
+    def prefill_one_layer(self, tokens: np.ndarray, chunk: int = 2048) -> SeqState:
+        """prefill() of a slow stack with exactly one layer, by the short route.
+
+        With one layer, the K and V that position t leaves in the cache are
+        the layer's projections of its own input e_LM[tok_t] (RMSNorm, the k
+        and v rows of wqkv, QK-norm on k, RoPE at t, the cache rounding): no
+        other position enters them.  Only the last position's output is kept
+        after a prefill, so positions 0..n-2 need their K and V and nothing
+        else, and the last position runs the whole block over that cache.
+        The result equals prefill() up to the order of float rounding (a
+        test compares the two on a one-layer model); it costs a fifth of the
+        projections and no attention over the prompt, which is what makes
+        prompts of many thousands of tokens affordable on the host."""
+        cfg = self.cfg
+        assert cfg.n_layer == 1, "the short route holds for one slow layer only"
+        lw = self.w.slow[0]
+        tokens = np.asarray(tokens, np.int64)
+        n = tokens.size
+        hkv, hd = cfg.n_kv_head, cfg.head_dim
+        wk = lw.wqkv[cfg.q_dim:cfg.q_dim + cfg.kv_dim]
+        wv = lw.wqkv[cfg.q_dim + cfg.kv_dim:]
+        ks, vs = [], []
+        for c0 in range(0, n - 1, chunk):
+            c1 = min(c0 + chunk, n - 1)
+            u = rmsnorm(self.w.tok_emb[tokens[c0:c1]], lw.attn_norm, cfg.norm_eps)
+            k = (u @ wk.T).reshape(c1 - c0, hkv, hd)
+            v = (u @ wv.T).reshape(c1 - c0, hkv, hd)
+            if cfg.slow_qk_norm:
+                k = rmsnorm(k, lw.k_norm, cfg.norm_eps)
+            k = apply_rope(k, np.arange(c0, c1), self.cos, self.sin)
+            if self.slow_kv_bf16:
+                k, v = bf16_round(k), bf16_round(v)
+            ks.append(k.astype(np.float32))
+            vs.append(v.astype(np.float32))
+        seq = self.new_sequence()
+        if ks:
+            seq.kv[0] = [np.concatenate(ks), np.concatenate(vs)]
+        seq.pos = n - 1
+        hn = self.slow_rows(seq, self.w.tok_emb[tokens[-1:]])
+        seq.h_last = hn[-1].copy()
+        seq.z_last = self.restricted_logits(hn[-1])
+        return seq
+
     # ---- fast AR ---------------------------------------------------------
     def fast_forward(self, x: np.ndarray, pos: int, kv: list) -> np.ndarray:
         """One fast pass: the fast layers on one row at codebook position pos."""

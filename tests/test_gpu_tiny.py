@@ -275,6 +275,55 @@ def test_eos_and_finished_slot(dec):
     assert status.cpu().tolist() == [0]
 
 
+@pytest.mark.parametrize("rows", [2, 3])
+def test_replacement_flow_matches_oracle(dec, tiny_oracle, rows):
+    """A sequence finishes (forced <|im_end|>), its slot is released and
+    restarted from a queued prompt, and the batch decodes on: every live
+    row's slow and fast logits match the oracle (the restarted one against a
+    fresh oracle sequence), statuses and codes are exact, and the page tables
+    follow the page oracle through the release and the new prefill (the
+    freed pages are taken again, lowest first)."""
+    o = tiny_oracle
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=True)
+    lens = [30, 70, 45][:rows]
+    prompts = {s: g.make_prompt(TINY, n, seed=60 + s) for s, n in enumerate(lens)}
+    queued = g.make_prompt(TINY, 90, seed=69)
+    slots = list(range(rows))
+    pages = PageOracle(dec.max_pages, TINY.page_tokens)
+    seqs = {}
+    for s in slots:
+        dec.prefill(s, prompts[s])
+        seqs[s] = o.prefill(prompts[s])
+        pages.append(s, lens[s])
+    forced = g.make_forced_codes(4, rows, TINY, seed=61)
+    forced[1, 0, 0] = TINY.n_sem               # slot 0 ends at frame 1
+    uni = g.make_uniforms(4, rows, TINY, seed=62)
+    for f in range(4):
+        codes, status, slow, fast, _ = dec.decode_frame_forced(slots, dev(uni[f]), gpu_sampling(smp),
+                                                               dev(forced[f]))
+        dec.sync()
+        codes, status = codes.cpu().numpy(), status.cpu().numpy()
+        slow, fast = slow.cpu().numpy(), fast.cpu().numpy()
+        for i, s in enumerate(slots):
+            r = o.decode_frame(seqs[s], uni[f, i], smp, forced=forced[f, i])
+            assert status[i] == r.status
+            np.testing.assert_array_equal(codes[i], r.codes)
+            assert_logits_close(slow[i], r.slow_logits, f"slow logits f{f} slot {s}")
+            if r.status == 0:
+                assert_logits_close(fast[i], r.fast_logits, f"fast logits f{f} slot {s}")
+                pages.append(s, 1)
+        if f == 1:
+            assert status[0] == 1
+            dec.release(0)
+            pages.release(0)
+            dec.prefill(0, queued)
+            seqs[0] = o.prefill(queued)
+            pages.append(0, len(queued))
+        for s in slots:
+            assert dec.page_table(s) == pages.table[s], f"page table of slot {s} after frame {f}"
+    assert dec.slot_length(0) == len(queued) + 2
+
+
 def test_eos_excluded_when_disallowed(dec):
     """allow_eos = 0 removes <|im_end|> from the q0 candidates: with greedy
     sampling and the held logits unchanged, q0 is never <|im_end|>."""

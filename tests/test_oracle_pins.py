@@ -330,6 +330,33 @@ def test_fast_incremental_equals_full_recompute(tiny_oracle):
     np.testing.assert_allclose(logits, full, rtol=1e-4, atol=1e-5)
 
 
+@pytest.mark.parametrize("n", [1, 2, 64, 300])
+def test_one_layer_prefill_route_equals_prefill(n):
+    """With one slow layer, the short prefill route (K/V of the prompt rows
+    from their own inputs, the whole block for the last row only) leaves the
+    same cache and state as the plain prefill, with either cache precision,
+    and the next frame matches."""
+    cfg = dataclasses.replace(TINY, n_layer=1)
+    bits = g.make_weights(cfg, seed=0)
+    prompt = g.make_prompt(cfg, n, seed=40 + n)
+    for kv_bf16 in (True, False):
+        o = oracle.DualAROracle(cfg, bits, max_pos=512, slow_kv_bf16=kv_bf16)
+        a = o.prefill(prompt)
+        b = o.prefill_one_layer(prompt, chunk=48)
+        assert a.pos == b.pos == n
+        for x, y in zip(a.kv[0], b.kv[0]):
+            assert x.shape == y.shape
+            np.testing.assert_allclose(x, y, rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(b.h_last, a.h_last, rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(b.z_last, a.z_last, rtol=1e-5, atol=1e-5)
+        f = g.make_forced_codes(1, 1, cfg, seed=41)[0, 0]
+        u = g.make_uniforms(1, 1, cfg, seed=42)[0, 0]
+        ra = o.decode_frame(a, u, Sampling(allow_eos=False), forced=f)
+        rb = o.decode_frame(b, u, Sampling(allow_eos=False), forced=f)
+        np.testing.assert_allclose(rb.fast_logits, ra.fast_logits, rtol=1e-4, atol=1e-4)
+        np.testing.assert_allclose(b.z_last, a.z_last, rtol=1e-4, atol=1e-4)
+
+
 def _rne_8bit(x: np.ndarray) -> np.ndarray:
     """Round to 8 significant bits, ties to even, via frexp (normal numbers)."""
     m, e = np.frexp(np.asarray(x, np.float64))

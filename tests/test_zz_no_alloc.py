@@ -57,6 +57,45 @@ def test_noalloc_decode_matches_decode_frame(dev_weights):
     d.close()
 
 
+def test_noalloc_batch3_full_width_matches_decode_frame():
+    """Three sequences at the full model width (one layer each of the slow
+    and fast stacks), the largest batch the fixed array takes at that shape:
+    the attention runs on the tensor cores with its partials and arrival
+    counters in the array, over contexts of 11 to 46 pages (one page per
+    split-KV chunk at this batch).  Two calls in a row against the ordinary
+    call on copies of the same sequences."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling, build, upload_weights
+    from dualar_inputs.config import S2PRO_L1
+    build()
+    cfg = S2PRO_L1
+    w = upload_weights(g.make_weights(cfg, seed=0))
+    lens = (700, 1500, 2900)
+    d = DualARDecoder(cfg, w, max_pages=2 * sum(-(-(n + 4) // 64) for n in lens) + 4, max_seqs=6, max_ctx=3000)
+    for i, n in enumerate(lens):
+        p = g.make_prompt(cfg, n, seed=33 + i)
+        d.prefill(i, p)          # decoded with dualar_decode_frame
+        d.prefill(3 + i, p)      # decoded with dualar_decode_frame_noalloc
+    smp = Sampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
+    uni = torch.from_numpy(g.make_uniforms(2, 3, cfg, seed=36)).cuda()
+    codes_b = torch.empty((3, cfg.n_codebooks), dtype=torch.int32, device="cuda")
+    status_b = torch.empty((3,), dtype=torch.int32, device="cuda")
+    for call in range(2):
+        codes_a, status_a = d.decode_frame([0, 1, 2], uni[call], smp)
+        d.decode_frame_noalloc([3, 4, 5], uni[call], smp, codes_b, status_b)
+        d.sync()
+        assert d.last_launch_count() > 2
+        np.testing.assert_array_equal(codes_b.cpu().numpy(), codes_a.cpu().numpy())
+        np.testing.assert_array_equal(status_b.cpu().numpy(), 0)
+        for i in range(3):
+            ha, za = d.read_state(i)
+            hb, zb = d.read_state(3 + i)
+            assert_logits_close(zb, za, f"held logits, row {i}, call {call}")
+            assert_logits_close(hb, ha, f"held hidden state, row {i}, call {call}")
+    d.close()
+
+
 def test_noalloc_rejects_batches_beyond_the_array(dev_weights):
     from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling
     from dual_ar_tts_frame_gb300._lib import DualARError
