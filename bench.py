@@ -38,7 +38,7 @@ METRIC = "Dual-AR frames/s (and RTF) at batch 1 and 64 on 1 GB300; % of HBM roof
 
 WORKLOADS = {
     "s2pro_b1": dict(cfg="s2pro", batch=1, prompt=512, frames=256, temperature=0.8, top_p=0.8,
-                     ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 1, 512-token prompt, 256 frames, "
+                     ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 1, 512-token prompt, "
                                        "T=0.8 top-p 0.8 RAS window 10"),
     "s2pro_l1_b1": dict(cfg="s2pro_l1", batch=1, prompt=512, frames=16, temperature=0.8, top_p=0.8,
                         ras_win=10, desc="one-layer S2-Pro-shaped profiling case, batch 1, 512-token prompt"),
@@ -51,7 +51,7 @@ WORKLOADS = {
                                                 "[2048, 4096] that finish at seeded frames (uniform in [1, 64]) and "
                                                 "are replaced from a seeded queue, plus 4 resident contexts of 16384"),
     "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
-                    desc="tiny Dual-AR, batch 1, 32-token prompt, 16 frames"),
+                    desc="tiny Dual-AR, batch 1, 32-token prompt"),
 }
 
 
@@ -64,7 +64,8 @@ def parse():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="s2pro_b1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-b64", action="store_true", help="skip the batch-64 measurement")
+    ap.add_argument("--no-batches", action="store_true",
+                    help="skip the batch-16, batch-64 and batch-128 measurements")
     ap.add_argument("--no-w4a16", action="store_true", help="skip the 4-bit-weight measurement")
     return ap.parse_args()
 
@@ -172,9 +173,10 @@ def replica_throughput(units_per_rank: float, world_size: int, slowest_s: float)
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def time_oracle(cfg, bits, wl, prompt, uniforms, n_frames, budget_s):
-    from oracle import DualAROracle, Sampling as OSampling
-    o = DualAROracle(cfg, bits, max_pos=wl["prompt"] + wl["frames"] + 8)
+def time_oracle(o, wl, prompt, uniforms, n_frames, budget_s):
+    """The oracle's decode frames/s on one sequence after a prefill of the
+    workload's prompt (prefill untimed)."""
+    from oracle import Sampling as OSampling
     seq = o.prefill(prompt)
     smp = OSampling(temperature=wl["temperature"], top_p=wl["top_p"], ras_win=wl["ras_win"], allow_eos=False)
     done = 0
@@ -188,19 +190,78 @@ def time_oracle(cfg, bits, wl, prompt, uniforms, n_frames, budget_s):
     return done, el
 
 
+def oracle_synthetic_sequence(o, cfg, n_tokens: int, seed: int):
+    """An oracle sequence holding a context of n_tokens positions without a
+    prefill (a 36-layer prefill of thousands of tokens takes the host far
+    longer than the decode it precedes): cached K/V values seeded in [-1, 1)
+    and rounded to bf16 (one layer's worth, which every layer starts from:
+    the oracle appends by copying and never writes a cache in place), the
+    held hidden state seeded in [-1, 1) and the held logits the restricted
+    head's of it.  The values do not matter for timing; the shapes are the
+    workload's."""
+    from oracle import SeqState
+    u = gen.gen_uniform((2, n_tokens, cfg.n_kv_head, cfg.head_dim), seed, "oracle_ctx:kv")
+    x = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits((2.0 * u - 1.0).astype(np.float32)))
+    kv = [[x[0], x[1]] for _ in range(cfg.n_layer)]
+    h = (2.0 * gen.gen_uniform((cfg.dim,), seed, "oracle_ctx:h") - 1.0).astype(np.float32)
+    return SeqState(kv=kv, pos=n_tokens, h_last=h, z_last=o.restricted_logits(h))
+
+
+def time_oracle_batch(o, cfg, contexts, frames: int, budget_s: float) -> dict:
+    """Teacher-forced oracle frames on sequences of the given context lengths,
+    one after another (the oracle decodes a batch one sequence at a time, so
+    its batch throughput is its per-sequence rate)."""
+    from oracle import Sampling as OSampling
+    smp = OSampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
+    per, total_f, total_s = [], 0, 0.0
+    for i, n in enumerate(contexts):
+        seq = oracle_synthetic_sequence(o, cfg, int(n), seed=7000 + i)
+        forced = gen.make_forced_codes(frames, 1, cfg, seed=8000 + i)
+        uni = gen.make_uniforms(frames, 1, cfg, seed=9000 + i)
+        done = 0
+        t0 = time.perf_counter()
+        for f in range(frames):
+            o.decode_frame(seq, uni[f, 0], smp, forced=forced[f, 0])
+            done += 1
+            if time.perf_counter() - t0 > budget_s / len(contexts):
+                break
+        el = time.perf_counter() - t0
+        per.append({"context": int(n), "frames": done, "frames_per_s": done / el})
+        total_f += done
+        total_s += el
+        del seq
+    return {"value": total_f / total_s, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{total_f} teacher-forced frames over {len(contexts)} sequences of contexts "
+                      f"{', '.join(str(int(c)) for c in contexts)} (synthetic cached K/V, no prefill), "
+                      f"NumPy fp32 on {os.cpu_count()} host threads",
+            "per_sequence": per}
+
+
 # ---------------------------------------------------------------------------
 
-def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
-    """Batch 64 (the full-size batch-64 workload): 64 sequences with contexts
-    uniform in [1,024, 4,096] (seed 3) set up by the synthetic-context hook
-    (seeded K/V and held state, no prefill), then `warmup` + `frames` decode
-    steps with seeded uniforms (seed 1), T 0.8, top-p 0.8, resample window 10,
-    <|im_end|> excluded.  Device-timed with CUDA events."""
+BATCH_CONTEXTS = {
+    16: dict(lo=512, hi=2048, seed=2, stream="ctx_b16"),
+    64: dict(lo=1024, hi=4096, seed=3, stream="ctx_b64"),
+}
+
+
+def batch_contexts(b: int) -> np.ndarray:
+    c = BATCH_CONTEXTS[b]
+    return gen.make_lengths(b, c["lo"], c["hi"], seed=c["seed"], stream=c["stream"])
+
+
+def measure_batch(cfg, w, b: int, frames: int, warmup: int, peak: float) -> dict:
+    """A continuous batch of b sequences (b = 16: contexts uniform in [512,
+    2,048], seed 2; b = 64: [1,024, 4,096], seed 3) set up by the
+    synthetic-context hook (seeded K/V and held state, no prefill), then
+    `warmup` + `frames` decode steps with seeded uniforms (seed 1), T 0.8,
+    top-p 0.8, resample window 10, <|im_end|> excluded.  Device-timed with
+    CUDA events."""
     import torch
     from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling
     from dual_ar_tts_frame_gb300 import bytemodel
-    b = 64
-    ctx = gen.make_lengths(b, 1024, 4096, seed=3, stream="ctx_b64")
+    ctx = batch_contexts(b)
+    lim = BATCH_CONTEXTS[b]
     max_ctx = int(ctx.max()) + warmup + frames + 8
     pages = sum(-(-(int(c) + warmup + frames + 1) // cfg.page_tokens) for c in ctx) + 8
     dec = DualARDecoder(cfg, w, max_pages=pages, max_seqs=b, max_ctx=max_ctx)
@@ -230,13 +291,18 @@ def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
     bytes_total = sum(bytemodel.frame_bytes(cfg, [int(c) + f + 1 for c in ctx]) for f in range(warmup, warmup + frames))
     gbs = bytes_total / (ms / 1000.0) / 1e9
     dec.close()
-    return {"workload": "full S2-Pro-shaped Dual-AR, batch 64, contexts uniform in [1024, 4096] (seed 3, "
-                        "synthetic K/V and held state, no prefill), T=0.8 top-p 0.8 RAS window 10",
+    return {"workload": f"full S2-Pro-shaped Dual-AR, batch {b}, contexts uniform in [{lim['lo']}, {lim['hi']}] "
+                        f"(seed {lim['seed']}, synthetic K/V and held state, no prefill), T=0.8 top-p 0.8 "
+                        f"RAS window 10; {warmup + frames} steps ({warmup} warm-up, {frames} timed)",
             "value": b * frames / (ms / 1000.0), "unit": "frames/s", "steps": frames, "warmup": warmup,
             "ms_per_step": ms / frames, "rtf": FRAMES_PER_AUDIO_SECOND / (frames / (ms / 1000.0)),
             "frame_bytes_per_step": bytes_total / frames,
             "frame_roofline": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
             "gpu_launches_per_step": launches}
+
+
+def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
+    return measure_batch(cfg, w, 64, frames, warmup, peak)
 
 
 def measure_replacement(cfg, w, frames: int, peak: float, with_prefill: bool) -> dict:
@@ -407,7 +473,8 @@ def main():
     assert W >= 0 and K >= 1
     prompt = gen.make_prompt(cfg, wl["prompt"], seed=0)
     uni_all = gen.make_uniforms(W + K, wl["batch"], cfg, seed=1)
-    config = {"workload": f"{args.workload}: {wl['desc']}", "batch": wl["batch"],
+    config = {"workload": f"{args.workload}: {wl['desc']}; {W + K} frames ({W} warm-up, {K} timed)",
+              "batch": wl["batch"],
               "prompt_tokens": wl["prompt"], "frames": W + K,
               "l2": "inputs larger than L2 (9.1 GB of weights streamed per frame); no flush"}
     if args.workload != "s2pro_b1":
@@ -443,7 +510,9 @@ def main():
         if rank != 0:
             return
         bits = gen.make_weights(cfg, seed=0)
-        done, el = time_oracle(cfg, bits, wl, prompt, uni_all, W + K, budget_s=150.0)
+        from oracle import DualAROracle
+        o = DualAROracle(cfg, bits, max_pos=wl["prompt"] + W + K + 8)
+        done, el = time_oracle(o, wl, prompt, uni_all, W + K, budget_s=150.0)
         fps = done / el
         cores = os.cpu_count()
         line = {"impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": ws,
@@ -567,20 +636,31 @@ def main():
                "d2h_bytes_per_step": hc.numel() * 4 + hs.numel() * 4}
 
     dec.close()
-    b64 = None
-    if args.workload == "s2pro_b1" and not args.no_b64:
+    b16 = b64 = b128 = None
+    if args.workload == "s2pro_b1" and not args.no_batches:
+        b16 = measure_batch(cfg, w, 16, frames=24, warmup=4, peak=peak)
         b64 = measure_batch64(cfg, w, frames=24, warmup=4, peak=peak)
+        b128 = {"decode": measure_replacement(cfg, w, frames=64, peak=peak, with_prefill=False),
+                "prefill_included": measure_replacement(cfg, w, frames=64, peak=peak, with_prefill=True)}
     w4 = None
     if args.workload in ("s2pro_b1", "s2pro_l1_b1") and not args.no_w4a16:
         w4 = measure_w4a16(cfg, w, prompt, frames=64, warmup=8, peak=peak)
 
-    cpu = None
+    cpu = cpu_batch = None
     if rank == 0 and ws == 1 and bits is not None:
+        from oracle import DualAROracle
         n_or = 8 if cfg.name == "s2pro" else 16
-        done, el = time_oracle(cfg, bits, wl, prompt, uni_all, n_or, budget_s=25.0)
+        o = DualAROracle(cfg, bits, max_pos=max(16_400, wl["prompt"] + n_or + 8))
+        done, el = time_oracle(o, wl, prompt, uni_all, n_or, budget_s=25.0)
         cpu = {"value": done / el, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{done} frames of this workload after a {wl['prompt']}-token prefill "
                          f"(prefill untimed), batch 1, NumPy fp32"}
+        if args.workload == "s2pro_b1" and not args.no_batches:
+            repl = gen.make_replacement_workload(128, 4, 512, seed=4)["ctx"]
+            cpu_batch = {"batch16": time_oracle_batch(o, cfg, batch_contexts(16)[:2], 8, budget_s=12.0),
+                         "batch64": time_oracle_batch(o, cfg, batch_contexts(64)[:2], 8, budget_s=12.0),
+                         "batch128_replace": time_oracle_batch(o, cfg, [repl[0], repl[-1]], 8, budget_s=16.0)}
+        del o
 
     if rank == 0:
         clocks = clk.summary()
@@ -607,7 +687,10 @@ def main():
             "gpu_launches": launches_per_frame * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "cpu_baseline_batch": cpu_batch,
+            "batch16": b16,
             "batch64": b64,
+            "batch128_replace": b128,
             "w4a16": w4,
         }
         print(json.dumps(line), flush=True)

@@ -705,7 +705,7 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     mp.fusion = U16(h->w.fusion);
     mp.bar = h->bar_counter;
     mp.bar_extra = h->bar_extra;
-    const int64_t need = static_cast<int64_t>(h->n_sm) * mp.n_ops * 2 * 8;
+    const int64_t need = static_cast<int64_t>(h->n_sm) * mp.n_ops * 4 * 8;
     mp.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
     mp.prefetch_bytes = h->prefetch_bytes;
     mp.w4 = h->any_w4 ? 1 : 0;

@@ -454,9 +454,10 @@ DEVI void gemv_epilogue(const GemvArgs& a, const GemvGeo& g, const GemvPro<NB>& 
 // tiles follow, after (window free again).
 template <int NB>
 DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, const GemvPro<NB>& pr,
-                     int ntiles, bool more, uint32_t epoch) {
+                     int ntiles, bool more, uint32_t epoch, uint64_t* stamp = nullptr) {
   constexpr int NCT = kWarpsC * 32;
   named_barrier(1, NCT);
+  if (stamp && threadIdx.x == 0) *stamp = global_timer_ns();
   const int step = g.swiglu ? 2 : 1;   // SwiGLU: gate tile, then up tile
   const int per = g.R * NB;
   const int n = (ntiles / step) * per;
@@ -481,7 +482,8 @@ DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, c
 // Returns false if a wait gave up.
 template <int NB>
 DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
-                       const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr, uint32_t epoch = 0) {
+                       const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr, uint32_t epoch = 0,
+                       uint64_t* stamp = nullptr) {
   constexpr int kWin = GemvScratch<NB>::kPartTiles;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV = K >> 3;
@@ -564,7 +566,8 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
       tw = 0;
     }
   }
-  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch);
+  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch, stamp);
+  else if (stamp && threadIdx.x == 0) *stamp = global_timer_ns();
   return true;
 }
 
@@ -614,7 +617,7 @@ DEVI float2 w4_word(uint32_t wd, const float4 xa, const float4 xb) {
 template <int NB>
 DEVI bool gemv_consume_w4(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring, uint32_t& t,
                           const float* xs, const float* gsum, GemvScratch<NB>& sc, const GemvPro<NB>& pr,
-                          uint32_t epoch = 0) {
+                          uint32_t epoch = 0, uint64_t* stamp = nullptr) {
   constexpr int kWin = GemvScratch<NB>::kPartTiles;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV32 = K >> 5;
@@ -686,7 +689,8 @@ DEVI bool gemv_consume_w4(const GemvArgs& a, const GemvGeo& g, const GemvRing& r
       tw = 0;
     }
   }
-  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch);
+  if (tw > 0) gemv_flush<NB>(a, g, sc, pr, tw, false, epoch, stamp);
+  else if (stamp && threadIdx.x == 0) *stamp = global_timer_ns();
   return true;
 }
 

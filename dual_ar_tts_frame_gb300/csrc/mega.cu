@@ -295,8 +295,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       cp_async16(reinterpret_cast<uint4*>(&opb[(i + 1) & 1]) + tid, reinterpret_cast<const uint4*>(p.ops + i + 1) + tid);
       cp_async_commit();
     }
-    uint64_t* tr = p.trace ? p.trace + (static_cast<size_t>(cta) * p.n_ops + i) * 2 : nullptr;
-    if (tr && tid == 0) tr[0] = global_timer_ns();
+    uint64_t* tr = p.trace ? p.trace + (static_cast<size_t>(cta) * p.n_ops + i) * 4 : nullptr;
+    if (tr && tid == 0) {
+      tr[0] = global_timer_ns();
+      tr[1] = tr[2] = 0;
+    }
     switch (op.type) {
       case MOP_GEMV: {
         const bool w4op = W4 && op.g.w4;
@@ -319,14 +322,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         if constexpr (W4) {
           if (w4op) {
             gemv_stage_x<NB, true>(op.g, g, xs, pro, cta, true, ep, gsum);
-            ok = gemv_consume_w4<NB>(op.g, g, ring, t, xs, gsum, scr, pro, ep);
+            if (tr && tid == 0) tr[1] = global_timer_ns();
+            ok = gemv_consume_w4<NB>(op.g, g, ring, t, xs, gsum, scr, pro, ep, tr ? tr + 2 : nullptr);
           } else {
             gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
-            ok = gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep);
+            if (tr && tid == 0) tr[1] = global_timer_ns();
+            ok = gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep, tr ? tr + 2 : nullptr);
           }
         } else {
           gemv_stage_x<NB>(op.g, g, xs, pro, cta, true, ep);
-          ok = gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep);
+          if (tr && tid == 0) tr[1] = global_timer_ns();
+          ok = gemv_consume<NB>(op.g, g, ring, t, xs, scr, pro, ep, tr ? tr + 2 : nullptr);
         }
         if (!ok) {
           // the ring protocol is broken: stop streaming (the error word is set)
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       default:
         break;
     }
-    if (tr && tid == 0) tr[1] = global_timer_ns();
+    if (tr && tid == 0) tr[3] = global_timer_ns();
     if (fetch) cp_async_wait_all();
     if (i + 1 < p.n_ops) {
       if (i == 0) grid_barrier(p.bar, static_cast<uint32_t>(ncta) + p.bar_extra, d.err, d.wait_limit_ns);

@@ -375,9 +375,10 @@ int dualar_debug_synthetic_context(dualar_handle* h, int32_t slot, int32_t n_tok
 
 /* Per-op timeline of the persistent frame kernel.  device_buffer: device
  * memory of `bytes` bytes (NULL stops tracing).  While set, every persistent
- * launch whose program fits writes, per CTA and op, the global-timer stamps
- * (ns) at the op's start and at its end before the grid barrier:
- * uint64 [n_ctas][n_ops][2].  *n_ops / *n_ctas (optional) receive the sizes
+ * launch whose program fits writes, per CTA and op, four global-timer stamps
+ * (ns): the op's start; for a GEMV, when its input is staged and when all of
+ * its weight tiles are consumed (0 for other ops); the op's end before the
+ * grid barrier: uint64 [n_ctas][n_ops][4].  *n_ops / *n_ctas (optional) receive the sizes
  * for a batch of 1 (n_ops builds that program if needed). */
 int dualar_set_trace(dualar_handle* h, void* device_buffer, int64_t bytes, int32_t* n_ops,
                      int32_t* n_ctas);
