@@ -689,7 +689,6 @@ int decode_impl(dualar_handle* h, int32_t batch, const int32_t* slots, const flo
     h->epoch += 1;
     MegaParams mp{};
     mp.epoch = h->epoch;
-    mp.fkv_floats = 2 * c.n_codebooks * c.head_dim;
     mp.d = d;
     mp.ops = h->mega_ops[batch];
     mp.n_ops = h->mega_nops[batch];

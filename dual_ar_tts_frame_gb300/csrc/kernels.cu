@@ -528,7 +528,7 @@ __global__ void attn_fast_kernel(DevPtrs d, int layer, int pos, const uint16_t* 
   pdl_launch();
   constexpr int NT = 32 * (G + 1 > 2 ? G + 1 : 2);
   __shared__ FastAttnSmem<EPL * 32> sm;
-  attn_fast_unit<EPL, G, NT, true>(d, blockIdx.x, layer, pos, q_norm, k_norm, sm, OpTags{0u, 0u}, nullptr, hv);
+  attn_fast_unit<EPL, G, NT, true>(d, blockIdx.x, layer, pos, q_norm, k_norm, sm, OpTags{0u, 0u}, hv);
 }
 
 template <int EPL>

@@ -34,7 +34,7 @@
 namespace dualar {
 
 constexpr int kMegaNCT = kWarpsC * 32;   // consumer threads
-constexpr int kMegaMaxStages = 3;   // measured: a 4th stage does not help
+constexpr int kMegaMaxStages = 4;   // measured: 4 stages beat 3 with the fast K/V resident in shared memory
 constexpr size_t kMegaSmemLimit = 227 * 1024;
 // producer timing, in SM cycles (about 2 GHz)
 constexpr long long kIdleCycles = 3000;        // a wait this long: the consumers are not streaming
@@ -60,21 +60,16 @@ struct MegaLayout {
     u = u > sizeof(SampSmem<kMegaNCT>) ? u : sizeof(SampSmem<kMegaNCT>);
     return u;
   }
-  // fast-AR K/V of this CTA's unit, all layers, for the whole frame
-  __host__ __device__ static size_t fkv(int kmax) { return (uni + union_bytes(kmax) + 127) & ~size_t(127); }
-  __host__ __device__ static size_t ring(int kmax, size_t fkv_bytes) {
-    return (fkv(kmax) + fkv_bytes + 127) & ~size_t(127);
-  }
-  // as many 40 KB ring stages as fit next to the fixed area, the union and
-  // the fast K/V
-  __host__ __device__ static int stages(int kmax, size_t fkv_bytes) {
-    const size_t r = ring(kmax, fkv_bytes);
+  __host__ __device__ static size_t ring(int kmax) { return (uni + union_bytes(kmax) + 127) & ~size_t(127); }
+  // as many 40 KB ring stages as fit next to the fixed area and the union
+  __host__ __device__ static int stages(int kmax) {
+    const size_t r = ring(kmax);
     const size_t room = kMegaSmemLimit > r ? kMegaSmemLimit - r : 0;
     const int s = static_cast<int>(room / kStageBytes);
     return s > kMegaMaxStages ? kMegaMaxStages : s;
   }
-  __host__ __device__ static size_t total(int kmax, size_t fkv_bytes) {
-    return ring(kmax, fkv_bytes) + size_t(stages(kmax, fkv_bytes)) * kStageBytes;
+  __host__ __device__ static size_t total(int kmax) {
+    return ring(kmax) + size_t(stages(kmax)) * kStageBytes;
   }
 };
 
@@ -175,10 +170,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   GemvRing ring;
   ring.full = bars;
   ring.empty = bars + kMaxStagesRing;
-  const size_t fkv_bytes = sizeof(float) * static_cast<size_t>(p.fkv_floats) * p.d.fast_n_layer;
-  ring.base = smem + Lay::ring(p.kmax, fkv_bytes);
-  ring.stages = Lay::stages(p.kmax, fkv_bytes);
-  float* fkv = reinterpret_cast<float*>(smem + Lay::fkv(p.kmax));
+  ring.base = smem + Lay::ring(p.kmax);
+  ring.stages = Lay::stages(p.kmax);
   uint64_t* abars = bars + 2 * kMaxStagesRing;
   GemvScratch<NB>& scr = *reinterpret_cast<GemvScratch<NB>*>(smem + Lay::scratch);
   GemvPro<NB>& pro = *reinterpret_cast<GemvPro<NB>*>(smem + Lay::pro);
@@ -349,13 +342,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         att_pre = -1;
         break;
       case MOP_ATTN_FAST:
-        // unit u always runs on CTA u % ncta, so the fast KV written by one
-        // pass is read by the same CTA in later passes
+        // unit u always runs on CTA u % ncta, so the fast K/V that one pass
+        // writes to the global fast cache is read back by the same CTA in
+        // later passes
         for (int u = cta; u < p.nrows * hkv; u += ncta)
           attn_fast_unit<HD / 32, G, kMegaNCT>(d, u, op.layer, op.pos, op.q_norm, op.k_norm,
                                                *reinterpret_cast<FastAttnSmem<HD>*>(uni),
-                                               OpTags{op_tag(ep, op.in_src), op_tag(ep, i)},
-                                               fkv + static_cast<size_t>(op.layer) * p.fkv_floats);
+                                               OpTags{op_tag(ep, op.in_src), op_tag(ep, i)});
         break;
       case MOP_SAMPLE_Q0:
         for (int r = cta; r < p.nrows; r += ncta)
@@ -388,10 +381,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
 template <int NB, int HD, int G, bool W4>
 static cudaError_t mega_launch_t(const MegaParams& p, int n_sm, cudaStream_t st, bool* unsupported) {
   using Lay = MegaLayout<NB, HD, G, W4>;
-  const size_t fkv_bytes = sizeof(float) * static_cast<size_t>(p.fkv_floats) * p.d.fast_n_layer;
-  const size_t smem = Lay::total(p.kmax, fkv_bytes);
-  // one fast-attention unit per CTA (its K/V stay in that CTA's shared memory)
-  if (Lay::stages(p.kmax, fkv_bytes) < 2 || smem > kMegaSmemLimit || p.nrows * p.d.Hkv > n_sm) {
+  const size_t smem = Lay::total(p.kmax);
+  if (Lay::stages(p.kmax) < 2 || smem > kMegaSmemLimit) {
     *unsupported = true;
     return cudaSuccess;
   }

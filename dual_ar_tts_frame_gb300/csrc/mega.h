@@ -58,7 +58,6 @@ struct MegaParams {
   uint64_t* trace;          // optional: [n_sm][n_ops][4] global-timer stamps (op start, GEMV x staged, GEMV tiles consumed, op end)
   uint64_t prefetch_bytes;  // weight bytes per CTA kept in flight into L2 beyond the ring
   uint32_t epoch;           // launch epoch of the activation tags (1 .. 2^20 - 1)
-  int fkv_floats;           // fast K/V per layer kept in shared memory: 2 * N * head_dim
   int w4;                   // some GEMV of the program reads packed 4-bit rows
 };
 

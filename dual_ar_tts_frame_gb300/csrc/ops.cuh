@@ -520,7 +520,8 @@ DEVI void attn_paged_preload(const DevPtrs& d, const AttnPreload& a, int layer, 
 // One unit per (row, KV head g): warp G computes the new position's K (norm
 // if configured, RoPE at the codebook index) and V and appends them, while
 // warp h < G loads query head g*G+h; the K/V of earlier positions (written by
-// earlier passes of this frame) are read from shared memory.  [P2] "Two
+// earlier passes of this frame to the global fast cache) are staged in shared
+// memory first.  [P2] "Two
 // autoregressions": the fast AR's KV cache is num_codebooks long and is
 // overwritten every frame.
 template <int HD>
@@ -532,10 +533,7 @@ struct FastAttnSmem {
 template <int EPL, int G, int NT, bool HALVES = false>
 DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const uint16_t* q_norm,
                          const uint16_t* k_norm, FastAttnSmem<EPL * 32>& sm, OpTags tg = OpTags{0u, 0u},
-                         float* res = nullptr, AttnHalves hv = AttnHalves{nullptr, nullptr, 0}) {
-  // res (persistent frame kernel): this layer's K and V rows [2][N][HD], kept
-  // in shared memory for the whole frame by the one CTA that runs this unit;
-  // otherwise earlier positions come from the global fast cache
+                         AttnHalves hv = AttnHalves{nullptr, nullptr, 0}) {
   constexpr int HD = EPL * 32;
   static_assert(G + 1 <= NT / 32, "one warp per query head plus a K/V warp");
   const int r = unit / d.Hkv, g = unit % d.Hkv;
@@ -544,13 +542,12 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
   const size_t qkv = static_cast<size_t>(r) * d.qkv_dim;
   float* kb = d.fast_kv + (((static_cast<size_t>(r) * d.fast_n_layer + layer) * 2 + 0) * hkv + g) * N * HD;
   float* vb = kb + static_cast<size_t>(hkv) * N * HD;
-  float (*ks)[HD] = res ? reinterpret_cast<float (*)[HD]>(res) : sm.ks;
-  float (*vs)[HD] = res ? reinterpret_cast<float (*)[HD]>(res + static_cast<size_t>(N) * HD) : sm.vs;
-  if (res == nullptr)
-    for (int e = threadIdx.x; e < pos * HD; e += NT) {
-      ks[e / HD][e % HD] = ldf(kb + e);
-      vs[e / HD][e % HD] = ldf(vb + e);
-    }
+  float (*ks)[HD] = sm.ks;
+  float (*vs)[HD] = sm.vs;
+  for (int e = threadIdx.x; e < pos * HD; e += NT) {
+    ks[e / HD][e % HD] = ldf(kb + e);
+    vs[e / HD][e % HD] = ldf(vb + e);
+  }
   float q[EPL];
   if (warp < G) {
     act_load<EPL>(d.qkv, d.qkv_t, qkv + (g * G + warp) * HD + lane * EPL, tg.in, q, d);
@@ -562,10 +559,8 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
     head_norm_rope<EPL>(kv, k_norm, d.eps, pos, d, lane);
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      if (res == nullptr) {
-        kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
-        vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv[j];
-      }
+      kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
+      vb[static_cast<size_t>(pos) * HD + lane * EPL + j] = vv[j];
       ks[pos][lane * EPL + j] = kv[j];
       vs[pos][lane * EPL + j] = vv[j];
     }
@@ -1039,6 +1034,11 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
   } else if (tid >= 32 && tid < 32 + kRasRing) {
     sm.hist[tid - 32] = ldi(d.hist + slot * kRasRing + (tid - 32));
   }
+  // the draw's uniforms and the forced code are requested before the logits
+  // are waited on, so their round trips overlap
+  const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
+  const float u_normal = u[0], u_ras = u[1];
+  const int forced0 = (io.forced && tid == 0) ? io.forced[static_cast<size_t>(row) * io.ldf] : 0;
   const float* zsrc = d.z_last + static_cast<size_t>(slot) * (ns + 1);
   // [P2] "Two autoregressions": the bias keeps the semantic ids and <|im_end|>.
   const Cands c{ns + (io.sp.allow_eos ? 1 : 0), ns, d.sem_begin, d.im_end};
@@ -1065,11 +1065,10 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
     csync<NT>();
     return;
   }
-  const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
-  const int normal = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u[0], sm);
+  const int normal = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u_normal, sm);
   // [P2] "Two autoregressions": a second draw at temperature 1.0, top-p 0.9,
   // used when the normal draw repeats a semantic token of the last 10 frames.
-  const int ras = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.ras_temperature, io.sp.ras_top_p, u[1], sm);
+  const int ras = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.ras_temperature, io.sp.ras_top_p, u_ras, sm);
   if (tid == 0) {
     const int hn = sm.ibc[3];
     const int w = min(io.sp.ras_win, hn);
@@ -1078,7 +1077,7 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
       for (int j = 0; j < w; ++j)
         if (sm.hist[(hn - 1 - j) % kRasRing] == normal) repeat = true;
     const int chosen = (io.sp.ras_win > 0 && repeat) ? ras : normal;
-    const int commit = io.forced ? io.forced[static_cast<size_t>(row) * io.ldf] : chosen;
+    const int commit = io.forced ? forced0 : chosen;
     if (io.draws_out) {
       io.draws_out[row * (N + 2) + 0] = normal;
       io.draws_out[row * (N + 2) + 1] = ras;
@@ -1136,6 +1135,10 @@ DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, Sa
   const int N = d.N, Cf = d.Cf;
   const size_t zoff = static_cast<size_t>(row) * d.logit_ld;
   const Cands c{Cf, Cf, 0, -1};
+  // the draw's uniform and the forced code are requested before the logits
+  // are waited on, so their round trips overlap
+  const float uk = io.uniforms[static_cast<size_t>(row) * io.ldu + k + 1];
+  const int forced_k = (io.forced && tid == 0) ? io.forced[static_cast<size_t>(row) * io.ldf + k] : 0;
   float z[EPT];
   unsigned long long key[EPT];
   const float zmax = samp_load<NT, EPT>(d.logits + zoff, c, z, key, sm, d.logits_t + zoff, tg.in, &d);
@@ -1151,10 +1154,9 @@ DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, Sa
     csync<NT>();
     return;
   }
-  const float* u = io.uniforms + static_cast<size_t>(row) * io.ldu;
-  const int draw = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u[k + 1], sm);
+  const int draw = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, uk, sm);
   if (tid == 0) {
-    int commit = io.forced ? io.forced[static_cast<size_t>(row) * io.ldf + k] : draw;
+    int commit = io.forced ? forced_k : draw;
     if (commit < 0 || commit >= Cf) {
       raise_error(d.err, DEV_ERR_BAD_INDEX);
       commit = 0;
