@@ -137,7 +137,9 @@ typedef struct dualar_sampling {
 
 typedef struct dualar_handle dualar_handle;
 
-/* Creates a decoder on the current CUDA device.  cfg, w: host structs (read
+/* Library plumbing: the pages define no such call (they describe a Python
+ * engine); it sets up what the decode step below needs.
+ * Creates a decoder on the current CUDA device.  cfg, w: host structs (read
  * during the call).  cuda_stream: a cudaStream_t (NULL = legacy default
  * stream) on which all later work is queued.  Allocates the KV pool
  * (max_pages x n_layer x 2 x n_kv_head x page_tokens x head_dim bf16), the
@@ -215,7 +217,10 @@ int dualar_decode_frame_noalloc(dualar_handle* h, int32_t batch, const int32_t* 
                                 const float* uniforms, const dualar_sampling* sampling,
                                 int32_t* codes, int32_t* status);
 
-/* Ends the sequence in a slot and returns its KV pages to the pool (lowest
+/* Library plumbing with no passage of its own: the end of a sequence whose
+ * q0 was <|im_end|> ([P2] "Two autoregressions"), or its replacement by a
+ * queued request, frees its slot here.
+ * Ends the sequence in a slot and returns its KV pages to the pool (lowest
  * page numbers are handed out first); a page shared with other slots
  * (dualar_share_prefix) returns only when the last of them releases it.
  * Queues nothing on the GPU. */
@@ -299,15 +304,18 @@ typedef struct dualar_w4a16_layer {
  * in-dimension that is not a multiple of 128), CUDA. */
 int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dualar_w4a16_layer* fast);
 
-/* Synchronises the handle's stream and reports device-side errors:
+/* Library plumbing (no counterpart on the pages).
+ * Synchronises the handle's stream and reports device-side errors:
  * DUALAR_ERR_TIMEOUT if a bounded wait gave up, DUALAR_ERR_DEVICE if a bounds
  * check skipped an access.  Clears the device error word. */
 int dualar_sync(dualar_handle* h);
 
-/* Copies the last error message (NUL-terminated, truncated to len). */
+/* Library plumbing (no counterpart on the pages).
+ * Copies the last error message (NUL-terminated, truncated to len). */
 int dualar_get_error(const dualar_handle* h, char* buf, size_t len);
 
-/* Frees everything the handle allocated (after synchronising its stream). */
+/* Library plumbing (no counterpart on the pages).
+ * Frees everything the handle allocated (after synchronising its stream). */
 void dualar_destroy(dualar_handle* h);
 
 /* ---- inspection (tests) ------------------------------------------------ */
