@@ -66,6 +66,10 @@ struct dualar_handle {
   // packed 4-bit projections (dualar_set_w4a16); empty: all bf16
   std::vector<dualar_w4a16_layer> slow_q, fast_q;
   bool any_w4 = false;
+  // bf16 copy of one packed projection (a SwiGLU pair: both) for the
+  // tensor-core path at 9+ rows; sized for the largest packed projection
+  uint16_t* w4_bf16 = nullptr;
+  size_t w4_bf16_elems = 0;
 };
 
 namespace {
@@ -243,6 +247,25 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
     }
     CUDA_TRY(h, cudaEventRecord(e0, h->stream));
   }
+  // packed 4-bit weights at 9+ rows: expanded to exact bf16 hi/lo pairs
+  // (one pass over the packed bytes, launched plainly after everything
+  // before it) and multiplied on the tensor cores over 2K columns, instead
+  // of GEMV passes of 8 rows; that GEMM is launched plainly too, since it
+  // fetches weights before waiting for its predecessor
+  bool weights_pdl = true, w_hilo = false;
+  if (a.w4 && h->use_tc && h->w4_bf16 && a.nb >= kTcMinRows && a.nb <= kTcMaxRows) {
+    GemvArgs t = a;
+    t.w4 = 0;
+    t.w0 = h->w4_bf16;
+    t.w1 = a.n1 > 0 ? h->w4_bf16 + static_cast<size_t>(a.n0) * 2 * a.K : nullptr;
+    if (static_cast<size_t>(a.n0 + a.n1) * 2 * a.K <= h->w4_bf16_elems && tc_eligible(t, h->tc.ldx)) {
+      LAUNCH(h, launch_dequant_w4(a.w0, a.n0, a.K, h->w4_bf16, h->stream));
+      if (a.n1 > 0) LAUNCH(h, launch_dequant_w4(a.w1, a.n1, a.K, const_cast<uint16_t*>(t.w1), h->stream));
+      a = t;
+      weights_pdl = false;
+      w_hilo = true;
+    }
+  }
   if (!a.w4 && h->use_tc && tc_eligible(a, h->tc.ldx)) {
     // 9..128 rows: one pass over the weights on the tensor cores.  The
     // SwiGLU output feeds the down projection without norm: its reduce
@@ -268,7 +291,8 @@ int run_gemv(dualar_handle* h, GemvArgs a) {
                                  a.ldx == a.K && a.norm_w == nullptr && a.save_x == nullptr);
     const bool split_out = a.mode == GEMV_SWIGLU && a.out_map == nullptr && a.ldo == a.n0;
     h->tc_ready_x = nullptr;
-    const cudaError_t e = launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n, ready, split_out, &h->tc_pend);
+    const cudaError_t e =
+        launch_tc_gemm(a, h->tc, h->n_sm, h->stream, &n, ready, split_out, &h->tc_pend, weights_pdl, w_hilo);
     if (e == cudaSuccess && split_out) {
       h->tc_ready_x = a.out;
       h->tc_ready_k = a.n0;
@@ -1408,9 +1432,33 @@ int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dua
   if (slow) h->slow_q.assign(slow, slow + c.n_layer);
   if (fast) h->fast_q.assign(fast, fast + c.fast_n_layer);
   h->any_w4 = false;
+  size_t need = 0;   // 2 x the elements of the largest packed projection (SwiGLU: gate and up)
+  const size_t D = c.dim, F = c.ffn;
   for (const auto* v : {&h->slow_q, &h->fast_q})
-    for (const dualar_w4a16_layer& l : *v)
+    for (const dualar_w4a16_layer& l : *v) {
       if (l.wqkv || l.wo || l.w_gate || l.w_down) h->any_w4 = true;
+      if (l.wqkv) need = std::max(need, static_cast<size_t>(c.n_head + 2 * c.n_kv_head) * c.head_dim * D);
+      if (l.wo) need = std::max(need, D * qd);
+      if (l.w_gate) need = std::max(need, 2 * F * D);
+      if (l.w_down) need = std::max(need, D * F);
+    }
+  need *= 2;   // hi and lo halves
+  if (h->w4_bf16 && need != h->w4_bf16_elems) {
+    h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), static_cast<void*>(h->w4_bf16)), h->allocs.end());
+    cudaFree(h->w4_bf16);
+    h->w4_bf16 = nullptr;
+    h->w4_bf16_elems = 0;
+  }
+  if (need > 0 && !h->w4_bf16) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, need * sizeof(uint16_t)) != cudaSuccess) {
+      set_err(h, "cudaMalloc of the 4-bit projections' bf16 scratch failed");
+      return DUALAR_ERR_CUDA;
+    }
+    h->allocs.push_back(p);
+    h->w4_bf16 = static_cast<uint16_t*>(p);
+    h->w4_bf16_elems = need;
+  }
   return DUALAR_OK;
 }
 

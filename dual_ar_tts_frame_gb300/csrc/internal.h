@@ -197,6 +197,10 @@ cudaError_t launch_setup(const LaunchSetup& s, const DevPtrs& d, const uint16_t*
 cudaError_t launch_gemv(const GemvArgs& a, int n_sm, cudaStream_t st);
 // Packs a bf16 matrix [n][K] (K % 128 == 0) into 4-bit records (gemv.cuh).
 cudaError_t launch_quantize_w4(const uint16_t* w, int n, int K, unsigned char* out, cudaStream_t st);
+// Packed 4-bit rows [n][record] -> bf16 [n][2K]: each weight q * s as hi in
+// column k and lo in column K + k (hi + lo = q * s exactly), queued without
+// programmatic dependent launch.
+cudaError_t launch_dequant_w4(const void* packed, int n, int K, uint16_t* out, cudaStream_t st);
 cudaError_t launch_append(const DevPtrs& d, int nrows, int layer, bool fast, int fast_pos,
                           const uint16_t* q_norm, const uint16_t* k_norm, cudaStream_t st);
 cudaError_t launch_attn_paged(const DevPtrs& d, int nrows, int layer, int total_units,

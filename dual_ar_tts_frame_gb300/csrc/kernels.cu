@@ -333,6 +333,59 @@ cudaError_t launch_quantize_w4(const uint16_t* w, int n, int K, unsigned char* o
   return cudaGetLastError();
 }
 
+// Packed 4-bit rows back to bf16, for the tensor-core path: one thread per
+// 32-element vector (16 code bytes, all in one scale group).  A weight q * s
+// (exact in fp32: at most 4 + 8 significant bits) is written as two bf16
+// values, hi = bf16(q s) and lo = bf16(q s - hi), which add up to it
+// exactly: row r of out holds hi in columns [0, K) and lo in [K, 2K), so a
+// product over the 2K columns with x repeated gives W x exactly.  Launched
+// without programmatic dependent launch, so that it starts after everything
+// before it (a projection may still read the previous contents) and the next
+// kernel sees its writes.
+__global__ void dequant_w4_kernel(const unsigned char* packed, int n, int K, uint16_t* out) {
+  const int vpr = K / 32;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(n) * vpr) return;
+  const int row = static_cast<int>(idx / vpr), v = static_cast<int>(idx % vpr);
+  const unsigned char* rec = packed + static_cast<size_t>(row) * w4_row_bytes(K);
+  const uint4 c = *reinterpret_cast<const uint4*>(rec + static_cast<size_t>(v) * 16);
+  const float sc = bf16bits_to_f32(*reinterpret_cast<const uint16_t*>(rec + K / 2 + (v >> 2) * 2));
+  const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+  uint16_t* rowp = out + static_cast<size_t>(row) * 2 * K + static_cast<size_t>(v) * 32;
+  uint4* dhi = reinterpret_cast<uint4*>(rowp);
+  uint4* dlo = reinterpret_cast<uint4*>(rowp + K);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t oh[4], ol[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t byte = (wd[q] >> (8 * e)) & 0xFFu;   // elements 2e (low nibble) and 2e+1
+      uint32_t h2 = 0, l2 = 0;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float w = static_cast<float>(static_cast<int>((byte >> (4 * half)) & 0xFu) - 8) * sc;
+        const uint16_t hb = f32_to_bf16bits(w);
+        const uint16_t lb = f32_to_bf16bits(w - bf16bits_to_f32(hb));
+        h2 |= static_cast<uint32_t>(hb) << (16 * half);
+        l2 |= static_cast<uint32_t>(lb) << (16 * half);
+      }
+      oh[e] = h2;
+      ol[e] = l2;
+    }
+    dhi[q] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+    dlo[q] = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+  }
+}
+
+cudaError_t launch_dequant_w4(const void* packed, int n, int K, uint16_t* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (K <= 0 || K % kW4Group) return cudaErrorInvalidValue;
+  const long long threads = static_cast<long long>(n) * (K / 32);
+  dequant_w4_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(
+      static_cast<const unsigned char*>(packed), n, K, out);
+  return cudaGetLastError();
+}
+
 // ============================================================================
 // QK-norm + RoPE + KV append
 // ============================================================================

@@ -65,6 +65,7 @@ struct TcArgs {
   float* part;         // [slices][nb][ldp] partial sums
   int ldp;             // n0 + n1
   int tma_store;       // the partial tile goes out through the tensor map tp (else plain stores)
+  int kwrap;           // > 0: K runs over two weight halves; x's column is k mod kwrap (4-bit hi/lo)
   uint32_t* err;
   uint64_t wait_limit_ns;
 };
@@ -126,7 +127,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       auto load_x = [&](int i) {
         unsigned char* st = smem + (i % S) * SB;
-        const int kx = (c0 + i) * 64;
+        int kx = (c0 + i) * 64;
+        if (a.kwrap > 0 && kx >= a.kwrap) kx -= a.kwrap;
         tma_load_2d(st + 2 * kTcWTile, &txh, kx, 0, &full[i % S]);
         tma_load_2d(st + 2 * kTcWTile + XT, &txl, kx, 0, &full[i % S]);
       };
@@ -593,7 +595,7 @@ bool tc_eligible(const GemvArgs& a, int ldx) {
 template <int NBP>
 static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& xh,
                                    const CUtensorMap& xl, const CUtensorMap& tp, const TcArgs& t, dim3 grid,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool pdl) {
   static bool configured = false;
   const size_t smem = tc_smem_bytes(NBP);
   if (!configured) {
@@ -602,15 +604,20 @@ static cudaError_t launch_gemm_nbp(const CUtensorMap& w0, const CUtensorMap& w1,
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  if (!pdl) {
+    tc_gemm_kernel<NBP><<<grid, kTcThreads, smem, st>>>(w0, w1, xh, xl, tp, t);
+    return cudaGetLastError();
+  }
   return launch_pdl(tc_gemm_kernel<NBP>, grid, dim3(kTcThreads), smem, st, w0, w1, xh, xl, tp, t);
 }
 
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
-                           bool x_ready, bool split_out, TcPending* defer) {
+                           bool x_ready, bool split_out, TcPending* defer, bool weights_pdl, bool w_hilo) {
   const int nbp = a.nb <= 16 ? 16 : a.nb <= 32 ? 32 : a.nb <= 64 ? 64 : 128;
   const int n_rows = a.n0 + a.n1;   // virtual weight rows (SwiGLU: gate then up)
   const int tiles = (n_rows + 255) / 256;
-  const int kc = a.K / 64;
+  const int kw = w_hilo ? 2 * a.K : a.K;   // weight columns
+  const int kc = kw / 64;
   int slices = (n_sm + tiles / 2) / tiles;
   slices = slices < 1 ? 1 : slices > kTcMaxSlices ? kTcMaxSlices : slices;
   if (slices > kc) slices = kc;
@@ -620,8 +627,8 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
 
   CUtensorMap m0, m1, mh, ml;
   const int seg1 = a.n1 > 0 ? a.n1 : 1;
-  if (!cached_map(&m0, a.w0, a.K, a.n0, a.K, 128) ||
-      !cached_map(&m1, a.n1 > 0 ? a.w1 : a.w0, a.K, seg1, a.K, 128) ||
+  if (!cached_map(&m0, a.w0, kw, a.n0, kw, 128) ||
+      !cached_map(&m1, a.n1 > 0 ? a.w1 : a.w0, kw, seg1, kw, 128) ||
       !cached_map(&mh, b.xh, a.K, kTcMaxRows, b.ldx, nbp) || !cached_map(&ml, b.xl, a.K, kTcMaxRows, b.ldx, nbp))
     return cudaErrorInvalidValue;
 
@@ -636,13 +643,13 @@ cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cuda
   CUtensorMap mp;
   const bool tstore = n_rows % 4 == 0 && part_map(&mp, b.part, n_rows, a.nb, slices, nbp);
   if (!tstore) mp = m0;   // unused
-  TcArgs t{a.n0, a.n1, a.K, a.nb, kcps, b.part, n_rows, tstore ? 1 : 0, a.err, a.wait_limit_ns};
+  TcArgs t{a.n0, a.n1, kw, a.nb, kcps, b.part, n_rows, tstore ? 1 : 0, w_hilo ? a.K : 0, a.err, a.wait_limit_ns};
   const dim3 grid(tiles, slices);
   switch (nbp) {
-    case 16: e = launch_gemm_nbp<16>(m0, m1, mh, ml, mp, t, grid, st); break;
-    case 32: e = launch_gemm_nbp<32>(m0, m1, mh, ml, mp, t, grid, st); break;
-    case 64: e = launch_gemm_nbp<64>(m0, m1, mh, ml, mp, t, grid, st); break;
-    default: e = launch_gemm_nbp<128>(m0, m1, mh, ml, mp, t, grid, st); break;
+    case 16: e = launch_gemm_nbp<16>(m0, m1, mh, ml, mp, t, grid, st, weights_pdl); break;
+    case 32: e = launch_gemm_nbp<32>(m0, m1, mh, ml, mp, t, grid, st, weights_pdl); break;
+    case 64: e = launch_gemm_nbp<64>(m0, m1, mh, ml, mp, t, grid, st, weights_pdl); break;
+    default: e = launch_gemm_nbp<128>(m0, m1, mh, ml, mp, t, grid, st, weights_pdl); break;
   }
   if (e != cudaSuccess) return e;
   const int n_out = a.mode == GEMV_SWIGLU ? a.n0 : n_rows;

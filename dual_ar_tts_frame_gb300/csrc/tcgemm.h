@@ -48,9 +48,16 @@ struct TcPending {
 // residual-add projection whose output is one of the buffers' row blocks)
 // the reduce is not queued but described in *defer: the caller queues it
 // later, alone (launch_tc_pending) or fused with the next projection's
-// norm and split (launch_tc_reduce_norm).  *launches += count.
+// norm and split (launch_tc_reduce_norm).  weights_pdl false: the GEMM is
+// launched without programmatic dependent launch (it fetches its weights
+// before waiting for the kernel before it, so weights written by that
+// kernel need a plain launch).  w_hilo: the weights are [rows][2K], each
+// weight's bf16 hi half in column k and lo half in K + k
+// (launch_dequant_w4); the GEMM runs over 2K columns with x's column k mod
+// K.  *launches += count.
 cudaError_t launch_tc_gemm(const GemvArgs& a, const TcBuffers& b, int n_sm, cudaStream_t st, int* launches,
-                           bool x_ready = false, bool split_out = false, TcPending* defer = nullptr);
+                           bool x_ready = false, bool split_out = false, TcPending* defer = nullptr,
+                           bool weights_pdl = true, bool w_hilo = false);
 // Whether a deferred reduce can be fused into the split of projection a
 // (its input is the pending output, with a norm).
 bool tc_can_fuse(const TcPending& p, const GemvArgs& a);

@@ -293,15 +293,19 @@ typedef struct dualar_w4a16_layer {
  * the next call on (the caller keeps them valid until they are replaced or
  * the handle is destroyed).  slow: host array [n_layer] or NULL (all bf16);
  * fast: host array [fast_n_layer] or NULL.  Embeddings, norms and both heads
- * stay bf16.  Packed projections always run in the weight-streaming GEMV
- * (never on the tensor cores): inside the persistent frame kernel for
- * batches of 1-2 (dualar_set_persistent), otherwise one launch per
- * projection in passes of at most 8 rows (prefill chunks included).  The
- * call synchronises the handle's stream and drops the persistent kernel's
- * cached frame programs, which are built again for the new weights on the
- * next decode.  Both arrays NULL restores the all-bf16 decoder.  Errors:
- * INVALID_ARG (an unaligned pointer, a gate without its up matrix, an
- * in-dimension that is not a multiple of 128), CUDA. */
+ * stay bf16.  Up to 8 rows a packed projection runs in the weight-streaming
+ * GEMV on the packed bytes (exact products q * s * x): inside the persistent
+ * frame kernel for batches of 1-2 (dualar_set_persistent), otherwise one
+ * launch per projection in passes of at most 8 rows.  From 9 rows (decode
+ * batches, prefill chunks) it is first expanded, in a scratch buffer the
+ * handle allocates here (twice the largest packed projection's elements,
+ * gate and up together), into two bf16 matrices whose sum is exactly q * s,
+ * and multiplied on the tensor cores over both.  The call synchronises the handle's stream and drops the
+ * persistent kernel's cached frame programs, which are built again for the
+ * new weights on the next decode.  Both arrays NULL restores the all-bf16
+ * decoder and frees the scratch.  Errors: INVALID_ARG (an unaligned pointer,
+ * a gate without its up matrix, an in-dimension that is not a multiple of
+ * 128), CUDA (also when the scratch cannot be allocated). */
 int dualar_set_w4a16(dualar_handle* h, const dualar_w4a16_layer* slow, const dualar_w4a16_layer* fast);
 
 /* Library plumbing (no counterpart on the pages).

@@ -46,9 +46,11 @@ cudaError_t launch_synthetic_fill(const DevPtrs&, int, int, uint32_t, int, cudaS
 bool tc_available() { return false; }
 bool tc_eligible(const GemvArgs&, int) { return false; }
 bool tc_bf16_map(CUtensorMap*, const void*, int, int, int, int) { return false; }
-cudaError_t launch_tc_gemm(const GemvArgs&, const TcBuffers&, int, cudaStream_t, int*, bool, bool, TcPending*) {
+cudaError_t launch_tc_gemm(const GemvArgs&, const TcBuffers&, int, cudaStream_t, int*, bool, bool, TcPending*,
+                           bool, bool) {
   return cudaSuccess;
 }
+cudaError_t launch_dequant_w4(const void*, int, int, uint16_t*, cudaStream_t) { return cudaSuccess; }
 bool tc_can_fuse(const TcPending&, const GemvArgs&) { return false; }
 cudaError_t launch_tc_pending(const TcPending&, const TcBuffers&, int, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_tc_reduce_norm(const TcPending&, const GemvArgs&, const TcBuffers&, cudaStream_t) {
