@@ -50,6 +50,11 @@ WORKLOADS = {
                                ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 128: 124 contexts uniform in "
                                                 "[2048, 4096] that finish at seeded frames (uniform in [1, 64]) and "
                                                 "are replaced from a seeded queue, plus 4 resident contexts of 16384"),
+    "s2pro_b64_two_streams": dict(cfg="s2pro", batch=64, prompt=0, frames=20, temperature=0.8, top_p=0.8,
+                                  ras_win=10, desc="full S2-Pro-shaped Dual-AR, batch 64 (contexts uniform in "
+                                                   "[1024, 4096]) as one decoder, then as two decoders of 32 on "
+                                                   "two CUDA streams (co-scheduling the fast AR of one group with "
+                                                   "the slow step of the other)"),
     "tiny_b1": dict(cfg="tiny", batch=1, prompt=32, frames=16, temperature=0.8, top_p=0.8, ras_win=10,
                     desc="tiny Dual-AR, batch 1, 32-token prompt"),
 }
@@ -78,15 +83,27 @@ def peaks():
     return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+MEGA_SOURCES = ["dual_ar_tts_frame_gb300/csrc/mega.cu", "dual_ar_tts_frame_gb300/csrc/gemv.cuh",
+                "dual_ar_tts_frame_gb300/csrc/ops.cuh", "dual_ar_tts_frame_gb300/csrc/common.cuh",
+                "dual_ar_tts_frame_gb300/csrc/internal.h", "dual_ar_tts_frame_gb300/csrc/mega.h"]
+
+
+def sources_sha256(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()
+
+
 def traffic_record():
-    """ncu DRAM bytes per GEMV launch, if taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemv_traffic.json")
-    src = os.path.join(ROOT, "dual_ar_tts_frame_gb300", "csrc", "kernels.cu")
+    """ncu DRAM bytes per launch of the persistent frame kernel
+    (profiles/mega_traffic.json), if they were taken on the current sources
+    of that kernel; None otherwise."""
+    p = os.path.join(ROOT, "profiles", "mega_traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p))
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return rec if rec.get("kernels_sha256") == sha else None
+    return rec if rec.get("sources_sha256") == sources_sha256(rec.get("sources", MEGA_SOURCES)) else None
 
 
 class ClockSampler:
@@ -305,6 +322,94 @@ def measure_batch64(cfg, w, frames: int, warmup: int, peak: float) -> dict:
     return measure_batch(cfg, w, 64, frames, warmup, peak)
 
 
+def measure_two_streams(cfg, w, frames: int, warmup: int) -> dict:
+    """The batch-64 workload (contexts uniform in [1,024, 4,096], seed 3,
+    synthetic K/V) decoded by one decoder, then split into two decoders of
+    32 sequences on two CUDA streams whose steps run concurrently (with an
+    offset of 0 or 1 step), so the fast AR of one group can overlap the slow
+    step of the other.  Device-timed from one event before both streams to
+    one after both; frames/s over all 64 sequences."""
+    import torch
+    from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling
+    ctx = batch_contexts(64)
+    smp = Sampling(temperature=0.8, top_p=0.8, ras_win=10, allow_eos=False)
+    uni = torch.from_numpy(gen.make_uniforms(warmup + frames, 64, cfg, seed=1)).cuda()
+
+    def make(cs, stream, seed0):
+        pages = sum(-(-(int(c) + warmup + frames + 2) // cfg.page_tokens) for c in cs) + 8
+        d = DualARDecoder(cfg, w, max_pages=pages, max_seqs=len(cs), max_ctx=int(max(cs)) + warmup + frames + 8,
+                          stream=stream)
+        for s in range(len(cs)):
+            d.synthetic_context(s, int(cs[s]), seed=seed0 + s)
+        return d
+
+    def bufs(b):
+        return (torch.empty((b, cfg.n_codebooks), dtype=torch.int32, device="cuda"),
+                torch.empty((b,), dtype=torch.int32, device="cuda"))
+
+    out = {}
+    st = torch.cuda.Stream()
+    d = make(ctx, st, 1000)
+    c, s_ = bufs(64)
+    with torch.cuda.stream(st):
+        for f in range(warmup):
+            d.decode_frame(list(range(64)), uni[f], smp, c, s_)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    with torch.cuda.stream(st):
+        for f in range(warmup, warmup + frames):
+            d.decode_frame(list(range(64)), uni[f], smp, c, s_)
+    e1.record(st)
+    torch.cuda.synchronize()
+    d.sync()
+    d.close()
+    ms = e0.elapsed_time(e1)
+    out["one_decoder_b64"] = {"frames_per_s": 64 * frames / (ms / 1000.0), "ms_per_step": ms / frames}
+    torch.cuda.empty_cache()
+    for off in (0, 1):
+        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        da, db = make(ctx[:32], sa, 1000), make(ctx[32:], sb, 1032)
+        ua, ub = uni[:, :32].contiguous(), uni[:, 32:].contiguous()
+        (ca, sa_), (cb, sb_) = bufs(32), bufs(32)
+        for f in range(warmup):
+            with torch.cuda.stream(sa):
+                da.decode_frame(list(range(32)), ua[f], smp, ca, sa_)
+            with torch.cuda.stream(sb):
+                db.decode_frame(list(range(32)), ub[f], smp, cb, sb_)
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea, eb = torch.cuda.Event(), torch.cuda.Event()
+        t0.record(cur)
+        sa.wait_event(t0)
+        sb.wait_event(t0)
+        for f in range(warmup, warmup + frames):
+            with torch.cuda.stream(sa):
+                da.decode_frame(list(range(32)), ua[f], smp, ca, sa_)
+            if f - warmup >= off:
+                with torch.cuda.stream(sb):
+                    db.decode_frame(list(range(32)), ub[f - off], smp, cb, sb_)
+        for f in range(warmup + frames - off, warmup + frames):
+            with torch.cuda.stream(sb):
+                db.decode_frame(list(range(32)), ub[f], smp, cb, sb_)
+        ea.record(sa)
+        eb.record(sb)
+        cur.wait_event(ea)
+        cur.wait_event(eb)
+        t1.record(cur)
+        torch.cuda.synchronize()
+        da.sync()
+        db.sync()
+        da.close()
+        db.close()
+        ms = t0.elapsed_time(t1)
+        out[f"two_decoders_b32_offset{off}"] = {"frames_per_s": 64 * frames / (ms / 1000.0),
+                                                "ms_per_pair_of_steps": ms / frames}
+        torch.cuda.empty_cache()
+    return out
+
+
 def measure_replacement(cfg, w, frames: int, peak: float, with_prefill: bool) -> dict:
     """Batch 128 with replacement: 124 contexts uniform in [2,048, 4,096] and
     4 of 16,384 (seed 4), set up by the synthetic-context hook; every step
@@ -492,6 +597,18 @@ def main():
             r = measure_replacement(cfg, w, frames=W + K, peak=peak, with_prefill=with_prefill)
             print(json.dumps({"metric": METRIC, "impl": "ours", "config": {"workload": r["workload"]}, **r}),
                   flush=True)
+        return
+
+    if args.workload == "s2pro_b64_two_streams":
+        # the co-scheduling comparison alone (not part of the default line)
+        import torch
+        from dual_ar_tts_frame_gb300 import build, upload_weights
+        torch.cuda.set_device(local)
+        build()
+        w = upload_weights(gen.make_weights(cfg, seed=0))
+        r = measure_two_streams(cfg, w, frames=K, warmup=max(W, 3))
+        print(json.dumps({"metric": METRIC, "impl": "ours", "unit": "frames/s",
+                          "config": {"workload": f"{args.workload}: {wl['desc']}; {K} timed steps"}, **r}), flush=True)
         return
 
     if args.workload in ("s2pro_b64", "s2pro_l1_b64"):
