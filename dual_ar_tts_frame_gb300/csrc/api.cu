@@ -543,6 +543,7 @@ int build_mega_program(dualar_handle* h, int nb) {
       const int qkv = gemv(packed(args_qkv(h, lw, nb, nullptr), lq.wqkv), x, x_src, nullptr, -1, F(d.qkv_t), true);
       const int at = attn_op(MOP_ATTN_FAST, l, p, qkv, c.fast_qk_norm, lw);
       hf_src = gemv(packed(args_o(h, lw, nb, nullptr, nullptr), lq.wo), F(d.attn_t), at, x, x_src, F(d.hf_t), true);
+      ops[hf_src].g.x_scout = c.head_dim;   // one sentinel per query head
       const int act = gemv(packed(args_gateup(h, lw, nb, nullptr), lq.w_gate, lq.w_up), F(d.hf_t), hf_src,
                            nullptr, -1, F(d.act_t), true);
       hf_src = gemv(packed(args_down(h, lw, nb, nullptr), lq.w_down), F(d.act_t), act, F(d.hf_t), hf_src,
@@ -563,6 +564,7 @@ int build_mega_program(dualar_handle* h, int nb) {
     ops[qkv].pos = l + 1;   // its attention's first pages are fetched during it
     const int at = attn_op(MOP_ATTN_PAGED, l, 0, qkv, c.slow_qk_norm, lw);
     hs_src = gemv(packed(args_o(h, lw, nb, nullptr, nullptr), lq.wo), F(d.attn_t), at, x, x_src, F(d.hs_t), true);
+    ops[hs_src].g.x_scout = c.head_dim;
     const int act = gemv(packed(args_gateup(h, lw, nb, nullptr), lq.w_gate, lq.w_up), F(d.hs_t), hs_src, nullptr,
                          -1, F(d.act_t), true);
     hs_src = gemv(packed(args_down(h, lw, nb, nullptr), lq.w_down), F(d.act_t), act, F(d.hs_t), hs_src, F(d.hs_t),

@@ -301,6 +301,19 @@ DEVI void gemv_stage_x(const GemvArgs& a, const GemvGeo& g, float* xs, GemvPro<N
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
   const uint32_t xtag = a.x_src >= 0 ? op_tag(epoch, a.x_src) : 0u;
+  if (a.x_src >= 0 && a.x_scout > 0) {
+    if (warp == 0) {
+      const int nblk = K / a.x_scout;
+      for (int b = 0; b < NB; ++b) {
+        if (b >= a.nb) break;
+        for (int blk = lane; blk < nblk; blk += 32)
+          tag_wait1(reinterpret_cast<const uint64_t*>(a.x) + static_cast<size_t>(b) * a.ldx +
+                        static_cast<size_t>(blk + 1) * a.x_scout - 1,
+                    xtag, a.err, a.wait_limit_ns);
+      }
+    }
+    named_barrier(1, NCT);
+  }
   if constexpr (W4) {
     const int KV32 = K >> 5;
     for (int j0 = 0; j0 < KV; j0 += NCT) {   // uniform trip count: the quad shuffles below

@@ -107,6 +107,13 @@ struct GemvArgs {
   // 1: w0 / w1 hold 4-bit packed weights (gemv.cuh, "4-bit weights")
   // instead of bf16.
   int w4;
+  // Persistent kernel, x_src >= 0: with x_scout > 0, warp 0 first waits for
+  // the last word of every x_scout-word block of x (one word per lane) while
+  // the other consumer warps wait at a barrier; only then do all threads read
+  // x.  For inputs that every CTA waits on for a long time (the attention
+  // output, written by a few CTAs): a whole CTA polling every word of x
+  // crowds the lines that the writers are about to fill.
+  int x_scout;
 };
 
 // Device buffers of one handle that kernels need (plain pointers).

@@ -88,28 +88,46 @@ DEVI void act_store(float* plain, uint64_t* tagged, size_t off, uint32_t tag, fl
 // QK-norm (optional) + RoPE of one head vector held as EPL elements per lane.
 // [P2] "The slow AR is Qwen3-4B": qk-norm (slow AR only), rope_base 1e6;
 // "Streaming: whose numbers": bf16 tables.  Pairs (2i, 2i+1) rotate by
-// pos * base^(-2i/hd).
+// pos * base^(-2i/hd).  The gain and the table entries do not depend on the
+// activation, so callers load them (head_nr_load) before waiting for it.
 template <int EPL>
-DEVI void head_norm_rope(float (&v)[EPL], const uint16_t* nw, float eps, int pos, const DevPtrs& d,
-                         int lane) {
-  const int hd = EPL * 32, half = hd / 2;
-  if (nw != nullptr) {
+struct HeadNR {
+  float w[EPL];                 // norm gain of this lane's elements
+  float c[EPL / 2], s[EPL / 2]; // cos, sin of this lane's pairs
+};
+
+template <int EPL>
+DEVI HeadNR<EPL> head_nr_load(const uint16_t* nw, int pos, const DevPtrs& d, int lane) {
+  constexpr int half = EPL * 16;
+  HeadNR<EPL> t;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) t.w[j] = nw != nullptr ? bf16bits_to_f32(nw[lane * EPL + j]) : 1.f;
+#pragma unroll
+  for (int pp = 0; pp < EPL / 2; ++pp) {
+    const int i = (lane * EPL) / 2 + pp;
+    t.c[pp] = bf16bits_to_f32(d.rope_cos[static_cast<size_t>(pos) * half + i]);
+    t.s[pp] = bf16bits_to_f32(d.rope_sin[static_cast<size_t>(pos) * half + i]);
+  }
+  return t;
+}
+
+template <int EPL>
+DEVI void head_nr_apply(float (&v)[EPL], const HeadNR<EPL>& t, bool norm, float eps) {
+  constexpr int hd = EPL * 32;
+  if (norm) {
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) s += v[j] * v[j];
     s = warp_sum(s);
     const float inv = 1.0f / sqrtf(s / static_cast<float>(hd) + eps);
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) v[j] = (v[j] * inv) * bf16bits_to_f32(nw[lane * EPL + j]);
+    for (int j = 0; j < EPL; ++j) v[j] = (v[j] * inv) * t.w[j];
   }
 #pragma unroll
   for (int pp = 0; pp < EPL / 2; ++pp) {
-    const int i = (lane * EPL) / 2 + pp;
-    const float c = bf16bits_to_f32(d.rope_cos[static_cast<size_t>(pos) * half + i]);
-    const float sn = bf16bits_to_f32(d.rope_sin[static_cast<size_t>(pos) * half + i]);
     const float x0 = v[2 * pp], x1 = v[2 * pp + 1];
-    v[2 * pp] = x0 * c - x1 * sn;
-    v[2 * pp + 1] = x1 * c + x0 * sn;
+    v[2 * pp] = x0 * t.c[pp] - x1 * t.s[pp];
+    v[2 * pp + 1] = x1 * t.c[pp] + x0 * t.s[pp];
   }
 }
 
@@ -225,9 +243,10 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     if (fuse_append) {
       if (warp < G) {
         const int h = g * G + warp;
+        const HeadNR<EPL> nr = head_nr_load<EPL>(q_norm, ri.pos, d, lane);
         float v[EPL];
         act_load<EPL>(d.qkv, d.qkv_t, static_cast<size_t>(r) * d.qkv_dim + h * HD + lane * EPL, tg.in, v, d);
-        head_norm_rope<EPL>(v, q_norm, d.eps, ri.pos, d, lane);
+        head_nr_apply<EPL>(v, nr, q_norm != nullptr, d.eps);
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
           const int dd = lane * EPL + j;
@@ -236,11 +255,12 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
       }
       if (warp == (G % NW) && newest) {
         const size_t base = static_cast<size_t>(r) * d.qkv_dim;
+        const HeadNR<EPL> nr = head_nr_load<EPL>(k_norm, ri.pos, d, lane);
+        const int pg = ldi(d.page_table + static_cast<size_t>(ri.slot) * d.pages_per_seq + ri.pos / kPageTokens);
         float kv[EPL], vv[EPL];
         act_load<EPL>(d.qkv, d.qkv_t, base + hq * HD + g * HD + lane * EPL, tg.in, kv, d);
         act_load<EPL>(d.qkv, d.qkv_t, base + hq * HD + hkv * HD + g * HD + lane * EPL, tg.in, vv, d);
-        head_norm_rope<EPL>(kv, k_norm, d.eps, ri.pos, d, lane);
-        const int pg = ldi(d.page_table + static_cast<size_t>(ri.slot) * d.pages_per_seq + ri.pos / kPageTokens);
+        head_nr_apply<EPL>(kv, nr, k_norm != nullptr, d.eps);
         uint16_t* kd = d.kv_pool + (((static_cast<size_t>(pg) * d.n_layer + layer) * 2 + 0) * hkv + g) *
                                        page_stride + static_cast<size_t>(ri.pos % kPageTokens) * HD;
         uint16_t* vd = kd + static_cast<size_t>(hkv) * page_stride;
@@ -550,13 +570,15 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
   }
   float q[EPL];
   if (warp < G) {
+    const HeadNR<EPL> nr = head_nr_load<EPL>(q_norm, pos, d, lane);
     act_load<EPL>(d.qkv, d.qkv_t, qkv + (g * G + warp) * HD + lane * EPL, tg.in, q, d);
-    head_norm_rope<EPL>(q, q_norm, d.eps, pos, d, lane);
+    head_nr_apply<EPL>(q, nr, q_norm != nullptr, d.eps);
   } else if (warp == G) {
+    const HeadNR<EPL> nr = head_nr_load<EPL>(k_norm, pos, d, lane);
     float kv[EPL], vv[EPL];
     act_load<EPL>(d.qkv, d.qkv_t, qkv + hq * HD + g * HD + lane * EPL, tg.in, kv, d);
     act_load<EPL>(d.qkv, d.qkv_t, qkv + hq * HD + hkv * HD + g * HD + lane * EPL, tg.in, vv, d);
-    head_norm_rope<EPL>(kv, k_norm, d.eps, pos, d, lane);
+    head_nr_apply<EPL>(kv, nr, k_norm != nullptr, d.eps);
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
       kb[static_cast<size_t>(pos) * HD + lane * EPL + j] = kv[j];
