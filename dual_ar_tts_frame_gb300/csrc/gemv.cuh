@@ -491,6 +491,42 @@ DEVI void gemv_flush(const GemvArgs& a, const GemvGeo& g, GemvScratch<NB>& sc, c
   if (more) named_barrier(1, NCT);
 }
 
+// Lane sums of a group of kGrp tiles' per-lane partials pg[u][b], stored as
+// the warp's partials of window slots tw .. tw + ng - 1.  For kGrp = 8 one
+// butterfly serves all tiles: the same pairwise sums, in the same order, as
+// warp_sum per tile (so the same bits), with 9 shuffles instead of 5 per
+// tile; lane 4u ends with tile u's sum.
+template <int NB, int kGrp>
+DEVI void gemv_group_sums(const float (&pg)[kGrp][NB], int ng, GemvScratch<NB>& sc, int tw, int warp, int lane) {
+  static_assert(kGrp == 1 || kGrp == 8, "one tile, or eight in a butterfly");
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if constexpr (kGrp == 1) {
+      const float v = warp_sum(pg[0][b]);
+      if (lane == 0) sc.part[tw][warp][b] = v;
+    } else {
+      const bool l4 = lane & 16, l3 = lane & 8, l2 = lane & 4;
+      float h4[4], h3[2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float keep = l4 ? pg[i + 4][b] : pg[i][b], send = l4 ? pg[i][b] : pg[i + 4][b];
+        h4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float keep = l3 ? h4[i + 2] : h4[i], send = l3 ? h4[i] : h4[i + 2];
+        h3[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+      }
+      const float keep = l2 ? h3[1] : h3[0], send = l2 ? h3[0] : h3[1];
+      float v = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+      const int u = lane >> 2;
+      if ((lane & 3) == 0 && u < ng) sc.part[tw + u][warp][b] = v;
+    }
+  }
+}
+
 // Consumer side: consumes the tiles of one GEMV and writes the epilogue.
 // Returns false if a wait gave up.
 template <int NB>
@@ -498,6 +534,8 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
                        const float* xs, GemvScratch<NB>& sc, const GemvPro<NB>& pr, uint32_t epoch = 0,
                        uint64_t* stamp = nullptr) {
   constexpr int kWin = GemvScratch<NB>::kPartTiles;
+  constexpr int kGrp = NB <= 2 ? 8 : 1;   // tiles per transposed reduction (registers: kGrp x NB)
+  static_assert(kWin % kGrp == 0, "groups fill windows exactly");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, KV = K >> 3;
   const int r = warp / g.S, sg = warp % g.S;
@@ -518,63 +556,71 @@ DEVI bool gemv_consume(const GemvArgs& a, const GemvGeo& g, const GemvRing& ring
     }
   }
   TileIter it(a, g);
-  int row0, rows, part;
   int tw = 0;   // tiles in the current window
-  while (it.next(row0, rows, part)) {
-    const int s = static_cast<int>(t % ring.stages);
-    if (!mbar_wait(&ring.full[s], (t / ring.stages) & 1, a.err, a.wait_limit_ns)) return false;
-    const bool mine = r < rows;
-    float p[NB];
-    if (mine) {
-      const uint4* wr = reinterpret_cast<const uint4*>(ring.base + static_cast<size_t>(s) * kStageBytes) +
-                        static_cast<size_t>(r) * KV + j0;
-      uint4 w[kMaxVecPerLane];
+  bool more = true;
+  while (more) {
+    // kGrp tiles, then one transposed reduction for all of them
+    float pg[kGrp][NB];
 #pragma unroll
-      for (int q = 0; q < kMaxVecPerLane; ++q) {
-        const int j = lane + 32 * q;
-        w[q] = j < nvec ? wr[j] : make_uint4(0u, 0u, 0u, 0u);
+    for (int u = 0; u < kGrp; ++u)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) pg[u][b] = 0.f;
+    int ng = 0;
+#pragma unroll
+    for (int u = 0; u < kGrp; ++u) {
+      int row0, rows, part;
+      if (!it.next(row0, rows, part)) {
+        more = false;
+        break;
       }
+      const int s = static_cast<int>(t % ring.stages);
+      if (!mbar_wait(&ring.full[s], (t / ring.stages) & 1, a.err, a.wait_limit_ns)) return false;
+      if (r < rows) {
+        const uint4* wr = reinterpret_cast<const uint4*>(ring.base + static_cast<size_t>(s) * kStageBytes) +
+                          static_cast<size_t>(r) * KV + j0;
+        uint4 w[kMaxVecPerLane];
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        // one accumulator per vector: independent FMA chains
-        float acc[kMaxVecPerLane];
-        if (NB == 1) {
-#pragma unroll
-          for (int q = 0; q < kMaxVecPerLane; ++q) acc[q] = dot8(w[q], xra[q < XR ? q : 0], xrb[q < XR ? q : 0], 0.f);
-        } else {
-          const float4* xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K) + j0;
-          const float4* xb = xa + KV;
-#pragma unroll
-          for (int q = 0; q < kMaxVecPerLane; ++q) {
-            const int j = lane + 32 * q;
-            acc[q] = j < nvec ? dot8(w[q], xa[j], xb[j], 0.f) : 0.f;
-          }
+        for (int q = 0; q < kMaxVecPerLane; ++q) {
+          const int j = lane + 32 * q;
+          w[q] = j < nvec ? wr[j] : make_uint4(0u, 0u, 0u, 0u);
         }
-        float sum = 0.f;
 #pragma unroll
-        for (int q = 0; q < kMaxVecPerLane; ++q) sum += acc[q];
-        p[b] = sum;
+        for (int b = 0; b < NB; ++b) {
+          // one accumulator per vector: independent FMA chains
+          float acc[kMaxVecPerLane];
+          if (NB == 1) {
+#pragma unroll
+            for (int q = 0; q < kMaxVecPerLane; ++q)
+              acc[q] = dot8(w[q], xra[q < XR ? q : 0], xrb[q < XR ? q : 0], 0.f);
+          } else {
+            const float4* xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K) + j0;
+            const float4* xb = xa + KV;
+#pragma unroll
+            for (int q = 0; q < kMaxVecPerLane; ++q) {
+              const int j = lane + 32 * q;
+              acc[q] = j < nvec ? dot8(w[q], xa[j], xb[j], 0.f) : 0.f;
+            }
+          }
+          float sum = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxVecPerLane; ++q) sum += acc[q];
+          pg[u][b] = sum;
+        }
       }
+      // The stage is free once every lane's reads of it are done (the sums
+      // above depend on them; the arrive is a release): the producer
+      // refills it while this warp goes on.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
+      ++t;
+      if (threadIdx.x == 0) sc.tile[tw + u] = make_int2(row0, rows);
+      ng = u + 1;
     }
-    // The stage is free once every lane's reads of it are done (the sums
-    // above depend on them; the arrive is a release): the producer refills it
-    // while this warp still reduces its partial.
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ring.empty[s]);
-    ++t;
-    if (mine) {
-#pragma unroll
-      for (int b = 0; b < NB; ++b) p[b] = warp_sum(p[b]);
-      if (lane < NB) {
-        float y = p[0];
-#pragma unroll
-        for (int b = 1; b < NB; ++b)
-          if (lane == b) y = p[b];
-        sc.part[tw][warp][lane] = y;
-      }
-    }
-    if (threadIdx.x == 0) sc.tile[tw] = make_int2(row0, rows);
-    if (++tw == kWin) {
+    if (ng == 0) break;
+    gemv_group_sums<NB, kGrp>(pg, ng, sc, tw, warp, lane);
+    tw += ng;
+    if (!more) break;
+    if (tw == kWin) {
       gemv_flush<NB>(a, g, sc, pr, tw, true, epoch);
       tw = 0;
     }
