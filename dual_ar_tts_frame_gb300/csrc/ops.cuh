@@ -659,6 +659,7 @@ struct SampSmem {
   static constexpr int NW = NT / 32;
   unsigned long long hmass[kSampBins];   // per-bin mass, then its inclusive scan
   unsigned int hcnt[kSampBins];
+  unsigned int hhi[kSampBins];           // samp_hist: per-bin sum of mass >> 8
   unsigned long long lkey[kBinCap];      // candidates of the target bin
   unsigned int lmass[kBinCap];
   int nlist;
@@ -836,9 +837,16 @@ DEVI void samp_hist(const float (&z)[EPT], const uint32_t (&mass)[EPT], int n, f
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int BPT = kSampBins / NT;   // bins per thread (contiguous)
   static_assert(kSampBins % NT == 0 && BPT >= 1, "bins split evenly over the threads");
+  // A bin's mass is accumulated as two 32-bit sums, of mass & 255 (at most
+  // 4,097 x 255) and of mass >> 8 (at most 4,097 x 2^16): exact, and 32-bit
+  // shared-memory atomics.  The low sums live in the first half of hmass
+  // until the scan (read by every thread before the barrier that precedes
+  // the scan's writes).
+  unsigned int* hlo = reinterpret_cast<unsigned int*>(sm.hmass);
   for (int b = tid; b < kSampBins; b += NT) {
-    sm.hmass[b] = 0;
-    sm.hcnt[b] = 0;
+    hlo[b] = 0u;
+    sm.hhi[b] = 0u;
+    sm.hcnt[b] = 0u;
   }
   csync<NT>();
 #pragma unroll
@@ -846,7 +854,8 @@ DEVI void samp_hist(const float (&z)[EPT], const uint32_t (&mass)[EPT], int n, f
     const int i = tid + e * NT;
     if (i < n && mass[e] != 0u) {
       const int b = samp_bin(z[e], zmax, inv_t);
-      atomicAdd(&sm.hmass[b], static_cast<unsigned long long>(mass[e]));
+      atomicAdd(&hlo[b], mass[e] & 255u);
+      atomicAdd(&sm.hhi[b], mass[e] >> 8);
       atomicAdd(&sm.hcnt[b], 1u);
     }
   }
@@ -855,7 +864,8 @@ DEVI void samp_hist(const float (&z)[EPT], const uint32_t (&mass)[EPT], int n, f
   unsigned long long run = 0;
 #pragma unroll
   for (int j = 0; j < BPT; ++j) {
-    run += sm.hmass[tid * BPT + j];
+    const int b = tid * BPT + j;
+    run += (static_cast<unsigned long long>(sm.hhi[b]) << 8) + hlo[b];
     c[j] = run;
   }
   unsigned long long incl = run;
@@ -1161,6 +1171,7 @@ DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, Sa
   // are waited on, so their round trips overlap
   const float uk = io.uniforms[static_cast<size_t>(row) * io.ldu + k + 1];
   const int forced_k = (io.forced && tid == 0) ? io.forced[static_cast<size_t>(row) * io.ldf + k] : 0;
+  const int active = ldi(&d.rows[row].active);   // settled by the q0 draw
   float z[EPT];
   unsigned long long key[EPT];
   const float zmax = samp_load<NT, EPT>(d.logits + zoff, c, z, key, sm, d.logits_t + zoff, tg.in, &d);
@@ -1171,7 +1182,7 @@ DEVI void sample_fast_row(const DevPtrs& d, int row, int k, const SampIO& io, Sa
       if (i < Cf) io.fast_logits_out[(static_cast<size_t>(row) * (N - 1) + (k - 1)) * Cf + i] = z[e];
     }
   }
-  if (!ldi(&d.rows[row].active)) {
+  if (!active) {
     if (k + 1 < N) fin_zero<NT>(d, k + 1, row, tg.out);
     csync<NT>();
     return;
