@@ -264,6 +264,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         bulk_load_g2s(ring.base + static_cast<size_t>(s) * kStageBytes, src, bytes, &ring.full[s], pol);
         loaded += bytes;
         ++t;
+        // the prefetch cursor never falls behind the ring: otherwise the next
+        // ring-full wait would first walk every tile it missed, with the
+        // stage it waits for possibly long free
+        {
+          const uint16_t* ps;
+          uint32_t pb;
+          while (prefetched < loaded && pc.next(ps, pb)) prefetched += pb;
+        }
       }
       gemv_drain(ring, t, d.wait_limit_ns);
     }
