@@ -156,7 +156,7 @@ struct AttnSmall {
   static constexpr int TPT = NT / kPageTokens;   // threads per token (score pass)
   static constexpr int QD = HD / TPT;            // dims per thread (score pass)
   static constexpr int PARTS = NT / HD;          // token groups (value pass)
-  float qs[G][TPT][QD + 1];
+  float qs[G][TPT][QD + 4];   // rows 16-byte aligned, 80 B apart: conflict-free float4 reads
   float sc[G][kPageTokens];
   float ored[PARTS][G][HD];
   float knew[HD], vnew[HD];
@@ -317,9 +317,13 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
             const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
                                  bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+            for (int h = 0; h < G; ++h) {
+              const float4* q4 = reinterpret_cast<const float4*>(&sm.qs[h][qd][v8 * 8]);
+              const float4 qa = q4[0], qb = q4[1];
+              const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) s[h] = fmaf(sm.qs[h][qd][v8 * 8 + jj], kf[jj], s[h]);
+              for (int jj = 0; jj < 8; ++jj) s[h] = fmaf(qv[jj], kf[jj], s[h]);
+            }
           }
         }
       }
