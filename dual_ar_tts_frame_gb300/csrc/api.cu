@@ -561,7 +561,6 @@ int build_mega_program(dualar_handle* h, int nb) {
     float* x = l == 0 ? F(d.xs_t) : F(d.hs_t);
     const int x_src = hs_src;
     const int qkv = gemv(packed(args_qkv(h, lw, nb, nullptr), lq.wqkv), x, x_src, nullptr, -1, F(d.qkv_t), true);
-    ops[qkv].pos = l + 1;   // its attention's first pages are fetched during it
     const int at = attn_op(MOP_ATTN_PAGED, l, 0, qkv, c.slow_qk_norm, lw);
     hs_src = gemv(packed(args_o(h, lw, nb, nullptr, nullptr), lq.wo), F(d.attn_t), at, x, x_src, F(d.hs_t), true);
     ops[hs_src].g.x_scout = c.head_dim;

@@ -284,9 +284,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
   const uint32_t ep = p.epoch;
   // (thread 0) this CTA's first paged-attention unit, found at the first QKV
   // projection of the slow AR (after the q0 draw has settled the rows)
-  AttnPreload pre{-1, 0, 0};
-  bool pre_known = false;
-  int att_pre = -1;   // unit whose first page is in flight for the next op
   const int hkv = d.Hkv;
   for (int i = 0; i < p.n_ops; ++i) {
     const MegaOp& op = opb[i & 1];
@@ -307,18 +304,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
         const GemvGeo g = w4op ? gemv_geo<true>(op.g, cta, ncta) : gemv_geo(op.g, cta, ncta);
         float* xs = reinterpret_cast<float*>(uni);
         float* gsum = xs + static_cast<size_t>(NB) * op.g.K;   // packed rows: the 32-element sums of x
-        const size_t xbytes = sizeof(float) * static_cast<size_t>(NB) * (op.g.K + (w4op ? op.g.K / 32 : 0));
-        if (op.pos > 0 && tid == 0 && xbytes <= kAttnPageOffset) {
-          if (!pre_known) {
-            pre = attn_paged_first(d, p.nrows, p.units, p.chunk, cta);
-            pre_known = true;
-          }
-          if (pre.unit >= 0) {
-            attn_paged_preload<HD, G, kMegaNCT, 1>(d, pre, op.pos - 1,
-                                                   *reinterpret_cast<AttnSmem<HD, G, kMegaNCT, 1>*>(uni), abars);
-            att_pre = pre.unit;
-          }
-        }
         bool ok;
         if constexpr (W4) {
           if (w4op) {
@@ -345,9 +330,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) mega_kernel(const MegaParams 
       case MOP_ATTN_PAGED:
         attn_paged_units<HD, G, kMegaNCT, 1>(d, p.nrows, op.layer, p.units, p.chunk, true, op.q_norm,
                                           op.k_norm, *reinterpret_cast<AttnSmem<HD, G, kMegaNCT, 1>*>(uni),
-                                          abars, aphase, cta, ncta, OpTags{op_tag(ep, op.in_src), op_tag(ep, i)},
-                                          att_pre);
-        att_pre = -1;
+                                          abars, aphase, cta, ncta, OpTags{op_tag(ep, op.in_src), op_tag(ep, i)});
         break;
       case MOP_ATTN_FAST:
         // unit u always runs on CTA u % ncta, so the fast K/V that one pass

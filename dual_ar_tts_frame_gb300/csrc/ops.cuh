@@ -145,12 +145,6 @@ DEVI void head_nr_apply(float (&v)[EPL], const HeadNR<EPL>& t, bool norm, float 
 // and uses them directly.  [P2] fact table: 32 query heads over 8 KV heads.
 constexpr int kPageTokens = 64;
 
-// The page buffers start at kAttnPageOffset bytes or later: the x rows a
-// projection stages at the start of the same shared region (up to two rows
-// of 2,560) do not reach them, so the persistent kernel can fetch a unit's
-// first page during the QKV projection that precedes the attention.
-constexpr size_t kAttnPageOffset = 20480;
-
 template <int HD, int G, int NT>
 struct AttnSmall {
   static constexpr int TPT = NT / kPageTokens;   // threads per token (score pass)
@@ -169,8 +163,7 @@ template <int HD, int G, int NT, int NBUF = 2>
 struct AttnSmem : AttnSmall<HD, G, NT> {
   static constexpr int BUFS = NBUF;              // page buffers (a ring of NBUF pages in flight)
   static constexpr size_t kSmall = sizeof(AttnSmall<HD, G, NT>);
-  static constexpr size_t kKvAt =
-      kSmall + 1 <= kAttnPageOffset ? kAttnPageOffset : ((kSmall + 1 + 127) / 128) * 128;
+  static constexpr size_t kKvAt = ((kSmall + 1 + 127) / 128) * 128;   // page buffers 128-byte aligned
   unsigned char pad_[kKvAt - kSmall];
   uint16_t kv[NBUF][2][kPageTokens * HD];        // [buffer][K/V][tok][dim]
 };
@@ -179,7 +172,7 @@ template <int HD, int G, int NT, int NBUF>
 DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_units, int chunk_tokens,
                            bool fuse_append, const uint16_t* q_norm, const uint16_t* k_norm,
                            AttnSmem<HD, G, NT, NBUF>& sm, uint64_t* bars, uint32_t* phase, int cta,
-                           int ncta, OpTags tg = OpTags{0u, 0u}, int preloaded = -1) {
+                           int ncta, OpTags tg = OpTags{0u, 0u}) {
   using S = AttnSmem<HD, G, NT, NBUF>;
   constexpr int EPL = HD / 32;
   constexpr int TPT = S::TPT, QD = S::QD, PARTS = S::PARTS;
@@ -236,8 +229,7 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
       bulk_load_g2s_plain(sm.kv[buf][1], vp, kPageBytes, &bars[buf]);
     };
     if (tid == 0) {
-      // (unit `preloaded` already has its first page in buffer 0)
-      for (int p = u == preloaded ? 1 : 0; p < NBUF && p < npages; ++p) issue(p, p);
+      for (int p = 0; p < NBUF && p < npages; ++p) issue(p, p);
     }
 
     if (fuse_append) {
@@ -485,57 +477,6 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
     }
     csync<NT>();
   }
-}
-
-// This CTA's first unit of a paged-attention op (u = cta) and its first
-// page, for attn_paged_preload: the same for every layer of a launch (rows,
-// chunking and page tables do not change within it).  unit < 0: none.
-struct AttnPreload {
-  int unit, g, page;
-};
-
-DEVI AttnPreload attn_paged_first(const DevPtrs& d, int nrows, int total_units, int chunk_tokens, int cta) {
-  AttnPreload a{-1, 0, 0};
-  const int u = cta;
-  if (u >= total_units) return a;
-  int lo = 0, hi = nrows - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ldi(&d.rows[mid].unit0) <= u) lo = mid;
-    else hi = mid - 1;
-  }
-  const RowInfo ri = ld_row(&d.rows[lo]);
-  const int L = ri.pos + 1;
-  const int nch = (L + chunk_tokens - 1) / chunk_tokens;
-  const int local = u - ri.unit0;
-  const int g = local / nch, c = local % nch;
-  if (!ri.active || g >= d.Hkv) return a;
-  const int t0 = c * chunk_tokens, t1 = min(L, t0 + chunk_tokens);
-  const int npages = (t1 - t0 + kPageTokens - 1) / kPageTokens;
-  const int32_t* ptab = d.page_table + static_cast<size_t>(ri.slot) * d.pages_per_seq + t0 / kPageTokens;
-  for (int p = 0; p < npages; ++p) {
-    const int pg = ldi(ptab + p);
-    if (pg < 0 || pg >= d.max_pages) return a;   // the unit will be skipped: no preload
-  }
-  a.unit = u;
-  a.g = g;
-  a.page = ldi(ptab);
-  return a;
-}
-
-// One thread: copies the first page of unit a.unit (layer `layer`) into page
-// buffer 0, completing on bars[0] like the op's own first copy would.
-template <int HD, int G, int NT, int NBUF>
-DEVI void attn_paged_preload(const DevPtrs& d, const AttnPreload& a, int layer, AttnSmem<HD, G, NT, NBUF>& sm,
-                             uint64_t* bars) {
-  constexpr uint32_t kPageBytes = kPageTokens * HD * 2;
-  const size_t page_stride = static_cast<size_t>(kPageTokens) * HD;
-  const uint16_t* kp =
-      d.kv_pool + (((static_cast<size_t>(a.page) * d.n_layer + layer) * 2 + 0) * d.Hkv + a.g) * page_stride;
-  const uint16_t* vp = kp + static_cast<size_t>(d.Hkv) * page_stride;
-  mbar_arrive_expect_tx(&bars[0], 2 * kPageBytes);
-  bulk_load_g2s_plain(sm.kv[0][0], kp, kPageBytes, &bars[0]);
-  bulk_load_g2s_plain(sm.kv[0][1], vp, kPageBytes, &bars[0]);
 }
 
 // ============================================================================
