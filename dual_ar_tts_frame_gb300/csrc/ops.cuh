@@ -350,10 +350,21 @@ DEVI void attn_paged_units(const DevPtrs& d, int nrows, int layer, int total_uni
 #pragma unroll
       for (int h = 0; h < G; ++h) o[h] *= sm.scl[h];
       const int tb = vpart * TPP, te = min(ntok, tb + TPP);
-      for (int t = tb; t < te; ++t) {
-        const float v = (newest && ps + t == ri.pos) ? sm.vnew[vdim] : bf16bits_to_f32(vs[t * HD + vdim]);
+      if (te - tb == TPP && !(newest && ri.pos >= ps + tb && ri.pos < ps + te)) {
+        // a full run of cached tokens: every V load in flight before the FMAs
+        float vv[TPP];
 #pragma unroll
-        for (int h = 0; h < G; ++h) o[h] = fmaf(sm.sc[h][t], v, o[h]);
+        for (int k = 0; k < TPP; ++k) vv[k] = bf16bits_to_f32(vs[(tb + k) * HD + vdim]);
+#pragma unroll
+        for (int k = 0; k < TPP; ++k)
+#pragma unroll
+          for (int h = 0; h < G; ++h) o[h] = fmaf(sm.sc[h][tb + k], vv[k], o[h]);
+      } else {
+        for (int t = tb; t < te; ++t) {
+          const float v = (newest && ps + t == ri.pos) ? sm.vnew[vdim] : bf16bits_to_f32(vs[t * HD + vdim]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) o[h] = fmaf(sm.sc[h][t], v, o[h]);
+        }
       }
       csync<NT>();   // buffer `buf` is free again
       if (tid == 0 && p + NBUF < npages) issue(p + NBUF, buf);
