@@ -520,9 +520,26 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
   float* vb = kb + static_cast<size_t>(hkv) * N * HD;
   float (*ks)[HD] = sm.ks;
   float (*vs)[HD] = sm.vs;
-  for (int e = threadIdx.x; e < pos * HD; e += NT) {
-    ks[e / HD][e % HD] = ldf(kb + e);
-    vs[e / HD][e % HD] = ldf(vb + e);
+  {
+    // every load of the earlier positions in flight before the first store
+    constexpr int kIt = (kMaxCodebooks * HD + NT - 1) / NT;
+    float kt[kIt], vt[kIt];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int e = threadIdx.x + it * NT;
+      if (e < pos * HD) {
+        kt[it] = ldf(kb + e);
+        vt[it] = ldf(vb + e);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int e = threadIdx.x + it * NT;
+      if (e < pos * HD) {
+        ks[e / HD][e % HD] = kt[it];
+        vs[e / HD][e % HD] = vt[it];
+      }
+    }
   }
   float q[EPL];
   if (warp < G) {
@@ -548,16 +565,29 @@ DEVI void attn_fast_unit(const DevPtrs& d, int unit, int layer, int pos, const u
     const int h = g * G + warp;
     const float scale = 1.0f / sqrtf(static_cast<float>(HD));
     float s[kMaxCodebooks];
+#pragma unroll
+    for (int t = 0; t < kMaxCodebooks; ++t) {
+      float a = 0.f;
+      if (t <= pos) {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) a = fmaf(q[j], ks[t][lane * EPL + j], a);
+      }
+      s[t] = a;
+    }
+    // lane sums of every position's dot product with their shuffles
+    // interleaved (the butterfly of warp_sum, position by position)
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1)
+#pragma unroll
+      for (int t = 0; t < kMaxCodebooks; ++t) s[t] += __shfl_xor_sync(0xFFFFFFFFu, s[t], sh);
     float m = -INFINITY;
 #pragma unroll
     for (int t = 0; t < kMaxCodebooks; ++t) {
-      s[t] = -INFINITY;
       if (t <= pos) {
-        float a = 0.f;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) a = fmaf(q[j], ks[t][lane * EPL + j], a);
-        s[t] = warp_sum(a) * scale;
+        s[t] *= scale;
         m = fmaxf(m, s[t]);
+      } else {
+        s[t] = -INFINITY;
       }
     }
     float l = 0.f;
