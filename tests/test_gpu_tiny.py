@@ -139,26 +139,30 @@ def test_teacher_forced_b2(dec, tiny_oracle):
     run_forced(dec, tiny_oracle, prompts, 8, smp, seed=16)
 
 
-def test_paths_bit_identical(dev_weights):
+@pytest.mark.parametrize("rows", [1, 2])
+def test_paths_bit_identical(dev_weights, rows):
     """The persistent kernel and the per-op path commit the same codes and
-    hold bit-identical state after sampled frames."""
-    p = g.make_prompt(TINY, 90, seed=17)
-    uni = g.make_uniforms(8, 1, TINY, seed=18)
+    hold bit-identical state after sampled frames (one and two rows: the
+    GEMV consumer's grouped lane sums must give the per-tile sums' bits)."""
+    prompts = [g.make_prompt(TINY, 90, seed=17), g.make_prompt(TINY, 45, seed=19)][:rows]
+    uni = g.make_uniforms(8, rows, TINY, seed=18)
     smp = gpu_sampling(OSampling(temperature=0.8, top_p=0.8, ras_win=10))
     out = []
     for persistent in (True, False):
         d = make(dev_weights, persistent=persistent)
-        d.prefill(0, p)
+        for s, p in enumerate(prompts):
+            d.prefill(s, p)
         codes = []
         for f in range(8):
-            c, s_ = d.decode_frame([0], dev(uni[f]), smp)
+            c, s_ = d.decode_frame(list(range(rows)), dev(uni[f]), smp)
             codes.append(c.cpu().numpy())
         d.sync()
-        out.append((np.stack(codes), d.read_state(0)))
+        out.append((np.stack(codes), [d.read_state(s) for s in range(rows)]))
         d.close()
     np.testing.assert_array_equal(out[0][0], out[1][0])
-    np.testing.assert_array_equal(out[0][1][0], out[1][1][0])
-    np.testing.assert_array_equal(out[0][1][1], out[1][1][1])
+    for s in range(rows):
+        np.testing.assert_array_equal(out[0][1][s][0], out[1][1][s][0])
+        np.testing.assert_array_equal(out[0][1][s][1], out[1][1][s][1])
 
 
 def test_teacher_forced_ragged_batch(dec, tiny_oracle):
