@@ -1086,15 +1086,21 @@ DEVI void sample_q0_row(const DevPtrs& d, int row, const SampIO& io, SampSmem<NT
   const int normal = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.temperature, io.sp.top_p, u_normal, sm);
   // [P2] "Two autoregressions": a second draw at temperature 1.0, top-p 0.9,
   // used when the normal draw repeats a semantic token of the last 10 frames.
-  const int ras = samp_draw<NT, EPT>(z, key, c, zmax, io.sp.ras_temperature, io.sp.ras_top_p, u_ras, sm);
-  if (tid == 0) {
-    const int hn = sm.ibc[3];
+  // Every thread sees the same history, so the decision is uniform; the
+  // second draw runs only when it is used or the caller records both draws.
+  const int hn = sm.ibc[3];
+  bool repeat = false;
+  if (normal != ns) {
     const int w = min(io.sp.ras_win, hn);
-    bool repeat = false;
-    if (normal != ns)
-      for (int j = 0; j < w; ++j)
-        if (sm.hist[(hn - 1 - j) % kRasRing] == normal) repeat = true;
-    const int chosen = (io.sp.ras_win > 0 && repeat) ? ras : normal;
+    for (int j = 0; j < w; ++j)
+      if (sm.hist[(hn - 1 - j) % kRasRing] == normal) repeat = true;
+  }
+  const bool use_ras = io.sp.ras_win > 0 && repeat;
+  const int ras = (use_ras || io.draws_out)
+                      ? samp_draw<NT, EPT>(z, key, c, zmax, io.sp.ras_temperature, io.sp.ras_top_p, u_ras, sm)
+                      : -1;
+  if (tid == 0) {
+    const int chosen = use_ras ? ras : normal;
     const int commit = io.forced ? forced0 : chosen;
     if (io.draws_out) {
       io.draws_out[row * (N + 2) + 0] = normal;
