@@ -17,6 +17,7 @@ rank's time.  `--impl reference` times the CPU oracle on the same workload.
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import os
@@ -107,7 +108,9 @@ def traffic_record():
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 20 ms, started before the warm-up (the tool
+    takes a while to come up); summary() keeps the samples read between
+    mark_start() and mark_end(), the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -115,36 +118,48 @@ class ClockSampler:
     def __init__(self, gpu: int):
         self.gpu = gpu
         self.proc = None
-        self.lines = []
+        self.lines = []   # (host time of reading, line)
+        self.t0 = None
+        self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
+            atexit.register(self.__exit__, None, None, None)   # never left running
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc:
-            self.proc.terminate()
+            proc, self.proc = self.proc, None
+            proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                proc.kill()
             self.th.join(timeout=2)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if self.t0 is not None and self.t1 is not None and not (self.t0 <= t <= self.t1 + 0.02):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -651,6 +666,9 @@ def main():
     from dual_ar_tts_frame_gb300 import DualARDecoder, Sampling, build, upload_weights
     from dual_ar_tts_frame_gb300 import bytemodel
     build()
+    # the clock sampler starts now (nvidia-smi takes a while to come up) and
+    # keeps only the samples of the timed region below
+    clk = ClockSampler(local).__enter__()
     bits = gen.make_weights(cfg, seed=0)
     w = upload_weights(bits)
     if ws > 1 or args.no_cpu_baseline:
@@ -678,12 +696,14 @@ def main():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     dec.profile(True)
-    with ClockSampler(local) as clk:
-        ev0.record(stream)
-        for f in range(W, W + K):
-            dec.decode_frame(slots, uni[f], smp, codes, status)
-        ev1.record(stream)
-        torch.cuda.synchronize()
+    clk.mark_start()
+    ev0.record(stream)
+    for f in range(W, W + K):
+        dec.decode_frame(slots, uni[f], smp, codes, status)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk.mark_end()
+    clk.__exit__(None, None, None)
     dec.profile(False)
     dec.sync()
     prof = dec.profile_read()
